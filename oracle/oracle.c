@@ -1,0 +1,223 @@
+/*
+ * CPU oracle for the sparse-attention prefill indexer.
+ *
+ * TEST INFRASTRUCTURE, NOT PRODUCT CODE.  Only the test suite, the smoke check
+ * and the CPU-baseline leg of the benchmark may load or run this file.  It
+ * shares no code, header, table or constant with the CUDA library.
+ *
+ * It writes out the plain definition of what the indexer returns:
+ *
+ *   score    s[r,j] = k_scale[j] * sum_h w[r,h] * max(0, sum_d q[r,h,d] k[j,d])
+ *            for every visible key ks[r] <= j < ke[r], in fp64, every sum taken
+ *            in ascending index order.  Pages: "[sglang] logits를 쓰지 않는
+ *            top-k" introduction (an indexer score per query row over every
+ *            visible key) and section 1 (the heads are reduced per key); the
+ *            page does not print the formula, the ReLU-weighted head sum with a
+ *            per-key scale is the stated problem of this library.
+ *   select   order the visible keys by (score descending, key index
+ *            ascending), keep the first topk, return their row-relative
+ *            indices j - ks[r] in ascending order, then -1 up to topk.
+ *            Same page, section 1 (candidate indices are stored as
+ *            key - ks[row]) and section 3 (a consumer skips negative
+ *            positions); "[sglang] ROCm DSA Indexer Top-K 최적화", solution
+ *            section (exact top-k at torch.topk-level recall).
+ *
+ * Inputs are decoded exactly to fp64 from the bit formats:
+ *   e4m3 (fn):  1 sign, 4 exponent bits (bias 7), 3 mantissa bits, subnormals
+ *               at exponent 0, S.1111.111 is NaN, no infinities, max 448.
+ *   bfloat16:   1 sign, 8 exponent bits (bias 127), 7 mantissa bits.
+ *
+ * Build: plain C11, no fast-math and no FMA contraction (-ffp-contract=off),
+ * so the fp64 results are the same on every host.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+enum { ORC_BF16 = 1, ORC_E4M3 = 2 };
+
+/* ---------------------------------------------------------------- decoders */
+
+double orc_e4m3_to_f64(uint32_t code) {
+    const int sign = (code >> 7) & 1;
+    const int expo = (code >> 3) & 0xF;
+    const int mant = code & 0x7;
+    double v;
+    if (expo == 0xF && mant == 0x7) return NAN;
+    if (expo == 0)
+        v = ldexp((double)mant / 8.0, 1 - 7);          /* subnormal */
+    else
+        v = ldexp(1.0 + (double)mant / 8.0, expo - 7);  /* normal */
+    return sign ? -v : v;
+}
+
+double orc_bf16_to_f64(uint32_t code) {
+    const int sign = (code >> 15) & 1;
+    const int expo = (code >> 7) & 0xFF;
+    const int mant = code & 0x7F;
+    double v;
+    if (expo == 0xFF) v = mant ? NAN : INFINITY;
+    else if (expo == 0) v = ldexp((double)mant / 128.0, 1 - 127);
+    else v = ldexp(1.0 + (double)mant / 128.0, expo - 127);
+    return sign ? -v : v;
+}
+
+static double decode(const void* base, long long i, int dtype) {
+    if (dtype == ORC_E4M3) return orc_e4m3_to_f64(((const uint8_t*)base)[i]);
+    return orc_bf16_to_f64(((const uint16_t*)base)[i]);
+}
+
+/* ------------------------------------------------------------------ scores */
+
+/* Scores of one row over its visible keys, out[j - ks] for ks <= j < ke. */
+int orc_scores_row(const void* q, const void* k, int dtype, const float* k_scale,
+                   const float* w, int H, int D, long long r, long long ks,
+                   long long ke, double* out) {
+    if (ke <= ks) return 0;
+    double* qd = (double*)malloc(sizeof(double) * (size_t)H * D);
+    double* kd = (double*)malloc(sizeof(double) * (size_t)D);
+    double* dot = (double*)malloc(sizeof(double) * (size_t)H);
+    if (!qd || !kd || !dot) { free(qd); free(kd); free(dot); return -1; }
+    for (long long i = 0; i < (long long)H * D; ++i)
+        qd[i] = decode(q, r * (long long)H * D + i, dtype);
+    for (long long j = ks; j < ke; ++j) {
+        for (int d = 0; d < D; ++d) kd[d] = decode(k, j * (long long)D + d, dtype);
+        /* q[r,h,:] . k[j,:], summed over d in ascending order for every head */
+        for (int h = 0; h < H; ++h) dot[h] = 0.0;
+        for (int d = 0; d < D; ++d)
+            for (int h = 0; h < H; ++h) dot[h] += qd[(size_t)h * D + d] * kd[d];
+        double s = 0.0;
+        for (int h = 0; h < H; ++h) {
+            const double relu = dot[h] > 0.0 ? dot[h] : 0.0;
+            s += (double)w[r * H + h] * relu;
+        }
+        out[j - ks] = (double)k_scale[j] * s;
+    }
+    free(qd); free(kd); free(dot);
+    return 0;
+}
+
+/* --------------------------------------------------------------- selection */
+
+typedef struct { double s; long long j; } orc_item;
+
+/* score descending, then key index ascending */
+static int by_score_then_index(const void* a, const void* b) {
+    const orc_item* x = (const orc_item*)a;
+    const orc_item* y = (const orc_item*)b;
+    if (x->s > y->s) return -1;
+    if (x->s < y->s) return 1;
+    return (x->j > y->j) - (x->j < y->j);
+}
+
+static int by_index(const void* a, const void* b) {
+    const int32_t x = *(const int32_t*)a, y = *(const int32_t*)b;
+    return (x > y) - (x < y);
+}
+
+/* Top-k of s[0..n) (row-relative indices), written ascending into out[topk]
+ * and padded with -1.  A full sort: plain and slow on purpose. */
+int orc_select_row(const double* s, long long n, int topk, int32_t* out) {
+    if (n < 0) n = 0;
+    const long long take = n < topk ? n : topk;
+    orc_item* it = (orc_item*)malloc(sizeof(orc_item) * (size_t)(n > 0 ? n : 1));
+    if (!it) return -1;
+    for (long long j = 0; j < n; ++j) { it[j].s = s[j]; it[j].j = j; }
+    qsort(it, (size_t)n, sizeof(orc_item), by_score_then_index);
+    for (long long i = 0; i < take; ++i) out[i] = (int32_t)it[i].j;
+    qsort(out, (size_t)take, sizeof(int32_t), by_index);
+    for (long long i = take; i < topk; ++i) out[i] = -1;
+    free(it);
+    return 0;
+}
+
+/* ------------------------------------------------------ row-parallel driver */
+
+typedef struct {
+    /* indexer inputs (score_topk) */
+    const void* q; const void* k; int dtype; const float* k_scale; const float* w;
+    int H, D;
+    /* given scores (topk_from_scores) */
+    const float* scores; long long stride;
+    /* common */
+    const int32_t* ks; const int32_t* ke; const int32_t* rows; int nrows; int topk;
+    int32_t* out;          /* [nrows, topk] */
+    double* out_scores;    /* optional [nrows, score_stride] */
+    long long score_stride;
+    int next; pthread_mutex_t lock; int err;
+} orc_job;
+
+static int grab(orc_job* J) {
+    pthread_mutex_lock(&J->lock);
+    const int i = J->next < J->nrows ? J->next++ : -1;
+    pthread_mutex_unlock(&J->lock);
+    return i;
+}
+
+static void* worker(void* arg) {
+    orc_job* J = (orc_job*)arg;
+    for (int i = grab(J); i >= 0; i = grab(J)) {
+        const long long r = J->rows[i];
+        const long long ks = J->ks[r], ke = J->ke[r];
+        const long long n = ke > ks ? ke - ks : 0;
+        double* s = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+        if (!s) { J->err = -1; continue; }
+        int e;
+        if (J->scores) {
+            for (long long j = 0; j < n; ++j) s[j] = (double)J->scores[r * J->stride + ks + j];
+            e = 0;
+        } else {
+            e = orc_scores_row(J->q, J->k, J->dtype, J->k_scale, J->w, J->H, J->D, r, ks, ke, s);
+        }
+        if (!e && J->out) e = orc_select_row(s, n, J->topk, J->out + (long long)i * J->topk);
+        if (!e && J->out_scores)
+            for (long long j = 0; j < n && j < J->score_stride; ++j)
+                J->out_scores[(long long)i * J->score_stride + j] = s[j];
+        if (e) J->err = e;
+        free(s);
+    }
+    return NULL;
+}
+
+static int run(orc_job* J, int nthreads) {
+    J->next = 0; J->err = 0;
+    pthread_mutex_init(&J->lock, NULL);
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 1024) nthreads = 1024;
+    pthread_t th[1024];
+    int started = 0;
+    for (int t = 1; t < nthreads; ++t)
+        if (pthread_create(&th[started], NULL, worker, J) == 0) ++started;
+    worker(J);
+    for (int t = 0; t < started; ++t) pthread_join(th[t], NULL);
+    pthread_mutex_destroy(&J->lock);
+    return J->err;
+}
+
+/* Exact top-k of the indexer scores for the listed rows.
+ * out[i, :] belongs to rows[i]; out_scores (optional) receives the fp64 scores
+ * of rows[i] at [i, 0 .. ke-ks) with row pitch score_stride. */
+int orc_score_topk(const void* q, const void* k, int dtype, const float* k_scale,
+                   const float* w, const int32_t* ks, const int32_t* ke, int H, int D,
+                   const int32_t* rows, int nrows, int topk, int32_t* out,
+                   double* out_scores, long long score_stride, int nthreads) {
+    orc_job J;
+    memset(&J, 0, sizeof(J));
+    J.q = q; J.k = k; J.dtype = dtype; J.k_scale = k_scale; J.w = w; J.H = H; J.D = D;
+    J.ks = ks; J.ke = ke; J.rows = rows; J.nrows = nrows; J.topk = topk; J.out = out;
+    J.out_scores = out_scores; J.score_stride = score_stride;
+    return run(&J, nthreads);
+}
+
+/* Exact top-k of given fp32 scores [*, stride] for the listed rows. */
+int orc_topk_from_scores(const float* scores, long long stride, const int32_t* ks,
+                         const int32_t* ke, const int32_t* rows, int nrows, int topk,
+                         int32_t* out, int nthreads) {
+    orc_job J;
+    memset(&J, 0, sizeof(J));
+    J.scores = scores; J.stride = stride;
+    J.ks = ks; J.ke = ke; J.rows = rows; J.nrows = nrows; J.topk = topk; J.out = out;
+    return run(&J, nthreads);
+}

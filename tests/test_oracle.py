@@ -1,0 +1,262 @@
+"""Pins of the CPU oracle against facts that do not come from the oracle itself:
+the bit formats (checked against torch's own casts), a hand-worked example, closed
+forms of the score, identities of ReLU, brute-force subset enumeration of the
+selection rule, and invariants of every returned index set."""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ----------------------------------------------------------------- decoders
+
+def test_e4m3_decoder_exhaustive_matches_torch(orc):
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = orc.e4m3_to_f64(codes)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert nan.sum() == 2  # S.1111.111 only
+    assert np.array_equal(got[~nan], ref[~nan])
+    # format landmarks: max normal, smallest subnormal, one, sign
+    assert got[0x7E] == 448.0 and got[0x01] == 2.0 ** -9 and got[0x38] == 1.0
+    assert got[0xB8] == -1.0 and got[0x08] == 2.0 ** -6
+
+
+def test_bf16_decoder_exhaustive_matches_torch(orc):
+    codes = np.arange(65536, dtype=np.uint32)
+    ref = torch.from_numpy(codes.astype(np.int32).astype(np.int16)).view(torch.bfloat16) \
+        .to(torch.float64).numpy()
+    got = orc.bf16_to_f64(codes)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert got[0x3F80] == 1.0 and got[0x7F80] == math.inf and got[0x0001] == 2.0 ** -133
+
+
+# ------------------------------------------------------- hand-worked example
+
+def _golden_inputs(g, dtype):
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float8_e4m3fn
+    q = torch.tensor(g["q"], dtype=torch.float32).to(tdt)
+    k = torch.tensor(g["k"], dtype=torch.float32).to(tdt)
+    # every value of the fixture is exact in both formats
+    assert torch.equal(q.float(), torch.tensor(g["q"])) and torch.equal(k.float(), torch.tensor(g["k"]))
+    return q, k
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+def test_hand_worked_example(orc, dtype):
+    g = json.load(open(os.path.join(GOLDEN, "hand_scores.json")))
+    q, k = _golden_inputs(g, dtype)
+    w = torch.tensor(g["w"], dtype=torch.float32)
+    sc = torch.tensor(g["k_scale"], dtype=torch.float32)
+    full = synth.indexer_inputs  # noqa: F841  (shapes only come from the fixture)
+    for case in g["cases"]:
+        inp = synth.IndexerInputs(q=q, k=k, k_scale=sc, w=w,
+                                  ks=torch.tensor([case["ks"]], dtype=torch.int32),
+                                  ke=torch.tensor([case["ke"]], dtype=torch.int32),
+                                  topk=case["topk"])
+        s = orc.scores_row(inp, 0)
+        assert s.tolist() == g["scores_full"][case["ks"]:case["ke"]]
+        got = orc.score_topk(inp, nthreads=1)[0].tolist()
+        assert got == case["expect"], case["why"]
+
+
+# ---------------------------------------------------------- score closed forms
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+def test_unit_query_reads_first_coordinate(orc, dtype):
+    """H=1, w=1, scale=1, q=e_0  =>  s_j = ReLU(k[j,0])."""
+    inp = synth.indexer_inputs(1, 300, 1, 64, 8, dtype, seed=11, ranges="full", scale="one")
+    inp.q.zero_()
+    inp.q[0, 0, 0] = 1.0
+    inp.w.fill_(1.0)
+    s = orc.scores_row(inp, 0)
+    k0 = inp.k[:, 0].to(torch.float64).numpy()
+    assert np.array_equal(s, np.maximum(k0, 0.0))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+def test_relu_identity_gives_the_dot_product(orc, dtype):
+    """ReLU(x) - ReLU(-x) = x: for H=1, w=1, scale=1 the difference of the
+    scores of q and -q is q.k_j, here compared with a numpy matmul of the
+    torch-decoded inputs.  A dropped ReLU, a wrong d index or a transposed
+    operand breaks it."""
+    inp = synth.indexer_inputs(1, 257, 1, 128, 8, dtype, seed=12, ranges="full", scale="one")
+    inp.w.fill_(1.0)
+    pos = orc.scores_row(inp, 0)
+    neg_inp = synth.IndexerInputs(q=(-inp.q.float()).to(inp.q.dtype), k=inp.k, k_scale=inp.k_scale,
+                                  w=inp.w, ks=inp.ks, ke=inp.ke, topk=8)
+    neg = orc.scores_row(neg_inp, 0)
+    dots = inp.k.to(torch.float64).numpy() @ inp.q[0, 0].to(torch.float64).numpy()
+    np.testing.assert_allclose(pos - neg, dots, rtol=1e-12, atol=1e-12)
+    assert (pos >= 0).all() and (neg >= 0).all()
+    assert np.all((pos == 0) | (neg == 0))  # only one side of ReLU is open
+
+
+def test_heads_weights_and_scale_are_linear(orc):
+    """Doubling w doubles s; k_scale multiplies s per key; swapping two heads
+    (q and w together) leaves s unchanged; a head with w=0 contributes
+    nothing; every row uses its own q and w."""
+    inp = synth.indexer_inputs(3, 200, 4, 64, 8, "bf16", seed=13, ranges="full", scale="one")
+    base = np.stack([orc.scores_row(inp, r) for r in range(3)])
+    inp2 = synth.IndexerInputs(q=inp.q, k=inp.k, k_scale=inp.k_scale, w=inp.w * 2, ks=inp.ks,
+                               ke=inp.ke, topk=8)
+    assert np.array_equal(np.stack([orc.scores_row(inp2, r) for r in range(3)]), 2 * base)
+    sc = torch.arange(1, 201, dtype=torch.float32)
+    inp3 = synth.IndexerInputs(q=inp.q, k=inp.k, k_scale=sc, w=inp.w, ks=inp.ks, ke=inp.ke, topk=8)
+    np.testing.assert_allclose(np.stack([orc.scores_row(inp3, r) for r in range(3)]),
+                               base * sc.numpy()[None, :], rtol=1e-15)
+    perm = [2, 0, 3, 1]
+    inp4 = synth.IndexerInputs(q=inp.q[:, perm].contiguous(), k=inp.k, k_scale=inp.k_scale,
+                               w=inp.w[:, perm].contiguous(), ks=inp.ks, ke=inp.ke, topk=8)
+    np.testing.assert_allclose(np.stack([orc.scores_row(inp4, r) for r in range(3)]), base,
+                               rtol=1e-14)
+    # single head kept: equals w_h * ReLU(q_h . k) from the decoded inputs
+    w1 = torch.zeros_like(inp.w)
+    w1[1, 2] = 0.75
+    inp5 = synth.IndexerInputs(q=inp.q, k=inp.k, k_scale=inp.k_scale, w=w1, ks=inp.ks, ke=inp.ke,
+                               topk=8)
+    s5 = np.stack([orc.scores_row(inp5, r) for r in range(3)])
+    dots = inp.k.to(torch.float64).numpy() @ inp.q[1, 2].to(torch.float64).numpy()
+    assert np.array_equal(s5[0], np.zeros(200)) and np.array_equal(s5[2], np.zeros(200))
+    np.testing.assert_allclose(s5[1], 0.75 * np.maximum(dots, 0), rtol=1e-14)
+
+
+def test_zero_query_selects_the_first_keys(orc):
+    """q = 0  =>  every score is 0  =>  the first topk visible keys."""
+    inp = synth.indexer_inputs(4, 500, 8, 64, 37, "fp8", seed=14)
+    inp.q.zero_()
+    out = orc.score_topk(inp, nthreads=2)
+    for r in range(4):
+        n = int(inp.ke[r] - inp.ks[r])
+        assert out[r].tolist() == list(range(min(37, n))) + [-1] * (37 - min(37, n))
+
+
+def test_visible_range_is_relative(orc):
+    """Row scores over [ks, ke) equal the slice of the full-range scores."""
+    inp = synth.indexer_inputs(2, 400, 2, 64, 16, "bf16", seed=15, ranges="full")
+    full = orc.scores_row(inp, 1)
+    inp.ks[1], inp.ke[1] = 123, 345
+    part = orc.scores_row(inp, 1)
+    assert np.array_equal(part, full[123:345])
+    top = orc.score_topk(inp, rows=[1], nthreads=1)[0]
+    assert top.max() < 222 and top.min() >= 0
+
+
+# ------------------------------------------------------------------ selection
+
+def _brute_force_topk(s, topk):
+    """Enumerate every subset of size min(topk, n); the rule's answer is the
+    unique subset whose sorted (score desc, index asc) sequence is
+    lexicographically best."""
+    n = len(s)
+    m = min(topk, n)
+    best, best_key = None, None
+    for sub in itertools.combinations(range(n), m):
+        key = sorted(((-s[j], j) for j in sub))
+        if best_key is None or key < best_key:
+            best, best_key = sub, key
+    return list(best) + [-1] * (topk - m)
+
+
+def test_selection_matches_subset_enumeration(orc):
+    rng = np.random.default_rng(0)
+    for trial in range(60):
+        n = int(rng.integers(0, 9))
+        topk = int(rng.integers(1, 8))
+        s = rng.integers(-3, 4, size=n).astype(np.float64) / 2  # many exact ties
+        assert orc.select_row(s, topk).tolist() == _brute_force_topk(s, topk)
+
+
+def test_selection_matches_lexsort(orc):
+    rng = np.random.default_rng(1)
+    for trial in range(40):
+        n = int(rng.integers(1, 65))
+        topk = int(rng.integers(1, 70))
+        s = np.round(rng.normal(size=n), 1)
+        order = np.lexsort((np.arange(n), -s))[:topk]
+        expect = sorted(order.tolist()) + [-1] * (topk - min(topk, n))
+        assert orc.select_row(s, topk).tolist() == expect
+
+
+def test_selection_closed_forms(orc):
+    n, topk = 1000, 64
+    assert orc.select_row(np.arange(n, dtype=np.float64), topk).tolist() == list(range(n - topk, n))
+    assert orc.select_row(np.full(n, 0.5), topk).tolist() == list(range(topk))
+    s = np.zeros(n)
+    planted = [5, 77, 300, 301, 999]
+    s[planted] = 1.0
+    assert orc.select_row(s, 5).tolist() == planted
+    assert orc.select_row(s, 7).tolist() == [0, 1, 5, 77, 300, 301, 999]
+    assert orc.select_row(np.zeros(0), 3).tolist() == [-1, -1, -1]
+
+
+def test_signed_zero_ties_by_index(orc):
+    s = np.array([-0.0, 0.0, -0.0, 1.0, 0.0])
+    assert orc.select_row(s, 3).tolist() == [0, 1, 3]
+
+
+def _check_invariants(s, out, topk):
+    n = len(s)
+    m = min(topk, n)
+    sel = out[:m]
+    assert (out[m:] == -1).all()
+    assert (sel >= 0).all() and (sel < n).all()
+    assert len(set(sel.tolist())) == m
+    assert (np.diff(sel) > 0).all()
+    if m < n:
+        mask = np.zeros(n, bool)
+        mask[sel] = True
+        lo = s[mask].min()
+        assert lo >= s[~mask].max()
+        tied_out = np.flatnonzero(~mask & (s == lo))
+        tied_in = np.flatnonzero(mask & (s == lo))
+        if tied_out.size:
+            assert tied_in.max() < tied_out.min()
+
+
+def test_invariants_on_indexer_rows(orc):
+    inp = synth.indexer_inputs(16, 3000, 8, 64, 200, "fp8", seed=16)
+    out, sc = orc.score_topk(inp, want_scores=True, nthreads=4)
+    for i in range(16):
+        n = int(inp.ke[i] - inp.ks[i])
+        _check_invariants(sc[i, :n], out[i], 200)
+
+
+# ------------------------------------------------------ top-k on given scores
+
+def test_topk_from_scores_matches_lexsort_with_ties(orc):
+    inp = synth.score_inputs(24, 5000, 300, seed=17, short_frac=0.25)
+    out = orc.topk_from_scores(inp.scores, inp.ks, inp.ke, 300, nthreads=4)
+    S = inp.scores.numpy()
+    for r in range(24):
+        n = int(inp.ke[r])
+        s = S[r, :n].astype(np.float64)
+        order = np.lexsort((np.arange(n), -s))[:300]
+        expect = sorted(order.tolist()) + [-1] * (300 - min(300, n))
+        assert out[r].tolist() == expect
+        _check_invariants(s, out[r], 300)
+    # the bf16 grid leaves exact ties at the k-th value on the long rows
+    long_rows = [r for r in range(24) if int(inp.ke[r]) == 5000]
+    r = long_rows[0]
+    s = S[r].astype(np.float64)
+    kth = np.sort(s)[::-1][299]
+    assert (s == kth).sum() > 1
+
+
+def test_topk_from_scores_row_subset_and_stride(orc):
+    S = torch.arange(40, dtype=torch.float32).reshape(4, 10)
+    ks = torch.tensor([0, 2, 5, 9], dtype=torch.int32)
+    ke = torch.tensor([10, 7, 5, 10], dtype=torch.int32)
+    out = orc.topk_from_scores(S, ks, ke, 3, rows=[3, 1, 2])
+    assert out.tolist() == [[0, -1, -1], [2, 3, 4], [-1, -1, -1]]
