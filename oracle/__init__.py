@@ -42,7 +42,7 @@ def build(force: bool = False) -> str:
             return _LIB
         os.makedirs(_BUILD, exist_ok=True)
         tmp = _LIB + f".{os.getpid()}.tmp"
-        cmd = ["gcc", "-O2", "-std=gnu11", "-ffp-contract=off", "-fno-fast-math",
+        cmd = ["gcc", "-O3", "-std=gnu11", "-ffp-contract=off", "-fno-fast-math",
                "-fPIC", "-shared", "-pthread", "-o", tmp, _SRC, "-lm"]
         subprocess.run(cmd, check=True)
         os.replace(tmp, _LIB)

@@ -64,9 +64,20 @@ double orc_bf16_to_f64(uint32_t code) {
     return sign ? -v : v;
 }
 
+/* Every code of both formats decoded once by the functions above. */
+static double tab_e4m3[256];
+static double tab_bf16[65536];
+static pthread_once_t tab_once = PTHREAD_ONCE_INIT;
+
+static void fill_tables(void) {
+    for (uint32_t c = 0; c < 256; ++c) tab_e4m3[c] = orc_e4m3_to_f64(c);
+    for (uint32_t c = 0; c < 65536; ++c) tab_bf16[c] = orc_bf16_to_f64(c);
+}
+
 static double decode(const void* base, long long i, int dtype) {
-    if (dtype == ORC_E4M3) return orc_e4m3_to_f64(((const uint8_t*)base)[i]);
-    return orc_bf16_to_f64(((const uint16_t*)base)[i]);
+    pthread_once(&tab_once, fill_tables);
+    if (dtype == ORC_E4M3) return tab_e4m3[((const uint8_t*)base)[i]];
+    return tab_bf16[((const uint16_t*)base)[i]];
 }
 
 /* ------------------------------------------------------------------ scores */
@@ -80,14 +91,16 @@ int orc_scores_row(const void* q, const void* k, int dtype, const float* k_scale
     double* kd = (double*)malloc(sizeof(double) * (size_t)D);
     double* dot = (double*)malloc(sizeof(double) * (size_t)H);
     if (!qd || !kd || !dot) { free(qd); free(kd); free(dot); return -1; }
-    for (long long i = 0; i < (long long)H * D; ++i)
-        qd[i] = decode(q, r * (long long)H * D + i, dtype);
+    /* qd[d*H + h] = q[r,h,d]: heads contiguous for the inner loop below */
+    for (int h = 0; h < H; ++h)
+        for (int d = 0; d < D; ++d)
+            qd[(size_t)d * H + h] = decode(q, (r * (long long)H + h) * D + d, dtype);
     for (long long j = ks; j < ke; ++j) {
         for (int d = 0; d < D; ++d) kd[d] = decode(k, j * (long long)D + d, dtype);
         /* q[r,h,:] . k[j,:], summed over d in ascending order for every head */
         for (int h = 0; h < H; ++h) dot[h] = 0.0;
         for (int d = 0; d < D; ++d)
-            for (int h = 0; h < H; ++h) dot[h] += qd[(size_t)h * D + d] * kd[d];
+            for (int h = 0; h < H; ++h) dot[h] += qd[(size_t)d * H + h] * kd[d];
         double s = 0.0;
         for (int h = 0; h < H; ++h) {
             const double relu = dot[h] > 0.0 ? dot[h] : 0.0;
