@@ -1,0 +1,170 @@
+/*
+ * idx.h - C ABI of libidx, the GB300 (sm_103a) sparse-attention prefill indexer.
+ *
+ * Problem (page "[sglang] logits를 쓰지 않는 top-k: SGLang의 LiteTopK prefill
+ * indexer", introduction and section 1): for every query row r and every key j
+ * that the row can see, ks[r] <= j < ke[r], the indexer score is
+ *
+ *     s[r,j] = k_scale[j] * sum_h w[r,h] * max(0, q[r,h,:] . k[j,:])
+ *
+ * and the row keeps the topk best keys.  This library returns the EXACT top-k:
+ * keys ordered by (score descending, key index ascending), the first topk kept,
+ * reported as row-relative indices j - ks[r] (page 1, section 1: candidate
+ * indices are stored as key - ks[row]) in ascending order, followed by -1 when
+ * the row sees fewer than topk keys (page 1, section 3: a consumer skips
+ * negative positions).
+ *
+ * Conventions shared by every entry point
+ *  - Tensor arguments are DEVICE pointers owned by the caller; the library
+ *    keeps no pointer after the call returns and allocates no device memory.
+ *    Scratch memory is the caller's workspace `ws` of at least the size its
+ *    *_workspace query returns, 256-byte aligned.
+ *  - All layouts are row-major and contiguous:
+ *      q [rows, H, D], k [keys, D]  (both bf16 or both fp8 e4m3, see idx_dtype)
+ *      k_scale [keys] float32 (> 0), w [rows, H] float32 (>= 0)
+ *      ks, ke [rows] int32;  out_idx [rows, topk] int32
+ *  - `stream` is a cudaStream_t (NULL is the legacy default stream).  Calls are
+ *    asynchronous on that stream; the host never waits on the device.
+ *  - Arguments are validated on the host before anything is launched; a bad
+ *    argument returns an error and launches nothing.  Errors met on the
+ *    device (a visible range outside [0, keys], a wait that timed out) are
+ *    OR-ed into the optional device status word options->d_status as
+ *    IDX_DEV_* bits; nothing traps.
+ *  - Preconditions not checked: scores, q, k, k_scale, w hold no NaN/Inf;
+ *    k_scale > 0 and w >= 0 (the score formula relies on it).
+ *  - Supported: sm_103a; H in {8, 16, 32, 64}; D in {64, 128};
+ *    1 <= topk <= 4096; rows >= 0 (a row count of 0 is a no-op).
+ *    Anything else returns IDX_EUNSUPPORTED.
+ */
+#ifndef IDX_H_
+#define IDX_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    IDX_OK = 0,
+    IDX_EINVAL = 1,        /* a null pointer, a negative size, topk < 1 ... */
+    IDX_EALIGN = 2,        /* a tensor or the workspace is not 16 B (256 B for ws) aligned */
+    IDX_EWORKSPACE = 3,    /* ws_bytes smaller than the query returned */
+    IDX_EUNSUPPORTED = 4,  /* dtype, H, D, topk or the GPU architecture */
+    IDX_ECUDA = 5,         /* a CUDA runtime/driver call failed */
+    IDX_ETIMEOUT = 6       /* reserved for host-side reporting of IDX_DEV_TIMEOUT */
+} idx_status;
+
+/* bits OR-ed into *options->d_status by device code */
+#define IDX_DEV_TIMEOUT 0x1   /* a bounded wait inside a kernel gave up */
+#define IDX_DEV_RANGE   0x2   /* a row's [ks, ke) is not inside [0, keys] or exceeds max_len */
+#define IDX_DEV_STATE   0x4   /* the exact fallback ran out of its refinement levels */
+
+typedef enum { IDX_BF16 = 1, IDX_FP8_E4M3 = 2 } idx_dtype;
+
+/* Optional device-side counters (zero them before the call if you read them). */
+typedef struct idx_stats {
+    int emit_all_rows;   /* rows that see <= cap keys: every key became a candidate */
+    int overflow_rows;   /* rows whose candidate count exceeded the slab cap */
+    int short_rows;      /* rows with fewer than topk candidates although they see > cap keys */
+    int fallback_rows;   /* rows re-selected by the exact full-row rescan */
+    int max_count;       /* largest candidate count of any row */
+    int split_rows;      /* rows the standalone top-k selected with a multi-block row split */
+    int tie_rescan_rows; /* rows whose threshold bin overflowed the tie buffer */
+    int reserved;
+} idx_stats;
+
+/* Every field 0 selects the default.  Pass NULL for all defaults. */
+typedef struct idx_options {
+    float cap_factor;     /* slab cap = max(ceil(cap_factor*topk), 4096 clipped to 2*topk..);
+                             default 2.25 (page 1: about 2.25 x topk candidates) */
+    float target_factor;  /* expected candidates / topk that the sampled threshold aims
+                             at; default sqrt(cap/topk).  Test knob to force short or
+                             overflowing rows. */
+    int sample_stride;    /* odd stride S of the threshold sample; 0 = automatic */
+    int row_split;        /* standalone top-k: -1 or 0 = automatic ... see below */
+    int* d_status;        /* optional device int receiving IDX_DEV_* bits */
+    idx_stats* d_stats;   /* optional device counters */
+    int relative_rows;    /* idx_topk_from_scores: row r's visible scores start at
+                             column 0 of its row (the layout idx_score_materialise
+                             writes) instead of column ks[r] */
+    int reserved;
+} idx_options;
+
+/* row_split: 0 = automatic (page "[sglang] ROCm DSA Indexer Top-K 최적화",
+ * row_split function: split a row over g blocks when it is at least 65536 long
+ * and g = min(SMs / rows, 32) >= 4), -1 = never split, g >= 2 = force g blocks. */
+
+/* ------------------------------------------------------------------------
+ * idx_score_topk - fused score + exact top-k, without writing [rows, keys]
+ * logits (page 1, "Sampled Threshold" and section 1).
+ *
+ * Per row: a threshold T_r is taken from an odd-stride single-key sample of
+ * the row's own scores (page 1, section 2); one scoring pass emits only
+ * (score, key) pairs with score >= T_r into a per-row candidate slab of `cap`
+ * entries together with the exact count (page 1, section 1 parameter list);
+ * an exact radix top-k then selects from the slab.  Rows whose count ended
+ * below topk or above cap are re-selected exactly by a full-row rescan, so the
+ * result never depends on the sample (the page's own kernel stays lossy here;
+ * this library does not).
+ *
+ *   q, k, k_scale, w, ks, ke : inputs as in the conventions above
+ *   rows, keys, H, D, topk   : sizes; keys may exceed 2^31
+ *   max_len                  : an upper bound on ke[r] - ks[r] (0 = keys); it
+ *                              sizes the workspace
+ *   dt                       : element type of q and k
+ *   out_idx                  : [rows, topk] int32 result
+ *   ws, ws_bytes             : workspace, >= idx_score_topk_workspace(...)
+ * Returns IDX_OK or an error from the list above.
+ * ------------------------------------------------------------------------ */
+size_t idx_score_topk_workspace(int rows, long long keys, long long max_len, int H, int D,
+                                int topk, idx_dtype dt, const idx_options* opt);
+idx_status idx_score_topk(const void* q, const void* k, const float* k_scale, const float* w,
+                          const int* ks, const int* ke, int rows, long long keys,
+                          long long max_len, int H, int D, int topk, idx_dtype dt,
+                          int* out_idx, void* ws, size_t ws_bytes, const idx_options* opt,
+                          void* stream);
+
+/* ------------------------------------------------------------------------
+ * idx_topk_from_scores - exact top-k of given fp32 scores (page "[sglang] ROCm
+ * DSA Indexer Top-K 최적화": fp32 12-bit coarse histogram, radix tie
+ * refinement, full-row rescan when the threshold bin overflows the tie
+ * buffer, multi-block row split for long rows at low batch).
+ *
+ *   scores [rows, row_stride] fp32; row r's visible scores are
+ *          scores[r*row_stride + j] for ks[r] <= j < ke[r]
+ *          (or scores[r*row_stride + j - ks[r]] with options->relative_rows)
+ *   ks may be NULL (all rows start at 0).
+ *   out_idx [rows, topk]: ascending j - ks[r], then -1.
+ * The result is bit-exact: ties at equal fp32 values (+0 == -0) go to the
+ * lower index.  NaN scores are a precondition violation.
+ * ------------------------------------------------------------------------ */
+size_t idx_topk_workspace(int rows, long long row_stride, int topk, const idx_options* opt);
+idx_status idx_topk_from_scores(const float* scores, long long row_stride, const int* ks,
+                                const int* ke, int rows, int topk, int* out_idx, void* ws,
+                                size_t ws_bytes, const idx_options* opt, void* stream);
+
+/* ------------------------------------------------------------------------
+ * idx_score_materialise - the two-pass baseline's first pass (page 1,
+ * introduction: the full [rows, keys] logits written to global memory).
+ * Writes s[r,j] for ks[r] <= j < ke[r] to scores[r*row_stride + (j - ks[r])]
+ * (row_stride >= the longest visible range); other entries are not touched.
+ * Bit-identical to the scores the fused path compares against its threshold.
+ * Feed the result to idx_topk_from_scores with options->relative_rows = 1.
+ * ------------------------------------------------------------------------ */
+idx_status idx_score_materialise(const void* q, const void* k, const float* k_scale,
+                                 const float* w, const int* ks, const int* ke, int rows,
+                                 long long keys, int H, int D, idx_dtype dt, float* scores,
+                                 long long row_stride, const idx_options* opt, void* stream);
+
+/* Static text for a status code. */
+const char* idx_status_string(idx_status s);
+
+/* Library version, (major << 16) | minor. */
+int idx_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* IDX_H_ */

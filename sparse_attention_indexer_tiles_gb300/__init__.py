@@ -1,0 +1,215 @@
+"""Python binding of libidx, the GB300 (sm_103a) sparse-attention prefill indexer.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of ``libidx.so`` (built from ``csrc/`` by ``build.py``).  PyTorch
+provides device memory and the current stream.  There is no CPU path: when the
+library is missing or the GPU is not an sm_103 part, the calls raise.
+
+Entry points (same names as the C ABI in ``include/idx.h``):
+  idx_score_topk            fused score + exact top-k (no [rows, keys] logits)
+  idx_topk_from_scores      exact radix top-k of given fp32 scores
+  idx_score_materialise     the two-pass baseline's score pass
+  idx_score_topk_workspace, idx_topk_workspace, idx_status_string
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "IdxError", "Options", "Stats", "load", "idx_score_topk", "idx_score_topk_workspace",
+    "idx_topk_from_scores", "idx_topk_workspace", "idx_score_materialise",
+    "idx_status_string", "DTYPES", "STAT_FIELDS",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libidx.so")
+
+IDX_BF16, IDX_FP8_E4M3 = 1, 2
+DTYPES = {torch.bfloat16: IDX_BF16, torch.float8_e4m3fn: IDX_FP8_E4M3}
+STAT_FIELDS = ("emit_all_rows", "overflow_rows", "short_rows", "fallback_rows", "max_count",
+               "split_rows", "tie_rescan_rows", "reserved")
+
+
+class IdxError(RuntimeError):
+    def __init__(self, fn: str, code: int, text: str):
+        super().__init__(f"{fn} failed: {text} (status {code})")
+        self.code = code
+
+
+class Options(ctypes.Structure):
+    """Mirror of idx_options."""
+    _fields_ = [("cap_factor", ctypes.c_float), ("target_factor", ctypes.c_float),
+                ("sample_stride", ctypes.c_int), ("row_split", ctypes.c_int),
+                ("d_status", ctypes.c_void_p), ("d_stats", ctypes.c_void_p),
+                ("relative_rows", ctypes.c_int), ("reserved", ctypes.c_int)]
+
+
+class Stats:
+    """Device counters (idx_stats) plus the device status word."""
+
+    def __init__(self, device=None):
+        dev = device or torch.device("cuda", torch.cuda.current_device())
+        self.buf = torch.zeros(len(STAT_FIELDS) + 1, dtype=torch.int32, device=dev)
+
+    def reset(self):
+        self.buf.zero_()
+
+    @property
+    def stats_ptr(self) -> int:
+        return self.buf.data_ptr()
+
+    @property
+    def status_ptr(self) -> int:
+        return self.buf.data_ptr() + 4 * len(STAT_FIELDS)
+
+    def read(self) -> dict:
+        v = self.buf.cpu().tolist()
+        d = dict(zip(STAT_FIELDS, v[:len(STAT_FIELDS)]))
+        d["status"] = v[-1]
+        return d
+
+
+_lib = None
+
+
+def load(path: str | None = None):
+    """Load libidx.so (raises if it was not built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise ImportError(f"libidx.so not found at {p}; run "
+                          "`python -c 'import __graft_entry__ as g; g.build()'` first")
+    lib = ctypes.CDLL(p)
+    P, I, LL, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong, ctypes.c_size_t
+    lib.idx_score_topk_workspace.argtypes = [I, LL, LL, I, I, I, I, P]
+    lib.idx_score_topk_workspace.restype = SZ
+    lib.idx_score_topk.argtypes = [P, P, P, P, P, P, I, LL, LL, I, I, I, I, P, P, SZ, P, P]
+    lib.idx_score_topk.restype = I
+    lib.idx_topk_workspace.argtypes = [I, LL, I, P]
+    lib.idx_topk_workspace.restype = SZ
+    lib.idx_topk_from_scores.argtypes = [P, LL, P, P, I, I, P, P, SZ, P, P]
+    lib.idx_topk_from_scores.restype = I
+    lib.idx_score_materialise.argtypes = [P, P, P, P, P, P, I, LL, I, I, I, P, LL, P, P]
+    lib.idx_score_materialise.restype = I
+    lib.idx_status_string.argtypes = [I]
+    lib.idx_status_string.restype = ctypes.c_char_p
+    lib.idx_version.argtypes = []
+    lib.idx_version.restype = I
+    _lib = lib
+    return lib
+
+
+def idx_status_string(code: int) -> str:
+    return load().idx_status_string(int(code)).decode()
+
+
+def _check(fn: str, code: int):
+    if code != 0:
+        raise IdxError(fn, code, idx_status_string(code))
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _dev(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("idx: every tensor must live on a CUDA device")
+        if t is not None and not t.is_contiguous():
+            raise ValueError("idx: tensors must be contiguous")
+
+
+def make_options(options: Options | dict | None, stats: Stats | None = None) -> Options | None:
+    if options is None and stats is None:
+        return None
+    o = options if isinstance(options, Options) else Options(**(options or {}))
+    if stats is not None:
+        o.d_stats = stats.stats_ptr
+        o.d_status = stats.status_ptr
+    return o
+
+
+def _opt_ref(o: Options | None):
+    return None if o is None else ctypes.byref(o)
+
+
+def idx_score_topk_workspace(rows: int, keys: int, max_len: int, H: int, D: int, topk: int,
+                             dtype, options=None) -> int:
+    dt = DTYPES[dtype] if not isinstance(dtype, int) else dtype
+    o = make_options(options)
+    return int(load().idx_score_topk_workspace(rows, keys, max_len, H, D, topk, dt, _opt_ref(o)))
+
+
+def idx_score_topk(q, k, k_scale, w, ks, ke, topk: int, *, max_len: int = 0, out=None, ws=None,
+                   options=None, stats: Stats | None = None, stream=None):
+    """Exact top-k indices [rows, topk] int32 (ascending, -1 padded)."""
+    _dev(q, k, k_scale, w, ks, ke, out, ws)
+    rows, H, D = q.shape
+    keys = k.shape[0]
+    dt = DTYPES[q.dtype]
+    o = make_options(options, stats)
+    need = idx_score_topk_workspace(rows, keys, max_len, H, D, topk, dt, o)
+    if out is None:
+        out = torch.empty(rows, topk, dtype=torch.int32, device=q.device)
+    if ws is None:
+        ws = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _check("idx_score_topk", load().idx_score_topk(
+        _ptr(q), _ptr(k), _ptr(k_scale), _ptr(w), _ptr(ks), _ptr(ke), rows, keys, max_len, H, D,
+        topk, dt, _ptr(out), _ptr(ws), ws.numel() * ws.element_size(), _opt_ref(o),
+        _stream(stream)))
+    return out
+
+
+def idx_topk_workspace(rows: int, row_stride: int, topk: int, options=None) -> int:
+    return int(load().idx_topk_workspace(rows, row_stride, topk, _opt_ref(make_options(options))))
+
+
+def idx_topk_from_scores(scores, ks, ke, topk: int, *, out=None, ws=None, options=None,
+                         stats: Stats | None = None, stream=None):
+    """Exact top-k of fp32 scores [rows, row_stride]; ks may be None."""
+    _dev(scores, ks, ke, out, ws)
+    if scores.dtype != torch.float32:
+        raise ValueError("idx_topk_from_scores: scores must be float32")
+    rows, stride = scores.shape
+    o = make_options(options, stats)
+    need = int(load().idx_topk_workspace(rows, stride, topk, _opt_ref(o)))
+    if out is None:
+        out = torch.empty(rows, topk, dtype=torch.int32, device=scores.device)
+    if ws is None and need:
+        ws = torch.empty(need, dtype=torch.uint8, device=scores.device)
+    nbytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check("idx_topk_from_scores", load().idx_topk_from_scores(
+        _ptr(scores), stride, _ptr(ks), _ptr(ke), rows, topk, _ptr(out), _ptr(ws), nbytes,
+        _opt_ref(o), _stream(stream)))
+    return out
+
+
+def idx_score_materialise(q, k, k_scale, w, ks, ke, *, out=None, row_stride: int | None = None,
+                          options=None, stats: Stats | None = None, stream=None):
+    """fp32 scores [rows, row_stride]; row r's key j at column j - ks[r]."""
+    _dev(q, k, k_scale, w, ks, ke, out)
+    rows, H, D = q.shape
+    keys = k.shape[0]
+    if out is None:
+        stride = row_stride or keys
+        out = torch.empty(rows, stride, dtype=torch.float32, device=q.device)
+    stride = out.shape[1]
+    o = make_options(options, stats)
+    _check("idx_score_materialise", load().idx_score_materialise(
+        _ptr(q), _ptr(k), _ptr(k_scale), _ptr(w), _ptr(ks), _ptr(ke), rows, keys, H, D,
+        DTYPES[q.dtype], _ptr(out), stride, _opt_ref(o), _stream(stream)))
+    return out

@@ -1,0 +1,371 @@
+// C ABI of libidx: argument validation, workspace carving and the launch
+// sequence of each entry point.  Everything that computes runs in the kernels
+// of topk.cu and score_*.cu; this file only decides what to launch.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "plan.cuh"
+#include "score.cuh"
+#include "topk.cuh"
+
+namespace idx {
+
+cudaError_t launch_score_bf16(const ScoreLaunch& L, cudaStream_t s);
+cudaError_t launch_score_fp8(const ScoreLaunch& L, cudaStream_t s);
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+bool score_supported(idx_dtype dt, int H, int D) {
+    const bool h_ok = H == 8 || H == 16 || H == 32 || H == 64;
+    const bool d_ok = D == 64 || D == 128;
+    return h_ok && d_ok && (dt == IDX_BF16 || dt == IDX_FP8_E4M3);
+}
+
+cudaError_t launch_score(const ScoreLaunch& L, cudaStream_t s) {
+    if (L.dt == IDX_BF16) return launch_score_bf16(L, s);
+    return launch_score_fp8(L, s);
+}
+
+namespace {
+
+constexpr int kMaxTopk = 4096;
+constexpr int kMaxCap = 24576;
+constexpr uint32_t kPhaseSeed = 0x9E3779B9u;
+
+// Is the current device an sm_103 part?  Cached per device.
+bool arch_ok() {
+    static std::mutex mu;
+    static int cached[64];
+    static bool init = false;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+    std::lock_guard<std::mutex> g(mu);
+    if (!init) {
+        for (int& c : cached) c = -1;
+        init = true;
+    }
+    if (cached[dev] < 0) {
+        int maj = 0, min = 0;
+        cudaDeviceGetAttribute(&maj, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&min, cudaDevAttrComputeCapabilityMinor, dev);
+        cached[dev] = (maj == 10 && min == 3) ? 1 : 0;
+    }
+    return cached[dev] == 1;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+struct FusedParams {
+    int cap;
+    float target;
+    int S;
+};
+
+// Slab cap, threshold target and sample stride of the fused path.
+//   cap    = ceil(cap_factor * topk) when cap_factor is given, else
+//            max(ceil(2.25 * topk), 4096)
+//   target = expected candidates / topk the sampled threshold aims at; the
+//            geometric middle sqrt(cap / topk) of [1, cap / topk] by default
+//   S      = the largest odd stride from the table that still leaves about
+//            t = max(32, (4.5 / ln target)^2) sample hits above the threshold
+//            (the relative spread of the candidate count is ~ 1/sqrt(t), so
+//            4.5 spreads fit between topk and cap)
+FusedParams fused_params(int topk, const idx_options* opt) {
+    FusedParams p;
+    const double cf = opt && opt->cap_factor > 0.f ? (double)opt->cap_factor : 0.0;
+    if (cf > 0.0)
+        p.cap = (int)std::ceil(cf * topk);
+    else
+        p.cap = std::max((int)std::ceil(2.25 * topk), 4096);
+    if (p.cap < topk) p.cap = topk;
+    const double ratio = (double)p.cap / topk;
+    double target = opt && opt->target_factor > 0.f ? (double)opt->target_factor : std::sqrt(ratio);
+    p.target = (float)target;
+    if (opt && opt->sample_stride > 0) {
+        p.S = opt->sample_stride;
+    } else {
+        static const int table[] = {1, 3, 5, 7, 11, 15, 23, 31, 45, 63};
+        const double lt = std::log(std::max(target, 1.0001));
+        const double t = std::max(32.0, (4.5 / lt) * (4.5 / lt));
+        const double smax = target * topk / t;
+        p.S = 1;
+        for (int s : table)
+            if (s <= smax) p.S = s;
+    }
+    return p;
+}
+
+struct FusedLayout {
+    size_t plan, slab_s, slab_i, samp, fb_hist, total;
+    long long samp_stride;
+};
+
+FusedLayout fused_layout(int rows, long long max_len, int cap, int S) {
+    FusedLayout L;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off = align_up(off + bytes, 256);
+        return o;
+    };
+    L.samp_stride = max_len / S + 2;
+    L.plan = take((size_t)rows * sizeof(RowPlan));
+    L.slab_s = take((size_t)rows * cap * sizeof(float));
+    L.slab_i = take((size_t)rows * cap * sizeof(int));
+    L.samp = take(max_len > cap ? (size_t)rows * L.samp_stride * sizeof(float) : 0);
+    L.fb_hist = take(max_len > cap ? (size_t)rows * 4096 * sizeof(uint32_t) : 0);
+    L.total = off;
+    return L;
+}
+
+idx_status check_indexer_args(const void* q, const void* k, const float* k_scale, const float* w,
+                              const int* ks, const int* ke, int rows, long long keys, int H, int D,
+                              idx_dtype dt) {
+    if (rows < 0 || keys < 0) return IDX_EINVAL;
+    if (dt != IDX_BF16 && dt != IDX_FP8_E4M3) return IDX_EUNSUPPORTED;
+    if (!score_supported(dt, H, D)) return IDX_EUNSUPPORTED;
+    if (rows == 0) return IDX_OK;
+    if (!q || !k || !k_scale || !w || !ks || !ke) return IDX_EINVAL;
+    if (keys < 1 || keys > 0x7fffff00ll || (long long)rows * H > 0x7fffff00ll) return IDX_EUNSUPPORTED;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(k_scale, 4) || !aligned(w, 4) ||
+        !aligned(ks, 4) || !aligned(ke, 4))
+        return IDX_EALIGN;
+    if (!arch_ok()) return IDX_EUNSUPPORTED;
+    return IDX_OK;
+}
+
+ScoreLaunch make_score_launch(const void* q, const void* k, const float* k_scale, const float* w,
+                              const int* ks, const int* ke, int rows, long long keys, int H, int D,
+                              idx_dtype dt, int topk, const idx_options* opt) {
+    ScoreLaunch L;
+    std::memset(&L, 0, sizeof(L));
+    L.q = q;
+    L.k = k;
+    L.H = H;
+    L.D = D;
+    L.dt = dt;
+    L.a.k_scale = k_scale;
+    L.a.w = w;
+    L.a.ks = ks;
+    L.a.ke = ke;
+    L.a.rows = rows;
+    L.a.keys = keys;
+    L.a.topk = topk;
+    L.a.d_status = opt ? opt->d_status : nullptr;
+    L.a.d_stats = opt ? opt->d_stats : nullptr;
+    return L;
+}
+
+idx_status cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return IDX_OK;
+    cudaGetLastError();  // clear a sticky launch error of ours
+    return e == cudaErrorNotSupported ? IDX_EUNSUPPORTED : IDX_ECUDA;
+}
+
+}  // namespace
+}  // namespace idx
+
+using namespace idx;
+
+extern "C" {
+
+const char* idx_status_string(idx_status s) {
+    switch (s) {
+        case IDX_OK: return "ok";
+        case IDX_EINVAL: return "invalid argument";
+        case IDX_EALIGN: return "misaligned pointer";
+        case IDX_EWORKSPACE: return "workspace too small";
+        case IDX_EUNSUPPORTED: return "unsupported dtype, shape or GPU";
+        case IDX_ECUDA: return "CUDA error";
+        case IDX_ETIMEOUT: return "device wait timed out";
+    }
+    return "unknown status";
+}
+
+int idx_version(void) { return (0 << 16) | 1; }
+
+size_t idx_score_topk_workspace(int rows, long long keys, long long max_len, int H, int D,
+                                int topk, idx_dtype dt, const idx_options* opt) {
+    (void)H;
+    (void)D;
+    (void)dt;
+    if (rows <= 0 || topk < 1 || topk > kMaxTopk) return 0;
+    if (max_len <= 0 || max_len > keys) max_len = keys;
+    const FusedParams p = fused_params(topk, opt);
+    return fused_layout(rows, max_len, p.cap, p.S).total;
+}
+
+idx_status idx_score_topk(const void* q, const void* k, const float* k_scale, const float* w,
+                          const int* ks, const int* ke, int rows, long long keys, long long max_len,
+                          int H, int D, int topk, idx_dtype dt, int* out_idx, void* ws,
+                          size_t ws_bytes, const idx_options* opt, void* stream) {
+    if (topk < 1) return IDX_EINVAL;
+    if (topk > kMaxTopk) return IDX_EUNSUPPORTED;
+    idx_status st = check_indexer_args(q, k, k_scale, w, ks, ke, rows, keys, H, D, dt);
+    if (st != IDX_OK || rows == 0) return st;
+    if (!out_idx) return IDX_EINVAL;
+    if (!aligned(out_idx, 4)) return IDX_EALIGN;
+    if (max_len <= 0 || max_len > keys) max_len = keys;
+    const FusedParams p = fused_params(topk, opt);
+    if (p.cap > kMaxCap || p.S < 1) return IDX_EUNSUPPORTED;
+    const FusedLayout lay = fused_layout(rows, max_len, p.cap, p.S);
+    if (!ws || ws_bytes < lay.total) return IDX_EWORKSPACE;
+    if (!aligned(ws, 256)) return IDX_EALIGN;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    RowPlan* plan = reinterpret_cast<RowPlan*>(base + lay.plan);
+    float* slab_s = reinterpret_cast<float*>(base + lay.slab_s);
+    int* slab_i = reinterpret_cast<int*>(base + lay.slab_i);
+    float* samp = reinterpret_cast<float*>(base + lay.samp);
+    uint32_t* fb_hist = reinterpret_cast<uint32_t*>(base + lay.fb_hist);
+    int* d_status = opt ? opt->d_status : nullptr;
+    idx_stats* d_stats = opt ? opt->d_stats : nullptr;
+    const bool sampling = max_len > p.cap;
+
+    ScoreLaunch L = make_score_launch(q, k, k_scale, w, ks, ke, rows, keys, H, D, dt, topk, opt);
+    L.a.plan = plan;
+    L.a.slab_s = slab_s;
+    L.a.slab_i = slab_i;
+    L.a.cap = p.cap;
+    L.a.fb_hist = fb_hist;
+    L.a.S = p.S;
+    L.a.nsamp = keys / p.S;
+    L.a.samp = samp;
+    L.a.samp_stride = lay.samp_stride;
+    L.a.phase_seed = kPhaseSeed;
+    cudaError_t e;
+
+    if (sampling) {
+        // 1. score the odd-stride sample of every long row
+        L.a.mode = SM_SAMPLE;
+        if ((e = launch_score(L, s)) != cudaSuccess) return cuda_status(e);
+        // 2. T_r = exact t-th largest sample score of each row
+        TopkRowsArgs t;
+        std::memset(&t, 0, sizeof(t));
+        t.scores = samp;
+        t.row_stride = lay.samp_stride;
+        t.row_len = lay.samp_stride;
+        t.rows = rows;
+        t.topk = topk;
+        t.relative = 1;
+        t.mode = TOPK_THRESHOLD;
+        t.plan = plan;
+        t.vis_ks = ks;
+        t.vis_ke = ke;
+        t.cap = p.cap;
+        t.target = p.target;
+        t.S = p.S;
+        t.nsamp = keys / p.S;
+        t.rows_per_block = score_rows_per_block(H);
+        t.phase_seed = kPhaseSeed;
+        t.d_status = d_status;
+        t.d_stats = d_stats;
+        if ((e = launch_topk_rows(t, s)) != cudaSuccess) return cuda_status(e);
+    }
+    // 3. one scoring pass emits every key at or above T_r into the slab
+    L.a.mode = SM_EMIT;
+    if ((e = launch_score(L, s)) != cudaSuccess) return cuda_status(e);
+    // 4. exact top-k of every slab; rows whose count missed [topk, cap] are flagged
+    CandArgs c;
+    std::memset(&c, 0, sizeof(c));
+    c.slab_s = slab_s;
+    c.slab_i = slab_i;
+    c.plan = plan;
+    c.fb_hist = sampling ? fb_hist : nullptr;
+    c.ks = ks;
+    c.ke = ke;
+    c.rows = rows;
+    c.topk = topk;
+    c.cap = p.cap;
+    c.out = out_idx;
+    c.d_status = d_status;
+    c.d_stats = d_stats;
+    c.fallback = 0;
+    if ((e = launch_cand_topk(c, s)) != cudaSuccess) return cuda_status(e);
+    if (sampling) {
+        // 5. exact rescan of flagged rows: up to three digit passes, one re-emission
+        FbPickArgs fp{plan, fb_hist, rows, topk, p.cap, 0};
+        for (int level = 0; level <= 2; ++level) {
+            L.a.mode = SM_FB_HIST;
+            L.a.level = level;
+            if ((e = launch_score(L, s)) != cudaSuccess) return cuda_status(e);
+            fp.level = level;
+            if ((e = launch_fb_pick(fp, s)) != cudaSuccess) return cuda_status(e);
+        }
+        L.a.mode = SM_FB_EMIT;
+        if ((e = launch_score(L, s)) != cudaSuccess) return cuda_status(e);
+        c.fallback = 1;
+        if ((e = launch_cand_topk(c, s)) != cudaSuccess) return cuda_status(e);
+    }
+    return IDX_OK;
+}
+
+size_t idx_topk_workspace(int rows, long long row_stride, int topk, const idx_options* opt) {
+    (void)rows;
+    (void)row_stride;
+    (void)topk;
+    (void)opt;
+    return 0;
+}
+
+idx_status idx_topk_from_scores(const float* scores, long long row_stride, const int* ks,
+                                const int* ke, int rows, int topk, int* out_idx, void* ws,
+                                size_t ws_bytes, const idx_options* opt, void* stream) {
+    (void)ws;
+    (void)ws_bytes;
+    if (rows < 0 || topk < 1 || row_stride < 0) return IDX_EINVAL;
+    if (topk > kMaxTopk) return IDX_EUNSUPPORTED;
+    if (rows == 0) return IDX_OK;
+    if (!scores || !ke || !out_idx) return IDX_EINVAL;
+    if (!aligned(scores, 4) || !aligned(out_idx, 4) || !aligned(ke, 4) || (ks && !aligned(ks, 4)))
+        return IDX_EALIGN;
+    if (!arch_ok()) return IDX_EUNSUPPORTED;
+    TopkRowsArgs t;
+    std::memset(&t, 0, sizeof(t));
+    t.scores = scores;
+    t.row_stride = row_stride;
+    t.row_len = row_stride;
+    t.ks = ks;
+    t.ke = ke;
+    t.rows = rows;
+    t.topk = topk;
+    t.relative = opt ? opt->relative_rows : 0;
+    t.mode = TOPK_OUTPUT;
+    t.out = out_idx;
+    t.d_status = opt ? opt->d_status : nullptr;
+    t.d_stats = opt ? opt->d_stats : nullptr;
+    return cuda_status(launch_topk_rows(t, static_cast<cudaStream_t>(stream)));
+}
+
+idx_status idx_score_materialise(const void* q, const void* k, const float* k_scale,
+                                 const float* w, const int* ks, const int* ke, int rows,
+                                 long long keys, int H, int D, idx_dtype dt, float* scores,
+                                 long long row_stride, const idx_options* opt, void* stream) {
+    idx_status st = check_indexer_args(q, k, k_scale, w, ks, ke, rows, keys, H, D, dt);
+    if (st != IDX_OK || rows == 0) return st;
+    if (!scores || row_stride < 1) return IDX_EINVAL;
+    if (!aligned(scores, 4)) return IDX_EALIGN;
+    ScoreLaunch L = make_score_launch(q, k, k_scale, w, ks, ke, rows, keys, H, D, dt, 1, opt);
+    L.a.mode = SM_MATERIALISE;
+    L.a.out = scores;
+    L.a.out_stride = row_stride;
+    return cuda_status(launch_score(L, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

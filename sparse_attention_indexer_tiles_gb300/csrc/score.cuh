@@ -1,0 +1,66 @@
+// Host-visible interface of the tcgen05 scoring kernel.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/idx.h"
+#include "plan.cuh"
+
+namespace idx {
+
+// What the epilogue does with the fp32 scores of a key tile.
+enum : int {
+    SM_MATERIALISE = 0,  // write s[r, j - ks[r]]
+    SM_SAMPLE = 1,       // score the strided sample, write samp[r, i - a_r]
+    SM_EMIT = 2,         // main pass: emit key >= T_r into the slab
+    SM_FB_HIST = 3,      // exact rescan: histogram one digit of flagged rows
+    SM_FB_EMIT = 4,      // exact rescan: re-emit flagged rows with the refined rule
+};
+
+struct ScoreArgs {
+    const float* k_scale;
+    const float* w;
+    const int* ks;
+    const int* ke;
+    int rows;
+    int topk;
+    long long keys;
+    int mode;
+    // SM_MATERIALISE
+    float* out;
+    long long out_stride;
+    // SM_SAMPLE
+    float* samp;
+    long long samp_stride;
+    int S;
+    long long nsamp;
+    uint32_t phase_seed;
+    // SM_EMIT / SM_FB_*
+    RowPlan* plan;
+    float* slab_s;
+    int* slab_i;
+    int cap;
+    uint32_t* fb_hist;
+    int level;
+    int* d_status;
+    idx_stats* d_stats;
+};
+
+struct ScoreLaunch {
+    const void* q;
+    const void* k;
+    int H, D;
+    idx_dtype dt;
+    ScoreArgs a;
+};
+
+// Rows handled by one CTA (the MMA's N = rows x H = 256).
+inline int score_rows_per_block(int H) { return 256 / H; }
+
+bool score_supported(idx_dtype dt, int H, int D);
+cudaError_t launch_score(const ScoreLaunch& L, cudaStream_t s);
+
+}  // namespace idx

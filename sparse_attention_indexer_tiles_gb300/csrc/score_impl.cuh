@@ -1,0 +1,464 @@
+// The tcgen05 scoring kernel of libidx (sm_103a).
+//
+// Page "[sglang] logits를 쓰지 않는 top-k", section 1: a KV tile is the A
+// operand (M = keys) of the tensor-core MMA, the accumulator lives in TMEM,
+// every epilogue thread owns one key of the tile and reduces the heads in
+// registers.  Here:
+//   A = 128 keys x D        (TMA, 128/64-byte swizzle, a ring of stages)
+//   B = 256 (row, head) x D (TMA, loaded once: rows_per_block = 256 / H rows)
+//   D = 128 x 256 fp32 in TMEM, double buffered (2 x 256 columns), so the
+//       epilogue of tile t overlaps the MMA of tile t + 1.
+// Warp roles (12 warps): 0 = TMA producer, 1 = TMEM owner + MMA issuer,
+// 4..11 = epilogue (two warpgroups, each owning half of the block's rows; a
+// warp reads the TMEM lane quarter 32 * (warp % 4)).
+//
+// Score of (row, key), summed over heads in ascending order in fp32:
+//   s = k_scale[key] * sum_h fma(w[row,h], max(acc[h], 0), .)
+// Every mode runs the same arithmetic, so the fused path compares exactly the
+// scores that the materialising baseline writes.
+#pragma once
+
+#include "plan.cuh"
+#include "radix.cuh"
+#include "score.cuh"
+
+namespace idx {
+
+template <int DT, int H, int RB>
+struct ScoreCfg {
+    static constexpr int R = 256 / H;                       // rows per CTA
+    static constexpr int N = 256;                           // MMA N
+    static constexpr int M = 128;                           // keys per tile
+    static constexpr int CHUNK_B = RB >= 128 ? 128 : RB;    // swizzle width
+    static constexpr int NCHUNK = RB / CHUNK_B;             // 128-byte slices of a row
+    static constexpr int ELEM = DT == IDX_BF16 ? 2 : 1;
+    static constexpr int CHUNK_ELEMS = CHUNK_B / ELEM;
+    static constexpr int KSTEP_B = 32;                      // bytes of K per MMA
+    static constexpr int KSTEPS = CHUNK_B / KSTEP_B;
+    static constexpr int A_BYTES = M * RB;
+    static constexpr int A_CHUNK = M * CHUNK_B;
+    static constexpr int B_BYTES = N * RB;
+    static constexpr int B_CHUNK = N * CHUNK_B;
+    static constexpr int NS = RB >= 256 ? 4 : (RB == 128 ? 6 : 8);
+    static constexpr int RH = R / 2;                        // rows per epilogue warpgroup
+    static constexpr int THREADS = 384;
+    static constexpr uint32_t IDESC = instr_desc(DT == IDX_BF16 ? 1u : 0u, M, N);
+    // shared memory carve (offsets from a 1024-byte aligned base)
+    static constexpr int OFF_B = 0;
+    static constexpr int OFF_A = B_BYTES;
+    static constexpr int OFF_BAR = OFF_A + NS * A_BYTES;
+    static constexpr int NBAR = 2 * NS + 7;
+    static constexpr int OFF_TSLOT = OFF_BAR + NBAR * 8;
+    static constexpr int OFF_W = (OFF_TSLOT + 16 + 15) / 16 * 16;
+    static constexpr int OFF_META = OFF_W + R * H * 4;
+    static constexpr int META_WORDS = 12;                   // per row
+    static constexpr int OFF_BAL = OFF_META + R * META_WORDS * 4;
+    static constexpr int BAL_WORDS = 2 * 2 * RH * 4 * 2;    // parity x wg x row x warp x {above, tie}
+    static constexpr int OFF_MISC = OFF_BAL + BAL_WORDS * 4;
+    static constexpr int SMEM_USED = OFF_MISC + 64;
+    // at least ~120 KB so that one CTA owns an SM (and its 512 TMEM columns)
+    static constexpr int SMEM_ALLOC = (SMEM_USED + 1024 > 122880 ? SMEM_USED + 1024 : 122880);
+};
+
+// per-row metadata words in shared memory
+enum : int {
+    MW_ACTIVE = 0, MW_KS_LO, MW_KS_HI, MW_KE_LO, MW_KE_HI, MW_THR, MW_QUOTA, MW_PREFIX,
+    MW_SA_LO, MW_SA_HI, MW_SB_LO, MW_SB_HI
+};
+
+IDX_DEVI long long meta_ll(const int* m, int lo) {
+    return (long long)(((unsigned long long)(uint32_t)m[lo + 1] << 32) | (uint32_t)m[lo]);
+}
+IDX_DEVI void set_meta_ll(int* m, int lo, long long v) {
+    m[lo] = (int)(uint32_t)((unsigned long long)v & 0xffffffffull);
+    m[lo + 1] = (int)(uint32_t)((unsigned long long)v >> 32);
+}
+
+template <int DT, int H, int RB>
+__global__ void __launch_bounds__(384, 1)
+score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+             const __grid_constant__ CUtensorMap tm_ks, const __grid_constant__ ScoreArgs a) {
+    using C = ScoreCfg<DT, H, RB>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+    uint64_t* full = bars;
+    uint64_t* empty = bars + C::NS;
+    uint64_t* accf = bars + 2 * C::NS;
+    uint64_t* acce = accf + 2;
+    uint64_t* qfull = acce + 2;
+    uint64_t* exch = qfull + 1;  // [2]: the 4 warps of an epilogue warpgroup, once per tile
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + C::OFF_TSLOT);
+    float* w_s = reinterpret_cast<float*>(smem + C::OFF_W);
+    int* meta = reinterpret_cast<int*>(smem + C::OFF_META);
+    uint32_t* bal = reinterpret_cast<uint32_t*>(smem + C::OFF_BAL);
+    long long* misc_ll = reinterpret_cast<long long*>(smem + C::OFF_MISC);  // [0] t0, [1] ntiles
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 16);
+    int* misc_i = reinterpret_cast<int*>(smem + C::OFF_MISC + 20);          // [0] phase
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int r0 = blockIdx.x * C::R;
+    const int mode = a.mode;
+    const long long phase =
+        mode == SM_SAMPLE ? (long long)(hash32((uint32_t)blockIdx.x ^ a.phase_seed) % (uint32_t)a.S) : 0;
+
+    // ---- per-row metadata
+    if (tid < C::R) {
+        int* m = meta + tid * C::META_WORDS;
+        const int r = r0 + tid;
+        long long ks = 0, ke = 0;
+        int active = 0;
+        uint32_t thr = 0, prefix = 0;
+        int quota = 0;
+        if (r < a.rows) {
+            ks = a.ks[r];
+            ke = a.ke[r];
+            if (ks < 0 || ke > a.keys || ks > ke) {
+                if (ke > ks || ks < 0) raise_status(a.d_status, IDX_DEV_RANGE);
+                ks = ke = 0;
+            }
+            const long long n = ke - ks;
+            switch (mode) {
+                case SM_MATERIALISE:
+                    active = n > 0;
+                    if (n > a.out_stride) {
+                        raise_status(a.d_status, IDX_DEV_RANGE);
+                        active = 0;
+                    }
+                    break;
+                case SM_SAMPLE: active = n > a.cap; break;
+                case SM_EMIT:
+                    // rows that see at most cap keys emit every key (page 1,
+                    // section 1: blocks of short rows store every score)
+                    active = n > a.topk;
+                    if (active && n > a.cap) thr = a.plan[r].thr;
+                    break;
+                case SM_FB_HIST: {
+                    const RowPlan p = a.plan[r];
+                    active = n > 0 && p.state == ST_HIST && p.level == a.level;
+                    prefix = p.prefix;
+                } break;
+                case SM_FB_EMIT: {
+                    const RowPlan p = a.plan[r];
+                    active = n > 0 && p.state == ST_EMIT;
+                    thr = p.thr;
+                    quota = p.quota;
+                } break;
+            }
+        }
+        m[MW_ACTIVE] = active;
+        set_meta_ll(m, MW_KS_LO, ks);
+        set_meta_ll(m, MW_KE_LO, ke);
+        m[MW_THR] = (int)thr;
+        m[MW_QUOTA] = quota;
+        m[MW_PREFIX] = (int)prefix;
+        if (mode == SM_SAMPLE) {
+            const SampleSpan sp = sample_span(ks, ke, phase, a.S, a.nsamp);
+            if (active && sp.b - sp.a > a.samp_stride) {
+                raise_status(a.d_status, IDX_DEV_RANGE);  // longer than max_len
+                active = 0;
+                m[MW_ACTIVE] = 0;
+            }
+            set_meta_ll(m, MW_SA_LO, sp.a);
+            set_meta_ll(m, MW_SB_LO, sp.b);
+        } else {
+            set_meta_ll(m, MW_SA_LO, ks);
+            set_meta_ll(m, MW_SB_LO, ke);
+        }
+    }
+    for (int i = tid; i < C::R * H; i += C::THREADS) {
+        const long long r = r0 + i / H;
+        w_s[i] = r < a.rows ? a.w[(long long)r0 * H + i] : 0.f;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        long long lo = 0x7fffffffffffffffll, hi = -1;
+        for (int j = 0; j < C::R; ++j) {
+            const int* m = meta + j * C::META_WORDS;
+            if (!m[MW_ACTIVE]) continue;
+            const long long sa = meta_ll(m, MW_SA_LO), sb = meta_ll(m, MW_SB_LO);
+            if (sb <= sa) continue;
+            lo = sa < lo ? sa : lo;
+            hi = sb > hi ? sb : hi;
+        }
+        long long t0 = 0, nt = 0;
+        if (hi > lo) {
+            t0 = lo / C::M;
+            nt = (hi + C::M - 1) / C::M - t0;
+        }
+        misc_ll[0] = t0;
+        misc_ll[1] = nt;
+        *abort_flag = 0;
+        misc_i[0] = (int)phase;
+        for (int i = 0; i < C::NS; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&accf[i], 1);
+            mbar_init(&acce[i], 8);
+        }
+        mbar_init(qfull, 1);
+        mbar_init(&exch[0], 4);
+        mbar_init(&exch[1], 4);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    const long long t0 = misc_ll[0];
+    const long long ntiles = misc_ll[1];
+    if (ntiles == 0) return;  // no active row in this block
+
+    if (warp == 1) {
+        __syncwarp();
+        tmem_alloc(tslot, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            prefetch_tmap(&tm_q);
+            prefetch_tmap(mode == SM_SAMPLE ? (const void*)&tm_ks : (const void*)&tm_k);
+            mbar_arrive_expect_tx(qfull, C::B_BYTES);
+#pragma unroll
+            for (int c = 0; c < C::NCHUNK; ++c)
+                tma_load_2d(smem + C::OFF_B + c * C::B_CHUNK, &tm_q, qfull, c * C::CHUNK_ELEMS,
+                            r0 * H);
+            long long issued = 0;
+            for (long long i = 0; i < ntiles; ++i) {
+                const int s = (int)(i % C::NS);
+                const uint32_t use = (uint32_t)(i / C::NS);
+                if (i >= C::NS && !mbar_wait(&empty[s], (use & 1u) ^ 1u, abort_flag)) {
+                    *abort_flag = 1;
+                    raise_status(a.d_status, IDX_DEV_TIMEOUT);
+                    break;
+                }
+                mbar_arrive_expect_tx(&full[s], C::A_BYTES);
+                const int row0 = (int)((t0 + i) * C::M);
+#pragma unroll
+                for (int c = 0; c < C::NCHUNK; ++c) {
+                    uint8_t* dst = smem + C::OFF_A + s * C::A_BYTES + c * C::A_CHUNK;
+                    if (mode == SM_SAMPLE)
+                        tma_load_3d(dst, &tm_ks, &full[s], c * C::CHUNK_ELEMS, (int)phase, row0);
+                    else
+                        tma_load_2d(dst, &tm_k, &full[s], c * C::CHUNK_ELEMS, row0);
+                }
+                issued = i + 1;
+            }
+            // do not leave with copies in flight: wait (bounded) for the last stages
+            for (long long i = issued > C::NS ? issued - C::NS : 0; i < issued; ++i)
+                mbar_wait(&full[i % C::NS], (uint32_t)((i / C::NS) & 1), nullptr, 1ll << 28);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t a_base = smem_u32(smem + C::OFF_A);
+            const uint32_t b_base = smem_u32(smem + C::OFF_B);
+            bool ok = mbar_wait(qfull, 0, abort_flag);
+            long long issued = 0;
+            for (long long i = 0; ok && i < ntiles; ++i) {
+                const int s = (int)(i % C::NS);
+                const int b = (int)(i & 1);
+                if (i >= 2 && !mbar_wait(&acce[b], (uint32_t)(((i >> 1) & 1) ^ 1), abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                if (!mbar_wait(&full[s], (uint32_t)((i / C::NS) & 1), abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem + (uint32_t)(b * C::N);
+#pragma unroll
+                for (int c = 0; c < C::NCHUNK; ++c) {
+#pragma unroll
+                    for (int kk = 0; kk < C::KSTEPS; ++kk) {
+                        const uint64_t ad =
+                            smem_desc(a_base + s * C::A_BYTES + c * C::A_CHUNK + kk * C::KSTEP_B,
+                                      C::CHUNK_B);
+                        const uint64_t bd =
+                            smem_desc(b_base + c * C::B_CHUNK + kk * C::KSTEP_B, C::CHUNK_B);
+                        const uint32_t acc = (c | kk) != 0;
+                        if (DT == IDX_BF16)
+                            mma_bf16(d, ad, bd, C::IDESC, acc);
+                        else
+                            mma_fp8(d, ad, bd, C::IDESC, acc);
+                    }
+                }
+                mma_commit(&empty[s]);
+                mma_commit(&accf[b]);
+                issued = i + 1;
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                raise_status(a.d_status, IDX_DEV_TIMEOUT);
+            }
+            // wait (bounded) until the tensor core is done with TMEM
+            if (issued > 0)
+                mbar_wait(&accf[(issued - 1) & 1], (uint32_t)(((issued - 1) >> 1) & 1), nullptr,
+                          1ll << 28);
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------ epilogue
+        const int q = warp & 3;       // TMEM lane quarter
+        const int wg = (warp - 4) >> 2;
+        int cnt[C::RH];
+        int ties[C::RH];
+#pragma unroll
+        for (int j = 0; j < C::RH; ++j) cnt[j] = ties[j] = 0;
+
+        for (long long i = 0; i < ntiles; ++i) {
+            const int b = (int)(i & 1);
+            // warp-uniform outcome: the TMEM loads below are .sync.aligned
+            if (!__all_sync(0xffffffffu, mbar_wait(&accf[b], (uint32_t)((i >> 1) & 1), abort_flag))) {
+                *abort_flag = 1;
+                if (lane == 0) raise_status(a.d_status, IDX_DEV_TIMEOUT);
+                break;
+            }
+            tc_fence_after();
+            const long long kidx = (t0 + i) * C::M + q * 32 + lane;  // key, or sample index
+            const long long key = mode == SM_SAMPLE ? phase + (long long)a.S * kidx : kidx;
+            const bool in_keys = mode == SM_SAMPLE ? (kidx < a.nsamp) : (key < a.keys);
+            const float scale = in_keys ? __ldg(a.k_scale + key) : 0.f;
+
+            float sc[C::RH];
+#pragma unroll
+            for (int j = 0; j < C::RH; ++j) {
+                const int rr = wg * C::RH + j;
+                const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * C::N + rr * H);
+                float v[H];
+                if constexpr (H % 16 == 0) {
+#pragma unroll
+                    for (int c = 0; c < H / 16; ++c) tmem_ld16(taddr + c * 16, v + c * 16);
+                } else {
+                    tmem_ld8(taddr, v);
+                }
+                tmem_ld_wait();
+                const float* wr = w_s + rr * H;
+                float s = 0.f;
+#pragma unroll
+                for (int h = 0; h < H; ++h) s = fmaf(wr[h], fmaxf(v[h], 0.f), s);
+                sc[j] = s * scale;
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acce[b]);
+
+            if (mode == SM_MATERIALISE || mode == SM_SAMPLE) {
+#pragma unroll
+                for (int j = 0; j < C::RH; ++j) {
+                    const int rr = wg * C::RH + j;
+                    const int* m = meta + rr * C::META_WORDS;
+                    const long long lo = meta_ll(m, MW_SA_LO), hi = meta_ll(m, MW_SB_LO);
+                    if (m[MW_ACTIVE] && kidx >= lo && kidx < hi) {
+                        const long long r = r0 + rr;
+                        if (mode == SM_MATERIALISE)
+                            a.out[r * a.out_stride + (kidx - lo)] = sc[j];
+                        else
+                            a.samp[r * a.samp_stride + (kidx - lo)] = sc[j];
+                    }
+                }
+            } else if (mode == SM_FB_HIST) {
+#pragma unroll
+                for (int j = 0; j < C::RH; ++j) {
+                    const int rr = wg * C::RH + j;
+                    const int* m = meta + rr * C::META_WORDS;
+                    const long long lo = meta_ll(m, MW_KS_LO), hi = meta_ll(m, MW_KE_LO);
+                    const uint32_t kb = fkey(sc[j]);
+                    const bool valid = m[MW_ACTIVE] && kidx >= lo && kidx < hi &&
+                                       has_prefix(kb, a.level, (uint32_t)m[MW_PREFIX]);
+                    const uint32_t dg = digit_of(kb, a.level);
+                    const uint32_t grp = __match_any_sync(0xffffffffu, valid ? dg : (0x80000000u | lane));
+                    if (valid && lane == __ffs(grp) - 1)
+                        atomicAdd(&a.fb_hist[(long long)(r0 + rr) * kHistBins + dg], (uint32_t)__popc(grp));
+                }
+            } else {
+                // ordered emission into the slab (SM_EMIT, SM_FB_EMIT)
+                const int par = (int)(i & 1);
+#pragma unroll
+                for (int j = 0; j < C::RH; ++j) {
+                    const int rr = wg * C::RH + j;
+                    const int* m = meta + rr * C::META_WORDS;
+                    const long long lo = meta_ll(m, MW_KS_LO), hi = meta_ll(m, MW_KE_LO);
+                    const bool vis = m[MW_ACTIVE] && kidx >= lo && kidx < hi;
+                    const uint32_t thr = (uint32_t)m[MW_THR];
+                    const int quota = m[MW_QUOTA];
+                    const uint32_t kb = fkey(sc[j]);
+                    const bool above = vis && (quota > 0 ? kb > thr : kb >= thr);
+                    const bool tie = vis && quota > 0 && kb == thr;
+                    const uint32_t A = __ballot_sync(0xffffffffu, above);
+                    const uint32_t T = __ballot_sync(0xffffffffu, tie);
+                    if (lane == 0) {
+                        uint32_t* e = bal + (((par * 2 + wg) * C::RH + j) * 4 + q) * 2;
+                        e[0] = A;
+                        e[1] = T;
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&exch[wg]);
+                if (!__all_sync(0xffffffffu, mbar_wait(&exch[wg], (uint32_t)(i & 1), abort_flag))) {
+                    *abort_flag = 1;
+                    if (lane == 0) raise_status(a.d_status, IDX_DEV_TIMEOUT);
+                    break;
+                }
+                const uint32_t lt_mask = (1u << lane) - 1u;
+#pragma unroll
+                for (int j = 0; j < C::RH; ++j) {
+                    const int rr = wg * C::RH + j;
+                    const int* m = meta + rr * C::META_WORDS;
+                    const int quota = m[MW_QUOTA];
+                    const uint32_t* e = bal + (((par * 2 + wg) * C::RH + j) * 4) * 2;
+                    int ab = 0, tb = 0, ta = 0, tt = 0;
+#pragma unroll
+                    for (int qq = 0; qq < 4; ++qq) {
+                        const int pa = __popc(e[2 * qq]), pt = __popc(e[2 * qq + 1]);
+                        if (qq < q) { ab += pa; tb += pt; }
+                        ta += pa;
+                        tt += pt;
+                    }
+                    if (ta == 0 && tt == 0) continue;
+                    const uint32_t A = e[2 * q], T = e[2 * q + 1];
+                    const int room = quota > ties[j] ? quota - ties[j] : 0;
+                    const int above_before = ab + __popc(A & lt_mask);
+                    const int ties_before = tb + __popc(T & lt_mask);
+                    long long pos = -1;
+                    if ((A >> lane) & 1u)
+                        pos = cnt[j] + above_before + (ties_before < room ? ties_before : room);
+                    else if (((T >> lane) & 1u) && ties_before < room)
+                        pos = cnt[j] + above_before + ties_before;
+                    if (pos >= 0 && pos < a.cap) {
+                        const long long r = r0 + rr;
+                        a.slab_s[r * a.cap + pos] = sc[j];
+                        a.slab_i[r * a.cap + pos] = (int)(kidx - meta_ll(m, MW_KS_LO));
+                    }
+                    const int took = tt < room ? tt : room;
+                    cnt[j] += ta + took;
+                    ties[j] += took;
+                }
+            }
+        }
+        if ((mode == SM_EMIT || mode == SM_FB_EMIT) && q == 0 && lane == 0) {
+#pragma unroll
+            for (int j = 0; j < C::RH; ++j) {
+                const int rr = wg * C::RH + j;
+                const int* m = meta + rr * C::META_WORDS;
+                if (m[MW_ACTIVE]) a.plan[r0 + rr].count = cnt[j];
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+}  // namespace idx

@@ -1,0 +1,65 @@
+// Host-visible argument blocks and launchers of the top-k kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/idx.h"
+#include "plan.cuh"
+
+namespace idx {
+
+enum : int { TOPK_OUTPUT = 0, TOPK_THRESHOLD = 1 };
+
+struct TopkRowsArgs {
+    const float* scores;  // [rows, row_stride]
+    long long row_stride;
+    long long row_len;    // columns a row may address (bounds check)
+    const int* ks;        // may be null (0)
+    const int* ke;        // end of the visible range (or its length when ks is null)
+    int rows;
+    int topk;
+    int relative;         // row r's data starts at column 0 instead of ks[r]
+    int mode;             // TOPK_OUTPUT or TOPK_THRESHOLD
+    int* out;             // [rows, topk] (TOPK_OUTPUT)
+    // TOPK_THRESHOLD: per-row sample threshold written into plan[r]
+    RowPlan* plan;
+    const int* vis_ks;    // the row's visible key range, for the rank t
+    const int* vis_ke;
+    int cap;
+    float target;
+    int S;                // sample stride
+    long long nsamp;      // floor(keys / S)
+    int rows_per_block;   // rows sharing one sample phase
+    uint32_t phase_seed;
+    int* d_status;
+    idx_stats* d_stats;
+};
+
+struct CandArgs {
+    const float* slab_s;  // [rows, cap]
+    const int* slab_i;    // [rows, cap]
+    RowPlan* plan;
+    uint32_t* fb_hist;    // [rows, 4096]
+    const int* ks;
+    const int* ke;
+    int rows, topk, cap;
+    int fallback;         // 0: main pass (flags rows), 1: rows re-emitted by the rescan
+    int* out;
+    int* d_status;
+    idx_stats* d_stats;
+};
+
+struct FbPickArgs {
+    RowPlan* plan;
+    uint32_t* fb_hist;
+    int rows, topk, cap, level;
+};
+
+cudaError_t launch_topk_rows(const TopkRowsArgs& a, cudaStream_t s);
+cudaError_t launch_cand_topk(const CandArgs& a, cudaStream_t s);
+cudaError_t launch_fb_pick(const FbPickArgs& a, cudaStream_t s);
+size_t cand_smem_bytes(int cap);
+
+}  // namespace idx

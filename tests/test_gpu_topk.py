@@ -1,0 +1,124 @@
+"""idx_topk_from_scores against the oracle, byte for byte (the exact fp32
+top-k of "[sglang] ROCm DSA Indexer Top-K 최적화": 12-bit histogram, tie
+refinement, full-row rescan when the threshold bin overflows)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def idx():
+    import __graft_entry__
+    __graft_entry__.build()
+    import sparse_attention_indexer_tiles_gb300 as pkg
+    return pkg
+
+
+DEV = "cuda:0"
+
+
+def gpu_topk(idx, scores, ks, ke, topk, **kw):
+    out = idx.idx_topk_from_scores(scores.to(DEV), None if ks is None else ks.to(DEV),
+                                   ke.to(DEV), topk, **kw)
+    torch.cuda.synchronize()
+    return out.cpu().numpy()
+
+
+def test_small_rows_with_ties_and_short_rows(idx):
+    si = synth.score_inputs(48, 5000, 300, seed=21, short_frac=0.25)
+    got = gpu_topk(idx, si.scores, si.ks, si.ke, 300)
+    ref = oracle.topk_from_scores(si.scores, si.ks, si.ke, 300)
+    assert np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("topk", [1, 2, 7, 64, 1000, 2048, 4096])
+def test_topk_sizes(idx, topk):
+    si = synth.score_inputs(12, 6001, topk, seed=22 + topk, short_frac=0.0)
+    got = gpu_topk(idx, si.scores, si.ks, si.ke, topk)
+    ref = oracle.topk_from_scores(si.scores, si.ks, si.ke, topk)
+    assert np.array_equal(got, ref)
+
+
+def test_edge_lengths_offsets_and_odd_stride(idx):
+    """Rows of length 0, 1, topk-1, topk, topk+1 and longer, starting at odd
+    columns of an odd row stride (every alignment of the first element)."""
+    topk, stride = 257, 3001
+    g = torch.Generator().manual_seed(23)
+    S = (torch.randn(16, stride, generator=g) * 0.05).to(torch.bfloat16).float()
+    lens = [0, 1, topk - 1, topk, topk + 1, 2 * topk, 1000, 2999, 5, 300, 258, 3000, 17, 1234, 600, 2]
+    ks = torch.tensor([(3 * i + 1) % 7 for i in range(16)], dtype=torch.int32)
+    ke = torch.tensor([min(int(ks[i]) + lens[i], stride) for i in range(16)], dtype=torch.int32)
+    got = gpu_topk(idx, S, ks, ke, topk)
+    ref = oracle.topk_from_scores(S, ks, ke, topk)
+    assert np.array_equal(got, ref)
+    # ks = NULL means every row starts at column 0
+    got0 = gpu_topk(idx, S, None, ke - ks, topk)
+    ref0 = oracle.topk_from_scores(S, torch.zeros_like(ks), ke - ks, topk)
+    assert np.array_equal(got0, ref0)
+
+
+def test_relative_rows(idx):
+    """options.relative_rows: row r's data starts at column 0 although ks > 0."""
+    g = torch.Generator().manual_seed(24)
+    S = torch.randn(6, 4000, generator=g)
+    ks = torch.tensor([0, 10, 100, 1000, 3, 7], dtype=torch.int32)
+    ke = ks + torch.tensor([4000, 3990, 2000, 2500, 3997, 100], dtype=torch.int32)
+    got = gpu_topk(idx, S, ks, ke, 128, options={"relative_rows": 1})
+    ref = oracle.topk_from_scores(S, torch.zeros_like(ks), ke - ks, 128)
+    assert np.array_equal(got, ref)
+
+
+def test_massive_ties_take_the_rescan(idx):
+    """Rows whose threshold bin holds far more than the 4096-entry tie buffer:
+    all-equal rows, a two-valued row, and +0/-0 mixtures."""
+    n, topk = 20000, 1500
+    rows = []
+    rows.append(np.full(n, 0.25, np.float32))
+    two = np.full(n, 1.0, np.float32)
+    two[::3] = 2.0  # 6667 keys at 2.0 > topk: the result is the first 1500 of them
+    rows.append(two)
+    z = np.zeros(n, np.float32)
+    z[1::2] = -0.0
+    z[5] = 1.0
+    rows.append(z)
+    near = np.full(n, 1.0, np.float32)
+    near[np.arange(0, n, 2)] = np.nextafter(np.float32(1.0), np.float32(2.0))
+    rows.append(near)
+    S = torch.from_numpy(np.stack(rows))
+    ks = torch.zeros(4, dtype=torch.int32)
+    ke = torch.full((4,), n, dtype=torch.int32)
+    stats = idx.Stats(torch.device(DEV))
+    got = gpu_topk(idx, S, ks, ke, topk, stats=stats)
+    ref = oracle.topk_from_scores(S, ks, ke, topk)
+    assert np.array_equal(got, ref)
+    assert got[0].tolist() == list(range(topk))
+    st = stats.read()
+    assert st["tie_rescan_rows"] >= 3 and st["status"] == 0
+
+
+def test_extreme_values(idx):
+    g = torch.Generator().manual_seed(25)
+    S = torch.randn(4, 7000, generator=g) * 1e30
+    S[0, :100] = -3.4e38
+    S[1, 50:60] = 3.4e38
+    S[2] = -torch.rand(7000, generator=g)  # all negative
+    S[3, ::2] = 1e-40  # subnormals
+    ks = torch.zeros(4, dtype=torch.int32)
+    ke = torch.full((4,), 7000, dtype=torch.int32)
+    got = gpu_topk(idx, S, ks, ke, 999)
+    ref = oracle.topk_from_scores(S, ks, ke, 999)
+    assert np.array_equal(got, ref)
+
+
+def test_standalone_workload_full(idx):
+    """1024 rows x 131072 keys, topk 2048, bf16-grid N(0, 0.05), 5% short rows:
+    every row against the oracle."""
+    si = synth.workload("standalone_topk")
+    got = gpu_topk(idx, si.scores, si.ks, si.ke, 2048)
+    ref = oracle.topk_from_scores(si.scores, si.ks, si.ke, 2048)
+    assert np.array_equal(got, ref)
