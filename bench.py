@@ -1,0 +1,448 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 sparse-attention prefill indexer.
+
+One step = one idx_score_topk call (sampled thresholds, the tcgen05 scoring
+pass with candidate emission, the slab top-k and the exact rescan) on the fused
+prefill workload: 4096 query rows, 65536 keys, 64 heads, D = 128, topk 2048,
+fp8 e4m3 q/k, causal visible ranges.  Inputs are synthetic and seeded.
+
+Prints ONE JSON line (rank 0).  Timing: W untimed warm-up steps, then K steps
+timed on the device with CUDA events on the launching stream; the L2 is flushed
+(a 256 MiB write) between steps, outside the timed events.  --impl reference
+times the CPU oracle instead (rank 0, a bounded sample of the same workload).
+
+Multi-GPU (torchrun): every rank runs its own copy of the workload (the rows of
+different prefills are independent), no collective on the data path; value is
+the sum over ranks of the work divided by the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("scored row·key pairs/s (fused score+top-k) and top-k rows/s; % of roofline")
+WORKLOAD = "fused_prefill"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--no-extra", action="store_true", help="skip the secondary measurements")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--clocks-file", default=None)
+    p.add_argument("--rows", type=int, default=0,
+                   help="profiling: use only the last N query rows of the workload")
+    p.add_argument("--only", choices=["all", "fused", "topk"], default="all",
+                   help="profiling: run only the fused step or only the standalone top-k")
+    return p.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        m = json.load(open(path))
+        return {"hbm_gbs": float(m["hbm_gbs"]), "bf16_tflops": float(m["bf16_tflops"]),
+                "bf16_tflops_sustained": float(m.get("bf16_tflops_sustained", m["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def kernel_source_hash() -> str:
+    """Hash of the CUDA sources: a recorded ncu traffic figure is only valid
+    for the sources it was taken on."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "sparse_attention_indexer_tiles_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh")):
+            h.update(f.encode())
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        rec = json.load(open(path))
+    except ValueError:
+        return None
+    for e in rec.get("entries", []):
+        if e.get("kernel") == kernel and e.get("workload") == workload and \
+                e.get("source_hash") == kernel_source_hash():
+            return e.get("bytes_per_launch")
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, path: str | None):
+        self.path = path or os.path.join("/tmp", f"idx_clocks_{os.getpid()}.csv")
+        self.proc = None
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = list(csv.reader(io.StringIO(open(self.path).read())))
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+                power.append(float(r[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def cpu_baseline_sample(inp, target_s: float = 10.0, seed: int = 7):
+    """The oracle as it stands on the host cores, over a seeded row sample
+    sized to about `target_s` seconds of wall time."""
+    import oracle
+    import synth
+    threads = oracle.default_threads()
+    n_all = (inp.ke - inp.ks).clamp_min(0).long()
+    probe = synth.sample_rows(inp.ks, inp.ke, min(threads, inp.rows), seed)
+    t0 = time.perf_counter()
+    oracle.score_topk(inp, rows=probe, nthreads=threads)
+    dt = max(time.perf_counter() - t0, 1e-3)
+    per_row = dt / len(probe)
+    count = int(max(len(probe), min(inp.rows, target_s / per_row)))
+    rows = synth.sample_rows(inp.ks, inp.ke, count, seed + 1)
+    t0 = time.perf_counter()
+    oracle.score_topk(inp, rows=rows, nthreads=threads)
+    wall = time.perf_counter() - t0
+    pairs = int(n_all[rows].sum())
+    return {"value": pairs / wall, "unit": "pairs/s", "cores": threads, "kind": "oracle",
+            "sample": f"{len(rows)} seeded rows of the workload ({pairs} pairs), fp64 scores "
+                      f"+ full-sort top-k, {wall:.1f} s wall"}
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the CPU oracle timed on host cores (rank 0 only)."""
+    if rank != 0:
+        return
+    import oracle
+    import synth
+    inp = synth.workload(WORKLOAD)
+    threads = oracle.default_threads()
+    n_all = (inp.ke - inp.ks).clamp_min(0).long()
+    per_step_rows = max(threads, 16)
+    for i in range(args.warmup):
+        oracle.score_topk(inp, rows=synth.sample_rows(inp.ks, inp.ke, per_step_rows, 100 + i),
+                          nthreads=threads)
+    times, pairs = [], 0
+    for i in range(args.steps):
+        rows = synth.sample_rows(inp.ks, inp.ke, per_step_rows, 1000 + i)
+        t0 = time.perf_counter()
+        oracle.score_topk(inp, rows=rows, nthreads=threads)
+        times.append(time.perf_counter() - t0)
+        pairs += int(n_all[rows].sum())
+    total = sum(times)
+    value = pairs / total
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "pairs/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_block(inp),
+            "cpu_baseline": {"value": value, "unit": "pairs/s", "cores": threads,
+                             "kind": "oracle",
+                             "sample": f"{per_step_rows} seeded rows per step of the workload"},
+            "e2e": {"value": value, "unit": "pairs/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def config_block(inp):
+    return {"workload": f"{WORKLOAD}: rows={inp.rows} keys={inp.keys} H={inp.H} D={inp.D} "
+                        f"topk={inp.topk} fp8 e4m3 q/k, per-key scale U(0.5,2), causal",
+            "rows": inp.rows, "keys": inp.keys, "heads": inp.H, "dim": inp.D, "topk": inp.topk,
+            "pairs_per_step": inp.pairs(),
+            "l2": "flushed between timed steps (256 MiB write outside the events)"}
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        import torch
+        backend = "nccl" if torch.cuda.is_available() and args.impl == "ours" else "gloo"
+        dist.init_process_group(backend)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+
+    import torch
+
+    import synth
+    import sparse_attention_indexer_tiles_gb300 as idx
+    from sparse_attention_indexer_tiles_gb300 import build as _build
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    if rank == 0 or world == 1:
+        _build.build()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    pk = peaks()
+
+    if args.only == "topk":
+        print(json.dumps(standalone_topk(idx, dev, torch.empty(256 << 20, dtype=torch.uint8,
+                                                               device=dev), pk, args)))
+        return
+
+    # ---------------------------------------------------------------- inputs
+    inp = synth.workload(WORKLOAD)
+    if args.rows:
+        inp = last_rows(inp, args.rows)
+    g = {n: getattr(inp, n).to(dev) for n in ("q", "k", "k_scale", "w", "ks", "ke")}
+    pairs = inp.pairs()
+    out = torch.empty(inp.rows, inp.topk, dtype=torch.int32, device=dev)
+    need = idx.idx_score_topk_workspace(inp.rows, inp.keys, 0, inp.H, inp.D, inp.topk,
+                                        inp.q.dtype)
+    ws = torch.empty(need, dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stats = idx.Stats(dev)
+
+    def step(ev=None, o=None):
+        opts = o or idx.Options()
+        if ev is not None:
+            opts.stage_events = ev.ptr
+        idx.idx_score_topk(g["q"], g["k"], g["k_scale"], g["w"], g["ks"], g["ke"], inp.topk,
+                           out=out, ws=ws, options=opts)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    # one checked call: the counters of the path (rescans) on this workload
+    stats.reset()
+    step(o=idx.make_options(None, stats))
+    torch.cuda.synchronize()
+    path_stats = stats.read()
+
+    # ------------------------------------------------------------- timed loop
+    evs = [idx.StageEvents(5) for _ in range(args.steps)]
+    sampler = ClockSampler(local, args.clocks_file)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    launches0 = idx.idx_launch_count()
+    for i in range(args.steps):
+        flush.zero_()
+        step(evs[i])
+    torch.cuda.synchronize()
+    launches = idx.idx_launch_count() - launches0
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    step_ms = [e.elapsed(0, 4) for e in evs]
+    emit_ms = [e.elapsed(1, 2) for e in evs]
+    stage_ms = {
+        "sample_and_threshold": statistics.mean(e.elapsed(0, 1) for e in evs),
+        "score_and_emit": statistics.mean(emit_ms),
+        "slab_topk": statistics.mean(e.elapsed(2, 3) for e in evs),
+        "rescan": statistics.mean(e.elapsed(3, 4) for e in evs),
+    }
+    ms = statistics.mean(step_ms)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t)
+    value = world * pairs / (ms * 1e-3)
+
+    # --------------------------------------------------------------- roofline
+    flops = 2.0 * inp.H * inp.D * pairs
+    emit_s = statistics.mean(emit_ms) * 1e-3
+    fp8_peak = 2.0 * pk["bf16_tflops"]  # fp8 dense = 2 x bf16 dense (nominal ratio)
+    achieved = flops / emit_s / 1e12
+    traffic = recorded_traffic("score_kernel<fp8,H64,D128> emit", WORKLOAD)
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
+                "frac": achieved / fp8_peak, "traffic": traffic,
+                "kernel": "score_kernel<fp8,H64,D128> emit pass",
+                "algorithmic": f"2*H*D flop per visible pair = {flops:.4g} flop per launch",
+                "peak_note": f"{pk['source']} bf16 {pk['bf16_tflops']} TFLOP/s x 2 for fp8"}
+    whole_frac = flops / (ms * 1e-3) / 1e12 / fp8_peak
+
+    # ------------------------------------------------------------ end to end
+    host = {n: getattr(inp, n).contiguous().pin_memory() for n in ("q", "k", "k_scale", "w",
+                                                                    "ks", "ke")}
+    out_h = torch.empty(inp.rows, inp.topk, dtype=torch.int32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size()
+    e2e_steps = max(3, min(args.steps, 10))
+    e2e_ms = []
+    for i in range(e2e_steps + 2):
+        flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for n, t in host.items():
+            g[n].copy_(t, non_blocking=True)
+        step()
+        out_h.copy_(out, non_blocking=True)
+        b.record(stream)
+        b.synchronize()
+        if i >= 2:
+            e2e_ms.append(a.elapsed_time(b))
+    e2e_val = pairs / (statistics.mean(e2e_ms) * 1e-3) * world
+
+    line = {"metric": METRIC, "value": value, "unit": "pairs/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "e4m3", "data": "synthetic", "config": config_block(inp),
+            "roofline": roofline, "whole_step_tensor_frac": whole_frac,
+            "stage_ms": stage_ms, "path_stats": path_stats,
+            "e2e": {"value": e2e_val, "unit": "pairs/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": statistics.mean(e2e_ms)},
+            "gpu_launches": launches, "clocks": clocks}
+
+    # ------------------------------------------------------ secondary numbers
+    if not args.no_extra and rank == 0:
+        line["extra"] = secondary(idx, dev, g, inp, out, ws, flush, pk, args)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_sample(inp)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def last_rows(inp, n):
+    """The last n query rows of a workload (same keys): a smaller case of the
+    same kernel for profiling."""
+    import synth
+    return synth.IndexerInputs(q=inp.q[-n:].contiguous(), k=inp.k, k_scale=inp.k_scale,
+                               w=inp.w[-n:].contiguous(), ks=inp.ks[-n:].contiguous(),
+                               ke=inp.ke[-n:].contiguous(), topk=inp.topk, meta=inp.meta)
+
+
+def timed(fn, flush, reps):
+    import torch
+    ts = []
+    for _ in range(reps):
+        flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        b.synchronize()
+        ts.append(a.elapsed_time(b))
+    return statistics.mean(ts)
+
+
+def secondary(idx, dev, g, inp, out, ws, flush, pk, args):
+    """Standalone top-k rows/s (HBM roofline) and the two-pass baseline."""
+    import torch
+    import synth
+    res = {}
+    # two-pass baseline on the same workload: materialise [rows, keys] fp32, then top-k
+    n_max = int((inp.ke - inp.ks).max())
+    S = torch.empty(inp.rows, n_max, dtype=torch.float32, device=dev)
+    out2 = torch.empty_like(out)
+    rel = idx.Options(relative_rows=1)
+
+    def mat():
+        idx.idx_score_materialise(g["q"], g["k"], g["k_scale"], g["w"], g["ks"], g["ke"], out=S)
+
+    def tk():
+        idx.idx_topk_from_scores(S, g["ks"], g["ke"], inp.topk, out=out2, options=rel)
+
+    for _ in range(2):
+        mat()
+        tk()
+    t_mat = timed(mat, flush, 5)
+    t_tk = timed(tk, flush, 5)
+    res["two_pass_ms"] = {"materialise": t_mat, "topk": t_tk, "total": t_mat + t_tk}
+    res["two_pass_identical"] = bool(torch.equal(out, out2))
+    flops = 2.0 * inp.H * inp.D * inp.pairs()
+    res["materialise_roofline"] = {"bound": "tensor", "achieved": flops / (t_mat * 1e-3) / 1e12,
+                                   "unit": "TFLOP/s"}
+    del S
+    torch.cuda.empty_cache()
+
+    res["standalone_topk"] = standalone_topk(idx, dev, flush, pk, args)
+    return res
+
+
+def standalone_topk(idx, dev, flush, pk, args):
+    """idx_topk_from_scores on 1024 rows x 131072 fp32 scores, topk 2048."""
+    import torch
+    import synth
+    si = synth.workload("standalone_topk")
+    sc = si.scores.to(dev)
+    ks, ke = si.ks.to(dev), si.ke.to(dev)
+    o3 = torch.empty(si.rows, si.topk, dtype=torch.int32, device=dev)
+
+    def st():
+        idx.idx_topk_from_scores(sc, ks, ke, si.topk, out=o3)
+
+    for _ in range(args.warmup):
+        st()
+    t_st = timed(st, flush, max(5, args.steps))
+    vis = int((si.ke - si.ks).sum())
+    bytes_alg = 4 * vis + 4 * si.rows * si.topk
+    gbs = bytes_alg / (t_st * 1e-3) / 1e9
+    return {
+        "workload": "standalone_topk: rows=1024 keys=131072 topk=2048, fp32 N(0,0.05) on the "
+                    "bf16 grid, 5% rows shorter than topk",
+        "rows_per_s": si.rows / (t_st * 1e-3), "ms": t_st,
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": gbs / pk["hbm_gbs"], "traffic": recorded_traffic(
+                         "topk_rows_kernel", "standalone_topk"),
+                     "algorithmic": f"4 B per visible score + 4 B per output = {bytes_alg} B"}}
+
+if __name__ == "__main__":
+    main()

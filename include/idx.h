@@ -90,6 +90,12 @@ typedef struct idx_options {
                              column 0 of its row (the layout idx_score_materialise
                              writes) instead of column ks[r] */
     int reserved;
+    void* const* stage_events; /* optional array of cudaEvent_t, recorded on `stream`
+                             at stage boundaries (NULL entries are skipped).
+                             idx_score_topk: [0] start, [1] after the sample and its
+                             thresholds, [2] after the scoring/emit pass, [3] after
+                             the slab top-k, [4] after the exact rescan (end).
+                             The other entry points: [0] start, [1] end. */
 } idx_options;
 
 /* row_split: 0 = automatic (page "[sglang] ROCm DSA Indexer Top-K 최적화",
@@ -163,6 +169,10 @@ const char* idx_status_string(idx_status s);
 
 /* Library version, (major << 16) | minor. */
 int idx_version(void);
+
+/* Number of kernels this library has launched in this process (all devices,
+ * all threads); a diagnostic for benchmarks. */
+unsigned long long idx_launch_count(void);
 
 #ifdef __cplusplus
 }

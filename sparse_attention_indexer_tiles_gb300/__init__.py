@@ -21,7 +21,7 @@ import torch
 __all__ = [
     "IdxError", "Options", "Stats", "load", "idx_score_topk", "idx_score_topk_workspace",
     "idx_topk_from_scores", "idx_topk_workspace", "idx_score_materialise",
-    "idx_status_string", "DTYPES", "STAT_FIELDS",
+    "idx_status_string", "DTYPES", "STAT_FIELDS", "StageEvents", "idx_launch_count",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -44,7 +44,8 @@ class Options(ctypes.Structure):
     _fields_ = [("cap_factor", ctypes.c_float), ("target_factor", ctypes.c_float),
                 ("sample_stride", ctypes.c_int), ("row_split", ctypes.c_int),
                 ("d_status", ctypes.c_void_p), ("d_stats", ctypes.c_void_p),
-                ("relative_rows", ctypes.c_int), ("reserved", ctypes.c_int)]
+                ("relative_rows", ctypes.c_int), ("reserved", ctypes.c_int),
+                ("stage_events", ctypes.c_void_p)]
 
 
 class Stats:
@@ -100,8 +101,33 @@ def load(path: str | None = None):
     lib.idx_status_string.restype = ctypes.c_char_p
     lib.idx_version.argtypes = []
     lib.idx_version.restype = I
+    lib.idx_launch_count.argtypes = []
+    lib.idx_launch_count.restype = ctypes.c_ulonglong
     _lib = lib
     return lib
+
+
+def idx_launch_count() -> int:
+    """Kernels launched by libidx in this process so far."""
+    return int(load().idx_launch_count())
+
+
+class StageEvents:
+    """CUDA events the library records at its stage boundaries
+    (options.stage_events); elapsed(i, j) in ms after a synchronize."""
+
+    def __init__(self, n: int = 5):
+        self.events = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        for e in self.events:
+            e.record()  # torch creates its events lazily, on the first record
+        self._arr = (ctypes.c_void_p * n)(*[e.cuda_event for e in self.events])
+
+    @property
+    def ptr(self) -> int:
+        return ctypes.cast(self._arr, ctypes.c_void_p).value
+
+    def elapsed(self, i: int, j: int) -> float:
+        return self.events[i].elapsed_time(self.events[j])
 
 
 def idx_status_string(code: int) -> str:

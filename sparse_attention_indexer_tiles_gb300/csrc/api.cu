@@ -1,6 +1,7 @@
 // C ABI of libidx: argument validation, workspace carving and the launch
 // sequence of each entry point.  Everything that computes runs in the kernels
 // of topk.cu and score_*.cu; this file only decides what to launch.
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -37,15 +38,20 @@ bool score_supported(idx_dtype dt, int H, int D) {
     return h_ok && d_ok && (dt == IDX_BF16 || dt == IDX_FP8_E4M3);
 }
 
+std::atomic<unsigned long long> g_launches{0};
+
+void count_launches(unsigned n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
 cudaError_t launch_score(const ScoreLaunch& L, cudaStream_t s) {
-    if (L.dt == IDX_BF16) return launch_score_bf16(L, s);
-    return launch_score_fp8(L, s);
+    const cudaError_t e = L.dt == IDX_BF16 ? launch_score_bf16(L, s) : launch_score_fp8(L, s);
+    if (e == cudaSuccess && L.a.rows > 0) count_launches(1);
+    return e;
 }
 
 namespace {
 
 constexpr int kMaxTopk = 4096;
-constexpr int kMaxCap = 24576;
+constexpr int kMaxCap = 12288;
 constexpr uint32_t kPhaseSeed = 0x9E3779B9u;
 
 // Is the current device an sm_103 part?  Cached per device.
@@ -72,7 +78,9 @@ bool arch_ok() {
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 struct FusedParams {
-    int cap;
+    int cap;    // nominal slab cap
+    int cap_q;  // one warp run: ceil(cap / 4) + 64 (a contiguous range of n keys puts
+                // at most n / 4 + 64 of them into one 32-key column of the tiles)
     float target;
     int S;
 };
@@ -94,6 +102,7 @@ FusedParams fused_params(int topk, const idx_options* opt) {
     else
         p.cap = std::max((int)std::ceil(2.25 * topk), 4096);
     if (p.cap < topk) p.cap = topk;
+    p.cap_q = (p.cap + 3) / 4 + 64;
     const double ratio = (double)p.cap / topk;
     double target = opt && opt->target_factor > 0.f ? (double)opt->target_factor : std::sqrt(ratio);
     p.target = (float)target;
@@ -112,11 +121,11 @@ FusedParams fused_params(int topk, const idx_options* opt) {
 }
 
 struct FusedLayout {
-    size_t plan, slab_s, slab_i, samp, fb_hist, total;
+    size_t plan, run_cnt, slab_s, slab_i, samp, fb_hist, total;
     long long samp_stride;
 };
 
-FusedLayout fused_layout(int rows, long long max_len, int cap, int S) {
+FusedLayout fused_layout(int rows, long long max_len, int cap, int cap_q, int S) {
     FusedLayout L;
     size_t off = 0;
     auto take = [&](size_t bytes) {
@@ -126,8 +135,9 @@ FusedLayout fused_layout(int rows, long long max_len, int cap, int S) {
     };
     L.samp_stride = max_len / S + 2;
     L.plan = take((size_t)rows * sizeof(RowPlan));
-    L.slab_s = take((size_t)rows * cap * sizeof(float));
-    L.slab_i = take((size_t)rows * cap * sizeof(int));
+    L.run_cnt = take((size_t)rows * 4 * sizeof(int));
+    L.slab_s = take((size_t)rows * 4 * cap_q * sizeof(float));
+    L.slab_i = take((size_t)rows * 4 * cap_q * sizeof(int));
     L.samp = take(max_len > cap ? (size_t)rows * L.samp_stride * sizeof(float) : 0);
     L.fb_hist = take(max_len > cap ? (size_t)rows * 4096 * sizeof(uint32_t) : 0);
     L.total = off;
@@ -172,6 +182,11 @@ ScoreLaunch make_score_launch(const void* q, const void* k, const float* k_scale
     return L;
 }
 
+void record(const idx_options* opt, int i, cudaStream_t s) {
+    if (opt && opt->stage_events && opt->stage_events[i])
+        cudaEventRecord(static_cast<cudaEvent_t>(opt->stage_events[i]), s);
+}
+
 idx_status cuda_status(cudaError_t e) {
     if (e == cudaSuccess) return IDX_OK;
     cudaGetLastError();  // clear a sticky launch error of ours
@@ -200,6 +215,8 @@ const char* idx_status_string(idx_status s) {
 
 int idx_version(void) { return (0 << 16) | 1; }
 
+unsigned long long idx_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
 size_t idx_score_topk_workspace(int rows, long long keys, long long max_len, int H, int D,
                                 int topk, idx_dtype dt, const idx_options* opt) {
     (void)H;
@@ -208,7 +225,7 @@ size_t idx_score_topk_workspace(int rows, long long keys, long long max_len, int
     if (rows <= 0 || topk < 1 || topk > kMaxTopk) return 0;
     if (max_len <= 0 || max_len > keys) max_len = keys;
     const FusedParams p = fused_params(topk, opt);
-    return fused_layout(rows, max_len, p.cap, p.S).total;
+    return fused_layout(rows, max_len, p.cap, p.cap_q, p.S).total;
 }
 
 idx_status idx_score_topk(const void* q, const void* k, const float* k_scale, const float* w,
@@ -224,12 +241,13 @@ idx_status idx_score_topk(const void* q, const void* k, const float* k_scale, co
     if (max_len <= 0 || max_len > keys) max_len = keys;
     const FusedParams p = fused_params(topk, opt);
     if (p.cap > kMaxCap || p.S < 1) return IDX_EUNSUPPORTED;
-    const FusedLayout lay = fused_layout(rows, max_len, p.cap, p.S);
+    const FusedLayout lay = fused_layout(rows, max_len, p.cap, p.cap_q, p.S);
     if (!ws || ws_bytes < lay.total) return IDX_EWORKSPACE;
     if (!aligned(ws, 256)) return IDX_EALIGN;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t* base = static_cast<uint8_t*>(ws);
     RowPlan* plan = reinterpret_cast<RowPlan*>(base + lay.plan);
+    int* run_cnt = reinterpret_cast<int*>(base + lay.run_cnt);
     float* slab_s = reinterpret_cast<float*>(base + lay.slab_s);
     int* slab_i = reinterpret_cast<int*>(base + lay.slab_i);
     float* samp = reinterpret_cast<float*>(base + lay.samp);
@@ -243,6 +261,8 @@ idx_status idx_score_topk(const void* q, const void* k, const float* k_scale, co
     L.a.slab_s = slab_s;
     L.a.slab_i = slab_i;
     L.a.cap = p.cap;
+    L.a.cap_q = p.cap_q;
+    L.a.run_cnt = run_cnt;
     L.a.fb_hist = fb_hist;
     L.a.S = p.S;
     L.a.nsamp = keys / p.S;
@@ -251,6 +271,7 @@ idx_status idx_score_topk(const void* q, const void* k, const float* k_scale, co
     L.a.phase_seed = kPhaseSeed;
     cudaError_t e;
 
+    record(opt, 0, s);
     if (sampling) {
         // 1. score the odd-stride sample of every long row
         L.a.mode = SM_SAMPLE;
@@ -277,15 +298,20 @@ idx_status idx_score_topk(const void* q, const void* k, const float* k_scale, co
         t.d_status = d_status;
         t.d_stats = d_stats;
         if ((e = launch_topk_rows(t, s)) != cudaSuccess) return cuda_status(e);
+        count_launches(1);
     }
+    record(opt, 1, s);
     // 3. one scoring pass emits every key at or above T_r into the slab
     L.a.mode = SM_EMIT;
     if ((e = launch_score(L, s)) != cudaSuccess) return cuda_status(e);
+    record(opt, 2, s);
     // 4. exact top-k of every slab; rows whose count missed [topk, cap] are flagged
     CandArgs c;
     std::memset(&c, 0, sizeof(c));
     c.slab_s = slab_s;
     c.slab_i = slab_i;
+    c.run_cnt = run_cnt;
+    c.cap_q = p.cap_q;
     c.plan = plan;
     c.fb_hist = sampling ? fb_hist : nullptr;
     c.ks = ks;
@@ -298,6 +324,8 @@ idx_status idx_score_topk(const void* q, const void* k, const float* k_scale, co
     c.d_stats = d_stats;
     c.fallback = 0;
     if ((e = launch_cand_topk(c, s)) != cudaSuccess) return cuda_status(e);
+    count_launches(1);
+    record(opt, 3, s);
     if (sampling) {
         // 5. exact rescan of flagged rows: up to three digit passes, one re-emission
         FbPickArgs fp{plan, fb_hist, rows, topk, p.cap, 0};
@@ -307,12 +335,15 @@ idx_status idx_score_topk(const void* q, const void* k, const float* k_scale, co
             if ((e = launch_score(L, s)) != cudaSuccess) return cuda_status(e);
             fp.level = level;
             if ((e = launch_fb_pick(fp, s)) != cudaSuccess) return cuda_status(e);
+            count_launches(1);
         }
         L.a.mode = SM_FB_EMIT;
         if ((e = launch_score(L, s)) != cudaSuccess) return cuda_status(e);
         c.fallback = 1;
         if ((e = launch_cand_topk(c, s)) != cudaSuccess) return cuda_status(e);
+        count_launches(1);
     }
+    record(opt, 4, s);
     return IDX_OK;
 }
 
@@ -350,7 +381,12 @@ idx_status idx_topk_from_scores(const float* scores, long long row_stride, const
     t.out = out_idx;
     t.d_status = opt ? opt->d_status : nullptr;
     t.d_stats = opt ? opt->d_stats : nullptr;
-    return cuda_status(launch_topk_rows(t, static_cast<cudaStream_t>(stream)));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    record(opt, 0, s);
+    const cudaError_t e = launch_topk_rows(t, s);
+    if (e == cudaSuccess) count_launches(1);
+    record(opt, 1, s);
+    return cuda_status(e);
 }
 
 idx_status idx_score_materialise(const void* q, const void* k, const float* k_scale,
@@ -365,7 +401,11 @@ idx_status idx_score_materialise(const void* q, const void* k, const float* k_sc
     L.a.mode = SM_MATERIALISE;
     L.a.out = scores;
     L.a.out_stride = row_stride;
-    return cuda_status(launch_score(L, static_cast<cudaStream_t>(stream)));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    record(opt, 0, s);
+    const cudaError_t e = launch_score(L, s);
+    record(opt, 1, s);
+    return cuda_status(e);
 }
 
 }  // extern "C"

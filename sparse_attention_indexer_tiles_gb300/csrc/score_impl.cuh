@@ -40,20 +40,22 @@ struct ScoreCfg {
     static constexpr int B_BYTES = N * RB;
     static constexpr int B_CHUNK = N * CHUNK_B;
     static constexpr int NS = RB >= 256 ? 4 : (RB == 128 ? 6 : 8);
-    static constexpr int RH = R / 2;                        // rows per epilogue warpgroup
-    static constexpr int THREADS = 384;
+    static constexpr int EPI_WARPS = 16;                    // 4 per SM sub-partition
+    static constexpr int NGROUPS = EPI_WARPS / 4;           // warps sharing a lane quarter
+    static constexpr int RG = R / NGROUPS;                  // rows per epilogue warp
+    static constexpr int THREADS = 32 * (4 + EPI_WARPS);
     static constexpr uint32_t IDESC = instr_desc(DT == IDX_BF16 ? 1u : 0u, M, N);
     // shared memory carve (offsets from a 1024-byte aligned base)
     static constexpr int OFF_B = 0;
     static constexpr int OFF_A = B_BYTES;
     static constexpr int OFF_BAR = OFF_A + NS * A_BYTES;
-    static constexpr int NBAR = 2 * NS + 7;
+    static constexpr int NBAR = 2 * NS + 5 + NGROUPS;
     static constexpr int OFF_TSLOT = OFF_BAR + NBAR * 8;
     static constexpr int OFF_W = (OFF_TSLOT + 16 + 15) / 16 * 16;
     static constexpr int OFF_META = OFF_W + R * H * 4;
     static constexpr int META_WORDS = 12;                   // per row
     static constexpr int OFF_BAL = OFF_META + R * META_WORDS * 4;
-    static constexpr int BAL_WORDS = 2 * 2 * RH * 4 * 2;    // parity x wg x row x warp x {above, tie}
+    static constexpr int BAL_WORDS = 2 * NGROUPS * RG * 4 * 2;  // parity x group x row x warp x {above, tie}
     static constexpr int OFF_MISC = OFF_BAL + BAL_WORDS * 4;
     static constexpr int SMEM_USED = OFF_MISC + 64;
     // at least ~120 KB so that one CTA owns an SM (and its 512 TMEM columns)
@@ -75,7 +77,7 @@ IDX_DEVI void set_meta_ll(int* m, int lo, long long v) {
 }
 
 template <int DT, int H, int RB>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(ScoreCfg<DT, H, RB>::THREADS, 1)
 score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
              const __grid_constant__ CUtensorMap tm_ks, const __grid_constant__ ScoreArgs a) {
     using C = ScoreCfg<DT, H, RB>;
@@ -88,7 +90,7 @@ score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     uint64_t* accf = bars + 2 * C::NS;
     uint64_t* acce = accf + 2;
     uint64_t* qfull = acce + 2;
-    uint64_t* exch = qfull + 1;  // [2]: the 4 warps of an epilogue warpgroup, once per tile
+    uint64_t* exch = qfull + 1;  // [NGROUPS]: the 4 warps of one row group, once per tile
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + C::OFF_TSLOT);
     float* w_s = reinterpret_cast<float*>(smem + C::OFF_W);
     int* meta = reinterpret_cast<int*>(smem + C::OFF_META);
@@ -197,11 +199,10 @@ score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&accf[i], 1);
-            mbar_init(&acce[i], 8);
+            mbar_init(&acce[i], C::EPI_WARPS);
         }
         mbar_init(qfull, 1);
-        mbar_init(&exch[0], 4);
-        mbar_init(&exch[1], 4);
+        for (int i = 0; i < C::NGROUPS; ++i) mbar_init(&exch[i], 4);
         fence_barrier_init();
     }
     __syncthreads();
@@ -305,12 +306,13 @@ score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         }
     } else if (warp >= 4) {
         // ------------------------------------------------ epilogue
-        const int q = warp & 3;       // TMEM lane quarter
-        const int wg = (warp - 4) >> 2;
-        int cnt[C::RH];
-        int ties[C::RH];
+        const int q = warp & 3;              // TMEM lane quarter
+        const int grp = (warp - 4) >> 2;     // row group: rows [grp * RG, (grp + 1) * RG)
+        const uint32_t lt = (1u << lane) - 1u;
+        int cnt[C::RG];
+        int ties[C::RG];
 #pragma unroll
-        for (int j = 0; j < C::RH; ++j) cnt[j] = ties[j] = 0;
+        for (int j = 0; j < C::RG; ++j) cnt[j] = ties[j] = 0;
 
         for (long long i = 0; i < ntiles; ++i) {
             const int b = (int)(i & 1);
@@ -324,26 +326,34 @@ score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             const long long kidx = (t0 + i) * C::M + q * 32 + lane;  // key, or sample index
             const long long key = mode == SM_SAMPLE ? phase + (long long)a.S * kidx : kidx;
             const bool in_keys = mode == SM_SAMPLE ? (kidx < a.nsamp) : (key < a.keys);
-            const float scale = in_keys ? __ldg(a.k_scale + key) : 0.f;
+            // x + |x| = 2 ReLU(x) runs on the FMA pipe; the 1/2 folds into the scale
+            const float half_scale = in_keys ? 0.5f * __ldg(a.k_scale + key) : 0.f;
 
-            float sc[C::RH];
+            float sc[C::RG];
 #pragma unroll
-            for (int j = 0; j < C::RH; ++j) {
-                const int rr = wg * C::RH + j;
-                const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * C::N + rr * H);
-                float v[H];
-                if constexpr (H % 16 == 0) {
-#pragma unroll
-                    for (int c = 0; c < H / 16; ++c) tmem_ld16(taddr + c * 16, v + c * 16);
-                } else {
-                    tmem_ld8(taddr, v);
-                }
-                tmem_ld_wait();
+            for (int j = 0; j < C::RG; ++j) {
+                const int rr = grp * C::RG + j;
+                const uint32_t taddr =
+                    tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * C::N + rr * H);
                 const float* wr = w_s + rr * H;
-                float s = 0.f;
+                float acc[8];
 #pragma unroll
-                for (int h = 0; h < H; ++h) s = fmaf(wr[h], fmaxf(v[h], 0.f), s);
-                sc[j] = s * scale;
+                for (int u = 0; u < 8; ++u) acc[u] = 0.f;
+                constexpr int CH = H >= 32 ? 32 : H;
+#pragma unroll
+                for (int c = 0; c < H / CH; ++c) {
+                    float v[CH];
+                    if constexpr (CH == 32) tmem_ld32(taddr + c * 32, v);
+                    else if constexpr (CH == 16) tmem_ld16(taddr, v);
+                    else tmem_ld8(taddr, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int h = 0; h < CH; ++h)
+                        acc[h & 7] = fmaf(wr[c * CH + h], v[h] + fabsf(v[h]), acc[h & 7]);
+                }
+                const float sum = ((acc[0] + acc[1]) + (acc[2] + acc[3])) +
+                                  ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+                sc[j] = sum * half_scale;
             }
             tc_fence_before();
             __syncwarp();
@@ -351,8 +361,8 @@ score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
 
             if (mode == SM_MATERIALISE || mode == SM_SAMPLE) {
 #pragma unroll
-                for (int j = 0; j < C::RH; ++j) {
-                    const int rr = wg * C::RH + j;
+                for (int j = 0; j < C::RG; ++j) {
+                    const int rr = grp * C::RG + j;
                     const int* m = meta + rr * C::META_WORDS;
                     const long long lo = meta_ll(m, MW_SA_LO), hi = meta_ll(m, MW_SB_LO);
                     if (m[MW_ACTIVE] && kidx >= lo && kidx < hi) {
@@ -363,26 +373,48 @@ score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                             a.samp[r * a.samp_stride + (kidx - lo)] = sc[j];
                     }
                 }
+            } else if (mode == SM_EMIT) {
+                // main pass: each warp appends its keys >= T_r, in key order, to
+                // its own run q of the row's slab; no cross-warp traffic
+#pragma unroll
+                for (int j = 0; j < C::RG; ++j) {
+                    const int rr = grp * C::RG + j;
+                    const int* m = meta + rr * C::META_WORDS;
+                    const long long lo = meta_ll(m, MW_KS_LO), hi = meta_ll(m, MW_KE_LO);
+                    const bool hit = m[MW_ACTIVE] && kidx >= lo && kidx < hi &&
+                                     fkey(sc[j]) >= (uint32_t)m[MW_THR];
+                    const uint32_t A = __ballot_sync(0xffffffffu, hit);
+                    if (A) {
+                        const int pos = cnt[j] + __popc(A & lt);
+                        if (hit && pos < a.cap_q) {
+                            const long long slot = ((long long)(r0 + rr) * 4 + q) * a.cap_q + pos;
+                            a.slab_s[slot] = sc[j];
+                            a.slab_i[slot] = (int)(kidx - lo);
+                        }
+                        cnt[j] += __popc(A);
+                    }
+                }
             } else if (mode == SM_FB_HIST) {
 #pragma unroll
-                for (int j = 0; j < C::RH; ++j) {
-                    const int rr = wg * C::RH + j;
+                for (int j = 0; j < C::RG; ++j) {
+                    const int rr = grp * C::RG + j;
                     const int* m = meta + rr * C::META_WORDS;
                     const long long lo = meta_ll(m, MW_KS_LO), hi = meta_ll(m, MW_KE_LO);
                     const uint32_t kb = fkey(sc[j]);
                     const bool valid = m[MW_ACTIVE] && kidx >= lo && kidx < hi &&
                                        has_prefix(kb, a.level, (uint32_t)m[MW_PREFIX]);
                     const uint32_t dg = digit_of(kb, a.level);
-                    const uint32_t grp = __match_any_sync(0xffffffffu, valid ? dg : (0x80000000u | lane));
-                    if (valid && lane == __ffs(grp) - 1)
-                        atomicAdd(&a.fb_hist[(long long)(r0 + rr) * kHistBins + dg], (uint32_t)__popc(grp));
+                    const uint32_t same = __match_any_sync(0xffffffffu, valid ? dg : (0x80000000u | lane));
+                    if (valid && lane == __ffs(same) - 1)
+                        atomicAdd(&a.fb_hist[(long long)(r0 + rr) * kHistBins + dg], (uint32_t)__popc(same));
                 }
             } else {
-                // ordered emission into the slab (SM_EMIT, SM_FB_EMIT)
+                // rescan re-emission (SM_FB_EMIT): one run per row in key order,
+                // ties at the exact threshold limited to the first `quota`
                 const int par = (int)(i & 1);
 #pragma unroll
-                for (int j = 0; j < C::RH; ++j) {
-                    const int rr = wg * C::RH + j;
+                for (int j = 0; j < C::RG; ++j) {
+                    const int rr = grp * C::RG + j;
                     const int* m = meta + rr * C::META_WORDS;
                     const long long lo = meta_ll(m, MW_KS_LO), hi = meta_ll(m, MW_KE_LO);
                     const bool vis = m[MW_ACTIVE] && kidx >= lo && kidx < hi;
@@ -394,25 +426,25 @@ score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                     const uint32_t A = __ballot_sync(0xffffffffu, above);
                     const uint32_t T = __ballot_sync(0xffffffffu, tie);
                     if (lane == 0) {
-                        uint32_t* e = bal + (((par * 2 + wg) * C::RH + j) * 4 + q) * 2;
+                        uint32_t* e = bal + (((par * C::NGROUPS + grp) * C::RG + j) * 4 + q) * 2;
                         e[0] = A;
                         e[1] = T;
                     }
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&exch[wg]);
-                if (!__all_sync(0xffffffffu, mbar_wait(&exch[wg], (uint32_t)(i & 1), abort_flag))) {
+                if (lane == 0) mbar_arrive(&exch[grp]);
+                if (!__all_sync(0xffffffffu, mbar_wait(&exch[grp], (uint32_t)(i & 1), abort_flag))) {
                     *abort_flag = 1;
                     if (lane == 0) raise_status(a.d_status, IDX_DEV_TIMEOUT);
                     break;
                 }
-                const uint32_t lt_mask = (1u << lane) - 1u;
+                const int run_cap = 4 * a.cap_q;
 #pragma unroll
-                for (int j = 0; j < C::RH; ++j) {
-                    const int rr = wg * C::RH + j;
+                for (int j = 0; j < C::RG; ++j) {
+                    const int rr = grp * C::RG + j;
                     const int* m = meta + rr * C::META_WORDS;
                     const int quota = m[MW_QUOTA];
-                    const uint32_t* e = bal + (((par * 2 + wg) * C::RH + j) * 4) * 2;
+                    const uint32_t* e = bal + (((par * C::NGROUPS + grp) * C::RG + j) * 4) * 2;
                     int ab = 0, tb = 0, ta = 0, tt = 0;
 #pragma unroll
                     for (int qq = 0; qq < 4; ++qq) {
@@ -424,17 +456,17 @@ score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                     if (ta == 0 && tt == 0) continue;
                     const uint32_t A = e[2 * q], T = e[2 * q + 1];
                     const int room = quota > ties[j] ? quota - ties[j] : 0;
-                    const int above_before = ab + __popc(A & lt_mask);
-                    const int ties_before = tb + __popc(T & lt_mask);
+                    const int above_before = ab + __popc(A & lt);
+                    const int ties_before = tb + __popc(T & lt);
                     long long pos = -1;
                     if ((A >> lane) & 1u)
                         pos = cnt[j] + above_before + (ties_before < room ? ties_before : room);
                     else if (((T >> lane) & 1u) && ties_before < room)
                         pos = cnt[j] + above_before + ties_before;
-                    if (pos >= 0 && pos < a.cap) {
-                        const long long r = r0 + rr;
-                        a.slab_s[r * a.cap + pos] = sc[j];
-                        a.slab_i[r * a.cap + pos] = (int)(kidx - meta_ll(m, MW_KS_LO));
+                    if (pos >= 0 && pos < run_cap) {
+                        const long long slot = (long long)(r0 + rr) * run_cap + pos;
+                        a.slab_s[slot] = sc[j];
+                        a.slab_i[slot] = (int)(kidx - meta_ll(m, MW_KS_LO));
                     }
                     const int took = tt < room ? tt : room;
                     cnt[j] += ta + took;
@@ -442,12 +474,19 @@ score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 }
             }
         }
-        if ((mode == SM_EMIT || mode == SM_FB_EMIT) && q == 0 && lane == 0) {
+        if (lane == 0 && (mode == SM_EMIT || (mode == SM_FB_EMIT && q == 0))) {
 #pragma unroll
-            for (int j = 0; j < C::RH; ++j) {
-                const int rr = wg * C::RH + j;
+            for (int j = 0; j < C::RG; ++j) {
+                const int rr = grp * C::RG + j;
                 const int* m = meta + rr * C::META_WORDS;
-                if (m[MW_ACTIVE]) a.plan[r0 + rr].count = cnt[j];
+                if (!m[MW_ACTIVE]) continue;
+                int* rc = a.run_cnt + (long long)(r0 + rr) * 4;
+                if (mode == SM_EMIT) {
+                    rc[q] = cnt[j];
+                } else {
+                    rc[0] = cnt[j];
+                    rc[1] = rc[2] = rc[3] = 0;
+                }
             }
         }
     }

@@ -205,18 +205,173 @@ IDX_DEVI void ordered_output(const RowView& v, Threshold th, uint32_t k, int* ou
     }
 }
 
-// Shared memory of topk_rows_kernel: histogram, tie buffer (keys, positions),
-// scan scratch.
-constexpr size_t kRowsSmem = (kHistBins + 2 * kTieCap + 64) * sizeof(uint32_t);
+// ------------------------------------------------------- one-pass path
+//
+// A row is streamed from HBM once.  A lower bound L on the threshold is
+// estimated from the 12-bit histogram of the row's first 4096 values (aiming at
+// about 2 k keys >= L); every key >= L is appended to its warp's run in shared
+// memory.  Warp w owns the contiguous slice w of the row and appends in index
+// order, so the runs, taken in warp order, list the candidates in ascending
+// index order.  The exact threshold is then refined over the candidates and an
+// ordered compaction writes the result.  When L was too high (fewer than k
+// candidates) or a run overflowed, the row falls back to the multi-pass path
+// above, which is exact for any input.
+
+constexpr int kRunCap = 512;       // candidates per warp run
+constexpr int kPrefix = 4096;      // values that estimate L
+
+template <int THREADS>
+struct StreamSmem {
+    static constexpr int W = THREADS / 32;
+    static constexpr int RUN_WORDS = W * kRunCap;          // per array
+    static_assert(2 * RUN_WORDS >= 2 * kTieCap, "tie buffer aliases the runs");
+    // hist | scratch(64) | rcnt(W) | wsum(2W) | run keys | run idx
+    static constexpr size_t BYTES =
+        (kHistBins + 64 + 3 * W + 2 * (size_t)RUN_WORDS) * sizeof(uint32_t);
+};
+
+// Append every key >= L of warp w's slice to its run; returns through rcnt[w].
+template <int THREADS, int UNROLL>
+IDX_DEVI void stream_collect(const RowView& v, uint32_t L, uint32_t* rkey, uint32_t* ridx,
+                             uint32_t* rcnt) {
+    constexpr int W = THREADS / 32;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const long long seg = (v.nvec + W - 1) / W;
+    const long long s0 = (long long)w * seg;
+    const long long s1 = s0 + seg < v.nvec ? s0 + seg : v.nvec;
+    uint32_t* mk = rkey + w * kRunCap;
+    uint32_t* mi = ridx + w * kRunCap;
+    uint32_t cnt = 0;
+    for (long long base = s0; base < s1; base += 32 * UNROLL) {
+        float4 f[UNROLL];
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            const long long sl = base + u * 32 + lane;
+            f[u] = sl < s1 ? ldg4(v.base + sl) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            const long long sl = base + u * 32 + lane;
+            const float e[4] = {f[u].x, f[u].y, f[u].z, f[u].w};
+            uint32_t keys[4];
+            uint32_t hits = 0;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const long long p = 4 * sl + c - v.off;
+                keys[c] = fkey(e[c]);
+                const bool h = sl < s1 && p >= 0 && p < v.n && keys[c] >= L;
+                hits |= (h ? 1u : 0u) << c;
+            }
+            if (!__any_sync(0xffffffffu, hits != 0)) continue;
+            // exclusive prefix of the hit counts over the lanes (index order)
+            const uint32_t mine = __popc(hits);
+            uint32_t incl = mine;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += t;
+            }
+            uint32_t pos = cnt + incl - mine;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                if ((hits >> c) & 1u) {
+                    if (pos < (uint32_t)kRunCap) {
+                        mk[pos] = keys[c];
+                        mi[pos] = static_cast<uint32_t>(4 * sl + c - v.off);
+                    }
+                    ++pos;
+                }
+            }
+            cnt += __shfl_sync(0xffffffffu, incl, 31);
+        }
+    }
+    if (lane == 0) rcnt[w] = cnt;
+}
+
+// Exact threshold of the k largest keys held in the warp runs.
+template <int THREADS>
+IDX_DEVI Threshold refine_runs(const uint32_t* rkey, const uint32_t* rcnt, uint32_t k,
+                               uint32_t* hist, uint32_t* scratch) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const uint32_t cnt = rcnt[w];
+    const uint32_t* mk = rkey + w * kRunCap;
+    uint32_t prefix = 0, need = k;
+    for (int lev = 0; lev <= 2; ++lev) {
+        zero_shared<THREADS>(hist, kHistBins);
+        __syncthreads();
+        for (uint32_t i = lane; i < cnt; i += 32) {
+            const uint32_t key = mk[i];
+            if (has_prefix(key, lev, prefix)) atomicAdd(&hist[digit_of(key, lev)], 1u);
+        }
+        __syncthreads();
+        const DigitPick pk = pick_digit<THREADS>(hist, 1 << digit_bits(lev), need, scratch);
+        need -= pk.above;
+        prefix = (prefix << digit_bits(lev)) | pk.digit;
+    }
+    return {prefix, need};
+}
+
+// Ordered output from the runs: key > T, plus the first `need` keys == T.
+template <int THREADS>
+IDX_DEVI void ordered_output_runs(const uint32_t* rkey, const uint32_t* ridx,
+                                  const uint32_t* rcnt, uint32_t* wsum, Threshold th,
+                                  uint32_t k, int* out) {
+    constexpr int W = THREADS / 32;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const uint32_t cnt = rcnt[w];
+    const uint32_t* mk = rkey + w * kRunCap;
+    const uint32_t* mi = ridx + w * kRunCap;
+    uint32_t na = 0, nt = 0;
+    for (uint32_t i = lane; i < cnt; i += 32) {
+        na += mk[i] > th.key;
+        nt += mk[i] == th.key;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        na += __shfl_xor_sync(0xffffffffu, na, o);
+        nt += __shfl_xor_sync(0xffffffffu, nt, o);
+    }
+    if (lane == 0) {
+        wsum[w] = na;
+        wsum[W + w] = nt;
+    }
+    __syncthreads();
+    uint32_t a_run = 0, t_run = 0;
+    for (int j = 0; j < w; ++j) {
+        a_run += wsum[j];
+        t_run += wsum[W + j];
+    }
+    const uint32_t lt = (1u << lane) - 1u;
+    for (uint32_t base = 0; base < cnt; base += 32) {
+        const uint32_t i = base + lane;
+        const uint32_t key = i < cnt ? mk[i] : 0u;
+        const bool ab = i < cnt && key > th.key;
+        const bool tb = i < cnt && key == th.key;
+        const uint32_t A = __ballot_sync(0xffffffffu, ab), T = __ballot_sync(0xffffffffu, tb);
+        const uint32_t a_b = a_run + __popc(A & lt), t_b = t_run + __popc(T & lt);
+        if (ab) {
+            const uint32_t pos = a_b + min(t_b, th.need);
+            if (pos < k) out[pos] = static_cast<int>(mi[i]);
+        } else if (tb && t_b < th.need && a_b + t_b < k) {
+            out[a_b + t_b] = static_cast<int>(mi[i]);
+        }
+        a_run += __popc(A);
+        t_run += __popc(T);
+    }
+}
 
 template <int THREADS, int UNROLL>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(THREADS)
 topk_rows_kernel(TopkRowsArgs a) {
+    using SM = StreamSmem<THREADS>;
+    constexpr int W = SM::W;
     extern __shared__ __align__(16) uint32_t smem[];
     uint32_t* hist = smem;
-    uint32_t* tkey = hist + kHistBins;
-    uint32_t* tpos = tkey + kTieCap;
-    uint32_t* scratch = tpos + kTieCap;
+    uint32_t* scratch = hist + kHistBins;
+    uint32_t* rcnt = scratch + 64;
+    uint32_t* wsum = rcnt + W;
+    uint32_t* rkey = wsum + 2 * W;
+    uint32_t* ridx = rkey + SM::RUN_WORDS;
 
     const int r = blockIdx.x;
     long long n, col0;
@@ -263,12 +418,49 @@ topk_rows_kernel(TopkRowsArgs a) {
     }
 
     const RowView v = make_view(a.scores + (long long)r * a.row_stride + col0, n);
-    int rescans = 0;
-    const Threshold th = find_threshold<THREADS, UNROLL>(v, k, hist, tkey, tpos, scratch, &rescans);
-    if (rescans && threadIdx.x == 0 && a.d_stats) atomicAdd(&a.d_stats->tie_rescan_rows, 1);
+
+    // lower bound L of the threshold (0 takes every key when the runs hold the row)
+    uint32_t L = 0u;
+    const long long per_warp = 4 * ((v.nvec + W - 1) / W);
+    if (per_warp > kRunCap) {
+        const long long P = n < kPrefix ? n : kPrefix;
+        const float* row = reinterpret_cast<const float*>(v.base) + v.off;
+        zero_shared<THREADS>(hist, kHistBins);
+        __syncthreads();
+        for (long long p = threadIdx.x; p < P; p += THREADS)
+            atomicAdd(&hist[fkey(__ldg(row + p)) >> 20], 1u);
+        __syncthreads();
+        double tg = ceil(2.0 * (double)k * (double)P / (double)n);
+        if (tg < 1.0) tg = 1.0;
+        if (tg > (double)P) tg = (double)P;
+        L = pick_digit<THREADS>(hist, kHistBins, (uint32_t)tg, scratch).digit << 20;
+    }
+    stream_collect<THREADS, UNROLL>(v, L, rkey, ridx, rcnt);
+    __syncthreads();
+    uint32_t total = 0;
+    bool fits = true;
+    for (int j = 0; j < W; ++j) {
+        total += rcnt[j];
+        fits = fits && rcnt[j] <= (uint32_t)kRunCap;
+    }
+    Threshold th;
+    bool runs_ok = fits && total >= k;
+    if (runs_ok) {
+        th = refine_runs<THREADS>(rkey, rcnt, k, hist, scratch);
+    } else {
+        // the estimate missed: exact multi-pass path over the row
+        __syncthreads();
+        int rescans = 0;
+        th = find_threshold<THREADS, 4>(v, k, hist, rkey, ridx, scratch, &rescans);
+        if (threadIdx.x == 0 && a.d_stats) atomicAdd(&a.d_stats->tie_rescan_rows, 1);
+    }
 
     if (a.mode == TOPK_OUTPUT) {
-        ordered_output<THREADS>(v, th, k, a.out + (long long)r * a.topk, scratch);
+        int* out = a.out + (long long)r * a.topk;
+        if (runs_ok)
+            ordered_output_runs<THREADS>(rkey, ridx, rcnt, wsum, th, k, out);
+        else
+            ordered_output<THREADS>(v, th, k, out, scratch);
     } else if (threadIdx.x == 0) {
         RowPlan* plan = a.plan + r;
         plan->thr = th.key;
@@ -279,47 +471,69 @@ topk_rows_kernel(TopkRowsArgs a) {
 }
 
 // ---------------------------------------------------------------- slab
+//
+// The main scoring pass leaves each row's candidates in four runs (one per
+// TMEM lane quarter, i.e. per 32-key column of a 128-key tile), each in
+// ascending key order; the rescan re-emission leaves a single ordered run.
+// The kernel loads the runs into shared memory, finds the exact threshold key
+// T by radix refinement, keeps the lowest indices among the keys equal to T,
+// compacts the selected entries run by run and merges the runs into ascending
+// order by ranking every entry against the other runs (binary search).
 
-// Threshold of the k largest among `cnt` keys in shared memory.
-template <int THREADS>
-IDX_DEVI Threshold smem_threshold(const uint32_t* keys, uint32_t cnt, uint32_t k, uint32_t* hist,
-                                  uint32_t* scratch) {
-    return refine_in_smem<THREADS>(keys, cnt, 0, 0u, k, hist, scratch);
+IDX_DEVI uint32_t lower_bound_u32(const uint32_t* a, uint32_t n, uint32_t v) {
+    uint32_t lo = 0, hi = n;
+    while (lo < hi) {
+        const uint32_t mid = (lo + hi) >> 1;
+        if (a[mid] < v) lo = mid + 1;
+        else hi = mid;
+    }
+    return lo;
 }
 
 template <int THREADS>
 __global__ void __launch_bounds__(THREADS)
 cand_topk_kernel(CandArgs a) {
     extern __shared__ __align__(16) uint32_t smem[];
+    const int C4 = 4 * a.cap_q;
     uint32_t* hist = smem;
-    uint32_t* scratch = hist + kHistBins;
+    uint32_t* scratch = hist + kHistBins;   // [0,35) scans, [48,64) row state
     uint32_t* keys = scratch + 64;
-    int32_t* idxs = reinterpret_cast<int32_t*>(keys + a.cap);
+    uint32_t* idxs = keys + C4;
+    uint32_t* tmp = idxs + C4;              // ~index of the ties, then the selected list
 
     const int r = blockIdx.x;
     RowPlan* plan = a.plan + r;
     const long long n = (long long)a.ke[r] - (long long)a.ks[r];
     int* out = a.out + (long long)r * a.topk;
-    // one read of the row's plan, shared by the block before anyone writes it
+    const int nruns = a.fallback ? 1 : 4;
+    const int run_cap = a.fallback ? C4 : a.cap_q;
     if (threadIdx.x == 0) {
         scratch[48] = (uint32_t)plan->state;
-        scratch[49] = (uint32_t)plan->count;
+        uint32_t off = 0, total = 0, trunc = 0;
+        for (int q = 0; q < nruns; ++q) {
+            const uint32_t c = (uint32_t)a.run_cnt[(long long)r * 4 + q];
+            trunc |= c > (uint32_t)run_cap;
+            total += c;
+            scratch[50 + q] = off;                       // run start in smem
+            off += c < (uint32_t)run_cap ? c : (uint32_t)run_cap;
+        }
+        scratch[50 + nruns] = off;
+        scratch[49] = trunc;
+        scratch[55] = total;
     }
     __syncthreads();
     const int state = (int)scratch[48];
-
     if (a.fallback) {
         if (state != ST_EMIT) return;
-    } else {
-        if (n <= a.topk) {
-            for (int i = threadIdx.x; i < a.topk; i += THREADS) out[i] = i < n ? i : -1;
-            if (threadIdx.x == 0) plan->state = ST_DONE;
-            return;
-        }
+    } else if (n <= a.topk) {
+        for (int i = threadIdx.x; i < a.topk; i += THREADS) out[i] = i < n ? i : -1;
+        if (threadIdx.x == 0) plan->state = ST_DONE;
+        return;
     }
-    const int count = (int)scratch[49];
-    if (threadIdx.x == 0 && a.d_stats && !a.fallback) atomicMax(&a.d_stats->max_count, count);
-    if (count < a.topk || count > a.cap) {
+    const uint32_t total = scratch[55];
+    const bool trunc = scratch[49] != 0;
+    if (threadIdx.x == 0 && a.d_stats && !a.fallback) atomicMax(&a.d_stats->max_count, (int)total);
+    if (trunc || total < (uint32_t)a.topk) {
         if (!a.fallback && !a.fb_hist) {
             // no rescan storage: the row was longer than the max_len the
             // workspace was sized for
@@ -338,7 +552,7 @@ cand_topk_kernel(CandArgs a) {
                 plan->prefix = 0u;
                 plan->above = 0;
                 if (a.d_stats) {
-                    atomicAdd(count > a.cap ? &a.d_stats->overflow_rows : &a.d_stats->short_rows, 1);
+                    atomicAdd(trunc ? &a.d_stats->overflow_rows : &a.d_stats->short_rows, 1);
                     atomicAdd(&a.d_stats->fallback_rows, 1);
                 }
             }
@@ -349,46 +563,80 @@ cand_topk_kernel(CandArgs a) {
         return;
     }
 
-    const float* ss = a.slab_s + (long long)r * a.cap;
-    const int* si = a.slab_i + (long long)r * a.cap;
-    for (int e = threadIdx.x; e < count; e += THREADS) {
-        keys[e] = fkey(ss[e]);
-        idxs[e] = si[e];
+    // load the runs back to back
+    const long long row_base = (long long)r * C4;
+    for (int q = 0; q < nruns; ++q) {
+        const uint32_t o = scratch[50 + q], c = scratch[51 + q] - o;
+        const float* ss = a.slab_s + row_base + (long long)q * a.cap_q;
+        const int* si = a.slab_i + row_base + (long long)q * a.cap_q;
+        for (uint32_t e = threadIdx.x; e < c; e += THREADS) {
+            keys[o + e] = fkey(ss[e]);
+            idxs[o + e] = (uint32_t)si[e];
+        }
+    }
+    const uint32_t cnt = scratch[50 + nruns];
+    __syncthreads();
+    const Threshold th = refine_in_smem<THREADS>(keys, cnt, 0, 0u, a.topk, hist, scratch);
+
+    // lowest indices among the keys equal to T
+    uint32_t* ntie = scratch + 56;
+    if (threadIdx.x == 0) *ntie = 0u;
+    __syncthreads();
+    for (uint32_t e = threadIdx.x; e < cnt; e += THREADS)
+        if (keys[e] == th.key) tmp[atomicAdd(ntie, 1u)] = ~idxs[e];
+    __syncthreads();
+    uint32_t idx_cut = 0xffffffffu;
+    if (*ntie > th.need) {
+        const Threshold ti = refine_in_smem<THREADS>(tmp, *ntie, 0, 0u, th.need, hist, scratch);
+        idx_cut = ~ti.key;
     }
     __syncthreads();
-    const Threshold th = smem_threshold<THREADS>(keys, count, a.topk, hist, scratch);
 
-    // ordered compaction over the slab, which is in ascending key order
-    uint32_t a_run = 0, e_run = 0;
-    for (int base = 0; base < count; base += THREADS * 4) {
-        uint32_t ab = 0, tb = 0;
+    // ordered compaction of the selected entries into tmp (runs stay contiguous)
+    uint32_t* run_sel = scratch + 57;  // [nruns + 1] start of each run in the list
+    uint32_t done = 0;
+    for (uint32_t base = 0; base < cnt; base += THREADS * 4) {
+        uint32_t sel = 0;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-            const int e = base + threadIdx.x * 4 + c;
-            if (e < count) {
-                ab |= (keys[e] > th.key ? 1u : 0u) << c;
-                tb |= (keys[e] == th.key ? 1u : 0u) << c;
-            }
+            const uint32_t e = base + threadIdx.x * 4 + c;
+            const bool s_ = e < cnt && (keys[e] > th.key || (keys[e] == th.key && idxs[e] <= idx_cut));
+            sel |= (s_ ? 1u : 0u) << c;
         }
-        const uint32_t mine = (__popc(ab) << 16) | __popc(tb);
         uint32_t tot;
-        const uint32_t incl = block_incl_scan<THREADS>(mine, scratch, &tot);
-        const uint32_t excl = incl - mine;
-        uint32_t a_b = a_run + (excl >> 16), e_b = e_run + (excl & 0xFFFFu);
+        const uint32_t incl = block_incl_scan<THREADS>(__popc(sel), scratch, &tot);
+        uint32_t pos = done + incl - __popc(sel);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-            const int e = base + threadIdx.x * 4 + c;
-            if ((ab >> c) & 1u) {
-                const uint32_t pos = a_b + min(e_b, th.need);
-                if (pos < (uint32_t)a.topk) out[pos] = idxs[e];
-                ++a_b;
-            } else if ((tb >> c) & 1u) {
-                if (e_b < th.need && a_b + e_b < (uint32_t)a.topk) out[a_b + e_b] = idxs[e];
-                ++e_b;
+            const uint32_t e = base + threadIdx.x * 4 + c;
+            if (e < cnt) {
+                for (int q = 0; q <= nruns; ++q)
+                    if (scratch[50 + q] == e) run_sel[q] = pos;  // first entry of run q
+            }
+            if ((sel >> c) & 1u) {
+                if (pos < (uint32_t)C4) tmp[pos] = idxs[e];
+                ++pos;
             }
         }
-        a_run += tot >> 16;
-        e_run += tot & 0xFFFFu;
+        done += tot;
+    }
+    if (threadIdx.x == 0) {
+        // runs that start at or past the end of the list
+        for (int q = 0; q <= nruns; ++q)
+            if (scratch[50 + q] >= cnt) run_sel[q] = done;
+    }
+    __syncthreads();
+
+    // merge: output rank = rank in own run + entries of the other runs below it
+    const uint32_t nsel = done < (uint32_t)a.topk ? done : (uint32_t)a.topk;
+    for (uint32_t p = threadIdx.x; p < nsel; p += THREADS) {
+        const uint32_t v = tmp[p];
+        int q = 0;
+        while (q + 1 < nruns && p >= run_sel[q + 1]) ++q;
+        uint32_t pos = p - run_sel[q];
+        for (int o = 0; o < nruns; ++o)
+            if (o != q) pos += lower_bound_u32(tmp + run_sel[o], run_sel[o + 1] - run_sel[o], v);
+        if (pos < (uint32_t)a.topk) out[pos] = (int)v;
     }
     if (threadIdx.x == 0) plan->state = ST_DONE;
 }
@@ -433,24 +681,25 @@ fb_pick_kernel(FbPickArgs a) {
 // ------------------------------------------------------------ launchers
 
 cudaError_t launch_topk_rows(const TopkRowsArgs& a, cudaStream_t s) {
-    constexpr int T = 1024, U = 4;
+    constexpr int T = 512, U = 8;
+    constexpr size_t SMEM = StreamSmem<T>::BYTES;
     auto kern = topk_rows_kernel<T, U>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kRowsSmem);
-    if (e != cudaSuccess) return e;
+    static cudaError_t attr = cudaFuncSetAttribute(
+        kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM);
+    if (attr != cudaSuccess) return attr;
     if (a.rows == 0) return cudaSuccess;
-    kern<<<a.rows, T, kRowsSmem, s>>>(a);
+    kern<<<a.rows, T, SMEM, s>>>(a);
     return cudaGetLastError();
 }
 
-size_t cand_smem_bytes(int cap) {
-    return (kHistBins + 64) * sizeof(uint32_t) + (size_t)cap * 2 * sizeof(uint32_t);
+size_t cand_smem_bytes(int cap_q) {
+    return (kHistBins + 64) * sizeof(uint32_t) + (size_t)cap_q * 4 * 3 * sizeof(uint32_t);
 }
 
 cudaError_t launch_cand_topk(const CandArgs& a, cudaStream_t s) {
     constexpr int T = 512;
     auto kern = cand_topk_kernel<T>;
-    const size_t sm = cand_smem_bytes(a.cap);
+    const size_t sm = cand_smem_bytes(a.cap_q);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e != cudaSuccess) return e;
     if (a.rows == 0) return cudaSuccess;

@@ -38,8 +38,10 @@ struct TopkRowsArgs {
 };
 
 struct CandArgs {
-    const float* slab_s;  // [rows, cap]
-    const int* slab_i;    // [rows, cap]
+    const float* slab_s;  // [rows, 4, cap_q]
+    const int* slab_i;    // [rows, 4, cap_q]
+    const int* run_cnt;   // [rows, 4]
+    int cap_q;
     RowPlan* plan;
     uint32_t* fb_hist;    // [rows, 4096]
     const int* ks;
@@ -60,6 +62,6 @@ struct FbPickArgs {
 cudaError_t launch_topk_rows(const TopkRowsArgs& a, cudaStream_t s);
 cudaError_t launch_cand_topk(const CandArgs& a, cudaStream_t s);
 cudaError_t launch_fb_pick(const FbPickArgs& a, cudaStream_t s);
-size_t cand_smem_bytes(int cap);
+size_t cand_smem_bytes(int cap_q);
 
 }  // namespace idx

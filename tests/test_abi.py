@@ -78,8 +78,9 @@ def test_argument_checks_before_cuda(lib):
 
 def test_options_struct_layout():
     import sparse_attention_indexer_tiles_gb300 as pkg
-    assert ctypes.sizeof(pkg.Options) == 40
+    assert ctypes.sizeof(pkg.Options) == 48
     assert pkg.Options.d_status.offset == 16 and pkg.Options.relative_rows.offset == 32
+    assert pkg.Options.stage_events.offset == 40
 
 
 def test_product_path_has_no_oracle_import():
