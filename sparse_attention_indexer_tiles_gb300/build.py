@@ -40,15 +40,18 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra: list[str] | None = None) -> str:
-    if not force and up_to_date():
+def build(force: bool = False, verbose: bool = False, extra: list[str] | None = None,
+          out_dir: str | None = None) -> str:
+    out_dir = out_dir or OUT_DIR
+    lib = os.path.join(out_dir, "libidx.so")
+    if not force and out_dir == OUT_DIR and up_to_date():
         return LIB
-    os.makedirs(OUT_DIR, exist_ok=True)
+    os.makedirs(out_dir, exist_ok=True)
     nvcc = _nvcc()
     flags = ARCH + NVCC_FLAGS + (extra or [])
 
     def compile_one(src):
-        obj = os.path.join(OUT_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(out_dir, os.path.basename(src)[:-3] + ".o")
         cmd = [nvcc, *flags, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         return src, obj, r
@@ -61,14 +64,14 @@ def build(force: bool = False, verbose: bool = False, extra: list[str] | None = 
             sys.stderr.write(r.stdout + r.stderr)
     if errors:
         raise RuntimeError("nvcc failed for: " + ", ".join(os.path.basename(s) for s, _ in errors))
-    tmp = LIB + f".{os.getpid()}.tmp"
+    tmp = lib + f".{os.getpid()}.tmp"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *[o for _, o, _ in results], "-lcudart"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         sys.stderr.write(r.stdout + r.stderr)
         raise RuntimeError("link of libidx.so failed")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -55,8 +55,23 @@ IDX_DEVI void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+#ifndef IDX_WAIT_HINT_NS
+#define IDX_WAIT_HINT_NS 0
+#endif
+
+// One test of the phase.  With a suspend-time hint (ns) the thread may sleep in
+// hardware until the phase completes instead of spinning.
 IDX_DEVI bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     uint32_t ok;
+#if IDX_WAIT_HINT_NS > 0
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"((uint32_t)IDX_WAIT_HINT_NS)
+        : "memory");
+#else
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
@@ -64,6 +79,7 @@ IDX_DEVI bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
         : "=r"(ok)
         : "r"(smem_u32(bar)), "r"(parity)
         : "memory");
+#endif
     return ok != 0;
 }
 
@@ -74,12 +90,10 @@ IDX_DEVI bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                         long long limit = (1ll << 32)) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
-    for (uint32_t it = 0;; ++it) {
+    for (;;) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 63u) {
-            if (abort && *abort) return false;
-            if (clock64() - t0 > limit) return false;
-        }
+        if (abort && *abort) return false;
+        if (clock64() - t0 > limit) return false;
     }
 }
 
@@ -201,6 +215,16 @@ IDX_DEVI void tmem_ld8(uint32_t taddr, float* v) {
 }
 
 IDX_DEVI void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Warpgroup-wide register reallocation (all 128 threads of the warpgroup).
+template <uint32_t N>
+IDX_DEVI void setmaxnreg_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+IDX_DEVI void setmaxnreg_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
 
 IDX_DEVI void named_bar_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");

@@ -39,7 +39,7 @@ struct ScoreCfg {
     static constexpr int A_CHUNK = M * CHUNK_B;
     static constexpr int B_BYTES = N * RB;
     static constexpr int B_CHUNK = N * CHUNK_B;
-    static constexpr int NS = RB >= 256 ? 4 : (RB == 128 ? 6 : 8);
+    static constexpr int NS = RB >= 256 ? 4 : (RB == 128 ? 8 : 12);
     static constexpr int EPI_WARPS = 16;                    // 4 per SM sub-partition
     static constexpr int NGROUPS = EPI_WARPS / 4;           // warps sharing a lane quarter
     static constexpr int RG = R / NGROUPS;                  // rows per epilogue warp
@@ -74,6 +74,106 @@ IDX_DEVI long long meta_ll(const int* m, int lo) {
 IDX_DEVI void set_meta_ll(int* m, int lo, long long v) {
     m[lo] = (int)(uint32_t)((unsigned long long)v & 0xffffffffull);
     m[lo + 1] = (int)(uint32_t)((unsigned long long)v >> 32);
+}
+
+#ifndef IDX_EPI
+#define IDX_EPI 5
+#endif
+#ifndef IDX_ONE_WAIT
+#define IDX_ONE_WAIT 0
+#endif
+#ifndef IDX_SETMAXNREG
+#define IDX_SETMAXNREG 0
+#endif
+
+// Per-head weights are stored pre-multiplied by this factor per head parity.
+__host__ __device__ constexpr float epi_w_factor(int h) {
+    return (IDX_EPI == 3 && (h & 1)) ? 0.5f : 1.0f;
+}
+// ... and the head sum is multiplied by this factor (with the key scale).
+__host__ __device__ constexpr float epi_post() {
+    return (IDX_EPI == 0 || IDX_EPI == 2 || IDX_EPI == 5) ? 0.5f : 1.0f;
+}
+
+// sum_h w[h] * ReLU(acc[h]) for one (row, key): the TMEM row of this thread,
+// H consecutive columns from taddr, up to a constant factor (epi_post).
+// Eight partial sums in a fixed combine order break the dependency chain.
+template <int H>
+IDX_DEVI float head_reduce(uint32_t taddr, const float* wr) {
+    constexpr int CH = H >= 32 ? 32 : H;
+#if IDX_EPI >= 3
+    float2 acc2[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) acc2[u] = make_float2(0.f, 0.f);
+#else
+    float acc[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) acc[u] = 0.f;
+#endif
+#if IDX_ONE_WAIT
+    float vv[H];
+    if constexpr (CH == 32) {
+#pragma unroll
+        for (int c = 0; c < H / 32; ++c) tmem_ld32(taddr + c * 32, vv + c * 32);
+    } else if constexpr (CH == 16) {
+        tmem_ld16(taddr, vv);
+    } else {
+        tmem_ld8(taddr, vv);
+    }
+    tmem_ld_wait();  // one TMEM round trip per (row, tile)
+#endif
+#pragma unroll
+    for (int c = 0; c < H / CH; ++c) {
+#if IDX_ONE_WAIT
+        const float* v = vv + c * CH;
+#else
+        float v[CH];
+        if constexpr (CH == 32) tmem_ld32(taddr + c * 32, v);
+        else if constexpr (CH == 16) tmem_ld16(taddr, v);
+        else tmem_ld8(taddr, v);
+        tmem_ld_wait();
+#endif
+#if IDX_EPI == 0
+#pragma unroll
+        for (int h = 0; h < CH; ++h)
+            acc[h & 7] = fmaf(wr[c * CH + h], v[h] + fabsf(v[h]), acc[h & 7]);
+#else
+        const float4* w4 = reinterpret_cast<const float4*>(wr + c * CH);
+#pragma unroll
+        for (int h4 = 0; h4 < CH / 4; ++h4) {
+            const float4 wq = w4[h4];
+            float t[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float x = v[4 * h4 + u];
+#if IDX_EPI == 1 || IDX_EPI == 4
+                t[u] = fmaxf(x, 0.f);
+#elif IDX_EPI == 2 || IDX_EPI == 5
+                t[u] = x + fabsf(x);
+#else
+                t[u] = (u & 1) ? x + fabsf(x) : fmaxf(x, 0.f);
+#endif
+            }
+#if IDX_EPI >= 3
+            acc2[(2 * h4) & 3] = __ffma2_rn(make_float2(wq.x, wq.y), make_float2(t[0], t[1]),
+                                            acc2[(2 * h4) & 3]);
+            acc2[(2 * h4 + 1) & 3] = __ffma2_rn(make_float2(wq.z, wq.w), make_float2(t[2], t[3]),
+                                                acc2[(2 * h4 + 1) & 3]);
+#else
+            acc[(4 * h4 + 0) & 7] = fmaf(wq.x, t[0], acc[(4 * h4 + 0) & 7]);
+            acc[(4 * h4 + 1) & 7] = fmaf(wq.y, t[1], acc[(4 * h4 + 1) & 7]);
+            acc[(4 * h4 + 2) & 7] = fmaf(wq.z, t[2], acc[(4 * h4 + 2) & 7]);
+            acc[(4 * h4 + 3) & 7] = fmaf(wq.w, t[3], acc[(4 * h4 + 3) & 7]);
+#endif
+        }
+#endif
+    }
+#if IDX_EPI >= 3
+    return ((acc2[0].x + acc2[0].y) + (acc2[1].x + acc2[1].y)) +
+           ((acc2[2].x + acc2[2].y) + (acc2[3].x + acc2[3].y));
+#else
+    return ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+#endif
 }
 
 template <int DT, int H, int RB>
@@ -171,7 +271,7 @@ score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     }
     for (int i = tid; i < C::R * H; i += C::THREADS) {
         const long long r = r0 + i / H;
-        w_s[i] = r < a.rows ? a.w[(long long)r0 * H + i] : 0.f;
+        w_s[i] = r < a.rows ? a.w[(long long)r0 * H + i] * epi_w_factor(i % H) : 0.f;
     }
     __syncthreads();
     if (tid == 0) {
@@ -220,6 +320,12 @@ score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     tc_fence_after();
     const uint32_t tmem = *tslot;
 
+#if IDX_SETMAXNREG
+    // launch: 640 threads x 96 registers = 61440.  Warpgroup 0 (producer, MMA)
+    // keeps 40, the four epilogue warpgroups take 104: 128*40 + 512*104 = 58368.
+    if (warp < 4) setmaxnreg_dec<40>();
+    else setmaxnreg_inc<104>();
+#endif
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
@@ -311,11 +417,32 @@ score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         const uint32_t lt = (1u << lane) - 1u;
         int cnt[C::RG];
         int ties[C::RG];
+        // per-row visible range [lo, hi) in tile index space (sample indices in
+        // SM_SAMPLE), empty for inactive rows, and the emit threshold key
+        int rlo[C::RG], rhi[C::RG];
+        uint32_t rthr[C::RG];
 #pragma unroll
-        for (int j = 0; j < C::RG; ++j) cnt[j] = ties[j] = 0;
+        for (int j = 0; j < C::RG; ++j) {
+            cnt[j] = ties[j] = 0;
+            const int* m = meta + (grp * C::RG + j) * C::META_WORDS;
+            const bool span = mode == SM_MATERIALISE || mode == SM_SAMPLE;
+            rlo[j] = m[MW_ACTIVE] ? (int)meta_ll(m, span ? MW_SA_LO : MW_KS_LO) : 0;
+            rhi[j] = m[MW_ACTIVE] ? (int)meta_ll(m, span ? MW_SB_LO : MW_KE_LO) : 0;
+            rthr[j] = (uint32_t)m[MW_THR];
+        }
 
+        // per-key scale of the next tile, loaded one tile ahead
+        auto scale_of = [&](long long t) -> float {
+            const long long ki = (t0 + t) * C::M + q * 32 + lane;
+            const long long kk = mode == SM_SAMPLE ? phase + (long long)a.S * ki : ki;
+            const bool ok = t < ntiles && (mode == SM_SAMPLE ? ki < a.nsamp : kk < a.keys);
+            return ok ? __ldg(a.k_scale + kk) : 0.f;
+        };
+        float next_scale = scale_of(0);
         for (long long i = 0; i < ntiles; ++i) {
             const int b = (int)(i & 1);
+            const float cur_scale = next_scale;
+            next_scale = scale_of(i + 1);
             // warp-uniform outcome: the TMEM loads below are .sync.aligned
             if (!__all_sync(0xffffffffu, mbar_wait(&accf[b], (uint32_t)((i >> 1) & 1), abort_flag))) {
                 *abort_flag = 1;
@@ -324,10 +451,7 @@ score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             }
             tc_fence_after();
             const long long kidx = (t0 + i) * C::M + q * 32 + lane;  // key, or sample index
-            const long long key = mode == SM_SAMPLE ? phase + (long long)a.S * kidx : kidx;
-            const bool in_keys = mode == SM_SAMPLE ? (kidx < a.nsamp) : (key < a.keys);
-            // x + |x| = 2 ReLU(x) runs on the FMA pipe; the 1/2 folds into the scale
-            const float half_scale = in_keys ? 0.5f * __ldg(a.k_scale + key) : 0.f;
+            const float post_scale = epi_post() * cur_scale;
 
             float sc[C::RG];
 #pragma unroll
@@ -335,42 +459,23 @@ score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 const int rr = grp * C::RG + j;
                 const uint32_t taddr =
                     tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * C::N + rr * H);
-                const float* wr = w_s + rr * H;
-                float acc[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) acc[u] = 0.f;
-                constexpr int CH = H >= 32 ? 32 : H;
-#pragma unroll
-                for (int c = 0; c < H / CH; ++c) {
-                    float v[CH];
-                    if constexpr (CH == 32) tmem_ld32(taddr + c * 32, v);
-                    else if constexpr (CH == 16) tmem_ld16(taddr, v);
-                    else tmem_ld8(taddr, v);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int h = 0; h < CH; ++h)
-                        acc[h & 7] = fmaf(wr[c * CH + h], v[h] + fabsf(v[h]), acc[h & 7]);
-                }
-                const float sum = ((acc[0] + acc[1]) + (acc[2] + acc[3])) +
-                                  ((acc[4] + acc[5]) + (acc[6] + acc[7]));
-                sc[j] = sum * half_scale;
+                sc[j] = head_reduce<H>(taddr, w_s + rr * H) * post_scale;
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&acce[b]);
 
+            const int k32 = (int)kidx;
             if (mode == SM_MATERIALISE || mode == SM_SAMPLE) {
 #pragma unroll
                 for (int j = 0; j < C::RG; ++j) {
-                    const int rr = grp * C::RG + j;
-                    const int* m = meta + rr * C::META_WORDS;
-                    const long long lo = meta_ll(m, MW_SA_LO), hi = meta_ll(m, MW_SB_LO);
-                    if (m[MW_ACTIVE] && kidx >= lo && kidx < hi) {
-                        const long long r = r0 + rr;
+                    const int off = k32 - rlo[j];
+                    if ((uint32_t)off < (uint32_t)(rhi[j] - rlo[j])) {
+                        const long long r = r0 + grp * C::RG + j;
                         if (mode == SM_MATERIALISE)
-                            a.out[r * a.out_stride + (kidx - lo)] = sc[j];
+                            a.out[r * a.out_stride + off] = sc[j];
                         else
-                            a.samp[r * a.samp_stride + (kidx - lo)] = sc[j];
+                            a.samp[r * a.samp_stride + off] = sc[j];
                     }
                 }
             } else if (mode == SM_EMIT) {
@@ -378,18 +483,17 @@ score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 // its own run q of the row's slab; no cross-warp traffic
 #pragma unroll
                 for (int j = 0; j < C::RG; ++j) {
-                    const int rr = grp * C::RG + j;
-                    const int* m = meta + rr * C::META_WORDS;
-                    const long long lo = meta_ll(m, MW_KS_LO), hi = meta_ll(m, MW_KE_LO);
-                    const bool hit = m[MW_ACTIVE] && kidx >= lo && kidx < hi &&
-                                     fkey(sc[j]) >= (uint32_t)m[MW_THR];
+                    const int off = k32 - rlo[j];
+                    const bool hit = (uint32_t)off < (uint32_t)(rhi[j] - rlo[j]) &&
+                                     fkey(sc[j]) >= rthr[j];
                     const uint32_t A = __ballot_sync(0xffffffffu, hit);
                     if (A) {
                         const int pos = cnt[j] + __popc(A & lt);
                         if (hit && pos < a.cap_q) {
-                            const long long slot = ((long long)(r0 + rr) * 4 + q) * a.cap_q + pos;
+                            const long long slot =
+                                ((long long)(r0 + grp * C::RG + j) * 4 + q) * a.cap_q + pos;
                             a.slab_s[slot] = sc[j];
-                            a.slab_i[slot] = (int)(kidx - lo);
+                            a.slab_i[slot] = off;
                         }
                         cnt[j] += __popc(A);
                     }
