@@ -79,8 +79,9 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 struct FusedParams {
     int cap;    // nominal slab cap
-    int cap_q;  // one warp run: ceil(cap / 4) + 64 (a contiguous range of n keys puts
-                // at most n / 4 + 64 of them into one 32-key column of the tiles)
+    int cap_q;  // one warp run: ceil(cap / 8) + 64 (a contiguous range of n keys puts
+                // at most n / 8 + 64 of them into the 32-key column of the
+                // even or of the odd 128-key tiles that one run collects)
     float target;
     int S;
 };
@@ -102,7 +103,7 @@ FusedParams fused_params(int topk, const idx_options* opt) {
     else
         p.cap = std::max((int)std::ceil(2.25 * topk), 4096);
     if (p.cap < topk) p.cap = topk;
-    p.cap_q = (p.cap + 3) / 4 + 64;
+    p.cap_q = (p.cap + kRuns - 1) / kRuns + 64;
     const double ratio = (double)p.cap / topk;
     double target = opt && opt->target_factor > 0.f ? (double)opt->target_factor : std::sqrt(ratio);
     p.target = (float)target;
@@ -135,9 +136,9 @@ FusedLayout fused_layout(int rows, long long max_len, int cap, int cap_q, int S)
     };
     L.samp_stride = max_len / S + 2;
     L.plan = take((size_t)rows * sizeof(RowPlan));
-    L.run_cnt = take((size_t)rows * 4 * sizeof(int));
-    L.slab_s = take((size_t)rows * 4 * cap_q * sizeof(float));
-    L.slab_i = take((size_t)rows * 4 * cap_q * sizeof(int));
+    L.run_cnt = take((size_t)rows * kRuns * sizeof(int));
+    L.slab_s = take((size_t)rows * kRuns * cap_q * sizeof(float));
+    L.slab_i = take((size_t)rows * kRuns * cap_q * sizeof(int));
     L.samp = take(max_len > cap ? (size_t)rows * L.samp_stride * sizeof(float) : 0);
     L.fb_hist = take(max_len > cap ? (size_t)rows * 4096 * sizeof(uint32_t) : 0);
     L.total = off;
@@ -327,9 +328,10 @@ idx_status idx_score_topk(const void* q, const void* k, const float* k_scale, co
     count_launches(1);
     record(opt, 3, s);
     if (sampling) {
-        // 5. exact rescan of flagged rows: up to three digit passes, one re-emission
+        // 5. exact rescan of flagged rows: up to six digit passes (three over the
+        //    score key, three over the index of exact ties), one re-emission
         FbPickArgs fp{plan, fb_hist, rows, topk, p.cap, 0};
-        for (int level = 0; level <= 2; ++level) {
+        for (int level = 0; level <= 5; ++level) {
             L.a.mode = SM_FB_HIST;
             L.a.level = level;
             if ((e = launch_score(L, s)) != cudaSuccess) return cuda_status(e);

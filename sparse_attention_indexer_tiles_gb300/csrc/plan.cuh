@@ -15,17 +15,29 @@ enum : int32_t {
     ST_DONE = 3,      // out_idx row is final
 };
 
+constexpr int32_t kAllIdx = 0x7fffffff;
+
+// Emit rule of a row: a key is a candidate when its order key is above thr,
+// or equal to thr with a row-relative index <= idx_cut.
+//
+// Exact rescan levels: 0..2 walk the order key from the top (12, 12, 8 bits);
+// once the threshold key T is exact and its ties still exceed the slab, 3..5
+// walk the row-relative index of the ties from the bottom (11, 10, 10 bits),
+// so that the lowest indices among the ties are the ones kept.
 struct RowPlan {
-    uint32_t thr;     // emit rule: key >= thr (quota == 0) ...
-    int32_t quota;    // ... or key > thr plus the first `quota` keys == thr in index order
+    uint32_t thr;
+    int32_t idx_cut;
     int32_t state;
-    int32_t level;    // digit level of the next histogram pass (ST_HIST)
-    uint32_t prefix;  // key bits above that digit (ST_HIST)
-    int32_t above;    // keys known to lie strictly above the prefix set
-    int32_t count;    // candidates of the last emit pass (may exceed cap)
-    int32_t pad;
+    int32_t level;
+    uint32_t prefix;     // key bits (levels 0..2) or index bits (3..5) above the digit
+    int32_t above;       // keys above the prefix set (0..2) / ties below it (3..5)
+    int32_t quota;       // levels 3..5: ties at T that belong to the result
+    int32_t above_thr;   // levels 3..5: keys strictly above T
 };
 static_assert(sizeof(RowPlan) == 32, "RowPlan layout");
+
+// Candidate runs per row: one per (TMEM lane quarter, epilogue team).
+constexpr int kRuns = 8;
 
 // Sample indices i of the strided threshold sample are keys phase + S*i
 // (i < nsamp = floor(keys / S)).  Row r sees samples [a, b).

@@ -25,6 +25,17 @@ IDX_DEVI bool has_prefix(uint32_t key, int level, uint32_t prefix) {
     return (key >> sh) == prefix;
 }
 
+// Index digits of the rescan levels 3..5: bits 30..20, 19..10, 9..0.
+IDX_DEVI int idx_digit_bits(int level) { return level == 3 ? 11 : 10; }
+IDX_DEVI int idx_digit_shift(int level) { return level == 3 ? 20 : (level == 4 ? 10 : 0); }
+IDX_DEVI uint32_t idx_digit_of(uint32_t idx, int level) {
+    return (idx >> idx_digit_shift(level)) & ((1u << idx_digit_bits(level)) - 1u);
+}
+IDX_DEVI bool idx_has_prefix(uint32_t idx, int level, uint32_t prefix) {
+    if (level == 3) return true;
+    return (idx >> (idx_digit_shift(level) + idx_digit_bits(level))) == prefix;
+}
+
 constexpr int kHistBins = 4096;
 
 // Inclusive block-wide sum scan of one uint32 per thread.  `warp_tot` is a

@@ -43,8 +43,8 @@ struct ScoreArgs {
     float* slab_s;
     int* slab_i;
     int cap;              // nominal slab cap (rows seeing <= cap keys emit every key)
-    int cap_q;            // capacity of one warp run: slab row = 4 runs of cap_q
-    int* run_cnt;         // [rows, 4] candidates appended per run (may exceed cap_q)
+    int cap_q;            // capacity of one warp run: slab row = kRuns runs of cap_q
+    int* run_cnt;         // [rows, kRuns] candidates appended per run (may exceed cap_q)
     uint32_t* fb_hist;
     int level;
     int* d_status;

@@ -24,6 +24,7 @@
 namespace idx {
 
 constexpr int kTieCap = 4096;
+constexpr int kCandScratch = 96;  // scan words + row state of cand_topk_kernel
 
 // A row of fp32 values addressed through an aligned float4 view: element p
 // (0 <= p < n) sits in slot p + off of the 16-byte aligned base.  Reads may
@@ -404,9 +405,8 @@ topk_rows_kernel(TopkRowsArgs a) {
         if (len <= a.cap || n <= 0 || n > a.row_len) {
             if (threadIdx.x == 0) {
                 plan->thr = 0u;  // every visible key becomes a candidate
-                plan->quota = 0;
+                plan->idx_cut = kAllIdx;
                 plan->state = ST_MAIN;
-                plan->count = 0;
                 if (a.d_stats && len > 0 && len <= a.cap) atomicAdd(&a.d_stats->emit_all_rows, 1);
             }
             return;
@@ -464,9 +464,8 @@ topk_rows_kernel(TopkRowsArgs a) {
     } else if (threadIdx.x == 0) {
         RowPlan* plan = a.plan + r;
         plan->thr = th.key;
-        plan->quota = 0;
+        plan->idx_cut = kAllIdx;
         plan->state = ST_MAIN;
-        plan->count = 0;
     }
 }
 
@@ -494,32 +493,32 @@ template <int THREADS>
 __global__ void __launch_bounds__(THREADS)
 cand_topk_kernel(CandArgs a) {
     extern __shared__ __align__(16) uint32_t smem[];
-    const int C4 = 4 * a.cap_q;
+    const int CR = kRuns * a.cap_q;
     uint32_t* hist = smem;
-    uint32_t* scratch = hist + kHistBins;   // [0,35) scans, [48,64) row state
-    uint32_t* keys = scratch + 64;
-    uint32_t* idxs = keys + C4;
-    uint32_t* tmp = idxs + C4;              // ~index of the ties, then the selected list
+    uint32_t* scratch = hist + kHistBins;   // [0,35) scans; row state from 48 on
+    uint32_t* keys = scratch + kCandScratch;
+    uint32_t* idxs = keys + CR;
+    uint32_t* tmp = idxs + CR;              // ~index of the ties, then the selected list
+    uint32_t* run_off = scratch + 50;       // [kRuns + 1] run starts in keys[]
+    uint32_t* run_sel = scratch + 64;       // [kRuns + 1] run starts in the selected list
 
     const int r = blockIdx.x;
     RowPlan* plan = a.plan + r;
     const long long n = (long long)a.ke[r] - (long long)a.ks[r];
     int* out = a.out + (long long)r * a.topk;
-    const int nruns = a.fallback ? 1 : 4;
-    const int run_cap = a.fallback ? C4 : a.cap_q;
     if (threadIdx.x == 0) {
         scratch[48] = (uint32_t)plan->state;
         uint32_t off = 0, total = 0, trunc = 0;
-        for (int q = 0; q < nruns; ++q) {
-            const uint32_t c = (uint32_t)a.run_cnt[(long long)r * 4 + q];
-            trunc |= c > (uint32_t)run_cap;
+        for (int q = 0; q < kRuns; ++q) {
+            const uint32_t c = (uint32_t)a.run_cnt[(long long)r * kRuns + q];
+            trunc |= c > (uint32_t)a.cap_q;
             total += c;
-            scratch[50 + q] = off;                       // run start in smem
-            off += c < (uint32_t)run_cap ? c : (uint32_t)run_cap;
+            run_off[q] = off;
+            off += c < (uint32_t)a.cap_q ? c : (uint32_t)a.cap_q;
         }
-        scratch[50 + nruns] = off;
+        run_off[kRuns] = off;
         scratch[49] = trunc;
-        scratch[55] = total;
+        scratch[60] = total;
     }
     __syncthreads();
     const int state = (int)scratch[48];
@@ -530,7 +529,7 @@ cand_topk_kernel(CandArgs a) {
         if (threadIdx.x == 0) plan->state = ST_DONE;
         return;
     }
-    const uint32_t total = scratch[55];
+    const uint32_t total = scratch[60];
     const bool trunc = scratch[49] != 0;
     if (threadIdx.x == 0 && a.d_stats && !a.fallback) atomicMax(&a.d_stats->max_count, (int)total);
     if (trunc || total < (uint32_t)a.topk) {
@@ -564,9 +563,9 @@ cand_topk_kernel(CandArgs a) {
     }
 
     // load the runs back to back
-    const long long row_base = (long long)r * C4;
-    for (int q = 0; q < nruns; ++q) {
-        const uint32_t o = scratch[50 + q], c = scratch[51 + q] - o;
+    const long long row_base = (long long)r * CR;
+    for (int q = 0; q < kRuns; ++q) {
+        const uint32_t o = run_off[q], c = run_off[q + 1] - o;
         const float* ss = a.slab_s + row_base + (long long)q * a.cap_q;
         const int* si = a.slab_i + row_base + (long long)q * a.cap_q;
         for (uint32_t e = threadIdx.x; e < c; e += THREADS) {
@@ -574,12 +573,12 @@ cand_topk_kernel(CandArgs a) {
             idxs[o + e] = (uint32_t)si[e];
         }
     }
-    const uint32_t cnt = scratch[50 + nruns];
+    const uint32_t cnt = run_off[kRuns];
     __syncthreads();
     const Threshold th = refine_in_smem<THREADS>(keys, cnt, 0, 0u, a.topk, hist, scratch);
 
     // lowest indices among the keys equal to T
-    uint32_t* ntie = scratch + 56;
+    uint32_t* ntie = scratch + 61;
     if (threadIdx.x == 0) *ntie = 0u;
     __syncthreads();
     for (uint32_t e = threadIdx.x; e < cnt; e += THREADS)
@@ -593,7 +592,6 @@ cand_topk_kernel(CandArgs a) {
     __syncthreads();
 
     // ordered compaction of the selected entries into tmp (runs stay contiguous)
-    uint32_t* run_sel = scratch + 57;  // [nruns + 1] start of each run in the list
     uint32_t done = 0;
     for (uint32_t base = 0; base < cnt; base += THREADS * 4) {
         uint32_t sel = 0;
@@ -610,11 +608,11 @@ cand_topk_kernel(CandArgs a) {
         for (int c = 0; c < 4; ++c) {
             const uint32_t e = base + threadIdx.x * 4 + c;
             if (e < cnt) {
-                for (int q = 0; q <= nruns; ++q)
-                    if (scratch[50 + q] == e) run_sel[q] = pos;  // first entry of run q
+                for (int q = 0; q <= kRuns; ++q)
+                    if (run_off[q] == e) run_sel[q] = pos;  // first entry of run q
             }
             if ((sel >> c) & 1u) {
-                if (pos < (uint32_t)C4) tmp[pos] = idxs[e];
+                if (pos < (uint32_t)CR) tmp[pos] = idxs[e];
                 ++pos;
             }
         }
@@ -622,8 +620,8 @@ cand_topk_kernel(CandArgs a) {
     }
     if (threadIdx.x == 0) {
         // runs that start at or past the end of the list
-        for (int q = 0; q <= nruns; ++q)
-            if (scratch[50 + q] >= cnt) run_sel[q] = done;
+        for (int q = 0; q <= kRuns; ++q)
+            if (run_off[q] >= cnt) run_sel[q] = done;
     }
     __syncthreads();
 
@@ -632,16 +630,16 @@ cand_topk_kernel(CandArgs a) {
     for (uint32_t p = threadIdx.x; p < nsel; p += THREADS) {
         const uint32_t v = tmp[p];
         int q = 0;
-        while (q + 1 < nruns && p >= run_sel[q + 1]) ++q;
+        while (q + 1 < kRuns && p >= run_sel[q + 1]) ++q;
         uint32_t pos = p - run_sel[q];
-        for (int o = 0; o < nruns; ++o)
+        for (int o = 0; o < kRuns; ++o)
             if (o != q) pos += lower_bound_u32(tmp + run_sel[o], run_sel[o + 1] - run_sel[o], v);
         if (pos < (uint32_t)a.topk) out[pos] = (int)v;
     }
     if (threadIdx.x == 0) plan->state = ST_DONE;
 }
 
-// One digit step of the exact rescan for rows in ST_HIST at `level`.
+// One digit step of the exact rescan for rows in ST_HIST at `level` (0..5).
 template <int THREADS>
 __global__ void __launch_bounds__(THREADS)
 fb_pick_kernel(FbPickArgs a) {
@@ -651,29 +649,54 @@ fb_pick_kernel(FbPickArgs a) {
     RowPlan* plan = a.plan + r;
     if (plan->state != ST_HIST || plan->level != a.level) return;
     const int level = a.level;
-    const int nb = 1 << digit_bits(level);
+    const bool by_key = level <= 2;
+    const int bits = by_key ? digit_bits(level) : idx_digit_bits(level);
+    const int nb = 1 << bits;
     uint32_t* gh = a.fb_hist + (long long)r * kHistBins;
-    for (int i = threadIdx.x; i < kHistBins; i += THREADS) hist[i] = i < nb ? gh[i] : 0u;
+    // key levels pick from the top; index levels from the bottom (read reversed)
+    for (int i = threadIdx.x; i < kHistBins; i += THREADS)
+        hist[i] = i < nb ? gh[by_key ? i : nb - 1 - i] : 0u;
     __syncthreads();
     for (int i = threadIdx.x; i < nb; i += THREADS) gh[i] = 0u;  // ready for the next level
     const uint32_t above = static_cast<uint32_t>(plan->above);
-    const uint32_t need = static_cast<uint32_t>(a.topk) - above;
+    const uint32_t quota = static_cast<uint32_t>(plan->quota);
+    const uint32_t need = by_key ? static_cast<uint32_t>(a.topk) - above : quota - above;
     const DigitPick pk = pick_digit<THREADS>(hist, nb, need, scratch);
     if (threadIdx.x == 0) {
-        const uint32_t above_new = above + pk.above;
-        const uint32_t prefix = (plan->prefix << digit_bits(level)) | pk.digit;
-        if (above_new + pk.count <= (uint32_t)a.cap) {
-            plan->thr = prefix << digit_shift(level);
-            plan->quota = 0;
-            plan->state = ST_EMIT;
-        } else if (level < 2) {
-            plan->prefix = prefix;
-            plan->above = static_cast<int32_t>(above_new);
-            plan->level = level + 1;
+        if (by_key) {
+            const uint32_t above_new = above + pk.above;
+            const uint32_t prefix = (plan->prefix << bits) | pk.digit;
+            if (above_new + pk.count <= (uint32_t)a.cap) {
+                plan->thr = prefix << digit_shift(level);
+                plan->idx_cut = kAllIdx;
+                plan->state = ST_EMIT;
+            } else if (level < 2) {
+                plan->prefix = prefix;
+                plan->above = static_cast<int32_t>(above_new);
+                plan->level = level + 1;
+            } else {
+                // T exact; its ties overflow the slab: keep the lowest indices
+                plan->thr = prefix;
+                plan->above_thr = static_cast<int32_t>(above_new);
+                plan->quota = a.topk - static_cast<int32_t>(above_new);
+                plan->prefix = 0u;
+                plan->above = 0;
+                plan->level = 3;
+            }
         } else {
-            plan->thr = prefix;  // exact key; ties taken in index order
-            plan->quota = a.topk - static_cast<int32_t>(above_new);
-            plan->state = ST_EMIT;
+            const uint32_t digit = (uint32_t)(nb - 1) - pk.digit;  // undo the reversal
+            const uint32_t below_new = above + pk.above;          // ties with a smaller index
+            const uint32_t prefix = (plan->prefix << bits) | digit;
+            const uint32_t keep = (uint32_t)plan->above_thr + below_new + pk.count;
+            const int sh = idx_digit_shift(level);
+            if (keep <= (uint32_t)a.cap || level == 5) {
+                plan->idx_cut = (int32_t)((prefix << sh) | ((1u << sh) - 1u));
+                plan->state = ST_EMIT;
+            } else {
+                plan->prefix = prefix;
+                plan->above = static_cast<int32_t>(below_new);
+                plan->level = level + 1;
+            }
         }
     }
 }
@@ -693,7 +716,8 @@ cudaError_t launch_topk_rows(const TopkRowsArgs& a, cudaStream_t s) {
 }
 
 size_t cand_smem_bytes(int cap_q) {
-    return (kHistBins + 64) * sizeof(uint32_t) + (size_t)cap_q * 4 * 3 * sizeof(uint32_t);
+    return (kHistBins + kCandScratch) * sizeof(uint32_t) +
+           (size_t)cap_q * kRuns * 3 * sizeof(uint32_t);
 }
 
 cudaError_t launch_cand_topk(const CandArgs& a, cudaStream_t s) {

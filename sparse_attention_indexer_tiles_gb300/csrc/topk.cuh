@@ -38,9 +38,9 @@ struct TopkRowsArgs {
 };
 
 struct CandArgs {
-    const float* slab_s;  // [rows, 4, cap_q]
-    const int* slab_i;    // [rows, 4, cap_q]
-    const int* run_cnt;   // [rows, 4]
+    const float* slab_s;  // [rows, kRuns, cap_q]
+    const int* slab_i;    // [rows, kRuns, cap_q]
+    const int* run_cnt;   // [rows, kRuns]
     int cap_q;
     RowPlan* plan;
     uint32_t* fb_hist;    // [rows, 4096]

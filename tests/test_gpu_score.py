@@ -168,6 +168,26 @@ def test_fused_all_ties(idx):
     assert st["fallback_rows"] == 9 and st["status"] == 0
 
 
+def test_fused_ties_below_positive_keys(idx):
+    """Only a few keys score above 0 and every other key ties at exactly 0: the
+    rescan keeps all positive keys plus the lowest-index zeros (index digits)."""
+    inp = synth.indexer_inputs(6, 12000, 32, 128, 400, "fp8", seed=46)
+    inp.q.zero_()
+    inp.q[:, 0, 0] = 1.0
+    k = inp.k.float()
+    k[:, 0] = -1.0
+    g = torch.Generator().manual_seed(47)
+    pos = torch.randperm(12000, generator=g)[:150]
+    k[pos, 0] = torch.rand(150, generator=g) * 4 + 0.5
+    inp.k = k.to(torch.float8_e4m3fn)
+    stats = idx.Stats(torch.device(DEV))
+    got = fused(idx, inp, stats=stats, cap_factor=2.0)
+    ref = oracle.score_topk(inp)
+    assert np.array_equal(got, ref)
+    st = stats.read()
+    assert st["fallback_rows"] == 6 and st["status"] == 0
+
+
 def test_fused_mixed_ranges(idx):
     """Rows of one CTA with different visible ranges, empty rows, rows shorter
     than topk (padded with -1) and rows longer than the slab."""
