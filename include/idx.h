@@ -164,6 +164,38 @@ idx_status idx_score_materialise(const void* q, const void* k, const float* k_sc
                                  long long keys, int H, int D, idx_dtype dt, float* scores,
                                  long long row_stride, const idx_options* opt, void* stream);
 
+/* ------------------------------------------------------------------------
+ * idx_score_topk_noalloc - idx_score_topk for callers that cannot allocate.
+ * The paper has no counterpart to this entry point.
+ *
+ * Some callers only hold pointers to memory that someone else owns (a plugin
+ * in a host framework that gives its extensions no allocator, or a serving
+ * loop that must not call cudaMalloc, which can synchronize the device) and so
+ * cannot pass a workspace.  This call takes the same arguments as
+ * idx_score_topk without ws/ws_bytes and runs the same kernels on a scratch
+ * array compiled into the library; it allocates no memory.
+ *
+ *  - Limit: the problem's idx_score_topk_workspace(...) must not exceed
+ *    IDX_NOALLOC_SCRATCH_BYTES (32 MiB); larger problems return
+ *    IDX_EWORKSPACE and launch nothing.  At topk 2048 with 64K-key rows that
+ *    is about 480 query rows per call.
+ *  - Every GPU that loads the library holds the 32 MiB array until the
+ *    process exits.
+ *  - The first call on a device looks up the array's device address (with
+ *    that device current) and caches it; make that first call before any
+ *    stream capture.
+ *  - All calls share the one array, and each call leaves its contents behind
+ *    (the kernels write every word they later read, so nothing needs
+ *    clearing).  Calls whose executions overlap on the GPU, on any stream or
+ *    from any thread, race on it: serialize them.
+ * ------------------------------------------------------------------------ */
+#define IDX_NOALLOC_SCRATCH_BYTES (32ull << 20)
+idx_status idx_score_topk_noalloc(const void* q, const void* k, const float* k_scale,
+                                  const float* w, const int* ks, const int* ke, int rows,
+                                  long long keys, long long max_len, int H, int D, int topk,
+                                  idx_dtype dt, int* out_idx, const idx_options* opt,
+                                  void* stream);
+
 /* Static text for a status code. */
 const char* idx_status_string(idx_status s);
 

@@ -22,6 +22,7 @@ __all__ = [
     "IdxError", "Options", "Stats", "load", "idx_score_topk", "idx_score_topk_workspace",
     "idx_topk_from_scores", "idx_topk_workspace", "idx_score_materialise",
     "idx_status_string", "DTYPES", "STAT_FIELDS", "StageEvents", "idx_launch_count",
+    "idx_score_topk_noalloc",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -238,4 +239,24 @@ def idx_score_materialise(q, k, k_scale, w, ks, ke, *, out=None, row_stride: int
     _check("idx_score_materialise", load().idx_score_materialise(
         _ptr(q), _ptr(k), _ptr(k_scale), _ptr(w), _ptr(ks), _ptr(ke), rows, keys, H, D,
         DTYPES[q.dtype], _ptr(out), stride, _opt_ref(o), _stream(stream)))
+    return out
+
+
+def idx_score_topk_noalloc(q, k, k_scale, w, ks, ke, topk: int, *, max_len: int = 0, out=None,
+                           options=None, stats: Stats | None = None, stream=None):
+    """idx_score_topk on the library's built-in scratch array (no workspace,
+    no allocation by the library; out is allocated here when not given)."""
+    _dev(q, k, k_scale, w, ks, ke, out)
+    lib = load()
+    fn = lib.idx_score_topk_noalloc
+    P, I, LL = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong
+    fn.argtypes = [P, P, P, P, P, P, I, LL, LL, I, I, I, I, P, P, P]
+    fn.restype = I
+    rows, H, D = q.shape
+    if out is None:
+        out = torch.empty(rows, topk, dtype=torch.int32, device=q.device)
+    o = make_options(options, stats)
+    _check("idx_score_topk_noalloc", fn(
+        _ptr(q), _ptr(k), _ptr(k_scale), _ptr(w), _ptr(ks), _ptr(ke), rows, k.shape[0], max_len,
+        H, D, topk, DTYPES[q.dtype], _ptr(out), _opt_ref(o), _stream(stream)))
     return out
