@@ -122,7 +122,7 @@ FusedParams fused_params(int topk, const idx_options* opt) {
 }
 
 struct FusedLayout {
-    size_t plan, run_cnt, slab_s, slab_i, samp, fb_hist, total;
+    size_t plan, run_cnt, slab_s, slab_i, samp, fb_hist, fb_cnt, total;
     long long samp_stride;
 };
 
@@ -141,6 +141,7 @@ FusedLayout fused_layout(int rows, long long max_len, int cap, int cap_q, int S)
     L.slab_i = take((size_t)rows * kRuns * cap_q * sizeof(int));
     L.samp = take(max_len > cap ? (size_t)rows * L.samp_stride * sizeof(float) : 0);
     L.fb_hist = take(max_len > cap ? (size_t)rows * 4096 * sizeof(uint32_t) : 0);
+    L.fb_cnt = take(8 * sizeof(int));
     L.total = off;
     return L;
 }
@@ -253,6 +254,7 @@ idx_status idx_score_topk(const void* q, const void* k, const float* k_scale, co
     int* slab_i = reinterpret_cast<int*>(base + lay.slab_i);
     float* samp = reinterpret_cast<float*>(base + lay.samp);
     uint32_t* fb_hist = reinterpret_cast<uint32_t*>(base + lay.fb_hist);
+    int* fb_cnt = reinterpret_cast<int*>(base + lay.fb_cnt);
     int* d_status = opt ? opt->d_status : nullptr;
     idx_stats* d_stats = opt ? opt->d_stats : nullptr;
     const bool sampling = max_len > p.cap;
@@ -265,6 +267,7 @@ idx_status idx_score_topk(const void* q, const void* k, const float* k_scale, co
     L.a.cap_q = p.cap_q;
     L.a.run_cnt = run_cnt;
     L.a.fb_hist = fb_hist;
+    L.a.fb_cnt = fb_cnt;
     L.a.S = p.S;
     L.a.nsamp = keys / p.S;
     L.a.samp = samp;
@@ -315,6 +318,7 @@ idx_status idx_score_topk(const void* q, const void* k, const float* k_scale, co
     c.cap_q = p.cap_q;
     c.plan = plan;
     c.fb_hist = sampling ? fb_hist : nullptr;
+    c.fb_cnt = fb_cnt;
     c.ks = ks;
     c.ke = ke;
     c.rows = rows;
@@ -329,15 +333,13 @@ idx_status idx_score_topk(const void* q, const void* k, const float* k_scale, co
     record(opt, 3, s);
     if (sampling) {
         // 5. exact rescan of flagged rows: up to six digit passes (three over the
-        //    score key, three over the index of exact ties), one re-emission
-        FbPickArgs fp{plan, fb_hist, rows, topk, p.cap, 0};
+        //    score key, three over the index of exact ties), each finishing its
+        //    digit step in the CTA that owns the row, then one re-emission;
+        //    passes with no row waiting exit at once
         for (int level = 0; level <= 5; ++level) {
             L.a.mode = SM_FB_HIST;
             L.a.level = level;
             if ((e = launch_score(L, s)) != cudaSuccess) return cuda_status(e);
-            fp.level = level;
-            if ((e = launch_fb_pick(fp, s)) != cudaSuccess) return cuda_status(e);
-            count_launches(1);
         }
         L.a.mode = SM_FB_EMIT;
         if ((e = launch_score(L, s)) != cudaSuccess) return cuda_status(e);

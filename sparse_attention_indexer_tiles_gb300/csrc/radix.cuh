@@ -9,6 +9,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "plan.cuh"
 
 namespace idx {
 
@@ -112,6 +113,101 @@ IDX_DEVI DigitPick pick_digit(const uint32_t* hist, int nbins, uint32_t need,
     DigitPick p{res[0], res[1], res[2]};
     __syncthreads();
     return p;
+}
+
+// ------------------------------------------------------ rescan digit step
+//
+// One warp, one row: given the histogram of this level's digit (global
+// memory, written by this CTA), pick the digit that holds the boundary of the
+// top-k and advance the row's plan.  Key levels 0..2 count from the top (the
+// largest keys), index levels 3..5 from the bottom (the lowest indices among
+// the keys equal to T).  The histogram row is cleared for the next level.
+// fb_cnt[l] counts the rows waiting for level l, fb_cnt[6] those ready to emit.
+IDX_DEVI void rescan_pick_warp(RowPlan* plan, uint32_t* hist, int level, int topk, int cap,
+                               int* fb_cnt) {
+    const int lane = threadIdx.x & 31;
+    const bool by_key = level <= 2;
+    const int bits = by_key ? digit_bits(level) : idx_digit_bits(level);
+    const int nb = 1 << bits;
+    const int per = nb / 32;
+    const uint32_t above = (uint32_t)plan->above;
+    const uint32_t need = by_key ? (uint32_t)topk - above : (uint32_t)plan->quota - above;
+    // lane l owns the l-th chunk of bins in scan order
+    auto bin_at = [&](int k) { return by_key ? nb - 1 - k : k; };
+    uint32_t local = 0;
+    for (int k = lane * per; k < (lane + 1) * per; ++k) local += __ldcg(hist + bin_at(k));
+    uint32_t incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    const uint32_t excl = incl - local;
+    const bool mine = excl < need && need <= incl;
+    uint32_t digit = 0, before = 0, count = 0;
+    if (mine) {
+        uint32_t cum = excl;
+        for (int k = lane * per; k < (lane + 1) * per; ++k) {
+            const uint32_t c = __ldcg(hist + bin_at(k));
+            if (cum + c >= need) {
+                digit = (uint32_t)bin_at(k);
+                before = cum;
+                count = c;
+                break;
+            }
+            cum += c;
+        }
+    }
+    const uint32_t who = __ballot_sync(0xffffffffu, mine);
+    const int src = who ? __ffs(who) - 1 : 0;
+    digit = __shfl_sync(0xffffffffu, digit, src);
+    before = __shfl_sync(0xffffffffu, before, src);
+    count = __shfl_sync(0xffffffffu, count, src);
+    for (int k = lane; k < nb; k += 32) hist[k] = 0u;  // ready for the next level
+    if (lane != 0) return;
+    if (!who) {  // inconsistent histogram: give up on the row
+        plan->state = ST_DONE;
+        return;
+    }
+    if (by_key) {
+        const uint32_t above_new = above + before;
+        const uint32_t prefix = (plan->prefix << bits) | digit;
+        if (above_new + count <= (uint32_t)cap) {
+            plan->thr = prefix << digit_shift(level);
+            plan->idx_cut = kAllIdx;
+            plan->state = ST_EMIT;
+            atomicAdd(&fb_cnt[6], 1);
+        } else if (level < 2) {
+            plan->prefix = prefix;
+            plan->above = (int32_t)above_new;
+            plan->level = level + 1;
+            atomicAdd(&fb_cnt[level + 1], 1);
+        } else {
+            // T exact; its ties overflow the slab: keep the lowest indices
+            plan->thr = prefix;
+            plan->above_thr = (int32_t)above_new;
+            plan->quota = topk - (int32_t)above_new;
+            plan->prefix = 0u;
+            plan->above = 0;
+            plan->level = 3;
+            atomicAdd(&fb_cnt[3], 1);
+        }
+    } else {
+        const uint32_t below_new = above + before;  // ties with a smaller index
+        const uint32_t prefix = (plan->prefix << bits) | digit;
+        const uint32_t keep = (uint32_t)plan->above_thr + below_new + count;
+        const int sh = idx_digit_shift(level);
+        if (keep <= (uint32_t)cap || level == 5) {
+            plan->idx_cut = (int32_t)((prefix << sh) | ((1u << sh) - 1u));
+            plan->state = ST_EMIT;
+            atomicAdd(&fb_cnt[6], 1);
+        } else {
+            plan->prefix = prefix;
+            plan->above = (int32_t)below_new;
+            plan->level = level + 1;
+            atomicAdd(&fb_cnt[level + 1], 1);
+        }
+    }
 }
 
 template <int THREADS>

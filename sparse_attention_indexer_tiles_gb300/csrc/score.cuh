@@ -46,6 +46,7 @@ struct ScoreArgs {
     int cap_q;            // capacity of one warp run: slab row = kRuns runs of cap_q
     int* run_cnt;         // [rows, kRuns] candidates appended per run (may exceed cap_q)
     uint32_t* fb_hist;
+    int* fb_cnt;          // [8] rows waiting per rescan level, [6] ready to emit
     int level;
     int* d_status;
     idx_stats* d_stats;

@@ -130,6 +130,10 @@ score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int r0 = blockIdx.x * C::R;
     const int mode = a.mode;
+    // exact rescan launches with no row waiting for them end here
+    if (mode == SM_FB_HIST && *(volatile int*)(a.fb_cnt + a.level) == 0) return;
+    if (mode == SM_FB_EMIT && *(volatile int*)(a.fb_cnt + 6) == 0) return;
+    if (mode == SM_SAMPLE && blockIdx.x == 0 && tid < 8) a.fb_cnt[tid] = 0;  // new call
     const int phase =
         mode == SM_SAMPLE ? (int)(hash32((uint32_t)blockIdx.x ^ a.phase_seed) % (uint32_t)a.S) : 0;
 
@@ -463,6 +467,16 @@ score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
 #undef RTHR
 #undef RCUT
 #undef RPRE
+        if (mode == SM_FB_HIST) {
+            // this CTA saw every key of its rows: finish the digit step here
+            __threadfence();  // the histogram atomics of every warp reached L2
+            named_bar_sync(1, 32 * C::EPI_WARPS);
+            for (int rr = e; rr < C::R; rr += C::EPI_WARPS) {
+                if (!meta[rr * C::META_WORDS + MW_ACTIVE]) continue;
+                rescan_pick_warp(a.plan + r0 + rr, a.fb_hist + (long long)(r0 + rr) * kHistBins,
+                                 a.level, a.topk, a.cap, a.fb_cnt);
+            }
+        }
         if (lane == 0 && (mode == SM_EMIT || mode == SM_FB_EMIT)) {
 #pragma unroll
             for (int j = 0; j < C::RG; ++j) {

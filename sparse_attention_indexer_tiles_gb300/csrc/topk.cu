@@ -16,7 +16,6 @@
 //                       memory (page 1: the small top-k over ~2.25 x topk
 //                       candidates); flags rows whose slab is short or
 //                       overflowed for the exact rescan.
-//  * fb_pick_kernel     one digit step of that rescan.
 #include "plan.cuh"
 #include "radix.cuh"
 #include "topk.cuh"
@@ -502,6 +501,7 @@ cand_topk_kernel(CandArgs a) {
     uint32_t* run_off = scratch + 50;       // [kRuns + 1] run starts in keys[]
     uint32_t* run_sel = scratch + 64;       // [kRuns + 1] run starts in the selected list
 
+    if (a.fallback && *(volatile int*)(a.fb_cnt + 6) == 0) return;  // no row was re-emitted
     const int r = blockIdx.x;
     RowPlan* plan = a.plan + r;
     const long long n = (long long)a.ke[r] - (long long)a.ks[r];
@@ -550,6 +550,7 @@ cand_topk_kernel(CandArgs a) {
                 plan->level = 0;
                 plan->prefix = 0u;
                 plan->above = 0;
+                atomicAdd(&a.fb_cnt[0], 1);
                 if (a.d_stats) {
                     atomicAdd(trunc ? &a.d_stats->overflow_rows : &a.d_stats->short_rows, 1);
                     atomicAdd(&a.d_stats->fallback_rows, 1);
@@ -639,68 +640,6 @@ cand_topk_kernel(CandArgs a) {
     if (threadIdx.x == 0) plan->state = ST_DONE;
 }
 
-// One digit step of the exact rescan for rows in ST_HIST at `level` (0..5).
-template <int THREADS>
-__global__ void __launch_bounds__(THREADS)
-fb_pick_kernel(FbPickArgs a) {
-    __shared__ uint32_t hist[kHistBins];
-    __shared__ uint32_t scratch[64];
-    const int r = blockIdx.x;
-    RowPlan* plan = a.plan + r;
-    if (plan->state != ST_HIST || plan->level != a.level) return;
-    const int level = a.level;
-    const bool by_key = level <= 2;
-    const int bits = by_key ? digit_bits(level) : idx_digit_bits(level);
-    const int nb = 1 << bits;
-    uint32_t* gh = a.fb_hist + (long long)r * kHistBins;
-    // key levels pick from the top; index levels from the bottom (read reversed)
-    for (int i = threadIdx.x; i < kHistBins; i += THREADS)
-        hist[i] = i < nb ? gh[by_key ? i : nb - 1 - i] : 0u;
-    __syncthreads();
-    for (int i = threadIdx.x; i < nb; i += THREADS) gh[i] = 0u;  // ready for the next level
-    const uint32_t above = static_cast<uint32_t>(plan->above);
-    const uint32_t quota = static_cast<uint32_t>(plan->quota);
-    const uint32_t need = by_key ? static_cast<uint32_t>(a.topk) - above : quota - above;
-    const DigitPick pk = pick_digit<THREADS>(hist, nb, need, scratch);
-    if (threadIdx.x == 0) {
-        if (by_key) {
-            const uint32_t above_new = above + pk.above;
-            const uint32_t prefix = (plan->prefix << bits) | pk.digit;
-            if (above_new + pk.count <= (uint32_t)a.cap) {
-                plan->thr = prefix << digit_shift(level);
-                plan->idx_cut = kAllIdx;
-                plan->state = ST_EMIT;
-            } else if (level < 2) {
-                plan->prefix = prefix;
-                plan->above = static_cast<int32_t>(above_new);
-                plan->level = level + 1;
-            } else {
-                // T exact; its ties overflow the slab: keep the lowest indices
-                plan->thr = prefix;
-                plan->above_thr = static_cast<int32_t>(above_new);
-                plan->quota = a.topk - static_cast<int32_t>(above_new);
-                plan->prefix = 0u;
-                plan->above = 0;
-                plan->level = 3;
-            }
-        } else {
-            const uint32_t digit = (uint32_t)(nb - 1) - pk.digit;  // undo the reversal
-            const uint32_t below_new = above + pk.above;          // ties with a smaller index
-            const uint32_t prefix = (plan->prefix << bits) | digit;
-            const uint32_t keep = (uint32_t)plan->above_thr + below_new + pk.count;
-            const int sh = idx_digit_shift(level);
-            if (keep <= (uint32_t)a.cap || level == 5) {
-                plan->idx_cut = (int32_t)((prefix << sh) | ((1u << sh) - 1u));
-                plan->state = ST_EMIT;
-            } else {
-                plan->prefix = prefix;
-                plan->above = static_cast<int32_t>(below_new);
-                plan->level = level + 1;
-            }
-        }
-    }
-}
-
 // ------------------------------------------------------------ launchers
 
 cudaError_t launch_topk_rows(const TopkRowsArgs& a, cudaStream_t s) {
@@ -731,10 +670,6 @@ cudaError_t launch_cand_topk(const CandArgs& a, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-cudaError_t launch_fb_pick(const FbPickArgs& a, cudaStream_t s) {
-    if (a.rows == 0) return cudaSuccess;
-    fb_pick_kernel<256><<<a.rows, 256, 0, s>>>(a);
-    return cudaGetLastError();
-}
+
 
 }  // namespace idx

@@ -44,6 +44,7 @@ struct CandArgs {
     int cap_q;
     RowPlan* plan;
     uint32_t* fb_hist;    // [rows, 4096]
+    int* fb_cnt;          // [8] rescan counters (see RowPlan)
     const int* ks;
     const int* ke;
     int rows, topk, cap;
@@ -53,15 +54,9 @@ struct CandArgs {
     idx_stats* d_stats;
 };
 
-struct FbPickArgs {
-    RowPlan* plan;
-    uint32_t* fb_hist;
-    int rows, topk, cap, level;
-};
 
 cudaError_t launch_topk_rows(const TopkRowsArgs& a, cudaStream_t s);
 cudaError_t launch_cand_topk(const CandArgs& a, cudaStream_t s);
-cudaError_t launch_fb_pick(const FbPickArgs& a, cudaStream_t s);
 size_t cand_smem_bytes(int cap_q);
 
 }  // namespace idx
