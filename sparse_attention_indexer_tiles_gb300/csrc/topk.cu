@@ -626,16 +626,61 @@ cand_topk_kernel(CandArgs a) {
     }
     __syncthreads();
 
-    // merge: output rank = rank in own run + entries of the other runs below it
+    // Output order.  An aligned block of 32 keys lies in one 32-key column of
+    // one tile, so all its candidates sit in one run, contiguous and ascending.
+    // Counting the selected entries per block and scanning the counts gives
+    // every entry its output position; rows with more blocks than the
+    // histogram (or keys[]) holds merge the runs by binary search instead.
     const uint32_t nsel = done < (uint32_t)a.topk ? done : (uint32_t)a.topk;
-    for (uint32_t p = threadIdx.x; p < nsel; p += THREADS) {
-        const uint32_t v = tmp[p];
-        int q = 0;
-        while (q + 1 < kRuns && p >= run_sel[q + 1]) ++q;
-        uint32_t pos = p - run_sel[q];
-        for (int o = 0; o < kRuns; ++o)
-            if (o != q) pos += lower_bound_u32(tmp + run_sel[o], run_sel[o + 1] - run_sel[o], v);
-        if (pos < (uint32_t)a.topk) out[pos] = (int)v;
+    const long long ks_r = a.ks[r];
+    const long long b_first = ks_r >> 5;
+    const long long nblk = n > 0 ? ((ks_r + n - 1) >> 5) - b_first + 1 : 0;
+    if (nblk <= kHistBins && nblk <= CR) {
+        uint32_t* first = keys;  // keys[] is free now: first list position of each block
+        zero_shared<THREADS>(hist, kHistBins);
+        __syncthreads();
+        for (uint32_t p = threadIdx.x; p < nsel; p += THREADS) {
+            const uint32_t b = (uint32_t)(((ks_r + tmp[p]) >> 5) - b_first);
+            atomicAdd(&hist[b], 1u);
+            int q = 0;
+            while (q + 1 < kRuns && p >= run_sel[q + 1]) ++q;
+            const bool head = p == run_sel[q] ||
+                              (uint32_t)(((ks_r + tmp[p - 1]) >> 5) - b_first) != b;
+            if (head) first[b] = p;
+        }
+        __syncthreads();
+        // exclusive scan of the block counts, BPT consecutive blocks per thread
+        constexpr int BPT = kHistBins / THREADS;
+        uint32_t c[BPT], local = 0;
+#pragma unroll
+        for (int j = 0; j < BPT; ++j) {
+            c[j] = hist[threadIdx.x * BPT + j];
+            local += c[j];
+        }
+        const uint32_t incl = block_incl_scan<THREADS>(local, scratch, nullptr);
+        uint32_t run_sum = incl - local;
+#pragma unroll
+        for (int j = 0; j < BPT; ++j) {
+            hist[threadIdx.x * BPT + j] = run_sum;
+            run_sum += c[j];
+        }
+        __syncthreads();
+        for (uint32_t p = threadIdx.x; p < nsel; p += THREADS) {
+            const uint32_t b = (uint32_t)(((ks_r + tmp[p]) >> 5) - b_first);
+            const uint32_t pos = hist[b] + (p - first[b]);
+            if (pos < (uint32_t)a.topk) out[pos] = (int)tmp[p];
+        }
+    } else {
+        // output rank = rank in own run + entries of the other runs below it
+        for (uint32_t p = threadIdx.x; p < nsel; p += THREADS) {
+            const uint32_t v = tmp[p];
+            int q = 0;
+            while (q + 1 < kRuns && p >= run_sel[q + 1]) ++q;
+            uint32_t pos = p - run_sel[q];
+            for (int o = 0; o < kRuns; ++o)
+                if (o != q) pos += lower_bound_u32(tmp + run_sel[o], run_sel[o + 1] - run_sel[o], v);
+            if (pos < (uint32_t)a.topk) out[pos] = (int)v;
+        }
     }
     if (threadIdx.x == 0) plan->state = ST_DONE;
 }
