@@ -113,8 +113,9 @@ score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
              const __grid_constant__ CUtensorMap tm_ks, const __grid_constant__ ScoreArgs a) {
     using C = ScoreCfg<DT, H, RB>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                               ~uintptr_t(1023));
+    // 1024-byte aligned base (TMA swizzle atoms), derived from smem_raw by an
+    // offset so that the compiler keeps every access in the shared space
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
     uint64_t* full = bars;
     uint64_t* empty = bars + C::NS;
