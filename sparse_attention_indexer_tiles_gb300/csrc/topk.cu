@@ -230,37 +230,54 @@ struct StreamSmem {
         (kHistBins + 64 + 3 * W + 2 * (size_t)RUN_WORDS) * sizeof(uint32_t);
 };
 
+// The float whose order key is L: for every non-NaN f, f >= it exactly when
+// fkey(f) >= L (fkey is monotone and folds -0 onto +0).  Keys below the one of
+// -inf admit every non-NaN value.
+IDX_DEVI float key_floor_float(uint32_t L) {
+    if (L <= 0x007fffffu) return -INFINITY;
+    return __uint_as_float((L & 0x80000000u) ? (L & 0x7fffffffu) : ~L);
+}
+
 // Append every key >= L of warp w's slice to its run; returns through rcnt[w].
+// The hot loop compares floats; order keys are formed for the few hits only,
+// and element bounds are checked only in the row's first and last 16 bytes.
 template <int THREADS, int UNROLL>
 IDX_DEVI void stream_collect(const RowView& v, uint32_t L, uint32_t* rkey, uint32_t* ridx,
                              uint32_t* rcnt) {
     constexpr int W = THREADS / 32;
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const long long seg = (v.nvec + W - 1) / W;
-    const long long s0 = (long long)w * seg;
-    const long long s1 = s0 + seg < v.nvec ? s0 + seg : v.nvec;
+    const int nvec = (int)v.nvec, n = (int)v.n, off = v.off;
+    const int seg = (nvec + W - 1) / W;
+    const int s0 = w * seg;
+    const int s1 = s0 + seg < nvec ? s0 + seg : nvec;
+    const float Lf = key_floor_float(L);
     uint32_t* mk = rkey + w * kRunCap;
     uint32_t* mi = ridx + w * kRunCap;
     uint32_t cnt = 0;
-    for (long long base = s0; base < s1; base += 32 * UNROLL) {
+    for (int base = s0; base < s1; base += 32 * UNROLL) {
         float4 f[UNROLL];
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
-            const long long sl = base + u * 32 + lane;
+            const int sl = base + u * 32 + lane;
             f[u] = sl < s1 ? ldg4(v.base + sl) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
+        // every slot of this step holds 4 visible values (warp-uniform)
+        const bool interior = base >= 1 && base + 32 * UNROLL <= s1 && base + 32 * UNROLL < nvec;
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
-            const long long sl = base + u * 32 + lane;
+            const int sl = base + u * 32 + lane;
             const float e[4] = {f[u].x, f[u].y, f[u].z, f[u].w};
-            uint32_t keys[4];
             uint32_t hits = 0;
+            if (interior) {
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const long long p = 4 * sl + c - v.off;
-                keys[c] = fkey(e[c]);
-                const bool h = sl < s1 && p >= 0 && p < v.n && keys[c] >= L;
-                hits |= (h ? 1u : 0u) << c;
+                for (int c = 0; c < 4; ++c) hits |= (e[c] >= Lf ? 1u : 0u) << c;
+            } else {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int p = 4 * sl + c - off;
+                    const bool h = sl < s1 && p >= 0 && p < n && (L == 0u || e[c] >= Lf);
+                    hits |= (h ? 1u : 0u) << c;
+                }
             }
             if (!__any_sync(0xffffffffu, hits != 0)) continue;
             // exclusive prefix of the hit counts over the lanes (index order)
@@ -276,8 +293,8 @@ IDX_DEVI void stream_collect(const RowView& v, uint32_t L, uint32_t* rkey, uint3
             for (int c = 0; c < 4; ++c) {
                 if ((hits >> c) & 1u) {
                     if (pos < (uint32_t)kRunCap) {
-                        mk[pos] = keys[c];
-                        mi[pos] = static_cast<uint32_t>(4 * sl + c - v.off);
+                        mk[pos] = fkey(e[c]);
+                        mi[pos] = static_cast<uint32_t>(4 * sl + c - off);
                     }
                     ++pos;
                 }
