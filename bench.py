@@ -201,6 +201,24 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def slowest_ms(ms: float, world: int, device=None) -> float:
+    """The slowest rank's time: every rank runs its own replica, the job is done
+    when the last one is."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64,
+                     device=device if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t)
+
+
+def job_throughput(units_per_rank: int, world: int, ms: float) -> float:
+    """Whole-job throughput (weak scaling): all ranks' units over the slowest time."""
+    return world * units_per_rank / (ms * 1e-3)
+
+
 def config_block(inp):
     return {"workload": f"{WORKLOAD}: rows={inp.rows} keys={inp.keys} H={inp.H} D={inp.D} "
                         f"topk={inp.topk} fp8 e4m3 q/k, per-key scale U(0.5,2), causal",
@@ -295,12 +313,8 @@ def main():
         "slab_topk": statistics.mean(e.elapsed(2, 3) for e in evs),
         "rescan": statistics.mean(e.elapsed(3, 4) for e in evs),
     }
-    ms = statistics.mean(step_ms)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t)
-    value = world * pairs / (ms * 1e-3)
+    ms = slowest_ms(statistics.mean(step_ms), world, dev)
+    value = job_throughput(pairs, world, ms)
 
     # --------------------------------------------------------------- roofline
     flops = 2.0 * inp.H * inp.D * pairs

@@ -71,19 +71,21 @@ typedef struct idx_stats {
     int fallback_rows;   /* rows re-selected by the exact full-row rescan */
     int max_count;       /* largest candidate count of any row */
     int split_rows;      /* rows the standalone top-k selected with a multi-block row split */
-    int tie_rescan_rows; /* rows whose threshold bin overflowed the tie buffer */
+    int tie_rescan_rows; /* standalone top-k rows that needed the multi-pass path (the
+                            one-pass candidate runs missed or overflowed) */
     int reserved;
 } idx_stats;
 
 /* Every field 0 selects the default.  Pass NULL for all defaults. */
 typedef struct idx_options {
-    float cap_factor;     /* slab cap = max(ceil(cap_factor*topk), 4096 clipped to 2*topk..);
-                             default 2.25 (page 1: about 2.25 x topk candidates) */
+    float cap_factor;     /* candidate slab cap = ceil(cap_factor * topk) when given;
+                             default max(ceil(2.25 * topk), 4096) (page 1: about
+                             2.25 x topk candidates).  Caps above 12288 are refused. */
     float target_factor;  /* expected candidates / topk that the sampled threshold aims
                              at; default sqrt(cap/topk).  Test knob to force short or
                              overflowing rows. */
     int sample_stride;    /* odd stride S of the threshold sample; 0 = automatic */
-    int row_split;        /* standalone top-k: -1 or 0 = automatic ... see below */
+    int row_split;        /* standalone top-k row split, see below */
     int* d_status;        /* optional device int receiving IDX_DEV_* bits */
     idx_stats* d_stats;   /* optional device counters */
     int relative_rows;    /* idx_topk_from_scores: row r's visible scores start at
@@ -100,7 +102,8 @@ typedef struct idx_options {
 
 /* row_split: 0 = automatic (page "[sglang] ROCm DSA Indexer Top-K 최적화",
  * row_split function: split a row over g blocks when it is at least 65536 long
- * and g = min(SMs / rows, 32) >= 4), -1 = never split, g >= 2 = force g blocks. */
+ * and g = min(SMs / rows, 32) >= 4), -1 = never split, g >= 2 = force g blocks.
+ * (This version selects every row with one CTA; the field is accepted.) */
 
 /* ------------------------------------------------------------------------
  * idx_score_topk - fused score + exact top-k, without writing [rows, keys]
@@ -116,7 +119,7 @@ typedef struct idx_options {
  * this library does not).
  *
  *   q, k, k_scale, w, ks, ke : inputs as in the conventions above
- *   rows, keys, H, D, topk   : sizes; keys may exceed 2^31
+ *   rows, keys, H, D, topk   : sizes; keys < 2^31 - 256 and rows * H < 2^31 - 256
  *   max_len                  : an upper bound on ke[r] - ks[r] (0 = keys); it
  *                              sizes the workspace
  *   dt                       : element type of q and k

@@ -1,0 +1,49 @@
+"""The multi-rank host path of bench.py on CPU: two gloo ranks, each with its own
+replica time; the job time is the slowest rank's and the throughput counts the
+work of every rank (weak scaling, no collective on the data path)."""
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank(rank, world, port, q):
+    import sys
+    import torch.distributed as dist
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    sys.path.insert(0, root)
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import bench
+    ms = bench.slowest_ms(10.0 + 5.0 * rank, world)  # rank 1 is slower
+    value = bench.job_throughput(1000, world, ms)
+    q.put((rank, ms, value))
+    dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_take_the_slowest_time():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert [r[1] for r in res] == [15.0, 15.0]
+    assert all(abs(r[2] - 2 * 1000 / 15e-3) < 1e-6 for r in res)
+
+
+def test_single_rank_is_unchanged():
+    import bench
+    assert bench.slowest_ms(7.5, 1) == 7.5
+    assert bench.job_throughput(10, 1, 2.0) == 5000.0
