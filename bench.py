@@ -428,7 +428,34 @@ def secondary(idx, dev, g, inp, out, ws, flush, pk, args):
     torch.cuda.empty_cache()
 
     res["standalone_topk"] = standalone_topk(idx, dev, flush, pk, args)
+    res["split_topk"] = split_topk(idx, dev, flush, pk, args)
     return res
+
+
+def split_topk(idx, dev, flush, pk, args):
+    """idx_topk_from_scores on 8 rows x 1M keys: low batch, long rows, the row split
+    path (g blocks per row)."""
+    import torch
+    import synth
+    si = synth.workload("split_topk")
+    sc = si.scores.to(dev)
+    ks, ke = si.ks.to(dev), si.ke.to(dev)
+    o = torch.empty(si.rows, si.topk, dtype=torch.int32, device=dev)
+    need = idx.idx_topk_workspace(si.rows, si.stride, si.topk)
+    ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+
+    def st():
+        idx.idx_topk_from_scores(sc, ks, ke, si.topk, out=o, ws=ws)
+
+    for _ in range(args.warmup):
+        st()
+    t = timed(st, flush, max(5, args.steps))
+    bytes_alg = 4 * int((si.ke - si.ks).sum()) + 4 * si.rows * si.topk
+    gbs = bytes_alg / (t * 1e-3) / 1e9
+    return {"workload": "split_topk: rows=8 keys=1048576 topk=2048 (row split)",
+            "rows_per_s": si.rows / (t * 1e-3), "ms": t,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / pk["hbm_gbs"]}}
 
 
 def standalone_topk(idx, dev, flush, pk, args):

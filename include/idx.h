@@ -102,8 +102,11 @@ typedef struct idx_options {
 
 /* row_split: 0 = automatic (page "[sglang] ROCm DSA Indexer Top-K 최적화",
  * row_split function: split a row over g blocks when it is at least 65536 long
- * and g = min(SMs / rows, 32) >= 4), -1 = never split, g >= 2 = force g blocks.
- * (This version selects every row with one CTA; the field is accepted.) */
+ * and g = min(SMs / rows, 32) >= 4), -1 or 1 = never split, g >= 2 = force
+ * g blocks (at most 64).  Grids with more than 65535 rows never split.  A
+ * split row is streamed once by g blocks, each over a contiguous slice; one
+ * more block per row selects from what they kept, or re-selects the whole row
+ * exactly when a slice kept more than it can hand over. */
 
 /* ------------------------------------------------------------------------
  * idx_score_topk - fused score + exact top-k, without writing [rows, keys]
@@ -148,6 +151,10 @@ idx_status idx_score_topk(const void* q, const void* k, const float* k_scale, co
  *   out_idx [rows, topk]: ascending j - ks[r], then -1.
  * The result is bit-exact: ties at equal fp32 values (+0 == -0) go to the
  * lower index.  NaN scores are a precondition violation.
+ * ws: idx_topk_workspace(...) bytes, 256-byte aligned (IDX_EWORKSPACE if
+ * smaller, IDX_EALIGN if misaligned); 0 bytes, and ws may be NULL, unless
+ * rows are split (row_split above): then 2 * 8192 * 4 + 4 bytes per block of
+ * a split row.  The call allocates nothing.
  * ------------------------------------------------------------------------ */
 size_t idx_topk_workspace(int rows, long long row_stride, int topk, const idx_options* opt);
 idx_status idx_topk_from_scores(const float* scores, long long row_stride, const int* ks,

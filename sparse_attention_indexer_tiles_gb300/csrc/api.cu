@@ -1,6 +1,7 @@
 // C ABI of libidx: argument validation, workspace carving and the launch
 // sequence of each entry point.  Everything that computes runs in the kernels
 // of topk.cu and score_*.cu; this file only decides what to launch.
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -76,6 +77,46 @@ bool arch_ok() {
 }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// SM count of the current device (cached); 148 when no device answers (a
+// host-only workspace query).
+int sm_count() {
+    static std::mutex mu;
+    static int cached[64];
+    static bool init = false;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return 148;
+    }
+    std::lock_guard<std::mutex> g(mu);
+    if (!init) {
+        for (int& c : cached) c = 0;
+        init = true;
+    }
+    if (cached[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+            cudaGetLastError();
+            n = 148;
+        }
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+
+// Blocks per row of the standalone top-k (page "[sglang] ROCm DSA Indexer
+// Top-K 최적화", row_split): none below 65536 columns; otherwise
+// g = min(SMs / rows, 32), and none when g < 4.  options->row_split: -1 or 1
+// never splits, g >= 2 forces g blocks (at most 64).
+int row_split_blocks(int rows, long long row_len_hint, const idx_options* opt) {
+    const int force = opt ? opt->row_split : 0;
+    if (force == -1 || force == 1 || rows > 65535) return 0;  // split grids keep rows in y
+    if (force >= 2) return force < 64 ? force : 64;
+    if (row_len_hint < 65536) return 0;
+    const int g = std::min(sm_count() / std::max(rows, 1), 32);
+    return g < 4 ? 0 : g;
+}
 
 struct FusedParams {
     int cap;    // nominal slab cap
@@ -352,18 +393,14 @@ idx_status idx_score_topk(const void* q, const void* k, const float* k_scale, co
 }
 
 size_t idx_topk_workspace(int rows, long long row_stride, int topk, const idx_options* opt) {
-    (void)rows;
-    (void)row_stride;
     (void)topk;
-    (void)opt;
-    return 0;
+    if (rows <= 0) return 0;
+    return split_workspace_bytes(rows, row_split_blocks(rows, row_stride, opt));
 }
 
 idx_status idx_topk_from_scores(const float* scores, long long row_stride, const int* ks,
                                 const int* ke, int rows, int topk, int* out_idx, void* ws,
                                 size_t ws_bytes, const idx_options* opt, void* stream) {
-    (void)ws;
-    (void)ws_bytes;
     if (rows < 0 || topk < 1 || row_stride < 0) return IDX_EINVAL;
     if (topk > kMaxTopk) return IDX_EUNSUPPORTED;
     if (rows == 0) return IDX_OK;
@@ -385,10 +422,22 @@ idx_status idx_topk_from_scores(const float* scores, long long row_stride, const
     t.out = out_idx;
     t.d_status = opt ? opt->d_status : nullptr;
     t.d_stats = opt ? opt->d_stats : nullptr;
+    const int g = row_split_blocks(rows, row_stride, opt);
+    if (g >= 2) {
+        const size_t need = split_workspace_bytes(rows, g);
+        if (!ws || ws_bytes < need) return IDX_EWORKSPACE;
+        if (!aligned(ws, 256)) return IDX_EALIGN;
+        const size_t slots = (size_t)rows * g;
+        uint8_t* base = static_cast<uint8_t*>(ws);
+        t.split = g;
+        t.split_keys = reinterpret_cast<uint32_t*>(base);
+        t.split_idx = t.split_keys + slots * kSplitCap;
+        t.split_cnt = reinterpret_cast<int*>(t.split_idx + slots * kSplitCap);
+    }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     record(opt, 0, s);
     const cudaError_t e = launch_topk_rows(t, s);
-    if (e == cudaSuccess) count_launches(1);
+    if (e == cudaSuccess) count_launches(g >= 2 ? 2 : 1);
     record(opt, 1, s);
     return cuda_status(e);
 }

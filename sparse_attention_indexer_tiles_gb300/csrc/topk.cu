@@ -377,6 +377,36 @@ IDX_DEVI void ordered_output_runs(const uint32_t* rkey, const uint32_t* ridx,
     }
 }
 
+// Visible length of row r and its first column; -1 marks a range that does
+// not fit the row.
+IDX_DEVI long long output_row(const TopkRowsArgs& a, int r, long long* col0) {
+    const long long ks = a.ks ? a.ks[r] : 0, ke = a.ke[r];
+    long long n = ke - ks;
+    *col0 = a.relative ? 0 : ks;
+    if (ks < 0 || n < 0 || *col0 + n > a.row_len || n > 0x7fffffffll) return ke > ks ? -1 : 0;
+    return n;
+}
+
+// Lower bound L of the threshold of the k largest of a row: the lower edge of
+// the 12-bit bin that holds about the 2 k * P / n-th largest of the row's
+// first P = 4096 values, so that about 2 k keys of the row reach it.
+template <int THREADS>
+IDX_DEVI uint32_t estimate_lower_bound(const RowView& v, uint32_t k, uint32_t* hist,
+                                       uint32_t* scratch) {
+    const long long n = v.n;
+    const long long P = n < kPrefix ? n : kPrefix;
+    const float* row = reinterpret_cast<const float*>(v.base) + v.off;
+    zero_shared<THREADS>(hist, kHistBins);
+    __syncthreads();
+    for (long long p = threadIdx.x; p < P; p += THREADS)
+        atomicAdd(&hist[fkey(__ldg(row + p)) >> 20], 1u);
+    __syncthreads();
+    double tg = ceil(2.0 * (double)k * (double)P / (double)n);
+    if (tg < 1.0) tg = 1.0;
+    if (tg > (double)P) tg = (double)P;
+    return pick_digit<THREADS>(hist, kHistBins, (uint32_t)tg, scratch).digit << 20;
+}
+
 template <int THREADS, int UNROLL>
 __global__ void __launch_bounds__(THREADS)
 topk_rows_kernel(TopkRowsArgs a) {
@@ -436,21 +466,8 @@ topk_rows_kernel(TopkRowsArgs a) {
     const RowView v = make_view(a.scores + (long long)r * a.row_stride + col0, n);
 
     // lower bound L of the threshold (0 takes every key when the runs hold the row)
-    uint32_t L = 0u;
     const long long per_warp = 4 * ((v.nvec + W - 1) / W);
-    if (per_warp > kRunCap) {
-        const long long P = n < kPrefix ? n : kPrefix;
-        const float* row = reinterpret_cast<const float*>(v.base) + v.off;
-        zero_shared<THREADS>(hist, kHistBins);
-        __syncthreads();
-        for (long long p = threadIdx.x; p < P; p += THREADS)
-            atomicAdd(&hist[fkey(__ldg(row + p)) >> 20], 1u);
-        __syncthreads();
-        double tg = ceil(2.0 * (double)k * (double)P / (double)n);
-        if (tg < 1.0) tg = 1.0;
-        if (tg > (double)P) tg = (double)P;
-        L = pick_digit<THREADS>(hist, kHistBins, (uint32_t)tg, scratch).digit << 20;
-    }
+    const uint32_t L = per_warp > kRunCap ? estimate_lower_bound<THREADS>(v, k, hist, scratch) : 0u;
     stream_collect<THREADS, UNROLL>(v, L, rkey, ridx, rcnt);
     __syncthreads();
     uint32_t total = 0;
@@ -483,6 +500,169 @@ topk_rows_kernel(TopkRowsArgs a) {
         plan->idx_cut = kAllIdx;
         plan->state = ST_MAIN;
     }
+}
+
+// ------------------------------------------------------- row split
+//
+// Page "[sglang] ROCm DSA Indexer Top-K 최적화", row_split / launch: at low
+// batch a long row is split over g blocks.  Here block (c, r) streams the c-th
+// contiguous slice of row r once, appends the values at or above the row's
+// lower bound L (the same estimate in every block of the row) to its warps'
+// runs and copies them, in index order, to the workspace; one block per row
+// then selects from the concatenation (already in index order), or takes the
+// exact multi-pass path over the row when a slice overflowed or L was too high.
+
+static_assert(kSplitCap == 16 * kRunCap, "a split block hands over its 16 warp runs");
+
+template <int THREADS, int UNROLL>
+__global__ void __launch_bounds__(THREADS)
+topk_split_collect_kernel(TopkRowsArgs a) {
+    using SM = StreamSmem<THREADS>;
+    constexpr int W = SM::W;
+    extern __shared__ __align__(16) uint32_t smem[];
+    uint32_t* hist = smem;
+    uint32_t* scratch = hist + kHistBins;
+    uint32_t* rcnt = scratch + 64;
+    uint32_t* wsum = rcnt + W;
+    uint32_t* rkey = wsum + 2 * W;
+    uint32_t* ridx = rkey + SM::RUN_WORDS;
+    (void)wsum;
+
+    const int c = blockIdx.x, r = blockIdx.y, g = gridDim.x;
+    long long col0;
+    const long long n = output_row(a, r, &col0);
+    if (n <= a.topk) return;  // the merge block writes such rows
+    const RowView v = make_view(a.scores + (long long)r * a.row_stride + col0, n);
+    const uint32_t L = estimate_lower_bound<THREADS>(v, (uint32_t)a.topk, hist, scratch);
+    // the slice as a view whose element indices stay row-relative
+    const long long per = (v.nvec + g - 1) / g;
+    const long long s0 = (long long)c * per;
+    const long long s1 = s0 + per < v.nvec ? s0 + per : v.nvec;
+    RowView sv;
+    sv.base = v.base + s0;
+    sv.off = v.off - (int)(4 * s0);
+    sv.n = v.n;
+    sv.nvec = s1 > s0 ? s1 - s0 : 0;
+    stream_collect<THREADS, UNROLL>(sv, L, rkey, ridx, rcnt);
+    __syncthreads();
+    // hand the runs over in warp (= index) order
+    const long long slot = (long long)r * g + c;
+    uint32_t* gk = a.split_keys + slot * kSplitCap;
+    uint32_t* gi = a.split_idx + slot * kSplitCap;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    uint32_t before = 0, total = 0;
+    bool over = false;
+    for (int j = 0; j < W; ++j) {
+        const uint32_t cj = rcnt[j];
+        over = over || cj > (uint32_t)kRunCap;
+        if (j < w) before += cj;
+        total += cj;
+    }
+    if (!over) {
+        for (uint32_t i = lane; i < rcnt[w]; i += 32) {
+            gk[before + i] = rkey[w * kRunCap + i];
+            gi[before + i] = ridx[w * kRunCap + i];
+        }
+    }
+    if (threadIdx.x == 0) a.split_cnt[slot] = over ? -1 : (int)total;
+}
+
+// Ordered compaction of cnt keys held in index order in shared memory.
+template <int THREADS>
+IDX_DEVI void ordered_output_smem(const uint32_t* keys, const uint32_t* idxs, uint32_t cnt,
+                                  Threshold th, uint32_t k, int* out, uint32_t* scratch) {
+    uint32_t a_run = 0, e_run = 0;
+    for (uint32_t base = 0; base < cnt; base += THREADS * 4) {
+        uint32_t ab = 0, tb = 0;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const uint32_t e = base + threadIdx.x * 4 + c;
+            if (e < cnt) {
+                ab |= (keys[e] > th.key ? 1u : 0u) << c;
+                tb |= (keys[e] == th.key ? 1u : 0u) << c;
+            }
+        }
+        const uint32_t mine = (__popc(ab) << 16) | __popc(tb);
+        uint32_t tot;
+        const uint32_t incl = block_incl_scan<THREADS>(mine, scratch, &tot);
+        const uint32_t excl = incl - mine;
+        uint32_t a_b = a_run + (excl >> 16), e_b = e_run + (excl & 0xFFFFu);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const uint32_t e = base + threadIdx.x * 4 + c;
+            if ((ab >> c) & 1u) {
+                const uint32_t pos = a_b + min(e_b, th.need);
+                if (pos < k) out[pos] = (int)idxs[e];
+                ++a_b;
+            } else if ((tb >> c) & 1u) {
+                if (e_b < th.need && a_b + e_b < k) out[a_b + e_b] = (int)idxs[e];
+                ++e_b;
+            }
+        }
+        a_run += tot >> 16;
+        e_run += tot & 0xFFFFu;
+    }
+}
+
+constexpr int kMergeCap = 16384;  // candidates of a split row selected in shared memory
+constexpr size_t kMergeSmem = (kHistBins + 64 + 2 * (size_t)kMergeCap) * sizeof(uint32_t);
+
+template <int THREADS>
+__global__ void __launch_bounds__(THREADS)
+topk_split_merge_kernel(TopkRowsArgs a, int g) {
+    extern __shared__ __align__(16) uint32_t smem[];
+    uint32_t* hist = smem;
+    uint32_t* scratch = hist + kHistBins;
+    uint32_t* keys = scratch + 64;
+    uint32_t* idxs = keys + kMergeCap;
+    const int r = blockIdx.x;
+    long long col0;
+    long long n = output_row(a, r, &col0);
+    int* out = a.out + (long long)r * a.topk;
+    if (n < 0) {
+        if (threadIdx.x == 0) raise_status(a.d_status, IDX_DEV_RANGE);
+        n = 0;
+    }
+    if (n <= a.topk) {
+        for (int i = threadIdx.x; i < a.topk; i += THREADS) out[i] = i < n ? i : -1;
+        return;
+    }
+    const uint32_t k = (uint32_t)a.topk;
+    if (threadIdx.x == 0) {
+        uint32_t total = 0, bad = 0;
+        for (int c = 0; c < g; ++c) {
+            const int cc = a.split_cnt[(long long)r * g + c];
+            bad |= cc < 0;
+            total += cc < 0 ? 0u : (uint32_t)cc;
+        }
+        scratch[48] = total;
+        scratch[49] = bad || total < k || total > (uint32_t)kMergeCap;
+        if (a.d_stats) atomicAdd(&a.d_stats->split_rows, 1);
+    }
+    __syncthreads();
+    const uint32_t total = scratch[48];
+    const RowView v = make_view(a.scores + (long long)r * a.row_stride + col0, n);
+    if (scratch[49]) {
+        // a slice overflowed or L was too high: exact multi-pass path
+        int rescans = 0;
+        const Threshold th = find_threshold<THREADS, 4>(v, k, hist, keys, idxs, scratch, &rescans);
+        if (threadIdx.x == 0 && a.d_stats) atomicAdd(&a.d_stats->tie_rescan_rows, 1);
+        ordered_output<THREADS>(v, th, k, out, scratch);
+        return;
+    }
+    uint32_t off = 0;
+    for (int c = 0; c < g; ++c) {
+        const long long slot = (long long)r * g + c;
+        const uint32_t cc = (uint32_t)a.split_cnt[slot];
+        for (uint32_t i = threadIdx.x; i < cc; i += THREADS) {
+            keys[off + i] = a.split_keys[slot * kSplitCap + i];
+            idxs[off + i] = a.split_idx[slot * kSplitCap + i];
+        }
+        off += cc;
+    }
+    __syncthreads();
+    const Threshold th = refine_in_smem<THREADS>(keys, total, 0, 0u, k, hist, scratch);
+    ordered_output_smem<THREADS>(keys, idxs, total, th, k, out, scratch);
 }
 
 // ---------------------------------------------------------------- slab
@@ -707,13 +887,35 @@ cand_topk_kernel(CandArgs a) {
 cudaError_t launch_topk_rows(const TopkRowsArgs& a, cudaStream_t s) {
     constexpr int T = 512, U = 8;
     constexpr size_t SMEM = StreamSmem<T>::BYTES;
+    if (a.rows == 0) return cudaSuccess;
+    if (a.mode == TOPK_OUTPUT && a.split > 1) {
+        auto coll = topk_split_collect_kernel<T, U>;
+        auto merge = topk_split_merge_kernel<T>;
+        static cudaError_t attr = [&] {
+            cudaError_t e = cudaFuncSetAttribute(coll, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)SMEM);
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(merge, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kMergeSmem);
+            return e;
+        }();
+        if (attr != cudaSuccess) return attr;
+        coll<<<dim3((unsigned)a.split, (unsigned)a.rows), T, SMEM, s>>>(a);
+        merge<<<a.rows, T, kMergeSmem, s>>>(a, a.split);
+        return cudaGetLastError();
+    }
     auto kern = topk_rows_kernel<T, U>;
     static cudaError_t attr = cudaFuncSetAttribute(
         kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM);
     if (attr != cudaSuccess) return attr;
-    if (a.rows == 0) return cudaSuccess;
     kern<<<a.rows, T, SMEM, s>>>(a);
     return cudaGetLastError();
+}
+
+size_t split_workspace_bytes(int rows, int g) {
+    if (g < 2) return 0;
+    const size_t slots = (size_t)rows * g;
+    return slots * (size_t)kSplitCap * 2 * sizeof(uint32_t) + slots * sizeof(int) + 256;
 }
 
 size_t cand_smem_bytes(int cap_q) {

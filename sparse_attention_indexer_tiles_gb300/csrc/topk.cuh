@@ -12,6 +12,9 @@ namespace idx {
 
 enum : int { TOPK_OUTPUT = 0, TOPK_THRESHOLD = 1 };
 
+// Candidates one block of a split row can hand over (16 warps x 512).
+constexpr int kSplitCap = 8192;
+
 struct TopkRowsArgs {
     const float* scores;  // [rows, row_stride]
     long long row_stride;
@@ -33,6 +36,11 @@ struct TopkRowsArgs {
     long long nsamp;      // floor(keys / S)
     int rows_per_block;   // rows sharing one sample phase
     uint32_t phase_seed;
+    // TOPK_OUTPUT row split: g blocks per row (0/1 = none) and their workspace
+    int split;
+    uint32_t* split_keys;  // [rows * g, kSplitCap]
+    uint32_t* split_idx;   // [rows * g, kSplitCap]
+    int* split_cnt;        // [rows * g] candidates handed over, -1 = a run overflowed
     int* d_status;
     idx_stats* d_stats;
 };
@@ -58,5 +66,6 @@ struct CandArgs {
 cudaError_t launch_topk_rows(const TopkRowsArgs& a, cudaStream_t s);
 cudaError_t launch_cand_topk(const CandArgs& a, cudaStream_t s);
 size_t cand_smem_bytes(int cap_q);
+size_t split_workspace_bytes(int rows, int g);
 
 }  // namespace idx

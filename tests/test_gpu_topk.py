@@ -122,3 +122,44 @@ def test_standalone_workload_full(idx):
     got = gpu_topk(idx, si.scores, si.ks, si.ke, 2048)
     ref = oracle.topk_from_scores(si.scores, si.ks, si.ke, 2048)
     assert np.array_equal(got, ref)
+
+
+# ------------------------------------------------------------ row split
+
+def test_row_split_workload(idx):
+    """8 rows x 1M keys: the automatic rule splits every row over g blocks
+    (g = min(SMs / rows, 32)); bit-exact on every row."""
+    si = synth.workload("split_topk")
+    stats = idx.Stats(torch.device(DEV))
+    got = gpu_topk(idx, si.scores, si.ks, si.ke, 2048, stats=stats)
+    ref = oracle.topk_from_scores(si.scores, si.ks, si.ke, 2048)
+    assert np.array_equal(got, ref)
+    st = stats.read()
+    assert st["split_rows"] == 8 and st["status"] == 0
+
+
+@pytest.mark.parametrize("g", [2, 5, 9])
+def test_forced_row_split(idx, g):
+    si = synth.score_inputs(12, 70000, 700, seed=26 + g, short_frac=0.2)
+    stats = idx.Stats(torch.device(DEV))
+    got = gpu_topk(idx, si.scores, si.ks, si.ke, 700, options={"row_split": g}, stats=stats)
+    ref = oracle.topk_from_scores(si.scores, si.ks, si.ke, 700)
+    assert np.array_equal(got, ref)
+    assert stats.read()["split_rows"] > 0
+
+
+def test_row_split_ties_fall_back(idx):
+    """All-equal and two-valued rows overflow the split candidate runs; the
+    merge block re-selects them exactly."""
+    n, topk = 90000, 1000
+    S = torch.full((3, n), 0.5)
+    S[1, ::7] = 2.0
+    S[2] = torch.arange(n, dtype=torch.float32) % 3
+    ks = torch.zeros(3, dtype=torch.int32)
+    ke = torch.full((3,), n, dtype=torch.int32)
+    stats = idx.Stats(torch.device(DEV))
+    got = gpu_topk(idx, S, ks, ke, topk, options={"row_split": 6}, stats=stats)
+    ref = oracle.topk_from_scores(S, ks, ke, topk)
+    assert np.array_equal(got, ref)
+    st = stats.read()
+    assert st["split_rows"] == 3 and st["tie_rescan_rows"] >= 2
