@@ -29,6 +29,14 @@ IDX_DEVI uint32_t fkey(float f) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// The float whose order key is L: for every non-NaN f, f >= it exactly when
+// fkey(f) >= L (fkey is monotone and folds -0 onto +0).  Keys below the one of
+// -inf admit every non-NaN value.
+IDX_DEVI float key_floor_float(uint32_t L) {
+    if (L <= 0x007fffffu) return -INFINITY;
+    return __uint_as_float((L & 0x80000000u) ? (L & 0x7fffffffu) : ~L);
+}
+
 // --------------------------------------------------------------- smem/ptx
 
 IDX_DEVI uint32_t smem_u32(const void* p) {

@@ -70,7 +70,7 @@ enum : int {
     MW_THR,         // emit / histogram threshold key
     MW_CUT,         // emit: largest index taken among keys equal to thr
     MW_PREFIX,      // histogram: bits above the digit
-    MW_PAD
+    MW_THRF,        // emit: the float whose key is thr (keys compare as floats)
 };
 
 // sum_h w[h] * (acc[h] + |acc[h]|) = 2 sum_h w[h] ReLU(acc[h]) for the TMEM row
@@ -201,7 +201,11 @@ score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         m[MW_THR] = (int)thr;
         m[MW_CUT] = cut;
         m[MW_PREFIX] = (int)prefix;
-        m[MW_PAD] = 0;
+        // the emit rule key > thr || (key == thr && idx <= cut) in floats: keys
+        // below the one of -inf admit every score, whatever the index
+        if (thr <= 0x007fffffu) cut = kAllIdx;
+        m[MW_CUT] = cut;
+        m[MW_THRF] = __float_as_int(key_floor_float(thr));
     }
     for (int i = tid; i < C::R * H; i += C::THREADS) {
         const long long r = r0 + i / H;
@@ -344,35 +348,35 @@ score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         const int run = q * 2 + team;        // candidate run of this warp
         const uint32_t lt = (1u << lane) - 1u;
         int cnt[C::RG];
-        // row metadata: in registers for up to 4 rows per warp, else read from
-        // shared memory each tile (many rows of few heads)
-        constexpr bool HOIST = C::RG <= 4;
-        constexpr int NH = HOIST ? C::RG : 1;
-        int hv[NH][6];
+        // row metadata from shared memory; the emit words of up to 2 rows per
+        // warp are held in registers across the tile loop
         const int* mrow = meta + grp * C::RG * C::META_WORDS;
+        auto row_word = [&](int j, int word) -> int { return mrow[j * C::META_WORDS + word]; };
+        constexpr bool HOIST = C::RG <= 2;
+        constexpr int NH = HOIST ? C::RG : 1;
+        int e_lo[NH], e_len[NH], e_cut[NH];
+        float e_thr[NH];
 #pragma unroll
         for (int j = 0; j < C::RG; ++j) {
             cnt[j] = 0;
             if constexpr (HOIST) {
-                const int* m = mrow + j * C::META_WORDS;
-                hv[j][0] = m[MW_LO];
-                hv[j][1] = m[MW_HI];
-                hv[j][2] = m[MW_KS];
-                hv[j][3] = m[MW_THR];
-                hv[j][4] = m[MW_CUT];
-                hv[j][5] = m[MW_PREFIX];
+                e_lo[j] = row_word(j, MW_LO);
+                e_len[j] = row_word(j, MW_HI) - e_lo[j];
+                e_cut[j] = row_word(j, MW_CUT);
+                e_thr[j] = __int_as_float(row_word(j, MW_THRF));
             }
         }
-        auto row_word = [&](int j, int slot, int word) -> int {
-            if constexpr (HOIST) return hv[HOIST ? j : 0][slot];
-            else return mrow[j * C::META_WORDS + word];
-        };
-#define RLO(j) row_word(j, 0, MW_LO)
-#define RHI(j) row_word(j, 1, MW_HI)
-#define RKS(j) row_word(j, 2, MW_KS)
-#define RTHR(j) ((uint32_t)row_word(j, 3, MW_THR))
-#define RCUT(j) row_word(j, 4, MW_CUT)
-#define RPRE(j) ((uint32_t)row_word(j, 5, MW_PREFIX))
+        // this warp's runs of its rows: row j's run at ps/pi + j * rstride
+        const long long rb = (long long)(r0 + grp * C::RG) * kRuns + run;
+        float* const ps = a.slab_s ? a.slab_s + rb * a.cap_q : nullptr;
+        int* const pi = a.slab_i ? a.slab_i + rb * a.cap_q : nullptr;
+        const int rstride = kRuns * a.cap_q;
+#define RLO(j) row_word(j, MW_LO)
+#define RHI(j) row_word(j, MW_HI)
+#define RKS(j) row_word(j, MW_KS)
+#define RTHR(j) ((uint32_t)row_word(j, MW_THR))
+#define RCUT(j) row_word(j, MW_CUT)
+#define RPRE(j) ((uint32_t)row_word(j, MW_PREFIX))
         // per-key scale of the team's next tile, loaded one tile ahead
         auto scale_of = [&](int t) -> float {
             const long long ki = (long long)(t0 + t) * C::M + q * 32 + lane;
@@ -407,8 +411,9 @@ score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             if (mode == SM_MATERIALISE || mode == SM_SAMPLE) {
 #pragma unroll
                 for (int j = 0; j < C::RG; ++j) {
-                    const int off = kidx - RLO(j);
-                    if ((uint32_t)off < (uint32_t)(RHI(j) - RLO(j))) {
+                    const int off = kidx - (HOIST ? e_lo[HOIST ? j : 0] : RLO(j));
+                    const int len = HOIST ? e_len[HOIST ? j : 0] : RHI(j) - RLO(j);
+                    if ((uint32_t)off < (uint32_t)len) {
                         const long long r = r0 + grp * C::RG + j;
                         if (mode == SM_MATERIALISE)
                             a.out[r * a.out_stride + off] = sc[j];
@@ -444,18 +449,20 @@ score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 // rule to this warp's run, in key order; no cross-warp traffic
 #pragma unroll
                 for (int j = 0; j < C::RG; ++j) {
-                    const int off = kidx - RLO(j);
-                    const uint32_t kb = fkey(sc[j]);
-                    const bool hit = (uint32_t)off < (uint32_t)(RHI(j) - RLO(j)) &&
-                                     (kb > RTHR(j) || (kb == RTHR(j) && off <= RCUT(j)));
+                    const int lo = HOIST ? e_lo[HOIST ? j : 0] : RLO(j);
+                    const int len = HOIST ? e_len[HOIST ? j : 0] : RHI(j) - RLO(j);
+                    const float thr = HOIST ? e_thr[HOIST ? j : 0]
+                                            : __int_as_float(row_word(j, MW_THRF));
+                    const int cut = HOIST ? e_cut[HOIST ? j : 0] : RCUT(j);
+                    const int off = kidx - lo;
+                    const bool hit = (uint32_t)off < (uint32_t)len &&
+                                     (sc[j] > thr || (sc[j] == thr && off <= cut));
                     const uint32_t A = __ballot_sync(0xffffffffu, hit);
                     if (A) {
                         const int pos = cnt[j] + __popc(A & lt);
                         if (hit && pos < a.cap_q) {
-                            const long long slot =
-                                ((long long)(r0 + grp * C::RG + j) * kRuns + run) * a.cap_q + pos;
-                            a.slab_s[slot] = sc[j];
-                            a.slab_i[slot] = off;
+                            ps[j * rstride + pos] = sc[j];
+                            pi[j * rstride + pos] = off;
                         }
                         cnt[j] += __popc(A);
                     }

@@ -230,14 +230,6 @@ struct StreamSmem {
         (kHistBins + 64 + 3 * W + 2 * (size_t)RUN_WORDS) * sizeof(uint32_t);
 };
 
-// The float whose order key is L: for every non-NaN f, f >= it exactly when
-// fkey(f) >= L (fkey is monotone and folds -0 onto +0).  Keys below the one of
-// -inf admit every non-NaN value.
-IDX_DEVI float key_floor_float(uint32_t L) {
-    if (L <= 0x007fffffu) return -INFINITY;
-    return __uint_as_float((L & 0x80000000u) ? (L & 0x7fffffffu) : ~L);
-}
-
 // Append every key >= L of warp w's slice to its run; returns through rcnt[w].
 // The hot loop compares floats; order keys are formed for the few hits only,
 // and element bounds are checked only in the row's first and last 16 bytes.
