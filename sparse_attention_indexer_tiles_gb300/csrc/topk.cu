@@ -414,8 +414,7 @@ topk_rows_kernel(TopkRowsArgs a) {
 
     const int r = blockIdx.x;
     long long n, col0;
-    uint32_t k;
-    if (a.mode == TOPK_OUTPUT) {
+    {
         const long long ks = a.ks ? a.ks[r] : 0, ke = a.ke[r];
         n = ke - ks;
         col0 = a.relative ? 0 : ks;
@@ -428,32 +427,8 @@ topk_rows_kernel(TopkRowsArgs a) {
             for (int i = threadIdx.x; i < a.topk; i += THREADS) out[i] = i < n ? i : -1;
             return;
         }
-        k = static_cast<uint32_t>(a.topk);
-    } else {
-        // Threshold of the strided sample of row r: the t-th largest of its m
-        // sample scores, t = ceil(m * target * topk / len) with len the row's
-        // visible length, so that about target * topk keys reach it.
-        RowPlan* plan = a.plan + r;
-        const long long vks = a.vis_ks[r], vke = a.vis_ke[r];
-        const long long len = vke - vks;
-        const long long phase = hash32((uint32_t)(r / a.rows_per_block) ^ a.phase_seed) % a.S;
-        const SampleSpan sp = sample_span(vks, vke, phase, a.S, a.nsamp);
-        n = sp.b - sp.a;
-        col0 = 0;
-        if (len <= a.cap || n <= 0 || n > a.row_len) {
-            if (threadIdx.x == 0) {
-                plan->thr = 0u;  // every visible key becomes a candidate
-                plan->idx_cut = kAllIdx;
-                plan->state = ST_MAIN;
-                if (a.d_stats && len > 0 && len <= a.cap) atomicAdd(&a.d_stats->emit_all_rows, 1);
-            }
-            return;
-        }
-        double t = ceil((double)n * (double)a.target * (double)a.topk / (double)len);
-        if (t < 1.0) t = 1.0;
-        if (t > (double)n) t = (double)n;
-        k = static_cast<uint32_t>(t);
     }
+    const uint32_t k = static_cast<uint32_t>(a.topk);
 
     const RowView v = make_view(a.scores + (long long)r * a.row_stride + col0, n);
 
@@ -480,15 +455,104 @@ topk_rows_kernel(TopkRowsArgs a) {
         if (threadIdx.x == 0 && a.d_stats) atomicAdd(&a.d_stats->tie_rescan_rows, 1);
     }
 
-    if (a.mode == TOPK_OUTPUT) {
-        int* out = a.out + (long long)r * a.topk;
-        if (runs_ok)
-            ordered_output_runs<THREADS>(rkey, ridx, rcnt, wsum, th, k, out);
-        else
-            ordered_output<THREADS>(v, th, k, out, scratch);
-    } else if (threadIdx.x == 0) {
-        RowPlan* plan = a.plan + r;
-        plan->thr = th.key;
+    int* out = a.out + (long long)r * a.topk;
+    if (runs_ok)
+        ordered_output_runs<THREADS>(rkey, ridx, rcnt, wsum, th, k, out);
+    else
+        ordered_output<THREADS>(v, th, k, out, scratch);
+}
+
+// ------------------------------------------------------ sample threshold
+//
+// Page 1, "Sampled Threshold": T_r is the t-th largest of the m scores of row
+// r's strided sample, t = ceil(m * target * topk / len) with len the row's
+// visible length, so that about target * topk keys of the row reach it.  One
+// warp per row finds the exact t-th largest order key with four 8-bit radix
+// passes over the sample (a warp-private 256-bin histogram each), reading the
+// sample from L2; no block-wide synchronisation.
+template <int WARPS>
+__global__ void __launch_bounds__(WARPS * 32)
+sample_threshold_kernel(TopkRowsArgs a) {
+    __shared__ uint32_t hist_all[WARPS][256];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int r = blockIdx.x * WARPS + w;
+    if (r >= a.rows) return;  // whole warps only: nothing below syncs the block
+    uint32_t* hist = hist_all[w];
+    RowPlan* plan = a.plan + r;
+    const long long vks = a.vis_ks[r], vke = a.vis_ke[r];
+    const long long len = vke - vks;
+    const long long phase = hash32((uint32_t)(r / a.rows_per_block) ^ a.phase_seed) % a.S;
+    const SampleSpan sp = sample_span(vks, vke, phase, a.S, a.nsamp);
+    const long long n = sp.b - sp.a;
+    if (len <= a.cap || n <= 0 || n > a.row_len) {
+        if (lane == 0) {
+            plan->thr = 0u;  // every visible key becomes a candidate
+            plan->idx_cut = kAllIdx;
+            plan->state = ST_MAIN;
+            if (a.d_stats && len > 0 && len <= a.cap) atomicAdd(&a.d_stats->emit_all_rows, 1);
+        }
+        return;
+    }
+    double t = ceil((double)n * (double)a.target * (double)a.topk / (double)len);
+    if (t < 1.0) t = 1.0;
+    if (t > (double)n) t = (double)n;
+    const float* row = a.scores + (long long)r * a.row_stride;
+    uint32_t prefix = 0u, need = (uint32_t)t;
+    bool ok = true;
+    for (int lev = 0; lev < 4; ++lev) {
+        const int shift = 24 - 8 * lev;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) hist[lane * 8 + j] = 0u;
+        __syncwarp();
+        for (long long e = lane; e < n; e += 32) {
+            const uint32_t key = fkey(__ldg(row + e));
+            if (lev == 0 || (key >> (shift + 8)) == prefix)
+                atomicAdd(&hist[(key >> shift) & 255u], 1u);
+        }
+        __syncwarp();
+        // lane l holds bins 255 - 8l ... 248 - 8l (from the largest keys down)
+        uint32_t c[8], local = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            c[j] = hist[255 - 8 * lane - j];
+            local += c[j];
+        }
+        uint32_t incl = local;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const uint32_t o = __shfl_up_sync(0xffffffffu, incl, d);
+            if (lane >= d) incl += o;
+        }
+        const uint32_t excl = incl - local;
+        const uint32_t owner = __ballot_sync(0xffffffffu, excl < need && need <= incl);
+        if (owner == 0u) {  // cannot happen: need never exceeds the keys left
+            ok = false;
+            break;
+        }
+        const int src = __ffs(owner) - 1;
+        uint32_t digit = 0u, above = 0u;
+        if (lane == src) {
+            uint32_t cum = excl;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                if (cum + c[j] >= need) {
+                    digit = 255u - 8u * (uint32_t)lane - (uint32_t)j;
+                    above = cum;
+                    break;
+                }
+                cum += c[j];
+            }
+        }
+        digit = __shfl_sync(0xffffffffu, digit, src);
+        above = __shfl_sync(0xffffffffu, above, src);
+        need -= above;
+        prefix = (prefix << 8) | digit;
+        __syncwarp();
+    }
+    if (lane == 0) {
+        // a failed pick leaves thr = 0: every key a candidate, the slab
+        // overflows and the exact rescan takes the row
+        plan->thr = ok ? prefix : 0u;
         plan->idx_cut = kAllIdx;
         plan->state = ST_MAIN;
     }
@@ -880,7 +944,12 @@ cudaError_t launch_topk_rows(const TopkRowsArgs& a, cudaStream_t s) {
     constexpr int T = 512, U = 8;
     constexpr size_t SMEM = StreamSmem<T>::BYTES;
     if (a.rows == 0) return cudaSuccess;
-    if (a.mode == TOPK_OUTPUT && a.split > 1) {
+    if (a.mode == TOPK_THRESHOLD) {
+        constexpr int WARPS = 8;
+        sample_threshold_kernel<WARPS><<<(a.rows + WARPS - 1) / WARPS, WARPS * 32, 0, s>>>(a);
+        return cudaGetLastError();
+    }
+    if (a.split > 1) {
         auto coll = topk_split_collect_kernel<T, U>;
         auto merge = topk_split_merge_kernel<T>;
         static cudaError_t attr = [&] {
