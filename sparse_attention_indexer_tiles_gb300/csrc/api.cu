@@ -369,6 +369,7 @@ idx_status idx_score_topk(const void* q, const void* k, const float* k_scale, co
     c.d_status = d_status;
     c.d_stats = d_stats;
     c.fallback = 0;
+    c.grid_limit = 2 * sm_count();
     if ((e = launch_cand_topk(c, s)) != cudaSuccess) return cuda_status(e);
     count_launches(1);
     record(opt, 3, s);

@@ -723,219 +723,237 @@ topk_split_merge_kernel(TopkRowsArgs a, int g) {
 
 // ---------------------------------------------------------------- slab
 //
-// The main scoring pass leaves each row's candidates in four runs (one per
-// TMEM lane quarter, i.e. per 32-key column of a 128-key tile), each in
-// ascending key order; the rescan re-emission leaves a single ordered run.
-// The kernel loads the runs into shared memory, finds the exact threshold key
-// T by radix refinement, keeps the lowest indices among the keys equal to T,
-// compacts the selected entries run by run and merges the runs into ascending
-// order by ranking every entry against the other runs (binary search).
+// Page 1, "Sampled Threshold": the small exact top-k over the ~2.25 x topk
+// candidates of a row.  The scoring pass leaves each row's candidates in
+// eight runs, each in ascending key order; the rescan re-emission leaves a
+// single ordered run.  One CTA of 256 threads per row loads the runs into
+// shared memory as (order key, index), finds the exact threshold key T with
+// four 8-bit radix passes (per-warp histograms), keeps the lowest indices
+// among the keys equal to T, and writes the selected indices in ascending order through a bitmap of
+// the index range (65536 indices per pass): each thread owns eight bitmap
+// words, and a block scan of their popcounts gives every set bit its output
+// position.
 
-IDX_DEVI uint32_t lower_bound_u32(const uint32_t* a, uint32_t n, uint32_t v) {
-    uint32_t lo = 0, hi = n;
-    while (lo < hi) {
-        const uint32_t mid = (lo + hi) >> 1;
-        if (a[mid] < v) lo = mid + 1;
-        else hi = mid;
+constexpr int kCandThreads = 256;
+constexpr int kCandWarps = kCandThreads / 32;
+constexpr int kBitmapWords = kCandWarps * 256;  // the histograms' words, 65536 bits
+
+// Exact need-th largest value among the elements e < cnt with valid(e), of
+// the 32-bit values val(e), by four 8-bit digits from the top.  Returns the
+// value and, through *need_at, how many elements equal to it are taken.
+template <class Valid, class Val>
+IDX_DEVI uint32_t cand_select(uint32_t cnt, uint32_t need, Valid valid, Val val, uint32_t* hist,
+                              uint32_t* scratch, uint32_t* need_at) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    uint32_t* hw = hist + w * 256;
+    uint32_t prefix = 0u;
+    for (int lev = 0; lev < 4; ++lev) {
+        const int shift = 24 - 8 * lev;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) hw[lane * 8 + j] = 0u;
+        __syncwarp();
+        for (uint32_t base = 0; base < cnt; base += 4 * kCandThreads) {
+            uint32_t v[4];
+            bool in[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const uint32_t e = base + u * kCandThreads + threadIdx.x;
+                in[u] = e < cnt && valid(e);
+                v[u] = in[u] ? val(e) : 0u;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (in[u] && (lev == 0 || (v[u] >> (shift + 8)) == prefix))
+                    atomicAdd(&hw[(v[u] >> shift) & 255u], 1u);
+        }
+        __syncthreads();
+        // thread t owns digit 255 - t: a scan from the top digit down
+        uint32_t c = 0;
+#pragma unroll
+        for (int ww = 0; ww < kCandWarps; ++ww) c += hist[ww * 256 + 255 - threadIdx.x];
+        const uint32_t incl = block_incl_scan<kCandThreads>(c, scratch, nullptr);
+        const uint32_t excl = incl - c;
+        if (excl < need && need <= incl) {
+            scratch[40] = 255u - threadIdx.x;
+            scratch[41] = excl;
+        }
+        __syncthreads();
+        need -= scratch[41];
+        prefix = (prefix << 8) | scratch[40];
+        __syncthreads();
     }
-    return lo;
+    *need_at = need;
+    return prefix;
 }
 
-template <int THREADS>
-__global__ void __launch_bounds__(THREADS)
+__global__ void __launch_bounds__(kCandThreads)
 cand_topk_kernel(CandArgs a) {
+    constexpr int THREADS = kCandThreads;
     extern __shared__ __align__(16) uint32_t smem[];
     const int CR = kRuns * a.cap_q;
-    uint32_t* hist = smem;
-    uint32_t* scratch = hist + kHistBins;   // [0,35) scans; row state from 48 on
+    uint32_t* hist = smem;                     // [kCandWarps][256], later the bitmap
+    uint32_t* scratch = hist + kBitmapWords;   // [0,35) scans; row state from 48 on
     uint32_t* keys = scratch + kCandScratch;
     uint32_t* idxs = keys + CR;
-    uint32_t* tmp = idxs + CR;              // ~index of the ties, then the selected list
-    uint32_t* run_off = scratch + 50;       // [kRuns + 1] run starts in keys[]
-    uint32_t* run_sel = scratch + 64;       // [kRuns + 1] run starts in the selected list
+    uint32_t* run_off = scratch + 50;          // [kRuns + 1] run starts in keys[]
 
     if (a.fallback && *(volatile int*)(a.fb_cnt + 6) == 0) return;  // no row was re-emitted
-    const int r = blockIdx.x;
-    RowPlan* plan = a.plan + r;
-    const long long n = (long long)a.ke[r] - (long long)a.ks[r];
-    int* out = a.out + (long long)r * a.topk;
-    if (threadIdx.x == 0) {
-        scratch[48] = (uint32_t)plan->state;
-        uint32_t off = 0, total = 0, trunc = 0;
-        for (int q = 0; q < kRuns; ++q) {
-            const uint32_t c = (uint32_t)a.run_cnt[(long long)r * kRuns + q];
-            trunc |= c > (uint32_t)a.cap_q;
-            total += c;
-            run_off[q] = off;
-            off += c < (uint32_t)a.cap_q ? c : (uint32_t)a.cap_q;
+    for (int r = blockIdx.x; r < a.rows; r += gridDim.x) {
+        __syncthreads();  // the previous row's shared state is no longer read
+        RowPlan* plan = a.plan + r;
+        const long long n = (long long)a.ke[r] - (long long)a.ks[r];
+        int* out = a.out + (long long)r * a.topk;
+        if (threadIdx.x == 0) {
+            scratch[48] = (uint32_t)plan->state;
+            uint32_t off = 0, total = 0, trunc = 0;
+            for (int q = 0; q < kRuns; ++q) {
+                const uint32_t c = (uint32_t)a.run_cnt[(long long)r * kRuns + q];
+                trunc |= c > (uint32_t)a.cap_q;
+                total += c;
+                run_off[q] = off;
+                off += c < (uint32_t)a.cap_q ? c : (uint32_t)a.cap_q;
+            }
+            run_off[kRuns] = off;
+            scratch[49] = trunc;
+            scratch[60] = total;
         }
-        run_off[kRuns] = off;
-        scratch[49] = trunc;
-        scratch[60] = total;
-    }
-    __syncthreads();
-    const int state = (int)scratch[48];
-    if (a.fallback) {
-        if (state != ST_EMIT) return;
-    } else if (n <= a.topk) {
-        for (int i = threadIdx.x; i < a.topk; i += THREADS) out[i] = i < n ? i : -1;
-        if (threadIdx.x == 0) plan->state = ST_DONE;
-        return;
-    }
-    const uint32_t total = scratch[60];
-    const bool trunc = scratch[49] != 0;
-    if (threadIdx.x == 0 && a.d_stats && !a.fallback) atomicMax(&a.d_stats->max_count, (int)total);
-    if (trunc || total < (uint32_t)a.topk) {
-        if (!a.fallback && !a.fb_hist) {
-            // no rescan storage: the row was longer than the max_len the
-            // workspace was sized for
-            for (int i = threadIdx.x; i < a.topk; i += THREADS) out[i] = -1;
-            if (threadIdx.x == 0) {
-                raise_status(a.d_status, IDX_DEV_RANGE);
+        __syncthreads();
+        const int state = (int)scratch[48];
+        if (a.fallback) {
+            if (state != ST_EMIT) continue;
+        } else if (n <= a.topk) {
+            for (int i = threadIdx.x; i < a.topk; i += THREADS) out[i] = i < n ? i : -1;
+            if (threadIdx.x == 0) plan->state = ST_DONE;
+            continue;
+        }
+        const uint32_t total = scratch[60];
+        const bool trunc = scratch[49] != 0;
+        if (threadIdx.x == 0 && a.d_stats && !a.fallback) atomicMax(&a.d_stats->max_count, (int)total);
+        if (trunc || total < (uint32_t)a.topk) {
+            if (!a.fallback && !a.fb_hist) {
+                // no rescan storage: the row was longer than the max_len the
+                // workspace was sized for
+                for (int i = threadIdx.x; i < a.topk; i += THREADS) out[i] = -1;
+                if (threadIdx.x == 0) {
+                    raise_status(a.d_status, IDX_DEV_RANGE);
+                    plan->state = ST_DONE;
+                }
+            } else if (!a.fallback) {
+                // the sampled threshold missed: exact full-row rescan
+                for (int i = threadIdx.x; i < kHistBins; i += THREADS)
+                    a.fb_hist[(long long)r * kHistBins + i] = 0u;
+                if (threadIdx.x == 0) {
+                    plan->state = ST_HIST;
+                    plan->level = 0;
+                    plan->prefix = 0u;
+                    plan->above = 0;
+                    atomicAdd(&a.fb_cnt[0], 1);
+                    if (a.d_stats) {
+                        atomicAdd(trunc ? &a.d_stats->overflow_rows : &a.d_stats->short_rows, 1);
+                        atomicAdd(&a.d_stats->fallback_rows, 1);
+                    }
+                }
+            } else if (threadIdx.x == 0) {
+                raise_status(a.d_status, IDX_DEV_STATE);
                 plan->state = ST_DONE;
             }
-        } else if (!a.fallback) {
-            // the sampled threshold missed: exact full-row rescan
-            for (int i = threadIdx.x; i < kHistBins; i += THREADS)
-                a.fb_hist[(long long)r * kHistBins + i] = 0u;
-            if (threadIdx.x == 0) {
-                plan->state = ST_HIST;
-                plan->level = 0;
-                plan->prefix = 0u;
-                plan->above = 0;
-                atomicAdd(&a.fb_cnt[0], 1);
-                if (a.d_stats) {
-                    atomicAdd(trunc ? &a.d_stats->overflow_rows : &a.d_stats->short_rows, 1);
-                    atomicAdd(&a.d_stats->fallback_rows, 1);
+            continue;
+        }
+
+        // load the runs back to back, four independent loads per thread in flight
+        const float* ss = a.slab_s + (long long)r * CR;
+        const int* si = a.slab_i + (long long)r * CR;
+        const uint32_t cnt = run_off[kRuns];
+        for (uint32_t base = 0; base < cnt; base += 4 * THREADS) {
+            float sv[4];
+            int iv[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const uint32_t e = base + u * THREADS + threadIdx.x;
+                if (e < cnt) {
+                    int q = 0;
+#pragma unroll
+                    for (int j = 1; j < kRuns; ++j) q += e >= run_off[j];
+                    const uint32_t src = (uint32_t)q * (uint32_t)a.cap_q + (e - run_off[q]);
+                    sv[u] = ss[src];
+                    iv[u] = si[src];
                 }
             }
-        } else if (threadIdx.x == 0) {
-            raise_status(a.d_status, IDX_DEV_STATE);
-            plan->state = ST_DONE;
-        }
-        return;
-    }
-
-    // load the runs back to back
-    const long long row_base = (long long)r * CR;
-    for (int q = 0; q < kRuns; ++q) {
-        const uint32_t o = run_off[q], c = run_off[q + 1] - o;
-        const float* ss = a.slab_s + row_base + (long long)q * a.cap_q;
-        const int* si = a.slab_i + row_base + (long long)q * a.cap_q;
-        for (uint32_t e = threadIdx.x; e < c; e += THREADS) {
-            keys[o + e] = fkey(ss[e]);
-            idxs[o + e] = (uint32_t)si[e];
-        }
-    }
-    const uint32_t cnt = run_off[kRuns];
-    __syncthreads();
-    const Threshold th = refine_in_smem<THREADS>(keys, cnt, 0, 0u, a.topk, hist, scratch);
-
-    // lowest indices among the keys equal to T
-    uint32_t* ntie = scratch + 61;
-    if (threadIdx.x == 0) *ntie = 0u;
-    __syncthreads();
-    for (uint32_t e = threadIdx.x; e < cnt; e += THREADS)
-        if (keys[e] == th.key) tmp[atomicAdd(ntie, 1u)] = ~idxs[e];
-    __syncthreads();
-    uint32_t idx_cut = 0xffffffffu;
-    if (*ntie > th.need) {
-        const Threshold ti = refine_in_smem<THREADS>(tmp, *ntie, 0, 0u, th.need, hist, scratch);
-        idx_cut = ~ti.key;
-    }
-    __syncthreads();
-
-    // ordered compaction of the selected entries into tmp (runs stay contiguous)
-    uint32_t done = 0;
-    for (uint32_t base = 0; base < cnt; base += THREADS * 4) {
-        uint32_t sel = 0;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const uint32_t e = base + threadIdx.x * 4 + c;
-            const bool s_ = e < cnt && (keys[e] > th.key || (keys[e] == th.key && idxs[e] <= idx_cut));
-            sel |= (s_ ? 1u : 0u) << c;
-        }
-        uint32_t tot;
-        const uint32_t incl = block_incl_scan<THREADS>(__popc(sel), scratch, &tot);
-        uint32_t pos = done + incl - __popc(sel);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const uint32_t e = base + threadIdx.x * 4 + c;
-            if (e < cnt) {
-                for (int q = 0; q <= kRuns; ++q)
-                    if (run_off[q] == e) run_sel[q] = pos;  // first entry of run q
-            }
-            if ((sel >> c) & 1u) {
-                if (pos < (uint32_t)CR) tmp[pos] = idxs[e];
-                ++pos;
+            for (int u = 0; u < 4; ++u) {
+                const uint32_t e = base + u * THREADS + threadIdx.x;
+                if (e < cnt) {
+                    keys[e] = fkey(sv[u]);
+                    idxs[e] = (uint32_t)iv[u];
+                }
             }
         }
-        done += tot;
-    }
-    if (threadIdx.x == 0) {
-        // runs that start at or past the end of the list
-        for (int q = 0; q <= kRuns; ++q)
-            if (run_off[q] >= cnt) run_sel[q] = done;
-    }
-    __syncthreads();
+        __syncthreads();
 
-    // Output order.  An aligned block of 32 keys lies in one 32-key column of
-    // one tile, so all its candidates sit in one run, contiguous and ascending.
-    // Counting the selected entries per block and scanning the counts gives
-    // every entry its output position; rows with more blocks than the
-    // histogram (or keys[]) holds merge the runs by binary search instead.
-    const uint32_t nsel = done < (uint32_t)a.topk ? done : (uint32_t)a.topk;
-    const long long ks_r = a.ks[r];
-    const long long b_first = ks_r >> 5;
-    const long long nblk = n > 0 ? ((ks_r + n - 1) >> 5) - b_first + 1 : 0;
-    if (nblk <= kHistBins && nblk <= CR) {
-        uint32_t* first = keys;  // keys[] is free now: first list position of each block
-        zero_shared<THREADS>(hist, kHistBins);
-        __syncthreads();
-        for (uint32_t p = threadIdx.x; p < nsel; p += THREADS) {
-            const uint32_t b = (uint32_t)(((ks_r + tmp[p]) >> 5) - b_first);
-            atomicAdd(&hist[b], 1u);
-            int q = 0;
-            while (q + 1 < kRuns && p >= run_sel[q + 1]) ++q;
-            const bool head = p == run_sel[q] ||
-                              (uint32_t)(((ks_r + tmp[p - 1]) >> 5) - b_first) != b;
-            if (head) first[b] = p;
+        // exact threshold key T and how many keys equal to T are taken
+        uint32_t need;
+        const uint32_t T = cand_select(
+            cnt, (uint32_t)a.topk, [](uint32_t) { return true; },
+            [&](uint32_t e) { return keys[e]; }, hist, scratch, &need);
+        // the lowest `need` indices among the keys equal to T
+        uint32_t nt = 0;
+        for (uint32_t e = threadIdx.x; e < cnt; e += THREADS) nt += keys[e] == T;
+        uint32_t ntie;
+        block_incl_scan<THREADS>(nt, scratch, &ntie);
+        uint32_t idx_cut = 0xffffffffu;
+        if (ntie > need) {
+            uint32_t unused;
+            idx_cut = ~cand_select(
+                cnt, need, [&](uint32_t e) { return keys[e] == T; },
+                [&](uint32_t e) { return ~idxs[e]; }, hist, scratch, &unused);
         }
-        __syncthreads();
-        // exclusive scan of the block counts, BPT consecutive blocks per thread
-        constexpr int BPT = kHistBins / THREADS;
-        uint32_t c[BPT], local = 0;
+
+        // ascending output through the index bitmap, 65536 indices per pass
+        uint32_t* bm = hist;
+        constexpr int WPT = kBitmapWords / THREADS;  // bitmap words per thread
+        uint32_t written = 0;
+        for (long long c0 = 0; c0 < n && written < (uint32_t)a.topk; c0 += 32ll * kBitmapWords) {
 #pragma unroll
-        for (int j = 0; j < BPT; ++j) {
-            c[j] = hist[threadIdx.x * BPT + j];
-            local += c[j];
-        }
-        const uint32_t incl = block_incl_scan<THREADS>(local, scratch, nullptr);
-        uint32_t run_sum = incl - local;
+            for (int j = 0; j < WPT; ++j) bm[threadIdx.x * WPT + j] = 0u;
+            __syncthreads();
+            for (uint32_t base = 0; base < cnt; base += 4 * THREADS) {
 #pragma unroll
-        for (int j = 0; j < BPT; ++j) {
-            hist[threadIdx.x * BPT + j] = run_sum;
-            run_sum += c[j];
+                for (int u = 0; u < 4; ++u) {
+                    const uint32_t e = base + u * THREADS + threadIdx.x;
+                    if (e < cnt) {
+                        const uint32_t ky = keys[e], ix = idxs[e];
+                        const long long rel = (long long)ix - c0;
+                        if ((ky > T || (ky == T && ix <= idx_cut)) && rel >= 0 &&
+                            rel < 32ll * kBitmapWords)
+                            atomicOr(&bm[rel >> 5], 1u << (rel & 31));
+                    }
+                }
+            }
+            __syncthreads();
+            uint32_t wv[WPT], local = 0;
+#pragma unroll
+            for (int j = 0; j < WPT; ++j) {
+                wv[j] = bm[threadIdx.x * WPT + j];
+                local += __popc(wv[j]);
+            }
+            uint32_t tot;
+            const uint32_t incl = block_incl_scan<THREADS>(local, scratch, &tot);
+            uint32_t pos = written + incl - local;
+#pragma unroll
+            for (int j = 0; j < WPT; ++j) {
+                uint32_t x = wv[j];
+                const long long wbase = c0 + 32ll * (threadIdx.x * WPT + j);
+                while (x) {
+                    const int bit = __ffs(x) - 1;
+                    if (pos < (uint32_t)a.topk) out[pos] = (int)(wbase + bit);
+                    ++pos;
+                    x &= x - 1u;
+                }
+            }
+            written += tot;
         }
-        __syncthreads();
-        for (uint32_t p = threadIdx.x; p < nsel; p += THREADS) {
-            const uint32_t b = (uint32_t)(((ks_r + tmp[p]) >> 5) - b_first);
-            const uint32_t pos = hist[b] + (p - first[b]);
-            if (pos < (uint32_t)a.topk) out[pos] = (int)tmp[p];
-        }
-    } else {
-        // output rank = rank in own run + entries of the other runs below it
-        for (uint32_t p = threadIdx.x; p < nsel; p += THREADS) {
-            const uint32_t v = tmp[p];
-            int q = 0;
-            while (q + 1 < kRuns && p >= run_sel[q + 1]) ++q;
-            uint32_t pos = p - run_sel[q];
-            for (int o = 0; o < kRuns; ++o)
-                if (o != q) pos += lower_bound_u32(tmp + run_sel[o], run_sel[o + 1] - run_sel[o], v);
-            if (pos < (uint32_t)a.topk) out[pos] = (int)v;
-        }
+        if (threadIdx.x == 0) plan->state = ST_DONE;
     }
-    if (threadIdx.x == 0) plan->state = ST_DONE;
 }
 
 // ------------------------------------------------------------ launchers
@@ -980,21 +998,21 @@ size_t split_workspace_bytes(int rows, int g) {
 }
 
 size_t cand_smem_bytes(int cap_q) {
-    return (kHistBins + kCandScratch) * sizeof(uint32_t) +
-           (size_t)cap_q * kRuns * 3 * sizeof(uint32_t);
+    return (kBitmapWords + kCandScratch) * sizeof(uint32_t) +
+           (size_t)cap_q * kRuns * 2 * sizeof(uint32_t);
 }
 
 cudaError_t launch_cand_topk(const CandArgs& a, cudaStream_t s) {
-    constexpr int T = 512;
-    auto kern = cand_topk_kernel<T>;
     const size_t sm = cand_smem_bytes(a.cap_q);
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    cudaError_t e =
+        cudaFuncSetAttribute(cand_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e != cudaSuccess) return e;
     if (a.rows == 0) return cudaSuccess;
-    kern<<<a.rows, T, sm, s>>>(a);
+    // the rescan's pass usually has no row to select: a short grid that strides
+    // over the rows exits at once
+    const int grid = a.fallback ? (a.rows < a.grid_limit ? a.rows : a.grid_limit) : a.rows;
+    cand_topk_kernel<<<grid, kCandThreads, sm, s>>>(a);
     return cudaGetLastError();
 }
-
-
 
 }  // namespace idx

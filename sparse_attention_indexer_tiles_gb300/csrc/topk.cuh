@@ -57,6 +57,7 @@ struct CandArgs {
     const int* ke;
     int rows, topk, cap;
     int fallback;         // 0: main pass (flags rows), 1: rows re-emitted by the rescan
+    int grid_limit;       // CTAs of the rescan's pass (they stride over the rows)
     int* out;
     int* d_status;
     idx_stats* d_stats;
