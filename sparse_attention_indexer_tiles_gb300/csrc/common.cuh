@@ -222,6 +222,37 @@ IDX_DEVI void tmem_ld8(uint32_t taddr, float* v) {
     for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 16x256b shape, R repetitions along the columns (R in {1, 2, 4}): thread t
+// gets, for repetition j, lanes t/4 and t/4 + 8 (relative to taddr's lane) at
+// columns 8j + 2(t%4) and 8j + 2(t%4) + 1, in the order (lane t/4, col even),
+// (t/4, odd), (t/4 + 8, even), (t/4 + 8, odd).
+template <int R>
+IDX_DEVI void tmem_ld16x256b(uint32_t taddr, float* v) {
+    uint32_t r[4 * R];
+    if constexpr (R == 1) {
+        asm volatile("tcgen05.ld.sync.aligned.16x256b.x1.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                     : "r"(taddr));
+    } else if constexpr (R == 2) {
+        asm volatile(
+            "tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+              "=r"(r[7])
+            : "r"(taddr));
+    } else {
+        static_assert(R == 4, "1, 2 or 4 repetitions");
+        asm volatile(
+            "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, "
+            "%10, %11, %12, %13, %14, %15}, [%16];"
+            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+              "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+              "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+            : "r"(taddr));
+    }
+#pragma unroll
+    for (int i = 0; i < 4 * R; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 IDX_DEVI void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // Warpgroup-wide register reallocation (all 128 threads of the warpgroup).

@@ -73,38 +73,53 @@ enum : int {
     MW_THRF,        // emit: the float whose key is thr (keys compare as floats)
 };
 
-// sum_h w[h] * (acc[h] + |acc[h]|) = 2 sum_h w[h] ReLU(acc[h]) for the TMEM row
-// of this thread, H consecutive columns from taddr.  x + |x| stays on the FMA
-// pipe; packed FFMA2 accumulates two heads per instruction into eight
-// partial sums that are combined in a fixed order.
+// Head reduce of one row for the 32 keys of a warp's TMEM lane quarter.
+// The accumulator columns are read in the 16x256b shape: for each half of the
+// quarter (16 lanes) thread t holds keys t/4 and t/4 + 8 at heads
+// 8j + 2c, 8j + 2c + 1 (c = t % 4), so a thread needs only H/4 of the row's
+// weights (held in registers for the whole kernel).  Each thread forms
+//   P_k = sum over its heads of w[h] * (acc[h] + |acc[h]|)
+// for its four keys k (x + |x| = 2 ReLU(x) stays on the FMA pipe; packed FFMA2
+// takes two heads per instruction), and two butterfly steps over the four
+// threads of a key group leave thread t with the full sum of one key,
+// quarter offset key_off(t) = t/4 + 16 (t & 1) + 8 ((t >> 1) & 1).  The
+// summation order is fixed, so every scoring mode gets the same bits.
+IDX_DEVI int quad_key_off(int lane) { return (lane >> 2) + 16 * (lane & 1) + 8 * ((lane >> 1) & 1); }
+
 template <int H>
-IDX_DEVI float head_reduce2(uint32_t taddr, const float* wr) {
-    constexpr int CH = H >= 32 ? 32 : H;
-    float2 acc[4];
+IDX_DEVI float head_reduce_quad(uint32_t taddr, const float2* wq) {
+    constexpr int REPS = H / 8;                   // 8-column groups of the row
+    constexpr int RL = REPS < 2 ? REPS : 2;       // repetitions per load
+    const int lane = threadIdx.x & 31;
+    float P[4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) acc[u] = make_float2(0.f, 0.f);
+    for (int half = 0; half < 2; ++half) {
+        float2 lo = make_float2(0.f, 0.f), hi = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int c = 0; c < H / CH; ++c) {
-        float v[CH];
-        if constexpr (CH == 32) tmem_ld32(taddr + c * 32, v);
-        else if constexpr (CH == 16) tmem_ld16(taddr, v);
-        else tmem_ld8(taddr, v);
-        tmem_ld_wait();
-        const float4* w4 = reinterpret_cast<const float4*>(wr + c * CH);
+        for (int j0 = 0; j0 < REPS; j0 += RL) {
+            float v[4 * RL];
+            tmem_ld16x256b<RL>(taddr + ((uint32_t)(half * 16) << 16) + (uint32_t)(j0 * 8), v);
+            tmem_ld_wait();
 #pragma unroll
-        for (int h4 = 0; h4 < CH / 4; ++h4) {
-            const float4 wq = w4[h4];
-            const float* x = v + 4 * h4;
-            acc[(2 * h4) & 3] = __ffma2_rn(make_float2(wq.x, wq.y),
-                                           make_float2(x[0] + fabsf(x[0]), x[1] + fabsf(x[1])),
-                                           acc[(2 * h4) & 3]);
-            acc[(2 * h4 + 1) & 3] = __ffma2_rn(make_float2(wq.z, wq.w),
-                                               make_float2(x[2] + fabsf(x[2]), x[3] + fabsf(x[3])),
-                                               acc[(2 * h4 + 1) & 3]);
+            for (int j = 0; j < RL; ++j) {
+                const float* y = v + 4 * j;
+                lo = __ffma2_rn(wq[j0 + j], make_float2(y[0] + fabsf(y[0]), y[1] + fabsf(y[1])), lo);
+                hi = __ffma2_rn(wq[j0 + j], make_float2(y[2] + fabsf(y[2]), y[3] + fabsf(y[3])), hi);
+            }
         }
+        P[2 * half] = lo.x + lo.y;      // key t/4 + 16 half
+        P[2 * half + 1] = hi.x + hi.y;  // key t/4 + 8 + 16 half
     }
-    return ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) +
-           ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
+    // P = keys g, g + 8, g + 16, g + 24 (g = t / 4); reduce over t % 4
+    const bool b0 = lane & 1, b1 = (lane >> 1) & 1;
+    const float s0 = b0 ? P[0] : P[2], s1 = b0 ? P[1] : P[3];
+    const float r0 = __shfl_xor_sync(0xffffffffu, s0, 1);
+    const float r1 = __shfl_xor_sync(0xffffffffu, s1, 1);
+    const float k0 = (b0 ? P[2] : P[0]) + r0;  // key g (+16 when b0)
+    const float k1 = (b0 ? P[3] : P[1]) + r1;  // key g + 8 (+16 when b0)
+    const float sx = b1 ? k0 : k1;
+    const float rx = __shfl_xor_sync(0xffffffffu, sx, 2);
+    return (b1 ? k1 : k0) + rx;
 }
 
 template <int DT, int H, int RB>
@@ -346,7 +361,10 @@ score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         const int q = warp & 3;              // TMEM lane quarter
         const int grp = (e >> 2) & 1;        // half of the rows
         const int run = q * 2 + team;        // candidate run of this warp
-        const uint32_t lt = (1u << lane) - 1u;
+        // lanes whose key comes earlier (candidates are appended in key order)
+        uint32_t lt = 0u;
+#pragma unroll
+        for (int l = 0; l < 32; ++l) lt |= (quad_key_off(l) < quad_key_off(lane) ? 1u : 0u) << l;
         int cnt[C::RG];
         // row metadata from shared memory; the emit words of up to 2 rows per
         // warp are held in registers across the tile loop
@@ -379,11 +397,20 @@ score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
 #define RPRE(j) ((uint32_t)row_word(j, MW_PREFIX))
         // per-key scale of the team's next tile, loaded one tile ahead
         auto scale_of = [&](int t) -> float {
-            const long long ki = (long long)(t0 + t) * C::M + q * 32 + lane;
+            const long long ki = (long long)(t0 + t) * C::M + q * 32 + quad_key_off(lane);
             const long long kk = mode == SM_SAMPLE ? phase + (long long)a.S * ki : ki;
             const bool ok = t < ntiles && (mode == SM_SAMPLE ? ki < a.nsamp : kk < a.keys);
             return ok ? __ldg(a.k_scale + kk) : 0.f;
         };
+        // this thread's weights: row j, head pair (8 rep + 2c, 8 rep + 2c + 1)
+        const int kq = quad_key_off(lane);  // this thread's key in the quarter
+        float2 wq[C::RG][H / 8];
+#pragma unroll
+        for (int j = 0; j < C::RG; ++j) {
+            const float* wr = w_s + (grp * C::RG + j) * H + 2 * (lane & 3);
+#pragma unroll
+            for (int rp = 0; rp < H / 8; ++rp) wq[j][rp] = make_float2(wr[8 * rp], wr[8 * rp + 1]);
+        }
         float next_scale = scale_of(team);
         const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(team * C::N);
         for (int i = team, u = 0; i < ntiles; i += 2, ++u) {
@@ -396,13 +423,13 @@ score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 break;
             }
             tc_fence_after();
-            const int kidx = (t0 + i) * C::M + q * 32 + lane;  // key, or sample index
+            const int kidx = (t0 + i) * C::M + q * 32 + kq;  // key, or sample index
             const float post_scale = 0.5f * cur_scale;
             float sc[C::RG];
 #pragma unroll
             for (int j = 0; j < C::RG; ++j) {
                 const int rr = grp * C::RG + j;
-                sc[j] = head_reduce2<H>(tbase + (uint32_t)(rr * H), w_s + rr * H) * post_scale;
+                sc[j] = head_reduce_quad<H>(tbase + (uint32_t)(rr * H), wq[j]) * post_scale;
             }
             tc_fence_before();
             __syncwarp();
