@@ -429,7 +429,61 @@ def secondary(idx, dev, g, inp, out, ws, flush, pk, args):
 
     res["standalone_topk"] = standalone_topk(idx, dev, flush, pk, args)
     res["split_topk"] = split_topk(idx, dev, flush, pk, args)
+    for name in ("long_context", "mixed_batch"):
+        res[name] = other_fused(idx, dev, flush, pk, args, name)
+        torch.cuda.empty_cache()
     return res
+
+
+def other_fused(idx, dev, flush, pk, args, name):
+    """idx_score_topk on another fused workload: whole-call pairs/s and the
+    emit pass against the fp8 tensor peak, with the path counters."""
+    import torch
+    import synth
+    inp = synth.workload(name)
+    g = {n: getattr(inp, n).to(dev) for n in ("q", "k", "k_scale", "w", "ks", "ke")}
+    out = torch.empty(inp.rows, inp.topk, dtype=torch.int32, device=dev)
+    need = idx.idx_score_topk_workspace(inp.rows, inp.keys, 0, inp.H, inp.D, inp.topk,
+                                        inp.q.dtype)
+    ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    stats = idx.Stats(dev)
+
+    def call(ev=None, o=None):
+        opts = o or idx.Options()
+        if ev is not None:
+            opts.stage_events = ev.ptr
+        idx.idx_score_topk(g["q"], g["k"], g["k_scale"], g["w"], g["ks"], g["ke"], inp.topk,
+                           out=out, ws=ws, options=opts)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        call()
+    stats.reset()
+    call(o=idx.make_options(None, stats))
+    torch.cuda.synchronize()
+    reps = max(3, min(args.steps, 5))
+    evs = [idx.StageEvents(5) for _ in range(reps)]
+    for e in evs:
+        flush.zero_()
+        call(e)
+    torch.cuda.synchronize()
+    ms = statistics.mean(e.elapsed(0, 4) for e in evs)
+    emit_ms = statistics.mean(e.elapsed(1, 2) for e in evs)
+    pairs = inp.pairs()
+    flops = 2.0 * inp.H * inp.D * pairs
+    peak = 2.0 * pk["bf16_tflops"]
+    emit_tf = flops / (emit_ms * 1e-3) / 1e12
+    return {"workload": f"{name}: rows={inp.rows} keys={inp.keys} H={inp.H} D={inp.D} "
+                        f"topk={inp.topk}",
+            "pairs_per_s": pairs / (ms * 1e-3), "ms": ms,
+            "stage_ms": {"sample_and_threshold": statistics.mean(e.elapsed(0, 1) for e in evs),
+                         "score_and_emit": emit_ms,
+                         "slab_topk": statistics.mean(e.elapsed(2, 3) for e in evs),
+                         "rescan": statistics.mean(e.elapsed(3, 4) for e in evs)},
+            "emit_roofline": {"bound": "tensor", "achieved": emit_tf, "peak": peak,
+                              "unit": "TFLOP/s", "frac": emit_tf / peak},
+            "whole_call_tensor_frac": flops / (ms * 1e-3) / 1e12 / peak,
+            "path_stats": stats.read()}
 
 
 def split_topk(idx, dev, flush, pk, args):
