@@ -89,7 +89,7 @@ IDX_DEVI int quad_key_off(int lane) { return (lane >> 2) + 16 * (lane & 1) + 8 *
 template <int H>
 IDX_DEVI float head_reduce_quad(uint32_t taddr, const float2* wq) {
     constexpr int REPS = H / 8;                   // 8-column groups of the row
-    constexpr int RL = REPS < 2 ? REPS : 2;       // repetitions per load
+    constexpr int RL = H >= 64 ? 2 : (REPS < 4 ? REPS : 4);       // repetitions per load
     const int lane = threadIdx.x & 31;
     float P[4];
 #pragma unroll
@@ -140,7 +140,8 @@ score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + C::OFF_TSLOT);
     float* w_s = reinterpret_cast<float*>(smem + C::OFF_W);
     int* meta = reinterpret_cast<int*>(smem + C::OFF_META);
-    int* misc = reinterpret_cast<int*>(smem + C::OFF_MISC);  // [0] t0, [1] ntiles
+    // [0] t0, [1] ntiles, [2] abort flag, [3, 4) keys every active row sees
+    int* misc = reinterpret_cast<int*>(smem + C::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 2);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -220,7 +221,8 @@ score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         // below the one of -inf admit every score, whatever the index
         if (thr <= 0x007fffffu) cut = kAllIdx;
         m[MW_CUT] = cut;
-        m[MW_THRF] = __float_as_int(key_floor_float(thr));
+        // rows that take no part: a threshold no score reaches
+        m[MW_THRF] = __float_as_int(active ? key_floor_float(thr) : INFINITY);
     }
     for (int i = tid; i < C::R * H; i += C::THREADS) {
         const long long r = r0 + i / H;
@@ -228,13 +230,17 @@ score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     }
     __syncthreads();
     if (tid == 0) {
-        int lo = 0x7fffffff, hi = -1;
+        int lo = 0x7fffffff, hi = -1, all_lo = -1, all_hi = 0x7fffffff;
         for (int j = 0; j < C::R; ++j) {
             const int* m = meta + j * C::META_WORDS;
             if (m[MW_HI] <= m[MW_LO]) continue;
             lo = m[MW_LO] < lo ? m[MW_LO] : lo;
             hi = m[MW_HI] > hi ? m[MW_HI] : hi;
+            all_lo = m[MW_LO] > all_lo ? m[MW_LO] : all_lo;
+            all_hi = m[MW_HI] < all_hi ? m[MW_HI] : all_hi;
         }
+        misc[3] = all_lo;
+        misc[4] = all_hi;
         int t0 = 0, nt = 0;
         if (hi > lo) {
             t0 = lo / C::M;
@@ -411,6 +417,7 @@ score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
 #pragma unroll
             for (int rp = 0; rp < H / 8; ++rp) wq[j][rp] = make_float2(wr[8 * rp], wr[8 * rp + 1]);
         }
+        const int all_lo = misc[3], all_hi = misc[4];
         float next_scale = scale_of(team);
         const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(team * C::N);
         for (int i = team, u = 0; i < ntiles; i += 2, ++u) {
@@ -470,6 +477,27 @@ score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                     if (valid && lane == __ffs(same) - 1)
                         atomicAdd(&a.fb_hist[(long long)(r0 + grp * C::RG + j) * kHistBins + dg],
                                   (uint32_t)__popc(same));
+                }
+            } else if (C::RG > 2 && mode == SM_EMIT && (t0 + i) * C::M >= all_lo &&
+                       (t0 + i + 1) * C::M <= all_hi) {
+                // SM_EMIT on a tile every active row sees whole: the rule is
+                // s >= T_r (rows that take no part have T = +inf).  Taken for
+                // four or more rows per warp (H <= 32), where the per-row test
+                // is a large share of the epilogue.
+#pragma unroll
+                for (int j = 0; j < C::RG; ++j) {
+                    const float thr = HOIST ? e_thr[HOIST ? j : 0]
+                                            : __int_as_float(row_word(j, MW_THRF));
+                    const bool hit = sc[j] >= thr;
+                    const uint32_t A = __ballot_sync(0xffffffffu, hit);
+                    if (A) {
+                        const int pos = cnt[j] + __popc(A & lt);
+                        if (hit && pos < a.cap_q) {
+                            ps[j * rstride + pos] = sc[j];
+                            pi[j * rstride + pos] = kidx - (HOIST ? e_lo[HOIST ? j : 0] : RLO(j));
+                        }
+                        cnt[j] += __popc(A);
+                    }
                 }
             } else {
                 // SM_EMIT / SM_FB_EMIT: append every key that passes the row's
