@@ -520,9 +520,11 @@ def standalone_topk(idx, dev, flush, pk, args):
     sc = si.scores.to(dev)
     ks, ke = si.ks.to(dev), si.ke.to(dev)
     o3 = torch.empty(si.rows, si.topk, dtype=torch.int32, device=dev)
+    need = idx.idx_topk_workspace(si.rows, si.stride, si.topk)
+    ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
 
     def st():
-        idx.idx_topk_from_scores(sc, ks, ke, si.topk, out=o3)
+        idx.idx_topk_from_scores(sc, ks, ke, si.topk, out=o3, ws=ws)
 
     for _ in range(args.warmup):
         st()
