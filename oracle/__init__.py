@@ -14,6 +14,8 @@ the header of ``oracle.c``:
                       ascending row-relative indices padded with -1.
 * ``score_topk``      both, for a list of rows, on host threads.
 * ``topk_from_scores``the selection applied to given fp32 scores.
+* ``page_transform``  row-relative positions -> physical KV slots of a paged
+                      cache (page size P): table[t, p // P] * P + p % P, -1 kept.
 """
 from __future__ import annotations
 
@@ -197,3 +199,23 @@ def topk_from_scores(scores, ks, ke, topk: int, rows=None, nthreads: int | None 
     if e:
         raise MemoryError("oracle topk_from_scores failed")
     return out
+
+
+def page_transform(idx, table, page_size: int = 64, row_map=None):
+    """Page-table transform of idx [rows, topk] (a new array) and the number
+    of positions whose page lies outside the table row (set to -1)."""
+    ix = _np(idx, np.int32)
+    tb = _np(table, np.int32)
+    rows, topk = ix.shape
+    rm = None if row_map is None else _np(row_map, np.int32)
+    out = np.empty_like(ix)
+    lib = _load()
+    fn = lib.orc_page_transform
+    P, i32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong
+    fn.argtypes = [P, i32, i32, P, i64, P, i32, P]
+    fn.restype = i64
+    bad = fn(_ptr(ix), rows, topk, _ptr(tb), tb.shape[1], None if rm is None else _ptr(rm),
+             page_size, _ptr(out))
+    if bad < 0:
+        raise ValueError("oracle page_transform: bad arguments")
+    return out, int(bad)

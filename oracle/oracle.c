@@ -21,6 +21,12 @@
  *            key - ks[row]) and section 3 (a consumer skips negative
  *            positions); "[sglang] ROCm DSA Indexer Top-K 최적화", solution
  *            section (exact top-k at torch.topk-level recall).
+ *   page     map a row-relative position p >= 0 to the physical KV slot
+ *            table[t, p / P] * P + p % P of a paged cache with page size P,
+ *            where t is the page-table row of the query row; negative
+ *            positions (the -1 padding) stay as they are.  "[sglang] logits를
+ *            쓰지 않는 top-k", section 3 (the page-table transform for paged
+ *            output, page size 64).
  *
  * Inputs are decoded exactly to fp64 from the bit formats:
  *   e4m3 (fn):  1 sign, 4 exponent bits (bias 7), 3 mantissa bits, subnormals
@@ -233,4 +239,33 @@ int orc_topk_from_scores(const float* scores, long long stride, const int32_t* k
     J.scores = scores; J.stride = stride;
     J.ks = ks; J.ke = ke; J.rows = rows; J.nrows = nrows; J.topk = topk; J.out = out;
     return run(&J, nthreads);
+}
+
+/* Page-table transform of idx [rows, topk] into out (same shape).
+ * table is [*, table_stride]; row r uses table row row_map[r] (row_map NULL:
+ * row r).  Returns the number of positions whose page lies outside the table
+ * row (those become -1), or -1 for bad arguments. */
+long long orc_page_transform(const int32_t* idx, int rows, int topk, const int32_t* table,
+                             long long table_stride, const int32_t* row_map, int page_size,
+                             int32_t* out) {
+    if (rows < 0 || topk < 0 || page_size < 1 || table_stride < 0) return -1;
+    long long bad = 0;
+    for (int r = 0; r < rows; ++r) {
+        const long long t = row_map ? (long long)row_map[r] : (long long)r;
+        for (int i = 0; i < topk; ++i) {
+            const long long p = idx[(long long)r * topk + i];
+            long long v = p;
+            if (p >= 0) {
+                const long long page = p / page_size;
+                if (page < table_stride) {
+                    v = (long long)table[t * table_stride + page] * page_size + p % page_size;
+                } else {
+                    v = -1;
+                    ++bad;
+                }
+            }
+            out[(long long)r * topk + i] = (int32_t)v;
+        }
+    }
+    return bad;
 }

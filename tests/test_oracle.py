@@ -260,3 +260,42 @@ def test_topk_from_scores_row_subset_and_stride(orc):
     ke = torch.tensor([10, 7, 5, 10], dtype=torch.int32)
     out = orc.topk_from_scores(S, ks, ke, 3, rows=[3, 1, 2])
     assert out.tolist() == [[0, -1, -1], [2, 3, 4], [-1, -1, -1]]
+
+
+# ------------------------------------------------------------ page transform
+
+def test_page_transform_hand_example(orc):
+    g = json.load(open(os.path.join(GOLDEN, "page_transform.json")))
+    idx = np.array([r["idx"] for r in g["rows"]], dtype=np.int32)
+    rmap = np.array([r["table_row"] for r in g["rows"]], dtype=np.int32)
+    got, bad = orc.page_transform(idx, np.array(g["table"], np.int32), g["page_size"], rmap)
+    assert got.tolist() == [r["expect"] for r in g["rows"]]
+    assert bad == g["out_of_range"]
+
+
+def test_page_transform_identity_table_is_identity(orc):
+    rng = np.random.default_rng(5)
+    idx = rng.integers(-1, 4096, size=(7, 33)).astype(np.int32)
+    table = np.tile(np.arange(64, dtype=np.int32), (7, 1))  # page j is physical page j
+    got, bad = orc.page_transform(idx, table, 64)
+    assert bad == 0 and np.array_equal(got, idx)
+
+
+def test_page_transform_permuted_table_inverts(orc):
+    """A table row that permutes the pages is undone by the inverse permutation,
+    and distinct positions stay distinct; the -1 padding passes through."""
+    rng = np.random.default_rng(6)
+    P, pages = 64, 40
+    table = np.stack([rng.permutation(pages).astype(np.int32) + 100 * t for t in range(3)])
+    idx = np.stack([rng.choice(P * pages, 50, replace=False) for _ in range(5)]).astype(np.int32)
+    idx[:, -3:] = -1
+    rmap = np.array([2, 0, 1, 2, 0], np.int32)
+    got, bad = orc.page_transform(idx, table, P, rmap)
+    assert bad == 0
+    for r in range(5):
+        t = rmap[r]
+        inv = {int(v): j for j, v in enumerate(table[t])}
+        back = [inv[int(x) // P] * P + int(x) % P for x in got[r, :-3]]
+        assert back == idx[r, :-3].tolist()
+        assert (got[r, -3:] == -1).all()
+        assert len(set(got[r, :-3].tolist())) == 47
