@@ -432,7 +432,38 @@ def secondary(idx, dev, g, inp, out, ws, flush, pk, args):
     for name in ("long_context", "mixed_batch"):
         res[name] = other_fused(idx, dev, flush, pk, args, name)
         torch.cuda.empty_cache()
+    res["page_table_transform"] = page_transform(idx, dev, flush, pk, out, inp)
     return res
+
+
+def page_transform(idx, dev, flush, pk, out, inp):
+    """idx_page_table_transform on the fused step's output (rows x topk), one
+    request of keys / 64 pages: HBM roofline on 8 B per entry."""
+    import torch
+    import synth
+    table, row_map = synth.paged_layout(1, (inp.keys + 63) // 64, inp.rows, seed=77)
+    table, row_map = table.to(dev), row_map.to(dev)
+    work = torch.empty_like(out)
+    ts = []
+    for it in range(13):
+        work.copy_(out)
+        flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        idx.idx_page_table_transform(work, table, 64, row_map=row_map)
+        b.record()
+        b.synchronize()
+        if it >= 3:
+            ts.append(a.elapsed_time(b))
+    ms = statistics.mean(ts)
+    nbytes = 8 * out.numel()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"workload": f"fused_prefill output: rows={out.shape[0]} topk={out.shape[1]}, page 64",
+            "ms": ms, "entries_per_s": out.numel() / (ms * 1e-3),
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / pk["hbm_gbs"],
+                         "algorithmic": f"4 B read + 4 B written per entry = {nbytes} B"}}
 
 
 def other_fused(idx, dev, flush, pk, args, name):

@@ -206,6 +206,29 @@ idx_status idx_score_topk_noalloc(const void* q, const void* k, const float* k_s
                                   idx_dtype dt, int* out_idx, const idx_options* opt,
                                   void* stream);
 
+/* ------------------------------------------------------------------------
+ * idx_page_table_transform - row-relative top-k positions to physical KV
+ * slots of a paged cache (page "[sglang] logits를 쓰지 않는 top-k", section 3:
+ * the page-table transform for paged output, page size 64).
+ *
+ *   idx   [rows, topk] int32, device, rewritten in place: every p >= 0
+ *         becomes table[t, p / page_size] * page_size + p % page_size, with
+ *         t = row_map[r] (or r when row_map is NULL); negative entries (the
+ *         -1 padding) are left as they are.
+ *   table [table_rows, table_stride] int32, device: physical page of each
+ *         logical page of a table row.
+ *   row_map [rows] int32, device, optional: the table row of each query row
+ *         (all query rows of one request share its row).
+ * A page past table_stride, or a table row outside [0, table_rows), gives -1
+ * and raises IDX_DEV_RANGE in options->d_status.  The physical slot must fit
+ * in int32 (a precondition, not checked).  Four entries per thread with one
+ * 16-byte load and store when topk % 4 == 0 and idx is 16-byte aligned, one
+ * otherwise.  No workspace; asynchronous on `stream`.
+ * ------------------------------------------------------------------------ */
+idx_status idx_page_table_transform(int* idx, int rows, int topk, const int* table,
+                                    int table_rows, long long table_stride, const int* row_map,
+                                    int page_size, const idx_options* opt, void* stream);
+
 /* Static text for a status code. */
 const char* idx_status_string(idx_status s);
 

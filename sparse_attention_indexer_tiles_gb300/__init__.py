@@ -22,7 +22,7 @@ __all__ = [
     "IdxError", "Options", "Stats", "load", "idx_score_topk", "idx_score_topk_workspace",
     "idx_topk_from_scores", "idx_topk_workspace", "idx_score_materialise",
     "idx_status_string", "DTYPES", "STAT_FIELDS", "StageEvents", "idx_launch_count",
-    "idx_score_topk_noalloc",
+    "idx_score_topk_noalloc", "idx_page_table_transform",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -98,6 +98,8 @@ def load(path: str | None = None):
     lib.idx_topk_from_scores.restype = I
     lib.idx_score_materialise.argtypes = [P, P, P, P, P, P, I, LL, I, I, I, P, LL, P, P]
     lib.idx_score_materialise.restype = I
+    lib.idx_page_table_transform.argtypes = [P, I, I, P, I, LL, P, I, P, P]
+    lib.idx_page_table_transform.restype = I
     lib.idx_status_string.argtypes = [I]
     lib.idx_status_string.restype = ctypes.c_char_p
     lib.idx_version.argtypes = []
@@ -260,3 +262,21 @@ def idx_score_topk_noalloc(q, k, k_scale, w, ks, ke, topk: int, *, max_len: int 
         _ptr(q), _ptr(k), _ptr(k_scale), _ptr(w), _ptr(ks), _ptr(ke), rows, k.shape[0], max_len,
         H, D, topk, DTYPES[q.dtype], _ptr(out), _opt_ref(o), _stream(stream)))
     return out
+
+
+def idx_page_table_transform(idx, table, page_size: int = 64, *, row_map=None, options=None,
+                             stats: Stats | None = None, stream=None):
+    """In place: every position p >= 0 of idx [rows, topk] int32 becomes
+    table[t, p // page_size] * page_size + p % page_size (t = row_map[r] or r);
+    -1 entries stay.  Returns idx."""
+    _dev(idx, table, row_map)
+    if idx.dtype != torch.int32 or table.dtype != torch.int32:
+        raise ValueError("idx_page_table_transform: idx and table must be int32")
+    if row_map is not None and row_map.dtype != torch.int32:
+        raise ValueError("idx_page_table_transform: row_map must be int32")
+    rows, topk = idx.shape
+    o = make_options(options, stats)
+    _check("idx_page_table_transform", load().idx_page_table_transform(
+        _ptr(idx), rows, topk, _ptr(table), table.shape[0], table.shape[1], _ptr(row_map),
+        page_size, _opt_ref(o), _stream(stream)))
+    return idx

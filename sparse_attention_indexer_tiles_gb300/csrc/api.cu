@@ -10,6 +10,7 @@
 
 #include <cudaTypedefs.h>
 
+#include "page_table.cuh"
 #include "plan.cuh"
 #include "score.cuh"
 #include "topk.cuh"
@@ -458,6 +459,36 @@ idx_status idx_score_materialise(const void* q, const void* k, const float* k_sc
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     record(opt, 0, s);
     const cudaError_t e = launch_score(L, s);
+    record(opt, 1, s);
+    return cuda_status(e);
+}
+
+idx_status idx_page_table_transform(int* idx_out, int rows, int topk, const int* table,
+                                    int table_rows, long long table_stride, const int* row_map,
+                                    int page_size, const idx_options* opt, void* stream) {
+    if (rows < 0 || topk < 0 || table_rows < 0 || table_stride < 0 || page_size < 1)
+        return IDX_EINVAL;
+    if (rows == 0 || topk == 0) return IDX_OK;
+    if (!idx_out || (!table && table_rows > 0)) return IDX_EINVAL;
+    if (!aligned(idx_out, 4) || (table && !aligned(table, 4)) || (row_map && !aligned(row_map, 4)))
+        return IDX_EALIGN;
+    if (!arch_ok()) return IDX_EUNSUPPORTED;
+    PageArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.idx = idx_out;
+    a.rows = rows;
+    a.topk = topk;
+    a.table = table;
+    a.table_rows = table_rows;
+    a.table_stride = table_stride;
+    a.row_map = row_map;
+    a.page_size = page_size;
+    a.vec = (topk % 4 == 0 && aligned(idx_out, 16)) ? 1 : 0;
+    a.d_status = opt ? opt->d_status : nullptr;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    record(opt, 0, s);
+    const cudaError_t e = launch_page_transform(a, sm_count(), s);
+    if (e == cudaSuccess) count_launches(1);
     record(opt, 1, s);
     return cuda_status(e);
 }

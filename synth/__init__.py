@@ -235,6 +235,20 @@ def _mixed_batch(seed: int, requests: int = 64, rows_per_request: int = 128,
 # The named workloads: small case first, then the standalone top-k, the fused
 # prefill, the long-context stress and the mixed batch, plus the low-batch
 # long-row top-k that exercises the multi-block row split.
+def paged_layout(requests: int, pages_per_request: int, rows_per_request: int, seed: int,
+                 pool_pages: int | None = None):
+    """A paged KV cache: each request owns pages_per_request distinct physical
+    pages drawn at random (seeded) from a pool shared by all requests, and its
+    query rows use its table row.  Returns (table [requests, pages] int32,
+    row_map [requests * rows_per_request] int32)."""
+    g = _gen(seed)
+    pool = pool_pages or 2 * requests * pages_per_request
+    perm = torch.randperm(pool, generator=g)[: requests * pages_per_request]
+    table = perm.view(requests, pages_per_request).to(torch.int32).contiguous()
+    row_map = torch.arange(requests, dtype=torch.int32).repeat_interleave(rows_per_request)
+    return table, row_map
+
+
 WORKLOADS = {
     "tiny": dict(kind="indexer", rows=64, keys=4096, H=8, D=64, topk=256,
                  dtype="bf16", seed=0, scale="one"),
