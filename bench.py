@@ -47,6 +47,9 @@ def parse():
     p.add_argument("--clocks-file", default=None)
     p.add_argument("--rows", type=int, default=0,
                    help="profiling: use only the last N query rows of the workload")
+    p.add_argument("--route-sweep", action="store_true",
+                   help="time the fused and the two-pass path over short key lengths (the "
+                        "routing gate's crossover) and print one JSON line per case")
     p.add_argument("--only", choices=["all", "fused", "topk"], default="all",
                    help="profiling: run only the fused step or only the standalone top-k")
     return p.parse_args()
@@ -256,6 +259,10 @@ def main():
     stream = torch.cuda.current_stream()
     pk = peaks()
 
+    if args.route_sweep:
+        route_sweep(idx, dev)
+        return
+
     if args.only == "topk":
         print(json.dumps(standalone_topk(idx, dev, torch.empty(256 << 20, dtype=torch.uint8,
                                                                device=dev), pk, args)))
@@ -464,6 +471,45 @@ def page_transform(idx, dev, flush, pk, out, inp):
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
                          "frac": gbs / pk["hbm_gbs"],
                          "algorithmic": f"4 B read + 4 B written per entry = {nbytes} B"}}
+
+
+def route_sweep(idx, dev):
+    """Fused vs two-pass (materialise + top-k) over key lengths around the
+    routing gate: 4096 causal rows of e4m3 q/k, H 64 / 32, topk 2048 / 512."""
+    import torch
+    import synth
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for H, topk in ((64, 2048), (32, 2048), (64, 512)):
+        for keys in (4096, 6144, 8192, 12288, 16384, 24576, 32768, 65536):
+            rows = 4096
+            inp = synth.indexer_inputs(rows, keys, H, 128, topk, "fp8", seed=90)
+            g = {n: getattr(inp, n).to(dev) for n in ("q", "k", "k_scale", "w", "ks", "ke")}
+            out = torch.empty(rows, topk, dtype=torch.int32, device=dev)
+            out2 = torch.empty_like(out)
+            need = idx.idx_score_topk_workspace(rows, keys, 0, H, 128, topk, inp.q.dtype)
+            ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+            S = torch.empty(rows, int((inp.ke - inp.ks).max()), dtype=torch.float32, device=dev)
+            rel = idx.Options(relative_rows=1)
+
+            def fused():
+                idx.idx_score_topk(g["q"], g["k"], g["k_scale"], g["w"], g["ks"], g["ke"], topk,
+                                   out=out, ws=ws)
+
+            def two_pass():
+                idx.idx_score_materialise(g["q"], g["k"], g["k_scale"], g["w"], g["ks"], g["ke"],
+                                          out=S)
+                idx.idx_topk_from_scores(S, g["ks"], g["ke"], topk, out=out2, options=rel)
+
+            for _ in range(2):
+                fused()
+                two_pass()
+            tf, tt = timed(fused, flush, 6), timed(two_pass, flush, 6)
+            print(json.dumps({"H": H, "topk": topk, "rows": rows, "keys": keys,
+                              "fused_ms": tf, "two_pass_ms": tt, "two_pass_over_fused": tt / tf,
+                              "identical": bool(torch.equal(out, out2)),
+                              "gate_fused": idx.idx_route_fused(keys, topk)}), flush=True)
+            del S, g, inp
+            torch.cuda.empty_cache()
 
 
 def other_fused(idx, dev, flush, pk, args, name):

@@ -207,6 +207,34 @@ idx_status idx_score_topk_noalloc(const void* q, const void* k, const float* k_s
                                   void* stream);
 
 /* ------------------------------------------------------------------------
+ * idx_score_topk_routed - the same result as idx_score_topk, by the faster
+ * path for the call's longest row (page "[sglang] logits를 쓰지 않는 top-k",
+ * section 4: the fused path is used only when the longest row sees enough
+ * keys; below that the filter passes most keys and the dense path is
+ * faster).
+ *
+ * idx_route_fused(max_len, topk) is the gate: 1 (the fused path) when
+ * max_len >= 12288 keys, or when every row fits the default candidate slab
+ * (max_len <= max(ceil(2.25 topk), 4096): all keys are emitted, no sampling);
+ * 0 otherwise (idx_score_materialise into the workspace, then
+ * idx_topk_from_scores).  12288 is the crossover measured on GB300 for e4m3
+ * q/k with H = 32 and 64 and topk 512 and 2048 (4096 causal rows): the
+ * two-pass path is faster at 6144 and 8192 keys, the fused one from 12288 on;
+ * the page's own rule (8 x topk keys, 16384 at topk 2048) sits above it.  Both
+ * paths select exactly the same keys (they compare the same fp32 scores).
+ * Arguments as idx_score_topk; max_len 0 = keys.  The workspace of the
+ * two-pass route holds the [rows, max_len] fp32 logits.
+ * ------------------------------------------------------------------------ */
+int idx_route_fused(long long max_len, int topk);
+size_t idx_score_topk_routed_workspace(int rows, long long keys, long long max_len, int H,
+                                       int D, int topk, idx_dtype dt, const idx_options* opt);
+idx_status idx_score_topk_routed(const void* q, const void* k, const float* k_scale,
+                                 const float* w, const int* ks, const int* ke, int rows,
+                                 long long keys, long long max_len, int H, int D, int topk,
+                                 idx_dtype dt, int* out_idx, void* ws, size_t ws_bytes,
+                                 const idx_options* opt, void* stream);
+
+/* ------------------------------------------------------------------------
  * idx_page_table_transform - row-relative top-k positions to physical KV
  * slots of a paged cache (page "[sglang] logits를 쓰지 않는 top-k", section 3:
  * the page-table transform for paged output, page size 64).

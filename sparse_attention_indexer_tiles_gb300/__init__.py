@@ -22,7 +22,8 @@ __all__ = [
     "IdxError", "Options", "Stats", "load", "idx_score_topk", "idx_score_topk_workspace",
     "idx_topk_from_scores", "idx_topk_workspace", "idx_score_materialise",
     "idx_status_string", "DTYPES", "STAT_FIELDS", "StageEvents", "idx_launch_count",
-    "idx_score_topk_noalloc", "idx_page_table_transform",
+    "idx_score_topk_noalloc", "idx_page_table_transform", "idx_route_fused",
+    "idx_score_topk_routed", "idx_score_topk_routed_workspace",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -98,6 +99,13 @@ def load(path: str | None = None):
     lib.idx_topk_from_scores.restype = I
     lib.idx_score_materialise.argtypes = [P, P, P, P, P, P, I, LL, I, I, I, P, LL, P, P]
     lib.idx_score_materialise.restype = I
+    lib.idx_route_fused.argtypes = [LL, I]
+    lib.idx_route_fused.restype = I
+    lib.idx_score_topk_routed_workspace.argtypes = [I, LL, LL, I, I, I, I, P]
+    lib.idx_score_topk_routed_workspace.restype = SZ
+    lib.idx_score_topk_routed.argtypes = [P, P, P, P, P, P, I, LL, LL, I, I, I, I, P, P, SZ, P,
+                                          P]
+    lib.idx_score_topk_routed.restype = I
     lib.idx_page_table_transform.argtypes = [P, I, I, P, I, LL, P, I, P, P]
     lib.idx_page_table_transform.restype = I
     lib.idx_status_string.argtypes = [I]
@@ -280,3 +288,39 @@ def idx_page_table_transform(idx, table, page_size: int = 64, *, row_map=None, o
         _ptr(idx), rows, topk, _ptr(table), table.shape[0], table.shape[1], _ptr(row_map),
         page_size, _opt_ref(o), _stream(stream)))
     return idx
+
+
+def idx_route_fused(max_len: int, topk: int) -> bool:
+    """The routing gate: True when a call whose longest row sees max_len keys
+    takes the fused path."""
+    return bool(load().idx_route_fused(max_len, topk))
+
+
+def idx_score_topk_routed_workspace(rows: int, keys: int, max_len: int, H: int, D: int,
+                                    topk: int, dtype, options=None) -> int:
+    dt = DTYPES[dtype] if not isinstance(dtype, int) else dtype
+    o = make_options(options)
+    return int(load().idx_score_topk_routed_workspace(rows, keys, max_len, H, D, topk, dt,
+                                                      _opt_ref(o)))
+
+
+def idx_score_topk_routed(q, k, k_scale, w, ks, ke, topk: int, *, max_len: int = 0, out=None,
+                          ws=None, options=None, stats: Stats | None = None, stream=None):
+    """idx_score_topk by the faster path for the longest row (fused, or the
+    logits then their top-k); the same indices either way."""
+    _dev(q, k, k_scale, w, ks, ke, out, ws)
+    rows, H, D = q.shape
+    keys = k.shape[0]
+    dt = DTYPES[q.dtype]
+    o = make_options(options, stats)
+    need = int(load().idx_score_topk_routed_workspace(rows, keys, max_len, H, D, topk, dt,
+                                                      _opt_ref(o)))
+    if out is None:
+        out = torch.empty(rows, topk, dtype=torch.int32, device=q.device)
+    if ws is None:
+        ws = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _check("idx_score_topk_routed", load().idx_score_topk_routed(
+        _ptr(q), _ptr(k), _ptr(k_scale), _ptr(w), _ptr(ks), _ptr(ke), rows, keys, max_len, H, D,
+        topk, dt, _ptr(out), _ptr(ws), ws.numel() * ws.element_size(), _opt_ref(o),
+        _stream(stream)))
+    return out

@@ -54,6 +54,13 @@ namespace {
 
 constexpr int kMaxTopk = 4096;
 constexpr int kMaxCap = 12288;
+// Route to the fused path from this many keys in the longest row on (measured
+// fused / two-pass crossover on GB300, see idx_score_topk_routed).
+constexpr long long kRouteMinKeys = 12288;
+
+size_t logits_bytes(int rows, long long stride) {
+    return ((size_t)rows * (size_t)stride * sizeof(float) + 255) / 256 * 256;
+}
 constexpr uint32_t kPhaseSeed = 0x9E3779B9u;
 
 // Is the current device an sm_103 part?  Cached per device.
@@ -461,6 +468,63 @@ idx_status idx_score_materialise(const void* q, const void* k, const float* k_sc
     const cudaError_t e = launch_score(L, s);
     record(opt, 1, s);
     return cuda_status(e);
+}
+
+int idx_route_fused(long long max_len, int topk) {
+    // rows that fit the default slab are emitted whole (no sampling): fused
+    const long long cap = std::max<long long>((long long)std::ceil(2.25 * topk), 4096);
+    return (max_len <= cap || max_len >= kRouteMinKeys) ? 1 : 0;
+}
+
+size_t idx_score_topk_routed_workspace(int rows, long long keys, long long max_len, int H,
+                                       int D, int topk, idx_dtype dt, const idx_options* opt) {
+    if (rows <= 0 || topk < 1 || topk > kMaxTopk) return 0;
+    if (max_len <= 0 || max_len > keys) max_len = keys;
+    if (idx_route_fused(max_len, topk))
+        return idx_score_topk_workspace(rows, keys, max_len, H, D, topk, dt, opt);
+    const long long stride = max_len > 0 ? max_len : 1;
+    return logits_bytes(rows, stride) + idx_topk_workspace(rows, stride, topk, opt);
+}
+
+idx_status idx_score_topk_routed(const void* q, const void* k, const float* k_scale,
+                                 const float* w, const int* ks, const int* ke, int rows,
+                                 long long keys, long long max_len, int H, int D, int topk,
+                                 idx_dtype dt, int* out_idx, void* ws, size_t ws_bytes,
+                                 const idx_options* opt, void* stream) {
+    if (topk < 1) return IDX_EINVAL;
+    if (topk > kMaxTopk) return IDX_EUNSUPPORTED;
+    const long long ml = (max_len <= 0 || max_len > keys) ? keys : max_len;
+    if (idx_route_fused(ml, topk))
+        return idx_score_topk(q, k, k_scale, w, ks, ke, rows, keys, max_len, H, D, topk, dt,
+                              out_idx, ws, ws_bytes, opt, stream);
+    // dense route: the logits [rows, max_len] in the workspace, then their top-k
+    idx_status st = check_indexer_args(q, k, k_scale, w, ks, ke, rows, keys, H, D, dt);
+    if (st != IDX_OK || rows == 0) return st;
+    if (!out_idx) return IDX_EINVAL;
+    if (!aligned(out_idx, 4)) return IDX_EALIGN;
+    const long long stride = ml > 0 ? ml : 1;
+    const size_t lb = logits_bytes(rows, stride);
+    const size_t need = lb + idx_topk_workspace(rows, stride, topk, opt);
+    if (!ws || ws_bytes < need) return IDX_EWORKSPACE;
+    if (!aligned(ws, 256)) return IDX_EALIGN;
+    idx_options o;
+    std::memset(&o, 0, sizeof(o));
+    if (opt) o = *opt;
+    o.stage_events = nullptr;  // the stage boundaries are recorded here
+    o.relative_rows = 1;       // the logits start at column 0 of each row
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    record(opt, 0, s);
+    record(opt, 1, s);
+    st = idx_score_materialise(q, k, k_scale, w, ks, ke, rows, keys, H, D, dt,
+                               reinterpret_cast<float*>(base), stride, &o, stream);
+    if (st != IDX_OK) return st;
+    record(opt, 2, s);
+    st = idx_topk_from_scores(reinterpret_cast<const float*>(base), stride, ks, ke, rows, topk,
+                              out_idx, base + lb, ws_bytes - lb, &o, stream);
+    record(opt, 3, s);
+    record(opt, 4, s);
+    return st;
 }
 
 idx_status idx_page_table_transform(int* idx_out, int rows, int topk, const int* table,
