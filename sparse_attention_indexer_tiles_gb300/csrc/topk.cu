@@ -22,6 +22,8 @@
 
 namespace idx {
 
+void count_launches(unsigned n);  // api.cu
+
 constexpr int kTieCap = 4096;
 constexpr int kCandScratch = 96;  // scan words + row state of cand_topk_kernel
 
@@ -470,6 +472,9 @@ topk_rows_kernel(TopkRowsArgs a) {
 // warp per row finds the exact t-th largest order key with four 8-bit radix
 // passes over the sample (a warp-private 256-bin histogram each), reading the
 // sample from L2; no block-wide synchronisation.
+// Samples longer than this go to sample_threshold_cta_kernel.
+constexpr long long kThrCtaMin = 8192;
+
 template <int WARPS>
 __global__ void __launch_bounds__(WARPS * 32)
 sample_threshold_kernel(TopkRowsArgs a) {
@@ -493,6 +498,7 @@ sample_threshold_kernel(TopkRowsArgs a) {
         }
         return;
     }
+    if (a.split > 1 && n > kThrCtaMin) return;  // a whole CTA takes this row
     double t = ceil((double)n * (double)a.target * (double)a.topk / (double)len);
     if (t < 1.0) t = 1.0;
     if (t > (double)n) t = (double)n;
@@ -553,6 +559,43 @@ sample_threshold_kernel(TopkRowsArgs a) {
         // a failed pick leaves thr = 0: every key a candidate, the slab
         // overflows and the exact rescan takes the row
         plan->thr = ok ? prefix : 0u;
+        plan->idx_cut = kAllIdx;
+        plan->state = ST_MAIN;
+    }
+}
+
+// The same threshold for long samples (tens of thousands of scores per row):
+// one 256-thread CTA per row, a 12-bit histogram pass over the sample, then
+// the values of the threshold bin gathered into shared memory and refined
+// there (further passes over the sample only if that bin holds more than
+// 4096), i.e. two passes over the sample instead of four.
+constexpr int kThrCtaThreads = 256;
+constexpr size_t kThrCtaSmem = (kHistBins + 64 + 2 * (size_t)kTieCap) * sizeof(uint32_t);
+
+__global__ void __launch_bounds__(kThrCtaThreads) sample_threshold_cta_kernel(TopkRowsArgs a) {
+    extern __shared__ __align__(16) uint32_t smem[];
+    uint32_t* hist = smem;
+    uint32_t* scratch = hist + kHistBins;
+    uint32_t* tkey = scratch + 64;
+    uint32_t* tpos = tkey + kTieCap;
+    const int r = blockIdx.x;
+    RowPlan* plan = a.plan + r;
+    const long long vks = a.vis_ks[r], vke = a.vis_ke[r];
+    const long long len = vke - vks;
+    const long long phase = hash32((uint32_t)(r / a.rows_per_block) ^ a.phase_seed) % a.S;
+    const SampleSpan sp = sample_span(vks, vke, phase, a.S, a.nsamp);
+    const long long n = sp.b - sp.a;
+    // rows the warp kernel handled (short samples, or no sampling at all)
+    if (len <= a.cap || n <= kThrCtaMin || n > a.row_len) return;
+    double t = ceil((double)n * (double)a.target * (double)a.topk / (double)len);
+    if (t < 1.0) t = 1.0;
+    if (t > (double)n) t = (double)n;
+    const RowView v = make_view(a.scores + (long long)r * a.row_stride, n);
+    int rescans = 0;
+    const Threshold th =
+        find_threshold<kThrCtaThreads, 4>(v, (uint32_t)t, hist, tkey, tpos, scratch, &rescans);
+    if (threadIdx.x == 0) {
+        plan->thr = th.key;
         plan->idx_cut = kAllIdx;
         plan->state = ST_MAIN;
     }
@@ -963,8 +1006,21 @@ cudaError_t launch_topk_rows(const TopkRowsArgs& a, cudaStream_t s) {
     constexpr size_t SMEM = StreamSmem<T>::BYTES;
     if (a.rows == 0) return cudaSuccess;
     if (a.mode == TOPK_THRESHOLD) {
+        // one warp per row; when some row's sample may exceed kThrCtaMin
+        // scores, those rows are left to one CTA each (two passes over the
+        // sample instead of four), flagged to the warp kernel by split = 2
         constexpr int WARPS = 8;
-        sample_threshold_kernel<WARPS><<<(a.rows + WARPS - 1) / WARPS, WARPS * 32, 0, s>>>(a);
+        TopkRowsArgs b = a;
+        b.split = a.row_len > kThrCtaMin ? 2 : 0;
+        sample_threshold_kernel<WARPS><<<(a.rows + WARPS - 1) / WARPS, WARPS * 32, 0, s>>>(b);
+        if (b.split) {
+            static cudaError_t attr = cudaFuncSetAttribute(
+                sample_threshold_cta_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                (int)kThrCtaSmem);
+            if (attr != cudaSuccess) return attr;
+            sample_threshold_cta_kernel<<<a.rows, kThrCtaThreads, kThrCtaSmem, s>>>(b);
+            count_launches(1);
+        }
         return cudaGetLastError();
     }
     if (a.split > 1) {
