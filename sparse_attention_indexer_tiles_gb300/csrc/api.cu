@@ -175,7 +175,7 @@ struct FusedLayout {
     long long samp_stride;
 };
 
-FusedLayout fused_layout(int rows, long long max_len, int cap, int cap_q, int S) {
+FusedLayout fused_layout(int rows, long long max_len, int cap, int cap_q, int S, int nruns) {
     FusedLayout L;
     size_t off = 0;
     auto take = [&](size_t bytes) {
@@ -185,9 +185,9 @@ FusedLayout fused_layout(int rows, long long max_len, int cap, int cap_q, int S)
     };
     L.samp_stride = max_len / S + 2;
     L.plan = take((size_t)rows * sizeof(RowPlan));
-    L.run_cnt = take((size_t)rows * kRuns * sizeof(int));
-    L.slab_s = take((size_t)rows * kRuns * cap_q * sizeof(float));
-    L.slab_i = take((size_t)rows * kRuns * cap_q * sizeof(int));
+    L.run_cnt = take((size_t)rows * nruns * sizeof(int));
+    L.slab_s = take((size_t)rows * nruns * cap_q * sizeof(float));
+    L.slab_i = take((size_t)rows * nruns * cap_q * sizeof(int));
     L.samp = take(max_len > cap ? (size_t)rows * L.samp_stride * sizeof(float) : 0);
     L.fb_hist = take(max_len > cap ? (size_t)rows * 4096 * sizeof(uint32_t) : 0);
     L.fb_cnt = take(8 * sizeof(int));
@@ -230,7 +230,33 @@ ScoreLaunch make_score_launch(const void* q, const void* k, const float* k_scale
     L.a.topk = topk;
     L.a.d_status = opt ? opt->d_status : nullptr;
     L.a.d_stats = opt ? opt->d_stats : nullptr;
+    L.a.ksplit = 1;
+    L.a.nruns = kRuns;
     return L;
+}
+
+// Key splits of a scoring launch: the CTAs of one wave are SM-count many, so
+// a grid of nblk row blocks leaves the last wave partly idle; splitting every
+// block's key tiles into k contiguous parts (grid.y = k) is taken for the
+// smallest k <= 8 whose grid fills its last wave to >= 95 %, or the best k
+// found, as long as every part keeps >= 64 tiles.
+int score_ksplit(int rows, int H, long long max_len) {
+    const int nblk = (rows + score_rows_per_block(H) - 1) / score_rows_per_block(H);
+    const long long tiles = (max_len + 127) / 128;
+    const double sm = (double)sm_count();
+    int best = 1;
+    double best_eff = 0.0;
+    for (int k = 1; k <= 8; ++k) {
+        if (k > 1 && tiles / k < 64) break;
+        const double waves = nblk * (double)k / sm;
+        const double eff = waves / std::ceil(waves);
+        if (eff >= 0.95) return k;
+        if (eff > best_eff + 1e-9) {
+            best_eff = eff;
+            best = k;
+        }
+    }
+    return best;
 }
 
 void record(const idx_options* opt, int i, cudaStream_t s) {
@@ -276,7 +302,8 @@ size_t idx_score_topk_workspace(int rows, long long keys, long long max_len, int
     if (rows <= 0 || topk < 1 || topk > kMaxTopk) return 0;
     if (max_len <= 0 || max_len > keys) max_len = keys;
     const FusedParams p = fused_params(topk, opt);
-    return fused_layout(rows, max_len, p.cap, p.cap_q, p.S).total;
+    const int nruns = kRuns * score_ksplit(rows, H, max_len);
+    return fused_layout(rows, max_len, p.cap, p.cap_q, p.S, nruns).total;
 }
 
 idx_status idx_score_topk(const void* q, const void* k, const float* k_scale, const float* w,
@@ -292,7 +319,9 @@ idx_status idx_score_topk(const void* q, const void* k, const float* k_scale, co
     if (max_len <= 0 || max_len > keys) max_len = keys;
     const FusedParams p = fused_params(topk, opt);
     if (p.cap > kMaxCap || p.S < 1) return IDX_EUNSUPPORTED;
-    const FusedLayout lay = fused_layout(rows, max_len, p.cap, p.cap_q, p.S);
+    const int ksplit = score_ksplit(rows, H, max_len);
+    const int nruns = kRuns * ksplit;
+    const FusedLayout lay = fused_layout(rows, max_len, p.cap, p.cap_q, p.S, nruns);
     if (!ws || ws_bytes < lay.total) return IDX_EWORKSPACE;
     if (!aligned(ws, 256)) return IDX_EALIGN;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -314,6 +343,7 @@ idx_status idx_score_topk(const void* q, const void* k, const float* k_scale, co
     L.a.slab_i = slab_i;
     L.a.cap = p.cap;
     L.a.cap_q = p.cap_q;
+    L.a.nruns = nruns;
     L.a.run_cnt = run_cnt;
     L.a.fb_hist = fb_hist;
     L.a.fb_cnt = fb_cnt;
@@ -355,8 +385,11 @@ idx_status idx_score_topk(const void* q, const void* k, const float* k_scale, co
     }
     record(opt, 1, s);
     // 3. one scoring pass emits every key at or above T_r into the slab
+    //    (key splits write runs of their own)
     L.a.mode = SM_EMIT;
+    L.a.ksplit = ksplit;
     if ((e = launch_score(L, s)) != cudaSuccess) return cuda_status(e);
+    L.a.ksplit = 1;
     record(opt, 2, s);
     // 4. exact top-k of every slab; rows whose count missed [topk, cap] are flagged
     CandArgs c;
@@ -365,6 +398,7 @@ idx_status idx_score_topk(const void* q, const void* k, const float* k_scale, co
     c.slab_i = slab_i;
     c.run_cnt = run_cnt;
     c.cap_q = p.cap_q;
+    c.nruns = nruns;
     c.plan = plan;
     c.fb_hist = sampling ? fb_hist : nullptr;
     c.fb_cnt = fb_cnt;
@@ -463,6 +497,7 @@ idx_status idx_score_materialise(const void* q, const void* k, const float* k_sc
     L.a.mode = SM_MATERIALISE;
     L.a.out = scores;
     L.a.out_stride = row_stride;
+    L.a.ksplit = score_ksplit(rows, H, std::min<long long>(keys, row_stride));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     record(opt, 0, s);
     const cudaError_t e = launch_score(L, s);

@@ -43,8 +43,11 @@ struct ScoreArgs {
     float* slab_s;
     int* slab_i;
     int cap;              // nominal slab cap (rows seeing <= cap keys emit every key)
-    int cap_q;            // capacity of one warp run: slab row = kRuns runs of cap_q
-    int* run_cnt;         // [rows, kRuns] candidates appended per run (may exceed cap_q)
+    int cap_q;            // capacity of one warp run: slab row = nruns runs of cap_q
+    int* run_cnt;         // [rows, nruns] candidates appended per run (may exceed cap_q)
+    int nruns;            // runs per row: kRuns per key split of the main emit pass
+    int ksplit;           // key splits of this launch (grid.y): CTA (b, c) scores the
+                          // c-th contiguous part of row block b's key tiles
     uint32_t* fb_hist;
     int* fb_cnt;          // [8] rows waiting per rescan level, [6] ready to emit
     int level;

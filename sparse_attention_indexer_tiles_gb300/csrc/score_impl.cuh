@@ -122,7 +122,10 @@ IDX_DEVI float head_reduce_quad(uint32_t taddr, const float2* wq) {
     return (b1 ? k1 : k0) + rx;
 }
 
-template <int DT, int H, int RB>
+// SPLIT: the launch splits row blocks over key ranges (grid.y) or addresses a
+// slab with more than kRuns runs per row; without it the kernel is compiled
+// with kRuns runs per row and no split arithmetic.
+template <int DT, int H, int RB, bool SPLIT>
 __global__ void __launch_bounds__(ScoreCfg<DT, H, RB>::THREADS, 1)
 score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
              const __grid_constant__ CUtensorMap tm_ks, const __grid_constant__ ScoreArgs a) {
@@ -210,6 +213,10 @@ score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             }
         }
         if (!active) lo = hi = 0;
+        // the re-emission (one launch over whole rows) leaves the runs of the
+        // main pass's other key splits empty
+        if (SPLIT && mode == SM_FB_EMIT && active)
+            for (int c = kRuns; c < a.nruns; ++c) a.run_cnt[(long long)r * a.nruns + c] = 0;
         m[MW_ACTIVE] = active;
         m[MW_LO] = lo;
         m[MW_HI] = hi;
@@ -246,8 +253,17 @@ score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             t0 = lo / C::M;
             nt = (hi + C::M - 1) / C::M - t0;
         }
-        misc[0] = t0;
-        misc[1] = nt;
+        if (SPLIT) {
+            // key split c of gridDim.y: a contiguous part of the block's tiles
+            const int per = (nt + (int)gridDim.y - 1) / (int)gridDim.y;
+            const int ts = (int)blockIdx.y * per;
+            const int te = ts + per < nt ? ts + per : nt;
+            misc[0] = t0 + ts;
+            misc[1] = te > ts ? te - ts : 0;
+        } else {
+            misc[0] = t0;
+            misc[1] = nt;
+        }
         *abort_flag = 0;
         for (int i = 0; i < C::NS; ++i) {
             mbar_init(&full[i], 1);
@@ -263,7 +279,18 @@ score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     __syncthreads();
     const int t0 = misc[0];
     const int ntiles = misc[1];
-    if (ntiles == 0) return;  // no active row in this block
+    if (ntiles == 0) {
+        // nothing to score in this part; its runs of the active rows are empty
+        if (SPLIT && mode == SM_EMIT) {
+            for (int i = tid; i < C::R * kRuns; i += C::THREADS) {
+                const int rr = i / kRuns;
+                if (meta[rr * C::META_WORDS + MW_ACTIVE])
+                    a.run_cnt[(long long)(r0 + rr) * a.nruns + (int)blockIdx.y * kRuns +
+                              i % kRuns] = 0;
+            }
+        }
+        return;
+    }
 
     if (warp == 1) {
         __syncwarp();
@@ -366,7 +393,7 @@ score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         const int team = e >> 3;             // TMEM buffer and tile parity
         const int q = warp & 3;              // TMEM lane quarter
         const int grp = (e >> 2) & 1;        // half of the rows
-        const int run = q * 2 + team;        // candidate run of this warp
+        const int run = q * 2 + team;        // candidate run of this warp (in its key split)
         // lanes whose key comes earlier (candidates are appended in key order)
         uint32_t lt = 0u;
 #pragma unroll
@@ -391,10 +418,12 @@ score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             }
         }
         // this warp's runs of its rows: row j's run at ps/pi + j * rstride
-        const long long rb = (long long)(r0 + grp * C::RG) * kRuns + run;
+        const int nruns = SPLIT ? a.nruns : kRuns;
+        const int split_run0 = SPLIT ? (int)blockIdx.y * kRuns : 0;
+        const long long rb = (long long)(r0 + grp * C::RG) * nruns + split_run0 + run;
         float* const ps = a.slab_s ? a.slab_s + rb * a.cap_q : nullptr;
         int* const pi = a.slab_i ? a.slab_i + rb * a.cap_q : nullptr;
-        const int rstride = kRuns * a.cap_q;
+        const int rstride = nruns * a.cap_q;
 #define RLO(j) row_word(j, MW_LO)
 #define RHI(j) row_word(j, MW_HI)
 #define RKS(j) row_word(j, MW_KS)
@@ -545,7 +574,7 @@ score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             for (int j = 0; j < C::RG; ++j) {
                 const int rr = grp * C::RG + j;
                 if (meta[rr * C::META_WORDS + MW_ACTIVE])
-                    a.run_cnt[(long long)(r0 + rr) * kRuns + run] = cnt[j];
+                    a.run_cnt[(long long)(r0 + rr) * nruns + split_run0 + run] = cnt[j];
             }
         }
     }

@@ -67,15 +67,20 @@ cudaError_t launch_score_t(const ScoreLaunch& L, cudaStream_t s) {
     } else {
         tks = tk;
     }
-    auto kern = score_kernel<DT, H, RB>;
+    const bool split = a.ksplit > 1 || a.nruns != kRuns;
+    auto kern = split ? score_kernel<DT, H, RB, true> : score_kernel<DT, H, RB, false>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
-        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        C::SMEM_ALLOC);
+        attr_err = cudaFuncSetAttribute(score_kernel<DT, H, RB, false>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+        if (attr_err == cudaSuccess)
+            attr_err = cudaFuncSetAttribute(score_kernel<DT, H, RB, true>,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            C::SMEM_ALLOC);
     });
     if (attr_err != cudaSuccess) return attr_err;
-    const unsigned grid = (unsigned)((a.rows + C::R - 1) / C::R);
+    const dim3 grid((unsigned)((a.rows + C::R - 1) / C::R), (unsigned)(a.ksplit > 1 ? a.ksplit : 1));
     kern<<<grid, C::THREADS, C::SMEM_ALLOC, s>>>(tq, tk, tks, a);
     return cudaGetLastError();
 }

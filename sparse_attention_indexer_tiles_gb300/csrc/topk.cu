@@ -833,12 +833,13 @@ __global__ void __launch_bounds__(kCandThreads)
 cand_topk_kernel(CandArgs a) {
     constexpr int THREADS = kCandThreads;
     extern __shared__ __align__(16) uint32_t smem[];
-    const int CR = kRuns * a.cap_q;
+    const int CR = a.nruns * a.cap_q;          // slab row (all key splits)
+    const int CS = kRuns * a.cap_q;            // candidates held in shared memory
     uint32_t* hist = smem;                     // [kCandWarps][256], later the bitmap
     uint32_t* scratch = hist + kBitmapWords;   // [0,35) scans; row state from 48 on
     uint32_t* keys = scratch + kCandScratch;
-    uint32_t* idxs = keys + CR;
-    uint32_t* run_off = scratch + 50;          // [kRuns + 1] run starts in keys[]
+    uint32_t* idxs = keys + CS;
+    uint32_t* run_off = idxs + CS;             // [nruns + 1] run starts in keys[]
 
     if (a.fallback && *(volatile int*)(a.fb_cnt + 6) == 0) return;  // no row was re-emitted
     for (int r = blockIdx.x; r < a.rows; r += gridDim.x) {
@@ -849,14 +850,17 @@ cand_topk_kernel(CandArgs a) {
         if (threadIdx.x == 0) {
             scratch[48] = (uint32_t)plan->state;
             uint32_t off = 0, total = 0, trunc = 0;
-            for (int q = 0; q < kRuns; ++q) {
-                const uint32_t c = (uint32_t)a.run_cnt[(long long)r * kRuns + q];
+            for (int q = 0; q < a.nruns; ++q) {
+                const uint32_t c = (uint32_t)a.run_cnt[(long long)r * a.nruns + q];
                 trunc |= c > (uint32_t)a.cap_q;
                 total += c;
                 run_off[q] = off;
                 off += c < (uint32_t)a.cap_q ? c : (uint32_t)a.cap_q;
             }
-            run_off[kRuns] = off;
+            // more candidates than shared memory holds (possible with key
+            // splits): the exact rescan takes the row
+            trunc |= off > (uint32_t)CS;
+            run_off[a.nruns] = off;
             scratch[49] = trunc;
             scratch[60] = total;
         }
@@ -906,7 +910,7 @@ cand_topk_kernel(CandArgs a) {
         // load the runs back to back, four independent loads per thread in flight
         const float* ss = a.slab_s + (long long)r * CR;
         const int* si = a.slab_i + (long long)r * CR;
-        const uint32_t cnt = run_off[kRuns];
+        const uint32_t cnt = run_off[a.nruns];
         for (uint32_t base = 0; base < cnt; base += 4 * THREADS) {
             float sv[4];
             int iv[4];
@@ -914,9 +918,19 @@ cand_topk_kernel(CandArgs a) {
             for (int u = 0; u < 4; ++u) {
                 const uint32_t e = base + u * THREADS + threadIdx.x;
                 if (e < cnt) {
+                    // the run holding entry e: the last q with run_off[q] <= e
                     int q = 0;
+                    if (a.nruns == kRuns) {
 #pragma unroll
-                    for (int j = 1; j < kRuns; ++j) q += e >= run_off[j];
+                        for (int j = 1; j < kRuns; ++j) q += e >= run_off[j];
+                    } else {
+                        int hi = a.nruns;
+                        while (hi - q > 1) {
+                            const int mid = (q + hi) >> 1;
+                            if (run_off[mid] <= e) q = mid;
+                            else hi = mid;
+                        }
+                    }
                     const uint32_t src = (uint32_t)q * (uint32_t)a.cap_q + (e - run_off[q]);
                     sv[u] = ss[src];
                     iv[u] = si[src];
@@ -1053,13 +1067,13 @@ size_t split_workspace_bytes(int rows, int g) {
     return slots * (size_t)kSplitCap * 2 * sizeof(uint32_t) + slots * sizeof(int) + 256;
 }
 
-size_t cand_smem_bytes(int cap_q) {
-    return (kBitmapWords + kCandScratch) * sizeof(uint32_t) +
+size_t cand_smem_bytes(int cap_q, int nruns) {
+    return (kBitmapWords + kCandScratch + (size_t)nruns + 1) * sizeof(uint32_t) +
            (size_t)cap_q * kRuns * 2 * sizeof(uint32_t);
 }
 
 cudaError_t launch_cand_topk(const CandArgs& a, cudaStream_t s) {
-    const size_t sm = cand_smem_bytes(a.cap_q);
+    const size_t sm = cand_smem_bytes(a.cap_q, a.nruns);
     cudaError_t e =
         cudaFuncSetAttribute(cand_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e != cudaSuccess) return e;

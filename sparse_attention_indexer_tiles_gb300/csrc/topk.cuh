@@ -46,9 +46,10 @@ struct TopkRowsArgs {
 };
 
 struct CandArgs {
-    const float* slab_s;  // [rows, kRuns, cap_q]
-    const int* slab_i;    // [rows, kRuns, cap_q]
-    const int* run_cnt;   // [rows, kRuns]
+    const float* slab_s;  // [rows, nruns, cap_q]
+    const int* slab_i;    // [rows, nruns, cap_q]
+    const int* run_cnt;   // [rows, nruns]
+    int nruns;            // kRuns per key split of the emit pass
     int cap_q;
     RowPlan* plan;
     uint32_t* fb_hist;    // [rows, 4096]
@@ -66,7 +67,7 @@ struct CandArgs {
 
 cudaError_t launch_topk_rows(const TopkRowsArgs& a, cudaStream_t s);
 cudaError_t launch_cand_topk(const CandArgs& a, cudaStream_t s);
-size_t cand_smem_bytes(int cap_q);
+size_t cand_smem_bytes(int cap_q, int nruns);
 size_t split_workspace_bytes(int rows, int g);
 
 }  // namespace idx

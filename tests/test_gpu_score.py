@@ -233,3 +233,32 @@ def test_mixed_batch_workload(idx):
     assert short.size > 0
     for r in short:
         assert got[r].tolist() == list(range(n[r])) + [-1] * (inp.topk - n[r])
+
+
+# ------------------------------------------------------ decode-like shapes
+
+@pytest.mark.parametrize("knob", [{}, {"target_factor": 30.0}, {"target_factor": 0.3}])
+def test_few_rows_long_keys_key_split(idx, knob):
+    """12 rows over 150000 keys (three row blocks): the scoring launches split
+    every block's keys over up to eight CTAs, each with runs of its own; the
+    rescan (forced by the knobs) re-emits over whole rows."""
+    inp = synth.indexer_inputs(12, 150000, 64, 128, 512, "fp8", seed=48, ranges="full")
+    stats = idx.Stats(torch.device(DEV))
+    got = fused(idx, inp, stats=stats, **knob)
+    assert np.array_equal(got, two_pass(idx, inp))
+    check_fused(inp, got, rows=[0, 5, 11])
+    st = stats.read()
+    assert st["status"] == 0
+    if knob:
+        assert st["fallback_rows"] == 12
+
+
+def test_materialise_few_rows_long_keys(idx):
+    ks = torch.tensor([0, 1000, 0, 77], dtype=torch.int32)
+    ke = torch.tensor([90000, 90000, 45000, 89999], dtype=torch.int32)
+    inp = synth.indexer_inputs(4, 90000, 32, 128, 16, "fp8", seed=49, ranges="given", ks=ks, ke=ke)
+    got = materialise(idx, inp)
+    _, sc = oracle.score_topk(inp, rows=[0, 2], want_scores=True)
+    for i, r in enumerate([0, 2]):
+        n = int(ke[r] - ks[r])
+        check_scores(got[r, :n], sc[i, :n])
