@@ -164,9 +164,19 @@ def cpu_baseline_sample(inp, target_s: float = 10.0, seed: int = 7):
     oracle.score_topk(inp, rows=rows, nthreads=threads)
     wall = time.perf_counter() - t0
     pairs = int(n_all[rows].sum())
+    # the oracle's selection alone on the standalone top-k workload (given scores)
+    si = synth.workload("standalone_topk")
+    trows = synth.sample_rows(si.ks, si.ke, 4 * threads, seed + 2)
+    t0 = time.perf_counter()
+    oracle.topk_from_scores(si.scores, si.ks, si.ke, si.topk, rows=trows, nthreads=threads)
+    twall = time.perf_counter() - t0
     return {"value": pairs / wall, "unit": "pairs/s", "cores": threads, "kind": "oracle",
             "sample": f"{len(rows)} seeded rows of the workload ({pairs} pairs), fp64 scores "
-                      f"+ full-sort top-k, {wall:.1f} s wall"}
+                      f"+ full-sort top-k, {wall:.1f} s wall",
+            "core_us_per_row": wall / len(rows) * threads * 1e6,
+            "standalone_topk_rows_per_s": len(trows) / twall,
+            "standalone_topk_sample": f"{len(trows)} seeded rows of standalone_topk (131072 "
+                                      f"scores each), full sort, {twall:.2f} s wall"}
 
 
 def run_reference(args, rank, world):
@@ -436,7 +446,7 @@ def secondary(idx, dev, g, inp, out, ws, flush, pk, args):
 
     res["standalone_topk"] = standalone_topk(idx, dev, flush, pk, args)
     res["split_topk"] = split_topk(idx, dev, flush, pk, args)
-    for name in ("long_context", "mixed_batch"):
+    for name in ("long_context", "mixed_batch", "tiny"):
         res[name] = other_fused(idx, dev, flush, pk, args, name)
         torch.cuda.empty_cache()
     res["page_table_transform"] = page_transform(idx, dev, flush, pk, out, inp)
@@ -548,7 +558,8 @@ def other_fused(idx, dev, flush, pk, args, name):
     emit_ms = statistics.mean(e.elapsed(1, 2) for e in evs)
     pairs = inp.pairs()
     flops = 2.0 * inp.H * inp.D * pairs
-    peak = 2.0 * pk["bf16_tflops"]
+    # fp8 dense = 2 x bf16 dense (nominal ratio); bf16 inputs run at the bf16 peak
+    peak = pk["bf16_tflops"] * (1.0 if inp.q.dtype == torch.bfloat16 else 2.0)
     emit_tf = flops / (emit_ms * 1e-3) / 1e12
     return {"workload": f"{name}: rows={inp.rows} keys={inp.keys} H={inp.H} D={inp.D} "
                         f"topk={inp.topk}",
