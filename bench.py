@@ -47,6 +47,10 @@ def parse():
     p.add_argument("--clocks-file", default=None)
     p.add_argument("--rows", type=int, default=0,
                    help="profiling: use only the last N query rows of the workload")
+    p.add_argument("--workload", default=WORKLOAD,
+                   choices=["fused_prefill", "long_context", "mixed_batch", "tiny"],
+                   help="fused workload of the main line (default: the one the metric is "
+                        "quoted on)")
     p.add_argument("--route-sweep", action="store_true",
                    help="time the fused and the two-pass path over short key lengths (the "
                         "routing gate's crossover) and print one JSON line per case")
@@ -185,7 +189,7 @@ def run_reference(args, rank, world):
         return
     import oracle
     import synth
-    inp = synth.workload(WORKLOAD)
+    inp = synth.workload(args.workload)
     threads = oracle.default_threads()
     n_all = (inp.ke - inp.ks).clamp_min(0).long()
     per_step_rows = max(threads, 16)
@@ -205,7 +209,7 @@ def run_reference(args, rank, world):
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": config_block(inp),
+            "config": config_block(inp, args.workload),
             "cpu_baseline": {"value": value, "unit": "pairs/s", "cores": threads,
                              "kind": "oracle",
                              "sample": f"{per_step_rows} seeded rows per step of the workload"},
@@ -232,12 +236,18 @@ def job_throughput(units_per_rank: int, world: int, ms: float) -> float:
     return world * units_per_rank / (ms * 1e-3)
 
 
-def config_block(inp):
-    return {"workload": f"{WORKLOAD}: rows={inp.rows} keys={inp.keys} H={inp.H} D={inp.D} "
-                        f"topk={inp.topk} fp8 e4m3 q/k, per-key scale U(0.5,2), causal",
+def config_block(inp, name):
+    dt = "bf16" if inp.q.dtype == torch_bf16() else "fp8 e4m3"
+    return {"workload": f"{name}: rows={inp.rows} keys={inp.keys} H={inp.H} D={inp.D} "
+                        f"topk={inp.topk} {dt} q/k, {inp.meta.get('ranges', 'given')} ranges",
             "rows": inp.rows, "keys": inp.keys, "heads": inp.H, "dim": inp.D, "topk": inp.topk,
             "pairs_per_step": inp.pairs(),
             "l2": "flushed between timed steps (256 MiB write outside the events)"}
+
+
+def torch_bf16():
+    import torch
+    return torch.bfloat16
 
 
 def main():
@@ -279,7 +289,7 @@ def main():
         return
 
     # ---------------------------------------------------------------- inputs
-    inp = synth.workload(WORKLOAD)
+    inp = synth.workload(args.workload)
     if args.rows:
         inp = last_rows(inp, args.rows)
     g = {n: getattr(inp, n).to(dev) for n in ("q", "k", "k_scale", "w", "ks", "ke")}
@@ -336,14 +346,18 @@ def main():
     # --------------------------------------------------------------- roofline
     flops = 2.0 * inp.H * inp.D * pairs
     emit_s = statistics.mean(emit_ms) * 1e-3
-    fp8_peak = 2.0 * pk["bf16_tflops"]  # fp8 dense = 2 x bf16 dense (nominal ratio)
+    # fp8 dense = 2 x bf16 dense (nominal ratio); bf16 inputs run at the bf16 peak
+    bf16_in = inp.q.dtype == torch.bfloat16
+    fp8_peak = pk["bf16_tflops"] * (1.0 if bf16_in else 2.0)
     achieved = flops / emit_s / 1e12
-    traffic = recorded_traffic("score_kernel<fp8,H64,D128> emit", WORKLOAD)
+    kname = f"score_kernel<{'bf16' if bf16_in else 'fp8'},H{inp.H},D{inp.D}> emit"
+    traffic = recorded_traffic(kname, args.workload)
     roofline = {"bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
                 "frac": achieved / fp8_peak, "traffic": traffic,
-                "kernel": "score_kernel<fp8,H64,D128> emit pass",
+                "kernel": kname + " pass",
                 "algorithmic": f"2*H*D flop per visible pair = {flops:.4g} flop per launch",
-                "peak_note": f"{pk['source']} bf16 {pk['bf16_tflops']} TFLOP/s x 2 for fp8"}
+                "peak_note": f"{pk['source']} bf16 {pk['bf16_tflops']} TFLOP/s"
+                             f"{'' if bf16_in else ' x 2 for fp8'}"}
     whole_frac = flops / (ms * 1e-3) / 1e12 / fp8_peak
 
     # ------------------------------------------------------------ end to end
@@ -372,7 +386,8 @@ def main():
     line = {"metric": METRIC, "value": value, "unit": "pairs/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "e4m3", "data": "synthetic", "config": config_block(inp),
+            "dtype": "bf16" if bf16_in else "e4m3", "data": "synthetic",
+            "config": config_block(inp, args.workload),
             "roofline": roofline, "whole_step_tensor_frac": whole_frac,
             "stage_ms": stage_ms, "path_stats": path_stats,
             "e2e": {"value": e2e_val, "unit": "pairs/s", "h2d_bytes_per_step": h2d,
