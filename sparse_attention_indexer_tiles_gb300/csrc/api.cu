@@ -236,26 +236,23 @@ ScoreLaunch make_score_launch(const void* q, const void* k, const float* k_scale
 }
 
 // Key splits of a scoring launch: the CTAs of one wave are SM-count many, so
-// a grid of nblk row blocks leaves the last wave partly idle; splitting every
-// block's key tiles into k contiguous parts (grid.y = k) is taken for the
-// smallest k <= 8 whose grid fills its last wave to >= 95 %, or the best k
-// found, as long as every part keeps >= 64 tiles.
+// a grid of nblk row blocks leaves the last wave partly idle.  When the
+// unsplit grid fills its last wave to less than 90 %, every block's key tiles
+// are split into k contiguous parts (grid.y = k), k <= 6 the one that fills
+// the last wave best (the smaller k within 1 %), every part keeping >= 64
+// tiles.  Each split of the emit pass adds kRuns runs per row to the slab.
 int score_ksplit(int rows, int H, long long max_len) {
     const int nblk = (rows + score_rows_per_block(H) - 1) / score_rows_per_block(H);
     const long long tiles = (max_len + 127) / 128;
     const double sm = (double)sm_count();
-    int best = 1;
-    double best_eff = 0.0;
-    for (int k = 1; k <= 8; ++k) {
-        if (k > 1 && tiles / k < 64) break;
+    auto eff = [&](int k) {
         const double waves = nblk * (double)k / sm;
-        const double eff = waves / std::ceil(waves);
-        if (eff >= 0.95) return k;
-        if (eff > best_eff + 1e-9) {
-            best_eff = eff;
-            best = k;
-        }
-    }
+        return waves / std::ceil(waves);
+    };
+    if (eff(1) >= 0.9) return 1;
+    int best = 1;
+    for (int k = 2; k <= 6 && tiles / k >= 64; ++k)
+        if (eff(k) > eff(best) + 0.01) best = k;
     return best;
 }
 
