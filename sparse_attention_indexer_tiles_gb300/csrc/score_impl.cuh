@@ -2,8 +2,7 @@
 //
 // Page "[sglang] logits를 쓰지 않는 top-k", section 1: a KV tile is the A
 // operand (M = keys) of the tensor-core MMA, the accumulator lives in TMEM,
-// every epilogue thread owns one key of the tile and reduces the heads in
-// registers.  Here:
+// and the heads are reduced per key in registers.  Here:
 //   A = 128 keys x D        (TMA, 128/64-byte swizzle, a ring of stages)
 //   B = 256 (row, head) x D (TMA, loaded once: rows_per_block = 256 / H rows)
 //   D = 128 x 256 fp32 in TMEM, double buffered (2 x 256 columns).
@@ -11,12 +10,19 @@
 // 4..19 = epilogue in two teams of 8 warps.  Team t owns TMEM buffer t and the
 // tiles i = t (mod 2), so one team reduces a tile while the other waits on
 // the tensor core or on its TMEM loads.  Inside a team a warp owns the TMEM
-// lane quarter warp % 4 (32 keys) and one of the two halves of the rows.
+// lane quarter warp % 4 (32 keys) and one of the two halves of the rows.  It
+// reads its accumulators in the 16x256b shape (four threads share a key, each
+// holding a quarter of the row's heads, whose weights stay in registers) and
+// two butterfly steps finish every key's sum.
 //
-// Score of (row, key), heads summed in fp32 as eight partial sums in a fixed
-// order:  s = k_scale[key] * sum_h w[row,h] * ReLU(acc[h]).
+// Score of (row, key), heads summed in fp32 in a fixed order:
+//   s = k_scale[key] * sum_h w[row,h] * ReLU(acc[h]).
 // Every mode runs the same arithmetic, so the fused path compares exactly the
 // scores that the materialising baseline writes.
+//
+// A launch may split every row block's key tiles into gridDim.y contiguous
+// parts (SPLIT instantiation); each part of the emit pass then fills runs of
+// its own.
 #pragma once
 
 #include "plan.cuh"
