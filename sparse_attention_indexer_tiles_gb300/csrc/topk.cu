@@ -247,6 +247,7 @@ IDX_DEVI void stream_collect(const RowView& v, uint32_t L, uint32_t* rkey, uint3
     const float Lf = key_floor_float(L);
     uint32_t* mk = rkey + w * kRunCap;
     uint32_t* mi = ridx + w * kRunCap;
+    const uint32_t lt = (1u << lane) - 1u;
     uint32_t cnt = 0;
     for (int base = s0; base < s1; base += 32 * UNROLL) {
         float4 f[UNROLL];
@@ -261,39 +262,39 @@ IDX_DEVI void stream_collect(const RowView& v, uint32_t L, uint32_t* rkey, uint3
         for (int u = 0; u < UNROLL; ++u) {
             const int sl = base + u * 32 + lane;
             const float e[4] = {f[u].x, f[u].y, f[u].z, f[u].w};
-            uint32_t hits = 0;
+            bool h[4];
             if (interior) {
 #pragma unroll
-                for (int c = 0; c < 4; ++c) hits |= (e[c] >= Lf ? 1u : 0u) << c;
+                for (int c = 0; c < 4; ++c) h[c] = e[c] >= Lf;
             } else {
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     const int p = 4 * sl + c - off;
-                    const bool h = sl < s1 && p >= 0 && p < n && (L == 0u || e[c] >= Lf);
-                    hits |= (h ? 1u : 0u) << c;
+                    h[c] = sl < s1 && p >= 0 && p < n && (L == 0u || e[c] >= Lf);
                 }
             }
-            if (!__any_sync(0xffffffffu, hits != 0)) continue;
-            // exclusive prefix of the hit counts over the lanes (index order)
-            const uint32_t mine = __popc(hits);
-            uint32_t incl = mine;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += t;
-            }
-            uint32_t pos = cnt + incl - mine;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                if ((hits >> c) & 1u) {
-                    if (pos < (uint32_t)kRunCap) {
-                        mk[pos] = fkey(e[c]);
-                        mi[pos] = static_cast<uint32_t>(4 * sl + c - off);
-                    }
-                    ++pos;
+            // one ballot per lane component: a hit's place in the run is the
+            // number of hits in lower lanes plus those of lower components
+            const uint32_t b0 = __ballot_sync(0xffffffffu, h[0]);
+            const uint32_t b1 = __ballot_sync(0xffffffffu, h[1]);
+            const uint32_t b2 = __ballot_sync(0xffffffffu, h[2]);
+            const uint32_t b3 = __ballot_sync(0xffffffffu, h[3]);
+            if ((b0 | b1 | b2 | b3) == 0u) continue;
+            uint32_t pos = cnt + __popc(b0 & lt) + __popc(b1 & lt) + __popc(b2 & lt) +
+                           __popc(b3 & lt);
+            cnt += __popc(b0) + __popc(b1) + __popc(b2) + __popc(b3);
+            uint32_t hits = (h[0] ? 1u : 0u) | (h[1] ? 2u : 0u) | (h[2] ? 4u : 0u) |
+                            (h[3] ? 8u : 0u);
+            while (hits) {  // per lane, one pass per hit (rarely more than one)
+                const int c = __ffs(hits) - 1;
+                const float xv = c == 0 ? e[0] : c == 1 ? e[1] : c == 2 ? e[2] : e[3];
+                if (pos < (uint32_t)kRunCap) {
+                    mk[pos] = fkey(xv);
+                    mi[pos] = static_cast<uint32_t>(4 * sl + c - off);
                 }
+                ++pos;
+                hits &= hits - 1u;
             }
-            cnt += __shfl_sync(0xffffffffu, incl, 31);
         }
     }
     if (lane == 0) rcnt[w] = cnt;
@@ -390,10 +391,19 @@ IDX_DEVI uint32_t estimate_lower_bound(const RowView& v, uint32_t k, uint32_t* h
     const long long n = v.n;
     const long long P = n < kPrefix ? n : kPrefix;
     const float* row = reinterpret_cast<const float*>(v.base) + v.off;
+    // all loads of the prefix are issued before the first atomic
+    constexpr int PER = (kPrefix + THREADS - 1) / THREADS;
+    float x[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        const long long p = threadIdx.x + (long long)i * THREADS;
+        x[i] = p < P ? __ldg(row + p) : 0.f;
+    }
     zero_shared<THREADS>(hist, kHistBins);
     __syncthreads();
-    for (long long p = threadIdx.x; p < P; p += THREADS)
-        atomicAdd(&hist[fkey(__ldg(row + p)) >> 20], 1u);
+#pragma unroll
+    for (int i = 0; i < PER; ++i)
+        if (threadIdx.x + (long long)i * THREADS < P) atomicAdd(&hist[fkey(x[i]) >> 20], 1u);
     __syncthreads();
     double tg = ceil(2.0 * (double)k * (double)P / (double)n);
     if (tg < 1.0) tg = 1.0;
