@@ -210,9 +210,11 @@ IDX_DEVI void ordered_output(const RowView& v, Threshold th, uint32_t k, int* ou
 // ------------------------------------------------------- one-pass path
 //
 // A row is streamed from HBM once.  A lower bound L on the threshold is
-// estimated from the 12-bit histogram of the row's first 4096 values (aiming at
-// about 2 k keys >= L); every key >= L is appended to its warp's run in shared
-// memory.  Warp w owns the contiguous slice w of the row and appends in index
+// estimated from the 12-bit histogram of a 4096-value sample (aiming at about
+// 2 k keys >= L): the first 256 values of each warp's slice, which the filter
+// loads first anyway.  Every key >= L is then appended to its warp's run in
+// shared memory, and the top digits of the appended keys are counted on the
+// way (level 0 of the refinement).  Warp w owns the contiguous slice w of the row and appends in index
 // order, so the runs, taken in warp order, list the candidates in ascending
 // index order.  The exact threshold is then refined over the candidates and an
 // ordered compaction writes the result.  When L was too high (fewer than k
@@ -232,22 +234,92 @@ struct StreamSmem {
         (kHistBins + 64 + 3 * W + 2 * (size_t)RUN_WORDS) * sizeof(uint32_t);
 };
 
+// One step of a warp's filter: lane `lane` holds the four values of float4
+// slot sl; every value >= L (key order; Lf is the float of L) is appended to
+// the warp's run in index order.  With HIST the 12-bit top digit of every hit
+// is counted in hist as well (level 0 of the refinement over the runs).
+template <bool HIST>
+IDX_DEVI void filter_step(const float4 f, int sl, bool interior, int s1, int n, int off,
+                          uint32_t L, float Lf, uint32_t lt, uint32_t& cnt, uint32_t* mk,
+                          uint32_t* mi, uint32_t* hist) {
+    const float e[4] = {f.x, f.y, f.z, f.w};
+    bool h[4];
+    if (interior) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) h[c] = e[c] >= Lf;
+    } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const int p = 4 * sl + c - off;
+            h[c] = sl < s1 && p >= 0 && p < n && (L == 0u || e[c] >= Lf);
+        }
+    }
+    const uint32_t hits = (h[0] ? 1u : 0u) | (h[1] ? 2u : 0u) | (h[2] ? 4u : 0u) |
+                          (h[3] ? 8u : 0u);
+    const uint32_t any = __ballot_sync(0xffffffffu, hits != 0u);
+    if (any == 0u) return;
+    if (!__any_sync(0xffffffffu, (hits & (hits - 1u)) != 0u)) {
+        // at most one hit per lane: its place is the number of lower lanes with a hit
+        if (hits) {
+            const uint32_t pos = cnt + __popc(any & lt);
+            const int c = __ffs(hits) - 1;
+            const uint32_t key = fkey(c == 0 ? e[0] : c == 1 ? e[1] : c == 2 ? e[2] : e[3]);
+            if (pos < (uint32_t)kRunCap) {
+                mk[pos] = key;
+                mi[pos] = static_cast<uint32_t>(4 * sl + c - off);
+            }
+            if (HIST) atomicAdd(&hist[key >> 20], 1u);
+        }
+        cnt += __popc(any);
+        return;
+    }
+    // some lane holds several hits: one ballot per lane component; a hit's
+    // place is the number of hits in lower lanes plus those of lower
+    // components in its own lane
+    const uint32_t b0 = __ballot_sync(0xffffffffu, h[0]);
+    const uint32_t b1 = __ballot_sync(0xffffffffu, h[1]);
+    const uint32_t b2 = __ballot_sync(0xffffffffu, h[2]);
+    const uint32_t b3 = __ballot_sync(0xffffffffu, h[3]);
+    uint32_t pos = cnt + __popc(b0 & lt) + __popc(b1 & lt) + __popc(b2 & lt) + __popc(b3 & lt);
+    cnt += __popc(b0) + __popc(b1) + __popc(b2) + __popc(b3);
+    uint32_t rest = hits;
+    while (rest) {
+        const int c = __ffs(rest) - 1;
+        const uint32_t key = fkey(c == 0 ? e[0] : c == 1 ? e[1] : c == 2 ? e[2] : e[3]);
+        if (pos < (uint32_t)kRunCap) {
+            mk[pos] = key;
+            mi[pos] = static_cast<uint32_t>(4 * sl + c - off);
+        }
+        if (HIST) atomicAdd(&hist[key >> 20], 1u);
+        ++pos;
+        rest &= rest - 1u;
+    }
+}
+
+// Warp w's contiguous slice [s0, s1) of the row's float4 slots.
+template <int THREADS>
+IDX_DEVI void warp_slice(const RowView& v, int w, int* s0, int* s1) {
+    constexpr int W = THREADS / 32;
+    const int nvec = (int)v.nvec;
+    const int seg = (nvec + W - 1) / W;
+    *s0 = w * seg;
+    *s1 = *s0 + seg < nvec ? *s0 + seg : nvec;
+}
+
 // Append every key >= L of warp w's slice to its run; returns through rcnt[w].
 // The hot loop compares floats; order keys are formed for the few hits only,
 // and element bounds are checked only in the row's first and last 16 bytes.
-template <int THREADS, int UNROLL>
+template <int THREADS, int UNROLL, bool HIST>
 IDX_DEVI void stream_collect(const RowView& v, uint32_t L, uint32_t* rkey, uint32_t* ridx,
-                             uint32_t* rcnt) {
-    constexpr int W = THREADS / 32;
+                             uint32_t* rcnt, uint32_t* hist) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int nvec = (int)v.nvec, n = (int)v.n, off = v.off;
-    const int seg = (nvec + W - 1) / W;
-    const int s0 = w * seg;
-    const int s1 = s0 + seg < nvec ? s0 + seg : nvec;
+    int s0, s1;
+    warp_slice<THREADS>(v, w, &s0, &s1);
     const float Lf = key_floor_float(L);
+    const uint32_t lt = (1u << lane) - 1u;
     uint32_t* mk = rkey + w * kRunCap;
     uint32_t* mi = ridx + w * kRunCap;
-    const uint32_t lt = (1u << lane) - 1u;
     uint32_t cnt = 0;
     for (int base = s0; base < s1; base += 32 * UNROLL) {
         float4 f[UNROLL];
@@ -259,48 +331,86 @@ IDX_DEVI void stream_collect(const RowView& v, uint32_t L, uint32_t* rkey, uint3
         // every slot of this step holds 4 visible values (warp-uniform)
         const bool interior = base >= 1 && base + 32 * UNROLL <= s1 && base + 32 * UNROLL < nvec;
 #pragma unroll
-        for (int u = 0; u < UNROLL; ++u) {
-            const int sl = base + u * 32 + lane;
-            const float e[4] = {f[u].x, f[u].y, f[u].z, f[u].w};
-            bool h[4];
-            if (interior) {
+        for (int u = 0; u < UNROLL; ++u)
+            filter_step<HIST>(f[u], base + u * 32 + lane, interior, s1, n, off, L, Lf, lt, cnt,
+                              mk, mi, hist);
+    }
+    if (lane == 0) rcnt[w] = cnt;
+}
+
+// The one-pass collection of a whole row by one CTA, lower bound included.
+// L is the lower edge of the 12-bit bin that holds about the 2 k P / n-th
+// largest of a sample of P values: the first two float4 slots of every lane
+// in the first step of every warp's slice (P = 4096 for 512 threads), values
+// the filter loads anyway.  hist leaves holding the top digits of the hits.
+template <int THREADS, int UNROLL>
+IDX_DEVI void stream_collect_estimate(const RowView& v, uint32_t k, uint32_t* hist,
+                                      uint32_t* scratch, uint32_t* rkey, uint32_t* ridx,
+                                      uint32_t* rcnt) {
+    constexpr int SAMPLE = 2;  // float4 slots per lane in the sample
+    static_assert(UNROLL >= SAMPLE, "the sample comes from the first step");
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int nvec = (int)v.nvec, n = (int)v.n, off = v.off;
+    int s0, s1;
+    warp_slice<THREADS>(v, w, &s0, &s1);
+    const uint32_t lt = (1u << lane) - 1u;
+    uint32_t* mk = rkey + w * kRunCap;
+    uint32_t* mi = ridx + w * kRunCap;
+    float4 f[UNROLL];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) h[c] = e[c] >= Lf;
-            } else {
+    for (int u = 0; u < UNROLL; ++u) {
+        const int sl = s0 + u * 32 + lane;
+        f[u] = sl < s1 ? ldg4(v.base + sl) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    zero_shared<THREADS>(hist, kHistBins);
+    if (threadIdx.x == 0) scratch[44] = 0u;
+    __syncthreads();
+    uint32_t ns = 0;
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const int p = 4 * sl + c - off;
-                    h[c] = sl < s1 && p >= 0 && p < n && (L == 0u || e[c] >= Lf);
-                }
-            }
-            // one ballot per lane component: a hit's place in the run is the
-            // number of hits in lower lanes plus those of lower components
-            const uint32_t b0 = __ballot_sync(0xffffffffu, h[0]);
-            const uint32_t b1 = __ballot_sync(0xffffffffu, h[1]);
-            const uint32_t b2 = __ballot_sync(0xffffffffu, h[2]);
-            const uint32_t b3 = __ballot_sync(0xffffffffu, h[3]);
-            if ((b0 | b1 | b2 | b3) == 0u) continue;
-            uint32_t pos = cnt + __popc(b0 & lt) + __popc(b1 & lt) + __popc(b2 & lt) +
-                           __popc(b3 & lt);
-            cnt += __popc(b0) + __popc(b1) + __popc(b2) + __popc(b3);
-            uint32_t hits = (h[0] ? 1u : 0u) | (h[1] ? 2u : 0u) | (h[2] ? 4u : 0u) |
-                            (h[3] ? 8u : 0u);
-            while (hits) {  // per lane, one pass per hit (rarely more than one)
-                const int c = __ffs(hits) - 1;
-                const float xv = c == 0 ? e[0] : c == 1 ? e[1] : c == 2 ? e[2] : e[3];
-                if (pos < (uint32_t)kRunCap) {
-                    mk[pos] = fkey(xv);
-                    mi[pos] = static_cast<uint32_t>(4 * sl + c - off);
-                }
-                ++pos;
-                hits &= hits - 1u;
+    for (int u = 0; u < SAMPLE; ++u) {
+        const int sl = s0 + u * 32 + lane;
+        const float e[4] = {f[u].x, f[u].y, f[u].z, f[u].w};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const int p = 4 * sl + c - off;
+            if (sl < s1 && p >= 0 && p < n) {
+                atomicAdd(&hist[fkey(e[c]) >> 20], 1u);
+                ++ns;
             }
         }
+    }
+    ns = __reduce_add_sync(0xffffffffu, ns);
+    if (lane == 0) atomicAdd(&scratch[44], ns);
+    __syncthreads();
+    const uint32_t P = scratch[44];
+    // ceil(2 k P / n) in integers: 2 k P < 2^25 and n < 2^31, so nothing wraps
+    uint32_t tg = (2u * k * P + (uint32_t)n - 1u) / (uint32_t)n;
+    tg = tg < 1u ? 1u : tg > P ? P : tg;
+    const uint32_t L = pick_digit<THREADS>(hist, kHistBins, tg, scratch).digit << 20;
+    zero_shared<THREADS>(hist, kHistBins);
+    __syncthreads();
+    const float Lf = key_floor_float(L);
+    uint32_t cnt = 0;
+    for (int base = s0; base < s1; base += 32 * UNROLL) {
+        if (base != s0) {
+#pragma unroll
+            for (int u = 0; u < UNROLL; ++u) {
+                const int sl = base + u * 32 + lane;
+                f[u] = sl < s1 ? ldg4(v.base + sl) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+        const bool interior = base >= 1 && base + 32 * UNROLL <= s1 && base + 32 * UNROLL < nvec;
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u)
+            filter_step<true>(f[u], base + u * 32 + lane, interior, s1, n, off, L, Lf, lt, cnt,
+                              mk, mi, hist);
     }
     if (lane == 0) rcnt[w] = cnt;
 }
 
 // Exact threshold of the k largest keys held in the warp runs.
+// hist holds the level-0 histogram of the runs on entry (built while they
+// were collected).
 template <int THREADS>
 IDX_DEVI Threshold refine_runs(const uint32_t* rkey, const uint32_t* rcnt, uint32_t k,
                                uint32_t* hist, uint32_t* scratch) {
@@ -309,11 +419,13 @@ IDX_DEVI Threshold refine_runs(const uint32_t* rkey, const uint32_t* rcnt, uint3
     const uint32_t* mk = rkey + w * kRunCap;
     uint32_t prefix = 0, need = k;
     for (int lev = 0; lev <= 2; ++lev) {
-        zero_shared<THREADS>(hist, kHistBins);
-        __syncthreads();
-        for (uint32_t i = lane; i < cnt; i += 32) {
-            const uint32_t key = mk[i];
-            if (has_prefix(key, lev, prefix)) atomicAdd(&hist[digit_of(key, lev)], 1u);
+        if (lev > 0) {
+            zero_shared<THREADS>(hist, kHistBins);
+            __syncthreads();
+            for (uint32_t i = lane; i < cnt; i += 32) {
+                const uint32_t key = mk[i];
+                if (has_prefix(key, lev, prefix)) atomicAdd(&hist[digit_of(key, lev)], 1u);
+            }
         }
         __syncthreads();
         const DigitPick pk = pick_digit<THREADS>(hist, 1 << digit_bits(lev), need, scratch);
@@ -384,7 +496,8 @@ IDX_DEVI long long output_row(const TopkRowsArgs& a, int r, long long* col0) {
 
 // Lower bound L of the threshold of the k largest of a row: the lower edge of
 // the 12-bit bin that holds about the 2 k * P / n-th largest of the row's
-// first P = 4096 values, so that about 2 k keys of the row reach it.
+// first P = 4096 values, so that about 2 k keys of the row reach it.  The
+// blocks of a split row all take this same L.
 template <int THREADS>
 IDX_DEVI uint32_t estimate_lower_bound(const RowView& v, uint32_t k, uint32_t* hist,
                                        uint32_t* scratch) {
@@ -405,10 +518,10 @@ IDX_DEVI uint32_t estimate_lower_bound(const RowView& v, uint32_t k, uint32_t* h
     for (int i = 0; i < PER; ++i)
         if (threadIdx.x + (long long)i * THREADS < P) atomicAdd(&hist[fkey(x[i]) >> 20], 1u);
     __syncthreads();
-    double tg = ceil(2.0 * (double)k * (double)P / (double)n);
-    if (tg < 1.0) tg = 1.0;
-    if (tg > (double)P) tg = (double)P;
-    return pick_digit<THREADS>(hist, kHistBins, (uint32_t)tg, scratch).digit << 20;
+    // ceil(2 k P / n) in integers: 2 k P < 2^25 and n < 2^31, so nothing wraps
+    uint32_t tg = (2u * k * (uint32_t)P + (uint32_t)n - 1u) / (uint32_t)n;
+    tg = tg < 1u ? 1u : tg > (uint32_t)P ? (uint32_t)P : tg;
+    return pick_digit<THREADS>(hist, kHistBins, tg, scratch).digit << 20;
 }
 
 template <int THREADS, int UNROLL>
@@ -444,10 +557,15 @@ topk_rows_kernel(TopkRowsArgs a) {
 
     const RowView v = make_view(a.scores + (long long)r * a.row_stride + col0, n);
 
-    // lower bound L of the threshold (0 takes every key when the runs hold the row)
+    // a lower bound L of the threshold, or L = 0 (every key) when the runs hold the row
     const long long per_warp = 4 * ((v.nvec + W - 1) / W);
-    const uint32_t L = per_warp > kRunCap ? estimate_lower_bound<THREADS>(v, k, hist, scratch) : 0u;
-    stream_collect<THREADS, UNROLL>(v, L, rkey, ridx, rcnt);
+    if (per_warp > kRunCap) {
+        stream_collect_estimate<THREADS, UNROLL>(v, k, hist, scratch, rkey, ridx, rcnt);
+    } else {
+        zero_shared<THREADS>(hist, kHistBins);
+        __syncthreads();
+        stream_collect<THREADS, UNROLL, true>(v, 0u, rkey, ridx, rcnt, hist);
+    }
     __syncthreads();
     uint32_t total = 0;
     bool fits = true;
@@ -652,7 +770,7 @@ topk_split_collect_kernel(TopkRowsArgs a) {
     sv.off = v.off - (int)(4 * s0);
     sv.n = v.n;
     sv.nvec = s1 > s0 ? s1 - s0 : 0;
-    stream_collect<THREADS, UNROLL>(sv, L, rkey, ridx, rcnt);
+    stream_collect<THREADS, UNROLL, false>(sv, L, rkey, ridx, rcnt, nullptr);
     __syncthreads();
     // hand the runs over in warp (= index) order
     const long long slot = (long long)r * g + c;
