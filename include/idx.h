@@ -214,13 +214,15 @@ idx_status idx_score_topk_noalloc(const void* q, const void* k, const float* k_s
  * faster).
  *
  * idx_route_fused(max_len, topk) is the gate: 1 (the fused path) when
- * max_len >= 12288 keys, or when every row fits the default candidate slab
+ * max_len >= 24576 keys, or when every row fits the default candidate slab
  * (max_len <= max(ceil(2.25 topk), 4096): all keys are emitted, no sampling);
  * 0 otherwise (idx_score_materialise into the workspace, then
- * idx_topk_from_scores).  12288 is the crossover measured on GB300 for e4m3
+ * idx_topk_from_scores).  24576 is the crossover measured on GB300 for e4m3
  * q/k with H = 32 and 64 and topk 512 and 2048 (4096 causal rows): the
- * two-pass path is faster at 6144 and 8192 keys, the fused one from 12288 on;
- * the page's own rule (8 x topk keys, 16384 at topk 2048) sits above it.  Both
+ * two-pass path is faster from 6144 to 16384 keys, the two are within 1 % at
+ * 24576 and 32768 (where the fused path needs no logits workspace), and the
+ * fused one is faster at 65536; the page's own rule (8 x topk keys, 16384 at
+ * topk 2048) sits below it.  Both
  * paths select exactly the same keys (they compare the same fp32 scores).
  * Arguments as idx_score_topk; max_len 0 = keys.  The workspace of the
  * two-pass route holds the [rows, max_len] fp32 logits.

@@ -56,7 +56,7 @@ constexpr int kMaxTopk = 4096;
 constexpr int kMaxCap = 12288;
 // Route to the fused path from this many keys in the longest row on (measured
 // fused / two-pass crossover on GB300, see idx_score_topk_routed).
-constexpr long long kRouteMinKeys = 12288;
+constexpr long long kRouteMinKeys = 24576;
 
 size_t logits_bytes(int rows, long long stride) {
     return ((size_t)rows * (size_t)stride * sizeof(float) + 255) / 256 * 256;

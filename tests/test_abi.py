@@ -94,13 +94,14 @@ def test_product_path_has_no_oracle_import():
 
 
 def test_routing_gate_rule(lib):
-    """The gate is host logic: fused from 12288 keys in the longest row on."""
+    """The gate is host logic: fused from 24576 keys in the longest row on."""
     import sparse_attention_indexer_tiles_gb300 as pkg
     assert pkg.idx_route_fused(4608, 2048)       # fits the slab: every key emitted
     assert not pkg.idx_route_fused(4609, 2048)
-    assert not pkg.idx_route_fused(12287, 2048)
+    assert not pkg.idx_route_fused(24575, 2048)
+    assert not pkg.idx_route_fused(12288, 2048)
     assert not pkg.idx_route_fused(6144, 512)
-    assert pkg.idx_route_fused(12288, 2048)
+    assert pkg.idx_route_fused(24576, 2048)
     assert pkg.idx_route_fused(1 << 20, 512)
     # the dense route's workspace holds the logits; the fused one its slab
     dense = pkg.idx_score_topk_routed_workspace(64, 8192, 0, 64, 128, 2048, 2)

@@ -29,8 +29,8 @@ def call(idx, fn, inp, **kw):
 
 
 @pytest.mark.parametrize("keys,H,topk,dense", [(6144, 64, 512, True), (9000, 32, 300, True),
-                                                (12288, 64, 256, False), (20000, 16, 128, False),
-                                                (3000, 64, 512, False)])
+                                                (20000, 16, 128, True), (24576, 64, 256, False),
+                                                (30000, 16, 128, False), (3000, 64, 512, False)])
 def test_routed_equals_fused(idx, keys, H, topk, dense):
     assert idx.idx_route_fused(keys, topk) == (not dense)
     inp = synth.indexer_inputs(256 // H * 4 + 3, keys, H, 128, topk, "fp8", seed=80 + H)
