@@ -16,6 +16,13 @@ the header of ``oracle.c``:
 * ``topk_from_scores``the selection applied to given fp32 scores.
 * ``page_transform``  row-relative positions -> physical KV slots of a paged
                       cache (page size P): table[t, p // P] * P + p % P, -1 kept.
+
+Input formats: bf16, e4m3 and MXFP4 (e2m1 elements packed two per byte with
+one e8m0 scale per 32 elements; ``q_sf`` / ``k_sf`` on the input set).
+
+``IDX_ORACLE_LIB`` names an already built oracle library to load instead of
+building ``oracle.c``; the mutation tests use it to run the pins against
+copies of the oracle with planted mistakes.
 """
 from __future__ import annotations
 
@@ -33,11 +40,14 @@ _LIB = os.path.join(_BUILD, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-BF16, E4M3 = 1, 2
+BF16, E4M3, MXFP4 = 1, 2, 3
 
 
 def build(force: bool = False) -> str:
     """Compile oracle.c into oracle/_build/liboracle.so (gcc, no GPU)."""
+    override = os.environ.get("IDX_ORACLE_LIB")
+    if override:
+        return override
     with _lock:
         if (not force and os.path.exists(_LIB)
                 and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
@@ -61,11 +71,15 @@ def _load():
         lib.orc_e4m3_to_f64.restype = ctypes.c_double
         lib.orc_bf16_to_f64.argtypes = [ctypes.c_uint32]
         lib.orc_bf16_to_f64.restype = ctypes.c_double
-        lib.orc_scores_row.argtypes = [P, P, i32, P, P, i32, i32, i64, i64, i64, P]
+        lib.orc_e2m1_to_f64.argtypes = [ctypes.c_uint32]
+        lib.orc_e2m1_to_f64.restype = ctypes.c_double
+        lib.orc_e8m0_to_f64.argtypes = [ctypes.c_uint32]
+        lib.orc_e8m0_to_f64.restype = ctypes.c_double
+        lib.orc_scores_row.argtypes = [P, P, P, P, i32, P, P, i32, i32, i64, i64, i64, P]
         lib.orc_scores_row.restype = i32
         lib.orc_select_row.argtypes = [P, i64, i32, P]
         lib.orc_select_row.restype = i32
-        lib.orc_score_topk.argtypes = [P, P, i32, P, P, P, P, i32, i32, P, i32, i32, P,
+        lib.orc_score_topk.argtypes = [P, P, P, P, i32, P, P, P, P, i32, i32, P, i32, i32, P,
                                        P, i64, i32]
         lib.orc_score_topk.restype = i32
         lib.orc_topk_from_scores.argtypes = [P, i64, P, P, P, i32, i32, P, i32]
@@ -125,24 +139,54 @@ def bf16_to_f64(codes) -> np.ndarray:
     return np.array([lib.orc_bf16_to_f64(int(v)) for v in c], dtype=np.float64)
 
 
-class _Indexer:
-    """Raw views of an indexer input set (q, k, k_scale, w, ks, ke)."""
+def e2m1_to_f64(codes) -> np.ndarray:
+    lib = _load()
+    c = np.asarray(codes, dtype=np.uint32).ravel()
+    return np.array([lib.orc_e2m1_to_f64(int(v)) for v in c], dtype=np.float64)
 
-    def __init__(self, q, k, k_scale, w, ks, ke):
-        self.dtype = _dtype_code(q)
-        self.q = _np(q)
-        self.k = _np(k)
+
+def e8m0_to_f64(codes) -> np.ndarray:
+    lib = _load()
+    c = np.asarray(codes, dtype=np.uint32).ravel()
+    return np.array([lib.orc_e8m0_to_f64(int(v)) for v in c], dtype=np.float64)
+
+
+class _Indexer:
+    """Raw views of an indexer input set (q, k, k_scale, w, ks, ke, and the
+    block scales q_sf, k_sf of MXFP4 inputs)."""
+
+    def __init__(self, q, k, k_scale, w, ks, ke, q_sf=None, k_sf=None):
+        mx = q_sf is not None or k_sf is not None
+        self.dtype = MXFP4 if mx else _dtype_code(q)
+        self.q = _np(q, np.uint8 if mx else None)
+        self.k = _np(k, np.uint8 if mx else None)
         self.k_scale = _np(k_scale, np.float32)
         self.w = _np(w, np.float32)
         self.ks = _np(ks, np.int32)
         self.ke = _np(ke, np.int32)
-        self.rows, self.H, self.D = self.q.shape
-        if self.k.shape[1] != self.D or self.w.shape != (self.rows, self.H):
+        self.rows, self.H, dq = self.q.shape
+        self.D = 2 * dq if mx else dq
+        if mx:
+            self.q_sf = _np(q_sf, np.uint8)
+            self.k_sf = _np(k_sf, np.uint8)
+            if (self.D % 32 or self.k.shape[1] * 2 != self.D
+                    or self.q_sf.shape != (self.rows, self.H, self.D // 32)
+                    or self.k_sf.shape != (self.k.shape[0], self.D // 32)):
+                raise ValueError("inconsistent MXFP4 input shapes")
+        else:
+            self.q_sf = self.k_sf = None
+        if self.w.shape != (self.rows, self.H) or (not mx and self.k.shape[1] != self.D):
             raise ValueError("inconsistent indexer input shapes")
+
+    def sf_ptrs(self):
+        if self.q_sf is None:
+            return None, None
+        return _ptr(self.q_sf), _ptr(self.k_sf)
 
 
 def _indexer(inp) -> _Indexer:
-    return _Indexer(inp.q, inp.k, inp.k_scale, inp.w, inp.ks, inp.ke)
+    return _Indexer(inp.q, inp.k, inp.k_scale, inp.w, inp.ks, inp.ke,
+                    getattr(inp, "q_sf", None), getattr(inp, "k_sf", None))
 
 
 def scores_row(inp, r: int) -> np.ndarray:
@@ -151,7 +195,8 @@ def scores_row(inp, r: int) -> np.ndarray:
     ks, ke = int(X.ks[r]), int(X.ke[r])
     out = np.zeros(max(ke - ks, 0), dtype=np.float64)
     if out.size:
-        e = _load().orc_scores_row(_ptr(X.q), _ptr(X.k), X.dtype, _ptr(X.k_scale),
+        qsf, ksf = X.sf_ptrs()
+        e = _load().orc_scores_row(_ptr(X.q), qsf, _ptr(X.k), ksf, X.dtype, _ptr(X.k_scale),
                                    _ptr(X.w), X.H, X.D, r, ks, ke, _ptr(out))
         if e:
             raise MemoryError("oracle scores_row failed")
@@ -178,9 +223,10 @@ def score_topk(inp, rows=None, nthreads: int | None = None, want_scores: bool = 
     lens = (X.ke.astype(np.int64) - X.ks.astype(np.int64)).clip(min=0)
     sstride = int(lens[rows].max()) if (want_scores and rows.size) else 0
     sc = np.zeros((rows.size, max(sstride, 1)), dtype=np.float64) if want_scores else None
-    e = _load().orc_score_topk(_ptr(X.q), _ptr(X.k), X.dtype, _ptr(X.k_scale), _ptr(X.w),
-                               _ptr(X.ks), _ptr(X.ke), X.H, X.D, _ptr(rows), rows.size,
-                               topk, _ptr(out), _ptr(sc) if want_scores else None,
+    qsf, ksf = X.sf_ptrs()
+    e = _load().orc_score_topk(_ptr(X.q), qsf, _ptr(X.k), ksf, X.dtype, _ptr(X.k_scale),
+                               _ptr(X.w), _ptr(X.ks), _ptr(X.ke), X.H, X.D, _ptr(rows),
+                               rows.size, topk, _ptr(out), _ptr(sc) if want_scores else None,
                                max(sstride, 1), nthreads or default_threads())
     if e:
         raise MemoryError("oracle score_topk failed")

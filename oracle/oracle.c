@@ -32,6 +32,17 @@
  *   e4m3 (fn):  1 sign, 4 exponent bits (bias 7), 3 mantissa bits, subnormals
  *               at exponent 0, S.1111.111 is NaN, no infinities, max 448.
  *   bfloat16:   1 sign, 8 exponent bits (bias 127), 7 mantissa bits.
+ *   MXFP4:      the OCP microscaling format with FP4 elements: every element
+ *               is an e2m1 code (1 sign, 2 exponent bits with bias 1, 1
+ *               mantissa bit; exponent 0 holds 0 and 0.5; no infinities or
+ *               NaN; max 6) times the e8m0 scale of its block of 32
+ *               consecutive elements along D (8 exponent bits, bias 127, no
+ *               sign or mantissa: 2^(c - 127); 0xFF is NaN).  Two elements per
+ *               byte, element 2i in bits 0..3 and element 2i+1 in bits 4..7;
+ *               scale bytes [rows, H, D/32] for q and [keys, D/32] for k.
+ *               "[sglang] logits를 쓰지 않는 top-k", section 1, names an
+ *               mxf4 scoring path with 64-byte keys (128 elements) but not the
+ *               scale layout; one scale per 32 elements is the OCP block size.
  *
  * Build: plain C11, no fast-math and no FMA contraction (-ffp-contract=off),
  * so the fp64 results are the same on every host.
@@ -42,7 +53,7 @@
 #include <stdlib.h>
 #include <string.h>
 
-enum { ORC_BF16 = 1, ORC_E4M3 = 2 };
+enum { ORC_BF16 = 1, ORC_E4M3 = 2, ORC_MXFP4 = 3 };
 
 /* ---------------------------------------------------------------- decoders */
 
@@ -70,28 +81,57 @@ double orc_bf16_to_f64(uint32_t code) {
     return sign ? -v : v;
 }
 
-/* Every code of both formats decoded once by the functions above. */
+double orc_e2m1_to_f64(uint32_t code) {
+    const int sign = (code >> 3) & 1;
+    const int expo = (code >> 1) & 0x3;
+    const int mant = code & 0x1;
+    double v;
+    if (expo == 0)
+        v = ldexp((double)mant / 2.0, 1 - 1);          /* subnormal: 0 or 0.5 */
+    else
+        v = ldexp(1.0 + (double)mant / 2.0, expo - 1);  /* normal */
+    return sign ? -v : v;
+}
+
+double orc_e8m0_to_f64(uint32_t code) {
+    if ((code & 0xFF) == 0xFF) return NAN;
+    return ldexp(1.0, (int)(code & 0xFF) - 127);
+}
+
+/* Every code of the formats decoded once by the functions above. */
 static double tab_e4m3[256];
 static double tab_bf16[65536];
+static double tab_e2m1[16];
+static double tab_e8m0[256];
 static pthread_once_t tab_once = PTHREAD_ONCE_INIT;
 
 static void fill_tables(void) {
     for (uint32_t c = 0; c < 256; ++c) tab_e4m3[c] = orc_e4m3_to_f64(c);
     for (uint32_t c = 0; c < 65536; ++c) tab_bf16[c] = orc_bf16_to_f64(c);
+    for (uint32_t c = 0; c < 16; ++c) tab_e2m1[c] = orc_e2m1_to_f64(c);
+    for (uint32_t c = 0; c < 256; ++c) tab_e8m0[c] = orc_e8m0_to_f64(c);
 }
 
-static double decode(const void* base, long long i, int dtype) {
+/* Element i of a row-major array of the format (flat index over [..., D]);
+ * sf holds the MXFP4 block scales ([..., D/32], so block i / 32). */
+static double decode(const void* base, const uint8_t* sf, long long i, int dtype) {
     pthread_once(&tab_once, fill_tables);
     if (dtype == ORC_E4M3) return tab_e4m3[((const uint8_t*)base)[i]];
+    if (dtype == ORC_MXFP4) {
+        const uint32_t byte = ((const uint8_t*)base)[i >> 1];
+        const uint32_t code = (i & 1) ? (byte >> 4) : (byte & 0xF);
+        return tab_e2m1[code] * tab_e8m0[sf[i / 32]];
+    }
     return tab_bf16[((const uint16_t*)base)[i]];
 }
 
 /* ------------------------------------------------------------------ scores */
 
-/* Scores of one row over its visible keys, out[j - ks] for ks <= j < ke. */
-int orc_scores_row(const void* q, const void* k, int dtype, const float* k_scale,
-                   const float* w, int H, int D, long long r, long long ks,
-                   long long ke, double* out) {
+/* Scores of one row over its visible keys, out[j - ks] for ks <= j < ke.
+ * q_sf / k_sf: the block scales of MXFP4 inputs (NULL for the other formats). */
+int orc_scores_row(const void* q, const uint8_t* q_sf, const void* k, const uint8_t* k_sf,
+                   int dtype, const float* k_scale, const float* w, int H, int D,
+                   long long r, long long ks, long long ke, double* out) {
     if (ke <= ks) return 0;
     double* qd = (double*)malloc(sizeof(double) * (size_t)H * D);
     double* kd = (double*)malloc(sizeof(double) * (size_t)D);
@@ -100,9 +140,9 @@ int orc_scores_row(const void* q, const void* k, int dtype, const float* k_scale
     /* qd[d*H + h] = q[r,h,d]: heads contiguous for the inner loop below */
     for (int h = 0; h < H; ++h)
         for (int d = 0; d < D; ++d)
-            qd[(size_t)d * H + h] = decode(q, (r * (long long)H + h) * D + d, dtype);
+            qd[(size_t)d * H + h] = decode(q, q_sf, (r * (long long)H + h) * D + d, dtype);
     for (long long j = ks; j < ke; ++j) {
-        for (int d = 0; d < D; ++d) kd[d] = decode(k, j * (long long)D + d, dtype);
+        for (int d = 0; d < D; ++d) kd[d] = decode(k, k_sf, j * (long long)D + d, dtype);
         /* q[r,h,:] . k[j,:], summed over d in ascending order for every head */
         for (int h = 0; h < H; ++h) dot[h] = 0.0;
         for (int d = 0; d < D; ++d)
@@ -156,7 +196,8 @@ int orc_select_row(const double* s, long long n, int topk, int32_t* out) {
 
 typedef struct {
     /* indexer inputs (score_topk) */
-    const void* q; const void* k; int dtype; const float* k_scale; const float* w;
+    const void* q; const uint8_t* q_sf; const void* k; const uint8_t* k_sf; int dtype;
+    const float* k_scale; const float* w;
     int H, D;
     /* given scores (topk_from_scores) */
     const float* scores; long long stride;
@@ -188,7 +229,8 @@ static void* worker(void* arg) {
             for (long long j = 0; j < n; ++j) s[j] = (double)J->scores[r * J->stride + ks + j];
             e = 0;
         } else {
-            e = orc_scores_row(J->q, J->k, J->dtype, J->k_scale, J->w, J->H, J->D, r, ks, ke, s);
+            e = orc_scores_row(J->q, J->q_sf, J->k, J->k_sf, J->dtype, J->k_scale, J->w, J->H,
+                               J->D, r, ks, ke, s);
         }
         if (!e && J->out) e = orc_select_row(s, n, J->topk, J->out + (long long)i * J->topk);
         if (!e && J->out_scores)
@@ -218,13 +260,13 @@ static int run(orc_job* J, int nthreads) {
 /* Exact top-k of the indexer scores for the listed rows.
  * out[i, :] belongs to rows[i]; out_scores (optional) receives the fp64 scores
  * of rows[i] at [i, 0 .. ke-ks) with row pitch score_stride. */
-int orc_score_topk(const void* q, const void* k, int dtype, const float* k_scale,
-                   const float* w, const int32_t* ks, const int32_t* ke, int H, int D,
-                   const int32_t* rows, int nrows, int topk, int32_t* out,
-                   double* out_scores, long long score_stride, int nthreads) {
+int orc_score_topk(const void* q, const uint8_t* q_sf, const void* k, const uint8_t* k_sf,
+                   int dtype, const float* k_scale, const float* w, const int32_t* ks,
+                   const int32_t* ke, int H, int D, const int32_t* rows, int nrows, int topk,
+                   int32_t* out, double* out_scores, long long score_stride, int nthreads) {
     orc_job J;
     memset(&J, 0, sizeof(J));
-    J.q = q; J.k = k; J.dtype = dtype; J.k_scale = k_scale; J.w = w; J.H = H; J.D = D;
+    J.q = q; J.q_sf = q_sf; J.k = k; J.k_sf = k_sf; J.dtype = dtype; J.k_scale = k_scale; J.w = w; J.H = H; J.D = D;
     J.ks = ks; J.ke = ke; J.rows = rows; J.nrows = nrows; J.topk = topk; J.out = out;
     J.out_scores = out_scores; J.score_stride = score_stride;
     return run(&J, nthreads);

@@ -12,8 +12,11 @@ keys) and the standalone exact top-k of "[sglang] ROCm DSA Indexer Top-K ìµœì í
 (fp32 scores, dense clustering, topk 2048).
 
 Layouts (row-major, contiguous):
-  q        [rows, H, D]  bfloat16 or float8_e4m3fn
-  k        [keys, D]     same dtype as q
+  q        [rows, H, D]  bfloat16 or float8_e4m3fn; MXFP4: uint8 [rows, H, D/2]
+                         (two e2m1 codes per byte, element 2i in the low
+                         nibble) with q_sf uint8 [rows, H, D/32] (e8m0 scales)
+  k        [keys, D]     same format as q; MXFP4: uint8 [keys, D/2], k_sf
+                         uint8 [keys, D/32]
   k_scale  [keys]        float32, > 0
   w        [rows, H]     float32, >= 0
   ks, ke   [rows]        int32, visible keys of row r are ks[r] <= j < ke[r]
@@ -27,7 +30,7 @@ from dataclasses import dataclass, field
 import torch
 
 __all__ = [
-    "IndexerInputs", "ScoreInputs", "indexer_inputs", "score_inputs",
+    "IndexerInputs", "ScoreInputs", "indexer_inputs", "score_inputs", "quantise_mxfp4",
     "causal_ranges", "mixed_batch_lengths", "planted_scale_factor",
     "workload", "WORKLOADS", "sample_rows",
 ]
@@ -43,6 +46,8 @@ class IndexerInputs:
     ke: torch.Tensor
     topk: int
     meta: dict = field(default_factory=dict)
+    q_sf: torch.Tensor | None = None  # MXFP4 block scales of q
+    k_sf: torch.Tensor | None = None  # MXFP4 block scales of k
 
     @property
     def rows(self) -> int:
@@ -58,10 +63,12 @@ class IndexerInputs:
 
     @property
     def D(self) -> int:
-        return int(self.q.shape[2])
+        return int(self.q.shape[2]) * (2 if self.q_sf is not None else 1)
 
     @property
     def dtype(self) -> str:
+        if self.q_sf is not None:
+            return "mxfp4"
         return "bf16" if self.q.dtype == torch.bfloat16 else "fp8_e4m3"
 
     def pairs(self) -> int:
@@ -133,6 +140,40 @@ def _quantise(x: torch.Tensor, dtype: str) -> torch.Tensor:
     raise ValueError(f"unknown dtype {dtype!r}")
 
 
+# magnitudes of the e2m1 codes 0..7 (code 8 + c is the negative of code c)
+_E2M1_MAG = torch.tensor([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0], dtype=torch.float64)
+
+
+def quantise_mxfp4(x: torch.Tensor):
+    """Encode fp32 x [..., D] (D a multiple of 32) as MXFP4: per block of 32
+    consecutive values the shared scale 2^e with e = floor(log2 max|x|) - 2
+    (the largest e2m1 magnitude is 1.5 * 2^2; the OCP recipe), clamped to
+    [-127, 127], stored as the e8m0 byte e + 127; each value divided by 2^e,
+    rounded to the nearest e2m1 magnitude (ties to the even code, i.e. the
+    mantissa bit 0), saturated at 6, and packed two per byte, element 2i in
+    the low nibble.  Returns (codes uint8 [..., D/2], scales uint8 [..., D/32]).
+    This is input encoding only; the indexer consumes the bytes."""
+    *lead, D = x.shape
+    if D % 32:
+        raise ValueError("MXFP4 needs D % 32 == 0")
+    xb = x.to(torch.float64).reshape(*lead, D // 32, 32)
+    amax = xb.abs().amax(-1)
+    _, ex = torch.frexp(amax)  # amax = m * 2^ex, 0.5 <= m < 1, so floor(log2 amax) = ex - 1
+    e = torch.where(amax > 0, ex.to(torch.int64) - 1 - 2, torch.zeros_like(ex, dtype=torch.int64))
+    e = e.clamp(-127, 127)
+    scaled = xb / torch.ldexp(torch.ones_like(amax), e)[..., None]
+    mag = scaled.abs().clamp(max=6.0)
+    lo = (torch.searchsorted(_E2M1_MAG, mag.contiguous(), right=True) - 1).clamp(0, 7)
+    hi = (lo + 1).clamp(max=7)
+    dl = mag - _E2M1_MAG[lo]
+    dh = _E2M1_MAG[hi] - mag
+    up = (dh < dl) | ((dh == dl) & (hi % 2 == 0) & (hi != lo))
+    code = torch.where(up, hi, lo) | ((scaled < 0).to(torch.int64) << 3)
+    code = code.reshape(*lead, D).to(torch.uint8)
+    packed = (code[..., 0::2] | (code[..., 1::2] << 4)).contiguous()
+    return packed, (e + 127).to(torch.uint8).contiguous()
+
+
 def indexer_inputs(rows: int, keys: int, H: int, D: int, topk: int, dtype: str,
                    seed: int, *, ranges: str = "causal", scale: str = "uniform",
                    planted_runs: int = 0, planted_len: int = 64,
@@ -146,8 +187,13 @@ def indexer_inputs(rows: int, keys: int, H: int, D: int, topk: int, dtype: str,
     uniform, not aligned to 64, and placed where every causal row sees them.
     """
     g = _gen(seed)
-    q = _quantise(torch.randn(rows, H, D, generator=g, dtype=torch.float32), dtype)
-    k = _quantise(torch.randn(keys, D, generator=g, dtype=torch.float32), dtype)
+    qf = torch.randn(rows, H, D, generator=g, dtype=torch.float32)
+    kf = torch.randn(keys, D, generator=g, dtype=torch.float32)
+    if dtype == "mxfp4":
+        (q, q_sf), (k, k_sf) = quantise_mxfp4(qf), quantise_mxfp4(kf)
+    else:
+        q, k, q_sf, k_sf = _quantise(qf, dtype), _quantise(kf, dtype), None, None
+    del qf, kf
     w = torch.rand(rows, H, generator=g, dtype=torch.float32) / H
     if scale == "uniform":
         k_scale = 0.5 + 1.5 * torch.rand(keys, generator=g, dtype=torch.float32)
@@ -184,7 +230,7 @@ def indexer_inputs(rows: int, keys: int, H: int, D: int, topk: int, dtype: str,
     else:
         raise ValueError(ranges)
     return IndexerInputs(q=q, k=k, k_scale=k_scale, w=w, ks=ks_t, ke=ke_t,
-                         topk=topk, meta=meta)
+                         topk=topk, meta=meta, q_sf=q_sf, k_sf=k_sf)
 
 
 def score_inputs(rows: int, keys: int, topk: int, seed: int, *,
@@ -232,9 +278,6 @@ def _mixed_batch(seed: int, requests: int = 64, rows_per_request: int = 128,
     return inp
 
 
-# The named workloads: small case first, then the standalone top-k, the fused
-# prefill, the long-context stress and the mixed batch, plus the low-batch
-# long-row top-k that exercises the multi-block row split.
 def paged_layout(requests: int, pages_per_request: int, rows_per_request: int, seed: int,
                  pool_pages: int | None = None):
     """A paged KV cache: each request owns pages_per_request distinct physical
@@ -249,6 +292,9 @@ def paged_layout(requests: int, pages_per_request: int, rows_per_request: int, s
     return table, row_map
 
 
+# The named workloads: small case first, then the standalone top-k, the fused
+# prefill, the long-context stress and the mixed batch, plus the low-batch
+# long-row top-k that exercises the multi-block row split.
 WORKLOADS = {
     "tiny": dict(kind="indexer", rows=64, keys=4096, H=8, D=64, topk=256,
                  dtype="bf16", seed=0, scale="one"),

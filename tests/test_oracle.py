@@ -299,3 +299,114 @@ def test_page_transform_permuted_table_inverts(orc):
         assert back == idx[r, :-3].tolist()
         assert (got[r, -3:] == -1).all()
         assert len(set(got[r, :-3].tolist())) == 47
+
+
+# ------------------------------------------------------------- MXFP4 inputs
+
+# OCP Microscaling Formats (MX) v1.0, FP4 E2M1: the magnitudes of codes 0..7.
+E2M1_VALUES = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def test_e2m1_decoder_exhaustive(orc):
+    got = orc.e2m1_to_f64(np.arange(16))
+    assert got[:8].tolist() == E2M1_VALUES
+    assert np.array_equal(got[8:], -got[:8]) and np.signbit(got[8])  # code 8 is -0
+    mld = pytest.importorskip("ml_dtypes")
+    ref = np.frombuffer(np.arange(16, dtype=np.uint8).tobytes(),
+                        dtype=mld.float4_e2m1fn).astype(np.float64)
+    assert np.array_equal(got, ref) and np.array_equal(np.signbit(got), np.signbit(ref))
+
+
+def test_e8m0_decoder_exhaustive_matches_torch(orc):
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e8m0fnu).to(torch.float64).numpy()
+    got = orc.e8m0_to_f64(codes)
+    nan = np.isnan(ref)
+    assert np.flatnonzero(nan).tolist() == [255]
+    assert np.array_equal(np.isnan(got), nan) and np.array_equal(got[~nan], ref[~nan])
+    assert got[127] == 1.0 and got[0] == 2.0 ** -127 and got[254] == 2.0 ** 127
+
+
+def _mx_inputs(q, q_sf, k, k_sf, topk=4, w=None, k_scale=None):
+    """An MXFP4 input set from raw bytes: w = 1 and k_scale = 1 unless given,
+    every row sees every key."""
+    rows, H = q.shape[0], q.shape[1]
+    keys = k.shape[0]
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.uint8))  # noqa: E731
+    return synth.IndexerInputs(
+        q=t(q), k=t(k), q_sf=t(q_sf), k_sf=t(k_sf),
+        k_scale=torch.ones(keys) if k_scale is None else k_scale,
+        w=torch.ones(rows, H) if w is None else w,
+        ks=torch.zeros(rows, dtype=torch.int32), ke=torch.full((rows,), keys, dtype=torch.int32),
+        topk=topk)
+
+
+def test_mxfp4_nibble_order_and_block_scales(orc):
+    """Closed forms with D = 128 (four scale blocks).  q holds 1.0 in every
+    even element and 0 in every odd one; k rows hold 1.0 in the even, the odd
+    and all elements: the scores 64, 0, 64 fix the nibble order.  Then all
+    elements 1.0, q's block b scaled by 2^b and k's blocks by 1, 1/2, 1, 2:
+    32 (1 + 2 + 4 + 8) = 480 and 32 (1 + 1 + 4 + 16) = 704 fix which scale
+    byte covers which element."""
+    D, one = 128, 0x2  # 0x2: the e2m1 code of 1.0
+    q = np.full((1, 1, D // 2), one, np.uint8)
+    k = np.array([[one] * (D // 2), [one << 4] * (D // 2), [one | one << 4] * (D // 2)])
+    unit = lambda *shape: np.full(shape, 127, np.uint8)  # noqa: E731  e8m0 of 1.0
+    s = orc.scores_row(_mx_inputs(q, unit(1, 1, D // 32), k, unit(3, D // 32)), 0)
+    assert s.tolist() == [64.0, 0.0, 64.0]
+    q2 = np.full((1, 1, D // 2), one | one << 4, np.uint8)
+    q2_sf = (127 + np.arange(D // 32)).reshape(1, 1, -1)
+    k2 = np.full((2, D // 2), one | one << 4, np.uint8)
+    k2_sf = np.array([[127, 127, 127, 127], [127, 126, 127, 128]])
+    s2 = orc.scores_row(_mx_inputs(q2, q2_sf, k2, k2_sf), 0)
+    assert s2.tolist() == [480.0, 704.0]
+
+
+def _decode_mx_independently(codes, sf):
+    """MXFP4 bytes -> fp64 values through ml_dtypes (e2m1) and torch (e8m0),
+    not through the oracle."""
+    mld = pytest.importorskip("ml_dtypes")
+    el = np.stack([codes & 0xF, codes >> 4], -1).reshape(*codes.shape[:-1], -1)
+    v = np.frombuffer(el.astype(np.uint8).tobytes(), dtype=mld.float4_e2m1fn)
+    v = v.astype(np.float64).reshape(el.shape)
+    sc = torch.from_numpy(np.ascontiguousarray(sf, np.uint8)).view(torch.float8_e8m0fnu)
+    return v * np.repeat(sc.to(torch.float64).numpy(), 32, axis=-1)
+
+
+def test_mxfp4_scores_equal_the_e4m3_scores_of_the_same_values(orc):
+    """Random MXFP4 bytes with block scales in 2^-3 .. 2^3: every value (an
+    e2m1 magnitude times its block scale, |v| <= 48, nonzero |v| >= 2^-4) is
+    exact in e4m3, so the oracle's MXFP4 scores equal, bit for bit, its e4m3
+    scores of the same values, which are decoded here by ml_dtypes and torch.
+    A swapped nibble, a misplaced scale block or a wrong bias breaks it."""
+    rng = np.random.default_rng(7)
+    rows, keys, H, D = 3, 50, 4, 64
+    q = rng.integers(0, 256, (rows, H, D // 2), dtype=np.uint8)
+    k = rng.integers(0, 256, (keys, D // 2), dtype=np.uint8)
+    q_sf = rng.integers(124, 131, (rows, H, D // 32), dtype=np.uint8)
+    k_sf = rng.integers(124, 131, (keys, D // 32), dtype=np.uint8)
+    qv = torch.from_numpy(_decode_mx_independently(q, q_sf))
+    kv = torch.from_numpy(_decode_mx_independently(k, k_sf))
+    q8, k8 = qv.to(torch.float8_e4m3fn), kv.to(torch.float8_e4m3fn)
+    assert torch.equal(q8.to(torch.float64), qv) and torch.equal(k8.to(torch.float64), kv)
+    g = torch.Generator().manual_seed(8)
+    w = torch.rand(rows, H, generator=g)
+    sc = 0.5 + torch.rand(keys, generator=g)
+    mx = _mx_inputs(q, q_sf, k, k_sf, topk=9, w=w, k_scale=sc)
+    e4 = synth.IndexerInputs(q=q8, k=k8, k_scale=sc, w=w, ks=mx.ks, ke=mx.ke, topk=9)
+    for r in range(rows):
+        assert np.array_equal(orc.scores_row(mx, r), orc.scores_row(e4, r))
+    assert np.array_equal(orc.score_topk(mx, nthreads=2), orc.score_topk(e4, nthreads=2))
+
+
+def test_mxfp4_generated_inputs_score_like_their_decoded_values(orc):
+    """synth's MXFP4 workload inputs: the oracle's scores equal a numpy
+    evaluation of the definition on the independently decoded values."""
+    inp = synth.indexer_inputs(2, 40, 3, 64, 5, "mxfp4", seed=9, ranges="full")
+    assert inp.D == 64 and inp.dtype == "mxfp4"
+    qv = _decode_mx_independently(inp.q.numpy(), inp.q_sf.numpy())
+    kv = _decode_mx_independently(inp.k.numpy(), inp.k_sf.numpy())
+    for r in range(2):
+        dots = kv @ qv[r].T  # [keys, H]
+        ref = inp.k_scale.double().numpy() * (np.maximum(dots, 0) @ inp.w[r].double().numpy())
+        np.testing.assert_allclose(orc.scores_row(inp, r), ref, rtol=1e-12, atol=1e-12)

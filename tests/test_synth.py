@@ -64,3 +64,34 @@ def test_sample_rows_keeps_extremes():
     rows = synth.sample_rows(ks, ke, 64, seed=2)
     assert len(rows) == 64 and 0 in rows and 499 in rows
     assert rows == synth.sample_rows(ks, ke, 64, seed=2)
+
+
+def test_mxfp4_encoding_recipe():
+    """quantise_mxfp4: each block's scale puts its largest magnitude in [4, 8)
+    (e = floor(log2 max|x|) - 2), every element is the nearest e2m1 value of
+    x / 2^e with ties to even and saturation at 6 (checked against ml_dtypes'
+    own rounding), two codes per byte with element 2i in the low nibble, and
+    the generator draws q and k from the same random stream as fp8/bf16."""
+    import pytest
+    mld = pytest.importorskip("ml_dtypes")
+    g = torch.Generator().manual_seed(1)
+    x = torch.randn(5, 3, 128, generator=g)
+    x[0, 0, :32] = 0.0                       # an all-zero block
+    x[0, 1, :32] = torch.linspace(-6, 6, 32)  # exact grid points and halves
+    codes, sf = synth.quantise_mxfp4(x)
+    assert codes.shape == (5, 3, 64) and sf.shape == (5, 3, 4)
+    assert codes.dtype == torch.uint8 and sf.dtype == torch.uint8
+    scale = np.ldexp(1.0, sf.numpy().astype(np.int64) - 127)
+    xb = x.double().numpy().reshape(5, 3, 4, 32)
+    amax = np.abs(xb).max(-1)
+    nz = amax > 0
+    assert np.all((amax[nz] / scale[nz] >= 4) & (amax[nz] / scale[nz] < 8))
+    el = np.stack([codes.numpy() & 0xF, codes.numpy() >> 4], -1).reshape(5, 3, 128)
+    got = np.frombuffer(el.astype(np.uint8).tobytes(), dtype=mld.float4_e2m1fn)
+    got = got.astype(np.float64).reshape(5, 3, 4, 32)
+    ref = np.clip(xb / scale[..., None], -6, 6).astype(mld.float4_e2m1fn).astype(np.float64)
+    assert np.array_equal(got, ref)
+    mx = synth.indexer_inputs(4, 100, 2, 64, 8, "mxfp4", seed=5)
+    e4 = synth.indexer_inputs(4, 100, 2, 64, 8, "fp8", seed=5)
+    assert torch.equal(mx.w, e4.w) and torch.equal(mx.k_scale, e4.k_scale)
+    assert mx.q.shape == (4, 2, 32) and mx.k_sf.shape == (100, 2) and mx.D == 64
