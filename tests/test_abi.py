@@ -2,6 +2,7 @@
 include/idx.h declares, and its host-only logic (workspace sizes, status text,
 argument checks that precede any CUDA call) behaves as documented."""
 import ctypes
+import math
 import os
 import re
 
@@ -108,3 +109,41 @@ def test_routing_gate_rule(lib):
     assert dense >= 64 * 8192 * 4
     assert pkg.idx_score_topk_routed_workspace(64, 65536, 0, 64, 128, 256, 2) == \
         pkg.idx_score_topk_workspace(64, 65536, 0, 64, 128, 256, 2)
+
+
+def _documented_workspace(rows, max_len, topk, nruns):
+    """The fused workspace as the layout is documented: 256-byte aligned
+    regions for the row plans (32 B each), the run counts [rows, nruns] int32,
+    the slab [rows, nruns, cap_q] fp32 scores and int32 indices with
+    cap_q = ceil(cap / 8) + 64, the sample scratch [rows, max_len // S + 2]
+    fp32 and the rescan histograms [rows, 4096] (both only when rows can see
+    more than cap keys), and eight rescan counters."""
+    def up(x):
+        return (x + 255) // 256 * 256
+    cap = max(math.ceil(2.25 * topk), 4096)
+    cap_q = -(-cap // 8) + 64
+    target = math.sqrt(cap / topk)
+    t = max(32.0, (4.5 / math.log(max(target, 1.0001))) ** 2)
+    S = max(s for s in (1, 3, 5, 7, 11, 15, 23, 31, 45, 63) if s <= target * topk / t)
+    sampled = max_len > cap
+    regions = [rows * 32, rows * nruns * 4, rows * nruns * cap_q * 4, rows * nruns * cap_q * 4,
+               rows * (max_len // S + 2) * 4 if sampled else 0,
+               rows * 4096 * 4 if sampled else 0, 8 * 4]
+    return sum(up(r) for r in regions), S
+
+
+def test_fused_workspace_follows_the_documented_layout(lib):
+    """Eight runs per row and key split: four row blocks of H = 64 rows fill
+    one wave, so a call with few rows splits every block's keys into as many
+    parts as keep >= 64 key tiles each (at most six); 4096 rows are not
+    split.  These cases do not depend on the GPU's SM count."""
+    import sparse_attention_indexer_tiles_gb300 as pkg
+    ws = pkg.idx_score_topk_workspace
+    cases = [  # rows, keys, topk, expected key splits
+        (4096, 65536, 2048, 1), (8, 65536, 2048, 6), (8, 16384, 2048, 2), (64, 65536, 512, 6),
+        (8, 4096, 2048, 1)]
+    for rows, keys, topk, k in cases:
+        expect, S = _documented_workspace(rows, keys, topk, 8 * k)
+        assert ws(rows, keys, 0, 64, 128, topk, 2) == expect, (rows, keys, topk, k)
+    assert _documented_workspace(1, 1, 2048, 8)[1] == 23  # the stride for topk 2048
+    assert _documented_workspace(1, 1, 512, 8)[1] == 45
