@@ -147,3 +147,29 @@ def test_fused_workspace_follows_the_documented_layout(lib):
         assert ws(rows, keys, 0, 64, 128, topk, 2) == expect, (rows, keys, topk, k)
     assert _documented_workspace(1, 1, 2048, 8)[1] == 23  # the stride for topk 2048
     assert _documented_workspace(1, 1, 512, 8)[1] == 45
+
+
+def test_bindings_refuse_host_tensors(lib):
+    """There is no CPU path: every compute entry point of the binding raises
+    before any library call when handed host tensors."""
+    import pytest
+    import torch
+    import sparse_attention_indexer_tiles_gb300 as pkg
+    q = torch.zeros(4, 8, 64, dtype=torch.bfloat16)
+    k = torch.zeros(100, 64, dtype=torch.bfloat16)
+    sc, w = torch.ones(100), torch.ones(4, 8)
+    ks, ke = torch.zeros(4, dtype=torch.int32), torch.full((4,), 100, dtype=torch.int32)
+    calls = [
+        lambda: pkg.idx_score_topk(q, k, sc, w, ks, ke, 16),
+        lambda: pkg.idx_score_topk_routed(q, k, sc, w, ks, ke, 16),
+        lambda: pkg.idx_score_topk_noalloc(q, k, sc, w, ks, ke, 16),
+        lambda: pkg.idx_score_materialise(q, k, sc, w, ks, ke),
+        lambda: pkg.idx_topk_from_scores(torch.zeros(4, 100), ks, ke, 16),
+        lambda: pkg.idx_page_table_transform(torch.zeros(4, 16, dtype=torch.int32),
+                                             torch.zeros(4, 2, dtype=torch.int32)),
+    ]
+    before = pkg.idx_launch_count()
+    for call in calls:
+        with pytest.raises(ValueError, match="CUDA device"):
+            call()
+    assert pkg.idx_launch_count() == before
