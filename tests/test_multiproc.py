@@ -4,7 +4,6 @@ work of every rank (weak scaling, no collective on the data path)."""
 import os
 import socket
 
-import pytest
 import torch.multiprocessing as mp
 
 
