@@ -38,7 +38,7 @@ WORKLOAD = "fused_prefill"
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--steps", type=int, default=100)
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-extra", action="store_true", help="skip the secondary measurements")
@@ -118,6 +118,21 @@ class ClockSampler:
                 stdout=self.fh, stderr=subprocess.DEVNULL)
         except (OSError, ValueError):
             self.proc = None
+
+    def wait_first(self, timeout: float = 3.0):
+        """Wait (at most `timeout` seconds) until the sampler has written its
+        first sample, so that it is already sampling when the timed region
+        starts."""
+        if self.proc is None:
+            return
+        t0 = time.time()
+        while time.time() - t0 < timeout:
+            try:
+                if os.path.getsize(self.path) > 0:
+                    return
+            except OSError:
+                return
+            time.sleep(0.02)
 
     def stop(self):
         if self.proc is None:
@@ -319,6 +334,7 @@ def main():
     # ------------------------------------------------------------- timed loop
     evs = [idx.StageEvents(5) for _ in range(args.steps)]
     sampler = ClockSampler(local, args.clocks_file)
+    sampler.wait_first()
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
