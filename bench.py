@@ -101,19 +101,35 @@ def recorded_traffic(kernel: str, workload: str):
     return None
 
 
+def smi_gpu_id(device) -> str:
+    """The id under which nvidia-smi knows a torch CUDA device.  nvidia-smi
+    numbers GPUs physically and ignores CUDA_VISIBLE_DEVICES, so the CUDA
+    ordinal can name another GPU of the machine; the device's UUID cannot."""
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(device).uuid)
+    except (AttributeError, RuntimeError):
+        u = ""
+    if u:
+        return u if u.startswith("GPU-") else f"GPU-{u}"
+    idx = device.index if hasattr(device, "index") else int(device)
+    return str(idx or 0)
+
+
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    """nvidia-smi clocks and throttle reasons sampled during the timed region.
+    gpu_id is what nvidia-smi's --id takes: a UUID ("GPU-...") or an index."""
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int, path: str | None):
+    def __init__(self, gpu_id, path: str | None):
         self.path = path or os.path.join("/tmp", f"idx_clocks_{os.getpid()}.csv")
         self.proc = None
         try:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.QUERY}",
+                ["nvidia-smi", f"--id={gpu_id}", f"--query-gpu={self.QUERY}",
                  "--format=csv,noheader,nounits", "-lms", "200"],
                 stdout=self.fh, stderr=subprocess.DEVNULL)
         except (OSError, ValueError):
@@ -333,7 +349,7 @@ def main():
 
     # ------------------------------------------------------------- timed loop
     evs = [idx.StageEvents(5) for _ in range(args.steps)]
-    sampler = ClockSampler(local, args.clocks_file)
+    sampler = ClockSampler(smi_gpu_id(dev), args.clocks_file)
     sampler.wait_first()
     if world > 1:
         torch.distributed.barrier()

@@ -265,6 +265,10 @@ const char* idx_status_string(idx_status s);
 /* Library version, (major << 16) | minor. */
 int idx_version(void);
 
+/* Text of the CUDA error behind the calling thread's last IDX_ECUDA or
+ * IDX_EUNSUPPORTED that came from a CUDA call ("" when there was none). */
+const char* idx_last_cuda_error(void);
+
 /* Number of kernels this library has launched in this process (all devices,
  * all threads); a diagnostic for benchmarks. */
 unsigned long long idx_launch_count(void);

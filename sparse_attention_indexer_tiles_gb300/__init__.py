@@ -112,6 +112,8 @@ def load(path: str | None = None):
     lib.idx_status_string.restype = ctypes.c_char_p
     lib.idx_version.argtypes = []
     lib.idx_version.restype = I
+    lib.idx_last_cuda_error.argtypes = []
+    lib.idx_last_cuda_error.restype = ctypes.c_char_p
     lib.idx_launch_count.argtypes = []
     lib.idx_launch_count.restype = ctypes.c_ulonglong
     _lib = lib
@@ -147,7 +149,9 @@ def idx_status_string(code: int) -> str:
 
 def _check(fn: str, code: int):
     if code != 0:
-        raise IdxError(fn, code, idx_status_string(code))
+        text = idx_status_string(code)
+        cuda = load().idx_last_cuda_error().decode() if code in (4, 5) else ""
+        raise IdxError(fn, code, f"{text} ({cuda})" if cuda else text)
 
 
 def _stream(stream) -> int:
@@ -163,11 +167,21 @@ def _ptr(t) -> int | None:
 
 
 def _dev(*ts):
+    """Check that every tensor is a contiguous CUDA tensor and that all of them
+    live on one device; returns that device."""
+    dev = None
     for t in ts:
-        if t is not None and not t.is_cuda:
+        if t is None:
+            continue
+        if not t.is_cuda:
             raise ValueError("idx: every tensor must live on a CUDA device")
-        if t is not None and not t.is_contiguous():
+        if not t.is_contiguous():
             raise ValueError("idx: tensors must be contiguous")
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise ValueError(f"idx: tensors on different devices ({dev} and {t.device})")
+    return dev
 
 
 def make_options(options: Options | dict | None, stats: Stats | None = None) -> Options | None:
@@ -194,21 +208,22 @@ def idx_score_topk_workspace(rows: int, keys: int, max_len: int, H: int, D: int,
 def idx_score_topk(q, k, k_scale, w, ks, ke, topk: int, *, max_len: int = 0, out=None, ws=None,
                    options=None, stats: Stats | None = None, stream=None):
     """Exact top-k indices [rows, topk] int32 (ascending, -1 padded)."""
-    _dev(q, k, k_scale, w, ks, ke, out, ws)
-    rows, H, D = q.shape
-    keys = k.shape[0]
-    dt = DTYPES[q.dtype]
-    o = make_options(options, stats)
-    need = idx_score_topk_workspace(rows, keys, max_len, H, D, topk, dt, o)
-    if out is None:
-        out = torch.empty(rows, topk, dtype=torch.int32, device=q.device)
-    if ws is None:
-        ws = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
-    _check("idx_score_topk", load().idx_score_topk(
-        _ptr(q), _ptr(k), _ptr(k_scale), _ptr(w), _ptr(ks), _ptr(ke), rows, keys, max_len, H, D,
-        topk, dt, _ptr(out), _ptr(ws), ws.numel() * ws.element_size(), _opt_ref(o),
-        _stream(stream)))
-    return out
+    dev = _dev(q, k, k_scale, w, ks, ke, out, ws)
+    with torch.cuda.device(dev):
+        rows, H, D = q.shape
+        keys = k.shape[0]
+        dt = DTYPES[q.dtype]
+        o = make_options(options, stats)
+        need = idx_score_topk_workspace(rows, keys, max_len, H, D, topk, dt, o)
+        if out is None:
+            out = torch.empty(rows, topk, dtype=torch.int32, device=q.device)
+        if ws is None:
+            ws = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+        _check("idx_score_topk", load().idx_score_topk(
+            _ptr(q), _ptr(k), _ptr(k_scale), _ptr(w), _ptr(ks), _ptr(ke), rows, keys, max_len, H, D,
+            topk, dt, _ptr(out), _ptr(ws), ws.numel() * ws.element_size(), _opt_ref(o),
+            _stream(stream)))
+        return out
 
 
 def idx_topk_workspace(rows: int, row_stride: int, topk: int, options=None) -> int:
@@ -218,58 +233,61 @@ def idx_topk_workspace(rows: int, row_stride: int, topk: int, options=None) -> i
 def idx_topk_from_scores(scores, ks, ke, topk: int, *, out=None, ws=None, options=None,
                          stats: Stats | None = None, stream=None):
     """Exact top-k of fp32 scores [rows, row_stride]; ks may be None."""
-    _dev(scores, ks, ke, out, ws)
-    if scores.dtype != torch.float32:
-        raise ValueError("idx_topk_from_scores: scores must be float32")
-    rows, stride = scores.shape
-    o = make_options(options, stats)
-    need = int(load().idx_topk_workspace(rows, stride, topk, _opt_ref(o)))
-    if out is None:
-        out = torch.empty(rows, topk, dtype=torch.int32, device=scores.device)
-    if ws is None and need:
-        ws = torch.empty(need, dtype=torch.uint8, device=scores.device)
-    nbytes = 0 if ws is None else ws.numel() * ws.element_size()
-    _check("idx_topk_from_scores", load().idx_topk_from_scores(
-        _ptr(scores), stride, _ptr(ks), _ptr(ke), rows, topk, _ptr(out), _ptr(ws), nbytes,
-        _opt_ref(o), _stream(stream)))
-    return out
+    dev = _dev(scores, ks, ke, out, ws)
+    with torch.cuda.device(dev):
+        if scores.dtype != torch.float32:
+            raise ValueError("idx_topk_from_scores: scores must be float32")
+        rows, stride = scores.shape
+        o = make_options(options, stats)
+        need = int(load().idx_topk_workspace(rows, stride, topk, _opt_ref(o)))
+        if out is None:
+            out = torch.empty(rows, topk, dtype=torch.int32, device=scores.device)
+        if ws is None and need:
+            ws = torch.empty(need, dtype=torch.uint8, device=scores.device)
+        nbytes = 0 if ws is None else ws.numel() * ws.element_size()
+        _check("idx_topk_from_scores", load().idx_topk_from_scores(
+            _ptr(scores), stride, _ptr(ks), _ptr(ke), rows, topk, _ptr(out), _ptr(ws), nbytes,
+            _opt_ref(o), _stream(stream)))
+        return out
 
 
 def idx_score_materialise(q, k, k_scale, w, ks, ke, *, out=None, row_stride: int | None = None,
                           options=None, stats: Stats | None = None, stream=None):
     """fp32 scores [rows, row_stride]; row r's key j at column j - ks[r]."""
-    _dev(q, k, k_scale, w, ks, ke, out)
-    rows, H, D = q.shape
-    keys = k.shape[0]
-    if out is None:
-        stride = row_stride or keys
-        out = torch.empty(rows, stride, dtype=torch.float32, device=q.device)
-    stride = out.shape[1]
-    o = make_options(options, stats)
-    _check("idx_score_materialise", load().idx_score_materialise(
-        _ptr(q), _ptr(k), _ptr(k_scale), _ptr(w), _ptr(ks), _ptr(ke), rows, keys, H, D,
-        DTYPES[q.dtype], _ptr(out), stride, _opt_ref(o), _stream(stream)))
-    return out
+    dev = _dev(q, k, k_scale, w, ks, ke, out)
+    with torch.cuda.device(dev):
+        rows, H, D = q.shape
+        keys = k.shape[0]
+        if out is None:
+            stride = row_stride or keys
+            out = torch.empty(rows, stride, dtype=torch.float32, device=q.device)
+        stride = out.shape[1]
+        o = make_options(options, stats)
+        _check("idx_score_materialise", load().idx_score_materialise(
+            _ptr(q), _ptr(k), _ptr(k_scale), _ptr(w), _ptr(ks), _ptr(ke), rows, keys, H, D,
+            DTYPES[q.dtype], _ptr(out), stride, _opt_ref(o), _stream(stream)))
+        return out
 
 
 def idx_score_topk_noalloc(q, k, k_scale, w, ks, ke, topk: int, *, max_len: int = 0, out=None,
                            options=None, stats: Stats | None = None, stream=None):
     """idx_score_topk on the library's built-in scratch array (no workspace,
     no allocation by the library; out is allocated here when not given)."""
-    _dev(q, k, k_scale, w, ks, ke, out)
-    lib = load()
-    fn = lib.idx_score_topk_noalloc
-    P, I, LL = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong
-    fn.argtypes = [P, P, P, P, P, P, I, LL, LL, I, I, I, I, P, P, P]
-    fn.restype = I
-    rows, H, D = q.shape
-    if out is None:
-        out = torch.empty(rows, topk, dtype=torch.int32, device=q.device)
-    o = make_options(options, stats)
-    _check("idx_score_topk_noalloc", fn(
-        _ptr(q), _ptr(k), _ptr(k_scale), _ptr(w), _ptr(ks), _ptr(ke), rows, k.shape[0], max_len,
-        H, D, topk, DTYPES[q.dtype], _ptr(out), _opt_ref(o), _stream(stream)))
-    return out
+    dev = _dev(q, k, k_scale, w, ks, ke, out)
+    with torch.cuda.device(dev):
+        lib = load()
+        fn = lib.idx_score_topk_noalloc
+        P, I, LL = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong
+        fn.argtypes = [P, P, P, P, P, P, I, LL, LL, I, I, I, I, P, P, P]
+        fn.restype = I
+        rows, H, D = q.shape
+        if out is None:
+            out = torch.empty(rows, topk, dtype=torch.int32, device=q.device)
+        o = make_options(options, stats)
+        _check("idx_score_topk_noalloc", fn(
+            _ptr(q), _ptr(k), _ptr(k_scale), _ptr(w), _ptr(ks), _ptr(ke), rows, k.shape[0], max_len,
+            H, D, topk, DTYPES[q.dtype], _ptr(out), _opt_ref(o), _stream(stream)))
+        return out
 
 
 def idx_page_table_transform(idx, table, page_size: int = 64, *, row_map=None, options=None,
@@ -277,17 +295,18 @@ def idx_page_table_transform(idx, table, page_size: int = 64, *, row_map=None, o
     """In place: every position p >= 0 of idx [rows, topk] int32 becomes
     table[t, p // page_size] * page_size + p % page_size (t = row_map[r] or r);
     -1 entries stay.  Returns idx."""
-    _dev(idx, table, row_map)
-    if idx.dtype != torch.int32 or table.dtype != torch.int32:
-        raise ValueError("idx_page_table_transform: idx and table must be int32")
-    if row_map is not None and row_map.dtype != torch.int32:
-        raise ValueError("idx_page_table_transform: row_map must be int32")
-    rows, topk = idx.shape
-    o = make_options(options, stats)
-    _check("idx_page_table_transform", load().idx_page_table_transform(
-        _ptr(idx), rows, topk, _ptr(table), table.shape[0], table.shape[1], _ptr(row_map),
-        page_size, _opt_ref(o), _stream(stream)))
-    return idx
+    dev = _dev(idx, table, row_map)
+    with torch.cuda.device(dev):
+        if idx.dtype != torch.int32 or table.dtype != torch.int32:
+            raise ValueError("idx_page_table_transform: idx and table must be int32")
+        if row_map is not None and row_map.dtype != torch.int32:
+            raise ValueError("idx_page_table_transform: row_map must be int32")
+        rows, topk = idx.shape
+        o = make_options(options, stats)
+        _check("idx_page_table_transform", load().idx_page_table_transform(
+            _ptr(idx), rows, topk, _ptr(table), table.shape[0], table.shape[1], _ptr(row_map),
+            page_size, _opt_ref(o), _stream(stream)))
+        return idx
 
 
 def idx_route_fused(max_len: int, topk: int) -> bool:
@@ -308,19 +327,20 @@ def idx_score_topk_routed(q, k, k_scale, w, ks, ke, topk: int, *, max_len: int =
                           ws=None, options=None, stats: Stats | None = None, stream=None):
     """idx_score_topk by the faster path for the longest row (fused, or the
     logits then their top-k); the same indices either way."""
-    _dev(q, k, k_scale, w, ks, ke, out, ws)
-    rows, H, D = q.shape
-    keys = k.shape[0]
-    dt = DTYPES[q.dtype]
-    o = make_options(options, stats)
-    need = int(load().idx_score_topk_routed_workspace(rows, keys, max_len, H, D, topk, dt,
-                                                      _opt_ref(o)))
-    if out is None:
-        out = torch.empty(rows, topk, dtype=torch.int32, device=q.device)
-    if ws is None:
-        ws = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
-    _check("idx_score_topk_routed", load().idx_score_topk_routed(
-        _ptr(q), _ptr(k), _ptr(k_scale), _ptr(w), _ptr(ks), _ptr(ke), rows, keys, max_len, H, D,
-        topk, dt, _ptr(out), _ptr(ws), ws.numel() * ws.element_size(), _opt_ref(o),
-        _stream(stream)))
-    return out
+    dev = _dev(q, k, k_scale, w, ks, ke, out, ws)
+    with torch.cuda.device(dev):
+        rows, H, D = q.shape
+        keys = k.shape[0]
+        dt = DTYPES[q.dtype]
+        o = make_options(options, stats)
+        need = int(load().idx_score_topk_routed_workspace(rows, keys, max_len, H, D, topk, dt,
+                                                          _opt_ref(o)))
+        if out is None:
+            out = torch.empty(rows, topk, dtype=torch.int32, device=q.device)
+        if ws is None:
+            ws = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+        _check("idx_score_topk_routed", load().idx_score_topk_routed(
+            _ptr(q), _ptr(k), _ptr(k_scale), _ptr(w), _ptr(ks), _ptr(ke), rows, keys, max_len, H, D,
+            topk, dt, _ptr(out), _ptr(ws), ws.numel() * ws.element_size(), _opt_ref(o),
+            _stream(stream)))
+        return out

@@ -129,8 +129,8 @@ int row_split_blocks(int rows, long long row_len_hint, const idx_options* opt) {
 struct FusedParams {
     int cap;    // nominal slab cap
     int cap_q;  // one warp run: ceil(cap / 8) + 64 (a contiguous range of n keys puts
-                // at most n / 8 + 64 of them into the 32-key column of the
-                // even or of the odd 128-key tiles that one run collects)
+                // at most n / 8 + 64 of them into the 32-key column of the even or of the odd
+                // 128-key tiles that one run collects)
     float target;
     int S;
 };
@@ -171,7 +171,7 @@ FusedParams fused_params(int topk, const idx_options* opt) {
 }
 
 struct FusedLayout {
-    size_t plan, run_cnt, slab_s, slab_i, samp, fb_hist, fb_cnt, total;
+    size_t plan, run_cnt, slab, samp, fb_hist, fb_cnt, total;
     long long samp_stride;
 };
 
@@ -186,8 +186,7 @@ FusedLayout fused_layout(int rows, long long max_len, int cap, int cap_q, int S,
     L.samp_stride = max_len / S + 2;
     L.plan = take((size_t)rows * sizeof(RowPlan));
     L.run_cnt = take((size_t)rows * nruns * sizeof(int));
-    L.slab_s = take((size_t)rows * nruns * cap_q * sizeof(float));
-    L.slab_i = take((size_t)rows * nruns * cap_q * sizeof(int));
+    L.slab = take((size_t)rows * nruns * cap_q * sizeof(int2));
     L.samp = take(max_len > cap ? (size_t)rows * L.samp_stride * sizeof(float) : 0);
     L.fb_hist = take(max_len > cap ? (size_t)rows * 4096 * sizeof(uint32_t) : 0);
     L.fb_cnt = take(8 * sizeof(int));
@@ -261,8 +260,12 @@ void record(const idx_options* opt, int i, cudaStream_t s) {
         cudaEventRecord(static_cast<cudaEvent_t>(opt->stage_events[i]), s);
 }
 
+// The CUDA error behind the calling thread's last failed call.
+thread_local cudaError_t t_last_cuda_error = cudaSuccess;
+
 idx_status cuda_status(cudaError_t e) {
     if (e == cudaSuccess) return IDX_OK;
+    t_last_cuda_error = e;
     cudaGetLastError();  // clear a sticky launch error of ours
     return e == cudaErrorNotSupported ? IDX_EUNSUPPORTED : IDX_ECUDA;
 }
@@ -287,7 +290,11 @@ const char* idx_status_string(idx_status s) {
     return "unknown status";
 }
 
-int idx_version(void) { return (0 << 16) | 1; }
+int idx_version(void) { return (0 << 16) | 2; }
+
+const char* idx_last_cuda_error(void) {
+    return t_last_cuda_error == cudaSuccess ? "" : cudaGetErrorString(t_last_cuda_error);
+}
 
 unsigned long long idx_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
@@ -325,8 +332,7 @@ idx_status idx_score_topk(const void* q, const void* k, const float* k_scale, co
     uint8_t* base = static_cast<uint8_t*>(ws);
     RowPlan* plan = reinterpret_cast<RowPlan*>(base + lay.plan);
     int* run_cnt = reinterpret_cast<int*>(base + lay.run_cnt);
-    float* slab_s = reinterpret_cast<float*>(base + lay.slab_s);
-    int* slab_i = reinterpret_cast<int*>(base + lay.slab_i);
+    int2* slab = reinterpret_cast<int2*>(base + lay.slab);
     float* samp = reinterpret_cast<float*>(base + lay.samp);
     uint32_t* fb_hist = reinterpret_cast<uint32_t*>(base + lay.fb_hist);
     int* fb_cnt = reinterpret_cast<int*>(base + lay.fb_cnt);
@@ -336,8 +342,7 @@ idx_status idx_score_topk(const void* q, const void* k, const float* k_scale, co
 
     ScoreLaunch L = make_score_launch(q, k, k_scale, w, ks, ke, rows, keys, H, D, dt, topk, opt);
     L.a.plan = plan;
-    L.a.slab_s = slab_s;
-    L.a.slab_i = slab_i;
+    L.a.slab = slab;
     L.a.cap = p.cap;
     L.a.cap_q = p.cap_q;
     L.a.nruns = nruns;
@@ -346,6 +351,7 @@ idx_status idx_score_topk(const void* q, const void* k, const float* k_scale, co
     L.a.fb_cnt = fb_cnt;
     L.a.S = p.S;
     L.a.nsamp = keys / p.S;
+    L.a.sampled = sampling ? 1 : 0;
     L.a.samp = samp;
     L.a.samp_stride = lay.samp_stride;
     L.a.phase_seed = kPhaseSeed;
@@ -391,8 +397,7 @@ idx_status idx_score_topk(const void* q, const void* k, const float* k_scale, co
     // 4. exact top-k of every slab; rows whose count missed [topk, cap] are flagged
     CandArgs c;
     std::memset(&c, 0, sizeof(c));
-    c.slab_s = slab_s;
-    c.slab_i = slab_i;
+    c.slab = slab;
     c.run_cnt = run_cnt;
     c.cap_q = p.cap_q;
     c.nruns = nruns;

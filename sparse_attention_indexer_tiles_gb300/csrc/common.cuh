@@ -105,6 +105,44 @@ IDX_DEVI bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
     }
 }
 
+#ifndef IDX_EPI_HINT_NS
+#define IDX_EPI_HINT_NS 0
+#endif
+IDX_DEVI bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+IDX_DEVI bool mbar_wait_epi(uint64_t* bar, uint32_t parity, volatile int* abort,
+                            long long limit = (1ll << 32)) {
+#if IDX_EPI_HINT_NS > 0
+    if (mbar_try_wait_hint(bar, parity, IDX_EPI_HINT_NS)) return true;
+    const long long t0 = clock64();
+    for (;;) {
+        if (mbar_try_wait_hint(bar, parity, IDX_EPI_HINT_NS)) return true;
+        if (abort && *abort) return false;
+        if (clock64() - t0 > limit) return false;
+    }
+#elif defined(IDX_EPI_SLEEP_NS)
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    for (;;) {
+        __nanosleep(IDX_EPI_SLEEP_NS);
+        if (mbar_try_wait(bar, parity)) return true;
+        if (abort && *abort) return false;
+        if (clock64() - t0 > limit) return false;
+    }
+#else
+    return mbar_wait(bar, parity, abort, limit);
+#endif
+}
+
 // ------------------------------------------------------------------- TMA
 
 IDX_DEVI void tma_load_2d(void* smem_dst, const void* tmap, uint64_t* bar, int c0, int c1) {
@@ -184,7 +222,7 @@ IDX_DEVI void mma_commit(uint64_t* bar) {
         : "memory");
 }
 
-// 16x256b shape, R repetitions along the columns (R in {1, 2, 4}): thread t
+// 16x256b shape, R repetitions along the columns (R in {1, 2, 4, 8}): thread t
 // gets, for repetition j, lanes t/4 and t/4 + 8 (relative to taddr's lane) at
 // columns 8j + 2(t%4) and 8j + 2(t%4) + 1, in the order (lane t/4, col even),
 // (t/4, odd), (t/4 + 8, even), (t/4 + 8, odd).
@@ -201,8 +239,20 @@ IDX_DEVI void tmem_ld16x256b(uint32_t taddr, float* v) {
             : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
               "=r"(r[7])
             : "r"(taddr));
+    } else if constexpr (R == 8) {
+        asm volatile(
+            "tcgen05.ld.sync.aligned.16x256b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, "
+            "%10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, "
+            "%26, %27, %28, %29, %30, %31}, [%32];"
+            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+              "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+              "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+              "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+              "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+              "=r"(r[31])
+            : "r"(taddr));
     } else {
-        static_assert(R == 4, "1, 2 or 4 repetitions");
+        static_assert(R == 4, "1, 2, 4 or 8 repetitions");
         asm volatile(
             "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, "
             "%10, %11, %12, %13, %14, %15}, [%16];"

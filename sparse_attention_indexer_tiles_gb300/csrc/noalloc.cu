@@ -11,6 +11,7 @@
 #include <cstddef>
 #include <mutex>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "../../include/idx.h"
@@ -22,24 +23,55 @@ namespace {
 // the process exits.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[IDX_NOALLOC_SCRATCH_BYTES];
 
-// In host code the array's name is only a host-side stand-in, so the device
-// address is looked up once per device (with that device current) and cached.
+// In host code the array's name is only a host-side stand-in, so its device
+// address is looked up (cudaGetSymbolAddress, with the device current) the
+// first time a device calls, and cached together with the CUDA context it
+// belongs to: after cudaDeviceReset the device gets a new primary context and
+// a new copy of the array, and the next call looks the address up again.
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void* g_scratch_ptr[kMaxDevices] = {};
+CUcontext g_scratch_ctx[kMaxDevices] = {};
+
+using CtxGetCurrent = CUresult (*)(CUcontext*);
+
+CtxGetCurrent ctx_get_current() {
+    static std::once_flag once;
+    static CtxGetCurrent fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<CtxGetCurrent>(p);
+    });
+    return fn;
+}
 
 idx_status scratch_for_current_device(void** out) {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return IDX_ECUDA;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return IDX_ECUDA;
+    }
+    CtxGetCurrent get = ctx_get_current();
+    if (!get) return IDX_ECUDA;
+    CUcontext ctx = nullptr;
+    if (get(&ctx) != CUDA_SUCCESS) return IDX_ECUDA;
     std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_scratch_ptr[dev]) {
+    if (!ctx || !g_scratch_ptr[dev] || g_scratch_ctx[dev] != ctx) {
+        // the lookup also makes the device's primary context current when no
+        // context was yet
         void* p = nullptr;
         const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (e != cudaSuccess || !p) {
             cudaGetLastError();
             return IDX_ECUDA;
         }
+        if (get(&ctx) != CUDA_SUCCESS || !ctx) return IDX_ECUDA;
         g_scratch_ptr[dev] = p;
+        g_scratch_ctx[dev] = ctx;
     }
     *out = g_scratch_ptr[dev];
     return IDX_OK;
@@ -52,7 +84,10 @@ extern "C" idx_status idx_score_topk_noalloc(const void* q, const void* k, const
                                               int rows, long long keys, long long max_len, int H,
                                               int D, int topk, idx_dtype dt, int* out_idx,
                                               const idx_options* opt, void* stream) {
-    if (rows == 0) return IDX_OK;
+    // no rows: idx_score_topk validates the other arguments and launches nothing
+    if (rows <= 0)
+        return idx_score_topk(q, k, k_scale, w, ks, ke, rows, keys, max_len, H, D, topk, dt,
+                              out_idx, nullptr, 0, opt, stream);
     // the workspace this problem needs must fit in the built-in scratch array
     const size_t need = idx_score_topk_workspace(rows, keys, max_len, H, D, topk, dt, opt);
     if (need > (size_t)IDX_NOALLOC_SCRATCH_BYTES) return IDX_EWORKSPACE;

@@ -39,9 +39,9 @@ struct ScoreArgs {
     long long nsamp;
     uint32_t phase_seed;
     // SM_EMIT / SM_FB_*
+    int sampled;          // the call took thresholds from a sample (rows may exceed cap)
     RowPlan* plan;
-    float* slab_s;
-    int* slab_i;
+    int2* slab;           // [rows, nruns, cap_q] (score bits, row-relative index) pairs
     int cap;              // nominal slab cap (rows seeing <= cap keys emit every key)
     int cap_q;            // capacity of one warp run: slab row = nruns runs of cap_q
     int* run_cnt;         // [rows, nruns] candidates appended per run (may exceed cap_q)

@@ -95,7 +95,10 @@ IDX_DEVI int quad_key_off(int lane) { return (lane >> 2) + 16 * (lane & 1) + 8 *
 template <int H>
 IDX_DEVI float head_reduce_quad(uint32_t taddr, const float2* wq) {
     constexpr int REPS = H / 8;                   // 8-column groups of the row
-    constexpr int RL = H >= 64 ? 2 : (REPS < 4 ? REPS : 4);       // repetitions per load
+#ifndef IDX_RL64
+#define IDX_RL64 2
+#endif
+    constexpr int RL = H >= 64 ? IDX_RL64 : (REPS < 4 ? REPS : 4);  // repetitions per load
     const int lane = threadIdx.x & 31;
     float P[4];
 #pragma unroll
@@ -202,7 +205,17 @@ score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                     // rows that see at most cap keys emit every key (page 1,
                     // section 1: blocks of short rows store every score)
                     active = n > a.topk;
-                    if (active && n > a.cap) thr = a.plan[r].thr;
+                    if (active && n > a.cap) {
+                        if (a.sampled) {
+                            thr = a.plan[r].thr;
+                        } else {
+                            // longer than the max_len the call was sized for: no
+                            // threshold exists; emit nothing, so that the slab
+                            // top-k reports the row (IDX_DEV_RANGE, -1 output)
+                            thr = 0xffffffffu;
+                            raise_status(a.d_status, IDX_DEV_RANGE);
+                        }
+                    }
                     break;
                 case SM_FB_HIST: {
                     const RowPlan p = a.plan[r];
@@ -235,7 +248,8 @@ score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         if (thr <= 0x007fffffu) cut = kAllIdx;
         m[MW_CUT] = cut;
         // rows that take no part: a threshold no score reaches
-        m[MW_THRF] = __float_as_int(active ? key_floor_float(thr) : INFINITY);
+        m[MW_THRF] =
+            __float_as_int(active && thr != 0xffffffffu ? key_floor_float(thr) : INFINITY);
     }
     for (int i = tid; i < C::R * H; i += C::THREADS) {
         const long long r = r0 + i / H;
@@ -423,12 +437,12 @@ score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 e_thr[j] = __int_as_float(row_word(j, MW_THRF));
             }
         }
-        // this warp's runs of its rows: row j's run at ps/pi + j * rstride
+        // this warp's runs of its rows, (score bits, index) pairs: row j's run
+        // at pr + j * rstride
         const int nruns = SPLIT ? a.nruns : kRuns;
         const int split_run0 = SPLIT ? (int)blockIdx.y * kRuns : 0;
         const long long rb = (long long)(r0 + grp * C::RG) * nruns + split_run0 + run;
-        float* const ps = a.slab_s ? a.slab_s + rb * a.cap_q : nullptr;
-        int* const pi = a.slab_i ? a.slab_i + rb * a.cap_q : nullptr;
+        int2* const pr = a.slab ? a.slab + rb * a.cap_q : nullptr;
         const int rstride = nruns * a.cap_q;
 #define RLO(j) row_word(j, MW_LO)
 #define RHI(j) row_word(j, MW_HI)
@@ -436,15 +450,18 @@ score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
 #define RTHR(j) ((uint32_t)row_word(j, MW_THR))
 #define RCUT(j) row_word(j, MW_CUT)
 #define RPRE(j) ((uint32_t)row_word(j, MW_PREFIX))
-        // per-key scale of the team's next tile, loaded one tile ahead
-        auto scale_of = [&](int t) -> float {
-            const long long ki = (long long)(t0 + t) * C::M + q * 32 + quad_key_off(lane);
-            const long long kk = mode == SM_SAMPLE ? phase + (long long)a.S * ki : ki;
-            const bool ok = t < ntiles && (mode == SM_SAMPLE ? ki < a.nsamp : kk < a.keys);
-            return ok ? __ldg(a.k_scale + kk) : 0.f;
-        };
         // this thread's weights: row j, head pair (8 rep + 2c, 8 rep + 2c + 1)
         const int kq = quad_key_off(lane);  // this thread's key in the quarter
+        // Per-key scale of the team's next tile, loaded one tile ahead.  The
+        // thread's tile index i (a key, or a sample index in SM_SAMPLE) grows
+        // by 2 M per team tile; key = i, or phase + S i for the sample.
+        // (keys < 2^31 - 256, so i stays an int; the key offset is only used
+        // while i < ilim, so its 32-bit wrap past the end is harmless)
+        const uint32_t kmul = mode == SM_SAMPLE ? (uint32_t)a.S : 1u;
+        const int ilim = (int)(mode == SM_SAMPLE ? a.nsamp : a.keys);  // i must stay below
+        int s_i = (t0 + team) * C::M + q * 32 + kq;
+        uint32_t s_off = (mode == SM_SAMPLE ? (uint32_t)phase : 0u) + kmul * (uint32_t)s_i;
+        const uint32_t s_step = kmul * 2u * C::M;
         float2 wq[C::RG][H / 8];
 #pragma unroll
         for (int j = 0; j < C::RG; ++j) {
@@ -453,13 +470,15 @@ score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             for (int rp = 0; rp < H / 8; ++rp) wq[j][rp] = make_float2(wr[8 * rp], wr[8 * rp + 1]);
         }
         const int all_lo = misc[3], all_hi = misc[4];
-        float next_scale = scale_of(team);
+        float next_scale = team < ntiles && s_i < ilim ? __ldg(a.k_scale + s_off) : 0.f;
         const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(team * C::N);
         for (int i = team, u = 0; i < ntiles; i += 2, ++u) {
             const float cur_scale = next_scale;
-            next_scale = scale_of(i + 2);
+            s_i += 2 * C::M;
+            s_off += s_step;
+            next_scale = i + 2 < ntiles && s_i < ilim ? __ldg(a.k_scale + s_off) : 0.f;
             // warp-uniform outcome: the TMEM loads below are .sync.aligned
-            if (!__all_sync(0xffffffffu, mbar_wait(&accf[team], (uint32_t)(u & 1), abort_flag))) {
+            if (!__all_sync(0xffffffffu, mbar_wait_epi(&accf[team], (uint32_t)(u & 1), abort_flag))) {
                 *abort_flag = 1;
                 if (lane == 0) raise_status(a.d_status, IDX_DEV_TIMEOUT);
                 break;
@@ -513,26 +532,23 @@ score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                         atomicAdd(&a.fb_hist[(long long)(r0 + grp * C::RG + j) * kHistBins + dg],
                                   (uint32_t)__popc(same));
                 }
-            } else if (C::RG > 2 && mode == SM_EMIT && (t0 + i) * C::M >= all_lo &&
+            } else if (mode == SM_EMIT && (t0 + i) * C::M >= all_lo &&
                        (t0 + i + 1) * C::M <= all_hi) {
                 // SM_EMIT on a tile every active row sees whole: the rule is
-                // s >= T_r (rows that take no part have T = +inf).  Taken for
-                // four or more rows per warp (H <= 32), where the per-row test
-                // is a large share of the epilogue.
+                // s >= T_r (rows that take no part have T = +inf).  Branch
+                // free: a lane's place in the run is the number of hits of
+                // lower lanes (earlier keys).
 #pragma unroll
                 for (int j = 0; j < C::RG; ++j) {
                     const float thr = HOIST ? e_thr[HOIST ? j : 0]
                                             : __int_as_float(row_word(j, MW_THRF));
                     const bool hit = sc[j] >= thr;
                     const uint32_t A = __ballot_sync(0xffffffffu, hit);
-                    if (A) {
-                        const int pos = cnt[j] + __popc(A & lt);
-                        if (hit && pos < a.cap_q) {
-                            ps[j * rstride + pos] = sc[j];
-                            pi[j * rstride + pos] = kidx - (HOIST ? e_lo[HOIST ? j : 0] : RLO(j));
-                        }
-                        cnt[j] += __popc(A);
-                    }
+                    const int pos = cnt[j] + __popc(A & lt);
+                    if (hit && pos < a.cap_q)
+                        pr[j * rstride + pos] = make_int2(
+                            __float_as_int(sc[j]), kidx - (HOIST ? e_lo[HOIST ? j : 0] : RLO(j)));
+                    cnt[j] += __popc(A);
                 }
             } else {
                 // SM_EMIT / SM_FB_EMIT: append every key that passes the row's
@@ -548,14 +564,10 @@ score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                     const bool hit = (uint32_t)off < (uint32_t)len &&
                                      (sc[j] > thr || (sc[j] == thr && off <= cut));
                     const uint32_t A = __ballot_sync(0xffffffffu, hit);
-                    if (A) {
-                        const int pos = cnt[j] + __popc(A & lt);
-                        if (hit && pos < a.cap_q) {
-                            ps[j * rstride + pos] = sc[j];
-                            pi[j * rstride + pos] = off;
-                        }
-                        cnt[j] += __popc(A);
-                    }
+                    const int pos = cnt[j] + __popc(A & lt);
+                    if (hit && pos < a.cap_q)
+                        pr[j * rstride + pos] = make_int2(__float_as_int(sc[j]), off);
+                    cnt[j] += __popc(A);
                 }
             }
         }

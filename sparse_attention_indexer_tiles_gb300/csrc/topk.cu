@@ -1036,8 +1036,7 @@ cand_topk_kernel(CandArgs a) {
         }
 
         // load the runs back to back, four independent loads per thread in flight
-        const float* ss = a.slab_s + (long long)r * CR;
-        const int* si = a.slab_i + (long long)r * CR;
+        const int2* sl = a.slab + (long long)r * CR;
         const uint32_t cnt = run_off[a.nruns];
         for (uint32_t base = 0; base < cnt; base += 4 * THREADS) {
             float sv[4];
@@ -1060,8 +1059,9 @@ cand_topk_kernel(CandArgs a) {
                         }
                     }
                     const uint32_t src = (uint32_t)q * (uint32_t)a.cap_q + (e - run_off[q]);
-                    sv[u] = ss[src];
-                    iv[u] = si[src];
+                    const int2 c = sl[src];
+                    sv[u] = __int_as_float(c.x);
+                    iv[u] = c.y;
                 }
             }
 #pragma unroll

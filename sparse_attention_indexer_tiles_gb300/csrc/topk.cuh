@@ -46,8 +46,7 @@ struct TopkRowsArgs {
 };
 
 struct CandArgs {
-    const float* slab_s;  // [rows, nruns, cap_q]
-    const int* slab_i;    // [rows, nruns, cap_q]
+    const int2* slab;     // [rows, nruns, cap_q] (score bits, row-relative index) pairs
     const int* run_cnt;   // [rows, nruns]
     int nruns;            // kRuns per key split of the emit pass
     int cap_q;

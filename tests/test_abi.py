@@ -114,7 +114,7 @@ def test_routing_gate_rule(lib):
 def _documented_workspace(rows, max_len, topk, nruns):
     """The fused workspace as the layout is documented: 256-byte aligned
     regions for the row plans (32 B each), the run counts [rows, nruns] int32,
-    the slab [rows, nruns, cap_q] fp32 scores and int32 indices with
+    the slab [rows, nruns, cap_q] of (fp32 score, int32 index) pairs with
     cap_q = ceil(cap / 8) + 64, the sample scratch [rows, max_len // S + 2]
     fp32 and the rescan histograms [rows, 4096] (both only when rows can see
     more than cap keys), and eight rescan counters."""
@@ -126,7 +126,7 @@ def _documented_workspace(rows, max_len, topk, nruns):
     t = max(32.0, (4.5 / math.log(max(target, 1.0001))) ** 2)
     S = max(s for s in (1, 3, 5, 7, 11, 15, 23, 31, 45, 63) if s <= target * topk / t)
     sampled = max_len > cap
-    regions = [rows * 32, rows * nruns * 4, rows * nruns * cap_q * 4, rows * nruns * cap_q * 4,
+    regions = [rows * 32, rows * nruns * 4, rows * nruns * cap_q * 8,
                rows * (max_len // S + 2) * 4 if sampled else 0,
                rows * 4096 * 4 if sampled else 0, 8 * 4]
     return sum(up(r) for r in regions), S
@@ -173,3 +173,17 @@ def test_bindings_refuse_host_tensors(lib):
         with pytest.raises(ValueError, match="CUDA device"):
             call()
     assert pkg.idx_launch_count() == before
+
+
+def test_bindings_refuse_tensors_on_two_devices():
+    """Every tensor of a call must live on one device: the call runs with that
+    device current (its stream, its copy of the library's state)."""
+    import types
+    import pytest
+    import sparse_attention_indexer_tiles_gb300 as pkg
+
+    def fake(dev):
+        return types.SimpleNamespace(is_cuda=True, is_contiguous=lambda: True, device=dev)
+    assert pkg._dev(fake("cuda:1"), None, fake("cuda:1")) == "cuda:1"
+    with pytest.raises(ValueError, match="different devices"):
+        pkg._dev(fake("cuda:0"), fake("cuda:1"))

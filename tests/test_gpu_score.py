@@ -262,3 +262,53 @@ def test_materialise_few_rows_long_keys(idx):
     for i, r in enumerate([0, 2]):
         n = int(ke[r] - ks[r])
         check_scores(got[r, :n], sc[i, :n])
+
+
+def test_rows_beyond_max_len_are_reported(idx):
+    """A call sized for max_len <= cap takes no sample.  A row longer than that
+    bound is reported (IDX_DEV_RANGE, -1 output) and never selected from a
+    threshold an earlier call left in the workspace; rows within the bound are
+    exact."""
+    ks = torch.zeros(8, dtype=torch.int32)
+    ke = torch.tensor([3000, 20000, 2500, 20000, 4000, 20000, 100, 20000], dtype=torch.int32)
+    inp = synth.indexer_inputs(8, 20000, 64, 128, 256, "fp8", seed=51, ranges="given", ks=ks,
+                               ke=ke)
+    g = to_dev(inp)
+    need = idx.idx_score_topk_workspace(8, 20000, 0, 64, 128, 256, inp.q.dtype)
+    ws = torch.empty(need, dtype=torch.uint8, device=DEV)
+    # a sampled call first: it leaves row plans in the workspace
+    first = idx.idx_score_topk(g["q"], g["k"], g["k_scale"], g["w"], g["ks"], g["ke"], 256,
+                               ws=ws)
+    check_fused(inp, first.cpu().numpy())
+    stats = idx.Stats(torch.device(DEV))
+    got = idx.idx_score_topk(g["q"], g["k"], g["k_scale"], g["w"], g["ks"], g["ke"], 256,
+                             max_len=4096, ws=ws, stats=stats)
+    torch.cuda.synchronize()
+    got = got.cpu().numpy()
+    st = stats.read()
+    assert st["status"] & 2  # IDX_DEV_RANGE
+    long_rows = [1, 3, 5, 7]
+    assert (got[long_rows] == -1).all()
+    short = [r for r in range(8) if r not in long_rows]
+    check_fused(inp, got, rows=short)
+    assert np.array_equal(got[short], first.cpu().numpy()[short])
+
+
+@pytest.mark.parametrize("name", ["fused_prefill", "long_context"])
+def test_full_size_scores_on_sampled_rows(idx, name):
+    """Every score of 64 seeded rows of a full-size workload, computed by the
+    launch configuration of the whole workload (all row blocks, the key split
+    the full grid takes, key indices far beyond 2^16), within
+    1e-3 * max(1, |s|) of the oracle's fp64 scores."""
+    inp = synth.workload(name)
+    g = to_dev(inp)
+    n = (inp.ke - inp.ks).numpy()
+    S = torch.empty(inp.rows, int(n.max()), dtype=torch.float32, device=DEV)
+    idx.idx_score_materialise(g["q"], g["k"], g["k_scale"], g["w"], g["ks"], g["ke"], out=S)
+    rows = synth.sample_rows(inp.ks, inp.ke, 64, seed=inp.meta["seed"] + 7)
+    got = S[torch.as_tensor(rows, device=DEV)].cpu().numpy()
+    del S, g
+    torch.cuda.empty_cache()
+    _, sc = oracle.score_topk(inp, rows=rows, want_scores=True)
+    for i, r in enumerate(rows):
+        check_scores(got[i, :n[r]], sc[i, :n[r]])

@@ -65,11 +65,46 @@ def test_noalloc_matches_workspace_path_twice(lib):
     assert np.array_equal(got1, _with_workspace(inp1, g1))
 
     inp2, g2 = _inputs(91, 40, 30000, 32, 128, 300)
-    opts = pkg.Options(cap_factor=2.0, target_factor=0.5)
+    stats = pkg.Stats(torch.device(DEV))
+    opts = pkg.make_options(pkg.Options(cap_factor=2.0, target_factor=0.5), stats)
     st, got2 = _noalloc(lib, inp2, g2, opts)
     assert st == 0
+    rec = stats.read()
+    # the rescan really ran, on the plan, histograms and counters the first
+    # call left in the shared array
+    assert rec["fallback_rows"] > 0 and rec["status"] == 0
     assert np.array_equal(got2, _with_workspace(inp2, g2, pkg.Options(cap_factor=2.0,
                                                                       target_factor=0.5)))
+
+
+def test_noalloc_sampling_call_after_a_short_rows_call(lib):
+    # a call whose rows all fit the slab (no sample, no rescan counters reset)
+    # followed by one that samples and rescans: the second must not read
+    # anything the first left behind
+    import sparse_attention_indexer_tiles_gb300 as pkg
+    inp1, g1 = _inputs(93, 48, 3000, 64, 128, 256)
+    st, got1 = _noalloc(lib, inp1, g1)
+    assert st == 0
+    assert np.array_equal(got1, _with_workspace(inp1, g1))
+
+    inp2, g2 = _inputs(94, 24, 40000, 64, 128, 300)
+    stats = pkg.Stats(torch.device(DEV))
+    opts = pkg.make_options(pkg.Options(cap_factor=2.0, target_factor=0.5), stats)
+    st, got2 = _noalloc(lib, inp2, g2, opts)
+    assert st == 0
+    rec = stats.read()
+    assert rec["fallback_rows"] > 0 and rec["status"] == 0
+    assert np.array_equal(got2, _with_workspace(inp2, g2, pkg.Options(cap_factor=2.0,
+                                                                      target_factor=0.5)))
+
+
+def test_noalloc_without_rows_still_checks_its_arguments(lib):
+    # no rows launches nothing, but an invalid topk is refused as by idx_score_topk
+    null = None
+    assert lib.idx_score_topk_noalloc(null, null, null, null, null, null, 0, 100, 0, 64, 128, 16,
+                                      2, null, null, null) == 0
+    assert lib.idx_score_topk_noalloc(null, null, null, null, null, null, 0, 100, 0, 64, 128, 0,
+                                      2, null, null, null) == 1  # IDX_EINVAL
 
 
 def test_noalloc_refuses_problems_beyond_the_array(lib):
