@@ -105,44 +105,6 @@ IDX_DEVI bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
     }
 }
 
-#ifndef IDX_EPI_HINT_NS
-#define IDX_EPI_HINT_NS 0
-#endif
-IDX_DEVI bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity, uint32_t ns) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
-        : "memory");
-    return ok != 0;
-}
-IDX_DEVI bool mbar_wait_epi(uint64_t* bar, uint32_t parity, volatile int* abort,
-                            long long limit = (1ll << 32)) {
-#if IDX_EPI_HINT_NS > 0
-    if (mbar_try_wait_hint(bar, parity, IDX_EPI_HINT_NS)) return true;
-    const long long t0 = clock64();
-    for (;;) {
-        if (mbar_try_wait_hint(bar, parity, IDX_EPI_HINT_NS)) return true;
-        if (abort && *abort) return false;
-        if (clock64() - t0 > limit) return false;
-    }
-#elif defined(IDX_EPI_SLEEP_NS)
-    if (mbar_try_wait(bar, parity)) return true;
-    const long long t0 = clock64();
-    for (;;) {
-        __nanosleep(IDX_EPI_SLEEP_NS);
-        if (mbar_try_wait(bar, parity)) return true;
-        if (abort && *abort) return false;
-        if (clock64() - t0 > limit) return false;
-    }
-#else
-    return mbar_wait(bar, parity, abort, limit);
-#endif
-}
-
 // ------------------------------------------------------------------- TMA
 
 IDX_DEVI void tma_load_2d(void* smem_dst, const void* tmap, uint64_t* bar, int c0, int c1) {

@@ -95,10 +95,7 @@ IDX_DEVI int quad_key_off(int lane) { return (lane >> 2) + 16 * (lane & 1) + 8 *
 template <int H>
 IDX_DEVI float head_reduce_quad(uint32_t taddr, const float2* wq) {
     constexpr int REPS = H / 8;                   // 8-column groups of the row
-#ifndef IDX_RL64
-#define IDX_RL64 2
-#endif
-    constexpr int RL = H >= 64 ? IDX_RL64 : (REPS < 4 ? REPS : 4);  // repetitions per load
+    constexpr int RL = H >= 64 ? 2 : (REPS < 4 ? REPS : 4);       // repetitions per load
     const int lane = threadIdx.x & 31;
     float P[4];
 #pragma unroll
@@ -478,7 +475,7 @@ score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             s_off += s_step;
             next_scale = i + 2 < ntiles && s_i < ilim ? __ldg(a.k_scale + s_off) : 0.f;
             // warp-uniform outcome: the TMEM loads below are .sync.aligned
-            if (!__all_sync(0xffffffffu, mbar_wait_epi(&accf[team], (uint32_t)(u & 1), abort_flag))) {
+            if (!__all_sync(0xffffffffu, mbar_wait(&accf[team], (uint32_t)(u & 1), abort_flag))) {
                 *abort_flag = 1;
                 if (lane == 0) raise_status(a.d_status, IDX_DEV_TIMEOUT);
                 break;
