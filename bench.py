@@ -427,13 +427,45 @@ def main():
 
     # ------------------------------------------------------ secondary numbers
     if not args.no_extra and rank == 0:
-        line["extra"] = secondary(idx, dev, g, inp, out, ws, flush, pk, args)
+        line["extra"] = secondary(idx, dev, g, inp, out, ws, flush, pk, args, ms)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_sample(inp)
+    if "extra" in line:
+        # the headline figures of the other workloads, last on the line
+        line.update(summary(line))
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def summary(line):
+    """One short entry per measured workload, for the end of the JSON line:
+    the standalone top-k (rows/s, fraction of the HBM copy peak), each fused
+    workload's whole call against the fp8 tensor peak, and the fused over
+    two-pass speed-ups."""
+    ex = line["extra"]
+    st = ex["standalone_topk"]
+    out = {"standalone_topk": {"rows_per_s": st["rows_per_s"], "ms": st["ms"],
+                               "hbm_frac": st["roofline"]["frac"],
+                               "workload": st["workload"].split(",")[0]},
+           "fused_prefill": {"pairs_per_s": line["value"], "ms": line["ms_per_step"],
+                             "whole_call_tensor_frac": line["whole_step_tensor_frac"],
+                             "emit_tensor_frac": line["roofline"]["frac"],
+                             "fused_over_two_pass": ex["two_pass"]["fused_over_two_pass"]}}
+    for name in ("long_context", "mixed_batch", "decode"):
+        w = ex.get(name)
+        if not w:
+            continue
+        out[name] = {"pairs_per_s": w["pairs_per_s"], "ms": w["ms"],
+                     "whole_call_tensor_frac": w["whole_call_tensor_frac"],
+                     "emit_tensor_frac": w["emit_roofline"]["frac"],
+                     "fused_over_two_pass": w.get("two_pass", {}).get("fused_over_two_pass"),
+                     "fallback_rows": w["path_stats"]["fallback_rows"]}
+    sp = ex["split_topk"]
+    out["split_topk"] = {"rows_per_s": sp["rows_per_s"], "ms": sp["ms"],
+                         "hbm_frac": sp["roofline"]["frac"]}
+    return {"summary": out}
 
 
 def last_rows(inp, n):
@@ -460,42 +492,60 @@ def timed(fn, flush, reps):
     return statistics.mean(ts)
 
 
-def secondary(idx, dev, g, inp, out, ws, flush, pk, args):
-    """Standalone top-k rows/s (HBM roofline) and the two-pass baseline."""
+def two_pass(idx, dev, g, inp, out, flush, reps=5):
+    """The two-pass baseline on a workload: materialise the fp32 logits
+    [rows, longest visible range], then their exact top-k; timed separately,
+    L2 flushed before each, and checked against the fused path's indices."""
     import torch
-    import synth
-    res = {}
-    # two-pass baseline on the same workload: materialise [rows, keys] fp32, then top-k
     n_max = int((inp.ke - inp.ks).max())
     S = torch.empty(inp.rows, n_max, dtype=torch.float32, device=dev)
     out2 = torch.empty_like(out)
     rel = idx.Options(relative_rows=1)
+    need = idx.idx_topk_workspace(inp.rows, n_max, inp.topk, rel)
+    tws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
 
     def mat():
         idx.idx_score_materialise(g["q"], g["k"], g["k_scale"], g["w"], g["ks"], g["ke"], out=S)
 
     def tk():
-        idx.idx_topk_from_scores(S, g["ks"], g["ke"], inp.topk, out=out2, options=rel)
+        idx.idx_topk_from_scores(S, g["ks"], g["ke"], inp.topk, out=out2, ws=tws, options=rel)
 
     for _ in range(2):
         mat()
         tk()
-    t_mat = timed(mat, flush, 5)
-    t_tk = timed(tk, flush, 5)
-    res["two_pass_ms"] = {"materialise": t_mat, "topk": t_tk, "total": t_mat + t_tk}
-    res["two_pass_identical"] = bool(torch.equal(out, out2))
-    flops = 2.0 * inp.H * inp.D * inp.pairs()
-    res["materialise_roofline"] = {"bound": "tensor", "achieved": flops / (t_mat * 1e-3) / 1e12,
-                                   "unit": "TFLOP/s"}
-    del S
+    t_mat = timed(mat, flush, reps)
+    t_tk = timed(tk, flush, reps)
+    identical = bool(torch.equal(out, out2))
+    del S, out2, tws
     torch.cuda.empty_cache()
+    flops = 2.0 * inp.H * inp.D * inp.pairs()
+    return {"materialise_ms": t_mat, "topk_ms": t_tk, "total_ms": t_mat + t_tk,
+            "identical_indices": identical,
+            "logits_bytes": 4 * inp.rows * n_max,
+            "materialise_tflops": flops / (t_mat * 1e-3) / 1e12}
 
-    res["standalone_topk"] = standalone_topk(idx, dev, flush, pk, args)
+
+def secondary(idx, dev, g, inp, out, ws, flush, pk, args, fused_ms):
+    """Standalone top-k rows/s (HBM roofline), the row split, the other fused
+    workloads (with their two-pass baselines), a decode-shaped call, the tiny
+    workload and the page-table transform."""
+    import torch
+    import synth
+    res = {}
+    tp = two_pass(idx, dev, g, inp, out, flush)
+    tp["fused_over_two_pass"] = tp["total_ms"] / fused_ms
+    res["two_pass"] = tp
     res["split_topk"] = split_topk(idx, dev, flush, pk, args)
-    for name in ("long_context", "mixed_batch", "tiny"):
-        res[name] = other_fused(idx, dev, flush, pk, args, name)
-        torch.cuda.empty_cache()
+    res["long_context"] = other_fused(idx, dev, flush, pk, args, "long_context", with_two_pass=True)
+    torch.cuda.empty_cache()
+    res["mixed_batch"] = other_fused(idx, dev, flush, pk, args, "mixed_batch", with_two_pass=True)
+    torch.cuda.empty_cache()
+    dec = synth.indexer_inputs(16, 1 << 20, 32, 128, 2048, "fp8", seed=6, ranges="full")
+    res["decode"] = other_fused(idx, dev, flush, pk, args, "decode", inp=dec, with_two_pass=True)
+    torch.cuda.empty_cache()
+    res["tiny"] = other_fused(idx, dev, flush, pk, args, "tiny")
     res["page_table_transform"] = page_transform(idx, dev, flush, pk, out, inp)
+    res["standalone_topk"] = standalone_topk(idx, dev, flush, pk, args)
     return res
 
 
@@ -568,12 +618,13 @@ def route_sweep(idx, dev):
             torch.cuda.empty_cache()
 
 
-def other_fused(idx, dev, flush, pk, args, name):
+def other_fused(idx, dev, flush, pk, args, name, inp=None, with_two_pass=False):
     """idx_score_topk on another fused workload: whole-call pairs/s and the
-    emit pass against the fp8 tensor peak, with the path counters."""
+    emit pass against the fp8 tensor peak, with the path counters (and the
+    two-pass baseline on the same inputs when asked)."""
     import torch
     import synth
-    inp = synth.workload(name)
+    inp = inp if inp is not None else synth.workload(name)
     g = {n: getattr(inp, n).to(dev) for n in ("q", "k", "k_scale", "w", "ks", "ke")}
     out = torch.empty(inp.rows, inp.topk, dtype=torch.int32, device=dev)
     need = idx.idx_score_topk_workspace(inp.rows, inp.keys, 0, inp.H, inp.D, inp.topk,
@@ -607,9 +658,9 @@ def other_fused(idx, dev, flush, pk, args, name):
     # fp8 dense = 2 x bf16 dense (nominal ratio); bf16 inputs run at the bf16 peak
     peak = pk["bf16_tflops"] * (1.0 if inp.q.dtype == torch.bfloat16 else 2.0)
     emit_tf = flops / (emit_ms * 1e-3) / 1e12
-    return {"workload": f"{name}: rows={inp.rows} keys={inp.keys} H={inp.H} D={inp.D} "
-                        f"topk={inp.topk}",
-            "pairs_per_s": pairs / (ms * 1e-3), "ms": ms,
+    res = {"workload": f"{name}: rows={inp.rows} keys={inp.keys} H={inp.H} D={inp.D} "
+                       f"topk={inp.topk}",
+           "pairs_per_s": pairs / (ms * 1e-3), "rows_per_s": inp.rows / (ms * 1e-3), "ms": ms,
             "stage_ms": {"sample_and_threshold": statistics.mean(e.elapsed(0, 1) for e in evs),
                          "score_and_emit": emit_ms,
                          "slab_topk": statistics.mean(e.elapsed(2, 3) for e in evs),
@@ -618,6 +669,11 @@ def other_fused(idx, dev, flush, pk, args, name):
                               "unit": "TFLOP/s", "frac": emit_tf / peak},
             "whole_call_tensor_frac": flops / (ms * 1e-3) / 1e12 / peak,
             "path_stats": stats.read()}
+    if with_two_pass:
+        tp = two_pass(idx, dev, g, inp, out, flush, reps=3)
+        tp["fused_over_two_pass"] = tp["total_ms"] / ms
+        res["two_pass"] = tp
+    return res
 
 
 def split_topk(idx, dev, flush, pk, args):

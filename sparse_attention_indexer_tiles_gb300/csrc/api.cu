@@ -171,11 +171,13 @@ FusedParams fused_params(int topk, const idx_options* opt) {
 }
 
 struct FusedLayout {
-    size_t plan, run_cnt, slab, samp, fb_hist, fb_cnt, total;
+    size_t plan, run_cnt, slab, samp, fb_hist, fb_blocks, fb_bflag, fb_cnt, total;
     long long samp_stride;
 };
 
-FusedLayout fused_layout(int rows, long long max_len, int cap, int cap_q, int S, int nruns) {
+FusedLayout fused_layout(int rows, long long max_len, int cap, int cap_q, int S, int nruns,
+                         int H) {
+    const size_t nblk = (size_t)((rows + score_rows_per_block(H) - 1) / score_rows_per_block(H));
     FusedLayout L;
     size_t off = 0;
     auto take = [&](size_t bytes) {
@@ -189,6 +191,8 @@ FusedLayout fused_layout(int rows, long long max_len, int cap, int cap_q, int S,
     L.slab = take((size_t)rows * nruns * cap_q * sizeof(int2));
     L.samp = take(max_len > cap ? (size_t)rows * L.samp_stride * sizeof(float) : 0);
     L.fb_hist = take(max_len > cap ? (size_t)rows * 4096 * sizeof(uint32_t) : 0);
+    L.fb_blocks = take(max_len > cap ? nblk * sizeof(int) : 0);
+    L.fb_bflag = take(max_len > cap ? nblk * sizeof(int) : 0);
     L.fb_cnt = take(8 * sizeof(int));
     L.total = off;
     return L;
@@ -307,7 +311,7 @@ size_t idx_score_topk_workspace(int rows, long long keys, long long max_len, int
     if (max_len <= 0 || max_len > keys) max_len = keys;
     const FusedParams p = fused_params(topk, opt);
     const int nruns = kRuns * score_ksplit(rows, H, max_len);
-    return fused_layout(rows, max_len, p.cap, p.cap_q, p.S, nruns).total;
+    return fused_layout(rows, max_len, p.cap, p.cap_q, p.S, nruns, H).total;
 }
 
 idx_status idx_score_topk(const void* q, const void* k, const float* k_scale, const float* w,
@@ -325,7 +329,7 @@ idx_status idx_score_topk(const void* q, const void* k, const float* k_scale, co
     if (p.cap > kMaxCap || p.S < 1) return IDX_EUNSUPPORTED;
     const int ksplit = score_ksplit(rows, H, max_len);
     const int nruns = kRuns * ksplit;
-    const FusedLayout lay = fused_layout(rows, max_len, p.cap, p.cap_q, p.S, nruns);
+    const FusedLayout lay = fused_layout(rows, max_len, p.cap, p.cap_q, p.S, nruns, H);
     if (!ws || ws_bytes < lay.total) return IDX_EWORKSPACE;
     if (!aligned(ws, 256)) return IDX_EALIGN;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -336,9 +340,11 @@ idx_status idx_score_topk(const void* q, const void* k, const float* k_scale, co
     float* samp = reinterpret_cast<float*>(base + lay.samp);
     uint32_t* fb_hist = reinterpret_cast<uint32_t*>(base + lay.fb_hist);
     int* fb_cnt = reinterpret_cast<int*>(base + lay.fb_cnt);
+    const bool sampling = max_len > p.cap;
+    int* fb_blocks = sampling ? reinterpret_cast<int*>(base + lay.fb_blocks) : nullptr;
+    int* fb_bflag = sampling ? reinterpret_cast<int*>(base + lay.fb_bflag) : nullptr;
     int* d_status = opt ? opt->d_status : nullptr;
     idx_stats* d_stats = opt ? opt->d_stats : nullptr;
-    const bool sampling = max_len > p.cap;
 
     ScoreLaunch L = make_score_launch(q, k, k_scale, w, ks, ke, rows, keys, H, D, dt, topk, opt);
     L.a.plan = plan;
@@ -349,6 +355,8 @@ idx_status idx_score_topk(const void* q, const void* k, const float* k_scale, co
     L.a.run_cnt = run_cnt;
     L.a.fb_hist = fb_hist;
     L.a.fb_cnt = fb_cnt;
+    L.a.fb_blocks = fb_blocks;
+    L.a.fb_bflag = fb_bflag;
     L.a.S = p.S;
     L.a.nsamp = keys / p.S;
     L.a.sampled = sampling ? 1 : 0;
@@ -404,6 +412,9 @@ idx_status idx_score_topk(const void* q, const void* k, const float* k_scale, co
     c.plan = plan;
     c.fb_hist = sampling ? fb_hist : nullptr;
     c.fb_cnt = fb_cnt;
+    c.fb_blocks = fb_blocks;
+    c.fb_bflag = fb_bflag;
+    c.rows_per_block = score_rows_per_block(H);
     c.ks = ks;
     c.ke = ke;
     c.rows = rows;
@@ -418,16 +429,13 @@ idx_status idx_score_topk(const void* q, const void* k, const float* k_scale, co
     count_launches(1);
     record(opt, 3, s);
     if (sampling) {
-        // 5. exact rescan of flagged rows: up to six digit passes (three over the
-        //    score key, three over the index of exact ties), each finishing its
-        //    digit step in the CTA that owns the row, then one re-emission;
-        //    passes with no row waiting exit at once
-        for (int level = 0; level <= 5; ++level) {
-            L.a.mode = SM_FB_HIST;
-            L.a.level = level;
-            if ((e = launch_score(L, s)) != cudaSuccess) return cuda_status(e);
-        }
-        L.a.mode = SM_FB_EMIT;
+        // 5. exact rescan of flagged rows, one launch: a grid of at most one CTA
+        //    per SM strides over the device list of flagged row blocks; per block
+        //    up to six digit passes (three over the score key, three over the
+        //    index of exact ties), each finishing its digit step in the CTA, then
+        //    one re-emission.  With no block listed every CTA ends at once.
+        L.a.mode = SM_RESCAN;
+        L.a.grid_x = sm_count();
         if ((e = launch_score(L, s)) != cudaSuccess) return cuda_status(e);
         c.fallback = 1;
         if ((e = launch_cand_topk(c, s)) != cudaSuccess) return cuda_status(e);

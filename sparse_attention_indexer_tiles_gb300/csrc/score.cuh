@@ -18,6 +18,8 @@ enum : int {
     SM_EMIT = 2,         // main pass: emit key >= T_r into the slab
     SM_FB_HIST = 3,      // exact rescan: histogram one digit of flagged rows
     SM_FB_EMIT = 4,      // exact rescan: re-emit flagged rows with the refined rule
+    SM_RESCAN = 5,       // the exact rescan as one launch: per flagged row block, the
+                         // SM_FB_HIST passes it needs, then SM_FB_EMIT
 };
 
 struct ScoreArgs {
@@ -49,7 +51,11 @@ struct ScoreArgs {
     int ksplit;           // key splits of this launch (grid.y): CTA (b, c) scores the
                           // c-th contiguous part of row block b's key tiles
     uint32_t* fb_hist;
-    int* fb_cnt;          // [8] rows waiting per rescan level, [6] ready to emit
+    int* fb_cnt;          // [8] rows waiting per rescan level, [6] ready to emit,
+                          // [7] row blocks listed in fb_blocks
+    int* fb_blocks;       // [row blocks] the blocks with a row in the rescan
+    int* fb_bflag;        // [row blocks] 1 once a block is listed
+    int grid_x;           // CTAs of an SM_RESCAN launch (they stride over the list)
     int level;
     int* d_status;
     idx_stats* d_stats;

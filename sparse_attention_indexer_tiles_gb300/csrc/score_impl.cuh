@@ -131,15 +131,16 @@ IDX_DEVI float head_reduce_quad(uint32_t taddr, const float2* wq) {
 // SPLIT: the launch splits row blocks over key ranges (grid.y) or addresses a
 // slab with more than kRuns runs per row; without it the kernel is compiled
 // with kRuns runs per row and no split arithmetic.
+// One pass of the CTA over row block blk in scoring mode `mode` (rescan
+// histogram passes: digit `level`).  Every thread of the CTA calls it; it ends
+// with the CTA synchronised and no copy or MMA in flight.  TMEM is taken by the
+// first pass that has tiles to score and kept until the kernel ends
+// (tslot[0] = address, tslot[1] = taken).
 template <int DT, int H, int RB, bool SPLIT>
-__global__ void __launch_bounds__(ScoreCfg<DT, H, RB>::THREADS, 1)
-score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-             const __grid_constant__ CUtensorMap tm_ks, const __grid_constant__ ScoreArgs a) {
+IDX_DEVI void score_pass(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+                         const CUtensorMap& tm_ks, const ScoreArgs& a, uint8_t* smem,
+                         const int blk, const int mode, const int level) {
     using C = ScoreCfg<DT, H, RB>;
-    extern __shared__ __align__(1024) uint8_t smem_raw[];
-    // 1024-byte aligned base (TMA swizzle atoms), derived from smem_raw by an
-    // offset so that the compiler keeps every access in the shared space
-    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
     uint64_t* full = bars;
     uint64_t* empty = bars + C::NS;
@@ -154,14 +155,9 @@ score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 2);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int r0 = blockIdx.x * C::R;
-    const int mode = a.mode;
-    // exact rescan launches with no row waiting for them end here
-    if (mode == SM_FB_HIST && *(volatile int*)(a.fb_cnt + a.level) == 0) return;
-    if (mode == SM_FB_EMIT && *(volatile int*)(a.fb_cnt + 6) == 0) return;
-    if (mode == SM_SAMPLE && blockIdx.x == 0 && tid < 8) a.fb_cnt[tid] = 0;  // new call
+    const int r0 = blk * C::R;
     const int phase =
-        mode == SM_SAMPLE ? (int)(hash32((uint32_t)blockIdx.x ^ a.phase_seed) % (uint32_t)a.S) : 0;
+        mode == SM_SAMPLE ? (int)(hash32((uint32_t)blk ^ a.phase_seed) % (uint32_t)a.S) : 0;
 
     // ---- per-row metadata
     if (tid < C::R) {
@@ -216,7 +212,7 @@ score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                     break;
                 case SM_FB_HIST: {
                     const RowPlan p = a.plan[r];
-                    active = n > 0 && p.state == ST_HIST && p.level == a.level;
+                    active = n > 0 && p.state == ST_HIST && p.level == level;
                     thr = p.thr;
                     prefix = p.prefix;
                 } break;
@@ -281,7 +277,6 @@ score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             misc[0] = t0;
             misc[1] = nt;
         }
-        *abort_flag = 0;
         for (int i = 0; i < C::NS; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], 1);
@@ -306,18 +301,23 @@ score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                               i % kRuns] = 0;
             }
         }
+        __syncthreads();  // every thread is done with this pass's shared state
         return;
     }
 
-    if (warp == 1) {
-        __syncwarp();
-        tmem_alloc(tslot, 512);
-        tmem_relinquish();
+    if (tslot[1] == 0) {
+        // the CTA's first pass with tiles: take the 512 TMEM columns
+        if (warp == 1) {
+            __syncwarp();
+            tmem_alloc(tslot, 512);
+            tmem_relinquish();
+        }
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        if (tid == 0) tslot[1] = 1;
     }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tslot;
+    const uint32_t tmem = tslot[0];
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
@@ -399,10 +399,14 @@ score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 *abort_flag = 1;
                 raise_status(a.d_status, IDX_DEV_TIMEOUT);
             }
-            // wait (bounded) until the tensor core is done with TMEM
+            // wait (bounded) until the tensor core is done with TMEM, and for the
+            // arrivals of the last stages' release commits: the next pass
+            // initialises these barriers again
             if (issued > 0)
                 mbar_wait(&accf[(issued - 1) & 1], (uint32_t)(((issued - 1) >> 1) & 1), nullptr,
                           1ll << 28);
+            for (int i = issued > C::NS ? issued - C::NS : 0; i < issued; ++i)
+                mbar_wait(&empty[i % C::NS], (uint32_t)((i / C::NS) & 1), nullptr, 1ll << 28);
         }
     } else if (warp >= 4) {
         // ------------------------------------------------ epilogue
@@ -513,7 +517,7 @@ score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                     const bool vis = (uint32_t)off < (uint32_t)(RHI(j) - RLO(j));
                     const uint32_t kb = fkey(sc[j]);
                     const uint32_t ix = (uint32_t)(kidx - RKS(j));
-                    const int lev = a.level;
+                    const int lev = level;
                     bool valid;
                     uint32_t dg;
                     if (lev <= 2) {
@@ -581,7 +585,7 @@ score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             for (int rr = e; rr < C::R; rr += C::EPI_WARPS) {
                 if (!meta[rr * C::META_WORDS + MW_ACTIVE]) continue;
                 rescan_pick_warp(a.plan + r0 + rr, a.fb_hist + (long long)(r0 + rr) * kHistBins,
-                                 a.level, a.topk, a.cap, a.fb_cnt);
+                                 level, a.topk, a.cap, a.fb_cnt);
             }
         }
         if (lane == 0 && (mode == SM_EMIT || mode == SM_FB_EMIT)) {
@@ -596,10 +600,55 @@ score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    tc_fence_after();
+}
+
+// The kernel: one CTA per row block (grid.x) and key split (grid.y), one pass
+// in the launch's mode; or, for the exact rescan (SM_RESCAN), a grid that
+// strides over the device list of flagged row blocks and runs, per block, the
+// histogram passes of the digits its rows still need and then the
+// re-emission.  A rescan launch with no block listed ends at once.
+template <int DT, int H, int RB, bool SPLIT>
+__global__ void __launch_bounds__(ScoreCfg<DT, H, RB>::THREADS, 1)
+score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+             const __grid_constant__ CUtensorMap tm_ks, const __grid_constant__ ScoreArgs a) {
+    using C = ScoreCfg<DT, H, RB>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // 1024-byte aligned base (TMA swizzle atoms), derived from smem_raw by an
+    // offset so that the compiler keeps every access in the shared space
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + C::OFF_TSLOT);
+    int* misc = reinterpret_cast<int*>(smem + C::OFF_MISC);
+    const int tid = threadIdx.x, warp = tid >> 5;
+    if (a.mode == SM_RESCAN && *(volatile int*)(a.fb_cnt + 7) == 0) return;  // none flagged
+    if (a.mode == SM_SAMPLE && blockIdx.y == 0) {
+        // a new call: the rescan counters and this block's rescan flag start at 0
+        if (blockIdx.x == 0 && tid < 8) a.fb_cnt[tid] = 0;
+        if (tid == 0 && a.fb_bflag) a.fb_bflag[blockIdx.x] = 0;
+    }
+    if (tid == 0) {
+        tslot[1] = 0;
+        misc[2] = 0;  // abort flag: a wait that timed out releases every later wait
+    }
+    // (the first synchronisation inside the pass orders these writes)
+    // one call site of the pass (it is inlined once): a plain launch makes one
+    // pass over its own row block; the rescan makes 7 passes per listed block
+    const bool rescan = a.mode == SM_RESCAN;
+    const int nb = rescan ? *(volatile int*)(a.fb_cnt + 7) : 1;
+    const int npass = rescan ? 7 : 1;
+    for (int wi = rescan ? (int)blockIdx.x : 0; wi < nb; wi += rescan ? (int)gridDim.x : 1) {
+        const int blk = rescan ? a.fb_blocks[wi] : (int)blockIdx.x;
+        for (int pass = 0; pass < npass; ++pass) {
+            const int mode = rescan ? (pass < 6 ? SM_FB_HIST : SM_FB_EMIT) : a.mode;
+            score_pass<DT, H, RB, SPLIT>(tm_q, tm_k, tm_ks, a, smem, blk, mode,
+                                         rescan ? pass : a.level);
+        }
+    }
+    __syncthreads();
+    if (tslot[1] && warp == 1) {
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem, 512);
+        tmem_dealloc(tslot[0], 512);
     }
 }
 

@@ -80,7 +80,9 @@ cudaError_t launch_score_t(const ScoreLaunch& L, cudaStream_t s) {
                                             C::SMEM_ALLOC);
     });
     if (attr_err != cudaSuccess) return attr_err;
-    const dim3 grid((unsigned)((a.rows + C::R - 1) / C::R), (unsigned)(a.ksplit > 1 ? a.ksplit : 1));
+    const int nblk = (a.rows + C::R - 1) / C::R;
+    const int gx = a.mode == SM_RESCAN && a.grid_x > 0 && a.grid_x < nblk ? a.grid_x : nblk;
+    const dim3 grid((unsigned)gx, (unsigned)(a.ksplit > 1 && a.mode != SM_RESCAN ? a.ksplit : 1));
     kern<<<grid, C::THREADS, C::SMEM_ALLOC, s>>>(tq, tk, tks, a);
     return cudaGetLastError();
 }

@@ -1023,6 +1023,10 @@ cand_topk_kernel(CandArgs a) {
                     plan->prefix = 0u;
                     plan->above = 0;
                     atomicAdd(&a.fb_cnt[0], 1);
+                    // list the row's block once for the rescan launch
+                    const int blk = r / a.rows_per_block;
+                    if (atomicExch(&a.fb_bflag[blk], 1) == 0)
+                        a.fb_blocks[atomicAdd(&a.fb_cnt[7], 1)] = blk;
                     if (a.d_stats) {
                         atomicAdd(trunc ? &a.d_stats->overflow_rows : &a.d_stats->short_rows, 1);
                         atomicAdd(&a.d_stats->fallback_rows, 1);

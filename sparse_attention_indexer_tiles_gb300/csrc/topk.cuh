@@ -52,7 +52,10 @@ struct CandArgs {
     int cap_q;
     RowPlan* plan;
     uint32_t* fb_hist;    // [rows, 4096]
-    int* fb_cnt;          // [8] rescan counters (see RowPlan)
+    int* fb_cnt;          // [8] rescan counters (see ScoreArgs)
+    int* fb_blocks;       // [row blocks] list of row blocks with a flagged row
+    int* fb_bflag;        // [row blocks] listed-once flags
+    int rows_per_block;   // rows of one scoring row block
     const int* ks;
     const int* ke;
     int rows, topk, cap;

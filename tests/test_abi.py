@@ -116,8 +116,9 @@ def _documented_workspace(rows, max_len, topk, nruns):
     regions for the row plans (32 B each), the run counts [rows, nruns] int32,
     the slab [rows, nruns, cap_q] of (fp32 score, int32 index) pairs with
     cap_q = ceil(cap / 8) + 64, the sample scratch [rows, max_len // S + 2]
-    fp32 and the rescan histograms [rows, 4096] (both only when rows can see
-    more than cap keys), and eight rescan counters."""
+    fp32, the rescan histograms [rows, 4096] and the rescan's list and flags
+    of row blocks [blocks] int32 (these only when rows can see more than cap
+    keys), and eight rescan counters."""
     def up(x):
         return (x + 255) // 256 * 256
     cap = max(math.ceil(2.25 * topk), 4096)
@@ -126,9 +127,11 @@ def _documented_workspace(rows, max_len, topk, nruns):
     t = max(32.0, (4.5 / math.log(max(target, 1.0001))) ** 2)
     S = max(s for s in (1, 3, 5, 7, 11, 15, 23, 31, 45, 63) if s <= target * topk / t)
     sampled = max_len > cap
+    nblk = -(-rows // 4)  # row blocks of 256 / H rows at H = 64
     regions = [rows * 32, rows * nruns * 4, rows * nruns * cap_q * 8,
                rows * (max_len // S + 2) * 4 if sampled else 0,
-               rows * 4096 * 4 if sampled else 0, 8 * 4]
+               rows * 4096 * 4 if sampled else 0,
+               nblk * 4 if sampled else 0, nblk * 4 if sampled else 0, 8 * 4]
     return sum(up(r) for r in regions), S
 
 
