@@ -152,7 +152,7 @@ FusedParams fused_params(int topk, const idx_options* opt) {
     else
         p.cap = std::max((int)std::ceil(2.25 * topk), 4096);
     if (p.cap < topk) p.cap = topk;
-    p.cap_q = (p.cap + kRuns - 1) / kRuns + 64;
+    p.cap_q = ((p.cap + kRuns - 1) / kRuns + 64 + 1) / 2 * 2;  // even: 16-byte run copies
     const double ratio = (double)p.cap / topk;
     double target = opt && opt->target_factor > 0.f ? (double)opt->target_factor : std::sqrt(ratio);
     p.target = (float)target;
@@ -239,11 +239,14 @@ ScoreLaunch make_score_launch(const void* q, const void* k, const float* k_scale
 }
 
 // Key splits of a scoring launch: the CTAs of one wave are SM-count many, so
-// a grid of nblk row blocks leaves the last wave partly idle.  When the
-// unsplit grid fills its last wave to less than 90 %, every block's key tiles
-// are split into k contiguous parts (grid.y = k), k <= 6 the one that fills
-// the last wave best (the smaller k within 1 %), every part keeping >= 64
-// tiles.  Each split of the emit pass adds kRuns runs per row to the slab.
+// a grid of nblk row blocks leaves the last wave partly idle, and a call with
+// few rows (a decode-like shape: few query rows over long rows) leaves most of
+// the GPU idle.  When the unsplit grid fills its last wave to less than 90 %,
+// every block's key tiles are split into k contiguous parts (grid.y = k), the
+// k that fills the last wave best (the smaller k within 1 %), every part
+// keeping >= 32 tiles: k <= 6 for grids of at least half a wave, up to one
+// wave's worth (SMs / nblk, at most 128) for fewer blocks.  Each split of the
+// emit pass adds kRuns runs per row to the slab.
 int score_ksplit(int rows, int H, long long max_len) {
     const int nblk = (rows + score_rows_per_block(H) - 1) / score_rows_per_block(H);
     const long long tiles = (max_len + 127) / 128;
@@ -253,8 +256,9 @@ int score_ksplit(int rows, int H, long long max_len) {
         return waves / std::ceil(waves);
     };
     if (eff(1) >= 0.9) return 1;
+    const int kmax = 2 * nblk <= sm ? std::min(128, (int)(sm / nblk)) : 6;
     int best = 1;
-    for (int k = 2; k <= 6 && tiles / k >= 64; ++k)
+    for (int k = 2; k <= kmax && tiles / k >= 32; ++k)
         if (eff(k) > eff(best) + 0.01) best = k;
     return best;
 }
@@ -367,9 +371,12 @@ idx_status idx_score_topk(const void* q, const void* k, const float* k_scale, co
 
     record(opt, 0, s);
     if (sampling) {
-        // 1. score the odd-stride sample of every long row
+        // 1. score the odd-stride sample of every long row (key splits over the
+        //    sample index range, as for the emit pass)
         L.a.mode = SM_SAMPLE;
+        L.a.ksplit = score_ksplit(rows, H, max_len / p.S + 1);
         if ((e = launch_score(L, s)) != cudaSuccess) return cuda_status(e);
+        L.a.ksplit = 1;
         // 2. T_r = exact t-th largest sample score of each row
         TopkRowsArgs t;
         std::memset(&t, 0, sizeof(t));

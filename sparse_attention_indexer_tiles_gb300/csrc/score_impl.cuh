@@ -128,6 +128,33 @@ IDX_DEVI float head_reduce_quad(uint32_t taddr, const float2* wq) {
     return (b1 ? k1 : k0) + rx;
 }
 
+// Head reduce of one row for H <= 32, one key per thread: the 32x32b shape
+// gives thread t the accumulators of key t of the lane quarter at all H heads
+// of the row, so no cross-thread sum is needed.  The row's weights are the
+// same for every lane and come from shared memory (broadcast loads issued
+// while the TMEM load is in flight).  Two packed accumulators take heads
+// (4i, 4i + 1) and (4i + 2, 4i + 3); the order is fixed, so every scoring mode
+// gets the same bits.
+template <int H>
+IDX_DEVI float head_reduce_lane(uint32_t taddr, const float* w_row) {
+    float v[H];
+    tmem_ld32x32b<H>(taddr, v);
+    float4 w4[H / 4];
+#pragma unroll
+    for (int i = 0; i < H / 4; ++i) w4[i] = reinterpret_cast<const float4*>(w_row)[i];
+    tmem_ld_wait();
+    float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < H / 4; ++i) {
+        const float* y = v + 4 * i;
+        a0 = __ffma2_rn(make_float2(w4[i].x, w4[i].y),
+                        make_float2(y[0] + fabsf(y[0]), y[1] + fabsf(y[1])), a0);
+        a1 = __ffma2_rn(make_float2(w4[i].z, w4[i].w),
+                        make_float2(y[2] + fabsf(y[2]), y[3] + fabsf(y[3])), a1);
+    }
+    return (a0.x + a0.y) + (a1.x + a1.y);
+}
+
 // SPLIT: the launch splits row blocks over key ranges (grid.y) or addresses a
 // slab with more than kRuns runs per row; without it the kernel is compiled
 // with kRuns runs per row and no split arithmetic.
@@ -416,9 +443,17 @@ IDX_DEVI void score_pass(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
         const int grp = (e >> 2) & 1;        // half of the rows
         const int run = q * 2 + team;        // candidate run of this warp (in its key split)
         // lanes whose key comes earlier (candidates are appended in key order)
+        // H <= 32: one key per lane (32x32b loads); H = 64: four lanes per key
+        // (16x256b loads and a butterfly)
+        constexpr bool LANE_KEYS = H <= 32;
         uint32_t lt = 0u;
+        if constexpr (LANE_KEYS) {
+            lt = (1u << lane) - 1u;
+        } else {
 #pragma unroll
-        for (int l = 0; l < 32; ++l) lt |= (quad_key_off(l) < quad_key_off(lane) ? 1u : 0u) << l;
+            for (int l = 0; l < 32; ++l)
+                lt |= (quad_key_off(l) < quad_key_off(lane) ? 1u : 0u) << l;
+        }
         int cnt[C::RG];
         // row metadata from shared memory; the emit words of up to 2 rows per
         // warp are held in registers across the tile loop
@@ -452,7 +487,7 @@ IDX_DEVI void score_pass(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
 #define RCUT(j) row_word(j, MW_CUT)
 #define RPRE(j) ((uint32_t)row_word(j, MW_PREFIX))
         // this thread's weights: row j, head pair (8 rep + 2c, 8 rep + 2c + 1)
-        const int kq = quad_key_off(lane);  // this thread's key in the quarter
+        const int kq = LANE_KEYS ? lane : quad_key_off(lane);  // this thread's key in the quarter
         // Per-key scale of the team's next tile, loaded one tile ahead.  The
         // thread's tile index i (a key, or a sample index in SM_SAMPLE) grows
         // by 2 M per team tile; key = i, or phase + S i for the sample.
@@ -463,12 +498,18 @@ IDX_DEVI void score_pass(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
         int s_i = (t0 + team) * C::M + q * 32 + kq;
         uint32_t s_off = (mode == SM_SAMPLE ? (uint32_t)phase : 0u) + kmul * (uint32_t)s_i;
         const uint32_t s_step = kmul * 2u * C::M;
-        float2 wq[C::RG][H / 8];
+        // H = 64: this thread's weights of row j, head pair (8 rep + 2c, 8 rep + 2c + 1),
+        // held in registers for the whole pass
+        constexpr int WR = LANE_KEYS ? 1 : C::RG, WC = LANE_KEYS ? 1 : H / 8;
+        float2 wq[WR][WC];
+        if constexpr (!LANE_KEYS) {
 #pragma unroll
-        for (int j = 0; j < C::RG; ++j) {
-            const float* wr = w_s + (grp * C::RG + j) * H + 2 * (lane & 3);
+            for (int j = 0; j < C::RG; ++j) {
+                const float* wr = w_s + (grp * C::RG + j) * H + 2 * (lane & 3);
 #pragma unroll
-            for (int rp = 0; rp < H / 8; ++rp) wq[j][rp] = make_float2(wr[8 * rp], wr[8 * rp + 1]);
+                for (int rp = 0; rp < H / 8; ++rp)
+                    wq[j][rp] = make_float2(wr[8 * rp], wr[8 * rp + 1]);
+            }
         }
         const int all_lo = misc[3], all_hi = misc[4];
         float next_scale = team < ntiles && s_i < ilim ? __ldg(a.k_scale + s_off) : 0.f;
@@ -491,7 +532,12 @@ IDX_DEVI void score_pass(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
 #pragma unroll
             for (int j = 0; j < C::RG; ++j) {
                 const int rr = grp * C::RG + j;
-                sc[j] = head_reduce_quad<H>(tbase + (uint32_t)(rr * H), wq[j]) * post_scale;
+                if constexpr (LANE_KEYS)
+                    sc[j] = head_reduce_lane<H>(tbase + (uint32_t)(rr * H), w_s + rr * H) *
+                            post_scale;
+                else
+                    sc[j] = head_reduce_quad<H>(tbase + (uint32_t)(rr * H), wq[LANE_KEYS ? 0 : j]) *
+                            post_scale;
             }
             tc_fence_before();
             __syncwarp();

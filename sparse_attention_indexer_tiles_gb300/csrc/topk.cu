@@ -25,7 +25,6 @@ namespace idx {
 void count_launches(unsigned n);  // api.cu
 
 constexpr int kTieCap = 4096;
-constexpr int kCandScratch = 96;  // scan words + row state of cand_topk_kernel
 
 // A row of fp32 values addressed through an aligned float4 view: element p
 // (0 <= p < n) sits in slot p + off of the 16-byte aligned base.  Reads may
@@ -895,129 +894,245 @@ topk_split_merge_kernel(TopkRowsArgs a, int g) {
 // ---------------------------------------------------------------- slab
 //
 // Page 1, "Sampled Threshold": the small exact top-k over the ~2.25 x topk
-// candidates of a row.  The scoring pass leaves each row's candidates in
-// eight runs, each in ascending key order; the rescan re-emission leaves a
-// single ordered run.  One CTA of 256 threads per row loads the runs into
-// shared memory as (order key, index), finds the exact threshold key T with
-// four 8-bit radix passes (per-warp histograms), keeps the lowest indices
-// among the keys equal to T, and writes the selected indices in ascending order through a bitmap of
-// the index range (65536 indices per pass): each thread owns eight bitmap
-// words, and a block scan of their popcounts gives every set bit its output
-// position.
+// candidates of a row.  The scoring pass leaves each row's candidates in runs
+// of (score, row-relative index) pairs, each run in ascending index order
+// (eight runs per key split; the rescan's re-emission uses the first eight).
+// One CTA of 256 threads per row:
+//   1. copies the runs into shared memory with one bulk copy per run (run
+//      lengths rounded up to an even count, the extra slot marked empty) and
+//      turns the scores into order keys;
+//   2. finds the exact threshold key T by radix selection that starts below
+//      the bits all candidates share (their maximum and minimum agree there):
+//      one 8-bit digit pass over every candidate, then the candidates of the
+//      threshold digit are gathered and refined alone (or, when that digit
+//      holds too many, over all candidates);
+//   3. keeps the lowest indices among the keys equal to T;
+//   4. writes the selected indices in ascending order: the selected entries of
+//      each run are compacted in run order, so every run's selection is
+//      sorted, and an entry's output position is its rank in its own run plus
+//      its lower bound in each other run of the same key split (the splits
+//      cover ascending key ranges and follow each other).
+// Rows whose candidate count fell below topk, or whose runs overflowed, are
+// flagged for the exact rescan instead.
 
 constexpr int kCandThreads = 256;
 constexpr int kCandWarps = kCandThreads / 32;
-constexpr int kBitmapWords = kCandWarps * 256;  // the histograms' words, 65536 bits
+constexpr uint32_t kEmptyKey = 0u;  // below the key of every finite score
 
-// Exact need-th largest value among the elements e < cnt with valid(e), of
-// the 32-bit values val(e), by four 8-bit digits from the top.  Returns the
-// value and, through *need_at, how many elements equal to it are taken.
+// Block-wide maximum and minimum of one value per thread (scratch >= 16 words).
+IDX_DEVI void block_max_min(uint32_t& mx, uint32_t& mn, uint32_t* scratch) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    }
+    if (lane == 0) {
+        scratch[w] = mx;
+        scratch[8 + w] = mn;
+    }
+    __syncthreads();
+    mx = scratch[0];
+    mn = scratch[8];
+#pragma unroll
+    for (int j = 1; j < kCandWarps; ++j) {
+        mx = max(mx, scratch[j]);
+        mn = min(mn, scratch[8 + j]);
+    }
+    __syncthreads();
+}
+
+// One digit of a radix selection from the top: among the elements e < cnt
+// with valid(e) whose value v = val(e) has bits above `shift + width` equal to
+// `pre`, histogram the digit (v >> shift) & (2^width - 1) in per-warp bins and
+// pick the digit that holds the need-th largest.  Returns the digit; *above =
+// elements of larger digits, *count = elements of that digit.
 template <class Valid, class Val>
-IDX_DEVI uint32_t cand_select(uint32_t cnt, uint32_t need, Valid valid, Val val, uint32_t* hist,
-                              uint32_t* scratch, uint32_t* need_at) {
+IDX_DEVI uint32_t cand_digit(uint32_t cnt, uint32_t need, int shift, int width, uint64_t pre,
+                             Valid valid, Val val, uint32_t* hist, uint32_t* scratch,
+                             uint32_t* above, uint32_t* count) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     uint32_t* hw = hist + w * 256;
-    uint32_t prefix = 0u;
-    for (int lev = 0; lev < 4; ++lev) {
-        const int shift = 24 - 8 * lev;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) hw[lane * 8 + j] = 0u;
-        __syncwarp();
-        for (uint32_t base = 0; base < cnt; base += 4 * kCandThreads) {
-            uint32_t v[4];
-            bool in[4];
+    for (int j = 0; j < 8; ++j) hw[lane * 8 + j] = 0u;
+    __syncthreads();
+    const uint32_t mask = (1u << width) - 1u;
+    for (uint32_t base = 0; base < cnt; base += 4 * kCandThreads) {
+        uint32_t v[4];
+        bool in[4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const uint32_t e = base + u * kCandThreads + threadIdx.x;
-                in[u] = e < cnt && valid(e);
-                v[u] = in[u] ? val(e) : 0u;
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-                if (in[u] && (lev == 0 || (v[u] >> (shift + 8)) == prefix))
-                    atomicAdd(&hw[(v[u] >> shift) & 255u], 1u);
+        for (int u = 0; u < 4; ++u) {
+            const uint32_t e = base + u * kCandThreads + threadIdx.x;
+            in[u] = e < cnt && valid(e);
+            v[u] = in[u] ? val(e) : 0u;
         }
-        __syncthreads();
-        // thread t owns digit 255 - t: a scan from the top digit down
-        uint32_t c = 0;
 #pragma unroll
-        for (int ww = 0; ww < kCandWarps; ++ww) c += hist[ww * 256 + 255 - threadIdx.x];
-        const uint32_t incl = block_incl_scan<kCandThreads>(c, scratch, nullptr);
-        const uint32_t excl = incl - c;
-        if (excl < need && need <= incl) {
-            scratch[40] = 255u - threadIdx.x;
-            scratch[41] = excl;
-        }
-        __syncthreads();
-        need -= scratch[41];
-        prefix = (prefix << 8) | scratch[40];
-        __syncthreads();
+        for (int u = 0; u < 4; ++u)
+            if (in[u] && ((uint64_t)v[u] >> (shift + width)) == pre)
+                atomicAdd(&hw[(v[u] >> shift) & mask], 1u);
+    }
+    __syncthreads();
+    // thread t owns digit 255 - t: a scan from the top digit down
+    uint32_t c = 0;
+#pragma unroll
+    for (int ww = 0; ww < kCandWarps; ++ww) c += hist[ww * 256 + 255 - threadIdx.x];
+    const uint32_t incl = block_incl_scan<kCandThreads>(c, scratch, nullptr);
+    const uint32_t excl = incl - c;
+    if (excl < need && need <= incl) {
+        scratch[40] = 255u - threadIdx.x;
+        scratch[41] = excl;
+        scratch[42] = c;
+    }
+    __syncthreads();
+    const uint32_t d = scratch[40];
+    *above = scratch[41];
+    *count = scratch[42];
+    __syncthreads();
+    return d;
+}
+
+// Exact need-th largest value, walking digits of <= 8 bits from bit `top`
+// down to bit 0 among the elements whose bits above `top` equal `pre`.
+// Returns the value; *need_at = how many elements equal to it are taken.
+template <class Valid, class Val>
+IDX_DEVI uint32_t cand_select(uint32_t cnt, uint32_t need, int top, uint64_t pre, Valid valid,
+                              Val val, uint32_t* hist, uint32_t* scratch, uint32_t* need_at) {
+    int bit = top + 1;
+    while (bit > 0) {
+        const int width = bit >= 8 ? 8 : bit;
+        const int shift = bit - width;
+        uint32_t above, count;
+        const uint32_t d =
+            cand_digit(cnt, need, shift, width, pre, valid, val, hist, scratch, &above, &count);
+        need -= above;
+        pre = (pre << width) | d;
+        bit = shift;
     }
     *need_at = need;
-    return prefix;
+    return (uint32_t)pre;
 }
+
+// Shared memory of cand_topk_kernel, in 32-bit words.  The per-warp
+// histograms and the compacted selection share one region (the selection is
+// written once the histograms are no longer read).
+constexpr int kCandBins = 1024;   // first-digit bins, and output buckets
+constexpr int kCandGather = 256;  // candidates of the threshold digit ranked alone
+struct CandSmem {
+    int nruns, topk, cap;  // cap: pairs the row buffer holds
+    __host__ __device__ CandSmem(int nruns_, int topk_, int cap_q) : nruns(nruns_), topk(topk_) {
+        cap = kRuns * cap_q + nruns;
+    }
+    __host__ __device__ int hist() const { return 0; }  // [1024]: digit bins, then buckets
+    __host__ __device__ int sel() const { return kCandBins; }               // [topk]
+    // 16-byte boundaries for the mbarrier (8-byte aligned) and the bulk-copy
+    // destination (16-byte aligned); the dynamic shared memory base is 16-byte aligned
+    // (cand_select's per-warp histograms take 8 x 256 words from 0: before the
+    // selection is written they may cover sel, never scratch and what follows)
+    __host__ __device__ int scratch() const {
+        const int e = (sel() + topk + 3) / 4 * 4;
+        return e > kCandWarps * 256 ? e : kCandWarps * 256;
+    }  // 64
+    __host__ __device__ int bar() const { return scratch() + 64; }          // 2 (8-byte aligned)
+    __host__ __device__ int run_off() const { return bar() + 2; }           // [nruns + 1]
+    // the gathered candidates of the threshold digit live in sel (written
+    // later) when it is large enough, else after the run offsets
+    __host__ __device__ bool gather_in_sel() const { return topk >= 2 * kCandGather; }
+    __host__ __device__ int gather() const {
+        return gather_in_sel() ? sel() : (run_off() + nruns + 1 + 1) / 2 * 2;
+    }
+    __host__ __device__ int pairs() const {
+        const int end = gather_in_sel() ? run_off() + nruns + 1 : gather() + 2 * kCandGather;
+        return (end + 3) / 4 * 4;
+    }
+    __host__ __device__ int words() const { return pairs() + 2 * cap; }
+};
 
 __global__ void __launch_bounds__(kCandThreads)
 cand_topk_kernel(CandArgs a) {
     constexpr int THREADS = kCandThreads;
     extern __shared__ __align__(16) uint32_t smem[];
-    const int CR = a.nruns * a.cap_q;          // slab row (all key splits)
-    const int CS = kRuns * a.cap_q;            // candidates held in shared memory
-    uint32_t* hist = smem;                     // [kCandWarps][256], later the bitmap
-    uint32_t* scratch = hist + kBitmapWords;   // [0,35) scans; row state from 48 on
-    uint32_t* keys = scratch + kCandScratch;
-    uint32_t* idxs = keys + CS;
-    uint32_t* run_off = idxs + CS;             // [nruns + 1] run starts in keys[]
+    const CandSmem L(a.nruns, a.topk, a.cap_q);
+    uint32_t* hist = smem + L.hist();
+    uint32_t* scratch = smem + L.scratch();  // [0,35) scans, [40,48) results, [48,64) row state
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L.bar());
+    uint32_t* run_off = smem + L.run_off();
+    uint32_t* sel = smem + L.sel();
+    int2* cmp = reinterpret_cast<int2*>(smem + L.gather());  // (key, index) of one digit
+    int2* pairs = reinterpret_cast<int2*>(smem + L.pairs());
+    const int tid = threadIdx.x;
+    const int CR = a.nruns * a.cap_q;  // slab row (all key splits)
+    const uint32_t k = (uint32_t)a.topk;
 
     if (a.fallback && *(volatile int*)(a.fb_cnt + 6) == 0) return;  // no row was re-emitted
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        fence_barrier_init();
+    }
+    uint32_t phase = 0;
+    // runs of this thread: a contiguous range, so that offsets follow run order
+    const int per = (a.nruns + THREADS - 1) / THREADS;
+    const int q0 = tid * per < a.nruns ? tid * per : a.nruns;
+    const int q1 = q0 + per < a.nruns ? q0 + per : a.nruns;
+
     for (int r = blockIdx.x; r < a.rows; r += gridDim.x) {
         __syncthreads();  // the previous row's shared state is no longer read
         RowPlan* plan = a.plan + r;
         const long long n = (long long)a.ke[r] - (long long)a.ks[r];
         int* out = a.out + (long long)r * a.topk;
-        if (threadIdx.x == 0) {
+        if (tid == 0) {
             scratch[48] = (uint32_t)plan->state;
-            uint32_t off = 0, total = 0, trunc = 0;
-            for (int q = 0; q < a.nruns; ++q) {
-                const uint32_t c = (uint32_t)a.run_cnt[(long long)r * a.nruns + q];
-                trunc |= c > (uint32_t)a.cap_q;
-                total += c;
-                run_off[q] = off;
-                off += c < (uint32_t)a.cap_q ? c : (uint32_t)a.cap_q;
-            }
-            // more candidates than shared memory holds (possible with key
-            // splits): the exact rescan takes the row
-            trunc |= off > (uint32_t)CS;
-            run_off[a.nruns] = off;
-            scratch[49] = trunc;
-            scratch[60] = total;
+            scratch[49] = 0u;  // candidates (uncapped)
         }
         __syncthreads();
         const int state = (int)scratch[48];
         if (a.fallback) {
             if (state != ST_EMIT) continue;
         } else if (n <= a.topk) {
-            for (int i = threadIdx.x; i < a.topk; i += THREADS) out[i] = i < n ? i : -1;
-            if (threadIdx.x == 0) plan->state = ST_DONE;
+            for (int i = tid; i < a.topk; i += THREADS) out[i] = i < n ? i : -1;
+            if (tid == 0) plan->state = ST_DONE;
             continue;
         }
-        const uint32_t total = scratch[60];
-        const bool trunc = scratch[49] != 0;
-        if (threadIdx.x == 0 && a.d_stats && !a.fallback) atomicMax(&a.d_stats->max_count, (int)total);
-        if (trunc || total < (uint32_t)a.topk) {
+
+        // ---- run offsets (even lengths, 16-byte aligned copies)
+        const int* rc = a.run_cnt + (long long)r * a.nruns;
+        uint32_t lpad = 0, lcnt = 0;
+        bool ltr = false;
+        for (int q = q0; q < q1; ++q) {
+            const uint32_t c = (uint32_t)rc[q];
+            const uint32_t cl = c < (uint32_t)a.cap_q ? c : (uint32_t)a.cap_q;
+            ltr |= c > (uint32_t)a.cap_q;
+            lcnt += c;
+            lpad += (cl + 1u) & ~1u;
+        }
+        uint32_t ptot;
+        uint32_t off = block_incl_scan<THREADS>(lpad, scratch, &ptot) - lpad;
+        for (int q = q0; q < q1; ++q) {
+            const uint32_t c = (uint32_t)rc[q];
+            const uint32_t cl = c < (uint32_t)a.cap_q ? c : (uint32_t)a.cap_q;
+            run_off[q] = off;
+            off += (cl + 1u) & ~1u;
+        }
+        if (tid == 0) run_off[a.nruns] = ptot;
+        atomicAdd(&scratch[49], lcnt);
+        // more candidates than the buffer holds (possible with key splits):
+        // the exact rescan takes the row
+        const bool trunc = __syncthreads_or(ltr || ptot > (uint32_t)L.cap);
+        const uint32_t total = scratch[49];
+        if (tid == 0 && a.d_stats && !a.fallback) atomicMax(&a.d_stats->max_count, (int)total);
+        if (trunc || total < k) {
             if (!a.fallback && !a.fb_hist) {
                 // no rescan storage: the row was longer than the max_len the
                 // workspace was sized for
-                for (int i = threadIdx.x; i < a.topk; i += THREADS) out[i] = -1;
-                if (threadIdx.x == 0) {
+                for (int i = tid; i < a.topk; i += THREADS) out[i] = -1;
+                if (tid == 0) {
                     raise_status(a.d_status, IDX_DEV_RANGE);
                     plan->state = ST_DONE;
                 }
             } else if (!a.fallback) {
                 // the sampled threshold missed: exact full-row rescan
-                for (int i = threadIdx.x; i < kHistBins; i += THREADS)
+                for (int i = tid; i < kHistBins; i += THREADS)
                     a.fb_hist[(long long)r * kHistBins + i] = 0u;
-                if (threadIdx.x == 0) {
+                if (tid == 0) {
                     plan->state = ST_HIST;
                     plan->level = 0;
                     plan->prefix = 0u;
@@ -1032,116 +1147,201 @@ cand_topk_kernel(CandArgs a) {
                         atomicAdd(&a.d_stats->fallback_rows, 1);
                     }
                 }
-            } else if (threadIdx.x == 0) {
+            } else if (tid == 0) {
                 raise_status(a.d_status, IDX_DEV_STATE);
                 plan->state = ST_DONE;
             }
             continue;
         }
 
-        // load the runs back to back, four independent loads per thread in flight
-        const int2* sl = a.slab + (long long)r * CR;
-        const uint32_t cnt = run_off[a.nruns];
-        for (uint32_t base = 0; base < cnt; base += 4 * THREADS) {
-            float sv[4];
-            int iv[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const uint32_t e = base + u * THREADS + threadIdx.x;
-                if (e < cnt) {
-                    // the run holding entry e: the last q with run_off[q] <= e
-                    int q = 0;
-                    if (a.nruns == kRuns) {
-#pragma unroll
-                        for (int j = 1; j < kRuns; ++j) q += e >= run_off[j];
-                    } else {
-                        int hi = a.nruns;
-                        while (hi - q > 1) {
-                            const int mid = (q + hi) >> 1;
-                            if (run_off[mid] <= e) q = mid;
-                            else hi = mid;
-                        }
-                    }
-                    const uint32_t src = (uint32_t)q * (uint32_t)a.cap_q + (e - run_off[q]);
-                    const int2 c = sl[src];
-                    sv[u] = __int_as_float(c.x);
-                    iv[u] = c.y;
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const uint32_t e = base + u * THREADS + threadIdx.x;
-                if (e < cnt) {
-                    keys[e] = fkey(sv[u]);
-                    idxs[e] = (uint32_t)iv[u];
-                }
+        // ---- the runs into shared memory, one bulk copy each
+        if (tid == 0) mbar_arrive_expect_tx(bar, ptot * (uint32_t)sizeof(int2));
+        __syncthreads();
+        const int2* srow = a.slab + (long long)r * CR;
+        for (int q = q0; q < q1; ++q) {
+            const uint32_t len = run_off[q + 1] - run_off[q];
+            if (len) bulk_g2s(pairs + run_off[q], srow + (long long)q * a.cap_q, len * 8u, bar);
+        }
+        if (!mbar_wait(bar, phase, nullptr, 1ll << 30)) {
+            // copies that never completed: report and leave (bounded wait for them)
+            if (tid == 0) raise_status(a.d_status, IDX_DEV_TIMEOUT);
+            mbar_wait(bar, phase, nullptr, 1ll << 30);
+            return;
+        }
+        phase ^= 1u;
+        // the slot that rounded a run up to an even length holds no candidate
+        for (int q = q0; q < q1; ++q) {
+            const uint32_t c = (uint32_t)rc[q];
+            const uint32_t cl = c < (uint32_t)a.cap_q ? c : (uint32_t)a.cap_q;
+            if (cl & 1u) pairs[run_off[q] + cl].x = -1;  // 0xffffffff: order key kEmptyKey
+        }
+        __syncthreads();
+        uint32_t mx = 0u, mn = 0xffffffffu;
+        for (uint32_t e = tid; e < ptot; e += THREADS) {
+            const uint32_t key = fkey(__int_as_float(pairs[e].x));
+            pairs[e].x = (int)key;
+            if (key != kEmptyKey) {
+                mx = max(mx, key);
+                mn = min(mn, key);
             }
         }
         __syncthreads();
+        block_max_min(mx, mn, scratch);
 
-        // exact threshold key T and how many keys equal to T are taken
-        uint32_t need;
-        const uint32_t T = cand_select(
-            cnt, (uint32_t)a.topk, [](uint32_t) { return true; },
-            [&](uint32_t e) { return keys[e]; }, hist, scratch, &need);
-        // the lowest `need` indices among the keys equal to T
-        uint32_t nt = 0;
-        for (uint32_t e = threadIdx.x; e < cnt; e += THREADS) nt += keys[e] == T;
-        uint32_t ntie;
-        block_incl_scan<THREADS>(nt, scratch, &ntie);
-        uint32_t idx_cut = 0xffffffffu;
-        if (ntie > need) {
-            uint32_t unused;
-            idx_cut = ~cand_select(
-                cnt, need, [&](uint32_t e) { return keys[e] == T; },
-                [&](uint32_t e) { return ~idxs[e]; }, hist, scratch, &unused);
-        }
-
-        // ascending output through the index bitmap, 65536 indices per pass
-        uint32_t* bm = hist;
-        constexpr int WPT = kBitmapWords / THREADS;  // bitmap words per thread
-        uint32_t written = 0;
-        for (long long c0 = 0; c0 < n && written < (uint32_t)a.topk; c0 += 32ll * kBitmapWords) {
-#pragma unroll
-            for (int j = 0; j < WPT; ++j) bm[threadIdx.x * WPT + j] = 0u;
+        // ---- the selection rule: key > T, or key == T and index <= idx_cut
+        auto key_of = [&](uint32_t e) { return (uint32_t)pairs[e].x; };
+        auto real = [&](uint32_t e) { return (uint32_t)pairs[e].x != kEmptyKey; };
+        uint32_t T = mx, need = k, idx_cut = 0xffffffffu;
+        bool gathered = false;
+        if (mx != mn) {
+            // one digit of up to 10 bits from the highest bit in which the
+            // candidates differ, over one 1024-bin histogram
+            const int top = 31 - __clz(mx ^ mn);
+            const int width = top + 1 >= 10 ? 10 : top + 1;
+            const int shift = top + 1 - width;
+            const uint32_t nb = 1u << width;
+            for (int i = tid; i < kCandBins; i += THREADS) hist[i] = 0u;
             __syncthreads();
-            for (uint32_t base = 0; base < cnt; base += 4 * THREADS) {
+            for (uint32_t e = tid; e < ptot; e += THREADS) {
+                const uint32_t key = key_of(e);
+                if (key != kEmptyKey) atomicAdd(&hist[(key >> shift) & (nb - 1u)], 1u);
+            }
+            __syncthreads();
+            // thread t owns the 4 bins 1023 - 4t ... 1020 - 4t, scanned from the top
+            constexpr int BPT = kCandBins / THREADS;
+            uint32_t cb[BPT], loc = 0;
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const uint32_t e = base + u * THREADS + threadIdx.x;
-                    if (e < cnt) {
-                        const uint32_t ky = keys[e], ix = idxs[e];
-                        const long long rel = (long long)ix - c0;
-                        if ((ky > T || (ky == T && ix <= idx_cut)) && rel >= 0 &&
-                            rel < 32ll * kBitmapWords)
-                            atomicOr(&bm[rel >> 5], 1u << (rel & 31));
+            for (int j = 0; j < BPT; ++j) {
+                cb[j] = hist[kCandBins - 1 - (BPT * tid + j)];
+                loc += cb[j];
+            }
+            const uint32_t incl = block_incl_scan<THREADS>(loc, scratch, nullptr);
+            uint32_t cum = incl - loc;
+            if (cum < k && k <= incl) {
+#pragma unroll
+                for (int j = 0; j < BPT; ++j) {
+                    if (cum + cb[j] >= k) {
+                        scratch[40] = (uint32_t)(kCandBins - 1 - (BPT * tid + j));
+                        scratch[41] = cum;
+                        scratch[42] = cb[j];
+                        break;
+                    }
+                    cum += cb[j];
+                }
+            }
+            __syncthreads();
+            const uint32_t d = scratch[40], count = scratch[42];
+            need = k - scratch[41];
+            const uint64_t pre = (((uint64_t)mx >> (top + 1)) << width) | d;
+            if (count <= (uint32_t)kCandGather) {
+                // gather that digit's candidates; the one ranked need-th among
+                // them by (key desc, index asc) fixes T and idx_cut at once
+                if (tid == 0) scratch[50] = 0u;
+                __syncthreads();
+                for (uint32_t e = tid; e < ptot; e += THREADS) {
+                    const int2 pv = pairs[e];
+                    if ((uint32_t)pv.x != kEmptyKey && ((uint64_t)(uint32_t)pv.x >> shift) == pre)
+                        cmp[atomicAdd(&scratch[50], 1u)] = pv;
+                }
+                __syncthreads();
+                const uint32_t ng = scratch[50];
+                for (uint32_t i = tid; i < ng; i += THREADS) {
+                    const uint32_t ki = (uint32_t)cmp[i].x, xi = (uint32_t)cmp[i].y;
+                    uint32_t rank = 0;
+                    for (uint32_t j = 0; j < ng; ++j) {
+                        const int2 cj = cmp[j];
+                        rank += (uint32_t)cj.x > ki || ((uint32_t)cj.x == ki && (uint32_t)cj.y < xi);
+                    }
+                    if (rank == need - 1u) {
+                        scratch[51] = ki;
+                        scratch[52] = xi;
                     }
                 }
+                __syncthreads();
+                T = scratch[51];
+                idx_cut = scratch[52];
+                gathered = true;
+            } else if (shift == 0) {
+                T = (uint32_t)pre;
+            } else {
+                T = cand_select(ptot, need, shift - 1, pre, real, key_of, hist, scratch, &need);
             }
-            __syncthreads();
-            uint32_t wv[WPT], local = 0;
-#pragma unroll
-            for (int j = 0; j < WPT; ++j) {
-                wv[j] = bm[threadIdx.x * WPT + j];
-                local += __popc(wv[j]);
-            }
-            uint32_t tot;
-            const uint32_t incl = block_incl_scan<THREADS>(local, scratch, &tot);
-            uint32_t pos = written + incl - local;
-#pragma unroll
-            for (int j = 0; j < WPT; ++j) {
-                uint32_t x = wv[j];
-                const long long wbase = c0 + 32ll * (threadIdx.x * WPT + j);
-                while (x) {
-                    const int bit = __ffs(x) - 1;
-                    if (pos < (uint32_t)a.topk) out[pos] = (int)(wbase + bit);
-                    ++pos;
-                    x &= x - 1u;
-                }
-            }
-            written += tot;
         }
-        if (threadIdx.x == 0) plan->state = ST_DONE;
+        if (!gathered) {
+            // the lowest `need` indices among the keys equal to T
+            uint32_t nt = 0;
+            for (uint32_t e = tid; e < ptot; e += THREADS) nt += key_of(e) == T;
+            uint32_t ntie;
+            block_incl_scan<THREADS>(nt, scratch, &ntie);
+            if (ntie > need) {
+                uint32_t unused;
+                idx_cut = ~cand_select(
+                    ptot, need, 31, 0ull, [&](uint32_t e) { return key_of(e) == T; },
+                    [&](uint32_t e) { return ~(uint32_t)pairs[e].y; }, hist, scratch, &unused);
+            }
+        }
+        __syncthreads();  // the histograms are done: the bucket counts reuse them
+
+        // ---- ascending output: the selected indices bucketed by index (1024
+        // buckets of a power-of-two width over the row), buckets placed by a
+        // scan, and each entry placed in its bucket by its rank among the
+        // bucket's entries (a bucket holds at most its width of indices)
+        auto chosen = [&](int2 pv) {
+            const uint32_t key = (uint32_t)pv.x;
+            return key > T || (key == T && (uint32_t)pv.y <= idx_cut);
+        };
+        int bsh = 0;  // bucket width 2^bsh >= n / kCandBins
+        while (((long long)kCandBins << bsh) < n) ++bsh;
+        for (int i = tid; i < kCandBins; i += THREADS) hist[i] = 0u;
+        __syncthreads();
+        for (uint32_t e = tid; e < ptot; e += THREADS) {
+            const int2 pv = pairs[e];
+            if (chosen(pv)) atomicAdd(&hist[(uint32_t)pv.y >> bsh], 1u);
+        }
+        __syncthreads();
+        {
+            // bucket starts: thread t owns buckets BPT t .. BPT t + BPT - 1
+            constexpr int BPT = kCandBins / THREADS;
+            uint32_t cb[BPT], loc = 0;
+#pragma unroll
+            for (int j = 0; j < BPT; ++j) {
+                cb[j] = hist[BPT * tid + j];
+                loc += cb[j];
+            }
+            uint32_t nsel;
+            uint32_t st = block_incl_scan<THREADS>(loc, scratch, &nsel) - loc;
+#pragma unroll
+            for (int j = 0; j < BPT; ++j) {
+                hist[BPT * tid + j] = st;
+                st += cb[j];
+            }
+            if (nsel != k) {
+                // cannot happen for finite scores: report it rather than write past
+                // the selection buffer
+                for (int i = tid; i < a.topk; i += THREADS) out[i] = -1;
+                if (tid == 0) {
+                    raise_status(a.d_status, IDX_DEV_STATE);
+                    plan->state = ST_DONE;
+                }
+                continue;
+            }
+        }
+        __syncthreads();
+        for (uint32_t e = tid; e < ptot; e += THREADS) {
+            const int2 pv = pairs[e];
+            if (chosen(pv)) sel[atomicAdd(&hist[(uint32_t)pv.y >> bsh], 1u)] = (uint32_t)pv.y;
+        }
+        __syncthreads();
+        // hist[b] is now the end of bucket b (the start of b + 1)
+        for (uint32_t p = tid; p < k; p += THREADS) {
+            const uint32_t x = sel[p];
+            const uint32_t b = x >> bsh;
+            const uint32_t lo = b ? hist[b - 1] : 0u, hi = hist[b];
+            uint32_t rank = 0;
+            for (uint32_t j = lo; j < hi; ++j) rank += sel[j] < x;
+            out[lo + rank] = (int)x;
+        }
+        if (tid == 0) plan->state = ST_DONE;
     }
 }
 
@@ -1199,13 +1399,16 @@ size_t split_workspace_bytes(int rows, int g) {
     return slots * (size_t)kSplitCap * 2 * sizeof(uint32_t) + slots * sizeof(int) + 256;
 }
 
-size_t cand_smem_bytes(int cap_q, int nruns) {
-    return (kBitmapWords + kCandScratch + (size_t)nruns + 1) * sizeof(uint32_t) +
-           (size_t)cap_q * kRuns * 2 * sizeof(uint32_t);
+size_t cand_smem_bytes(int cap_q, int nruns, int topk) {
+    return (size_t)CandSmem(nruns, topk, cap_q).words() * sizeof(uint32_t);
 }
 
 cudaError_t launch_cand_topk(const CandArgs& a, cudaStream_t s) {
-    const size_t sm = cand_smem_bytes(a.cap_q, a.nruns);
+    const CandSmem L(a.nruns, a.topk, a.cap_q);
+    // the mbarrier needs 8 bytes, the pair buffer (bulk copies) 16 bytes of alignment
+    if (L.bar() % 2 != 0 || L.gather() % 2 != 0 || L.pairs() % 4 != 0 || a.cap_q % 2 != 0)
+        return cudaErrorInvalidValue;
+    const size_t sm = cand_smem_bytes(a.cap_q, a.nruns, a.topk);
     cudaError_t e =
         cudaFuncSetAttribute(cand_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e != cudaSuccess) return e;

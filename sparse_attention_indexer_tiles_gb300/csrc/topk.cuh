@@ -69,7 +69,7 @@ struct CandArgs {
 
 cudaError_t launch_topk_rows(const TopkRowsArgs& a, cudaStream_t s);
 cudaError_t launch_cand_topk(const CandArgs& a, cudaStream_t s);
-size_t cand_smem_bytes(int cap_q, int nruns);
+size_t cand_smem_bytes(int cap_q, int nruns, int topk);
 size_t split_workspace_bytes(int rows, int g);
 
 }  // namespace idx

@@ -115,14 +115,14 @@ def _documented_workspace(rows, max_len, topk, nruns):
     """The fused workspace as the layout is documented: 256-byte aligned
     regions for the row plans (32 B each), the run counts [rows, nruns] int32,
     the slab [rows, nruns, cap_q] of (fp32 score, int32 index) pairs with
-    cap_q = ceil(cap / 8) + 64, the sample scratch [rows, max_len // S + 2]
+    cap_q = ceil(cap / 8) + 64 rounded up to even, the sample scratch [rows, max_len // S + 2]
     fp32, the rescan histograms [rows, 4096] and the rescan's list and flags
     of row blocks [blocks] int32 (these only when rows can see more than cap
     keys), and eight rescan counters."""
     def up(x):
         return (x + 255) // 256 * 256
     cap = max(math.ceil(2.25 * topk), 4096)
-    cap_q = -(-cap // 8) + 64
+    cap_q = (-(-cap // 8) + 64 + 1) // 2 * 2
     target = math.sqrt(cap / topk)
     t = max(32.0, (4.5 / math.log(max(target, 1.0001))) ** 2)
     S = max(s for s in (1, 3, 5, 7, 11, 15, 23, 31, 45, 63) if s <= target * topk / t)
@@ -136,15 +136,17 @@ def _documented_workspace(rows, max_len, topk, nruns):
 
 
 def test_fused_workspace_follows_the_documented_layout(lib):
-    """Eight runs per row and key split: four row blocks of H = 64 rows fill
-    one wave, so a call with few rows splits every block's keys into as many
-    parts as keep >= 64 key tiles each (at most six); 4096 rows are not
-    split.  These cases do not depend on the GPU's SM count."""
+    """Eight runs per row and key split.  With no device answering, the
+    library takes 148 SMs: 4096 rows (1024 row blocks of H = 64) fill their
+    last wave and are not split; 1024 rows split every block's keys in 4 (the
+    k <= 6 that fills the last wave best); calls with at most half a wave of
+    row blocks split up to one wave's worth (SMs / blocks), every part keeping
+    >= 32 key tiles."""
     import sparse_attention_indexer_tiles_gb300 as pkg
     ws = pkg.idx_score_topk_workspace
-    cases = [  # rows, keys, topk, expected key splits
-        (4096, 65536, 2048, 1), (8, 65536, 2048, 6), (8, 16384, 2048, 2), (64, 65536, 512, 6),
-        (8, 4096, 2048, 1)]
+    cases = [  # rows, keys, topk, expected key splits (148 SMs: no device answers here)
+        (4096, 65536, 2048, 1), (8, 65536, 2048, 16), (8, 16384, 2048, 4), (64, 65536, 512, 9),
+        (8, 4096, 2048, 1), (1024, 65536, 2048, 4), (16, 1 << 20, 2048, 37)]
     for rows, keys, topk, k in cases:
         expect, S = _documented_workspace(rows, keys, topk, 8 * k)
         assert ws(rows, keys, 0, 64, 128, topk, 2) == expect, (rows, keys, topk, k)
