@@ -185,11 +185,11 @@ FusedLayout fused_layout(int rows, long long max_len, int cap, int cap_q, int S,
         off = align_up(off + bytes, 256);
         return o;
     };
-    L.samp_stride = max_len / S + 2;
+    L.samp_stride = (max_len / S + 2 + 7) / 8 * 8;  // 16-byte aligned rows of 16-bit keys
     L.plan = take((size_t)rows * sizeof(RowPlan));
     L.run_cnt = take((size_t)rows * nruns * sizeof(int));
     L.slab = take((size_t)rows * nruns * cap_q * sizeof(int2));
-    L.samp = take(max_len > cap ? (size_t)rows * L.samp_stride * sizeof(float) : 0);
+    L.samp = take(max_len > cap ? (size_t)rows * L.samp_stride * sizeof(uint16_t) : 0);
     L.fb_hist = take(max_len > cap ? (size_t)rows * 4096 * sizeof(uint32_t) : 0);
     L.fb_blocks = take(max_len > cap ? nblk * sizeof(int) : 0);
     L.fb_bflag = take(max_len > cap ? nblk * sizeof(int) : 0);
@@ -341,7 +341,7 @@ idx_status idx_score_topk(const void* q, const void* k, const float* k_scale, co
     RowPlan* plan = reinterpret_cast<RowPlan*>(base + lay.plan);
     int* run_cnt = reinterpret_cast<int*>(base + lay.run_cnt);
     int2* slab = reinterpret_cast<int2*>(base + lay.slab);
-    float* samp = reinterpret_cast<float*>(base + lay.samp);
+    uint16_t* samp = reinterpret_cast<uint16_t*>(base + lay.samp);
     uint32_t* fb_hist = reinterpret_cast<uint32_t*>(base + lay.fb_hist);
     int* fb_cnt = reinterpret_cast<int*>(base + lay.fb_cnt);
     const bool sampling = max_len > p.cap;
@@ -380,7 +380,7 @@ idx_status idx_score_topk(const void* q, const void* k, const float* k_scale, co
         // 2. T_r = exact t-th largest sample score of each row
         TopkRowsArgs t;
         std::memset(&t, 0, sizeof(t));
-        t.scores = samp;
+        t.samp = samp;
         t.row_stride = lay.samp_stride;
         t.row_len = lay.samp_stride;
         t.rows = rows;

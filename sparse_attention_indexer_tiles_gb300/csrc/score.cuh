@@ -35,7 +35,7 @@ struct ScoreArgs {
     float* out;
     long long out_stride;
     // SM_SAMPLE
-    float* samp;
+    uint16_t* samp;       // [rows, samp_stride] the top 16 bits of each sample score's order key
     long long samp_stride;
     int S;
     long long nsamp;

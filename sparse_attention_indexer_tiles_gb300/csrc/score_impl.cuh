@@ -137,20 +137,24 @@ IDX_DEVI float head_reduce_quad(uint32_t taddr, const float2* wq) {
 // gets the same bits.
 template <int H>
 IDX_DEVI float head_reduce_lane(uint32_t taddr, const float* w_row) {
-    float v[H];
-    tmem_ld32x32b<H>(taddr, v);
-    float4 w4[H / 4];
-#pragma unroll
-    for (int i = 0; i < H / 4; ++i) w4[i] = reinterpret_cast<const float4*>(w_row)[i];
-    tmem_ld_wait();
+    constexpr int CH = H < 32 ? H : 32;  // columns per TMEM load
     float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int i = 0; i < H / 4; ++i) {
-        const float* y = v + 4 * i;
-        a0 = __ffma2_rn(make_float2(w4[i].x, w4[i].y),
-                        make_float2(y[0] + fabsf(y[0]), y[1] + fabsf(y[1])), a0);
-        a1 = __ffma2_rn(make_float2(w4[i].z, w4[i].w),
-                        make_float2(y[2] + fabsf(y[2]), y[3] + fabsf(y[3])), a1);
+    for (int c0 = 0; c0 < H; c0 += CH) {
+        float v[CH];
+        tmem_ld32x32b<CH>(taddr + (uint32_t)c0, v);
+        float4 w4[CH / 4];
+#pragma unroll
+        for (int i = 0; i < CH / 4; ++i) w4[i] = reinterpret_cast<const float4*>(w_row + c0)[i];
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < CH / 4; ++i) {
+            const float* y = v + 4 * i;
+            a0 = __ffma2_rn(make_float2(w4[i].x, w4[i].y),
+                            make_float2(y[0] + fabsf(y[0]), y[1] + fabsf(y[1])), a0);
+            a1 = __ffma2_rn(make_float2(w4[i].z, w4[i].w),
+                            make_float2(y[2] + fabsf(y[2]), y[3] + fabsf(y[3])), a1);
+        }
     }
     return (a0.x + a0.y) + (a1.x + a1.y);
 }
@@ -553,7 +557,7 @@ IDX_DEVI void score_pass(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                         if (mode == SM_MATERIALISE)
                             a.out[r * a.out_stride + off] = sc[j];
                         else
-                            a.samp[r * a.samp_stride + off] = sc[j];
+                            a.samp[r * a.samp_stride + off] = (uint16_t)(fkey(sc[j]) >> 16);
                     }
                 }
             } else if (mode == SM_FB_HIST) {

@@ -595,13 +595,48 @@ topk_rows_kernel(TopkRowsArgs a) {
 //
 // Page 1, "Sampled Threshold": T_r is the t-th largest of the m scores of row
 // r's strided sample, t = ceil(m * target * topk / len) with len the row's
-// visible length, so that about target * topk keys of the row reach it.  One
-// warp per row finds the exact t-th largest order key with four 8-bit radix
-// passes over the sample (a warp-private 256-bin histogram each), reading the
-// sample from L2; no block-wide synchronisation.
+// visible length, so that about target * topk keys of the row reach it.  The
+// scoring pass stores each sample as the top 16 bits of its order key; T_r is
+// the exact t-th largest of those 16-bit keys, and the emit pass takes every
+// key at or above T_r << 16.  The threshold only steers how many candidates
+// the slab receives (the slab top-k and the rescan make the result exact), so
+// the 16-bit resolution costs nothing but a few extra candidates; it halves
+// the sample's memory traffic and the radix passes.
 // Samples longer than this go to sample_threshold_cta_kernel.
 constexpr long long kThrCtaMin = 8192;
 
+// The row's sample and its rank t, or false for rows without a sample
+// threshold (plan->thr = 0: every visible key a candidate).
+struct SampleRow {
+    const uint16_t* keys;
+    uint32_t n, t;
+};
+
+IDX_DEVI bool sample_row(const TopkRowsArgs& a, int r, SampleRow* out) {
+    const long long vks = a.vis_ks[r], vke = a.vis_ke[r];
+    const long long len = vke - vks;
+    const long long phase = hash32((uint32_t)(r / a.rows_per_block) ^ a.phase_seed) % a.S;
+    const SampleSpan sp = sample_span(vks, vke, phase, a.S, a.nsamp);
+    const long long n = sp.b - sp.a;
+    if (len <= a.cap || n <= 0 || n > a.row_len) return false;
+    double t = ceil((double)n * (double)a.target * (double)a.topk / (double)len);
+    if (t < 1.0) t = 1.0;
+    if (t > (double)n) t = (double)n;
+    out->keys = a.samp + (long long)r * a.row_stride;
+    out->n = (uint32_t)n;
+    out->t = (uint32_t)t;
+    return true;
+}
+
+IDX_DEVI void set_plan_threshold(RowPlan* plan, uint32_t thr) {
+    plan->thr = thr;
+    plan->idx_cut = kAllIdx;
+    plan->state = ST_MAIN;
+}
+
+// One warp per row: two 8-bit radix passes over the row's 16-bit sample keys
+// (read from L2) with a warp-private 256-bin histogram; no block-wide
+// synchronisation.
 template <int WARPS>
 __global__ void __launch_bounds__(WARPS * 32)
 sample_threshold_kernel(TopkRowsArgs a) {
@@ -611,36 +646,26 @@ sample_threshold_kernel(TopkRowsArgs a) {
     if (r >= a.rows) return;  // whole warps only: nothing below syncs the block
     uint32_t* hist = hist_all[w];
     RowPlan* plan = a.plan + r;
-    const long long vks = a.vis_ks[r], vke = a.vis_ke[r];
-    const long long len = vke - vks;
-    const long long phase = hash32((uint32_t)(r / a.rows_per_block) ^ a.phase_seed) % a.S;
-    const SampleSpan sp = sample_span(vks, vke, phase, a.S, a.nsamp);
-    const long long n = sp.b - sp.a;
-    if (len <= a.cap || n <= 0 || n > a.row_len) {
+    SampleRow sr;
+    if (!sample_row(a, r, &sr)) {
         if (lane == 0) {
-            plan->thr = 0u;  // every visible key becomes a candidate
-            plan->idx_cut = kAllIdx;
-            plan->state = ST_MAIN;
+            set_plan_threshold(plan, 0u);  // every visible key becomes a candidate
+            const long long len = (long long)a.vis_ke[r] - a.vis_ks[r];
             if (a.d_stats && len > 0 && len <= a.cap) atomicAdd(&a.d_stats->emit_all_rows, 1);
         }
         return;
     }
-    if (a.split > 1 && n > kThrCtaMin) return;  // a whole CTA takes this row
-    double t = ceil((double)n * (double)a.target * (double)a.topk / (double)len);
-    if (t < 1.0) t = 1.0;
-    if (t > (double)n) t = (double)n;
-    const float* row = a.scores + (long long)r * a.row_stride;
-    uint32_t prefix = 0u, need = (uint32_t)t;
+    if (a.split > 1 && sr.n > kThrCtaMin) return;  // a whole CTA takes this row
+    uint32_t prefix = 0u, need = sr.t;
     bool ok = true;
-    for (int lev = 0; lev < 4; ++lev) {
-        const int shift = 24 - 8 * lev;
+    for (int lev = 0; lev < 2; ++lev) {
+        const int shift = 8 - 8 * lev;
 #pragma unroll
         for (int j = 0; j < 8; ++j) hist[lane * 8 + j] = 0u;
         __syncwarp();
-        for (long long e = lane; e < n; e += 32) {
-            const uint32_t key = fkey(__ldg(row + e));
-            if (lev == 0 || (key >> (shift + 8)) == prefix)
-                atomicAdd(&hist[(key >> shift) & 255u], 1u);
+        for (uint32_t e = lane; e < sr.n; e += 32) {
+            const uint32_t key = sr.keys[e];
+            if (lev == 0 || (key >> 8) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
         }
         __syncwarp();
         // lane l holds bins 255 - 8l ... 248 - 8l (from the largest keys down)
@@ -682,50 +707,71 @@ sample_threshold_kernel(TopkRowsArgs a) {
         prefix = (prefix << 8) | digit;
         __syncwarp();
     }
-    if (lane == 0) {
-        // a failed pick leaves thr = 0: every key a candidate, the slab
-        // overflows and the exact rescan takes the row
-        plan->thr = ok ? prefix : 0u;
-        plan->idx_cut = kAllIdx;
-        plan->state = ST_MAIN;
-    }
+    // a failed pick leaves thr = 0: every key a candidate, the slab overflows
+    // and the exact rescan takes the row
+    if (lane == 0) set_plan_threshold(plan, ok ? prefix << 16 : 0u);
 }
 
-// The same threshold for long samples (tens of thousands of scores per row):
-// one 256-thread CTA per row, a 12-bit histogram pass over the sample, then
-// the values of the threshold bin gathered into shared memory and refined
-// there (further passes over the sample only if that bin holds more than
-// 4096), i.e. two passes over the sample instead of four.
+// The same threshold for long samples (tens of thousands of keys per row):
+// one 256-thread CTA per row, the two 8-bit passes over per-warp histograms.
 constexpr int kThrCtaThreads = 256;
-constexpr size_t kThrCtaSmem = (kHistBins + 64 + 2 * (size_t)kTieCap) * sizeof(uint32_t);
 
 __global__ void __launch_bounds__(kThrCtaThreads) sample_threshold_cta_kernel(TopkRowsArgs a) {
-    extern __shared__ __align__(16) uint32_t smem[];
-    uint32_t* hist = smem;
-    uint32_t* scratch = hist + kHistBins;
-    uint32_t* tkey = scratch + 64;
-    uint32_t* tpos = tkey + kTieCap;
+    constexpr int THREADS = kThrCtaThreads, W = THREADS / 32;
+    __shared__ uint32_t hist[W * 256];
+    __shared__ uint32_t scratch[64];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int r = blockIdx.x;
-    RowPlan* plan = a.plan + r;
-    const long long vks = a.vis_ks[r], vke = a.vis_ke[r];
-    const long long len = vke - vks;
-    const long long phase = hash32((uint32_t)(r / a.rows_per_block) ^ a.phase_seed) % a.S;
-    const SampleSpan sp = sample_span(vks, vke, phase, a.S, a.nsamp);
-    const long long n = sp.b - sp.a;
+    SampleRow sr;
     // rows the warp kernel handled (short samples, or no sampling at all)
-    if (len <= a.cap || n <= kThrCtaMin || n > a.row_len) return;
-    double t = ceil((double)n * (double)a.target * (double)a.topk / (double)len);
-    if (t < 1.0) t = 1.0;
-    if (t > (double)n) t = (double)n;
-    const RowView v = make_view(a.scores + (long long)r * a.row_stride, n);
-    int rescans = 0;
-    const Threshold th =
-        find_threshold<kThrCtaThreads, 4>(v, (uint32_t)t, hist, tkey, tpos, scratch, &rescans);
-    if (threadIdx.x == 0) {
-        plan->thr = th.key;
-        plan->idx_cut = kAllIdx;
-        plan->state = ST_MAIN;
+    if (!sample_row(a, r, &sr) || sr.n <= kThrCtaMin) return;
+    uint32_t* hw = hist + w * 256;
+    uint32_t prefix = 0u, need = sr.t;
+    for (int lev = 0; lev < 2; ++lev) {
+        const int shift = 8 - 8 * lev;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) hw[lane * 8 + j] = 0u;
+        __syncthreads();
+        // four independent 16-byte loads of 8 keys each per thread in flight
+        const uint4* v4 = reinterpret_cast<const uint4*>(sr.keys);
+        const uint32_t n8 = sr.n / 8;
+        for (uint32_t base = threadIdx.x; base < n8; base += 4 * THREADS) {
+            uint4 x[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                x[u] = base + u * THREADS < n8 ? __ldcg(v4 + base + u * THREADS) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                if (base + u * THREADS >= n8) continue;
+                const uint32_t wd[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+#pragma unroll
+                for (int h = 0; h < 8; ++h) {
+                    const uint32_t key = (wd[h >> 1] >> (16 * (h & 1))) & 0xffffu;
+                    if (lev == 0 || (key >> 8) == prefix) atomicAdd(&hw[(key >> shift) & 255u], 1u);
+                }
+            }
+        }
+        for (uint32_t e = n8 * 8 + threadIdx.x; e < sr.n; e += THREADS) {
+            const uint32_t key = sr.keys[e];
+            if (lev == 0 || (key >> 8) == prefix) atomicAdd(&hw[(key >> shift) & 255u], 1u);
+        }
+        __syncthreads();
+        // thread t owns digit 255 - t: a scan from the top digit down
+        uint32_t c = 0;
+#pragma unroll
+        for (int ww = 0; ww < W; ++ww) c += hist[ww * 256 + 255 - threadIdx.x];
+        const uint32_t incl = block_incl_scan<THREADS>(c, scratch, nullptr);
+        const uint32_t excl = incl - c;
+        if (excl < need && need <= incl) {
+            scratch[40] = 255u - threadIdx.x;
+            scratch[41] = excl;
+        }
+        __syncthreads();
+        need -= scratch[41];
+        prefix = (prefix << 8) | scratch[40];
+        __syncthreads();
     }
+    if (threadIdx.x == 0) set_plan_threshold(a.plan + r, prefix << 16);
 }
 
 // ------------------------------------------------------- row split
@@ -1360,11 +1406,7 @@ cudaError_t launch_topk_rows(const TopkRowsArgs& a, cudaStream_t s) {
         b.split = a.row_len > kThrCtaMin ? 2 : 0;
         sample_threshold_kernel<WARPS><<<(a.rows + WARPS - 1) / WARPS, WARPS * 32, 0, s>>>(b);
         if (b.split) {
-            static cudaError_t attr = cudaFuncSetAttribute(
-                sample_threshold_cta_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                (int)kThrCtaSmem);
-            if (attr != cudaSuccess) return attr;
-            sample_threshold_cta_kernel<<<a.rows, kThrCtaThreads, kThrCtaSmem, s>>>(b);
+            sample_threshold_cta_kernel<<<a.rows, kThrCtaThreads, 0, s>>>(b);
             count_launches(1);
         }
         return cudaGetLastError();

@@ -26,7 +26,9 @@ struct TopkRowsArgs {
     int relative;         // row r's data starts at column 0 instead of ks[r]
     int mode;             // TOPK_OUTPUT or TOPK_THRESHOLD
     int* out;             // [rows, topk] (TOPK_OUTPUT)
-    // TOPK_THRESHOLD: per-row sample threshold written into plan[r]
+    // TOPK_THRESHOLD: per-row sample threshold written into plan[r], from the
+    // samples' 16-bit order keys samp [rows, row_stride]
+    const uint16_t* samp;
     RowPlan* plan;
     const int* vis_ks;    // the row's visible key range, for the rank t
     const int* vis_ke;

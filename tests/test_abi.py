@@ -115,8 +115,8 @@ def _documented_workspace(rows, max_len, topk, nruns):
     """The fused workspace as the layout is documented: 256-byte aligned
     regions for the row plans (32 B each), the run counts [rows, nruns] int32,
     the slab [rows, nruns, cap_q] of (fp32 score, int32 index) pairs with
-    cap_q = ceil(cap / 8) + 64 rounded up to even, the sample scratch [rows, max_len // S + 2]
-    fp32, the rescan histograms [rows, 4096] and the rescan's list and flags
+    cap_q = ceil(cap / 8) + 64 rounded up to even, the sample scratch [rows, max_len // S + 2
+    rounded up to a multiple of 8] of 16-bit keys, the rescan histograms [rows, 4096] and the rescan's list and flags
     of row blocks [blocks] int32 (these only when rows can see more than cap
     keys), and eight rescan counters."""
     def up(x):
@@ -129,7 +129,7 @@ def _documented_workspace(rows, max_len, topk, nruns):
     sampled = max_len > cap
     nblk = -(-rows // 4)  # row blocks of 256 / H rows at H = 64
     regions = [rows * 32, rows * nruns * 4, rows * nruns * cap_q * 8,
-               rows * (max_len // S + 2) * 4 if sampled else 0,
+               rows * ((max_len // S + 2 + 7) // 8 * 8) * 2 if sampled else 0,
                rows * 4096 * 4 if sampled else 0,
                nblk * 4 if sampled else 0, nblk * 4 if sampled else 0, 8 * 4]
     return sum(up(r) for r in regions), S
