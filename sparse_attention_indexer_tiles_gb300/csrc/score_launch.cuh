@@ -60,6 +60,7 @@ cudaError_t launch_score_t(const ScoreLaunch& L, cudaStream_t s) {
         make_map_2d(&tk, L.k, elem, (uint64_t)L.D, (uint64_t)a.keys, C::CHUNK_ELEMS, 128) !=
             CUDA_SUCCESS)
         return cudaErrorInvalidValue;
+    // the strided sample view for the launches that score the sample
     if (a.mode == SM_SAMPLE) {
         if (make_map_strided(&tks, L.k, elem, (uint64_t)L.D, (uint64_t)a.S, (uint64_t)a.nsamp,
                              C::CHUNK_ELEMS) != CUDA_SUCCESS)

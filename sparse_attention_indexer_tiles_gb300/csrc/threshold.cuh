@@ -1,0 +1,136 @@
+// The sample threshold T_r of one row, computed by one warp (page 1,
+// "Sampled Threshold": T_r is the t-th largest of the m scores of row r's
+// strided sample, t = ceil(m * target * topk / len) with len the row's
+// visible length, so that about target * topk keys of the row reach it).
+// The scoring pass stores each sample as the top 16 bits of its order key;
+// T_r is the exact t-th largest of those keys, by two 8-bit radix passes
+// over a warp-private 256-bin histogram, and the emit pass takes every key at
+// or above T_r << 16.  The threshold only steers how many candidates the slab
+// receives (the slab top-k and the rescan make the result exact), so the
+// 16-bit resolution costs nothing but a few extra candidates.
+#pragma once
+
+#include "common.cuh"
+#include "plan.cuh"
+
+namespace idx {
+
+struct ThrParams {
+    const int* ks;
+    const int* ke;
+    const uint16_t* samp;     // [rows, samp_stride] 16-bit sample keys
+    long long samp_stride;
+    long long nsamp;          // floor(keys / S)
+    int S;
+    int cap;
+    int topk;
+    float target;
+    int rows_per_block;       // rows sharing one sample phase
+    uint32_t phase_seed;
+    RowPlan* plan;
+    idx_stats* d_stats;
+};
+
+// The row's sample and its rank t, or false for rows without a sample
+// threshold (every visible key a candidate).
+struct SampleRow {
+    const uint16_t* keys;
+    uint32_t n, t;
+};
+
+IDX_DEVI bool sample_row(const ThrParams& p, int r, SampleRow* out) {
+    const long long vks = p.ks[r], vke = p.ke[r];
+    const long long len = vke - vks;
+    const long long phase = hash32((uint32_t)(r / p.rows_per_block) ^ p.phase_seed) % p.S;
+    const SampleSpan sp = sample_span(vks, vke, phase, p.S, p.nsamp);
+    const long long n = sp.b - sp.a;
+    if (len <= p.cap || n <= 0 || n > p.samp_stride) return false;
+    double t = ceil((double)n * (double)p.target * (double)p.topk / (double)len);
+    if (t < 1.0) t = 1.0;
+    if (t > (double)n) t = (double)n;
+    out->keys = p.samp + (long long)r * p.samp_stride;
+    out->n = (uint32_t)n;
+    out->t = (uint32_t)t;
+    return true;
+}
+
+IDX_DEVI void set_plan_threshold(RowPlan* plan, uint32_t thr) {
+    plan->thr = thr;
+    plan->idx_cut = kAllIdx;
+    plan->state = ST_MAIN;
+}
+
+// One warp: the threshold of row r into plan[r].  Rows with no sample
+// threshold get thr = 0 (every visible key a candidate).  `max_n` > 0 leaves
+// rows with longer samples alone (a CTA per row takes them) and returns false.
+IDX_DEVI bool warp_row_threshold(const ThrParams& p, int r, uint32_t* hist, uint32_t max_n = 0) {
+    const int lane = threadIdx.x & 31;
+    RowPlan* plan = p.plan + r;
+    SampleRow sr;
+    if (!sample_row(p, r, &sr)) {
+        if (lane == 0) {
+            set_plan_threshold(plan, 0u);
+            const long long len = (long long)p.ke[r] - p.ks[r];
+            if (p.d_stats && len > 0 && len <= p.cap) atomicAdd(&p.d_stats->emit_all_rows, 1);
+        }
+        return true;
+    }
+    if (max_n && sr.n > max_n) return false;
+    uint32_t prefix = 0u, need = sr.t;
+    bool ok = true;
+    for (int lev = 0; lev < 2; ++lev) {
+        const int shift = 8 - 8 * lev;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) hist[lane * 8 + j] = 0u;
+        __syncwarp();
+        for (uint32_t e = lane; e < sr.n; e += 32) {
+            const uint32_t key = sr.keys[e];
+            if (lev == 0 || (key >> 8) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+        }
+        __syncwarp();
+        // lane l holds bins 255 - 8l ... 248 - 8l (from the largest keys down)
+        uint32_t c[8], local = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            c[j] = hist[255 - 8 * lane - j];
+            local += c[j];
+        }
+        uint32_t incl = local;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const uint32_t o = __shfl_up_sync(0xffffffffu, incl, d);
+            if (lane >= d) incl += o;
+        }
+        const uint32_t excl = incl - local;
+        const uint32_t owner = __ballot_sync(0xffffffffu, excl < need && need <= incl);
+        if (owner == 0u) {  // cannot happen: need never exceeds the keys left
+            ok = false;
+            break;
+        }
+        const int src = __ffs(owner) - 1;
+        uint32_t digit = 0u, above = 0u;
+        if (lane == src) {
+            uint32_t cum = excl;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                if (cum + c[j] >= need) {
+                    digit = 255u - 8u * (uint32_t)lane - (uint32_t)j;
+                    above = cum;
+                    break;
+                }
+                cum += c[j];
+            }
+        }
+        digit = __shfl_sync(0xffffffffu, digit, src);
+        above = __shfl_sync(0xffffffffu, above, src);
+        need -= above;
+        prefix = (prefix << 8) | digit;
+        __syncwarp();
+    }
+    // a failed pick leaves thr = 0: every key a candidate, the slab overflows
+    // and the exact rescan takes the row
+    if (lane == 0) set_plan_threshold(plan, ok ? prefix << 16 : 0u);
+    return true;
+}
+
+}  // namespace idx

@@ -18,6 +18,7 @@
 //                       overflowed for the exact rescan.
 #include "plan.cuh"
 #include "radix.cuh"
+#include "threshold.cuh"
 #include "topk.cuh"
 
 namespace idx {
@@ -593,123 +594,36 @@ topk_rows_kernel(TopkRowsArgs a) {
 
 // ------------------------------------------------------ sample threshold
 //
-// Page 1, "Sampled Threshold": T_r is the t-th largest of the m scores of row
-// r's strided sample, t = ceil(m * target * topk / len) with len the row's
-// visible length, so that about target * topk keys of the row reach it.  The
-// scoring pass stores each sample as the top 16 bits of its order key; T_r is
-// the exact t-th largest of those 16-bit keys, and the emit pass takes every
-// key at or above T_r << 16.  The threshold only steers how many candidates
-// the slab receives (the slab top-k and the rescan make the result exact), so
-// the 16-bit resolution costs nothing but a few extra candidates; it halves
-// the sample's memory traffic and the radix passes.
-// Samples longer than this go to sample_threshold_cta_kernel.
+// T_r of every sampled row (threshold.cuh): one warp per row; rows whose
+// sample holds more than kThrCtaMin keys go to sample_threshold_cta_kernel.
 constexpr long long kThrCtaMin = 8192;
 
-// The row's sample and its rank t, or false for rows without a sample
-// threshold (plan->thr = 0: every visible key a candidate).
-struct SampleRow {
-    const uint16_t* keys;
-    uint32_t n, t;
-};
-
-IDX_DEVI bool sample_row(const TopkRowsArgs& a, int r, SampleRow* out) {
-    const long long vks = a.vis_ks[r], vke = a.vis_ke[r];
-    const long long len = vke - vks;
-    const long long phase = hash32((uint32_t)(r / a.rows_per_block) ^ a.phase_seed) % a.S;
-    const SampleSpan sp = sample_span(vks, vke, phase, a.S, a.nsamp);
-    const long long n = sp.b - sp.a;
-    if (len <= a.cap || n <= 0 || n > a.row_len) return false;
-    double t = ceil((double)n * (double)a.target * (double)a.topk / (double)len);
-    if (t < 1.0) t = 1.0;
-    if (t > (double)n) t = (double)n;
-    out->keys = a.samp + (long long)r * a.row_stride;
-    out->n = (uint32_t)n;
-    out->t = (uint32_t)t;
-    return true;
+IDX_DEVI ThrParams thr_params(const TopkRowsArgs& a) {
+    ThrParams p;
+    p.ks = a.vis_ks;
+    p.ke = a.vis_ke;
+    p.samp = a.samp;
+    p.samp_stride = a.row_stride;
+    p.nsamp = a.nsamp;
+    p.S = a.S;
+    p.cap = a.cap;
+    p.topk = a.topk;
+    p.target = a.target;
+    p.rows_per_block = a.rows_per_block;
+    p.phase_seed = a.phase_seed;
+    p.plan = a.plan;
+    p.d_stats = a.d_stats;
+    return p;
 }
 
-IDX_DEVI void set_plan_threshold(RowPlan* plan, uint32_t thr) {
-    plan->thr = thr;
-    plan->idx_cut = kAllIdx;
-    plan->state = ST_MAIN;
-}
-
-// One warp per row: two 8-bit radix passes over the row's 16-bit sample keys
-// (read from L2) with a warp-private 256-bin histogram; no block-wide
-// synchronisation.
 template <int WARPS>
 __global__ void __launch_bounds__(WARPS * 32)
 sample_threshold_kernel(TopkRowsArgs a) {
     __shared__ uint32_t hist_all[WARPS][256];
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int w = threadIdx.x >> 5;
     const int r = blockIdx.x * WARPS + w;
     if (r >= a.rows) return;  // whole warps only: nothing below syncs the block
-    uint32_t* hist = hist_all[w];
-    RowPlan* plan = a.plan + r;
-    SampleRow sr;
-    if (!sample_row(a, r, &sr)) {
-        if (lane == 0) {
-            set_plan_threshold(plan, 0u);  // every visible key becomes a candidate
-            const long long len = (long long)a.vis_ke[r] - a.vis_ks[r];
-            if (a.d_stats && len > 0 && len <= a.cap) atomicAdd(&a.d_stats->emit_all_rows, 1);
-        }
-        return;
-    }
-    if (a.split > 1 && sr.n > kThrCtaMin) return;  // a whole CTA takes this row
-    uint32_t prefix = 0u, need = sr.t;
-    bool ok = true;
-    for (int lev = 0; lev < 2; ++lev) {
-        const int shift = 8 - 8 * lev;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) hist[lane * 8 + j] = 0u;
-        __syncwarp();
-        for (uint32_t e = lane; e < sr.n; e += 32) {
-            const uint32_t key = sr.keys[e];
-            if (lev == 0 || (key >> 8) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
-        }
-        __syncwarp();
-        // lane l holds bins 255 - 8l ... 248 - 8l (from the largest keys down)
-        uint32_t c[8], local = 0;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            c[j] = hist[255 - 8 * lane - j];
-            local += c[j];
-        }
-        uint32_t incl = local;
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-            const uint32_t o = __shfl_up_sync(0xffffffffu, incl, d);
-            if (lane >= d) incl += o;
-        }
-        const uint32_t excl = incl - local;
-        const uint32_t owner = __ballot_sync(0xffffffffu, excl < need && need <= incl);
-        if (owner == 0u) {  // cannot happen: need never exceeds the keys left
-            ok = false;
-            break;
-        }
-        const int src = __ffs(owner) - 1;
-        uint32_t digit = 0u, above = 0u;
-        if (lane == src) {
-            uint32_t cum = excl;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                if (cum + c[j] >= need) {
-                    digit = 255u - 8u * (uint32_t)lane - (uint32_t)j;
-                    above = cum;
-                    break;
-                }
-                cum += c[j];
-            }
-        }
-        digit = __shfl_sync(0xffffffffu, digit, src);
-        above = __shfl_sync(0xffffffffu, above, src);
-        need -= above;
-        prefix = (prefix << 8) | digit;
-        __syncwarp();
-    }
-    // a failed pick leaves thr = 0: every key a candidate, the slab overflows
-    // and the exact rescan takes the row
-    if (lane == 0) set_plan_threshold(plan, ok ? prefix << 16 : 0u);
+    warp_row_threshold(thr_params(a), r, hist_all[w], a.split > 1 ? (uint32_t)kThrCtaMin : 0u);
 }
 
 // The same threshold for long samples (tens of thousands of keys per row):
@@ -724,7 +638,7 @@ __global__ void __launch_bounds__(kThrCtaThreads) sample_threshold_cta_kernel(To
     const int r = blockIdx.x;
     SampleRow sr;
     // rows the warp kernel handled (short samples, or no sampling at all)
-    if (!sample_row(a, r, &sr) || sr.n <= kThrCtaMin) return;
+    if (!sample_row(thr_params(a), r, &sr) || sr.n <= kThrCtaMin) return;
     uint32_t* hw = hist + w * 256;
     uint32_t prefix = 0u, need = sr.t;
     for (int lev = 0; lev < 2; ++lev) {
