@@ -91,7 +91,14 @@ typedef struct idx_options {
     int relative_rows;    /* idx_topk_from_scores: row r's visible scores start at
                              column 0 of its row (the layout idx_score_materialise
                              writes) instead of column ks[r] */
-    int reserved;
+    int test_stall_us;    /* test only, 0 = off.  n > 0: the TMA producer of every
+                             scoring pass issues no copy for key tile 1, and the
+                             scoring kernel's waits give up after about n
+                             microseconds (instead of about 2 s).  A pass with more
+                             than one tile then stops early with IDX_DEV_TIMEOUT in
+                             *d_status, leaving no copy or MMA in flight; the call
+                             returns and its results are meaningless.  It exists to
+                             run the timeout unwind on purpose. */
     void* const* stage_events; /* optional array of cudaEvent_t, recorded on `stream`
                              at stage boundaries (NULL entries are skipped).
                              idx_score_topk: [0] start, [1] after the sample and its

@@ -247,21 +247,26 @@ def topk_from_scores(scores, ks, ke, topk: int, rows=None, nthreads: int | None 
     return out
 
 
-def page_transform(idx, table, page_size: int = 64, row_map=None):
+def page_transform(idx, table, page_size: int = 64, row_map=None, table_rows=None):
     """Page-table transform of idx [rows, topk] (a new array) and the number
-    of positions whose page lies outside the table row (set to -1)."""
+    of positions set to -1 because their page lies outside the table row or
+    their table row (row_map entry) outside the table's first `table_rows`
+    rows (default: all of them)."""
     ix = _np(idx, np.int32)
     tb = _np(table, np.int32)
+    table_rows = tb.shape[0] if table_rows is None else int(table_rows)
+    if not 0 <= table_rows <= tb.shape[0]:
+        raise ValueError("oracle page_transform: table_rows outside the table")
     rows, topk = ix.shape
     rm = None if row_map is None else _np(row_map, np.int32)
     out = np.empty_like(ix)
     lib = _load()
     fn = lib.orc_page_transform
     P, i32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong
-    fn.argtypes = [P, i32, i32, P, i64, P, i32, P]
+    fn.argtypes = [P, i32, i32, P, i64, i64, P, i32, P]
     fn.restype = i64
-    bad = fn(_ptr(ix), rows, topk, _ptr(tb), tb.shape[1], None if rm is None else _ptr(rm),
-             page_size, _ptr(out))
+    bad = fn(_ptr(ix), rows, topk, _ptr(tb), table_rows, tb.shape[1],
+             None if rm is None else _ptr(rm), page_size, _ptr(out))
     if bad < 0:
         raise ValueError("oracle page_transform: bad arguments")
     return out, int(bad)

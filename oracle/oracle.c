@@ -284,22 +284,24 @@ int orc_topk_from_scores(const float* scores, long long stride, const int32_t* k
 }
 
 /* Page-table transform of idx [rows, topk] into out (same shape).
- * table is [*, table_stride]; row r uses table row row_map[r] (row_map NULL:
- * row r).  Returns the number of positions whose page lies outside the table
- * row (those become -1), or -1 for bad arguments. */
+ * table is [table_rows, table_stride]; row r uses table row row_map[r]
+ * (row_map NULL: row r).  A position whose page lies outside the table row,
+ * or whose table row lies outside [0, table_rows), has no physical slot: it
+ * becomes -1 and is counted.  Returns that count, or -1 for bad arguments. */
 long long orc_page_transform(const int32_t* idx, int rows, int topk, const int32_t* table,
-                             long long table_stride, const int32_t* row_map, int page_size,
-                             int32_t* out) {
-    if (rows < 0 || topk < 0 || page_size < 1 || table_stride < 0) return -1;
+                             long long table_rows, long long table_stride,
+                             const int32_t* row_map, int page_size, int32_t* out) {
+    if (rows < 0 || topk < 0 || page_size < 1 || table_stride < 0 || table_rows < 0) return -1;
     long long bad = 0;
     for (int r = 0; r < rows; ++r) {
         const long long t = row_map ? (long long)row_map[r] : (long long)r;
+        const int row_ok = t >= 0 && t < table_rows;
         for (int i = 0; i < topk; ++i) {
             const long long p = idx[(long long)r * topk + i];
             long long v = p;
             if (p >= 0) {
                 const long long page = p / page_size;
-                if (page < table_stride) {
+                if (row_ok && page < table_stride) {
                     v = (long long)table[t * table_stride + page] * page_size + p % page_size;
                 } else {
                     v = -1;

@@ -46,7 +46,7 @@ class Options(ctypes.Structure):
     _fields_ = [("cap_factor", ctypes.c_float), ("target_factor", ctypes.c_float),
                 ("sample_stride", ctypes.c_int), ("row_split", ctypes.c_int),
                 ("d_status", ctypes.c_void_p), ("d_stats", ctypes.c_void_p),
-                ("relative_rows", ctypes.c_int), ("reserved", ctypes.c_int),
+                ("relative_rows", ctypes.c_int), ("test_stall_us", ctypes.c_int),
                 ("stage_events", ctypes.c_void_p)]
 
 

@@ -235,6 +235,11 @@ ScoreLaunch make_score_launch(const void* q, const void* k, const float* k_scale
     L.a.d_stats = opt ? opt->d_stats : nullptr;
     L.a.ksplit = 1;
     L.a.nruns = kRuns;
+    // about 2 s at the GB300's clock; the test knob shortens it and withholds
+    // key tile 1 of every scoring pass
+    const int stall_us = opt ? opt->test_stall_us : 0;
+    L.a.wait_limit = stall_us > 0 ? 2100LL * stall_us : (1LL << 32);
+    L.a.withhold_tile = stall_us > 0 ? 1 : -1;
     return L;
 }
 

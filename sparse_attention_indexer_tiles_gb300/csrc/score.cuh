@@ -57,6 +57,11 @@ struct ScoreArgs {
     int* fb_bflag;        // [row blocks] 1 once a block is listed
     int grid_x;           // CTAs of an SM_RESCAN launch (they stride over the list)
     int level;
+    // bounded waits: a wait on the pipeline gives up after wait_limit clock
+    // cycles; withhold_tile >= 0 (a test of that path) makes the producer issue
+    // no copy for that tile of every pass, so the waits on it run out
+    long long wait_limit;
+    int withhold_tile;
     int* d_status;
     idx_stats* d_stats;
 };

@@ -364,11 +364,14 @@ IDX_DEVI void score_pass(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
             for (int i = 0; i < ntiles; ++i) {
                 const int s = i % C::NS;
                 const uint32_t use = (uint32_t)(i / C::NS);
-                if (i >= C::NS && !mbar_wait(&empty[s], (use & 1u) ^ 1u, abort_flag)) {
+                if (i >= C::NS &&
+                    !mbar_wait(&empty[s], (use & 1u) ^ 1u, abort_flag, a.wait_limit)) {
                     *abort_flag = 1;
                     raise_status(a.d_status, IDX_DEV_TIMEOUT);
                     break;
                 }
+                issued = i + 1;
+                if (i == a.withhold_tile) continue;  // (test) no copy: its waits run out
                 mbar_arrive_expect_tx(&full[s], C::A_BYTES);
                 const int row0 = (t0 + i) * C::M;
 #pragma unroll
@@ -379,28 +382,29 @@ IDX_DEVI void score_pass(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                     else
                         tma_load_2d(dst, &tm_k, &full[s], c * C::CHUNK_ELEMS, row0);
                 }
-                issued = i + 1;
             }
             // do not leave with copies in flight: wait (bounded) for the last stages
             for (int i = issued > C::NS ? issued - C::NS : 0; i < issued; ++i)
-                mbar_wait(&full[i % C::NS], (uint32_t)((i / C::NS) & 1), nullptr, 1ll << 28);
+                if (i != a.withhold_tile)
+                    mbar_wait(&full[i % C::NS], (uint32_t)((i / C::NS) & 1), nullptr, 1ll << 28);
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
             const uint32_t a_base = smem_u32(smem + C::OFF_A);
             const uint32_t b_base = smem_u32(smem + C::OFF_B);
-            bool ok = mbar_wait(qfull, 0, abort_flag);
+            bool ok = mbar_wait(qfull, 0, abort_flag, a.wait_limit);
             int issued = 0;
             for (int i = 0; ok && i < ntiles; ++i) {
                 const int s = i % C::NS;
                 const int b = i & 1;
                 // buffer b is free once its team has read tile i - 2
-                if (i >= 2 && !mbar_wait(&acce[b], (uint32_t)(((i >> 1) & 1) ^ 1), abort_flag)) {
+                if (i >= 2 && !mbar_wait(&acce[b], (uint32_t)(((i >> 1) & 1) ^ 1), abort_flag,
+                                         a.wait_limit)) {
                     ok = false;
                     break;
                 }
-                if (!mbar_wait(&full[s], (uint32_t)((i / C::NS) & 1), abort_flag)) {
+                if (!mbar_wait(&full[s], (uint32_t)((i / C::NS) & 1), abort_flag, a.wait_limit)) {
                     ok = false;
                     break;
                 }
@@ -524,7 +528,8 @@ IDX_DEVI void score_pass(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
             s_off += s_step;
             next_scale = i + 2 < ntiles && s_i < ilim ? __ldg(a.k_scale + s_off) : 0.f;
             // warp-uniform outcome: the TMEM loads below are .sync.aligned
-            if (!__all_sync(0xffffffffu, mbar_wait(&accf[team], (uint32_t)(u & 1), abort_flag))) {
+            if (!__all_sync(0xffffffffu,
+                            mbar_wait(&accf[team], (uint32_t)(u & 1), abort_flag, a.wait_limit))) {
                 *abort_flag = 1;
                 if (lane == 0) raise_status(a.d_status, IDX_DEV_TIMEOUT);
                 break;

@@ -100,7 +100,10 @@ def test_out_of_range_pages_and_rows_raise(idx):
     assert got[0].tolist() == [t[0, 0] * 64, t[0, 0] * 64 + 63, -1, -1]
     assert got[1].tolist() == [t[1, 0] * 64 + 5, t[1, 7] * 64 + 1, -1, t[1, 0] * 64 + 3]
     assert got[2].tolist() == [-1, -1, -1, -1]
-    assert stats.read()["status"] != 0
+    assert stats.read()["status"] & 0x2  # IDX_DEV_RANGE
+    # the oracle, given the table's row bound, agrees entry for entry
+    ref, bad = oracle.page_transform(pos, table, 64, row_map)
+    assert np.array_equal(got, ref) and bad == 6
 
 
 def test_after_the_fused_top_k(idx):

@@ -268,7 +268,14 @@ def test_page_transform_hand_example(orc):
     g = json.load(open(os.path.join(GOLDEN, "page_transform.json")))
     idx = np.array([r["idx"] for r in g["rows"]], dtype=np.int32)
     rmap = np.array([r["table_row"] for r in g["rows"]], dtype=np.int32)
-    got, bad = orc.page_transform(idx, np.array(g["table"], np.int32), g["page_size"], rmap)
+    table = np.array(g["table"], np.int32)
+    # first with a third row present in memory but outside the declared table:
+    # the row bound, not the array's end, decides
+    padded = np.vstack([table, np.ones((1, table.shape[1]), np.int32)])
+    got, bad = orc.page_transform(idx, padded, g["page_size"], rmap, table_rows=len(table))
+    assert got.tolist() == [r["expect"] for r in g["rows"]]
+    assert bad == g["out_of_range"]
+    got, bad = orc.page_transform(idx, table, g["page_size"], rmap)
     assert got.tolist() == [r["expect"] for r in g["rows"]]
     assert bad == g["out_of_range"]
 

@@ -56,6 +56,8 @@ MUTANTS = [
     ("page-table row ignored",
      "v = (long long)table[t * table_stride + page] * page_size + p % page_size;",
      "v = (long long)table[page] * page_size + p % page_size;"),
+    ("table-row bound ignored",
+     "const int row_ok = t >= 0 && t < table_rows;", "const int row_ok = t >= 0;"),
     ("offset within the page dropped",
      "v = (long long)table[t * table_stride + page] * page_size + p % page_size;",
      "v = (long long)table[t * table_stride + page] * page_size;"),
