@@ -8,7 +8,10 @@ fp8 e4m3 q/k, causal visible ranges.  Inputs are synthetic and seeded.
 
 Prints ONE JSON line (rank 0).  Timing: W untimed warm-up steps, then K steps
 timed on the device with CUDA events on the launching stream; the L2 is flushed
-(a 256 MiB write) between steps, outside the timed events.  --impl reference
+between steps, outside the timed events (a 256 MiB write, then a 256 MiB read
+that writes the dirty lines back), and a short device-side spin keeps the
+stream busy while the host issues the next call, so that the events time the
+device work.  --impl reference
 times the CPU oracle instead (rank 0, a bounded sample of the same workload).
 
 Multi-GPU (torchrun): every rank runs its own copy of the workload (the rows of
@@ -272,7 +275,8 @@ def config_block(inp, name):
                         f"topk={inp.topk} {dt} q/k, {inp.meta.get('ranges', 'given')} ranges",
             "rows": inp.rows, "keys": inp.keys, "heads": inp.H, "dim": inp.D, "topk": inp.topk,
             "pairs_per_step": inp.pairs(),
-            "l2": "flushed between timed steps (256 MiB write outside the events)"}
+            "l2": "flushed between timed steps (256 MiB write + 256 MiB read, outside "
+                  "the events: inputs cold, L2 clean)"}
 
 
 def torch_bf16():
@@ -328,7 +332,7 @@ def main():
     need = idx.idx_score_topk_workspace(inp.rows, inp.keys, 0, inp.H, inp.D, inp.topk,
                                         inp.q.dtype)
     ws = torch.empty(need, dtype=torch.uint8, device=dev)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     stats = idx.Stats(dev)
 
     def step(ev=None, o=None):
@@ -357,6 +361,7 @@ def main():
     launches0 = idx.idx_launch_count()
     for i in range(args.steps):
         flush.zero_()
+        hold_gpu()
         step(evs[i])
     torch.cuda.synchronize()
     launches = idx.idx_launch_count() - launches0
@@ -477,11 +482,37 @@ def last_rows(inp, n):
                                ke=inp.ke[-n:].contiguous(), topk=inp.topk, meta=inp.meta)
 
 
+class L2Flush:
+    """Before each timed call: write a 256 MiB buffer, so the 129 MB L2 keeps
+    no line of the previous call, then read another 256 MiB, so the write's
+    dirty lines go back to HBM now and not inside the next timed region."""
+
+    def __init__(self, dev):
+        import torch
+        self.w = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        self.r = torch.zeros(32 << 20, dtype=torch.int64, device=dev)
+        self.acc = torch.empty((), dtype=torch.int64, device=dev)
+
+    def zero_(self):
+        import torch
+        self.w.zero_()
+        torch.sum(self.r, dim=0, out=self.acc)
+
+
+def hold_gpu():
+    """Keep the stream busy (~50 us spin) while the host issues the next
+    call, so that the events around a short launch time the device work and
+    not the binding's host overhead (the end-to-end figures include that)."""
+    import torch
+    torch.cuda._sleep(100_000)
+
+
 def timed(fn, flush, reps):
     import torch
     ts = []
     for _ in range(reps):
         flush.zero_()
+        hold_gpu()
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record()
@@ -561,6 +592,7 @@ def page_transform(idx, dev, flush, pk, out, inp):
     for it in range(13):
         work.copy_(out)
         flush.zero_()
+        hold_gpu()
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record()
@@ -584,7 +616,7 @@ def route_sweep(idx, dev):
     routing gate: 4096 causal rows of e4m3 q/k, H 64 / 32, topk 2048 / 512."""
     import torch
     import synth
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     for H, topk in ((64, 2048), (32, 2048), (64, 512)):
         for keys in (4096, 6144, 8192, 12288, 16384, 24576, 32768, 65536):
             rows = 4096
@@ -649,6 +681,7 @@ def other_fused(idx, dev, flush, pk, args, name, inp=None, with_two_pass=False):
     evs = [idx.StageEvents(5) for _ in range(reps)]
     for e in evs:
         flush.zero_()
+        hold_gpu()
         call(e)
     torch.cuda.synchronize()
     ms = statistics.mean(e.elapsed(0, 4) for e in evs)

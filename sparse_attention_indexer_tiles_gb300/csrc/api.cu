@@ -498,11 +498,13 @@ idx_status idx_topk_from_scores(const float* scores, long long row_stride, const
         t.split_keys = reinterpret_cast<uint32_t*>(base);
         t.split_idx = t.split_keys + slots * kSplitCap;
         t.split_cnt = reinterpret_cast<int*>(t.split_idx + slots * kSplitCap);
+        t.split_lb = reinterpret_cast<uint32_t*>(t.split_cnt + slots);
+        t.split_ticket = reinterpret_cast<int*>(t.split_lb + slots);
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     record(opt, 0, s);
     const cudaError_t e = launch_topk_rows(t, s);
-    if (e == cudaSuccess) count_launches(g >= 2 ? 2 : 1);
+    if (e == cudaSuccess) count_launches(1);
     record(opt, 1, s);
     return cuda_status(e);
 }

@@ -5,12 +5,19 @@
 // positions (the -1 padding) are kept.  The indices are rewritten in place.
 //
 // The grid is flat over all rows x topk entries (a row count above 65535 needs
-// no second grid dimension) and strides over them; with topk % 4 == 0 and a
-// 16-byte aligned array every thread moves four entries with one 16-byte load
-// and store.  The page size is a template constant for the common 64 (shift
-// and mask) and a runtime divisor otherwise.  HBM-bound: 8 bytes per entry
-// plus the page-table reads, which stay in L2 (a table row is a few KB).
+// no second grid dimension): each 256-thread block owns a contiguous chunk of
+// 1024 units (a unit is four entries, one 16-byte load and store, when
+// topk % 4 == 0 and the array is 16-byte aligned; else one entry).  A thread
+// issues the loads of its four units before it uses any, then the page-table
+// reads of all of them, so a thread has several independent HBM and L2 reads
+// in flight instead of a chain per unit.  The block finds its first row with
+// one 64-bit division; a unit's row is that row plus a 32-bit quotient (at
+// most a few rows per chunk).  The page size is a template constant for the
+// common 64 (shift and mask) and a runtime divisor otherwise.  HBM-bound: 8
+// bytes per entry plus the page-table reads, which stay in L2 (a table row
+// is a few KB).
 #include <cstdint>
+#include <type_traits>
 
 #include "common.cuh"
 #include "page_table.cuh"
@@ -31,29 +38,50 @@ IDX_DEVI int map_pos(int p, const int* trow, long long pages, int page_size, boo
     return __ldg(trow + page) * P + (p - page * P);
 }
 
+constexpr int kUnitsPerThread = 4;
+constexpr int kChunk = 256 * kUnitsPerThread;  // units per block
+
 template <int PS, bool VEC>
 __global__ void __launch_bounds__(256) page_transform_kernel(PageArgs a) {
-    const long long stride = (long long)gridDim.x * blockDim.x;
-    const long long per_row = VEC ? a.topk / 4 : a.topk;
+    using Unit = typename std::conditional<VEC, int4, int>::type;
+    const int per_row = VEC ? a.topk / 4 : a.topk;  // units per row
     const long long n = (long long)a.rows * per_row;
+    const long long base = (long long)blockIdx.x * kChunk;
+    const long long r0 = base / per_row;
+    const int off0 = (int)(base - r0 * per_row);
+    Unit* const p = reinterpret_cast<Unit*>(a.idx);
+    Unit v[kUnitsPerThread];
+    long long t[kUnitsPerThread];
+#pragma unroll
+    for (int i = 0; i < kUnitsPerThread; ++i) {
+        const int j = (int)threadIdx.x + 256 * i;
+        const long long row = r0 + (off0 + j) / per_row;
+        t[i] = base + j < n ? (a.row_map ? (long long)a.row_map[row] : row) : -1;
+        if constexpr (VEC)
+            v[i] = make_int4(-1, -1, -1, -1);  // past the end: padding, left alone
+        else
+            v[i] = -1;
+        if (base + j < n) v[i] = p[base + j];
+    }
     bool bad = false;
-    for (long long q = (long long)blockIdx.x * blockDim.x + threadIdx.x; q < n; q += stride) {
-        const long long row = q / per_row;
-        const long long t = a.row_map ? (long long)a.row_map[row] : row;
-        const bool trow_ok = t >= 0 && t < a.table_rows;
-        const int* trow = a.table + (trow_ok ? t : 0) * a.table_stride;
+#pragma unroll
+    for (int i = 0; i < kUnitsPerThread; ++i) {
+        const bool trow_ok = t[i] >= 0 && t[i] < a.table_rows;
+        const int* trow = a.table + (trow_ok ? t[i] : 0) * a.table_stride;
         const long long pages = trow_ok ? a.table_stride : 0;
-        if (VEC) {
-            int4* p4 = reinterpret_cast<int4*>(a.idx) + q;
-            int4 v = *p4;
-            v.x = map_pos<PS>(v.x, trow, pages, a.page_size, bad);
-            v.y = map_pos<PS>(v.y, trow, pages, a.page_size, bad);
-            v.z = map_pos<PS>(v.z, trow, pages, a.page_size, bad);
-            v.w = map_pos<PS>(v.w, trow, pages, a.page_size, bad);
-            *p4 = v;
+        if constexpr (VEC) {
+            v[i].x = map_pos<PS>(v[i].x, trow, pages, a.page_size, bad);
+            v[i].y = map_pos<PS>(v[i].y, trow, pages, a.page_size, bad);
+            v[i].z = map_pos<PS>(v[i].z, trow, pages, a.page_size, bad);
+            v[i].w = map_pos<PS>(v[i].w, trow, pages, a.page_size, bad);
         } else {
-            a.idx[q] = map_pos<PS>(a.idx[q], trow, pages, a.page_size, bad);
+            v[i] = map_pos<PS>(v[i], trow, pages, a.page_size, bad);
         }
+    }
+#pragma unroll
+    for (int i = 0; i < kUnitsPerThread; ++i) {
+        const int j = (int)threadIdx.x + 256 * i;
+        if (base + j < n) p[base + j] = v[i];
     }
     if (bad) raise_status(a.d_status, IDX_DEV_RANGE);
 }
@@ -70,12 +98,12 @@ cudaError_t launch_ps(const PageArgs& a, int grid, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_page_transform(const PageArgs& a, int sm_count, cudaStream_t s) {
+    (void)sm_count;
     const long long units = (long long)a.rows * (a.vec ? a.topk / 4 : a.topk);
     if (units == 0) return cudaSuccess;
-    const long long want = (units + 255) / 256;
-    const long long cap = 8ll * sm_count;  // eight 256-thread blocks per SM, then stride
-    const int grid = (int)(want < cap ? want : cap);
-    return a.page_size == 64 ? launch_ps<64>(a, grid, s) : launch_ps<0>(a, grid, s);
+    const long long grid = (units + kChunk - 1) / kChunk;
+    if (grid > 0x7fffffffll) return cudaErrorInvalidValue;
+    return a.page_size == 64 ? launch_ps<64>(a, (int)grid, s) : launch_ps<0>(a, (int)grid, s);
 }
 
 }  // namespace idx

@@ -494,36 +494,6 @@ IDX_DEVI long long output_row(const TopkRowsArgs& a, int r, long long* col0) {
     return n;
 }
 
-// Lower bound L of the threshold of the k largest of a row: the lower edge of
-// the 12-bit bin that holds about the 2 k * P / n-th largest of the row's
-// first P = 4096 values, so that about 2 k keys of the row reach it.  The
-// blocks of a split row all take this same L.
-template <int THREADS>
-IDX_DEVI uint32_t estimate_lower_bound(const RowView& v, uint32_t k, uint32_t* hist,
-                                       uint32_t* scratch) {
-    const long long n = v.n;
-    const long long P = n < kPrefix ? n : kPrefix;
-    const float* row = reinterpret_cast<const float*>(v.base) + v.off;
-    // all loads of the prefix are issued before the first atomic
-    constexpr int PER = (kPrefix + THREADS - 1) / THREADS;
-    float x[PER];
-#pragma unroll
-    for (int i = 0; i < PER; ++i) {
-        const long long p = threadIdx.x + (long long)i * THREADS;
-        x[i] = p < P ? __ldg(row + p) : 0.f;
-    }
-    zero_shared<THREADS>(hist, kHistBins);
-    __syncthreads();
-#pragma unroll
-    for (int i = 0; i < PER; ++i)
-        if (threadIdx.x + (long long)i * THREADS < P) atomicAdd(&hist[fkey(x[i]) >> 20], 1u);
-    __syncthreads();
-    // ceil(2 k P / n) in integers: 2 k P < 2^25 and n < 2^31, so nothing wraps
-    uint32_t tg = (2u * k * (uint32_t)P + (uint32_t)n - 1u) / (uint32_t)n;
-    tg = tg < 1u ? 1u : tg > (uint32_t)P ? (uint32_t)P : tg;
-    return pick_digit<THREADS>(hist, kHistBins, tg, scratch).digit << 20;
-}
-
 template <int THREADS, int UNROLL>
 __global__ void __launch_bounds__(THREADS)
 topk_rows_kernel(TopkRowsArgs a) {
@@ -692,163 +662,317 @@ __global__ void __launch_bounds__(kThrCtaThreads) sample_threshold_cta_kernel(To
 //
 // Page "[sglang] ROCm DSA Indexer Top-K 최적화", row_split / launch: at low
 // batch a long row is split over g blocks.  Here block (c, r) streams the c-th
-// contiguous slice of row r once, appends the values at or above the row's
-// lower bound L (the same estimate in every block of the row) to its warps'
-// runs and copies them, in index order, to the workspace; one block per row
-// then selects from the concatenation (already in index order), or takes the
-// exact multi-pass path over the row when a slice overflowed or L was too high.
-
+// contiguous slice of row r once, appends the values at or above a lower
+// bound L_c to its warps' runs and copies them, in index order, to the
+// workspace together with L_c.  L_c comes from the values the block loads
+// first (the lower edge of the 12-bit bin of about the 2 k P / n-th largest of
+// its P sampled values: about 2 k n_c / n of its n_c values reach it), so no
+// block waits for another read.  The block of the row that finishes last (it
+// draws the last ticket of a per-row counter that the launch starts at 0)
+// then selects from the concatenation, already in index order.  The result is
+// exact when the k-th largest candidate T' is >= every L_c: a value a block
+// left out is below its L_c <= T', hence below the row's k-th largest, and
+// every value >= T' is a candidate.  Otherwise (or when a slice overflowed or
+// fewer than k values reached their bounds) the block takes the exact
+// multi-pass path over the row.  Selection thus starts as soon as a row's
+// slices are in, in the same launch.
 static_assert(kSplitCap == 16 * kRunCap, "a split block hands over its 16 warp runs");
 
+constexpr int kMergeCap = 16384;  // candidates of a split row selected in shared memory
+constexpr int kMaxSplit = 64;
+
+template <int THREADS>
+struct SplitSmem {
+    // collection: the StreamSmem layout; selection, over the same memory:
+    // hist | scratch (64) | slice offsets (kMaxSplit + 4) | keys | idxs
+    static constexpr size_t COLLECT = StreamSmem<THREADS>::BYTES;
+    static constexpr int OFFS = kHistBins + 64;
+    static constexpr int KEYS = OFFS + kMaxSplit + 4;
+    static constexpr size_t MERGE = (KEYS + 2 * (size_t)kMergeCap) * sizeof(uint32_t);
+    static constexpr size_t BYTES = COLLECT > MERGE ? COLLECT : MERGE;
+};
+
+// The UNROLL float4 slots of one step of a warp's part, from slot `base`.
+template <int UNROLL>
+IDX_DEVI void load_step(const RowView& v, int base, int s1, int lane, float4 (&f)[UNROLL]) {
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) {
+        const int sl = base + u * 32 + lane;
+        f[u] = sl < s1 ? ldg4(v.base + sl) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+}
+
+// Ordered compaction of cnt keys held in index order in shared memory: key >
+// T, plus the first `need` keys equal to T.  Warp w takes the w-th contiguous
+// chunk; one count pass, one synchronisation for the chunk offsets, then each
+// warp writes its chunk with ballot ranks (32 keys per step).
+template <int THREADS>
+IDX_DEVI void ordered_output_chunks(const uint32_t* keys, const uint32_t* idxs, uint32_t cnt,
+                                    Threshold th, uint32_t k, int* out, uint32_t* wsum) {
+    constexpr int W = THREADS / 32;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const uint32_t per = (cnt + W * 32 - 1) / (W * 32) * 32;
+    const uint32_t c0 = min(cnt, w * per), c1 = min(cnt, c0 + per);
+    uint32_t na = 0, nt = 0;
+    for (uint32_t i = c0 + lane; i < c1; i += 32) {
+        na += keys[i] > th.key;
+        nt += keys[i] == th.key;
+    }
+    na = __reduce_add_sync(0xffffffffu, na);
+    nt = __reduce_add_sync(0xffffffffu, nt);
+    if (lane == 0) {
+        wsum[w] = na;
+        wsum[W + w] = nt;
+    }
+    __syncthreads();
+    uint32_t a_run = 0, t_run = 0;
+    for (int j = 0; j < w; ++j) {
+        a_run += wsum[j];
+        t_run += wsum[W + j];
+    }
+    const uint32_t lt = (1u << lane) - 1u;
+    for (uint32_t base = c0; base < c1; base += 32) {
+        const uint32_t i = base + lane;
+        const uint32_t key = i < c1 ? keys[i] : 0u;
+        const bool ab = i < c1 && key > th.key;
+        const bool tb = i < c1 && key == th.key;
+        const uint32_t A = __ballot_sync(0xffffffffu, ab), T = __ballot_sync(0xffffffffu, tb);
+        const uint32_t a_b = a_run + __popc(A & lt), t_b = t_run + __popc(T & lt);
+        if (ab) {
+            const uint32_t pos = a_b + min(t_b, th.need);
+            if (pos < k) out[pos] = static_cast<int>(idxs[i]);
+        } else if (tb && t_b < th.need && a_b + t_b < k) {
+            out[a_b + t_b] = static_cast<int>(idxs[i]);
+        }
+        a_run += __popc(A);
+        t_run += __popc(T);
+    }
+}
+
 template <int THREADS, int UNROLL>
-__global__ void __launch_bounds__(THREADS)
-topk_split_collect_kernel(TopkRowsArgs a) {
+__global__ void __launch_bounds__(THREADS, 1)
+topk_split_kernel(TopkRowsArgs a) {
     using SM = StreamSmem<THREADS>;
+    using SS = SplitSmem<THREADS>;
     constexpr int W = SM::W;
     extern __shared__ __align__(16) uint32_t smem[];
+    __shared__ int s_last;
     uint32_t* hist = smem;
     uint32_t* scratch = hist + kHistBins;
     uint32_t* rcnt = scratch + 64;
-    uint32_t* wsum = rcnt + W;
-    uint32_t* rkey = wsum + 2 * W;
+    uint32_t* rkey = rcnt + 3 * W;
     uint32_t* ridx = rkey + SM::RUN_WORDS;
-    (void)wsum;
 
     const int c = blockIdx.x, r = blockIdx.y, g = gridDim.x;
-    long long col0;
-    const long long n = output_row(a, r, &col0);
-    if (n <= a.topk) return;  // the merge block writes such rows
-    const RowView v = make_view(a.scores + (long long)r * a.row_stride + col0, n);
-    const uint32_t L = estimate_lower_bound<THREADS>(v, (uint32_t)a.topk, hist, scratch);
-    // the slice as a view whose element indices stay row-relative
-    const long long per = (v.nvec + g - 1) / g;
-    const long long s0 = (long long)c * per;
-    const long long s1 = s0 + per < v.nvec ? s0 + per : v.nvec;
-    RowView sv;
-    sv.base = v.base + s0;
-    sv.off = v.off - (int)(4 * s0);
-    sv.n = v.n;
-    sv.nvec = s1 > s0 ? s1 - s0 : 0;
-    stream_collect<THREADS, UNROLL, false>(sv, L, rkey, ridx, rcnt, nullptr);
-    __syncthreads();
-    // hand the runs over in warp (= index) order
-    const long long slot = (long long)r * g + c;
-    uint32_t* gk = a.split_keys + slot * kSplitCap;
-    uint32_t* gi = a.split_idx + slot * kSplitCap;
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    uint32_t before = 0, total = 0;
-    bool over = false;
-    for (int j = 0; j < W; ++j) {
-        const uint32_t cj = rcnt[j];
-        over = over || cj > (uint32_t)kRunCap;
-        if (j < w) before += cj;
-        total += cj;
-    }
-    if (!over) {
-        for (uint32_t i = lane; i < rcnt[w]; i += 32) {
-            gk[before + i] = rkey[w * kRunCap + i];
-            gi[before + i] = ridx[w * kRunCap + i];
-        }
-    }
-    if (threadIdx.x == 0) a.split_cnt[slot] = over ? -1 : (int)total;
-}
-
-// Ordered compaction of cnt keys held in index order in shared memory.
-template <int THREADS>
-IDX_DEVI void ordered_output_smem(const uint32_t* keys, const uint32_t* idxs, uint32_t cnt,
-                                  Threshold th, uint32_t k, int* out, uint32_t* scratch) {
-    uint32_t a_run = 0, e_run = 0;
-    for (uint32_t base = 0; base < cnt; base += THREADS * 4) {
-        uint32_t ab = 0, tb = 0;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const uint32_t e = base + threadIdx.x * 4 + c;
-            if (e < cnt) {
-                ab |= (keys[e] > th.key ? 1u : 0u) << c;
-                tb |= (keys[e] == th.key ? 1u : 0u) << c;
-            }
-        }
-        const uint32_t mine = (__popc(ab) << 16) | __popc(tb);
-        uint32_t tot;
-        const uint32_t incl = block_incl_scan<THREADS>(mine, scratch, &tot);
-        const uint32_t excl = incl - mine;
-        uint32_t a_b = a_run + (excl >> 16), e_b = e_run + (excl & 0xFFFFu);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const uint32_t e = base + threadIdx.x * 4 + c;
-            if ((ab >> c) & 1u) {
-                const uint32_t pos = a_b + min(e_b, th.need);
-                if (pos < k) out[pos] = (int)idxs[e];
-                ++a_b;
-            } else if ((tb >> c) & 1u) {
-                if (e_b < th.need && a_b + e_b < k) out[a_b + e_b] = (int)idxs[e];
-                ++e_b;
-            }
-        }
-        a_run += tot >> 16;
-        e_run += tot & 0xFFFFu;
-    }
-}
-
-constexpr int kMergeCap = 16384;  // candidates of a split row selected in shared memory
-constexpr size_t kMergeSmem = (kHistBins + 64 + 2 * (size_t)kMergeCap) * sizeof(uint32_t);
-
-template <int THREADS>
-__global__ void __launch_bounds__(THREADS)
-topk_split_merge_kernel(TopkRowsArgs a, int g) {
-    extern __shared__ __align__(16) uint32_t smem[];
-    uint32_t* hist = smem;
-    uint32_t* scratch = hist + kHistBins;
-    uint32_t* keys = scratch + 64;
-    uint32_t* idxs = keys + kMergeCap;
-    const int r = blockIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     long long col0;
     long long n = output_row(a, r, &col0);
-    int* out = a.out + (long long)r * a.topk;
-    if (n < 0) {
-        if (threadIdx.x == 0) raise_status(a.d_status, IDX_DEV_RANGE);
-        n = 0;
-    }
     if (n <= a.topk) {
-        for (int i = threadIdx.x; i < a.topk; i += THREADS) out[i] = i < n ? i : -1;
+        // the same decision in every block of the row: the first writes it
+        if (c != 0) return;
+        if (n < 0) {
+            if (tid == 0) raise_status(a.d_status, IDX_DEV_RANGE);
+            n = 0;
+        }
+        int* out = a.out + (long long)r * a.topk;
+        for (int i = tid; i < a.topk; i += THREADS) out[i] = i < n ? i : -1;
         return;
     }
     const uint32_t k = (uint32_t)a.topk;
-    if (threadIdx.x == 0) {
-        uint32_t total = 0, bad = 0;
-        for (int c = 0; c < g; ++c) {
-            const int cc = a.split_cnt[(long long)r * g + c];
-            bad |= cc < 0;
-            total += cc < 0 ? 0u : (uint32_t)cc;
+    const RowView v = make_view(a.scores + (long long)r * a.row_stride + col0, n);
+    // the slice as a view whose element indices stay row-relative
+    const long long per = (v.nvec + g - 1) / g;
+    const long long c0 = (long long)c * per;
+    const long long c1 = c0 + per < v.nvec ? c0 + per : v.nvec;
+    RowView sv;
+    sv.base = v.base + c0;
+    sv.off = v.off - (int)(4 * c0);
+    sv.n = v.n;
+    sv.nvec = c1 > c0 ? c1 - c0 : 0;
+
+    // ---- collection: the loads of the first two steps are in flight while L
+    // is estimated from the first two slots of every lane; after that the
+    // loads of step i + 2 go out before step i is filtered
+    int s0, s1;
+    warp_slice<THREADS>(sv, w, &s0, &s1);
+    constexpr int STEP = 32 * UNROLL, SAMPLE = 2;
+    static_assert(UNROLL >= SAMPLE, "the sample comes from the first step");
+    float4 f[UNROLL], nf[UNROLL];
+    load_step<UNROLL>(sv, s0, s1, lane, f);
+    load_step<UNROLL>(sv, s0 + STEP, s1, lane, nf);
+    uint32_t L;
+    {
+        const int nn = (int)sv.n, off = sv.off;
+        zero_shared<THREADS>(hist, kHistBins);
+        if (tid == 0) scratch[44] = 0u;
+        __syncthreads();
+        uint32_t ns = 0;
+#pragma unroll
+        for (int u = 0; u < SAMPLE; ++u) {
+            const int sl = s0 + u * 32 + lane;
+            const float e[4] = {f[u].x, f[u].y, f[u].z, f[u].w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int p = 4 * sl + q - off;
+                if (sl < s1 && p >= 0 && p < nn) {
+                    atomicAdd(&hist[fkey(e[q]) >> 20], 1u);
+                    ++ns;
+                }
+            }
         }
-        scratch[48] = total;
-        scratch[49] = bad || total < k || total > (uint32_t)kMergeCap;
-        if (a.d_stats) atomicAdd(&a.d_stats->split_rows, 1);
+        ns = __reduce_add_sync(0xffffffffu, ns);
+        if (lane == 0 && ns) atomicAdd(&scratch[44], ns);
+        __syncthreads();
+        const uint32_t P = scratch[44];
+        // ceil(2 k P / n) in integers: 2 k P < 2^25 and n < 2^31, so nothing wraps
+        uint32_t tg = (2u * k * P + (uint32_t)n - 1u) / (uint32_t)n;
+        tg = tg < 1u ? 1u : tg > P ? P : tg;
+        const uint32_t d = pick_digit<THREADS>(hist, kHistBins, tg, scratch).digit;
+        L = P ? d << 20 : 0u;  // an empty slice takes nothing and bounds nothing
+    }
+    {
+        const int nvec = (int)sv.nvec, nn = (int)sv.n, off = sv.off;
+        const float Lf = key_floor_float(L);
+        const uint32_t lt = (1u << lane) - 1u;
+        uint32_t* mk = rkey + w * kRunCap;
+        uint32_t* mi = ridx + w * kRunCap;
+        uint32_t cnt = 0;
+        for (int base = s0; base < s1; base += STEP) {
+            const int nb = base + STEP;
+            const bool interior = base >= 1 && nb <= s1 && nb < nvec;
+#pragma unroll
+            for (int u = 0; u < UNROLL; ++u)
+                filter_step<false>(f[u], base + u * 32 + lane, interior, s1, nn, off, L, Lf, lt,
+                                   cnt, mk, mi, nullptr);
+#pragma unroll
+            for (int u = 0; u < UNROLL; ++u) f[u] = nf[u];
+            if (nb + STEP < s1) load_step<UNROLL>(sv, nb + STEP, s1, lane, nf);
+        }
+        if (lane == 0) rcnt[w] = cnt;
     }
     __syncthreads();
-    const uint32_t total = scratch[48];
-    const RowView v = make_view(a.scores + (long long)r * a.row_stride + col0, n);
-    if (scratch[49]) {
-        // a slice overflowed or L was too high: exact multi-pass path
+    // hand the runs over in warp (= index) order
+    const long long slot = (long long)r * g + c;
+    {
+        uint32_t* gk = a.split_keys + slot * kSplitCap;
+        uint32_t* gi = a.split_idx + slot * kSplitCap;
+        uint32_t before = 0, total = 0;
+        bool over = false;
+        for (int j = 0; j < W; ++j) {
+            const uint32_t cj = rcnt[j];
+            over = over || cj > (uint32_t)kRunCap;
+            if (j < w) before += cj;
+            total += cj;
+        }
+        if (!over) {
+            for (uint32_t i = lane; i < rcnt[w]; i += 32) {
+                gk[before + i] = rkey[w * kRunCap + i];
+                gi[before + i] = ridx[w * kRunCap + i];
+            }
+        }
+        if (tid == 0) {
+            a.split_cnt[slot] = over ? -1 : (int)total;
+            a.split_lb[slot] = L;
+        }
+    }
+    // publish, then draw a ticket: the row's last block goes on
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_last = atomicAdd(a.split_ticket + r, 1) == g - 1;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+
+    // ---- selection by the row's last block (reads bypass L1: other SMs wrote)
+    uint32_t* soff = smem + SS::OFFS;  // [g + 1] slice offsets, [kMaxSplit + 2] total, +3 bad
+    uint32_t* keys = smem + SS::KEYS;
+    uint32_t* idxs = keys + kMergeCap;
+    int* out = a.out + (long long)r * a.topk;
+    if (w == 0) {
+        const int j0 = lane, j1 = lane + 32;
+        const int n0 = j0 < g ? __ldcg(a.split_cnt + (long long)r * g + j0) : 0;
+        const int n1 = j1 < g ? __ldcg(a.split_cnt + (long long)r * g + j1) : 0;
+        const uint32_t l0 = j0 < g ? __ldcg(a.split_lb + (long long)r * g + j0) : 0u;
+        const uint32_t l1 = j1 < g ? __ldcg(a.split_lb + (long long)r * g + j1) : 0u;
+        const uint32_t lmax = __reduce_max_sync(0xffffffffu, l0 > l1 ? l0 : l1);
+        const bool bad = __any_sync(0xffffffffu, n0 < 0 || n1 < 0);
+        uint32_t i0 = n0 > 0 ? (uint32_t)n0 : 0u, i1 = n1 > 0 ? (uint32_t)n1 : 0u;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t u0 = __shfl_up_sync(0xffffffffu, i0, o);
+            const uint32_t u1 = __shfl_up_sync(0xffffffffu, i1, o);
+            if (lane >= o) {
+                i0 += u0;
+                i1 += u1;
+            }
+        }
+        const uint32_t t0 = __shfl_sync(0xffffffffu, i0, 31);
+        const uint32_t total = t0 + __shfl_sync(0xffffffffu, i1, 31);
+        if (lane == 0) soff[0] = 0u;
+        if (j0 < g) soff[j0 + 1] = i0;
+        if (j1 < g) soff[j1 + 1] = t0 + i1;
+        if (lane == 0) {
+            soff[kMaxSplit + 1] = lmax;
+            soff[kMaxSplit + 2] = total;
+            soff[kMaxSplit + 3] = bad || total < k || total > (uint32_t)kMergeCap;
+            if (a.d_stats) atomicAdd(&a.d_stats->split_rows, 1);
+        }
+    }
+    __syncthreads();
+    const uint32_t total = soff[kMaxSplit + 2];
+    const uint32_t lmax = soff[kMaxSplit + 1];
+    auto exact_path = [&]() {
         int rescans = 0;
         const Threshold th = find_threshold<THREADS, 4>(v, k, hist, keys, idxs, scratch, &rescans);
-        if (threadIdx.x == 0 && a.d_stats) atomicAdd(&a.d_stats->tie_rescan_rows, 1);
+        if (tid == 0 && a.d_stats) atomicAdd(&a.d_stats->tie_rescan_rows, 1);
         ordered_output<THREADS>(v, th, k, out, scratch);
+    };
+    if (soff[kMaxSplit + 3]) {
+        // a slice overflowed or too few values reached their bounds
+        exact_path();
         return;
     }
-    uint32_t off = 0;
-    for (int c = 0; c < g; ++c) {
-        const long long slot = (long long)r * g + c;
-        const uint32_t cc = (uint32_t)a.split_cnt[slot];
-        for (uint32_t i = threadIdx.x; i < cc; i += THREADS) {
-            keys[off + i] = a.split_keys[slot * kSplitCap + i];
-            idxs[off + i] = a.split_idx[slot * kSplitCap + i];
+    // one warp per slice: 16-byte loads (a slot's arrays start 16-byte
+    // aligned; words past the count are loaded but not kept), four of each
+    // array per lane in flight
+    for (int cs = w; cs < g; cs += W) {
+        const uint32_t o = soff[cs], cnt = soff[cs + 1] - o;
+        const long long at = ((long long)r * g + cs) * kSplitCap;
+        const uint4* sk = reinterpret_cast<const uint4*>(a.split_keys + at);
+        const uint4* si = reinterpret_cast<const uint4*>(a.split_idx + at);
+        for (uint32_t b = 0; b < cnt; b += 4 * 128) {
+            uint4 kk[4], ii[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t e = b + j * 128 + 4 * lane;
+                if (e < cnt) {
+                    kk[j] = __ldcg(sk + e / 4);
+                    ii[j] = __ldcg(si + e / 4);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t e = b + j * 128 + 4 * lane;
+                const uint32_t kv[4] = {kk[j].x, kk[j].y, kk[j].z, kk[j].w};
+                const uint32_t iv[4] = {ii[j].x, ii[j].y, ii[j].z, ii[j].w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    if (e + q < cnt) {
+                        keys[o + e + q] = kv[q];
+                        idxs[o + e + q] = iv[q];
+                    }
+            }
         }
-        off += cc;
     }
     __syncthreads();
     const Threshold th = refine_in_smem<THREADS>(keys, total, 0, 0u, k, hist, scratch);
-    ordered_output_smem<THREADS>(keys, idxs, total, th, k, out, scratch);
+    if (th.key < lmax) {
+        // a slice's bound lies above the k-th candidate: it may have left
+        // out values of the top k
+        exact_path();
+        return;
+    }
+    ordered_output_chunks<THREADS>(keys, idxs, total, th, k, out, scratch);
 }
 
 // ---------------------------------------------------------------- slab
@@ -1326,19 +1450,16 @@ cudaError_t launch_topk_rows(const TopkRowsArgs& a, cudaStream_t s) {
         return cudaGetLastError();
     }
     if (a.split > 1) {
-        auto coll = topk_split_collect_kernel<T, U>;
-        auto merge = topk_split_merge_kernel<T>;
-        static cudaError_t attr = [&] {
-            cudaError_t e = cudaFuncSetAttribute(coll, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 (int)SMEM);
-            if (e == cudaSuccess)
-                e = cudaFuncSetAttribute(merge, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kMergeSmem);
-            return e;
-        }();
+        if (a.split > kMaxSplit) return cudaErrorInvalidValue;
+        auto kern = topk_split_kernel<T, U>;
+        constexpr size_t SPLIT_SMEM = SplitSmem<T>::BYTES;
+        static cudaError_t attr = cudaFuncSetAttribute(
+            kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SPLIT_SMEM);
         if (attr != cudaSuccess) return attr;
-        coll<<<dim3((unsigned)a.split, (unsigned)a.rows), T, SMEM, s>>>(a);
-        merge<<<a.rows, T, kMergeSmem, s>>>(a, a.split);
+        // the per-row tickets start at 0
+        const cudaError_t e = cudaMemsetAsync(a.split_ticket, 0, sizeof(int) * (size_t)a.rows, s);
+        if (e != cudaSuccess) return e;
+        kern<<<dim3((unsigned)a.split, (unsigned)a.rows), T, SPLIT_SMEM, s>>>(a);
         return cudaGetLastError();
     }
     auto kern = topk_rows_kernel<T, U>;
@@ -1352,7 +1473,8 @@ cudaError_t launch_topk_rows(const TopkRowsArgs& a, cudaStream_t s) {
 size_t split_workspace_bytes(int rows, int g) {
     if (g < 2) return 0;
     const size_t slots = (size_t)rows * g;
-    return slots * (size_t)kSplitCap * 2 * sizeof(uint32_t) + slots * sizeof(int) + 256;
+    return slots * (size_t)kSplitCap * 2 * sizeof(uint32_t) + 2 * slots * sizeof(int) +
+           (size_t)rows * sizeof(int) + 256;
 }
 
 size_t cand_smem_bytes(int cap_q, int nruns, int topk) {

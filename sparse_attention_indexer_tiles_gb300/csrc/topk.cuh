@@ -43,6 +43,8 @@ struct TopkRowsArgs {
     uint32_t* split_keys;  // [rows * g, kSplitCap]
     uint32_t* split_idx;   // [rows * g, kSplitCap]
     int* split_cnt;        // [rows * g] candidates handed over, -1 = a run overflowed
+    uint32_t* split_lb;    // [rows * g] the lower bound (order key) each block used
+    int* split_ticket;     // [rows] blocks of the row done so far (zeroed by the launch)
     int* d_status;
     idx_stats* d_stats;
 };

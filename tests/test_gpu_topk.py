@@ -148,6 +148,58 @@ def test_forced_row_split(idx, g):
     assert stats.read()["split_rows"] > 0
 
 
+def test_row_split_with_empty_slices_and_a_reused_workspace(idx):
+    """64 blocks per row (the most a split takes), rows from just above topk
+    (most blocks get an empty slice) to 70000 keys, ragged starts; two calls
+    on the same workspace (the per-row tickets start at 0 every launch)."""
+    rows, n, topk = 10, 70000, 100
+    si = synth.score_inputs(rows, n, topk, seed=41, short_frac=0.0)
+    ks = torch.tensor([0, 5, 0, 3, 0, 17, 1, 0, 2, 9], dtype=torch.int32)
+    ke = ks + torch.tensor([101, 150, 257, 1000, 4099, 65536, 69999 - 1, 300, 8191, 50000],
+                           dtype=torch.int32)
+    ke = torch.minimum(ke, torch.full_like(ke, n))
+    opts = {"row_split": 64}
+    S = si.scores.to(DEV)
+    need = idx.idx_topk_workspace(rows, n, topk, opts)
+    ws = torch.full((need,), 0xAB, dtype=torch.uint8, device=DEV)  # stale bytes
+    ref = oracle.topk_from_scores(si.scores, ks, ke, topk)
+    for _ in range(2):
+        stats = idx.Stats(torch.device(DEV))
+        got = idx.idx_topk_from_scores(S, ks.to(DEV), ke.to(DEV), topk, ws=ws, options=opts,
+                                       stats=stats)
+        torch.cuda.synchronize()
+        assert np.array_equal(got.cpu().numpy(), ref)
+        assert stats.read()["split_rows"] == rows and stats.read()["status"] == 0
+
+
+def test_row_split_bound_above_the_kth_falls_back(idx):
+    """A block takes its lower bound from the first two float4 slots of every
+    lane of each warp's part of its slice (512 threads, 16 warps).  Row 0's
+    first slice holds 10.0 exactly there (96 values, enough to set its bound
+    above 5.0) and 5.0 at 500 other places: values of the top k that this
+    block leaves out.  The selected threshold then lies below the block's
+    bound, and the row must be re-selected exactly."""
+    n, topk, g = 90000, 1000, 6
+    gen = torch.Generator().manual_seed(43)
+    S = torch.rand(2, n, generator=gen)
+    nvec = n // 4
+    per = -(-nvec // g)                  # float4 slots per block
+    seg = -(-per // 16)                  # per warp of block 0
+    S[0, :4 * per] = 0.0
+    for w in range(16):
+        S[0, 4 * seg * w: 4 * seg * w + 6] = 10.0
+    outside = [p for p in range(4 * per) if p % (4 * seg) >= 256]  # not sampled
+    S[0, outside[::20][:500]] = 5.0
+    ks = torch.zeros(2, dtype=torch.int32)
+    ke = torch.full((2,), n, dtype=torch.int32)
+    stats = idx.Stats(torch.device(DEV))
+    got = gpu_topk(idx, S, ks, ke, topk, options={"row_split": g}, stats=stats)
+    ref = oracle.topk_from_scores(S, ks, ke, topk)
+    assert np.array_equal(got, ref)
+    st = stats.read()
+    assert st["split_rows"] == 2 and st["tie_rescan_rows"] >= 1 and st["status"] == 0
+
+
 def test_row_split_ties_fall_back(idx):
     """All-equal and two-valued rows overflow the split candidate runs; the
     merge block re-selects them exactly."""
