@@ -233,6 +233,7 @@ ScoreLaunch make_score_launch(const void* q, const void* k, const float* k_scale
     L.a.topk = topk;
     L.a.d_status = opt ? opt->d_status : nullptr;
     L.a.d_stats = opt ? opt->d_stats : nullptr;
+    L.a.nwhole = (rows + score_rows_per_block(H) - 1) / score_rows_per_block(H);
     L.a.ksplit = 1;
     L.a.nruns = kRuns;
     // about 2 s at the GB300's clock; the test knob shortens it and withholds
@@ -243,29 +244,37 @@ ScoreLaunch make_score_launch(const void* q, const void* k, const float* k_scale
     return L;
 }
 
-// Key splits of a scoring launch: the CTAs of one wave are SM-count many, so
-// a grid of nblk row blocks leaves the last wave partly idle, and a call with
-// few rows (a decode-like shape: few query rows over long rows) leaves most of
-// the GPU idle.  When the unsplit grid fills its last wave to less than 90 %,
-// every block's key tiles are split into k contiguous parts (grid.y = k), the
-// k that fills the last wave best (the smaller k within 1 %), every part
-// keeping >= 32 tiles: k <= 6 for grids of at least half a wave, up to one
-// wave's worth (SMs / nblk, at most 128) for fewer blocks.  Each split of the
-// emit pass adds kRuns runs per row to the slab.
-int score_ksplit(int rows, int H, long long max_len) {
+// Key splits of a scoring launch.  One wave is SM-count many CTAs (one per
+// SM), so a grid of nblk row blocks runs floor(nblk / SMs) full waves and a
+// last one with only tail = nblk % SMs blocks, leaving the other SMs idle; a
+// call with fewer blocks than SMs (few query rows over long rows, a decode
+// shape) leaves most of the GPU idle.  So the full waves keep whole blocks,
+// and each of the tail blocks is cut into k contiguous parts of its key
+// tiles, one CTA each: the tail then takes ceil(tail k / SMs) rounds of 1 / k
+// of a block's time, plus a per-part overhead o (the CTA prologue and the
+// pipeline's fill and drain, about 8 tiles' worth: o = 8 / tiles of a block).
+// The k in [1, 128] with the smallest ceil(tail k / SMs) (1 / k + o) is taken
+// (a larger k only when it is 1 % cheaper), every part keeping >= 32 tiles.
+// Each key split adds kRuns runs per row to the emit pass's slab.
+SplitPlan score_split(int rows, int H, long long max_len) {
     const int nblk = (rows + score_rows_per_block(H) - 1) / score_rows_per_block(H);
     const long long tiles = (max_len + 127) / 128;
-    const double sm = (double)sm_count();
-    auto eff = [&](int k) {
-        const double waves = nblk * (double)k / sm;
-        return waves / std::ceil(waves);
-    };
-    if (eff(1) >= 0.9) return 1;
-    const int kmax = 2 * nblk <= sm ? std::min(128, (int)(sm / nblk)) : 6;
-    int best = 1;
-    for (int k = 2; k <= kmax && tiles / k >= 32; ++k)
-        if (eff(k) > eff(best) + 0.01) best = k;
-    return best;
+    const int sm = std::max(sm_count(), 1);
+    const int tail = nblk % sm;
+    SplitPlan p{nblk, 1};
+    if (tail == 0 || tiles < 64) return p;
+    const double o = 8.0 / (double)tiles;
+    double best = 1.0 + o;
+    for (int k = 2; k <= 128 && tiles / k >= 32; ++k) {
+        const double rounds = std::ceil((double)tail * k / sm);
+        const double cost = rounds * (1.0 / k + o);
+        if (cost < best * 0.99) {
+            best = cost;
+            p.k = k;
+        }
+    }
+    if (p.k > 1) p.nwhole = nblk - tail;
+    return p;
 }
 
 void record(const idx_options* opt, int i, cudaStream_t s) {
@@ -319,7 +328,7 @@ size_t idx_score_topk_workspace(int rows, long long keys, long long max_len, int
     if (rows <= 0 || topk < 1 || topk > kMaxTopk) return 0;
     if (max_len <= 0 || max_len > keys) max_len = keys;
     const FusedParams p = fused_params(topk, opt);
-    const int nruns = kRuns * score_ksplit(rows, H, max_len);
+    const int nruns = kRuns * score_split(rows, H, max_len).k;
     return fused_layout(rows, max_len, p.cap, p.cap_q, p.S, nruns, H).total;
 }
 
@@ -336,8 +345,8 @@ idx_status idx_score_topk(const void* q, const void* k, const float* k_scale, co
     if (max_len <= 0 || max_len > keys) max_len = keys;
     const FusedParams p = fused_params(topk, opt);
     if (p.cap > kMaxCap || p.S < 1) return IDX_EUNSUPPORTED;
-    const int ksplit = score_ksplit(rows, H, max_len);
-    const int nruns = kRuns * ksplit;
+    const SplitPlan split = score_split(rows, H, max_len);
+    const int nruns = kRuns * split.k;
     const FusedLayout lay = fused_layout(rows, max_len, p.cap, p.cap_q, p.S, nruns, H);
     if (!ws || ws_bytes < lay.total) return IDX_EWORKSPACE;
     if (!aligned(ws, 256)) return IDX_EALIGN;
@@ -379,9 +388,10 @@ idx_status idx_score_topk(const void* q, const void* k, const float* k_scale, co
         // 1. score the odd-stride sample of every long row (key splits over the
         //    sample index range, as for the emit pass)
         L.a.mode = SM_SAMPLE;
-        L.a.ksplit = score_ksplit(rows, H, max_len / p.S + 1);
+        const SplitPlan sp = score_split(rows, H, max_len / p.S + 1);
+        L.a.nwhole = sp.nwhole;
+        L.a.ksplit = sp.k;
         if ((e = launch_score(L, s)) != cudaSuccess) return cuda_status(e);
-        L.a.ksplit = 1;
         // 2. T_r = exact t-th largest sample score of each row
         TopkRowsArgs t;
         std::memset(&t, 0, sizeof(t));
@@ -410,9 +420,9 @@ idx_status idx_score_topk(const void* q, const void* k, const float* k_scale, co
     // 3. one scoring pass emits every key at or above T_r into the slab
     //    (key splits write runs of their own)
     L.a.mode = SM_EMIT;
-    L.a.ksplit = ksplit;
+    L.a.nwhole = split.nwhole;
+    L.a.ksplit = split.k;
     if ((e = launch_score(L, s)) != cudaSuccess) return cuda_status(e);
-    L.a.ksplit = 1;
     record(opt, 2, s);
     // 4. exact top-k of every slab; rows whose count missed [topk, cap] are flagged
     CandArgs c;
@@ -521,7 +531,9 @@ idx_status idx_score_materialise(const void* q, const void* k, const float* k_sc
     L.a.mode = SM_MATERIALISE;
     L.a.out = scores;
     L.a.out_stride = row_stride;
-    L.a.ksplit = score_ksplit(rows, H, std::min<long long>(keys, row_stride));
+    const SplitPlan sp = score_split(rows, H, std::min<long long>(keys, row_stride));
+    L.a.nwhole = sp.nwhole;
+    L.a.ksplit = sp.k;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     record(opt, 0, s);
     const cudaError_t e = launch_score(L, s);

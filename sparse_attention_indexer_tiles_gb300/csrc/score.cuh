@@ -48,8 +48,10 @@ struct ScoreArgs {
     int cap_q;            // capacity of one warp run: slab row = nruns runs of cap_q
     int* run_cnt;         // [rows, nruns] candidates appended per run (may exceed cap_q)
     int nruns;            // runs per row: kRuns per key split of the main emit pass
-    int ksplit;           // key splits of this launch (grid.y): CTA (b, c) scores the
-                          // c-th contiguous part of row block b's key tiles
+    int nwhole;           // CTAs 0 .. nwhole - 1 score row blocks 0 .. nwhole - 1 whole;
+    int ksplit;           // every later row block is split into ksplit contiguous parts
+                          // of its key tiles, one CTA each (CTA nwhole + ksplit * j + c
+                          // scores part c of block nwhole + j)
     uint32_t* fb_hist;
     int* fb_cnt;          // [8] rows waiting per rescan level, [6] ready to emit,
                           // [7] row blocks listed in fb_blocks
@@ -76,6 +78,13 @@ struct ScoreLaunch {
 
 // Rows handled by one CTA (the MMA's N = rows x H = 256).
 inline int score_rows_per_block(int H) { return 256 / H; }
+
+// How a scoring launch cuts row blocks into key parts: blocks 0 .. nwhole - 1
+// whole, every later block in k parts (ScoreArgs::nwhole, ::ksplit).
+struct SplitPlan {
+    int nwhole;
+    int k;
+};
 
 bool score_supported(idx_dtype dt, int H, int D);
 cudaError_t launch_score(const ScoreLaunch& L, cudaStream_t s);

@@ -20,9 +20,10 @@
 // Every mode runs the same arithmetic, so the fused path compares exactly the
 // scores that the materialising baseline writes.
 //
-// A launch may split every row block's key tiles into gridDim.y contiguous
-// parts (SPLIT instantiation); each part of the emit pass then fills runs of
-// its own.
+// A launch may split row blocks' key tiles into contiguous parts, one CTA
+// each (SPLIT instantiation): the blocks of the last, partly filled wave of an
+// otherwise whole grid, or every block of a grid too small to fill the GPU.
+// Each part of the emit pass fills runs of its own.
 #pragma once
 
 #include "plan.cuh"
@@ -159,18 +160,19 @@ IDX_DEVI float head_reduce_lane(uint32_t taddr, const float* w_row) {
     return (a0.x + a0.y) + (a1.x + a1.y);
 }
 
-// SPLIT: the launch splits row blocks over key ranges (grid.y) or addresses a
-// slab with more than kRuns runs per row; without it the kernel is compiled
-// with kRuns runs per row and no split arithmetic.
-// One pass of the CTA over row block blk in scoring mode `mode` (rescan
-// histogram passes: digit `level`).  Every thread of the CTA calls it; it ends
+// SPLIT: the launch splits row blocks over key ranges or addresses a slab
+// with more than kRuns runs per row; without it the kernel is compiled with
+// kRuns runs per row and no split arithmetic.
+// One pass of the CTA over part `part` of `nparts` of row block blk's key
+// tiles in scoring mode `mode` (rescan histogram passes: digit `level`).  Every thread of the CTA calls it; it ends
 // with the CTA synchronised and no copy or MMA in flight.  TMEM is taken by the
 // first pass that has tiles to score and kept until the kernel ends
 // (tslot[0] = address, tslot[1] = taken).
 template <int DT, int H, int RB, bool SPLIT>
 IDX_DEVI void score_pass(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                          const CUtensorMap& tm_ks, const ScoreArgs& a, uint8_t* smem,
-                         const int blk, const int mode, const int level) {
+                         const int blk, const int part, const int nparts, const int mode,
+                         const int level) {
     using C = ScoreCfg<DT, H, RB>;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
     uint64_t* full = bars;
@@ -189,6 +191,29 @@ IDX_DEVI void score_pass(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
     const int r0 = blk * C::R;
     const int phase =
         mode == SM_SAMPLE ? (int)(hash32((uint32_t)blk ^ a.phase_seed) % (uint32_t)a.S) : 0;
+
+    // The block's q rows do not depend on its metadata: thread 0 (the TMA
+    // producer) sets the pipeline's barriers up and starts the q copy first, so
+    // that it lands while the metadata is read.  (The previous pass ended with
+    // no copy or MMA in flight.)
+    if (tid == 0) {
+        for (int i = 0; i < C::NS; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&accf[i], 1);
+            mbar_init(&acce[i], C::TEAM_WARPS);
+        }
+        mbar_init(qfull, 1);
+        fence_barrier_init();
+        prefetch_tmap(&tm_q);
+        mbar_arrive_expect_tx(qfull, C::B_BYTES);
+#pragma unroll
+        for (int c = 0; c < C::NCHUNK; ++c)
+            tma_load_2d(smem + C::OFF_B + c * C::B_CHUNK, &tm_q, qfull, c * C::CHUNK_ELEMS,
+                        r0 * H);
+    }
 
     // ---- per-row metadata
     if (tid < C::R) {
@@ -256,9 +281,10 @@ IDX_DEVI void score_pass(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
             }
         }
         if (!active) lo = hi = 0;
-        // the re-emission (one launch over whole rows) leaves the runs of the
-        // main pass's other key splits empty
-        if (SPLIT && mode == SM_FB_EMIT && active)
+        // a pass over a whole row block (the re-emission, or an emit CTA of a
+        // block that the launch does not split) leaves the runs of the other
+        // key splits empty
+        if (SPLIT && active && (mode == SM_FB_EMIT || (mode == SM_EMIT && nparts == 1)))
             for (int c = kRuns; c < a.nruns; ++c) a.run_cnt[(long long)r * a.nruns + c] = 0;
         m[MW_ACTIVE] = active;
         m[MW_LO] = lo;
@@ -298,9 +324,9 @@ IDX_DEVI void score_pass(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
             nt = (hi + C::M - 1) / C::M - t0;
         }
         if (SPLIT) {
-            // key split c of gridDim.y: a contiguous part of the block's tiles
-            const int per = (nt + (int)gridDim.y - 1) / (int)gridDim.y;
-            const int ts = (int)blockIdx.y * per;
+            // part `part` of nparts: a contiguous range of the block's tiles
+            const int per = (nt + nparts - 1) / nparts;
+            const int ts = part * per;
             const int te = ts + per < nt ? ts + per : nt;
             misc[0] = t0 + ts;
             misc[1] = te > ts ? te - ts : 0;
@@ -308,28 +334,20 @@ IDX_DEVI void score_pass(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
             misc[0] = t0;
             misc[1] = nt;
         }
-        for (int i = 0; i < C::NS; ++i) {
-            mbar_init(&full[i], 1);
-            mbar_init(&empty[i], 1);
-        }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&accf[i], 1);
-            mbar_init(&acce[i], C::TEAM_WARPS);
-        }
-        mbar_init(qfull, 1);
-        fence_barrier_init();
     }
     __syncthreads();
     const int t0 = misc[0];
     const int ntiles = misc[1];
     if (ntiles == 0) {
-        // nothing to score in this part; its runs of the active rows are empty
+        // nothing to score in this part; its runs of the active rows are empty.
+        // The q copy is waited for (bounded): the next pass sets the barriers
+        // up again
+        if (tid == 0) mbar_wait(qfull, 0, nullptr, 1ll << 28);
         if (SPLIT && mode == SM_EMIT) {
             for (int i = tid; i < C::R * kRuns; i += C::THREADS) {
                 const int rr = i / kRuns;
                 if (meta[rr * C::META_WORDS + MW_ACTIVE])
-                    a.run_cnt[(long long)(r0 + rr) * a.nruns + (int)blockIdx.y * kRuns +
-                              i % kRuns] = 0;
+                    a.run_cnt[(long long)(r0 + rr) * a.nruns + part * kRuns + i % kRuns] = 0;
             }
         }
         __syncthreads();  // every thread is done with this pass's shared state
@@ -353,13 +371,7 @@ IDX_DEVI void score_pass(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
-            prefetch_tmap(&tm_q);
             prefetch_tmap(mode == SM_SAMPLE ? (const void*)&tm_ks : (const void*)&tm_k);
-            mbar_arrive_expect_tx(qfull, C::B_BYTES);
-#pragma unroll
-            for (int c = 0; c < C::NCHUNK; ++c)
-                tma_load_2d(smem + C::OFF_B + c * C::B_CHUNK, &tm_q, qfull, c * C::CHUNK_ELEMS,
-                            r0 * H);
             int issued = 0;
             for (int i = 0; i < ntiles; ++i) {
                 const int s = i % C::NS;
@@ -383,7 +395,8 @@ IDX_DEVI void score_pass(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                         tma_load_2d(dst, &tm_k, &full[s], c * C::CHUNK_ELEMS, row0);
                 }
             }
-            // do not leave with copies in flight: wait (bounded) for the last stages
+            // do not leave with copies in flight: wait (bounded) for q and the last stages
+            mbar_wait(qfull, 0, nullptr, 1ll << 28);
             for (int i = issued > C::NS ? issued - C::NS : 0; i < issued; ++i)
                 if (i != a.withhold_tile)
                     mbar_wait(&full[i % C::NS], (uint32_t)((i / C::NS) & 1), nullptr, 1ll << 28);
@@ -484,7 +497,7 @@ IDX_DEVI void score_pass(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
         // this warp's runs of its rows, (score bits, index) pairs: row j's run
         // at pr + j * rstride
         const int nruns = SPLIT ? a.nruns : kRuns;
-        const int split_run0 = SPLIT ? (int)blockIdx.y * kRuns : 0;
+        const int split_run0 = SPLIT ? part * kRuns : 0;
         const long long rb = (long long)(r0 + grp * C::RG) * nruns + split_run0 + run;
         int2* const pr = a.slab ? a.slab + rb * a.cap_q : nullptr;
         const int rstride = nruns * a.cap_q;
@@ -658,10 +671,10 @@ IDX_DEVI void score_pass(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
     tc_fence_after();
 }
 
-// The kernel: one CTA per row block (grid.x) and key split (grid.y), one pass
-// in the launch's mode; or, for the exact rescan (SM_RESCAN), a grid that
-// strides over the device list of flagged row blocks and runs, per block, the
-// histogram passes of the digits its rows still need and then the
+// The kernel: one CTA per row block or part of one (see ScoreArgs::nwhole),
+// one pass in the launch's mode; or, for the exact rescan (SM_RESCAN), a grid
+// that strides over the device list of flagged row blocks and runs, per
+// block, the histogram passes of the digits its rows still need and then the
 // re-emission.  A rescan launch with no block listed ends at once.
 template <int DT, int H, int RB, bool SPLIT>
 __global__ void __launch_bounds__(ScoreCfg<DT, H, RB>::THREADS, 1)
@@ -676,10 +689,19 @@ score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     int* misc = reinterpret_cast<int*>(smem + C::OFF_MISC);
     const int tid = threadIdx.x, warp = tid >> 5;
     if (a.mode == SM_RESCAN && *(volatile int*)(a.fb_cnt + 7) == 0) return;  // none flagged
-    if (a.mode == SM_SAMPLE && blockIdx.y == 0) {
+    const bool rescan = a.mode == SM_RESCAN;
+    // this CTA's row block and part of it
+    int blk0 = (int)blockIdx.x, part = 0, nparts = 1;
+    if (SPLIT && !rescan && (int)blockIdx.x >= a.nwhole) {
+        const int u = (int)blockIdx.x - a.nwhole;
+        blk0 = a.nwhole + u / a.ksplit;
+        part = u % a.ksplit;
+        nparts = a.ksplit;
+    }
+    if (a.mode == SM_SAMPLE && part == 0) {
         // a new call: the rescan counters and this block's rescan flag start at 0
         if (blockIdx.x == 0 && tid < 8) a.fb_cnt[tid] = 0;
-        if (tid == 0 && a.fb_bflag) a.fb_bflag[blockIdx.x] = 0;
+        if (tid == 0 && a.fb_bflag) a.fb_bflag[blk0] = 0;
     }
     if (tid == 0) {
         tslot[1] = 0;
@@ -688,14 +710,13 @@ score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     // (the first synchronisation inside the pass orders these writes)
     // one call site of the pass (it is inlined once): a plain launch makes one
     // pass over its own row block; the rescan makes 7 passes per listed block
-    const bool rescan = a.mode == SM_RESCAN;
     const int nb = rescan ? *(volatile int*)(a.fb_cnt + 7) : 1;
     const int npass = rescan ? 7 : 1;
     for (int wi = rescan ? (int)blockIdx.x : 0; wi < nb; wi += rescan ? (int)gridDim.x : 1) {
-        const int blk = rescan ? a.fb_blocks[wi] : (int)blockIdx.x;
+        const int blk = rescan ? a.fb_blocks[wi] : blk0;
         for (int pass = 0; pass < npass; ++pass) {
             const int mode = rescan ? (pass < 6 ? SM_FB_HIST : SM_FB_EMIT) : a.mode;
-            score_pass<DT, H, RB, SPLIT>(tm_q, tm_k, tm_ks, a, smem, blk, mode,
+            score_pass<DT, H, RB, SPLIT>(tm_q, tm_k, tm_ks, a, smem, blk, part, nparts, mode,
                                          rescan ? pass : a.level);
         }
     }

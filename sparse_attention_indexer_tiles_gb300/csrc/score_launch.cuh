@@ -82,9 +82,16 @@ cudaError_t launch_score_t(const ScoreLaunch& L, cudaStream_t s) {
     });
     if (attr_err != cudaSuccess) return attr_err;
     const int nblk = (a.rows + C::R - 1) / C::R;
-    const int gx = a.mode == SM_RESCAN && a.grid_x > 0 && a.grid_x < nblk ? a.grid_x : nblk;
-    const dim3 grid((unsigned)gx, (unsigned)(a.ksplit > 1 && a.mode != SM_RESCAN ? a.ksplit : 1));
-    kern<<<grid, C::THREADS, C::SMEM_ALLOC, s>>>(tq, tk, tks, a);
+    long long gx;
+    if (a.mode == SM_RESCAN) {
+        gx = a.grid_x > 0 && a.grid_x < nblk ? a.grid_x : nblk;
+    } else {
+        if (a.ksplit < 1 || a.nwhole < 0 || a.nwhole > nblk || (a.ksplit == 1 && a.nwhole != nblk))
+            return cudaErrorInvalidValue;
+        gx = a.nwhole + (long long)(nblk - a.nwhole) * a.ksplit;
+    }
+    if (gx > 0x7fffffffll) return cudaErrorInvalidValue;
+    kern<<<(unsigned)gx, C::THREADS, C::SMEM_ALLOC, s>>>(tq, tk, tks, a);
     return cudaGetLastError();
 }
 

@@ -83,7 +83,27 @@ IDX_DEVI bool warp_row_threshold(const ThrParams& p, int r, uint32_t* hist, uint
 #pragma unroll
         for (int j = 0; j < 8; ++j) hist[lane * 8 + j] = 0u;
         __syncwarp();
-        for (uint32_t e = lane; e < sr.n; e += 32) {
+        // 16-byte loads of eight keys (a row's sample starts 16-byte aligned),
+        // four per lane in flight, then the odd tail
+        const uint4* v4 = reinterpret_cast<const uint4*>(sr.keys);
+        const uint32_t n8 = sr.n / 8;
+        for (uint32_t base = lane; base < n8; base += 4 * 32) {
+            uint4 x[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                x[u] = base + u * 32 < n8 ? __ldcg(v4 + base + u * 32) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                if (base + u * 32 >= n8) continue;
+                const uint32_t wd[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+#pragma unroll
+                for (int h = 0; h < 8; ++h) {
+                    const uint32_t key = (wd[h >> 1] >> (16 * (h & 1))) & 0xffffu;
+                    if (lev == 0 || (key >> 8) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+                }
+            }
+        }
+        for (uint32_t e = n8 * 8 + lane; e < sr.n; e += 32) {
             const uint32_t key = sr.keys[e];
             if (lev == 0 || (key >> 8) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
         }

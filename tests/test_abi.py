@@ -137,11 +137,12 @@ def _documented_workspace(rows, max_len, topk, nruns):
 
 def test_fused_workspace_follows_the_documented_layout(lib):
     """Eight runs per row and key split.  With no device answering, the
-    library takes 148 SMs: 4096 rows (1024 row blocks of H = 64) fill their
-    last wave and are not split; 1024 rows split every block's keys in 4 (the
-    k <= 6 that fills the last wave best); calls with at most half a wave of
-    row blocks split up to one wave's worth (SMs / blocks), every part keeping
-    >= 32 key tiles."""
+    library takes 148 SMs.  Full waves keep whole row blocks; the blocks of the
+    last wave are cut into the k parts that minimise ceil(tail k / SMs) (1 / k
+    + 8 / tiles), every part keeping >= 32 key tiles: 4096 rows (1024 blocks
+    of H = 64, a 136-block tail) are not split; 1024 rows (256 blocks: one
+    whole wave and a 108-block tail) cut the tail in 4; calls with fewer blocks
+    than SMs cut every block into up to one wave's worth."""
     import sparse_attention_indexer_tiles_gb300 as pkg
     ws = pkg.idx_score_topk_workspace
     cases = [  # rows, keys, topk, expected key splits (148 SMs: no device answers here)

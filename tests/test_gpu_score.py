@@ -138,6 +138,22 @@ def test_fused_equals_two_pass_bitwise(idx):
     assert np.array_equal(got, two_pass(idx, inp))
 
 
+def test_tail_blocks_split_into_key_parts(idx):
+    """SMs + 3 row blocks (H = 64: 4 rows each): the full wave keeps whole
+    blocks and the last three are cut into key parts, each emitting runs of
+    its own while whole blocks leave those runs empty.  Every row equals the
+    two-pass result bitwise; rows of whole and of split blocks match the
+    oracle."""
+    sm = torch.cuda.get_device_properties(0).multi_processor_count
+    rows = (sm + 3) * 4
+    inp = synth.indexer_inputs(rows, 16384, 64, 128, 512, "fp8", seed=44)
+    stats = idx.Stats(torch.device(DEV))
+    got = fused(idx, inp, stats=stats)
+    assert np.array_equal(got, two_pass(idx, inp))
+    assert stats.read()["status"] == 0
+    check_fused(inp, got, rows=[0, 1, 5, rows // 2, rows - 13, rows - 12, rows - 7, rows - 1])
+
+
 @pytest.mark.parametrize("knob,stat", [({"target_factor": 0.3}, "short_rows"),
                                        ({"target_factor": 30.0}, "overflow_rows"),
                                        ({"sample_stride": 997}, None)])
