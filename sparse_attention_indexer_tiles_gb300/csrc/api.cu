@@ -193,7 +193,8 @@ FusedLayout fused_layout(int rows, long long max_len, int cap, int cap_q, int S,
     L.fb_hist = take(max_len > cap ? (size_t)rows * 4096 * sizeof(uint32_t) : 0);
     L.fb_blocks = take(max_len > cap ? nblk * sizeof(int) : 0);
     L.fb_bflag = take(max_len > cap ? nblk * sizeof(int) : 0);
-    L.fb_cnt = take(8 * sizeof(int));
+    // [0, 8) rescan counters, [8] [9] the sample and emit launches' unit counters
+    L.fb_cnt = take(16 * sizeof(int));
     L.total = off;
     return L;
 }
@@ -236,6 +237,7 @@ ScoreLaunch make_score_launch(const void* q, const void* k, const float* k_scale
     L.a.nwhole = (rows + score_rows_per_block(H) - 1) / score_rows_per_block(H);
     L.a.ksplit = 1;
     L.a.nruns = kRuns;
+    L.a.grid_x = sm_count();
     // about 2 s at the GB300's clock; the test knob shortens it and withholds
     // key tile 1 of every scoring pass
     const int stall_us = opt ? opt->test_stall_us : 0;
@@ -384,10 +386,14 @@ idx_status idx_score_topk(const void* q, const void* k, const float* k_scale, co
     cudaError_t e;
 
     record(opt, 0, s);
+    // the persistent scoring launches take units from counters that start at 0
+    if ((e = cudaMemsetAsync(fb_cnt + 8, 0, 2 * sizeof(int), s)) != cudaSuccess)
+        return cuda_status(e);
     if (sampling) {
         // 1. score the odd-stride sample of every long row (key splits over the
         //    sample index range, as for the emit pass)
         L.a.mode = SM_SAMPLE;
+        L.a.sched = fb_cnt + 8;
         const SplitPlan sp = score_split(rows, H, max_len / p.S + 1);
         L.a.nwhole = sp.nwhole;
         L.a.ksplit = sp.k;
@@ -422,6 +428,7 @@ idx_status idx_score_topk(const void* q, const void* k, const float* k_scale, co
     L.a.mode = SM_EMIT;
     L.a.nwhole = split.nwhole;
     L.a.ksplit = split.k;
+    L.a.sched = fb_cnt + 9;
     if ((e = launch_score(L, s)) != cudaSuccess) return cuda_status(e);
     record(opt, 2, s);
     // 4. exact top-k of every slab; rows whose count missed [topk, cap] are flagged

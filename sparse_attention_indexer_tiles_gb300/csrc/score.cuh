@@ -57,7 +57,11 @@ struct ScoreArgs {
                           // [7] row blocks listed in fb_blocks
     int* fb_blocks;       // [row blocks] the blocks with a row in the rescan
     int* fb_bflag;        // [row blocks] 1 once a block is listed
-    int grid_x;           // CTAs of an SM_RESCAN launch (they stride over the list)
+    int grid_x;           // at most this many CTAs (one per SM): a scoring launch's CTAs
+                          // take units in turn, a rescan's stride over its list
+    int* sched;           // optional launch counter, 0 before the launch: CTAs take
+                          // units gridDim.x + atomicAdd(sched, 1) in turn (null: every
+                          // gridDim.x-th unit)
     int level;
     // bounded waits: a wait on the pipeline gives up after wait_limit clock
     // cycles; withhold_tile >= 0 (a test of that path) makes the producer issue

@@ -53,19 +53,40 @@ struct ScoreCfg {
     static constexpr int RG = R / 2;                        // rows per epilogue warp
     static constexpr int THREADS = 32 * (4 + EPI_WARPS);
     static constexpr uint32_t IDESC = instr_desc(DT == IDX_BF16 ? 1u : 0u, M, N);
+    // q buffers: two let the next pass's q copy start during this pass
+    static constexpr int QB = RB >= 256 ? 1 : 2;
     // shared memory carve (offsets from a 1024-byte aligned base)
     static constexpr int OFF_B = 0;
-    static constexpr int OFF_A = B_BYTES;
+    static constexpr int OFF_A = QB * B_BYTES;
     static constexpr int OFF_BAR = OFF_A + NS * A_BYTES;
-    static constexpr int NBAR = 2 * NS + 5;
+    // full[NS], empty[NS], accf[2], acce[2] (set up again by every pass), then,
+    // kept for the whole kernel, qfull[QB] and pdone (the producer has issued
+    // the pass's last key tile)
+    static constexpr int NBAR = 2 * NS + 4 + QB + 1;
     static constexpr int OFF_TSLOT = OFF_BAR + NBAR * 8;
-    static constexpr int OFF_W = (OFF_TSLOT + 16 + 15) / 16 * 16;
-    static constexpr int OFF_META = OFF_W + R * H * 4;
+    static constexpr int OFF_CTL = OFF_TSLOT + 16;          // [0] abort flag, [1] next unit
+    // two slots of pass metadata (the pass that runs, the one being prepared):
+    // head weights [R * H], row words [R][META_WORDS], pass words [PASS_WORDS]
+    static constexpr int OFF_W = (OFF_CTL + 16 + 15) / 16 * 16;
+    static constexpr int OFF_META = OFF_W + 2 * R * H * 4;
     static constexpr int META_WORDS = 8;                    // per row
-    static constexpr int OFF_MISC = OFF_META + R * META_WORDS * 4;
-    static constexpr int SMEM_USED = OFF_MISC + 64;
+    static constexpr int OFF_MISC = OFF_META + 2 * R * META_WORDS * 4;
+    static constexpr int PASS_WORDS = 16;
+    static constexpr int SMEM_USED = OFF_MISC + 2 * PASS_WORDS * 4;
     // at least ~120 KB so that one CTA owns an SM (and its 512 TMEM columns)
     static constexpr int SMEM_ALLOC = (SMEM_USED + 1024 > 122880 ? SMEM_USED + 1024 : 122880);
+};
+
+// per-pass words of a metadata slot
+enum : int {
+    PW_T0 = 0,      // first key tile of the pass
+    PW_NT,          // key tiles of the pass
+    PW_ALL_LO,      // [all_lo, all_hi): keys every active row sees
+    PW_ALL_HI,
+    PW_PHASE,       // SM_SAMPLE: the block's sample phase
+    PW_BLK,         // row block, part, parts
+    PW_PART,
+    PW_NPARTS,
 };
 
 // per-row metadata words in shared memory
@@ -160,65 +181,26 @@ IDX_DEVI float head_reduce_lane(uint32_t taddr, const float* w_row) {
     return (a0.x + a0.y) + (a1.x + a1.y);
 }
 
-// SPLIT: the launch splits row blocks over key ranges or addresses a slab
-// with more than kRuns runs per row; without it the kernel is compiled with
-// kRuns runs per row and no split arithmetic.
-// One pass of the CTA over part `part` of `nparts` of row block blk's key
-// tiles in scoring mode `mode` (rescan histogram passes: digit `level`).  Every thread of the CTA calls it; it ends
-// with the CTA synchronised and no copy or MMA in flight.  TMEM is taken by the
-// first pass that has tiles to score and kept until the kernel ends
-// (tslot[0] = address, tslot[1] = taken).
-template <int DT, int H, int RB, bool SPLIT>
-IDX_DEVI void score_pass(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
-                         const CUtensorMap& tm_ks, const ScoreArgs& a, uint8_t* smem,
-                         const int blk, const int part, const int nparts, const int mode,
-                         const int level) {
+// The metadata of one pass over part `part` of `nparts` of row block blk in
+// scoring mode `mode` (rescan histogram passes: digit `level`) into metadata
+// slot `sl`: per row its visible range in the pass's index space, threshold
+// words and head weights; per pass its key tiles.  Run by the nthr threads
+// t = 0 .. nthr - 1 of a group that synchronises with bar() (the whole CTA
+// before the first pass or a rescan pass; two warps while another pass runs).
+template <int DT, int H, int RB, bool SPLIT, typename Bar>
+IDX_DEVI void prep_pass(const ScoreArgs& a, uint8_t* smem, const int sl, const int blk,
+                        const int part, const int nparts, const int mode, const int level,
+                        const int t, const int nthr, Bar bar) {
     using C = ScoreCfg<DT, H, RB>;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-    uint64_t* full = bars;
-    uint64_t* empty = bars + C::NS;
-    uint64_t* accf = bars + 2 * C::NS;
-    uint64_t* acce = accf + 2;
-    uint64_t* qfull = acce + 2;
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + C::OFF_TSLOT);
-    float* w_s = reinterpret_cast<float*>(smem + C::OFF_W);
-    int* meta = reinterpret_cast<int*>(smem + C::OFF_META);
-    // [0] t0, [1] ntiles, [2] abort flag, [3, 4) keys every active row sees
-    int* misc = reinterpret_cast<int*>(smem + C::OFF_MISC);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 2);
-
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    float* w_s = reinterpret_cast<float*>(smem + C::OFF_W) + sl * C::R * H;
+    int* meta = reinterpret_cast<int*>(smem + C::OFF_META) + sl * C::R * C::META_WORDS;
+    int* pw = reinterpret_cast<int*>(smem + C::OFF_MISC) + sl * C::PASS_WORDS;
     const int r0 = blk * C::R;
     const int phase =
         mode == SM_SAMPLE ? (int)(hash32((uint32_t)blk ^ a.phase_seed) % (uint32_t)a.S) : 0;
-
-    // The block's q rows do not depend on its metadata: thread 0 (the TMA
-    // producer) sets the pipeline's barriers up and starts the q copy first, so
-    // that it lands while the metadata is read.  (The previous pass ended with
-    // no copy or MMA in flight.)
-    if (tid == 0) {
-        for (int i = 0; i < C::NS; ++i) {
-            mbar_init(&full[i], 1);
-            mbar_init(&empty[i], 1);
-        }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&accf[i], 1);
-            mbar_init(&acce[i], C::TEAM_WARPS);
-        }
-        mbar_init(qfull, 1);
-        fence_barrier_init();
-        prefetch_tmap(&tm_q);
-        mbar_arrive_expect_tx(qfull, C::B_BYTES);
-#pragma unroll
-        for (int c = 0; c < C::NCHUNK; ++c)
-            tma_load_2d(smem + C::OFF_B + c * C::B_CHUNK, &tm_q, qfull, c * C::CHUNK_ELEMS,
-                        r0 * H);
-    }
-
-    // ---- per-row metadata
-    if (tid < C::R) {
-        int* m = meta + tid * C::META_WORDS;
-        const int r = r0 + tid;
+    if (t < C::R) {
+        int* m = meta + t * C::META_WORDS;
+        const int r = r0 + t;
         int ks = 0, ke = 0, active = 0, lo = 0, hi = 0, cut = kAllIdx;
         uint32_t thr = 0, prefix = 0;
         if (r < a.rows) {
@@ -301,12 +283,12 @@ IDX_DEVI void score_pass(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
         m[MW_THRF] =
             __float_as_int(active && thr != 0xffffffffu ? key_floor_float(thr) : INFINITY);
     }
-    for (int i = tid; i < C::R * H; i += C::THREADS) {
+    for (int i = t; i < C::R * H; i += nthr) {
         const long long r = r0 + i / H;
         w_s[i] = r < a.rows ? a.w[(long long)r0 * H + i] : 0.f;
     }
-    __syncthreads();
-    if (tid == 0) {
+    bar();
+    if (t == 0) {
         int lo = 0x7fffffff, hi = -1, all_lo = -1, all_hi = 0x7fffffff;
         for (int j = 0; j < C::R; ++j) {
             const int* m = meta + j * C::META_WORDS;
@@ -316,8 +298,8 @@ IDX_DEVI void score_pass(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
             all_lo = m[MW_LO] > all_lo ? m[MW_LO] : all_lo;
             all_hi = m[MW_HI] < all_hi ? m[MW_HI] : all_hi;
         }
-        misc[3] = all_lo;
-        misc[4] = all_hi;
+        pw[PW_ALL_LO] = all_lo;
+        pw[PW_ALL_HI] = all_hi;
         int t0 = 0, nt = 0;
         if (hi > lo) {
             t0 = lo / C::M;
@@ -328,28 +310,108 @@ IDX_DEVI void score_pass(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
             const int per = (nt + nparts - 1) / nparts;
             const int ts = part * per;
             const int te = ts + per < nt ? ts + per : nt;
-            misc[0] = t0 + ts;
-            misc[1] = te > ts ? te - ts : 0;
+            pw[PW_T0] = t0 + ts;
+            pw[PW_NT] = te > ts ? te - ts : 0;
         } else {
-            misc[0] = t0;
-            misc[1] = nt;
+            pw[PW_T0] = t0;
+            pw[PW_NT] = nt;
+        }
+        pw[PW_PHASE] = phase;
+        pw[PW_BLK] = blk;
+        pw[PW_PART] = part;
+        pw[PW_NPARTS] = nparts;
+        // a new call: this block's rescan flag starts at 0
+        if (mode == SM_SAMPLE && part == 0 && a.fb_bflag) a.fb_bflag[blk] = 0;
+    }
+    bar();
+    if (SPLIT && mode == SM_EMIT && pw[PW_NT] == 0) {
+        // nothing to score in this part: its runs of the active rows are empty
+        for (int i = t; i < C::R * kRuns; i += nthr) {
+            const int rr = i / kRuns;
+            if (meta[rr * C::META_WORDS + MW_ACTIVE])
+                a.run_cnt[(long long)(r0 + rr) * a.nruns + part * kRuns + i % kRuns] = 0;
+        }
+    }
+}
+
+// Issue the copy of row block blk's q rows into q buffer qs (thread of the
+// caller's choice; the buffer and its barrier must be idle).
+template <int DT, int H, int RB>
+IDX_DEVI void issue_q(const CUtensorMap& tm_q, uint8_t* smem, const int qs, const int blk) {
+    using C = ScoreCfg<DT, H, RB>;
+    uint64_t* qfull = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR) + 2 * C::NS + 4;
+    mbar_arrive_expect_tx(&qfull[qs], C::B_BYTES);
+#pragma unroll
+    for (int c = 0; c < C::NCHUNK; ++c)
+        tma_load_2d(smem + C::OFF_B + qs * C::B_BYTES + c * C::B_CHUNK, &tm_q, &qfull[qs],
+                    c * C::CHUNK_ELEMS, blk * C::R * H);
+}
+
+// SPLIT: the launch splits row blocks over key ranges or addresses a slab
+// with more than kRuns runs per row; without it the kernel is compiled with
+// kRuns runs per row and no split arithmetic.
+// One pass of the CTA over the part of a row block that metadata slot sl
+// describes (prep_pass), in scoring mode `mode` (rescan histogram passes:
+// digit `level`), with the block's q rows in q buffer qs (phase parity qpar of
+// its barrier); q_at_start: thread 0 issues that copy here, else it was issued
+// before.  Warps 2 and 3 run `side` meanwhile (the next pass's metadata, or
+// nothing), in a pass with tiles once the producer is 2 NS tiles short of the
+// pass's end (phase parity ppar of pdone): the next unit is taken late enough
+// that a CTA does not commit to it long before it can start it, and early
+// enough that its q copy and metadata are ready when the pass ends.  Every thread of the CTA calls it; it ends with the CTA
+// synchronised, no MMA in flight and the pass's copies landed.  TMEM is taken
+// by the first pass that has tiles to score and kept until the kernel ends
+// (tslot[0] = address, tslot[1] = taken).
+template <int DT, int H, int RB, bool SPLIT, typename Side>
+IDX_DEVI void score_pass(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+                         const CUtensorMap& tm_ks, const ScoreArgs& a, uint8_t* smem,
+                         const int sl, const int qs, const uint32_t qpar, const bool q_at_start,
+                         const uint32_t ppar, const int mode, const int level, Side side) {
+    using C = ScoreCfg<DT, H, RB>;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+    uint64_t* full = bars;
+    uint64_t* empty = bars + C::NS;
+    uint64_t* accf = bars + 2 * C::NS;
+    uint64_t* acce = accf + 2;
+    uint64_t* qfull = acce + 2 + qs;
+    uint64_t* pdone = acce + 2 + C::QB;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + C::OFF_TSLOT);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_CTL);
+    const float* w_s = reinterpret_cast<const float*>(smem + C::OFF_W) + sl * C::R * H;
+    const int* meta = reinterpret_cast<const int*>(smem + C::OFF_META) + sl * C::R * C::META_WORDS;
+    const int* pw = reinterpret_cast<const int*>(smem + C::OFF_MISC) + sl * C::PASS_WORDS;
+    uint8_t* const qbuf = smem + C::OFF_B + qs * C::B_BYTES;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int blk = pw[PW_BLK], part = pw[PW_PART];
+    const int r0 = blk * C::R;
+    const int phase = pw[PW_PHASE];
+    const int t0 = pw[PW_T0];
+    const int ntiles = pw[PW_NT];
+    (void)part;
+
+    // the pipeline's barriers, set up again for every pass (the previous pass
+    // ended with none in use)
+    if (tid == 0) {
+        for (int i = 0; i < C::NS; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&accf[i], 1);
+            mbar_init(&acce[i], C::TEAM_WARPS);
+        }
+        fence_barrier_init();
+        if (q_at_start) {
+            prefetch_tmap(&tm_q);
+            issue_q<DT, H, RB>(tm_q, smem, qs, blk);
         }
     }
     __syncthreads();
-    const int t0 = misc[0];
-    const int ntiles = misc[1];
     if (ntiles == 0) {
-        // nothing to score in this part; its runs of the active rows are empty.
-        // The q copy is waited for (bounded): the next pass sets the barriers
-        // up again
-        if (tid == 0) mbar_wait(qfull, 0, nullptr, 1ll << 28);
-        if (SPLIT && mode == SM_EMIT) {
-            for (int i = tid; i < C::R * kRuns; i += C::THREADS) {
-                const int rr = i / kRuns;
-                if (meta[rr * C::META_WORDS + MW_ACTIVE])
-                    a.run_cnt[(long long)(r0 + rr) * a.nruns + part * kRuns + i % kRuns] = 0;
-            }
-        }
+        // nothing to score: the q copy is waited for (bounded)
+        if (tid == 0) mbar_wait(qfull, qpar, nullptr, 1ll << 28);
+        if (warp == 2 || warp == 3) side();
         __syncthreads();  // every thread is done with this pass's shared state
         return;
     }
@@ -373,9 +435,16 @@ IDX_DEVI void score_pass(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
         if (lane == 0) {
             prefetch_tmap(mode == SM_SAMPLE ? (const void*)&tm_ks : (const void*)&tm_k);
             int issued = 0;
+            // the side job may take the next unit once this many tiles are issued
+            const int lead = ntiles > 2 * C::NS ? ntiles - 2 * C::NS : 0;
+            bool told = false;
             for (int i = 0; i < ntiles; ++i) {
                 const int s = i % C::NS;
                 const uint32_t use = (uint32_t)(i / C::NS);
+                if (i == lead) {
+                    mbar_arrive(pdone);
+                    told = true;
+                }
                 if (i >= C::NS &&
                     !mbar_wait(&empty[s], (use & 1u) ^ 1u, abort_flag, a.wait_limit)) {
                     *abort_flag = 1;
@@ -395,8 +464,9 @@ IDX_DEVI void score_pass(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                         tma_load_2d(dst, &tm_k, &full[s], c * C::CHUNK_ELEMS, row0);
                 }
             }
+            if (!told) mbar_arrive(pdone);  // (the loop stopped early)
             // do not leave with copies in flight: wait (bounded) for q and the last stages
-            mbar_wait(qfull, 0, nullptr, 1ll << 28);
+            mbar_wait(qfull, qpar, nullptr, 1ll << 28);
             for (int i = issued > C::NS ? issued - C::NS : 0; i < issued; ++i)
                 if (i != a.withhold_tile)
                     mbar_wait(&full[i % C::NS], (uint32_t)((i / C::NS) & 1), nullptr, 1ll << 28);
@@ -405,8 +475,8 @@ IDX_DEVI void score_pass(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
             const uint32_t a_base = smem_u32(smem + C::OFF_A);
-            const uint32_t b_base = smem_u32(smem + C::OFF_B);
-            bool ok = mbar_wait(qfull, 0, abort_flag, a.wait_limit);
+            const uint32_t b_base = smem_u32(qbuf);
+            bool ok = mbar_wait(qfull, qpar, abort_flag, a.wait_limit);
             int issued = 0;
             for (int i = 0; ok && i < ntiles; ++i) {
                 const int s = i % C::NS;
@@ -456,7 +526,12 @@ IDX_DEVI void score_pass(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
             for (int i = issued > C::NS ? issued - C::NS : 0; i < issued; ++i)
                 mbar_wait(&empty[i % C::NS], (uint32_t)((i / C::NS) & 1), nullptr, 1ll << 28);
         }
-    } else if (warp >= 4) {
+    } else if (warp < 4) {
+        // ------------------------------------------------ warps 2, 3: side job
+        // once the producer is done (bounded: after a time-out it goes ahead)
+        mbar_wait(pdone, ppar, abort_flag, a.wait_limit);
+        side();
+    } else {
         // ------------------------------------------------ epilogue
         const int e = warp - 4;
         const int team = e >> 3;             // TMEM buffer and tile parity
@@ -532,7 +607,7 @@ IDX_DEVI void score_pass(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                     wq[j][rp] = make_float2(wr[8 * rp], wr[8 * rp + 1]);
             }
         }
-        const int all_lo = misc[3], all_hi = misc[4];
+        const int all_lo = pw[PW_ALL_LO], all_hi = pw[PW_ALL_HI];
         float next_scale = team < ntiles && s_i < ilim ? __ldg(a.k_scale + s_off) : 0.f;
         const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(team * C::N);
         for (int i = team, u = 0; i < ntiles; i += 2, ++u) {
@@ -671,11 +746,35 @@ IDX_DEVI void score_pass(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
     tc_fence_after();
 }
 
-// The kernel: one CTA per row block or part of one (see ScoreArgs::nwhole),
-// one pass in the launch's mode; or, for the exact rescan (SM_RESCAN), a grid
+// Key tiles of the pass in metadata slot sl.
+template <int DT, int H, int RB>
+IDX_DEVI int pw_nt(const uint8_t* smem, int sl) {
+    using C = ScoreCfg<DT, H, RB>;
+    return reinterpret_cast<const int*>(smem + C::OFF_MISC)[sl * C::PASS_WORDS + PW_NT];
+}
+
+// Unit u of a scoring launch: a row block, or a part of one (ScoreArgs::nwhole,
+// ::ksplit).
+struct ScoreUnit {
+    int blk, part, nparts;
+};
+IDX_DEVI ScoreUnit score_unit(const ScoreArgs& a, int u) {
+    if (u < a.nwhole) return {u, 0, 1};
+    const int v = u - a.nwhole;
+    return {a.nwhole + v / a.ksplit, v % a.ksplit, a.ksplit};
+}
+
+// The kernel.  A scoring launch (SM_MATERIALISE, SM_SAMPLE, SM_EMIT) is
+// persistent: each CTA takes unit blockIdx.x, then the next unit of a launch
+// counter (a.sched; without one, every gridDim.x-th unit), one pass each.
+// While a pass runs, warps 2 and 3 take the next unit, start its q copy into
+// the other q buffer and write its metadata into the other slot, so that the
+// next pass starts with both at hand.  The exact rescan (SM_RESCAN) is a grid
 // that strides over the device list of flagged row blocks and runs, per
 // block, the histogram passes of the digits its rows still need and then the
-// re-emission.  A rescan launch with no block listed ends at once.
+// re-emission; each of those passes depends on the one before, so its
+// metadata is read just before it.  A rescan launch with no block listed ends
+// at once.
 template <int DT, int H, int RB, bool SPLIT>
 __global__ void __launch_bounds__(ScoreCfg<DT, H, RB>::THREADS, 1)
 score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -686,38 +785,87 @@ score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     // offset so that the compiler keeps every access in the shared space
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + C::OFF_TSLOT);
-    int* misc = reinterpret_cast<int*>(smem + C::OFF_MISC);
+    volatile int* ctl = reinterpret_cast<volatile int*>(smem + C::OFF_CTL);
+    uint64_t* qfull = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR) + 2 * C::NS + 4;
     const int tid = threadIdx.x, warp = tid >> 5;
     if (a.mode == SM_RESCAN && *(volatile int*)(a.fb_cnt + 7) == 0) return;  // none flagged
-    const bool rescan = a.mode == SM_RESCAN;
-    // this CTA's row block and part of it
-    int blk0 = (int)blockIdx.x, part = 0, nparts = 1;
-    if (SPLIT && !rescan && (int)blockIdx.x >= a.nwhole) {
-        const int u = (int)blockIdx.x - a.nwhole;
-        blk0 = a.nwhole + u / a.ksplit;
-        part = u % a.ksplit;
-        nparts = a.ksplit;
-    }
-    if (a.mode == SM_SAMPLE && part == 0) {
-        // a new call: the rescan counters and this block's rescan flag start at 0
-        if (blockIdx.x == 0 && tid < 8) a.fb_cnt[tid] = 0;
-        if (tid == 0 && a.fb_bflag) a.fb_bflag[blk0] = 0;
-    }
+    // a new call: the rescan counters start at 0
+    if (a.mode == SM_SAMPLE && blockIdx.x == 0 && tid < 8) a.fb_cnt[tid] = 0;
     if (tid == 0) {
         tslot[1] = 0;
-        misc[2] = 0;  // abort flag: a wait that timed out releases every later wait
+        ctl[0] = 0;  // abort flag: a wait that timed out releases every later wait
+        for (int i = 0; i < C::QB; ++i) mbar_init(&qfull[i], 1);
+        mbar_init(&qfull[C::QB], 1);  // pdone
+        fence_barrier_init();
     }
-    // (the first synchronisation inside the pass orders these writes)
-    // one call site of the pass (it is inlined once): a plain launch makes one
-    // pass over its own row block; the rescan makes 7 passes per listed block
-    const int nb = rescan ? *(volatile int*)(a.fb_cnt + 7) : 1;
-    const int npass = rescan ? 7 : 1;
-    for (int wi = rescan ? (int)blockIdx.x : 0; wi < nb; wi += rescan ? (int)gridDim.x : 1) {
-        const int blk = rescan ? a.fb_blocks[wi] : blk0;
-        for (int pass = 0; pass < npass; ++pass) {
-            const int mode = rescan ? (pass < 6 ? SM_FB_HIST : SM_FB_EMIT) : a.mode;
-            score_pass<DT, H, RB, SPLIT>(tm_q, tm_k, tm_ks, a, smem, blk, part, nparts, mode,
-                                         rescan ? pass : a.level);
+    __syncthreads();
+    auto cta_bar = [] { __syncthreads(); };
+    auto nothing = [] {};
+    if (a.mode == SM_RESCAN) {
+        const int nb = *(volatile int*)(a.fb_cnt + 7);
+        int n = 0, ptiles = 0;
+        for (int wi = (int)blockIdx.x; wi < nb; wi += (int)gridDim.x) {
+            const int blk = a.fb_blocks[wi];
+            for (int pass = 0; pass < 7; ++pass, ++n) {
+                const int mode = pass < 6 ? SM_FB_HIST : SM_FB_EMIT;
+                prep_pass<DT, H, RB, SPLIT>(a, smem, 0, blk, 0, 1, mode, pass, tid, C::THREADS,
+                                            cta_bar);
+                const bool tiles = pw_nt<DT, H, RB>(smem, 0) > 0;
+                score_pass<DT, H, RB, SPLIT>(tm_q, tm_k, tm_ks, a, smem, 0, 0,
+                                             (uint32_t)(n & 1), true, (uint32_t)(ptiles & 1),
+                                             mode, pass, nothing);
+                ptiles += tiles;
+            }
+        }
+    } else {
+        const int nblk = (a.rows + C::R - 1) / C::R;
+        const int nunits = a.nwhole + (nblk - a.nwhole) * a.ksplit;
+        int u = (int)blockIdx.x, n = 0, ptiles = 0;
+        if (u < nunits) {
+            const ScoreUnit x = score_unit(a, u);
+            if (C::QB == 2 && tid == 0) {
+                prefetch_tmap(&tm_q);
+                issue_q<DT, H, RB>(tm_q, smem, 0, x.blk);
+            }
+            prep_pass<DT, H, RB, SPLIT>(a, smem, 0, x.blk, x.part, x.nparts, a.mode, a.level, tid,
+                                        C::THREADS, cta_bar);
+        }
+        while (u < nunits) {
+            const int sl = n & 1;
+            // warps 2 and 3 during the pass: the next unit, its q copy and metadata
+            auto next_job = [&] {
+                const int t = tid - 64;
+                if (t == 0) {
+                    const int nx =
+                        a.sched ? (int)gridDim.x + atomicAdd(a.sched, 1) : u + (int)gridDim.x;
+                    ctl[1] = nx;
+                    if (C::QB == 2 && nx < nunits)
+                        issue_q<DT, H, RB>(tm_q, smem, (n + 1) & 1, score_unit(a, nx).blk);
+                }
+                named_bar_sync(2, 64);
+                const int nx = ctl[1];
+                if (nx < nunits) {
+                    const ScoreUnit x = score_unit(a, nx);
+                    prep_pass<DT, H, RB, SPLIT>(a, smem, sl ^ 1, x.blk, x.part, x.nparts, a.mode,
+                                                a.level, t, 64, [] { named_bar_sync(2, 64); });
+                }
+            };
+            const int qs = C::QB == 2 ? (n & 1) : 0;
+            const uint32_t qpar = C::QB == 2 ? (uint32_t)((n >> 1) & 1) : (uint32_t)(n & 1);
+            const bool tiles = pw_nt<DT, H, RB>(smem, sl) > 0;
+            score_pass<DT, H, RB, SPLIT>(tm_q, tm_k, tm_ks, a, smem, sl, qs, qpar, C::QB == 1,
+                                         (uint32_t)(ptiles & 1), a.mode, a.level, next_job);
+            ptiles += tiles;
+            const int nx = ctl[1];
+            if (ctl[0]) {
+                // a wait timed out: stop, once the next unit's q copy has landed
+                if (tid == 0 && C::QB == 2 && nx < nunits)
+                    mbar_wait(&qfull[(n + 1) & 1], (uint32_t)(((n + 1) >> 1) & 1), nullptr,
+                              1ll << 28);
+                break;
+            }
+            u = nx;
+            ++n;
         }
     }
     __syncthreads();

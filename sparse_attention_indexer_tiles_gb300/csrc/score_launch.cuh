@@ -88,7 +88,10 @@ cudaError_t launch_score_t(const ScoreLaunch& L, cudaStream_t s) {
     } else {
         if (a.ksplit < 1 || a.nwhole < 0 || a.nwhole > nblk || (a.ksplit == 1 && a.nwhole != nblk))
             return cudaErrorInvalidValue;
-        gx = a.nwhole + (long long)(nblk - a.nwhole) * a.ksplit;
+        // persistent: at most one CTA per SM, each taking units in turn
+        const long long units = a.nwhole + (long long)(nblk - a.nwhole) * a.ksplit;
+        if (units > 0x7fffffffll) return cudaErrorInvalidValue;
+        gx = a.grid_x > 0 && a.grid_x < units ? a.grid_x : units;
     }
     if (gx > 0x7fffffffll) return cudaErrorInvalidValue;
     kern<<<(unsigned)gx, C::THREADS, C::SMEM_ALLOC, s>>>(tq, tk, tks, a);
