@@ -419,6 +419,7 @@ idx_status idx_score_topk(const void* q, const void* k, const float* k_scale, co
         t.phase_seed = kPhaseSeed;
         t.d_status = d_status;
         t.d_stats = d_stats;
+        t.pdl = 1;  // after the sample pass
         if ((e = launch_topk_rows(t, s)) != cudaSuccess) return cuda_status(e);
         count_launches(1);
     }
@@ -429,6 +430,7 @@ idx_status idx_score_topk(const void* q, const void* k, const float* k_scale, co
     L.a.nwhole = split.nwhole;
     L.a.ksplit = split.k;
     L.a.sched = fb_cnt + 9;
+    L.pdl = sampling ? 1 : 0;  // after the thresholds (else the memset: plain launch)
     if ((e = launch_score(L, s)) != cudaSuccess) return cuda_status(e);
     record(opt, 2, s);
     // 4. exact top-k of every slab; rows whose count missed [topk, cap] are flagged
@@ -454,6 +456,7 @@ idx_status idx_score_topk(const void* q, const void* k, const float* k_scale, co
     c.d_stats = d_stats;
     c.fallback = 0;
     c.grid_limit = 2 * sm_count();
+    c.pdl = 1;  // after the emit pass
     if ((e = launch_cand_topk(c, s)) != cudaSuccess) return cuda_status(e);
     count_launches(1);
     record(opt, 3, s);

@@ -48,6 +48,15 @@ IDX_DEVI void mbar_init(uint64_t* bar, uint32_t count) {
                  : "memory");
 }
 
+// Programmatic dependent launch.  A kernel launched with the attribute (see
+// launch_k) is launched as the kernel before it on the stream finishes, its
+// CTAs taking SMs as that kernel's CTAs leave them: pdl_wait blocks until that
+// kernel has completed and its memory is visible (at once for a launch without
+// the attribute).  (No kernel here signals its dependents early: measured on
+// GB300, letting the next grid launch from the start of this one slowed the
+// long scoring passes it overlapped.)
+IDX_DEVI void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 IDX_DEVI void fence_barrier_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -313,6 +322,26 @@ __host__ __device__ constexpr uint32_t instr_desc(uint32_t ab_format, uint32_t M
            | (ab_format << 10)       // B format
            | ((N >> 3) << 17)        // N / 8
            | ((M >> 4) << 24);       // M / 16
+}
+
+
+// Launch `kern` on stream s; with pdl the launch may overlap the tail of the
+// kernel before it (the kernel must begin with pdl_wait before it touches that
+// kernel's results).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                            cudaStream_t s, bool pdl, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = pdl ? attr : nullptr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
 }  // namespace idx

@@ -77,6 +77,7 @@ struct ScoreLaunch {
     const void* k;
     int H, D;
     idx_dtype dt;
+    int pdl;  // launch overlapping the kernel before it on the stream
     ScoreArgs a;
 };
 

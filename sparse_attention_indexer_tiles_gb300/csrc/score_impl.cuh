@@ -788,9 +788,6 @@ score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     volatile int* ctl = reinterpret_cast<volatile int*>(smem + C::OFF_CTL);
     uint64_t* qfull = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR) + 2 * C::NS + 4;
     const int tid = threadIdx.x, warp = tid >> 5;
-    if (a.mode == SM_RESCAN && *(volatile int*)(a.fb_cnt + 7) == 0) return;  // none flagged
-    // a new call: the rescan counters start at 0
-    if (a.mode == SM_SAMPLE && blockIdx.x == 0 && tid < 8) a.fb_cnt[tid] = 0;
     if (tid == 0) {
         tslot[1] = 0;
         ctl[0] = 0;  // abort flag: a wait that timed out releases every later wait
@@ -798,6 +795,11 @@ score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         mbar_init(&qfull[C::QB], 1);  // pdone
         fence_barrier_init();
     }
+    // (a launch that overlaps the kernel before it waits here for its results)
+    pdl_wait();
+    if (a.mode == SM_RESCAN && *(volatile int*)(a.fb_cnt + 7) == 0) return;  // none flagged
+    // a new call: the rescan counters start at 0
+    if (a.mode == SM_SAMPLE && blockIdx.x == 0 && tid < 8) a.fb_cnt[tid] = 0;
     __syncthreads();
     auto cta_bar = [] { __syncthreads(); };
     auto nothing = [] {};

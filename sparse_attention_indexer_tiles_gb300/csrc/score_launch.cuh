@@ -94,8 +94,8 @@ cudaError_t launch_score_t(const ScoreLaunch& L, cudaStream_t s) {
         gx = a.grid_x > 0 && a.grid_x < units ? a.grid_x : units;
     }
     if (gx > 0x7fffffffll) return cudaErrorInvalidValue;
-    kern<<<(unsigned)gx, C::THREADS, C::SMEM_ALLOC, s>>>(tq, tk, tks, a);
-    return cudaGetLastError();
+    return launch_k(kern, dim3((unsigned)gx), dim3(C::THREADS), C::SMEM_ALLOC, s, L.pdl != 0, tq,
+                    tk, tks, a);
 }
 
 }  // namespace idx

@@ -590,6 +590,7 @@ template <int WARPS>
 __global__ void __launch_bounds__(WARPS * 32)
 sample_threshold_kernel(TopkRowsArgs a) {
     __shared__ uint32_t hist_all[WARPS][256];
+    pdl_wait();
     const int w = threadIdx.x >> 5;
     const int r = blockIdx.x * WARPS + w;
     if (r >= a.rows) return;  // whole warps only: nothing below syncs the block
@@ -604,6 +605,7 @@ __global__ void __launch_bounds__(kThrCtaThreads) sample_threshold_cta_kernel(To
     constexpr int THREADS = kThrCtaThreads, W = THREADS / 32;
     __shared__ uint32_t hist[W * 256];
     __shared__ uint32_t scratch[64];
+    pdl_wait();
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int r = blockIdx.x;
     SampleRow sr;
@@ -1135,6 +1137,7 @@ __global__ void __launch_bounds__(kCandThreads)
 cand_topk_kernel(CandArgs a) {
     constexpr int THREADS = kCandThreads;
     extern __shared__ __align__(16) uint32_t smem[];
+    pdl_wait();
     const CandSmem L(a.nruns, a.topk, a.cap_q);
     uint32_t* hist = smem + L.hist();
     uint32_t* scratch = smem + L.scratch();  // [0,35) scans, [40,48) results, [48,64) row state
@@ -1442,12 +1445,15 @@ cudaError_t launch_topk_rows(const TopkRowsArgs& a, cudaStream_t s) {
         constexpr int WARPS = 8;
         TopkRowsArgs b = a;
         b.split = a.row_len > kThrCtaMin ? 2 : 0;
-        sample_threshold_kernel<WARPS><<<(a.rows + WARPS - 1) / WARPS, WARPS * 32, 0, s>>>(b);
-        if (b.split) {
-            sample_threshold_cta_kernel<<<a.rows, kThrCtaThreads, 0, s>>>(b);
+        cudaError_t e = launch_k(sample_threshold_kernel<WARPS>,
+                                 dim3((unsigned)((a.rows + WARPS - 1) / WARPS)), dim3(WARPS * 32), 0,
+                                 s, a.pdl != 0, b);
+        if (e == cudaSuccess && b.split) {
+            e = launch_k(sample_threshold_cta_kernel, dim3((unsigned)a.rows), dim3(kThrCtaThreads),
+                         0, s, a.pdl != 0, b);
             count_launches(1);
         }
-        return cudaGetLastError();
+        return e;
     }
     if (a.split > 1) {
         if (a.split > kMaxSplit) return cudaErrorInvalidValue;
@@ -1494,8 +1500,8 @@ cudaError_t launch_cand_topk(const CandArgs& a, cudaStream_t s) {
     // the rescan's pass usually has no row to select: a short grid that strides
     // over the rows exits at once
     const int grid = a.fallback ? (a.rows < a.grid_limit ? a.rows : a.grid_limit) : a.rows;
-    cand_topk_kernel<<<grid, kCandThreads, sm, s>>>(a);
-    return cudaGetLastError();
+    return launch_k(cand_topk_kernel, dim3((unsigned)grid), dim3(kCandThreads), sm, s, a.pdl != 0,
+                    a);
 }
 
 }  // namespace idx

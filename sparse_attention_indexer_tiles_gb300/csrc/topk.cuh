@@ -45,6 +45,7 @@ struct TopkRowsArgs {
     int* split_cnt;        // [rows * g] candidates handed over, -1 = a run overflowed
     uint32_t* split_lb;    // [rows * g] the lower bound (order key) each block used
     int* split_ticket;     // [rows] blocks of the row done so far (zeroed by the launch)
+    int pdl;              // launch overlapping the kernel before it on the stream
     int* d_status;
     idx_stats* d_stats;
 };
@@ -66,6 +67,7 @@ struct CandArgs {
     int fallback;         // 0: main pass (flags rows), 1: rows re-emitted by the rescan
     int grid_limit;       // CTAs of the rescan's pass (they stride over the rows)
     int* out;
+    int pdl;              // launch overlapping the kernel before it on the stream
     int* d_status;
     idx_stats* d_stats;
 };
