@@ -56,8 +56,9 @@ def parse():
     p.add_argument("--route-sweep", action="store_true",
                    help="time the fused and the two-pass path over short key lengths (the "
                         "routing gate's crossover) and print one JSON line per case")
-    p.add_argument("--only", choices=["all", "fused", "topk"], default="all",
-                   help="profiling: run only the fused step or only the standalone top-k")
+    p.add_argument("--only", choices=["all", "fused", "topk", "split"], default="all",
+                   help="profiling: run only the fused step, the standalone top-k or the "
+                        "row split")
     return p.parse_args()
 
 
@@ -318,8 +319,10 @@ def main():
         return
 
     if args.only == "topk":
-        print(json.dumps(standalone_topk(idx, dev, torch.empty(256 << 20, dtype=torch.uint8,
-                                                               device=dev), pk, args)))
+        print(json.dumps(standalone_topk(idx, dev, L2Flush(dev), pk, args)))
+        return
+    if args.only == "split":
+        print(json.dumps(split_topk(idx, dev, L2Flush(dev), pk, args)))
         return
 
     # ---------------------------------------------------------------- inputs
