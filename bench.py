@@ -78,15 +78,24 @@ def peaks():
             "source": "fallback"}
 
 
-def kernel_source_hash() -> str:
-    """Hash of the CUDA sources: a recorded ncu traffic figure is only valid
-    for the sources it was taken on."""
+# The sources each recorded kernel is built from (a recorded ncu figure stays
+# valid while these are unchanged).
+KERNEL_SOURCES = {
+    "score_kernel": ["common.cuh", "plan.cuh", "radix.cuh", "score.cuh", "score_impl.cuh",
+                     "score_launch.cuh", "score_fp8.cu", "score_bf16.cu"],
+    "topk_rows_kernel": ["common.cuh", "plan.cuh", "radix.cuh", "threshold.cuh", "topk.cu",
+                         "topk.cuh"],
+}
+
+
+def kernel_source_hash(kernel: str = "score_kernel") -> str:
+    """Hash of the CUDA sources of `kernel` (its name up to the first '<'): a
+    recorded ncu traffic figure is only valid for the sources it was taken on."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "sparse_attention_indexer_tiles_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh")):
-            h.update(f.encode())
-            h.update(open(os.path.join(csrc, f), "rb").read())
+    for f in sorted(KERNEL_SOURCES[kernel.split("<")[0]]):
+        h.update(f.encode())
+        h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -100,7 +109,7 @@ def recorded_traffic(kernel: str, workload: str):
         return None
     for e in rec.get("entries", []):
         if e.get("kernel") == kernel and e.get("workload") == workload and \
-                e.get("source_hash") == kernel_source_hash():
+                e.get("source_hash") == kernel_source_hash(kernel):
             return e.get("bytes_per_launch")
     return None
 
@@ -473,6 +482,11 @@ def summary(line):
     sp = ex["split_topk"]
     out["split_topk"] = {"rows_per_s": sp["rows_per_s"], "ms": sp["ms"],
                          "hbm_frac": sp["roofline"]["frac"]}
+    mx = ex.get("mxfp4")
+    if mx:
+        out["mxfp4"] = {"pairs_per_s": mx["pairs_per_s"], "ms": mx["ms"],
+                        "whole_call_tensor_frac": mx["whole_call_tensor_frac"],
+                        "emit_tensor_frac": mx["emit_roofline"]["frac"]}
     return {"summary": out}
 
 
@@ -578,6 +592,8 @@ def secondary(idx, dev, g, inp, out, ws, flush, pk, args, fused_ms):
     res["decode"] = other_fused(idx, dev, flush, pk, args, "decode", inp=dec, with_two_pass=True)
     torch.cuda.empty_cache()
     res["tiny"] = other_fused(idx, dev, flush, pk, args, "tiny")
+    res["mxfp4"] = mxfp4_fused(idx, dev, flush, pk, args)
+    torch.cuda.empty_cache()
     res["page_table_transform"] = page_transform(idx, dev, flush, pk, out, inp)
     res["standalone_topk"] = standalone_topk(idx, dev, flush, pk, args)
     return res
@@ -710,6 +726,62 @@ def other_fused(idx, dev, flush, pk, args, name, inp=None, with_two_pass=False):
         tp["fused_over_two_pass"] = tp["total_ms"] / ms
         res["two_pass"] = tp
     return res
+
+
+def mxfp4_fused(idx, dev, flush, pk, args):
+    """idx_score_topk_mxfp4 on the fused-prefill shape with MXFP4 q/k (e2m1 +
+    e8m0 block scales): the whole call (the exact expansion to e4m3 included)
+    and its emit pass, whose MMAs run on e4m3 operands, against the fp8 peak."""
+    import torch
+    import synth
+    inp = synth.indexer_inputs(4096, 65536, 64, 128, 2048, "mxfp4", seed=2)
+    g = {n: getattr(inp, n).to(dev) for n in ("q", "q_sf", "k", "k_sf", "k_scale", "w", "ks",
+                                              "ke")}
+    out = torch.empty(inp.rows, inp.topk, dtype=torch.int32, device=dev)
+    need = int(idx.load().idx_score_topk_mxfp4_workspace(inp.rows, inp.keys, 0, inp.H, inp.D,
+                                                         inp.topk, None))
+    ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+
+    def call(ev=None):
+        o = idx.Options()
+        if ev is not None:
+            o.stage_events = ev.ptr
+        idx.idx_score_topk_mxfp4(g["q"], g["q_sf"], g["k"], g["k_sf"], g["k_scale"], g["w"],
+                                 g["ks"], g["ke"], inp.topk, out=out, ws=ws, options=o)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        call()
+    torch.cuda.synchronize()
+    reps = max(3, min(args.steps, 5))
+    evs = [idx.StageEvents(5) for _ in range(reps)]
+    ts = []
+    for e in evs:
+        flush.zero_()
+        hold_gpu()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        call(e)
+        b.record()
+        b.synchronize()
+        ts.append(a.elapsed_time(b))
+    ms = statistics.mean(ts)
+    emit_ms = statistics.mean(e.elapsed(1, 2) for e in evs)
+    pairs = inp.pairs()
+    flops = 2.0 * inp.H * inp.D * pairs
+    fp8_peak = pk["bf16_tflops"] * 2.0
+    emit_tf = flops / (emit_ms * 1e-3) / 1e12
+    return {"workload": f"mxfp4: rows={inp.rows} keys={inp.keys} H={inp.H} D={inp.D} "
+                        f"topk={inp.topk}, e2m1 + e8m0 q/k, causal ranges",
+            "ms": ms, "pairs_per_s": pairs / (ms * 1e-3),
+            "expand_ms": ms - statistics.mean(e.elapsed(0, 4) for e in evs),
+            "emit_roofline": {"bound": "tensor", "achieved": emit_tf, "peak": fp8_peak,
+                              "unit": "TFLOP/s", "frac": emit_tf / fp8_peak,
+                              "note": "MMAs on the exactly expanded e4m3 operands: fp8 peak "
+                                      "(measured bf16 x 2); the nominal fp4 dense rate is "
+                                      "twice that"},
+            "whole_call_tensor_frac": flops / (ms * 1e-3) / 1e12 / fp8_peak}
 
 
 def split_topk(idx, dev, flush, pk, args):

@@ -61,7 +61,10 @@ typedef enum {
 #define IDX_DEV_RANGE   0x2   /* a row's [ks, ke) is not inside [0, keys] or exceeds max_len */
 #define IDX_DEV_STATE   0x4   /* the exact fallback ran out of its refinement levels */
 
-typedef enum { IDX_BF16 = 1, IDX_FP8_E4M3 = 2 } idx_dtype;
+/* IDX_MXFP4 (the OCP MX format): e2m1 elements packed two per byte (element 2i in
+ * the low nibble) with one e8m0 scale per 32 consecutive elements along D; only
+ * the *_mxfp4 entry points below take it (they also take the scale arrays). */
+typedef enum { IDX_BF16 = 1, IDX_FP8_E4M3 = 2, IDX_MXFP4 = 3 } idx_dtype;
 
 /* Optional device-side counters (zero them before the call if you read them). */
 typedef struct idx_stats {
@@ -265,6 +268,48 @@ idx_status idx_score_topk_routed(const void* q, const void* k, const float* k_sc
 idx_status idx_page_table_transform(int* idx, int rows, int topk, const int* table,
                                     int table_rows, long long table_stride, const int* row_map,
                                     int page_size, const idx_options* opt, void* stream);
+
+/* ------------------------------------------------------------------------
+ * MXFP4 inputs (page "[sglang] logits를 쓰지 않는 top-k", section 1: an fp4
+ * indexer whose 128-element keys are 64 bytes).
+ *
+ * idx_mxfp4_to_e4m3 - n rows of D MXFP4 elements to e4m3, exactly.
+ *   x   [n, D/2] bytes, device, 16-byte aligned: two e2m1 elements per byte,
+ *       element 2i in the low nibble
+ *   sf  [n, D/32] bytes, device: the e8m0 scale (2^(sf - 127)) of each block of
+ *       32 consecutive elements
+ *   out [n, D] e4m3 bytes, device, 16-byte aligned
+ * An e2m1 value (0, ±0.5 ... ±6) times 2^e is an e4m3 value when e lies in
+ * [-8, 6] (the OCP recipe e = floor(log2 max|x|) - 2 gives that range for
+ * |x| in [2^-6, 2^8)); such elements are converted exactly.  Others (and the
+ * NaN scale 255) are saturated to ±448 or flushed to zero and raise
+ * IDX_DEV_RANGE.  D % 32 == 0 (IDX_EINVAL); misaligned x or out: IDX_EALIGN.
+ *
+ * idx_score_topk_mxfp4 / idx_score_materialise_mxfp4 - idx_score_topk and
+ * idx_score_materialise on MXFP4 q [rows, H, D/2] + q_sf [rows, H, D/32] and
+ * k [keys, D/2] + k_sf [keys, D/32]: q and k are expanded to e4m3 into the
+ * workspace and scored by the e4m3 tensor-core path, so the scores are those of
+ * the MXFP4 values (bit-identical to the e4m3 path on the same values).  Other
+ * arguments as there; the workspaces are the e4m3 path's plus rows*H*D +
+ * keys*D bytes (256-byte aligned regions).
+ * ------------------------------------------------------------------------ */
+idx_status idx_mxfp4_to_e4m3(const uint8_t* x, const uint8_t* sf, long long n, int D,
+                             uint8_t* out, const idx_options* opt, void* stream);
+size_t idx_score_topk_mxfp4_workspace(int rows, long long keys, long long max_len, int H,
+                                      int D, int topk, const idx_options* opt);
+idx_status idx_score_topk_mxfp4(const uint8_t* q, const uint8_t* q_sf, const uint8_t* k,
+                                const uint8_t* k_sf, const float* k_scale, const float* w,
+                                const int* ks, const int* ke, int rows, long long keys,
+                                long long max_len, int H, int D, int topk, int* out_idx,
+                                void* ws, size_t ws_bytes, const idx_options* opt,
+                                void* stream);
+size_t idx_score_materialise_mxfp4_workspace(int rows, long long keys, int H, int D);
+idx_status idx_score_materialise_mxfp4(const uint8_t* q, const uint8_t* q_sf, const uint8_t* k,
+                                       const uint8_t* k_sf, const float* k_scale,
+                                       const float* w, const int* ks, const int* ke, int rows,
+                                       long long keys, int H, int D, float* scores,
+                                       long long row_stride, void* ws, size_t ws_bytes,
+                                       const idx_options* opt, void* stream);
 
 /* Static text for a status code. */
 const char* idx_status_string(idx_status s);

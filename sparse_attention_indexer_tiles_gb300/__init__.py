@@ -9,6 +9,8 @@ Entry points (same names as the C ABI in ``include/idx.h``):
   idx_score_topk            fused score + exact top-k (no [rows, keys] logits)
   idx_topk_from_scores      exact radix top-k of given fp32 scores
   idx_score_materialise     the two-pass baseline's score pass
+  idx_score_topk_mxfp4, idx_score_materialise_mxfp4, idx_mxfp4_to_e4m3
+                            the same on MXFP4 inputs (expanded exactly to e4m3)
   idx_score_topk_workspace, idx_topk_workspace, idx_status_string
 """
 from __future__ import annotations
@@ -23,13 +25,14 @@ __all__ = [
     "idx_topk_from_scores", "idx_topk_workspace", "idx_score_materialise",
     "idx_status_string", "DTYPES", "STAT_FIELDS", "StageEvents", "idx_launch_count",
     "idx_score_topk_noalloc", "idx_page_table_transform", "idx_route_fused",
-    "idx_score_topk_routed", "idx_score_topk_routed_workspace",
+    "idx_score_topk_routed", "idx_score_topk_routed_workspace", "idx_mxfp4_to_e4m3",
+    "idx_score_topk_mxfp4", "idx_score_materialise_mxfp4",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libidx.so")
 
-IDX_BF16, IDX_FP8_E4M3 = 1, 2
+IDX_BF16, IDX_FP8_E4M3, IDX_MXFP4 = 1, 2, 3
 DTYPES = {torch.bfloat16: IDX_BF16, torch.float8_e4m3fn: IDX_FP8_E4M3}
 STAT_FIELDS = ("emit_all_rows", "overflow_rows", "short_rows", "fallback_rows", "max_count",
                "split_rows", "tie_rescan_rows", "reserved")
@@ -108,6 +111,18 @@ def load(path: str | None = None):
     lib.idx_score_topk_routed.restype = I
     lib.idx_page_table_transform.argtypes = [P, I, I, P, I, LL, P, I, P, P]
     lib.idx_page_table_transform.restype = I
+    lib.idx_mxfp4_to_e4m3.argtypes = [P, P, LL, I, P, P, P]
+    lib.idx_mxfp4_to_e4m3.restype = I
+    lib.idx_score_topk_mxfp4_workspace.argtypes = [I, LL, LL, I, I, I, P]
+    lib.idx_score_topk_mxfp4_workspace.restype = SZ
+    lib.idx_score_topk_mxfp4.argtypes = [P, P, P, P, P, P, P, P, I, LL, LL, I, I, I, P, P, SZ,
+                                         P, P]
+    lib.idx_score_topk_mxfp4.restype = I
+    lib.idx_score_materialise_mxfp4_workspace.argtypes = [I, LL, I, I]
+    lib.idx_score_materialise_mxfp4_workspace.restype = SZ
+    lib.idx_score_materialise_mxfp4.argtypes = [P, P, P, P, P, P, P, P, I, LL, I, I, P, LL, P,
+                                                SZ, P, P]
+    lib.idx_score_materialise_mxfp4.restype = I
     lib.idx_status_string.argtypes = [I]
     lib.idx_status_string.restype = ctypes.c_char_p
     lib.idx_version.argtypes = []
@@ -266,6 +281,79 @@ def idx_score_materialise(q, k, k_scale, w, ks, ke, *, out=None, row_stride: int
         _check("idx_score_materialise", load().idx_score_materialise(
             _ptr(q), _ptr(k), _ptr(k_scale), _ptr(w), _ptr(ks), _ptr(ke), rows, keys, H, D,
             DTYPES[q.dtype], _ptr(out), stride, _opt_ref(o), _stream(stream)))
+        return out
+
+
+def _mx_shapes(q, q_sf, k, k_sf):
+    """rows, H, D of MXFP4 q [rows, H, D/2] uint8 with q_sf [rows, H, D/32] and k
+    [keys, D/2] with k_sf [keys, D/32]."""
+    for t in (q, q_sf, k, k_sf):
+        if t.dtype != torch.uint8:
+            raise ValueError("MXFP4 elements and scales are uint8 tensors")
+    rows, H, half = q.shape
+    D = 2 * half
+    if q_sf.shape != (rows, H, D // 32) or k.shape[1] != half or \
+            k_sf.shape != (k.shape[0], D // 32):
+        raise ValueError("inconsistent MXFP4 shapes")
+    return rows, H, D
+
+
+def idx_mxfp4_to_e4m3(x, sf, *, out=None, options=None, stats: Stats | None = None,
+                      stream=None):
+    """MXFP4 rows x [n, D/2] + sf [n, D/32] -> e4m3 [n, D] (exact within the
+    e4m3 range, else IDX_DEV_RANGE)."""
+    dev = _dev(x, sf, out)
+    with torch.cuda.device(dev):
+        n, half = x.shape[0], x.shape[-1]
+        D = 2 * half
+        if out is None:
+            out = torch.empty(*x.shape[:-1], D, dtype=torch.float8_e4m3fn, device=x.device)
+        o = make_options(options, stats)
+        _check("idx_mxfp4_to_e4m3", load().idx_mxfp4_to_e4m3(
+            _ptr(x), _ptr(sf), x.numel() // half, D, _ptr(out), _opt_ref(o), _stream(stream)))
+        return out
+
+
+def idx_score_topk_mxfp4(q, q_sf, k, k_sf, k_scale, w, ks, ke, topk: int, *, max_len: int = 0,
+                         out=None, ws=None, options=None, stats: Stats | None = None,
+                         stream=None):
+    """idx_score_topk on MXFP4 q/k (with their e8m0 block scales)."""
+    dev = _dev(q, q_sf, k, k_sf, k_scale, w, ks, ke, out, ws)
+    with torch.cuda.device(dev):
+        rows, H, D = _mx_shapes(q, q_sf, k, k_sf)
+        keys = k.shape[0]
+        o = make_options(options, stats)
+        need = int(load().idx_score_topk_mxfp4_workspace(rows, keys, max_len, H, D, topk,
+                                                         _opt_ref(o)))
+        if out is None:
+            out = torch.empty(rows, topk, dtype=torch.int32, device=q.device)
+        if ws is None:
+            ws = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+        _check("idx_score_topk_mxfp4", load().idx_score_topk_mxfp4(
+            _ptr(q), _ptr(q_sf), _ptr(k), _ptr(k_sf), _ptr(k_scale), _ptr(w), _ptr(ks), _ptr(ke),
+            rows, keys, max_len, H, D, topk, _ptr(out), _ptr(ws), ws.numel() * ws.element_size(),
+            _opt_ref(o), _stream(stream)))
+        return out
+
+
+def idx_score_materialise_mxfp4(q, q_sf, k, k_sf, k_scale, w, ks, ke, *, out=None,
+                                row_stride: int | None = None, ws=None, options=None,
+                                stats: Stats | None = None, stream=None):
+    """idx_score_materialise on MXFP4 q/k (with their e8m0 block scales)."""
+    dev = _dev(q, q_sf, k, k_sf, k_scale, w, ks, ke, out, ws)
+    with torch.cuda.device(dev):
+        rows, H, D = _mx_shapes(q, q_sf, k, k_sf)
+        keys = k.shape[0]
+        if out is None:
+            out = torch.empty(rows, row_stride or keys, dtype=torch.float32, device=q.device)
+        need = int(load().idx_score_materialise_mxfp4_workspace(rows, keys, H, D))
+        if ws is None:
+            ws = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+        o = make_options(options, stats)
+        _check("idx_score_materialise_mxfp4", load().idx_score_materialise_mxfp4(
+            _ptr(q), _ptr(q_sf), _ptr(k), _ptr(k_sf), _ptr(k_scale), _ptr(w), _ptr(ks), _ptr(ke),
+            rows, keys, H, D, _ptr(out), out.shape[1], _ptr(ws), ws.numel() * ws.element_size(),
+            _opt_ref(o), _stream(stream)))
         return out
 
 

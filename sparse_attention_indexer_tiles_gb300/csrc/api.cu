@@ -10,6 +10,7 @@
 
 #include <cudaTypedefs.h>
 
+#include "mxfp4.cuh"
 #include "page_table.cuh"
 #include "plan.cuh"
 #include "score.cuh"
@@ -636,6 +637,114 @@ idx_status idx_page_table_transform(int* idx_out, int rows, int topk, const int*
     if (e == cudaSuccess) count_launches(1);
     record(opt, 1, s);
     return cuda_status(e);
+}
+
+
+// ---------------------------------------------------------------- MXFP4
+
+idx_status idx_mxfp4_to_e4m3(const uint8_t* x, const uint8_t* sf, long long n, int D,
+                             uint8_t* out, const idx_options* opt, void* stream) {
+    if (n < 0 || D < 32 || D % 32 != 0) return IDX_EINVAL;
+    if (n == 0) return IDX_OK;
+    if (!x || !sf || !out) return IDX_EINVAL;
+    if (!aligned(x, 16) || !aligned(out, 16)) return IDX_EALIGN;
+    if (!arch_ok()) return IDX_EUNSUPPORTED;
+    Mxfp4Args a;
+    a.x = x;
+    a.sf = sf;
+    a.n = n;
+    a.D = D;
+    a.out = out;
+    a.d_status = opt ? opt->d_status : nullptr;
+    const cudaError_t e = launch_mxfp4_to_e4m3(a, sm_count(), static_cast<cudaStream_t>(stream));
+    if (e == cudaSuccess) count_launches(1);
+    return cuda_status(e);
+}
+
+namespace {
+
+// The e4m3 copies of q and k at the front of an MXFP4 call's workspace, then
+// the e4m3 path's own workspace.
+struct Mxfp4Layout {
+    size_t q8, k8, rest, total;
+};
+
+Mxfp4Layout mxfp4_layout(int rows, long long keys, int H, int D, size_t rest_bytes) {
+    Mxfp4Layout L;
+    auto up = [](size_t b) { return (b + 255) / 256 * 256; };
+    L.q8 = 0;
+    L.k8 = up((size_t)rows * H * D);
+    L.rest = L.k8 + up((size_t)keys * D);
+    L.total = L.rest + rest_bytes;
+    return L;
+}
+
+// Expand q and k into the workspace (after the checks every MXFP4 entry point makes).
+idx_status mxfp4_expand_qk(const uint8_t* q, const uint8_t* q_sf, const uint8_t* k,
+                           const uint8_t* k_sf, int rows, long long keys, int H, int D,
+                           uint8_t* base, const Mxfp4Layout& L, const idx_options* opt,
+                           void* stream) {
+    if (!q || !q_sf || !k || !k_sf) return IDX_EINVAL;
+    idx_status st = idx_mxfp4_to_e4m3(q, q_sf, (long long)rows * H, D, base + L.q8, opt, stream);
+    if (st != IDX_OK) return st;
+    return idx_mxfp4_to_e4m3(k, k_sf, keys, D, base + L.k8, opt, stream);
+}
+
+}  // namespace
+
+size_t idx_score_topk_mxfp4_workspace(int rows, long long keys, long long max_len, int H,
+                                      int D, int topk, const idx_options* opt) {
+    if (rows <= 0) return 0;
+    const size_t rest = idx_score_topk_workspace(rows, keys, max_len, H, D, topk, IDX_FP8_E4M3, opt);
+    return mxfp4_layout(rows, keys, H, D, rest).total;
+}
+
+idx_status idx_score_topk_mxfp4(const uint8_t* q, const uint8_t* q_sf, const uint8_t* k,
+                                const uint8_t* k_sf, const float* k_scale, const float* w,
+                                const int* ks, const int* ke, int rows, long long keys,
+                                long long max_len, int H, int D, int topk, int* out_idx,
+                                void* ws, size_t ws_bytes, const idx_options* opt,
+                                void* stream) {
+    if (topk < 1) return IDX_EINVAL;
+    if (topk > kMaxTopk) return IDX_EUNSUPPORTED;
+    // the e4m3 path's checks, on the packed arrays (same alignment rules)
+    idx_status st = check_indexer_args(q, k, k_scale, w, ks, ke, rows, keys, H, D, IDX_FP8_E4M3);
+    if (st != IDX_OK || rows == 0) return st;
+    if (!out_idx) return IDX_EINVAL;
+    const size_t rest = idx_score_topk_workspace(rows, keys, max_len, H, D, topk, IDX_FP8_E4M3, opt);
+    const Mxfp4Layout L = mxfp4_layout(rows, keys, H, D, rest);
+    if (!ws || ws_bytes < L.total) return IDX_EWORKSPACE;
+    if (!aligned(ws, 256)) return IDX_EALIGN;
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    st = mxfp4_expand_qk(q, q_sf, k, k_sf, rows, keys, H, D, base, L, opt, stream);
+    if (st != IDX_OK) return st;
+    return idx_score_topk(base + L.q8, base + L.k8, k_scale, w, ks, ke, rows, keys, max_len, H, D,
+                          topk, IDX_FP8_E4M3, out_idx, base + L.rest, ws_bytes - L.rest, opt,
+                          stream);
+}
+
+size_t idx_score_materialise_mxfp4_workspace(int rows, long long keys, int H, int D) {
+    if (rows <= 0) return 0;
+    return mxfp4_layout(rows, keys, H, D, 0).total;
+}
+
+idx_status idx_score_materialise_mxfp4(const uint8_t* q, const uint8_t* q_sf, const uint8_t* k,
+                                       const uint8_t* k_sf, const float* k_scale,
+                                       const float* w, const int* ks, const int* ke, int rows,
+                                       long long keys, int H, int D, float* scores,
+                                       long long row_stride, void* ws, size_t ws_bytes,
+                                       const idx_options* opt, void* stream) {
+    idx_status st = check_indexer_args(q, k, k_scale, w, ks, ke, rows, keys, H, D, IDX_FP8_E4M3);
+    if (st != IDX_OK || rows == 0) return st;
+    if (!scores || row_stride < 1) return IDX_EINVAL;
+    const Mxfp4Layout L = mxfp4_layout(rows, keys, H, D, 0);
+    if (!ws || ws_bytes < L.total) return IDX_EWORKSPACE;
+    if (!aligned(ws, 256)) return IDX_EALIGN;
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    st = mxfp4_expand_qk(q, q_sf, k, k_sf, rows, keys, H, D, base, L, opt, stream);
+    if (st != IDX_OK) return st;
+    return idx_score_materialise(base + L.q8, base + L.k8, k_scale, w, ks, ke, rows, keys, H, D,
+                                 IDX_FP8_E4M3, scores, row_stride, opt, stream);
 }
 
 }  // extern "C"

@@ -75,6 +75,12 @@ def test_argument_checks_before_cuda(lib):
                                      100, None, None) == 0
     assert lib.idx_topk_from_scores(P, i64(10), P, P, 4, 0, P, None, 0, None, None) == 1
     assert lib.idx_topk_from_scores(P, i64(10), P, P, 4, 5000, P, None, 0, None, None) == 4
+    # MXFP4 expansion: D a multiple of 32, 16-byte aligned arrays, n = 0 a no-op
+    lib.idx_mxfp4_to_e4m3.argtypes = [ctypes.c_void_p, ctypes.c_void_p, i64, ctypes.c_int,
+                                      ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    assert lib.idx_mxfp4_to_e4m3(P, P, i64(4), 48, P, None, None) == 1
+    assert lib.idx_mxfp4_to_e4m3(ctypes.c_void_p(24), P, i64(4), 64, P, None, None) == 2
+    assert lib.idx_mxfp4_to_e4m3(None, None, i64(0), 64, None, None, None) == 0
 
 
 def test_options_struct_layout():
@@ -174,6 +180,12 @@ def test_bindings_refuse_host_tensors(lib):
         lambda: pkg.idx_topk_from_scores(torch.zeros(4, 100), ks, ke, 16),
         lambda: pkg.idx_page_table_transform(torch.zeros(4, 16, dtype=torch.int32),
                                              torch.zeros(4, 2, dtype=torch.int32)),
+        lambda: pkg.idx_mxfp4_to_e4m3(torch.zeros(4, 32, dtype=torch.uint8),
+                                      torch.zeros(4, 2, dtype=torch.uint8)),
+        lambda: pkg.idx_score_topk_mxfp4(torch.zeros(4, 8, 32, dtype=torch.uint8),
+                                         torch.zeros(4, 8, 2, dtype=torch.uint8),
+                                         torch.zeros(100, 32, dtype=torch.uint8),
+                                         torch.zeros(100, 2, dtype=torch.uint8), sc, w, ks, ke, 16),
     ]
     before = pkg.idx_launch_count()
     for call in calls:
