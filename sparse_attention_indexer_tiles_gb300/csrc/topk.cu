@@ -210,9 +210,9 @@ IDX_DEVI void ordered_output(const RowView& v, Threshold th, uint32_t k, int* ou
 // ------------------------------------------------------- one-pass path
 //
 // A row is streamed from HBM once.  A lower bound L on the threshold is
-// estimated from the 12-bit histogram of a 4096-value sample (aiming at about
-// 2 k keys >= L): the first 256 values of each warp's slice, which the filter
-// loads first anyway.  Every key >= L is then appended to its warp's run in
+// estimated from a sample of up to 8192 values (aiming at about 1.5 k keys >=
+// L): the first 512 values of each warp's slice, which the filter loads first
+// anyway.  Every key >= L is then appended to its warp's run in
 // shared memory, and the top digits of the appended keys are counted on the
 // way (level 0 of the refinement).  Warp w owns the contiguous slice w of the row and appends in index
 // order, so the runs, taken in warp order, list the candidates in ascending
@@ -222,7 +222,6 @@ IDX_DEVI void ordered_output(const RowView& v, Threshold th, uint32_t k, int* ou
 // above, which is exact for any input.
 
 constexpr int kRunCap = 512;       // candidates per warp run
-constexpr int kPrefix = 4096;      // values that estimate L
 
 template <int THREADS>
 struct StreamSmem {
@@ -234,65 +233,139 @@ struct StreamSmem {
         (kHistBins + 64 + 3 * W + 2 * (size_t)RUN_WORDS) * sizeof(uint32_t);
 };
 
-// One step of a warp's filter: lane `lane` holds the four values of float4
-// slot sl; every value >= L (key order; Lf is the float of L) is appended to
-// the warp's run in index order.  With HIST the 12-bit top digit of every hit
-// is counted in hist as well (level 0 of the refinement over the runs).
-template <bool HIST>
-IDX_DEVI void filter_step(const float4 f, int sl, bool interior, int s1, int n, int off,
-                          uint32_t L, float Lf, uint32_t lt, uint32_t& cnt, uint32_t* mk,
-                          uint32_t* mi, uint32_t* hist) {
-    const float e[4] = {f.x, f.y, f.z, f.w};
-    bool h[4];
+// One step of a warp's filter over the 32 · UNROLL float4 slots [base, base +
+// 32 · UNROLL) of its slice, lane l holding slots base + 32 u + l (u < UNROLL:
+// coalesced loads), so the step's index order is slot row u, then lane, then
+// component: every value >= L (key order; Lf is the float of L; L = 0 takes
+// every value) is appended to the warp's run in index order.  The step has two
+// halves.  hit_mask forms the lane's 32-bit hit mask (bit 4 u + c) from the
+// values in registers; after it the registers are free, so the caller issues
+// the next step's loads before append_hits, which packs the lane's eight
+// per-row hit counts into two words of 8-bit fields; two warp scans of those
+// words give every lane its place in every row at once.  Each lane then
+// appends only its own hits, re-reading their values (L1 hits, two loads in
+// flight at a time): the cross-lane work is paid once per 32 · UNROLL · 4
+// values.  With HIST every hit is counted in hist as well: rel = false, by its
+// 12-bit top digit (level 0 of the refinement over the runs); rel = true, in
+// bin min((key - hb) >> 12, 4095) of a histogram relative to hb, a key at or
+// below every hit.
+template <int UNROLL>
+IDX_DEVI uint32_t hit_mask(const float4 (&f)[UNROLL], int base, bool interior, int s1, int n,
+                           int off, uint32_t L, float Lf, int lane) {
+    static_assert(UNROLL == 8, "eight rows of 4 values: one 32-bit mask, two count words");
+    uint32_t m = 0u;
     if (interior) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) h[c] = e[c] >= Lf;
+        for (int u = 0; u < UNROLL; ++u) {
+            m |= (f[u].x >= Lf ? 1u : 0u) << (4 * u);
+            m |= (f[u].y >= Lf ? 1u : 0u) << (4 * u + 1);
+            m |= (f[u].z >= Lf ? 1u : 0u) << (4 * u + 2);
+            m |= (f[u].w >= Lf ? 1u : 0u) << (4 * u + 3);
+        }
     } else {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const int p = 4 * sl + c - off;
-            h[c] = sl < s1 && p >= 0 && p < n && (L == 0u || e[c] >= Lf);
-        }
-    }
-    const uint32_t hits = (h[0] ? 1u : 0u) | (h[1] ? 2u : 0u) | (h[2] ? 4u : 0u) |
-                          (h[3] ? 8u : 0u);
-    const uint32_t any = __ballot_sync(0xffffffffu, hits != 0u);
-    if (any == 0u) return;
-    if (!__any_sync(0xffffffffu, (hits & (hits - 1u)) != 0u)) {
-        // at most one hit per lane: its place is the number of lower lanes with a hit
-        if (hits) {
-            const uint32_t pos = cnt + __popc(any & lt);
-            const int c = __ffs(hits) - 1;
-            const uint32_t key = fkey(c == 0 ? e[0] : c == 1 ? e[1] : c == 2 ? e[2] : e[3]);
-            if (pos < (uint32_t)kRunCap) {
-                mk[pos] = key;
-                mi[pos] = static_cast<uint32_t>(4 * sl + c - off);
+        for (int u = 0; u < UNROLL; ++u) {
+            const int sl = base + 32 * u + lane;
+            const float e[4] = {f[u].x, f[u].y, f[u].z, f[u].w};
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int p = 4 * sl + c - off;
+                const bool h = sl < s1 && p >= 0 && p < n && (L == 0u || e[c] >= Lf);
+                m |= (h ? 1u : 0u) << (4 * u + c);
             }
-            if (HIST) atomicAdd(&hist[key >> 20], 1u);
         }
-        cnt += __popc(any);
-        return;
     }
-    // some lane holds several hits: one ballot per lane component; a hit's
-    // place is the number of hits in lower lanes plus those of lower
-    // components in its own lane
-    const uint32_t b0 = __ballot_sync(0xffffffffu, h[0]);
-    const uint32_t b1 = __ballot_sync(0xffffffffu, h[1]);
-    const uint32_t b2 = __ballot_sync(0xffffffffu, h[2]);
-    const uint32_t b3 = __ballot_sync(0xffffffffu, h[3]);
-    uint32_t pos = cnt + __popc(b0 & lt) + __popc(b1 & lt) + __popc(b2 & lt) + __popc(b3 & lt);
-    cnt += __popc(b0) + __popc(b1) + __popc(b2) + __popc(b3);
-    uint32_t rest = hits;
-    while (rest) {
-        const int c = __ffs(rest) - 1;
-        const uint32_t key = fkey(c == 0 ? e[0] : c == 1 ? e[1] : c == 2 ? e[2] : e[3]);
+    return m;
+}
+
+template <int UNROLL, bool HIST>
+IDX_DEVI void append_hits(const RowView& v, uint32_t m, int base, int off, int lane,
+                          uint32_t& cnt, uint32_t* mk, uint32_t* mi, uint32_t* hist,
+                          uint32_t hb = 0u, bool rel = false) {
+    if (!__any_sync(0xffffffffu, m != 0u)) return;
+    // per-row hit counts, four 8-bit fields per word (a row's warp total <= 128)
+    uint32_t w0 = 0u, w1 = 0u;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        w0 |= (uint32_t)__popc((m >> (4 * u)) & 15u) << (8 * u);
+        w1 |= (uint32_t)__popc((m >> (4 * u + 16)) & 15u) << (8 * u);
+    }
+    uint32_t i0 = w0, i1 = w1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t0 = __shfl_up_sync(0xffffffffu, i0, o);
+        const uint32_t t1 = __shfl_up_sync(0xffffffffu, i1, o);
+        if (lane >= o) {
+            i0 += t0;
+            i1 += t1;
+        }
+    }
+    const uint32_t t0 = __shfl_sync(0xffffffffu, i0, 31), t1 = __shfl_sync(0xffffffffu, i1, 31);
+    const uint32_t e0 = i0 - w0, e1 = i1 - w1;  // lanes below, per row
+    // where row u starts in the run: cnt + the totals of rows 0 .. u - 1
+    const uint32_t r1 = t0 & 0xffu, r2 = r1 + ((t0 >> 8) & 0xffu), r3 = r2 + ((t0 >> 16) & 0xffu),
+                   r4 = r3 + (t0 >> 24);
+    const uint32_t r5 = r4 + (t1 & 0xffu), r6 = r5 + ((t1 >> 8) & 0xffu),
+                   r7 = r6 + ((t1 >> 16) & 0xffu), r8 = r7 + (t1 >> 24);
+    const uint32_t rs[UNROLL] = {0u, r1, r2, r3, r4, r5, r6, r7};
+    const float* vals = reinterpret_cast<const float*>(v.base);
+    const uint32_t m0 = m;  // the lane's hits (m loses them one by one below)
+    // run position and value address of hit bit i
+    auto place = [&](int i, uint32_t* pos) {
+        const int u = i >> 2, c = i & 3;
+        const uint32_t below = u < 4 ? (e0 >> (8 * u)) & 0xffu : (e1 >> (8 * (u - 4))) & 0xffu;
+        uint32_t start = 0u;
+#pragma unroll
+        for (int j = 1; j < UNROLL; ++j) start = u == j ? rs[j] : start;
+        *pos = cnt + start + below + (uint32_t)__popc((m0 >> (4 * u)) & ((1u << c) - 1u));
+        return 4 * (base + 32 * u + lane) + c;  // float offset from v.base
+    };
+    auto put = [&](uint32_t pos, int e, float x) {
+        const uint32_t key = fkey(x);
         if (pos < (uint32_t)kRunCap) {
             mk[pos] = key;
-            mi[pos] = static_cast<uint32_t>(4 * sl + c - off);
+            mi[pos] = static_cast<uint32_t>(e - off);
         }
-        if (HIST) atomicAdd(&hist[key >> 20], 1u);
-        ++pos;
-        rest &= rest - 1u;
+        if (HIST) {
+            const uint32_t d = (key - hb) >> 12;
+            atomicAdd(&hist[rel ? (d < (uint32_t)kHistBins ? d : (uint32_t)kHistBins - 1u)
+                                : key >> 20],
+                      1u);
+        }
+    };
+    while (m) {
+        // two hits per round, both loads in flight before either value is used
+        const int i0 = __ffs(m) - 1;
+        m &= m - 1u;
+        const bool two = m != 0u;
+        const int i1 = two ? __ffs(m) - 1 : i0;
+        if (two) m &= m - 1u;
+        uint32_t p0, p1;
+        const int a0 = place(i0, &p0), a1 = place(i1, &p1);
+        const float x0 = __ldg(vals + a0), x1 = __ldg(vals + a1);
+        put(p0, a0, x0);
+        if (two) put(p1, a1, x1);
+    }
+    cnt += r8;
+}
+
+// Both halves of a step on values already in registers.
+template <int UNROLL, bool HIST>
+IDX_DEVI void filter_block(const RowView& v, const float4 (&f)[UNROLL], int base, bool interior,
+                           int s1, int n, int off, uint32_t L, float Lf, int lane, uint32_t& cnt,
+                           uint32_t* mk, uint32_t* mi, uint32_t* hist) {
+    const uint32_t m = hit_mask<UNROLL>(f, base, interior, s1, n, off, L, Lf, lane);
+    append_hits<UNROLL, HIST>(v, m, base, off, lane, cnt, mk, mi, hist);
+}
+
+// The UNROLL float4 slots of lane `lane` in one step of a warp's part: slots
+// base + 32 u + lane (coalesced; see filter_block).
+template <int UNROLL>
+IDX_DEVI void load_step(const RowView& v, int base, int s1, int lane, float4 (&f)[UNROLL]) {
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) {
+        const int sl = base + 32 * u + lane;
+        f[u] = sl < s1 ? ldg4(v.base + sl) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 }
 
@@ -317,63 +390,65 @@ IDX_DEVI void stream_collect(const RowView& v, uint32_t L, uint32_t* rkey, uint3
     int s0, s1;
     warp_slice<THREADS>(v, w, &s0, &s1);
     const float Lf = key_floor_float(L);
-    const uint32_t lt = (1u << lane) - 1u;
     uint32_t* mk = rkey + w * kRunCap;
     uint32_t* mi = ridx + w * kRunCap;
     uint32_t cnt = 0;
+    float4 f[UNROLL];
+    load_step<UNROLL>(v, s0, s1, lane, f);
     for (int base = s0; base < s1; base += 32 * UNROLL) {
-        float4 f[UNROLL];
-#pragma unroll
-        for (int u = 0; u < UNROLL; ++u) {
-            const int sl = base + u * 32 + lane;
-            f[u] = sl < s1 ? ldg4(v.base + sl) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
+        const int nb = base + 32 * UNROLL;
         // every slot of this step holds 4 visible values (warp-uniform)
-        const bool interior = base >= 1 && base + 32 * UNROLL <= s1 && base + 32 * UNROLL < nvec;
-#pragma unroll
-        for (int u = 0; u < UNROLL; ++u)
-            filter_step<HIST>(f[u], base + u * 32 + lane, interior, s1, n, off, L, Lf, lt, cnt,
-                              mk, mi, hist);
+        const bool interior = base >= 1 && nb <= s1 && nb < nvec;
+        const uint32_t m = hit_mask<UNROLL>(f, base, interior, s1, n, off, L, Lf, lane);
+        if (nb < s1) load_step<UNROLL>(v, nb, s1, lane, f);  // in flight during the append
+        append_hits<UNROLL, HIST>(v, m, base, off, lane, cnt, mk, mi, hist);
     }
     if (lane == 0) rcnt[w] = cnt;
 }
 
 // The one-pass collection of a whole row by one CTA, lower bound included.
-// L is the lower edge of the 12-bit bin that holds about the 2 k P / n-th
-// largest of a sample of P values: the first two float4 slots of every lane
-// in the first step of every warp's slice (P = 4096 for 512 threads), values
-// the filter loads anyway.  hist leaves holding the top digits of the hits.
+// The sample is the first SAMPLE float4 slots of every lane in the first step
+// of every warp's slice (P <= 8192 values for 512 threads), values the filter
+// loads anyway.  With tg = ceil(3 k P / (2 n)), L is the 20-bit floor of the
+// sample's tg-th largest order key: the 12-bit digit that holds it, then the
+// next 8 bits among the sample keys of that digit.  The number of keys >= L is
+// then about 1.5 k; it falls below k only when tg or more sample keys exceed
+// the row's k-th largest, a binomial count whose mean is 2 tg / 3 (for n =
+// 131072: 192 against a mean of 128, 5.7 standard deviations).  A miss costs
+// time only (the row takes the exact multi-pass path).  hist leaves holding
+// the histogram of the hits relative to the returned key B (bins of 4096 keys
+// from B up, the last bin open), B being the order key of the float bound
+// (every hit has key >= B; a bound of +0 admits -0, whose key is one less).
 template <int THREADS, int UNROLL>
-IDX_DEVI void stream_collect_estimate(const RowView& v, uint32_t k, uint32_t* hist,
+IDX_DEVI uint32_t stream_collect_estimate(const RowView& v, uint32_t k, uint32_t* hist,
                                       uint32_t* scratch, uint32_t* rkey, uint32_t* ridx,
                                       uint32_t* rcnt) {
-    constexpr int SAMPLE = 2;  // float4 slots per lane in the sample
+    constexpr int SAMPLE = 4;  // float4 slots per lane in the sample
     static_assert(UNROLL >= SAMPLE, "the sample comes from the first step");
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int nvec = (int)v.nvec, n = (int)v.n, off = v.off;
     int s0, s1;
     warp_slice<THREADS>(v, w, &s0, &s1);
-    const uint32_t lt = (1u << lane) - 1u;
     uint32_t* mk = rkey + w * kRunCap;
     uint32_t* mi = ridx + w * kRunCap;
     float4 f[UNROLL];
-#pragma unroll
-    for (int u = 0; u < UNROLL; ++u) {
-        const int sl = s0 + u * 32 + lane;
-        f[u] = sl < s1 ? ldg4(v.base + sl) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
+    load_step<UNROLL>(v, s0, s1, lane, f);
     zero_shared<THREADS>(hist, kHistBins);
     if (threadIdx.x == 0) scratch[44] = 0u;
     __syncthreads();
+    // in_sample(u, c): slot s0 + 32 u + lane holds visible value c
+    auto in_sample = [&](int u, int c) {
+        const int sl = s0 + 32 * u + lane;
+        const int p = 4 * sl + c - off;
+        return sl < s1 && p >= 0 && p < n;
+    };
     uint32_t ns = 0;
 #pragma unroll
     for (int u = 0; u < SAMPLE; ++u) {
-        const int sl = s0 + u * 32 + lane;
         const float e[4] = {f[u].x, f[u].y, f[u].z, f[u].w};
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-            const int p = 4 * sl + c - off;
-            if (sl < s1 && p >= 0 && p < n) {
+            if (in_sample(u, c)) {
                 atomicAdd(&hist[fkey(e[c]) >> 20], 1u);
                 ++ns;
             }
@@ -383,43 +458,52 @@ IDX_DEVI void stream_collect_estimate(const RowView& v, uint32_t k, uint32_t* hi
     if (lane == 0) atomicAdd(&scratch[44], ns);
     __syncthreads();
     const uint32_t P = scratch[44];
-    // ceil(2 k P / n) in integers: 2 k P < 2^25 and n < 2^31, so nothing wraps
-    uint32_t tg = (2u * k * P + (uint32_t)n - 1u) / (uint32_t)n;
-    tg = tg < 1u ? 1u : tg > P ? P : tg;
-    const uint32_t L = pick_digit<THREADS>(hist, kHistBins, tg, scratch).digit << 20;
+    unsigned long long tg64 = (3ull * k * P + 2ull * (uint32_t)n - 1ull) / (2ull * (uint32_t)n);
+    const uint32_t tg = tg64 < 1ull ? 1u : tg64 > P ? P : (uint32_t)tg64;
+    const DigitPick d0 = pick_digit<THREADS>(hist, kHistBins, tg, scratch);
+    // the next 8 bits of the sample keys in digit d0 (pick_digit ends on a barrier)
+    zero_shared<THREADS>(hist, 256);
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < SAMPLE; ++u) {
+        const float e[4] = {f[u].x, f[u].y, f[u].z, f[u].w};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const uint32_t key = fkey(e[c]);
+            if (in_sample(u, c) && (key >> 20) == d0.digit) atomicAdd(&hist[(key >> 12) & 0xffu], 1u);
+        }
+    }
+    __syncthreads();
+    const DigitPick d1 = pick_digit<THREADS>(hist, 256, tg - d0.above, scratch);
+    const uint32_t L = (d0.digit << 20) | (d1.digit << 12);
     zero_shared<THREADS>(hist, kHistBins);
     __syncthreads();
     const float Lf = key_floor_float(L);
+    const uint32_t B = Lf == 0.f ? 0x7fffffffu : fkey(Lf);
     uint32_t cnt = 0;
     for (int base = s0; base < s1; base += 32 * UNROLL) {
-        if (base != s0) {
-#pragma unroll
-            for (int u = 0; u < UNROLL; ++u) {
-                const int sl = base + u * 32 + lane;
-                f[u] = sl < s1 ? ldg4(v.base + sl) : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-        }
-        const bool interior = base >= 1 && base + 32 * UNROLL <= s1 && base + 32 * UNROLL < nvec;
-#pragma unroll
-        for (int u = 0; u < UNROLL; ++u)
-            filter_step<true>(f[u], base + u * 32 + lane, interior, s1, n, off, L, Lf, lt, cnt,
-                              mk, mi, hist);
+        const int nb = base + 32 * UNROLL;
+        const bool interior = base >= 1 && nb <= s1 && nb < nvec;
+        const uint32_t m = hit_mask<UNROLL>(f, base, interior, s1, n, off, L, Lf, lane);
+        if (nb < s1) load_step<UNROLL>(v, nb, s1, lane, f);  // in flight during the append
+        append_hits<UNROLL, true>(v, m, base, off, lane, cnt, mk, mi, hist, B, true);
     }
     if (lane == 0) rcnt[w] = cnt;
+    return B;
 }
 
-// Exact threshold of the k largest keys held in the warp runs.
-// hist holds the level-0 histogram of the runs on entry (built while they
-// were collected).
+// Exact threshold of the k largest keys held in the warp runs, by the three
+// key levels.  With lev0_ready hist holds the level-0 histogram of the runs on
+// entry (built while they were collected); otherwise it is built here.
 template <int THREADS>
 IDX_DEVI Threshold refine_runs(const uint32_t* rkey, const uint32_t* rcnt, uint32_t k,
-                               uint32_t* hist, uint32_t* scratch) {
+                               uint32_t* hist, uint32_t* scratch, bool lev0_ready) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const uint32_t cnt = rcnt[w];
     const uint32_t* mk = rkey + w * kRunCap;
     uint32_t prefix = 0, need = k;
     for (int lev = 0; lev <= 2; ++lev) {
-        if (lev > 0) {
+        if (lev > 0 || !lev0_ready) {
             zero_shared<THREADS>(hist, kHistBins);
             __syncthreads();
             for (uint32_t i = lane; i < cnt; i += 32) {
@@ -435,31 +519,101 @@ IDX_DEVI Threshold refine_runs(const uint32_t* rkey, const uint32_t* rcnt, uint3
     return {prefix, need};
 }
 
+// Exact threshold of the k largest keys held in the warp runs, from hist, the
+// histogram of the run keys relative to B (bin min((key - B) >> 12, 4095),
+// every key >= B) built while they were collected.  The bin that holds the
+// k-th largest key gives T's top bits; one pass over the runs then takes the
+// least and the largest key of that bin and counts, per warp, the keys above
+// the bin and in it.  When the bin holds a single key value (always for
+// scores on the bf16 grid, whose low 16 bits are constant) that value is T
+// and the per-warp counts are those of keys > T and == T, left in wsum for the
+// output (*counted); otherwise the bin's low 12 bits are resolved by one more
+// histogram.  Returns false when the k-th largest key lies in the open last
+// bin (the runs then take the three-level refinement).
+template <int THREADS>
+IDX_DEVI bool refine_runs_rel(const uint32_t* rkey, const uint32_t* rcnt, uint32_t k,
+                              uint32_t B, uint32_t* hist, uint32_t* scratch, uint32_t* wsum,
+                              Threshold* th, bool* counted) {
+    constexpr int W = THREADS / 32;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const uint32_t cnt = rcnt[w];
+    const uint32_t* mk = rkey + w * kRunCap;
+    if (threadIdx.x == 0) {
+        scratch[48] = 0xffffffffu;  // least in-bin offset
+        scratch[49] = 0u;           // largest in-bin offset
+    }
+    __syncthreads();
+    const DigitPick pk = pick_digit<THREADS>(hist, kHistBins, k, scratch);
+    if (pk.digit == (uint32_t)kHistBins - 1u) return false;
+    const uint32_t lo = B + (pk.digit << 12);  // the bin holds keys lo .. lo + 4095
+    uint32_t mn = 0xffffffffu, mx = 0u, na = 0u, nt = 0u;
+    for (uint32_t i = lane; i < cnt; i += 32) {
+        const uint32_t key = mk[i], d = key - lo;
+        if (d < 4096u) {
+            mn = min(mn, d);
+            mx = max(mx, d);
+            ++nt;
+        } else {
+            na += key > lo;
+        }
+    }
+    mn = __reduce_min_sync(0xffffffffu, mn);
+    mx = __reduce_max_sync(0xffffffffu, mx);
+    na = __reduce_add_sync(0xffffffffu, na);
+    nt = __reduce_add_sync(0xffffffffu, nt);
+    if (lane == 0) {
+        wsum[w] = na;
+        wsum[W + w] = nt;
+        if (nt) {
+            atomicMin(&scratch[48], mn);
+            atomicMax(&scratch[49], mx);
+        }
+    }
+    __syncthreads();
+    const uint32_t need = k - pk.above;
+    if (scratch[48] == scratch[49]) {
+        *th = {lo + scratch[48], need};
+        *counted = true;
+        return true;
+    }
+    zero_shared<THREADS>(hist, kHistBins);
+    __syncthreads();
+    for (uint32_t i = lane; i < cnt; i += 32) {
+        const uint32_t d = mk[i] - lo;
+        if (d < 4096u) atomicAdd(&hist[d], 1u);
+    }
+    __syncthreads();
+    const DigitPick p2 = pick_digit<THREADS>(hist, kHistBins, need, scratch);
+    *th = {lo + p2.digit, need - p2.above};
+    *counted = false;
+    return true;
+}
+
 // Ordered output from the runs: key > T, plus the first `need` keys == T.
+// With counted, wsum already holds every warp's counts of keys > T and == T.
 template <int THREADS>
 IDX_DEVI void ordered_output_runs(const uint32_t* rkey, const uint32_t* ridx,
                                   const uint32_t* rcnt, uint32_t* wsum, Threshold th,
-                                  uint32_t k, int* out) {
+                                  uint32_t k, int* out, bool counted) {
     constexpr int W = THREADS / 32;
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const uint32_t cnt = rcnt[w];
     const uint32_t* mk = rkey + w * kRunCap;
     const uint32_t* mi = ridx + w * kRunCap;
-    uint32_t na = 0, nt = 0;
-    for (uint32_t i = lane; i < cnt; i += 32) {
-        na += mk[i] > th.key;
-        nt += mk[i] == th.key;
+    if (!counted) {
+        uint32_t na = 0, nt = 0;
+        for (uint32_t i = lane; i < cnt; i += 32) {
+            na += mk[i] > th.key;
+            nt += mk[i] == th.key;
+        }
+        na = __reduce_add_sync(0xffffffffu, na);
+        nt = __reduce_add_sync(0xffffffffu, nt);
+        if (lane == 0) {
+            wsum[w] = na;
+            wsum[W + w] = nt;
+        }
+        __syncthreads();
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        na += __shfl_xor_sync(0xffffffffu, na, o);
-        nt += __shfl_xor_sync(0xffffffffu, nt, o);
-    }
-    if (lane == 0) {
-        wsum[w] = na;
-        wsum[W + w] = nt;
-    }
-    __syncthreads();
     uint32_t a_run = 0, t_run = 0;
     for (int j = 0; j < w; ++j) {
         a_run += wsum[j];
@@ -529,8 +683,10 @@ topk_rows_kernel(TopkRowsArgs a) {
 
     // a lower bound L of the threshold, or L = 0 (every key) when the runs hold the row
     const long long per_warp = 4 * ((v.nvec + W - 1) / W);
-    if (per_warp > kRunCap) {
-        stream_collect_estimate<THREADS, UNROLL>(v, k, hist, scratch, rkey, ridx, rcnt);
+    const bool rel = per_warp > kRunCap;  // hist relative to B (else level 0 by absolute digit)
+    uint32_t B = 0u;
+    if (rel) {
+        B = stream_collect_estimate<THREADS, UNROLL>(v, k, hist, scratch, rkey, ridx, rcnt);
     } else {
         zero_shared<THREADS>(hist, kHistBins);
         __syncthreads();
@@ -544,9 +700,11 @@ topk_rows_kernel(TopkRowsArgs a) {
         fits = fits && rcnt[j] <= (uint32_t)kRunCap;
     }
     Threshold th;
-    bool runs_ok = fits && total >= k;
+    bool counted = false;
+    const bool runs_ok = fits && total >= k;
     if (runs_ok) {
-        th = refine_runs<THREADS>(rkey, rcnt, k, hist, scratch);
+        if (!rel || !refine_runs_rel<THREADS>(rkey, rcnt, k, B, hist, scratch, wsum, &th, &counted))
+            th = refine_runs<THREADS>(rkey, rcnt, k, hist, scratch, !rel);
     } else {
         // the estimate missed: exact multi-pass path over the row
         __syncthreads();
@@ -557,7 +715,7 @@ topk_rows_kernel(TopkRowsArgs a) {
 
     int* out = a.out + (long long)r * a.topk;
     if (runs_ok)
-        ordered_output_runs<THREADS>(rkey, ridx, rcnt, wsum, th, k, out);
+        ordered_output_runs<THREADS>(rkey, ridx, rcnt, wsum, th, k, out, counted);
     else
         ordered_output<THREADS>(v, th, k, out, scratch);
 }
@@ -694,16 +852,6 @@ struct SplitSmem {
     static constexpr size_t BYTES = COLLECT > MERGE ? COLLECT : MERGE;
 };
 
-// The UNROLL float4 slots of one step of a warp's part, from slot `base`.
-template <int UNROLL>
-IDX_DEVI void load_step(const RowView& v, int base, int s1, int lane, float4 (&f)[UNROLL]) {
-#pragma unroll
-    for (int u = 0; u < UNROLL; ++u) {
-        const int sl = base + u * 32 + lane;
-        f[u] = sl < s1 ? ldg4(v.base + sl) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-}
-
 // Ordered compaction of cnt keys held in index order in shared memory: key >
 // T, plus the first `need` keys equal to T.  Warp w takes the w-th contiguous
 // chunk; one count pass, one synchronisation for the chunk offsets, then each
@@ -811,7 +959,7 @@ topk_split_kernel(TopkRowsArgs a) {
         uint32_t ns = 0;
 #pragma unroll
         for (int u = 0; u < SAMPLE; ++u) {
-            const int sl = s0 + u * 32 + lane;
+            const int sl = s0 + 32 * u + lane;
             const float e[4] = {f[u].x, f[u].y, f[u].z, f[u].w};
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
@@ -835,17 +983,14 @@ topk_split_kernel(TopkRowsArgs a) {
     {
         const int nvec = (int)sv.nvec, nn = (int)sv.n, off = sv.off;
         const float Lf = key_floor_float(L);
-        const uint32_t lt = (1u << lane) - 1u;
         uint32_t* mk = rkey + w * kRunCap;
         uint32_t* mi = ridx + w * kRunCap;
         uint32_t cnt = 0;
         for (int base = s0; base < s1; base += STEP) {
             const int nb = base + STEP;
             const bool interior = base >= 1 && nb <= s1 && nb < nvec;
-#pragma unroll
-            for (int u = 0; u < UNROLL; ++u)
-                filter_step<false>(f[u], base + u * 32 + lane, interior, s1, nn, off, L, Lf, lt,
-                                   cnt, mk, mi, nullptr);
+            filter_block<UNROLL, false>(sv, f, base, interior, s1, nn, off, L, Lf, lane, cnt, mk,
+                                        mi, nullptr);
 #pragma unroll
             for (int u = 0; u < UNROLL; ++u) f[u] = nf[u];
             if (nb + STEP < s1) load_step<UNROLL>(sv, nb + STEP, s1, lane, nf);

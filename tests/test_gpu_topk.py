@@ -101,6 +101,38 @@ def test_massive_ties_take_the_rescan(idx):
     assert st["tie_rescan_rows"] >= 3 and st["status"] == 0
 
 
+def test_one_pass_refinement_paths(idx):
+    """Rows long enough for the sampled lower bound (more than 512 values per
+    warp), one per branch of the refinement over the collected candidates:
+    fp32 scores (the threshold bin holds several keys: a second histogram),
+    bf16-grid scores (one key per bin), k planted values far above the rest
+    (the boundary lands in the open last bin: the three-level refinement), a
+    threshold among +0 and -0 (the float bound +0 admits -0), and an ascending
+    row (the sample misses: the exact multi-pass path)."""
+    n, topk = 40000, 1500
+    g = torch.Generator().manual_seed(27)
+    rows = [torch.randn(n, generator=g),
+            (torch.randn(n, generator=g) * 0.05).to(torch.bfloat16).float()]
+    planted = torch.randn(n, generator=g)
+    pos = torch.randperm(n, generator=g)[:topk]
+    planted[pos] = 100.0 + torch.arange(topk, dtype=torch.float32) * 1e-3
+    rows.append(planted)
+    z = -torch.rand(n, generator=g) - 0.5  # negative bulk
+    perm = torch.randperm(n, generator=g)
+    z[perm[:1000]] = torch.rand(1000, generator=g) + 0.5  # 1000 positives
+    z[perm[1000:2000]] = 0.0
+    z[perm[2000:3000]] = -0.0
+    rows.append(z)
+    rows.append(torch.arange(n, dtype=torch.float32))
+    S = torch.stack(rows)
+    R = S.shape[0]
+    ks = torch.zeros(R, dtype=torch.int32)
+    ke = torch.full((R,), n, dtype=torch.int32)
+    got = gpu_topk(idx, S, ks, ke, topk)
+    ref = oracle.topk_from_scores(S, ks, ke, topk)
+    assert np.array_equal(got, ref)
+
+
 def test_extreme_values(idx):
     g = torch.Generator().manual_seed(25)
     S = torch.randn(4, 7000, generator=g) * 1e30
