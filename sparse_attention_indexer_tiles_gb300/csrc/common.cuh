@@ -43,6 +43,14 @@ IDX_DEVI uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// 16-byte asynchronous global -> shared copy (L2 only), and the wait for
+// every copy this thread issued.
+IDX_DEVI void cp_async16(void* smem_dst, const void* gsrc) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gsrc)
+                 : "memory");
+}
+IDX_DEVI void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 IDX_DEVI void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
                  : "memory");

@@ -679,20 +679,24 @@ IDX_DEVI void score_pass(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
             } else if (mode == SM_EMIT && (t0 + i) * C::M >= all_lo &&
                        (t0 + i + 1) * C::M <= all_hi) {
                 // SM_EMIT on a tile every active row sees whole: the rule is
-                // s >= T_r (rows that take no part have T = +inf).  Branch
-                // free: a lane's place in the run is the number of hits of
-                // lower lanes (earlier keys).
+                // s >= T_r (rows that take no part have T = +inf).  A lane's
+                // place in the run is the number of hits of lower lanes
+                // (earlier keys); a row whose 32 keys hold no hit (most of
+                // them: about 1.5 topk candidates per row) costs one vote.
 #pragma unroll
                 for (int j = 0; j < C::RG; ++j) {
                     const float thr = HOIST ? e_thr[HOIST ? j : 0]
                                             : __int_as_float(row_word(j, MW_THRF));
                     const bool hit = sc[j] >= thr;
                     const uint32_t A = __ballot_sync(0xffffffffu, hit);
-                    const int pos = cnt[j] + __popc(A & lt);
-                    if (hit && pos < a.cap_q)
-                        pr[j * rstride + pos] = make_int2(
-                            __float_as_int(sc[j]), kidx - (HOIST ? e_lo[HOIST ? j : 0] : RLO(j)));
-                    cnt[j] += __popc(A);
+                    if (A != 0u) {  // warp-uniform
+                        const int pos = cnt[j] + __popc(A & lt);
+                        if (hit && pos < a.cap_q)
+                            pr[j * rstride + pos] =
+                                make_int2(__float_as_int(sc[j]),
+                                          kidx - (HOIST ? e_lo[HOIST ? j : 0] : RLO(j)));
+                        cnt[j] += __popc(A);
+                    }
                 }
             } else {
                 // SM_EMIT / SM_FB_EMIT: append every key that passes the row's
@@ -708,10 +712,12 @@ IDX_DEVI void score_pass(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                     const bool hit = (uint32_t)off < (uint32_t)len &&
                                      (sc[j] > thr || (sc[j] == thr && off <= cut));
                     const uint32_t A = __ballot_sync(0xffffffffu, hit);
-                    const int pos = cnt[j] + __popc(A & lt);
-                    if (hit && pos < a.cap_q)
-                        pr[j * rstride + pos] = make_int2(__float_as_int(sc[j]), off);
-                    cnt[j] += __popc(A);
+                    if (A != 0u) {  // warp-uniform
+                        const int pos = cnt[j] + __popc(A & lt);
+                        if (hit && pos < a.cap_q)
+                            pr[j * rstride + pos] = make_int2(__float_as_int(sc[j]), off);
+                        cnt[j] += __popc(A);
+                    }
                 }
             }
         }

@@ -60,10 +60,15 @@ IDX_DEVI void set_plan_threshold(RowPlan* plan, uint32_t thr) {
     plan->state = ST_MAIN;
 }
 
+// Sample keys one warp stages in shared memory (kThrStage x 16 bytes).
+constexpr int kThrStage = 384;
+
 // One warp: the threshold of row r into plan[r].  Rows with no sample
 // threshold get thr = 0 (every visible key a candidate).  `max_n` > 0 leaves
 // rows with longer samples alone (a CTA per row takes them) and returns false.
-IDX_DEVI bool warp_row_threshold(const ThrParams& p, int r, uint32_t* hist, uint32_t max_n = 0) {
+// `stage`, when given, is the warp's kThrStage-entry staging buffer.
+IDX_DEVI bool warp_row_threshold(const ThrParams& p, int r, uint32_t* hist, uint32_t max_n = 0,
+                                 uint4* stage = nullptr) {
     const int lane = threadIdx.x & 31;
     RowPlan* plan = p.plan + r;
     SampleRow sr;
@@ -78,31 +83,46 @@ IDX_DEVI bool warp_row_threshold(const ThrParams& p, int r, uint32_t* hist, uint
     if (max_n && sr.n > max_n) return false;
     uint32_t prefix = 0u, need = sr.t;
     bool ok = true;
+    // A sample of up to 8 * kThrStage keys is staged in shared memory once
+    // (16-byte asynchronous copies of eight keys, all in flight at once; a
+    // row's sample starts 16-byte aligned) and read there by both levels; a
+    // longer one is read from global memory by each level.
+    const uint4* v4 = reinterpret_cast<const uint4*>(sr.keys);
+    const uint32_t n8 = sr.n / 8;
+    const bool staged = stage && n8 <= (uint32_t)kThrStage;
+    if (staged) {
+        for (uint32_t i = lane; i < n8; i += 32) cp_async16(stage + i, v4 + i);
+        cp_async_wait_all();
+        __syncwarp();
+    }
     for (int lev = 0; lev < 2; ++lev) {
         const int shift = 8 - 8 * lev;
 #pragma unroll
         for (int j = 0; j < 8; ++j) hist[lane * 8 + j] = 0u;
         __syncwarp();
-        // 16-byte loads of eight keys (a row's sample starts 16-byte aligned),
-        // four per lane in flight, then the odd tail
-        const uint4* v4 = reinterpret_cast<const uint4*>(sr.keys);
-        const uint32_t n8 = sr.n / 8;
-        for (uint32_t base = lane; base < n8; base += 4 * 32) {
-            uint4 x[4];
+        auto count8 = [&](const uint4& x) {
+            const uint32_t wd[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
-                x[u] = base + u * 32 < n8 ? __ldcg(v4 + base + u * 32) : make_uint4(0, 0, 0, 0);
+            for (int h = 0; h < 8; ++h) {
+                const uint32_t key = (wd[h >> 1] >> (16 * (h & 1))) & 0xffffu;
+                if (lev == 0 || (key >> 8) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+            }
+        };
+        if (staged) {
+            for (uint32_t i = lane; i < n8; i += 32) count8(stage[i]);
+        } else {
+            // four loads per lane in flight, then the next four
+            for (uint32_t base = lane; base < n8; base += 4 * 32) {
+                uint4 x[4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                if (base + u * 32 >= n8) continue;
-                const uint32_t wd[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+                for (int u = 0; u < 4; ++u)
+                    x[u] = base + u * 32 < n8 ? __ldcg(v4 + base + u * 32) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-                for (int h = 0; h < 8; ++h) {
-                    const uint32_t key = (wd[h >> 1] >> (16 * (h & 1))) & 0xffffu;
-                    if (lev == 0 || (key >> 8) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
-                }
+                for (int u = 0; u < 4; ++u)
+                    if (base + u * 32 < n8) count8(x[u]);
             }
         }
+        // the odd tail
         for (uint32_t e = n8 * 8 + lane; e < sr.n; e += 32) {
             const uint32_t key = sr.keys[e];
             if (lev == 0 || (key >> 8) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);

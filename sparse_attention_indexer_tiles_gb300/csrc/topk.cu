@@ -748,11 +748,13 @@ template <int WARPS>
 __global__ void __launch_bounds__(WARPS * 32)
 sample_threshold_kernel(TopkRowsArgs a) {
     __shared__ uint32_t hist_all[WARPS][256];
+    __shared__ uint4 stage_all[WARPS][kThrStage];
     pdl_wait();
     const int w = threadIdx.x >> 5;
     const int r = blockIdx.x * WARPS + w;
     if (r >= a.rows) return;  // whole warps only: nothing below syncs the block
-    warp_row_threshold(thr_params(a), r, hist_all[w], a.split > 1 ? (uint32_t)kThrCtaMin : 0u);
+    warp_row_threshold(thr_params(a), r, hist_all[w], a.split > 1 ? (uint32_t)kThrCtaMin : 0u,
+                       stage_all[w]);
 }
 
 // The same threshold for long samples (tens of thousands of keys per row):
@@ -1587,7 +1589,7 @@ cudaError_t launch_topk_rows(const TopkRowsArgs& a, cudaStream_t s) {
         // one warp per row; when some row's sample may exceed kThrCtaMin
         // scores, those rows are left to one CTA each (two passes over the
         // sample instead of four), flagged to the warp kernel by split = 2
-        constexpr int WARPS = 8;
+        constexpr int WARPS = 4;
         TopkRowsArgs b = a;
         b.split = a.row_len > kThrCtaMin ? 2 : 0;
         cudaError_t e = launch_k(sample_threshold_kernel<WARPS>,
