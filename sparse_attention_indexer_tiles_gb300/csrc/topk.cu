@@ -519,25 +519,24 @@ IDX_DEVI Threshold refine_runs(const uint32_t* rkey, const uint32_t* rcnt, uint3
     return {prefix, need};
 }
 
-// Exact threshold of the k largest keys held in the warp runs, from hist, the
-// histogram of the run keys relative to B (bin min((key - B) >> 12, 4095),
-// every key >= B) built while they were collected.  The bin that holds the
-// k-th largest key gives T's top bits; one pass over the runs then takes the
-// least and the largest key of that bin and counts, per warp, the keys above
-// the bin and in it.  When the bin holds a single key value (always for
-// scores on the bf16 grid, whose low 16 bits are constant) that value is T
-// and the per-warp counts are those of keys > T and == T, left in wsum for the
-// output (*counted); otherwise the bin's low 12 bits are resolved by one more
-// histogram.  Returns false when the k-th largest key lies in the open last
-// bin (the runs then take the three-level refinement).
+// Exact threshold of the k largest of the keys held in shared memory, warp w
+// holding those in [lo, hi) (its run, or its chunk), from hist, the histogram
+// of all of them relative to B (bin min((key - B) >> 12, 4095), every key >=
+// B).  The bin that holds the k-th largest key gives T's top bits; one pass
+// then takes the least and the largest key of that bin and counts, per warp,
+// the keys above the bin and in it.  When the bin holds a single key value
+// (always for scores on the bf16 grid, whose low 16 bits are constant) that
+// value is T and the per-warp counts are those of keys > T and == T, left in
+// wsum for the output (*counted); otherwise the bin's low 12 bits are
+// resolved by one more histogram.  Returns false when the k-th largest key
+// lies in the open last bin (the caller then refines by absolute digits).
+// wsum may alias scratch (the counts take its first 2 W words).
 template <int THREADS>
-IDX_DEVI bool refine_runs_rel(const uint32_t* rkey, const uint32_t* rcnt, uint32_t k,
-                              uint32_t B, uint32_t* hist, uint32_t* scratch, uint32_t* wsum,
-                              Threshold* th, bool* counted) {
+IDX_DEVI bool refine_rel(const uint32_t* keys, uint32_t lo, uint32_t hi, uint32_t k, uint32_t B,
+                         uint32_t* hist, uint32_t* scratch, uint32_t* wsum, Threshold* th,
+                         bool* counted) {
     constexpr int W = THREADS / 32;
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const uint32_t cnt = rcnt[w];
-    const uint32_t* mk = rkey + w * kRunCap;
     if (threadIdx.x == 0) {
         scratch[48] = 0xffffffffu;  // least in-bin offset
         scratch[49] = 0u;           // largest in-bin offset
@@ -545,16 +544,16 @@ IDX_DEVI bool refine_runs_rel(const uint32_t* rkey, const uint32_t* rcnt, uint32
     __syncthreads();
     const DigitPick pk = pick_digit<THREADS>(hist, kHistBins, k, scratch);
     if (pk.digit == (uint32_t)kHistBins - 1u) return false;
-    const uint32_t lo = B + (pk.digit << 12);  // the bin holds keys lo .. lo + 4095
+    const uint32_t bl = B + (pk.digit << 12);  // the bin holds keys bl .. bl + 4095
     uint32_t mn = 0xffffffffu, mx = 0u, na = 0u, nt = 0u;
-    for (uint32_t i = lane; i < cnt; i += 32) {
-        const uint32_t key = mk[i], d = key - lo;
+    for (uint32_t i = lo + lane; i < hi; i += 32) {
+        const uint32_t key = keys[i], d = key - bl;
         if (d < 4096u) {
             mn = min(mn, d);
             mx = max(mx, d);
             ++nt;
         } else {
-            na += key > lo;
+            na += key > bl;
         }
     }
     mn = __reduce_min_sync(0xffffffffu, mn);
@@ -572,39 +571,40 @@ IDX_DEVI bool refine_runs_rel(const uint32_t* rkey, const uint32_t* rcnt, uint32
     __syncthreads();
     const uint32_t need = k - pk.above;
     if (scratch[48] == scratch[49]) {
-        *th = {lo + scratch[48], need};
+        *th = {bl + scratch[48], need};
         *counted = true;
         return true;
     }
     zero_shared<THREADS>(hist, kHistBins);
     __syncthreads();
-    for (uint32_t i = lane; i < cnt; i += 32) {
-        const uint32_t d = mk[i] - lo;
+    for (uint32_t i = lo + lane; i < hi; i += 32) {
+        const uint32_t d = keys[i] - bl;
         if (d < 4096u) atomicAdd(&hist[d], 1u);
     }
     __syncthreads();
     const DigitPick p2 = pick_digit<THREADS>(hist, kHistBins, need, scratch);
-    *th = {lo + p2.digit, need - p2.above};
+    *th = {bl + p2.digit, need - p2.above};
     *counted = false;
     return true;
 }
 
-// Ordered output from the runs: key > T, plus the first `need` keys == T.
-// With counted, wsum already holds every warp's counts of keys > T and == T.
+// Ordered output from keys held in index order in shared memory, warp w
+// holding [lo, hi) and the warps following each other: key > T, plus the
+// first `need` keys == T.  One count pass (skipped with counted: wsum already
+// holds every warp's counts of keys > T and == T), one synchronisation for
+// the warp offsets, then each warp writes its range with ballot ranks (32 keys
+// per step).
 template <int THREADS>
-IDX_DEVI void ordered_output_runs(const uint32_t* rkey, const uint32_t* ridx,
-                                  const uint32_t* rcnt, uint32_t* wsum, Threshold th,
-                                  uint32_t k, int* out, bool counted) {
+IDX_DEVI void ordered_output_range(const uint32_t* keys, const uint32_t* idxs, uint32_t lo,
+                                   uint32_t hi, uint32_t* wsum, Threshold th, uint32_t k,
+                                   int* out, bool counted) {
     constexpr int W = THREADS / 32;
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const uint32_t cnt = rcnt[w];
-    const uint32_t* mk = rkey + w * kRunCap;
-    const uint32_t* mi = ridx + w * kRunCap;
     if (!counted) {
         uint32_t na = 0, nt = 0;
-        for (uint32_t i = lane; i < cnt; i += 32) {
-            na += mk[i] > th.key;
-            nt += mk[i] == th.key;
+        for (uint32_t i = lo + lane; i < hi; i += 32) {
+            na += keys[i] > th.key;
+            nt += keys[i] == th.key;
         }
         na = __reduce_add_sync(0xffffffffu, na);
         nt = __reduce_add_sync(0xffffffffu, nt);
@@ -620,18 +620,18 @@ IDX_DEVI void ordered_output_runs(const uint32_t* rkey, const uint32_t* ridx,
         t_run += wsum[W + j];
     }
     const uint32_t lt = (1u << lane) - 1u;
-    for (uint32_t base = 0; base < cnt; base += 32) {
+    for (uint32_t base = lo; base < hi; base += 32) {
         const uint32_t i = base + lane;
-        const uint32_t key = i < cnt ? mk[i] : 0u;
-        const bool ab = i < cnt && key > th.key;
-        const bool tb = i < cnt && key == th.key;
+        const uint32_t key = i < hi ? keys[i] : 0u;
+        const bool ab = i < hi && key > th.key;
+        const bool tb = i < hi && key == th.key;
         const uint32_t A = __ballot_sync(0xffffffffu, ab), T = __ballot_sync(0xffffffffu, tb);
         const uint32_t a_b = a_run + __popc(A & lt), t_b = t_run + __popc(T & lt);
         if (ab) {
             const uint32_t pos = a_b + min(t_b, th.need);
-            if (pos < k) out[pos] = static_cast<int>(mi[i]);
+            if (pos < k) out[pos] = static_cast<int>(idxs[i]);
         } else if (tb && t_b < th.need && a_b + t_b < k) {
-            out[a_b + t_b] = static_cast<int>(mi[i]);
+            out[a_b + t_b] = static_cast<int>(idxs[i]);
         }
         a_run += __popc(A);
         t_run += __popc(T);
@@ -702,8 +702,11 @@ topk_rows_kernel(TopkRowsArgs a) {
     Threshold th;
     bool counted = false;
     const bool runs_ok = fits && total >= k;
+    const int w = threadIdx.x >> 5;
     if (runs_ok) {
-        if (!rel || !refine_runs_rel<THREADS>(rkey, rcnt, k, B, hist, scratch, wsum, &th, &counted))
+        const uint32_t lo = w * kRunCap;
+        if (!rel || !refine_rel<THREADS>(rkey, lo, lo + rcnt[w], k, B, hist, scratch, wsum, &th,
+                                         &counted))
             th = refine_runs<THREADS>(rkey, rcnt, k, hist, scratch, !rel);
     } else {
         // the estimate missed: exact multi-pass path over the row
@@ -715,7 +718,8 @@ topk_rows_kernel(TopkRowsArgs a) {
 
     int* out = a.out + (long long)r * a.topk;
     if (runs_ok)
-        ordered_output_runs<THREADS>(rkey, ridx, rcnt, wsum, th, k, out, counted);
+        ordered_output_range<THREADS>(rkey, ridx, w * kRunCap, w * kRunCap + rcnt[w], wsum, th,
+                                      k, out, counted);
     else
         ordered_output<THREADS>(v, th, k, out, scratch);
 }
@@ -846,60 +850,13 @@ constexpr int kMaxSplit = 64;
 template <int THREADS>
 struct SplitSmem {
     // collection: the StreamSmem layout; selection, over the same memory:
-    // hist | scratch (64) | slice offsets (kMaxSplit + 4) | keys | idxs
+    // hist | scratch (64) | slice offsets and row words (kMaxSplit + 8) | keys | idxs
     static constexpr size_t COLLECT = StreamSmem<THREADS>::BYTES;
     static constexpr int OFFS = kHistBins + 64;
-    static constexpr int KEYS = OFFS + kMaxSplit + 4;
+    static constexpr int KEYS = OFFS + kMaxSplit + 8;
     static constexpr size_t MERGE = (KEYS + 2 * (size_t)kMergeCap) * sizeof(uint32_t);
     static constexpr size_t BYTES = COLLECT > MERGE ? COLLECT : MERGE;
 };
-
-// Ordered compaction of cnt keys held in index order in shared memory: key >
-// T, plus the first `need` keys equal to T.  Warp w takes the w-th contiguous
-// chunk; one count pass, one synchronisation for the chunk offsets, then each
-// warp writes its chunk with ballot ranks (32 keys per step).
-template <int THREADS>
-IDX_DEVI void ordered_output_chunks(const uint32_t* keys, const uint32_t* idxs, uint32_t cnt,
-                                    Threshold th, uint32_t k, int* out, uint32_t* wsum) {
-    constexpr int W = THREADS / 32;
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const uint32_t per = (cnt + W * 32 - 1) / (W * 32) * 32;
-    const uint32_t c0 = min(cnt, w * per), c1 = min(cnt, c0 + per);
-    uint32_t na = 0, nt = 0;
-    for (uint32_t i = c0 + lane; i < c1; i += 32) {
-        na += keys[i] > th.key;
-        nt += keys[i] == th.key;
-    }
-    na = __reduce_add_sync(0xffffffffu, na);
-    nt = __reduce_add_sync(0xffffffffu, nt);
-    if (lane == 0) {
-        wsum[w] = na;
-        wsum[W + w] = nt;
-    }
-    __syncthreads();
-    uint32_t a_run = 0, t_run = 0;
-    for (int j = 0; j < w; ++j) {
-        a_run += wsum[j];
-        t_run += wsum[W + j];
-    }
-    const uint32_t lt = (1u << lane) - 1u;
-    for (uint32_t base = c0; base < c1; base += 32) {
-        const uint32_t i = base + lane;
-        const uint32_t key = i < c1 ? keys[i] : 0u;
-        const bool ab = i < c1 && key > th.key;
-        const bool tb = i < c1 && key == th.key;
-        const uint32_t A = __ballot_sync(0xffffffffu, ab), T = __ballot_sync(0xffffffffu, tb);
-        const uint32_t a_b = a_run + __popc(A & lt), t_b = t_run + __popc(T & lt);
-        if (ab) {
-            const uint32_t pos = a_b + min(t_b, th.need);
-            if (pos < k) out[pos] = static_cast<int>(idxs[i]);
-        } else if (tb && t_b < th.need && a_b + t_b < k) {
-            out[a_b + t_b] = static_cast<int>(idxs[i]);
-        }
-        a_run += __popc(A);
-        t_run += __popc(T);
-    }
-}
 
 template <int THREADS, int UNROLL>
 __global__ void __launch_bounds__(THREADS, 1)
@@ -1033,7 +990,9 @@ topk_split_kernel(TopkRowsArgs a) {
     __threadfence();
 
     // ---- selection by the row's last block (reads bypass L1: other SMs wrote)
-    uint32_t* soff = smem + SS::OFFS;  // [g + 1] slice offsets, [kMaxSplit + 2] total, +3 bad
+    // [g + 1] slice offsets; [kMaxSplit + 1] the largest bound, +2 total, +3 bad,
+    // +4 the least bound of a slice with candidates
+    uint32_t* soff = smem + SS::OFFS;
     uint32_t* keys = smem + SS::KEYS;
     uint32_t* idxs = keys + kMergeCap;
     int* out = a.out + (long long)r * a.topk;
@@ -1044,6 +1003,8 @@ topk_split_kernel(TopkRowsArgs a) {
         const uint32_t l0 = j0 < g ? __ldcg(a.split_lb + (long long)r * g + j0) : 0u;
         const uint32_t l1 = j1 < g ? __ldcg(a.split_lb + (long long)r * g + j1) : 0u;
         const uint32_t lmax = __reduce_max_sync(0xffffffffu, l0 > l1 ? l0 : l1);
+        const uint32_t m0 = n0 > 0 ? l0 : 0xffffffffu, m1 = n1 > 0 ? l1 : 0xffffffffu;
+        const uint32_t lmin = __reduce_min_sync(0xffffffffu, m0 < m1 ? m0 : m1);
         const bool bad = __any_sync(0xffffffffu, n0 < 0 || n1 < 0);
         uint32_t i0 = n0 > 0 ? (uint32_t)n0 : 0u, i1 = n1 > 0 ? (uint32_t)n1 : 0u;
 #pragma unroll
@@ -1064,6 +1025,7 @@ topk_split_kernel(TopkRowsArgs a) {
             soff[kMaxSplit + 1] = lmax;
             soff[kMaxSplit + 2] = total;
             soff[kMaxSplit + 3] = bad || total < k || total > (uint32_t)kMergeCap;
+            soff[kMaxSplit + 4] = lmin;
             if (a.d_stats) atomicAdd(&a.d_stats->split_rows, 1);
         }
     }
@@ -1113,15 +1075,31 @@ topk_split_kernel(TopkRowsArgs a) {
             }
         }
     }
+    // every candidate's key is at least B, the key of the least slice bound
+    // as a float (a bound of +0 admits -0, one key lower): histogram relative
+    // to B, then the one-bin refinement over the warps' chunks
+    const float Bf = key_floor_float(soff[kMaxSplit + 4]);
+    const uint32_t B = Bf == 0.f ? 0x7fffffffu : fkey(Bf);
+    zero_shared<THREADS>(hist, kHistBins);
     __syncthreads();
-    const Threshold th = refine_in_smem<THREADS>(keys, total, 0, 0u, k, hist, scratch);
+    for (uint32_t e = tid; e < total; e += THREADS) {
+        const uint32_t d = (keys[e] - B) >> 12;
+        atomicAdd(&hist[d < (uint32_t)kHistBins ? d : (uint32_t)kHistBins - 1u], 1u);
+    }
+    __syncthreads();
+    const uint32_t cper = (total + W * 32 - 1) / (W * 32) * 32;
+    const uint32_t m0 = min(total, w * cper), m1 = min(total, m0 + cper);  // this warp's chunk
+    Threshold th;
+    bool counted = false;
+    if (!refine_rel<THREADS>(keys, m0, m1, k, B, hist, scratch, scratch, &th, &counted))
+        th = refine_in_smem<THREADS>(keys, total, 0, 0u, k, hist, scratch);
     if (th.key < lmax) {
         // a slice's bound lies above the k-th candidate: it may have left
         // out values of the top k
         exact_path();
         return;
     }
-    ordered_output_chunks<THREADS>(keys, idxs, total, th, k, out, scratch);
+    ordered_output_range<THREADS>(keys, idxs, m0, m1, scratch, th, k, out, counted);
 }
 
 // ---------------------------------------------------------------- slab
@@ -1136,15 +1114,15 @@ topk_split_kernel(TopkRowsArgs a) {
 //      turns the scores into order keys;
 //   2. finds the exact threshold key T by radix selection that starts below
 //      the bits all candidates share (their maximum and minimum agree there):
-//      one 8-bit digit pass over every candidate, then the candidates of the
-//      threshold digit are gathered and refined alone (or, when that digit
-//      holds too many, over all candidates);
+//      one digit of up to 10 bits over every candidate, then, when that digit
+//      holds at most kCandGather candidates, they are gathered and the one
+//      ranked need-th by (key descending, index ascending) fixes T and the
+//      index cut at once (else the digit passes continue over all candidates);
 //   3. keeps the lowest indices among the keys equal to T;
-//   4. writes the selected indices in ascending order: the selected entries of
-//      each run are compacted in run order, so every run's selection is
-//      sorted, and an entry's output position is its rank in its own run plus
-//      its lower bound in each other run of the same key split (the splits
-//      cover ascending key ranges and follow each other).
+//   4. writes the selected indices in ascending order: they are bucketed by
+//      index (1024 buckets of a power-of-two width), the buckets placed by a
+//      scan, and each index placed in its bucket by its rank among the
+//      bucket's indices.
 // Rows whose candidate count fell below topk, or whose runs overflowed, are
 // flagged for the exact rescan instead.
 

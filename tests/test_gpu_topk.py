@@ -180,6 +180,36 @@ def test_forced_row_split(idx, g):
     assert stats.read()["split_rows"] > 0
 
 
+def test_row_split_merge_refinement_paths(idx):
+    """The merge block's refinement over the slices' candidates, one row per
+    branch: fp32 scores (several keys in the threshold bin: a second
+    histogram), bf16-grid scores (one key per bin), k planted values far above
+    the rest (the open last bin: refinement by absolute digits) and a
+    threshold among +0 and -0."""
+    n, topk = 120000, 1500
+    g = torch.Generator().manual_seed(44)
+    rows = [torch.randn(n, generator=g),
+            (torch.randn(n, generator=g) * 0.05).to(torch.bfloat16).float()]
+    planted = torch.randn(n, generator=g)
+    planted[torch.randperm(n, generator=g)[:topk]] = 100.0 + torch.arange(topk) * 1e-3
+    rows.append(planted)
+    z = -torch.rand(n, generator=g) - 0.5
+    perm = torch.randperm(n, generator=g)
+    z[perm[:1000]] = torch.rand(1000, generator=g) + 0.5
+    z[perm[1000:2500]] = 0.0
+    z[perm[2500:4000]] = -0.0
+    rows.append(z)
+    S = torch.stack(rows)
+    R = S.shape[0]
+    ks = torch.zeros(R, dtype=torch.int32)
+    ke = torch.full((R,), n, dtype=torch.int32)
+    stats = idx.Stats(torch.device(DEV))
+    got = gpu_topk(idx, S, ks, ke, topk, options={"row_split": 4}, stats=stats)
+    ref = oracle.topk_from_scores(S, ks, ke, topk)
+    assert np.array_equal(got, ref)
+    assert stats.read()["split_rows"] == R
+
+
 def test_row_split_with_empty_slices_and_a_reused_workspace(idx):
     """64 blocks per row (the most a split takes), rows from just above topk
     (most blocks get an empty slice) to 70000 keys, ragged starts; two calls
