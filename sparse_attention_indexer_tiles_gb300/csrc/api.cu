@@ -172,7 +172,7 @@ FusedParams fused_params(int topk, const idx_options* opt) {
 }
 
 struct FusedLayout {
-    size_t plan, run_cnt, slab, samp, fb_hist, fb_blocks, fb_bflag, fb_cnt, total;
+    size_t plan, run_cnt, slab, samp, fb_hist, fb_blocks, fb_bflag, order, fb_cnt, total;
     long long samp_stride;
 };
 
@@ -194,6 +194,7 @@ FusedLayout fused_layout(int rows, long long max_len, int cap, int cap_q, int S,
     L.fb_hist = take(max_len > cap ? (size_t)rows * 4096 * sizeof(uint32_t) : 0);
     L.fb_blocks = take(max_len > cap ? nblk * sizeof(int) : 0);
     L.fb_bflag = take(max_len > cap ? nblk * sizeof(int) : 0);
+    L.order = take(max_len > cap ? nblk * sizeof(int) : 0);  // the emit pass's block order
     // [0, 8) rescan counters, [8] [9] the sample and emit launches' unit counters
     L.fb_cnt = take(16 * sizeof(int));
     L.total = off;
@@ -364,6 +365,7 @@ idx_status idx_score_topk(const void* q, const void* k, const float* k_scale, co
     const bool sampling = max_len > p.cap;
     int* fb_blocks = sampling ? reinterpret_cast<int*>(base + lay.fb_blocks) : nullptr;
     int* fb_bflag = sampling ? reinterpret_cast<int*>(base + lay.fb_bflag) : nullptr;
+    int* order = sampling ? reinterpret_cast<int*>(base + lay.order) : nullptr;
     int* d_status = opt ? opt->d_status : nullptr;
     idx_stats* d_stats = opt ? opt->d_stats : nullptr;
 
@@ -421,6 +423,10 @@ idx_status idx_score_topk(const void* q, const void* k, const float* k_scale, co
         t.d_status = d_status;
         t.d_stats = d_stats;
         t.pdl = 1;  // after the sample pass
+        // the same launch orders the row blocks for the emit pass, longest first
+        t.order = order;
+        t.order_nblk = (rows + score_rows_per_block(H) - 1) / score_rows_per_block(H);
+        t.order_rpb = score_rows_per_block(H);
         if ((e = launch_topk_rows(t, s)) != cudaSuccess) return cuda_status(e);
         count_launches(1);
     }
@@ -431,6 +437,7 @@ idx_status idx_score_topk(const void* q, const void* k, const float* k_scale, co
     L.a.nwhole = split.nwhole;
     L.a.ksplit = split.k;
     L.a.sched = fb_cnt + 9;
+    L.a.order = order;  // (null without a sample: block order)
     L.pdl = sampling ? 1 : 0;  // after the thresholds (else the memset: plain launch)
     if ((e = launch_score(L, s)) != cudaSuccess) return cuda_status(e);
     record(opt, 2, s);

@@ -62,6 +62,8 @@ struct ScoreArgs {
     int* sched;           // optional launch counter, 0 before the launch: CTAs take
                           // units gridDim.x + atomicAdd(sched, 1) in turn (null: every
                           // gridDim.x-th unit)
+    const int* order;     // optional [row blocks]: the i-th block the units take (whole
+                          // blocks, then the split tail) is order[i] (null: block i)
     int level;
     // bounded waits: a wait on the pipeline gives up after wait_limit clock
     // cycles; withhold_tile >= 0 (a test of that path) makes the producer issue

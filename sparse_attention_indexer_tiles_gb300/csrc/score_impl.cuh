@@ -760,14 +760,19 @@ IDX_DEVI int pw_nt(const uint8_t* smem, int sl) {
 }
 
 // Unit u of a scoring launch: a row block, or a part of one (ScoreArgs::nwhole,
-// ::ksplit).
+// ::ksplit), the blocks taken in ScoreArgs::order when there is one.
 struct ScoreUnit {
     int blk, part, nparts;
 };
 IDX_DEVI ScoreUnit score_unit(const ScoreArgs& a, int u) {
-    if (u < a.nwhole) return {u, 0, 1};
-    const int v = u - a.nwhole;
-    return {a.nwhole + v / a.ksplit, v % a.ksplit, a.ksplit};
+    int i = u, part = 0, nparts = 1;
+    if (u >= a.nwhole) {
+        const int v = u - a.nwhole;
+        i = a.nwhole + v / a.ksplit;
+        part = v % a.ksplit;
+        nparts = a.ksplit;
+    }
+    return {a.order ? __ldg(a.order + i) : i, part, nparts};
 }
 
 // The kernel.  A scoring launch (SM_MATERIALISE, SM_SAMPLE, SM_EMIT) is

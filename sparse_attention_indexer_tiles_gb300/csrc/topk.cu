@@ -748,12 +748,81 @@ IDX_DEVI ThrParams thr_params(const TopkRowsArgs& a) {
     return p;
 }
 
+// The emit pass's block order (TopkRowsArgs::order): row blocks by the number
+// of 128-key tiles their rows' visible ranges span, longest first, so that the
+// persistent launch hands out the long units before the short ones (a long
+// unit taken last leaves the other SMs idle while it runs).  A counting sort
+// over 1024 buckets, 32 per octave of the tile count (bucket 0: nothing to
+// score); the order within a bucket is arbitrary.
+template <int THREADS>
+IDX_DEVI void block_order(const TopkRowsArgs& a, uint32_t* bins /* 1024 + 32 */) {
+    constexpr int NB = 1024, BPT = NB / THREADS;
+    static_assert(NB % THREADS == 0 && THREADS % 32 == 0, "bins per thread");
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const int nblk = a.order_nblk, R = a.order_rpb;
+    auto bucket = [&](int b) -> uint32_t {
+        long long lo = 0x7fffffffffffffffll, hi = -1;
+        for (int j = 0; j < R; ++j) {
+            const long long r = (long long)b * R + j;
+            if (r >= a.rows) break;
+            const long long s0 = a.vis_ks[r], s1 = a.vis_ke[r];
+            if (s1 > s0) {
+                lo = s0 < lo ? s0 : lo;
+                hi = s1 > hi ? s1 : hi;
+            }
+        }
+        if (hi <= lo) return 0u;
+        const long long tl = (hi - lo + 127) / 128;
+        const uint32_t t = tl < (1ll << 30) ? (uint32_t)tl : (1u << 30);
+        const int e = 31 - __clz(t);
+        const uint32_t m = e >= 5 ? (t >> (e - 5)) & 31u : (t << (5 - e)) & 31u;
+        return 1u + 32u * (uint32_t)e + m;  // < 1 + 32 * 31 + 32 = 1025: <= 1023 for e <= 30
+    };
+    for (int i = tid; i < NB; i += THREADS) bins[i] = 0u;
+    __syncthreads();
+    for (int b = tid; b < nblk; b += THREADS) atomicAdd(&bins[min(bucket(b), (uint32_t)NB - 1u)], 1u);
+    __syncthreads();
+    // bucket starts, the largest bucket first: thread t owns buckets
+    // NB - 1 - BPT t ... NB - BPT (t + 1)
+    uint32_t c[BPT], loc = 0;
+#pragma unroll
+    for (int j = 0; j < BPT; ++j) {
+        c[j] = bins[NB - 1 - (BPT * tid + j)];
+        loc += c[j];
+    }
+    uint32_t incl = loc;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t x = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += x;
+    }
+    uint32_t* wsum = bins + NB;
+    if (lane == 31) wsum[w] = incl;
+    __syncthreads();
+    uint32_t st = incl - loc;
+    for (int j = 0; j < w; ++j) st += wsum[j];
+#pragma unroll
+    for (int j = 0; j < BPT; ++j) {
+        bins[NB - 1 - (BPT * tid + j)] = st;
+        st += c[j];
+    }
+    __syncthreads();
+    for (int b = tid; b < nblk; b += THREADS)
+        a.order[atomicAdd(&bins[min(bucket(b), (uint32_t)NB - 1u)], 1u)] = b;
+}
+
 template <int WARPS>
 __global__ void __launch_bounds__(WARPS * 32)
 sample_threshold_kernel(TopkRowsArgs a) {
     __shared__ uint32_t hist_all[WARPS][256];
     __shared__ uint4 stage_all[WARPS][kThrStage];
+    static_assert(sizeof(stage_all) >= (1024 + 32) * sizeof(uint32_t), "order bins");
     pdl_wait();
+    if (a.order && blockIdx.x == gridDim.x - 1) {
+        // the last CTA: the emit pass's block order
+        block_order<WARPS * 32>(a, reinterpret_cast<uint32_t*>(&stage_all[0][0]));
+        return;
+    }
     const int w = threadIdx.x >> 5;
     const int r = blockIdx.x * WARPS + w;
     if (r >= a.rows) return;  // whole warps only: nothing below syncs the block
@@ -1570,9 +1639,10 @@ cudaError_t launch_topk_rows(const TopkRowsArgs& a, cudaStream_t s) {
         constexpr int WARPS = 4;
         TopkRowsArgs b = a;
         b.split = a.row_len > kThrCtaMin ? 2 : 0;
+        // (one more CTA for the block order)
         cudaError_t e = launch_k(sample_threshold_kernel<WARPS>,
-                                 dim3((unsigned)((a.rows + WARPS - 1) / WARPS)), dim3(WARPS * 32), 0,
-                                 s, a.pdl != 0, b);
+                                 dim3((unsigned)((a.rows + WARPS - 1) / WARPS + (a.order ? 1 : 0))),
+                                 dim3(WARPS * 32), 0, s, a.pdl != 0, b);
         if (e == cudaSuccess && b.split) {
             e = launch_k(sample_threshold_cta_kernel, dim3((unsigned)a.rows), dim3(kThrCtaThreads),
                          0, s, a.pdl != 0, b);

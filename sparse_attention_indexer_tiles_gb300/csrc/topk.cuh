@@ -45,6 +45,12 @@ struct TopkRowsArgs {
     int* split_cnt;        // [rows * g] candidates handed over, -1 = a run overflowed
     uint32_t* split_lb;    // [rows * g] the lower bound (order key) each block used
     int* split_ticket;     // [rows] blocks of the row done so far (zeroed by the launch)
+    // TOPK_THRESHOLD, optional: one more CTA writes order[order_nblk], the
+    // scoring row blocks (order_rpb rows each) by their key span in tiles,
+    // longest first, for the emit pass's units
+    int* order;
+    int order_nblk;
+    int order_rpb;
     int pdl;              // launch overlapping the kernel before it on the stream
     int* d_status;
     idx_stats* d_stats;

@@ -124,7 +124,8 @@ def _documented_workspace(rows, max_len, topk, nruns):
     cap_q = ceil(cap / 8) + 64 rounded up to even, the sample scratch [rows, max_len // S + 2
     rounded up to a multiple of 8] of 16-bit keys, the rescan histograms [rows, 4096] and the rescan's list and flags
     of row blocks [blocks] int32 (these only when rows can see more than cap
-    keys), and sixteen counters (the rescan's and the scoring launches' unit
+    keys), the emit pass's order of the row blocks [blocks] int32 (also only
+    then), and sixteen counters (the rescan's and the scoring launches' unit
     counters)."""
     def up(x):
         return (x + 255) // 256 * 256
@@ -138,7 +139,8 @@ def _documented_workspace(rows, max_len, topk, nruns):
     regions = [rows * 32, rows * nruns * 4, rows * nruns * cap_q * 8,
                rows * ((max_len // S + 2 + 7) // 8 * 8) * 2 if sampled else 0,
                rows * 4096 * 4 if sampled else 0,
-               nblk * 4 if sampled else 0, nblk * 4 if sampled else 0, 16 * 4]
+               nblk * 4 if sampled else 0, nblk * 4 if sampled else 0,
+               nblk * 4 if sampled else 0, 16 * 4]
     return sum(up(r) for r in regions), S
 
 
