@@ -1563,14 +1563,57 @@ cand_topk_kernel(CandArgs a) {
         }
         __syncthreads();  // the histograms are done: the bucket counts reuse them
 
-        // ---- ascending output: the selected indices bucketed by index (1024
-        // buckets of a power-of-two width over the row), buckets placed by a
-        // scan, and each entry placed in its bucket by its rank among the
-        // bucket's entries (a bucket holds at most its width of indices)
         auto chosen = [&](int2 pv) {
             const uint32_t key = (uint32_t)pv.x;
             return key > T || (key == T && (uint32_t)pv.y <= idx_cut);
         };
+        // ---- ascending output, rows of at most 32 (1024 + topk) keys: a bitmap
+        // over the row's indices in the histogram and selection words (scratch
+        // follows them), one bit set per selected index; each thread then owns
+        // a contiguous range of bitmap words and writes the indices of their
+        // set bits from its offset in a block scan of the bit counts
+        const uint32_t bm_words = (uint32_t)((n + 31) / 32);
+        if (bm_words <= (uint32_t)L.sel() + (uint32_t)a.topk) {
+            uint32_t* bm = smem + L.hist();
+            for (uint32_t i = tid; i < bm_words; i += THREADS) bm[i] = 0u;
+            __syncthreads();
+            for (uint32_t e = tid; e < ptot; e += THREADS) {
+                const int2 pv = pairs[e];
+                if (chosen(pv)) atomicOr(&bm[(uint32_t)pv.y >> 5], 1u << ((uint32_t)pv.y & 31u));
+            }
+            __syncthreads();
+            const uint32_t per = (bm_words + THREADS - 1) / THREADS;
+            const uint32_t w0 = min(bm_words, tid * per), w1 = min(bm_words, w0 + per);
+            uint32_t c = 0;
+            for (uint32_t i = w0; i < w1; ++i) c += __popc(bm[i]);
+            uint32_t nsel;
+            uint32_t pos = block_incl_scan<THREADS>(c, scratch, &nsel) - c;
+            if (nsel != k) {
+                // cannot happen for finite scores: report it rather than write past
+                // the row's output
+                for (int i = tid; i < a.topk; i += THREADS) out[i] = -1;
+                if (tid == 0) {
+                    raise_status(a.d_status, IDX_DEV_STATE);
+                    plan->state = ST_DONE;
+                }
+                continue;
+            }
+            for (uint32_t i = w0; i < w1; ++i) {
+                uint32_t m = bm[i];
+                while (m) {
+                    const int b = __ffs(m) - 1;
+                    m &= m - 1u;
+                    out[pos++] = (int)(32u * i + (uint32_t)b);
+                }
+            }
+            if (tid == 0) plan->state = ST_DONE;
+            continue;
+        }
+        // ---- ascending output, longer rows: the selected indices bucketed by
+        // index (1024 buckets of a power-of-two width over the row), buckets
+        // placed by a scan, and each entry placed in its bucket by its rank
+        // among the bucket's entries (a bucket holds at most its width of
+        // indices)
         int bsh = 0;  // bucket width 2^bsh >= n / kCandBins
         while (((long long)kCandBins << bsh) < n) ++bsh;
         for (int i = tid; i < kCandBins; i += THREADS) hist[i] = 0u;
