@@ -163,8 +163,9 @@ idx_status idx_score_topk(const void* q, const void* k, const float* k_scale, co
  * lower index.  NaN scores are a precondition violation.
  * ws: idx_topk_workspace(...) bytes, 256-byte aligned (IDX_EWORKSPACE if
  * smaller, IDX_EALIGN if misaligned); 0 bytes, and ws may be NULL, unless
- * rows are split (row_split above): then 2 * 8192 * 4 + 4 bytes per block of
- * a split row.  The call allocates nothing.
+ * rows are split (row_split above): then 2 * 8192 * 4 + 8 bytes per block of
+ * a split row, 8 bytes per row and 256.  The call allocates nothing, and the
+ * workspace needs no clearing between calls.
  * ------------------------------------------------------------------------ */
 size_t idx_topk_workspace(int rows, long long row_stride, int topk, const idx_options* opt);
 idx_status idx_topk_from_scores(const float* scores, long long row_stride, const int* ks,

@@ -3,6 +3,7 @@
 // of topk.cu and score_*.cu; this file only decides what to launch.
 #include <algorithm>
 #include <atomic>
+#include <chrono>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -112,6 +113,16 @@ int sm_count() {
         cached[dev] = n;
     }
     return cached[dev];
+}
+
+// A per-call epoch for the split rows' ticket words (never 0).
+uint32_t next_epoch() {
+    static std::atomic<uint32_t> ctr{
+        0x9e3779b9u ^ (uint32_t)std::chrono::steady_clock::now().time_since_epoch().count()};
+    uint32_t e;
+    do e = ctr.fetch_add(1u, std::memory_order_relaxed) + 1u;
+    while (e == 0u);
+    return e;
 }
 
 // Blocks per row of the standalone top-k (page "[sglang] ROCm DSA Indexer
@@ -527,7 +538,8 @@ idx_status idx_topk_from_scores(const float* scores, long long row_stride, const
         t.split_idx = t.split_keys + slots * kSplitCap;
         t.split_cnt = reinterpret_cast<int*>(t.split_idx + slots * kSplitCap);
         t.split_lb = reinterpret_cast<uint32_t*>(t.split_cnt + slots);
-        t.split_ticket = reinterpret_cast<int*>(t.split_lb + slots);
+        t.split_ticket = reinterpret_cast<unsigned long long*>(t.split_lb + slots);
+        t.epoch = next_epoch();
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     record(opt, 0, s);

@@ -418,7 +418,8 @@ IDX_DEVI void stream_collect(const RowView& v, uint32_t L, uint32_t* rkey, uint3
 // time only (the row takes the exact multi-pass path).  hist leaves holding
 // the histogram of the hits relative to the returned key B (bins of 4096 keys
 // from B up, the last bin open), B being the order key of the float bound
-// (every hit has key >= B; a bound of +0 admits -0, whose key is one less).
+// (every hit has key >= B: fkey folds -0 onto +0, so a bound of zero holds
+// both zeros at B).
 template <int THREADS, int UNROLL>
 IDX_DEVI uint32_t stream_collect_estimate(const RowView& v, uint32_t k, uint32_t* hist,
                                       uint32_t* scratch, uint32_t* rkey, uint32_t* ridx,
@@ -479,7 +480,7 @@ IDX_DEVI uint32_t stream_collect_estimate(const RowView& v, uint32_t k, uint32_t
     zero_shared<THREADS>(hist, kHistBins);
     __syncthreads();
     const float Lf = key_floor_float(L);
-    const uint32_t B = Lf == 0.f ? 0x7fffffffu : fkey(Lf);
+    const uint32_t B = fkey(Lf);
     uint32_t cnt = 0;
     for (int base = s0; base < s1; base += 32 * UNROLL) {
         const int nb = base + 32 * UNROLL;
@@ -903,8 +904,10 @@ __global__ void __launch_bounds__(kThrCtaThreads) sample_threshold_cta_kernel(To
 // first (the lower edge of the 12-bit bin of about the 2 k P / n-th largest of
 // its P sampled values: about 2 k n_c / n of its n_c values reach it), so no
 // block waits for another read.  The block of the row that finishes last (it
-// draws the last ticket of a per-row counter that the launch starts at 0)
-// then selects from the concatenation, already in index order.  The result is
+// draws the last ticket of a per-row counter whose word carries the call's
+// epoch in its high half, so that a word left by another call, or never
+// written, counts as no ticket drawn: no clearing before the launch) then
+// selects from the concatenation, already in index order.  The result is
 // exact when the k-th largest candidate T' is >= every L_c: a value a block
 // left out is below its L_c <= T', hence below the row's k-th largest, and
 // every value >= T' is a candidate.  Otherwise (or when a slice overflowed or
@@ -1053,7 +1056,30 @@ topk_split_kernel(TopkRowsArgs a) {
     // publish, then draw a ticket: the row's last block goes on
     __threadfence();
     __syncthreads();
-    if (tid == 0) s_last = atomicAdd(a.split_ticket + r, 1) == g - 1;
+    if (tid == 0) {
+        // draw a ticket: a word of another epoch is first restarted at this
+        // call's first ticket by a compare-and-swap (one block wins, the others
+        // see the new epoch); a word of this epoch takes an add
+        unsigned long long* tk = a.split_ticket + r;
+        const unsigned long long ep = (unsigned long long)a.epoch << 32;
+        unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(tk);
+        int last = 0;
+        for (int it = 0; it < 64; ++it) {
+            if ((cur & 0xffffffff00000000ull) == ep) {
+                const unsigned long long old = atomicAdd(tk, 1ull);
+                last = (old & 0xffffffffull) + 1ull == (unsigned long long)g;
+                break;
+            }
+            const unsigned long long seen = atomicCAS(tk, cur, ep | 1ull);
+            if (seen == cur) {
+                last = g == 1;
+                break;
+            }
+            cur = seen;
+            if (it == 63) raise_status(a.d_status, IDX_DEV_STATE);
+        }
+        s_last = last;
+    }
     __syncthreads();
     if (!s_last) return;
     __threadfence();
@@ -1145,10 +1171,9 @@ topk_split_kernel(TopkRowsArgs a) {
         }
     }
     // every candidate's key is at least B, the key of the least slice bound
-    // as a float (a bound of +0 admits -0, one key lower): histogram relative
-    // to B, then the one-bin refinement over the warps' chunks
-    const float Bf = key_floor_float(soff[kMaxSplit + 4]);
-    const uint32_t B = Bf == 0.f ? 0x7fffffffu : fkey(Bf);
+    // as a float: histogram relative to B, then the one-bin refinement over
+    // the warps' chunks
+    const uint32_t B = fkey(key_floor_float(soff[kMaxSplit + 4]));
     zero_shared<THREADS>(hist, kHistBins);
     __syncthreads();
     for (uint32_t e = tid; e < total; e += THREADS) {
@@ -1700,9 +1725,7 @@ cudaError_t launch_topk_rows(const TopkRowsArgs& a, cudaStream_t s) {
         static cudaError_t attr = cudaFuncSetAttribute(
             kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SPLIT_SMEM);
         if (attr != cudaSuccess) return attr;
-        // the per-row tickets start at 0
-        const cudaError_t e = cudaMemsetAsync(a.split_ticket, 0, sizeof(int) * (size_t)a.rows, s);
-        if (e != cudaSuccess) return e;
+        if (a.epoch == 0u) return cudaErrorInvalidValue;
         kern<<<dim3((unsigned)a.split, (unsigned)a.rows), T, SPLIT_SMEM, s>>>(a);
         return cudaGetLastError();
     }
@@ -1718,7 +1741,7 @@ size_t split_workspace_bytes(int rows, int g) {
     if (g < 2) return 0;
     const size_t slots = (size_t)rows * g;
     return slots * (size_t)kSplitCap * 2 * sizeof(uint32_t) + 2 * slots * sizeof(int) +
-           (size_t)rows * sizeof(int) + 256;
+           (size_t)rows * sizeof(unsigned long long) + 256;
 }
 
 size_t cand_smem_bytes(int cap_q, int nruns, int topk) {

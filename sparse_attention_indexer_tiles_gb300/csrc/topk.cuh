@@ -44,7 +44,8 @@ struct TopkRowsArgs {
     uint32_t* split_idx;   // [rows * g, kSplitCap]
     int* split_cnt;        // [rows * g] candidates handed over, -1 = a run overflowed
     uint32_t* split_lb;    // [rows * g] the lower bound (order key) each block used
-    int* split_ticket;     // [rows] blocks of the row done so far (zeroed by the launch)
+    unsigned long long* split_ticket;  // [rows] (epoch << 32) | blocks of the row done so far
+    uint32_t epoch;        // this call's epoch, never 0: the tickets need no clearing
     // TOPK_THRESHOLD, optional: one more CTA writes order[order_nblk], the
     // scoring row blocks (order_rpb rows each) by their key span in tiles,
     // longest first, for the emit pass's units
