@@ -255,13 +255,24 @@ IDX_DEVI uint32_t hit_mask(const float4 (&f)[UNROLL], int base, bool interior, i
     static_assert(UNROLL == 8, "eight rows of 4 values: one 32-bit mask, two count words");
     uint32_t m = 0u;
     if (interior) {
+        // each compare gives 1.0 or 0.0 (one ALU instruction, the busiest pipe
+        // here); the bits are summed as exact powers of two on the FMA pipe,
+        // 16 per accumulator
+        auto ge = [](float x, float y) {
+            float r;
+            asm("set.ge.f32.f32 %0, %1, %2;" : "=f"(r) : "f"(x), "f"(y));
+            return r;
+        };
+        float acc[2] = {0.f, 0.f};
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
-            m |= (f[u].x >= Lf ? 1u : 0u) << (4 * u);
-            m |= (f[u].y >= Lf ? 1u : 0u) << (4 * u + 1);
-            m |= (f[u].z >= Lf ? 1u : 0u) << (4 * u + 2);
-            m |= (f[u].w >= Lf ? 1u : 0u) << (4 * u + 3);
+            const int h = u >> 2, b = 4 * (u & 3);
+            acc[h] = fmaf(ge(f[u].x, Lf), (float)(1u << b), acc[h]);
+            acc[h] = fmaf(ge(f[u].y, Lf), (float)(1u << (b + 1)), acc[h]);
+            acc[h] = fmaf(ge(f[u].z, Lf), (float)(1u << (b + 2)), acc[h]);
+            acc[h] = fmaf(ge(f[u].w, Lf), (float)(1u << (b + 3)), acc[h]);
         }
+        m = (uint32_t)acc[0] | ((uint32_t)acc[1] << 16);
     } else {
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
