@@ -294,13 +294,13 @@ IDX_DEVI void append_hits(const RowView& v, uint32_t m, int base, int off, int l
                           uint32_t& cnt, uint32_t* mk, uint32_t* mi, uint32_t* hist,
                           uint32_t hb = 0u, bool rel = false) {
     if (!__any_sync(0xffffffffu, m != 0u)) return;
-    // per-row hit counts, four 8-bit fields per word (a row's warp total <= 128)
-    uint32_t w0 = 0u, w1 = 0u;
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-        w0 |= (uint32_t)__popc((m >> (4 * u)) & 15u) << (8 * u);
-        w1 |= (uint32_t)__popc((m >> (4 * u + 16)) & 15u) << (8 * u);
-    }
+    // per-row hit counts, four 8-bit fields per word (a row's warp total <=
+    // 128): the eight nibble counts of m side by side (two SWAR steps), then
+    // rows 0-3 and 4-7 gathered into the bytes of w0 and w1
+    uint32_t x = m - ((m >> 1) & 0x55555555u);
+    x = (x & 0x33333333u) + ((x >> 2) & 0x33333333u);  // nibble u: hits of row u
+    const uint32_t ev = x & 0x0f0f0f0fu, od = (x >> 4) & 0x0f0f0f0fu;
+    const uint32_t w0 = __byte_perm(ev, od, 0x5140u), w1 = __byte_perm(ev, od, 0x7362u);
     uint32_t i0 = w0, i1 = w1;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -324,7 +324,7 @@ IDX_DEVI void append_hits(const RowView& v, uint32_t m, int base, int off, int l
     // run position and value address of hit bit i
     auto place = [&](int i, uint32_t* pos) {
         const int u = i >> 2, c = i & 3;
-        const uint32_t below = u < 4 ? (e0 >> (8 * u)) & 0xffu : (e1 >> (8 * (u - 4))) & 0xffu;
+        const uint32_t below = __byte_perm(e0, e1, (uint32_t)u) & 0xffu;  // byte u of (e1:e0)
         uint32_t start = 0u;
 #pragma unroll
         for (int j = 1; j < UNROLL; ++j) start = u == j ? rs[j] : start;
