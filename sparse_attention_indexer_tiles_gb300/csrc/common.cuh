@@ -80,23 +80,10 @@ IDX_DEVI void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
-#ifndef IDX_WAIT_HINT_NS
-#define IDX_WAIT_HINT_NS 0
-#endif
-
-// One test of the phase.  With a suspend-time hint (ns) the thread may sleep in
-// hardware until the phase completes instead of spinning.
+// One test of the phase (the thread may be suspended in hardware for a
+// system-dependent time while the phase is incomplete).
 IDX_DEVI bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     uint32_t ok;
-#if IDX_WAIT_HINT_NS > 0
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity), "r"((uint32_t)IDX_WAIT_HINT_NS)
-        : "memory");
-#else
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
@@ -104,7 +91,6 @@ IDX_DEVI bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
         : "=r"(ok)
         : "r"(smem_u32(bar)), "r"(parity)
         : "memory");
-#endif
     return ok != 0;
 }
 
@@ -291,16 +277,6 @@ IDX_DEVI void tmem_ld32x32b(uint32_t taddr, float* v) {
 }
 
 IDX_DEVI void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-
-// Warpgroup-wide register reallocation (all 128 threads of the warpgroup).
-template <uint32_t N>
-IDX_DEVI void setmaxnreg_dec() {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
-}
-template <uint32_t N>
-IDX_DEVI void setmaxnreg_inc() {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
-}
 
 IDX_DEVI void named_bar_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
