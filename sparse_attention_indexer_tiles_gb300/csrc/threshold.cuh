@@ -81,12 +81,10 @@ IDX_DEVI bool warp_row_threshold(const ThrParams& p, int r, uint32_t* hist, uint
         return true;
     }
     if (max_n && sr.n > max_n) return false;
-    uint32_t prefix = 0u, need = sr.t;
-    bool ok = true;
     // A sample of up to 8 * kThrStage keys is staged in shared memory once
     // (16-byte asynchronous copies of eight keys, all in flight at once; a
-    // row's sample starts 16-byte aligned) and read there by both levels; a
-    // longer one is read from global memory by each level.
+    // row's sample starts 16-byte aligned) and read there by every pass; a
+    // longer one is read from global memory by each pass.
     const uint4* v4 = reinterpret_cast<const uint4*>(sr.keys);
     const uint32_t n8 = sr.n / 8;
     const bool staged = stage && n8 <= (uint32_t)kThrStage;
@@ -95,21 +93,15 @@ IDX_DEVI bool warp_row_threshold(const ThrParams& p, int r, uint32_t* hist, uint
         cp_async_wait_all();
         __syncwarp();
     }
-    for (int lev = 0; lev < 2; ++lev) {
-        const int shift = 8 - 8 * lev;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) hist[lane * 8 + j] = 0u;
-        __syncwarp();
-        auto count8 = [&](const uint4& x) {
+    // fn(key) for every sample key this lane holds
+    auto each_key = [&](auto fn) {
+        auto do8 = [&](const uint4& x) {
             const uint32_t wd[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-            for (int h = 0; h < 8; ++h) {
-                const uint32_t key = (wd[h >> 1] >> (16 * (h & 1))) & 0xffffu;
-                if (lev == 0 || (key >> 8) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
-            }
+            for (int h = 0; h < 8; ++h) fn((wd[h >> 1] >> (16 * (h & 1))) & 0xffffu);
         };
         if (staged) {
-            for (uint32_t i = lane; i < n8; i += 32) count8(stage[i]);
+            for (uint32_t i = lane; i < n8; i += 32) do8(stage[i]);
         } else {
             // four loads per lane in flight, then the next four
             for (uint32_t base = lane; base < n8; base += 4 * 32) {
@@ -119,14 +111,26 @@ IDX_DEVI bool warp_row_threshold(const ThrParams& p, int r, uint32_t* hist, uint
                     x[u] = base + u * 32 < n8 ? __ldcg(v4 + base + u * 32) : make_uint4(0, 0, 0, 0);
 #pragma unroll
                 for (int u = 0; u < 4; ++u)
-                    if (base + u * 32 < n8) count8(x[u]);
+                    if (base + u * 32 < n8) do8(x[u]);
             }
         }
-        // the odd tail
-        for (uint32_t e = n8 * 8 + lane; e < sr.n; e += 32) {
-            const uint32_t key = sr.keys[e];
-            if (lev == 0 || (key >> 8) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
-        }
+        for (uint32_t e = n8 * 8 + lane; e < sr.n; e += 32) fn((uint32_t)sr.keys[e]);  // the odd tail
+    };
+    // The digit steps start below the bits every key shares (the sample's least
+    // and largest key agree there): an 8-bit digit from the highest differing
+    // bit down, then the bits below it among the keys of the chosen digit.  (A
+    // fixed top byte would put nearly every key of a row, whose scores span a
+    // few octaves, into one or two bins: serialised shared-memory atomics.)
+    uint32_t mn = 0xffffu, mx = 0u;
+    each_key([&](uint32_t k) {
+        mn = k < mn ? k : mn;
+        mx = k > mx ? k : mx;
+    });
+    mn = __reduce_min_sync(0xffffffffu, mn);
+    mx = __reduce_max_sync(0xffffffffu, mx);
+    // the digit of bins [0, 256) that holds the need-th largest key
+    uint32_t need = sr.t;
+    auto pick = [&](uint32_t* digit) -> bool {
         __syncwarp();
         // lane l holds bins 255 - 8l ... 248 - 8l (from the largest keys down)
         uint32_t c[8], local = 0;
@@ -143,33 +147,56 @@ IDX_DEVI bool warp_row_threshold(const ThrParams& p, int r, uint32_t* hist, uint
         }
         const uint32_t excl = incl - local;
         const uint32_t owner = __ballot_sync(0xffffffffu, excl < need && need <= incl);
-        if (owner == 0u) {  // cannot happen: need never exceeds the keys left
-            ok = false;
-            break;
-        }
+        if (owner == 0u) return false;  // cannot happen: need never exceeds the keys left
         const int src = __ffs(owner) - 1;
-        uint32_t digit = 0u, above = 0u;
+        uint32_t dg = 0u, above = 0u;
         if (lane == src) {
             uint32_t cum = excl;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 if (cum + c[j] >= need) {
-                    digit = 255u - 8u * (uint32_t)lane - (uint32_t)j;
+                    dg = 255u - 8u * (uint32_t)lane - (uint32_t)j;
                     above = cum;
                     break;
                 }
                 cum += c[j];
             }
         }
-        digit = __shfl_sync(0xffffffffu, digit, src);
-        above = __shfl_sync(0xffffffffu, above, src);
-        need -= above;
-        prefix = (prefix << 8) | digit;
+        *digit = __shfl_sync(0xffffffffu, dg, src);
+        need -= __shfl_sync(0xffffffffu, above, src);
         __syncwarp();
+        return true;
+    };
+    auto clear = [&] {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) hist[lane * 8 + j] = 0u;
+        __syncwarp();
+    };
+    bool ok = true;
+    uint32_t T = mx;  // every key equal: the largest is the t-th largest
+    if (mn != mx) {
+        const int hb = 31 - __clz(mn ^ mx);
+        const int w0 = hb + 1 < 8 ? hb + 1 : 8, s0 = hb + 1 - w0;
+        const uint32_t m0 = (1u << w0) - 1u;
+        clear();
+        each_key([&](uint32_t k) { atomicAdd(&hist[(k >> s0) & m0], 1u); });
+        uint32_t d0 = 0u, d1 = 0u;
+        ok = pick(&d0);
+        const uint32_t pre = ((mx >> (hb + 1)) << w0) | d0;  // the key's bits from s0 up
+        T = pre << s0;
+        if (ok && s0 > 0) {
+            const uint32_t m1 = (1u << s0) - 1u;
+            clear();
+            each_key([&](uint32_t k) {
+                if ((k >> s0) == pre) atomicAdd(&hist[k & m1], 1u);
+            });
+            ok = pick(&d1);
+            T |= d1;
+        }
     }
     // a failed pick leaves thr = 0: every key a candidate, the slab overflows
     // and the exact rescan takes the row
-    if (lane == 0) set_plan_threshold(plan, ok ? prefix << 16 : 0u);
+    if (lane == 0) set_plan_threshold(plan, ok ? T << 16 : 0u);
     return true;
 }
 
