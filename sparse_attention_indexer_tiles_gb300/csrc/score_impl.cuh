@@ -611,7 +611,11 @@ IDX_DEVI void score_pass(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
         const int all_lo = pw[PW_ALL_LO], all_hi = pw[PW_ALL_HI];
         float next_scale = team < ntiles && s_i < ilim ? __ldg(a.k_scale + s_off) : 0.f;
         const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(team * C::N);
-        for (int i = team, u = 0; i < ntiles; i += 2, ++u) {
+        for (int i = team, un = 0; i < ntiles; i += 2, ++un) {
+            // the team's tile count (accf parity): a counter of its own, or
+            // i / 2 (team is 0 or 1) -- measured faster at H = 64 and at H <= 32
+            // respectively (the register allocation differs)
+            const uint32_t u = H <= 32 ? (uint32_t)i >> 1 : (uint32_t)un;
             const float cur_scale = next_scale;
             s_i += 2 * C::M;
             s_off += s_step;
