@@ -661,23 +661,37 @@ idx_status idx_page_table_transform(int* idx_out, int rows, int topk, const int*
 
 // ---------------------------------------------------------------- MXFP4
 
-idx_status idx_mxfp4_to_e4m3(const uint8_t* x, const uint8_t* sf, long long n, int D,
-                             uint8_t* out, const idx_options* opt, void* stream) {
-    if (n < 0 || D < 32 || D % 32 != 0) return IDX_EINVAL;
-    if (n == 0) return IDX_OK;
-    if (!x || !sf || !out) return IDX_EINVAL;
-    if (!aligned(x, 16) || !aligned(out, 16)) return IDX_EALIGN;
+namespace {
+
+// One expansion launch over one or two arrays (seg[1].n == 0: one).
+idx_status mxfp4_launch(const Mxfp4Segment& s0, const Mxfp4Segment& s1, int D,
+                        const idx_options* opt, void* stream) {
+    if (D < 32 || D % 32 != 0) return IDX_EINVAL;
+    const Mxfp4Segment* seg[2] = {&s0, &s1};
+    for (const Mxfp4Segment* g : seg) {
+        if (g->n < 0) return IDX_EINVAL;
+        if (g->n == 0) continue;
+        if (!g->x || !g->sf || !g->out) return IDX_EINVAL;
+        if (!aligned(g->x, 16) || !aligned(g->out, 16)) return IDX_EALIGN;
+    }
+    if (s0.n + s1.n == 0) return IDX_OK;
     if (!arch_ok()) return IDX_EUNSUPPORTED;
     Mxfp4Args a;
-    a.x = x;
-    a.sf = sf;
-    a.n = n;
+    a.seg[0] = s0;
+    a.seg[1] = s1;
     a.D = D;
-    a.out = out;
     a.d_status = opt ? opt->d_status : nullptr;
-    const cudaError_t e = launch_mxfp4_to_e4m3(a, sm_count(), static_cast<cudaStream_t>(stream));
+    const cudaError_t e = launch_mxfp4_to_e4m3(a, static_cast<cudaStream_t>(stream));
     if (e == cudaSuccess) count_launches(1);
     return cuda_status(e);
+}
+
+}  // namespace
+
+idx_status idx_mxfp4_to_e4m3(const uint8_t* x, const uint8_t* sf, long long n, int D,
+                             uint8_t* out, const idx_options* opt, void* stream) {
+    return mxfp4_launch(Mxfp4Segment{x, sf, n, out}, Mxfp4Segment{nullptr, nullptr, 0, nullptr},
+                        D, opt, stream);
 }
 
 namespace {
@@ -698,15 +712,15 @@ Mxfp4Layout mxfp4_layout(int rows, long long keys, int H, int D, size_t rest_byt
     return L;
 }
 
-// Expand q and k into the workspace (after the checks every MXFP4 entry point makes).
+// Expand q and k into the workspace in one launch (after the checks every
+// MXFP4 entry point makes).
 idx_status mxfp4_expand_qk(const uint8_t* q, const uint8_t* q_sf, const uint8_t* k,
                            const uint8_t* k_sf, int rows, long long keys, int H, int D,
                            uint8_t* base, const Mxfp4Layout& L, const idx_options* opt,
                            void* stream) {
     if (!q || !q_sf || !k || !k_sf) return IDX_EINVAL;
-    idx_status st = idx_mxfp4_to_e4m3(q, q_sf, (long long)rows * H, D, base + L.q8, opt, stream);
-    if (st != IDX_OK) return st;
-    return idx_mxfp4_to_e4m3(k, k_sf, keys, D, base + L.k8, opt, stream);
+    return mxfp4_launch(Mxfp4Segment{q, q_sf, (long long)rows * H, base + L.q8},
+                        Mxfp4Segment{k, k_sf, keys, base + L.k8}, D, opt, stream);
 }
 
 }  // namespace

@@ -54,6 +54,30 @@ def test_expansion_is_exact_in_range(idx):
     assert stats.read()["status"] == 0
 
 
+def test_expansion_every_scale_code(idx):
+    """All 256 e8m0 codes in one launch, in-range and out-of-range blocks side
+    by side within a warp: an element exact in e4m3 is that value, one above
+    448 saturates to ±448, one below the subnormals (or between two of them)
+    flushes to ±0, signs kept (the NaN code 255 reads as 2^128: everything
+    nonzero saturates), and the launch raises IDX_DEV_RANGE."""
+    g = torch.Generator().manual_seed(83)
+    n, D = 256, 128
+    x = torch.randint(0, 256, (n, D // 2), generator=g, dtype=torch.uint8)
+    sf = (torch.randperm(n * D // 32, generator=g) % 256).to(torch.uint8).reshape(n, D // 32)
+    stats = idx.Stats(torch.device(DEV))
+    got = idx.idx_mxfp4_to_e4m3(x.to(DEV), sf.to(DEV), stats=stats)
+    torch.cuda.synchronize()
+    v = decode(x, sf)
+    f8 = torch.from_numpy(v).to(torch.float32).to(torch.float8_e4m3fn)
+    exact = f8.to(torch.float64).numpy() == v
+    sign = np.where(np.signbit(v), 0x80, 0x00)
+    want = np.where(exact, f8.view(torch.uint8).numpy(),
+                    np.where(np.abs(v) > 448.0, sign | 0x7E, sign)).astype(np.uint8)
+    assert (~exact).any() and exact.any()
+    assert np.array_equal(got.cpu().view(torch.uint8).numpy(), want)
+    assert stats.read()["status"] & IDX_DEV_RANGE
+
+
 @pytest.mark.parametrize("code,what", [(127 + 7, "saturates"), (127 - 12, "flushes")])
 def test_expansion_out_of_range_raises(idx, code, what):
     x = torch.full((4, 32), 0x77, dtype=torch.uint8)  # every element 6.0
