@@ -475,6 +475,7 @@ idx_status idx_score_topk(const void* q, const void* k, const float* k_scale, co
     c.d_stats = d_stats;
     c.fallback = 0;
     c.grid_limit = 2 * sm_count();
+    c.sm_count = sm_count();
     c.pdl = 1;  // after the emit pass
     if ((e = launch_cand_topk(c, s)) != cudaSuccess) return cuda_status(e);
     count_launches(1);

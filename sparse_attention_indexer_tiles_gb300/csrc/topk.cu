@@ -12,10 +12,11 @@
 //  * the same kernel in threshold mode returns only the exact t-th largest
 //    key of each row; the fused path uses it on the strided score sample
 //    (page "[sglang] logits를 쓰지 않는 top-k", section 2).
-//  * cand_topk_kernel   one CTA per row of the candidate slab held in shared
-//                       memory (page 1: the small top-k over ~2.25 x topk
-//                       candidates); flags rows whose slab is short or
-//                       overflowed for the exact rescan.
+//  * cand_topk_kernel   one CTA per row of the candidate slab (page 1: the
+//                       small top-k over ~2.25 x topk candidates), read from
+//                       global memory by every pass or, with key splits,
+//                       copied into shared memory first; flags rows whose
+//                       slab is short or overflowed for the exact rescan.
 #include "plan.cuh"
 #include "radix.cuh"
 #include "threshold.cuh"
@@ -1211,29 +1212,45 @@ topk_split_kernel(TopkRowsArgs a) {
 //
 // Page 1, "Sampled Threshold": the small exact top-k over the ~2.25 x topk
 // candidates of a row.  The scoring pass leaves each row's candidates in runs
-// of (score, row-relative index) pairs, each run in ascending index order
-// (eight runs per key split; the rescan's re-emission uses the first eight).
-// One CTA of 256 threads per row:
-//   1. copies the runs into shared memory with one bulk copy per run (run
-//      lengths rounded up to an even count, the extra slot marked empty) and
-//      turns the scores into order keys;
-//   2. finds the exact threshold key T by radix selection that starts below
-//      the bits all candidates share (their maximum and minimum agree there):
-//      one digit of up to 10 bits over every candidate, then, when that digit
-//      holds at most kCandGather candidates, they are gathered and the one
-//      ranked need-th by (key descending, index ascending) fixes T and the
-//      index cut at once (else the digit passes continue over all candidates);
-//   3. keeps the lowest indices among the keys equal to T;
-//   4. writes the selected indices in ascending order: they are bucketed by
-//      index (1024 buckets of a power-of-two width), the buckets placed by a
-//      scan, and each index placed in its bucket by its rank among the
-//      bucket's indices.
-// Rows whose candidate count fell below topk, or whose runs overflowed, are
-// flagged for the exact rescan instead.
+// of (score, row-relative index) pairs (eight runs per key split; the
+// rescan's re-emission uses the first eight).  One CTA of 256 threads per row.
+// A launch of many rows reads the runs from global memory in every pass (warp
+// w the runs w, w + 8, ...; a row's ~26 KB stay in L1/L2 between its passes)
+// and keeps no copy, so that six rows share an SM.  A launch of fewer rows
+// than three per SM over more than 64 runs (decode-like: a few rows whose
+// keys were split over many CTAs, so many short runs) first copies each row's
+// runs into shared memory, one bulk copy each (run lengths rounded up to an
+// even count, the extra slot marked empty), and the passes read that copy.
+// Then:
+//   1. a histogram of 1024 bins of the candidates' order keys above a base B.
+//      A row with a sampled threshold has every candidate at or above it, so
+//      B is that threshold and a bin is 2^14 keys wide (the bins span two
+//      octaves of the score above B; larger keys share the top bin); another
+//      row takes B = its smallest key and bins just wide enough for its
+//      largest (one more pass);
+//   2. the bin b that holds the topk-th largest key, scanned from the top:
+//      every candidate of a higher bin is selected, and when b holds at most
+//      kCandGather candidates they are gathered and the `need` of them ranked
+//      first by (key descending, index ascending) are selected; a fuller bin
+//      is resolved by radix selection over its keys (8-bit digits), then over
+//      the indices of the keys tied at the threshold;
+//   3. the selected indices in ascending order: from a bitmap over the row's
+//      indices (rows of up to 32 x kCandBitmapWords keys), else from a list
+//      bucketed by index (1024 buckets of a power-of-two width), the buckets
+//      placed by a scan and each index placed by its rank within its bucket.
+// Rows whose candidate count fell below topk, or that held more than a whole
+// row's slab (eight runs) or lost candidates to a full run, are flagged for
+// the exact rescan instead.
 
 constexpr int kCandThreads = 256;
 constexpr int kCandWarps = kCandThreads / 32;
-constexpr uint32_t kEmptyKey = 0u;  // below the key of every finite score
+constexpr int kCandBins = 1024;
+constexpr int kCandGather = 256;        // candidates of the threshold bin ranked directly
+constexpr int kCandBitmapWords = 4096;  // the bitmap output covers rows of up to 131072 keys
+constexpr int kCandRelShift = 14;       // bin width above a sampled threshold: 2^14 keys
+constexpr int kCandU = 4;               // pairs per lane in flight (streamed rows)
+constexpr uint32_t kEmptyKey = 0u;      // a padding slot of a copied run (no finite score)
+constexpr int kCandStreamRuns = 8 * kRuns;  // launches of few rows and more runs copy them
 
 // Block-wide maximum and minimum of one value per thread (scratch >= 16 words).
 IDX_DEVI void block_max_min(uint32_t& mx, uint32_t& mn, uint32_t* scratch) {
@@ -1258,139 +1275,158 @@ IDX_DEVI void block_max_min(uint32_t& mx, uint32_t& mn, uint32_t* scratch) {
     __syncthreads();
 }
 
-// One digit of a radix selection from the top: among the elements e < cnt
-// with valid(e) whose value v = val(e) has bits above `shift + width` equal to
-// `pre`, histogram the digit (v >> shift) & (2^width - 1) in per-warp bins and
-// pick the digit that holds the need-th largest.  Returns the digit; *above =
-// elements of larger digits, *count = elements of that digit.
-template <class Valid, class Val>
-IDX_DEVI uint32_t cand_digit(uint32_t cnt, uint32_t need, int shift, int width, uint64_t pre,
-                             Valid valid, Val val, uint32_t* hist, uint32_t* scratch,
-                             uint32_t* above, uint32_t* count) {
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    uint32_t* hw = hist + w * 256;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) hw[lane * 8 + j] = 0u;
-    __syncthreads();
-    const uint32_t mask = (1u << width) - 1u;
-    for (uint32_t base = 0; base < cnt; base += 4 * kCandThreads) {
-        uint32_t v[4];
-        bool in[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const uint32_t e = base + u * kCandThreads + threadIdx.x;
-            in[u] = e < cnt && valid(e);
-            v[u] = in[u] ? val(e) : 0u;
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-            if (in[u] && ((uint64_t)v[u] >> (shift + width)) == pre)
-                atomicAdd(&hw[(v[u] >> shift) & mask], 1u);
-    }
-    __syncthreads();
-    // thread t owns digit 255 - t: a scan from the top digit down
-    uint32_t c = 0;
-#pragma unroll
-    for (int ww = 0; ww < kCandWarps; ++ww) c += hist[ww * 256 + 255 - threadIdx.x];
-    const uint32_t incl = block_incl_scan<kCandThreads>(c, scratch, nullptr);
-    const uint32_t excl = incl - c;
-    if (excl < need && need <= incl) {
-        scratch[40] = 255u - threadIdx.x;
-        scratch[41] = excl;
-        scratch[42] = c;
-    }
-    __syncthreads();
-    const uint32_t d = scratch[40];
-    *above = scratch[41];
-    *count = scratch[42];
-    __syncthreads();
-    return d;
-}
-
-// Exact need-th largest value, walking digits of <= 8 bits from bit `top`
-// down to bit 0 among the elements whose bits above `top` equal `pre`.
-// Returns the value; *need_at = how many elements equal to it are taken.
-template <class Valid, class Val>
-IDX_DEVI uint32_t cand_select(uint32_t cnt, uint32_t need, int top, uint64_t pre, Valid valid,
-                              Val val, uint32_t* hist, uint32_t* scratch, uint32_t* need_at) {
-    int bit = top + 1;
-    while (bit > 0) {
-        const int width = bit >= 8 ? 8 : bit;
-        const int shift = bit - width;
-        uint32_t above, count;
-        const uint32_t d =
-            cand_digit(cnt, need, shift, width, pre, valid, val, hist, scratch, &above, &count);
-        need -= above;
-        pre = (pre << width) | d;
-        bit = shift;
-    }
-    *need_at = need;
-    return (uint32_t)pre;
-}
-
-// Shared memory of cand_topk_kernel, in 32-bit words.  The per-warp
-// histograms and the compacted selection share one region (the selection is
-// written once the histograms are no longer read).
-constexpr int kCandBins = 1024;   // first-digit bins, and output buckets
-constexpr int kCandGather = 256;  // candidates of the threshold digit ranked alone
-struct CandSmem {
-    int nruns, topk, cap;  // cap: pairs the row buffer holds
-    __host__ __device__ CandSmem(int nruns_, int topk_, int cap_q) : nruns(nruns_), topk(topk_) {
-        cap = kRuns * cap_q + nruns;
-    }
-    __host__ __device__ int hist() const { return 0; }  // [1024]: digit bins, then buckets
-    __host__ __device__ int sel() const { return kCandBins; }               // [topk]
-    // 16-byte boundaries for the mbarrier (8-byte aligned) and the bulk-copy
-    // destination (16-byte aligned); the dynamic shared memory base is 16-byte aligned
-    // (cand_select's per-warp histograms take 8 x 256 words from 0: before the
-    // selection is written they may cover sel, never scratch and what follows)
-    __host__ __device__ int scratch() const {
-        const int e = (sel() + topk + 3) / 4 * 4;
-        return e > kCandWarps * 256 ? e : kCandWarps * 256;
-    }  // 64
-    __host__ __device__ int bar() const { return scratch() + 64; }          // 2 (8-byte aligned)
-    __host__ __device__ int run_off() const { return bar() + 2; }           // [nruns + 1]
-    // the gathered candidates of the threshold digit live in sel (written
-    // later) when it is large enough, else after the run offsets
-    __host__ __device__ bool gather_in_sel() const { return topk >= 2 * kCandGather; }
-    __host__ __device__ int gather() const {
-        return gather_in_sel() ? sel() : (run_off() + nruns + 1 + 1) / 2 * 2;
-    }
-    __host__ __device__ int pairs() const {
-        const int end = gather_in_sel() ? run_off() + nruns + 1 : gather() + 2 * kCandGather;
-        return (end + 3) / 4 * 4;
-    }
-    __host__ __device__ int words() const { return pairs() + 2 * cap; }
+// A row's candidates.  Streamed: run q holds cnt[q] pairs from srow + q * cap_q
+// in global memory.  Staged: `pairs` holds n pairs (padding slots included)
+// in shared memory.
+struct CandRow {
+    const int2* srow;
+    const uint32_t* cnt;
+    int nruns, cap_q;
+    const int2* pairs;
+    uint32_t n;
 };
 
-__global__ void __launch_bounds__(kCandThreads)
+// f(key, index) for every candidate of a row.  Streamed: warp w reads runs w,
+// w + 8, ..., kCandU pairs per lane in flight.
+template <bool STAGED, class F>
+IDX_DEVI void cand_each(const CandRow& R, F&& f) {
+    if (STAGED) {
+        for (uint32_t e = threadIdx.x; e < R.n; e += kCandThreads) {
+            const int2 v = R.pairs[e];
+            const uint32_t key = fkey(__int_as_float(v.x));
+            if (key != kEmptyKey) f(key, (uint32_t)v.y);
+        }
+        return;
+    }
+    const int lane = threadIdx.x & 31;
+    for (int q = threadIdx.x >> 5; q < R.nruns; q += kCandWarps) {
+        const int c = (int)R.cnt[q];
+        const int2* src = R.srow + (long long)q * R.cap_q;
+        for (int j0 = 0; j0 < c; j0 += 32 * kCandU) {
+            int2 v[kCandU];
+#pragma unroll
+            for (int u = 0; u < kCandU; ++u) {
+                const int j = j0 + 32 * u + lane;
+                v[u] = j < c ? __ldg(src + j) : make_int2(0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < kCandU; ++u)
+                if (j0 + 32 * u + lane < c) f(fkey(__int_as_float(v[u].x)), (uint32_t)v[u].y);
+        }
+    }
+}
+
+// The bin of a histogram of nb <= 1024 bins that holds the need-th largest
+// element (count(> b) < need <= count(>= b), 1 <= need <= the total); every
+// thread gets it.  scratch: [0, 8) the scan, [40, 43) the result.
+IDX_DEVI DigitPick cand_pick(const uint32_t* hist, int nb, uint32_t need, uint32_t* scratch) {
+    constexpr int BPT = kCandBins / kCandThreads;
+    const int t = threadIdx.x;
+    uint32_t c[BPT], loc = 0;
+#pragma unroll
+    for (int j = 0; j < BPT; ++j) {
+        const int b = nb - 1 - (BPT * t + j);
+        c[j] = b >= 0 ? hist[b] : 0u;
+        loc += c[j];
+    }
+    const uint32_t incl = block_incl_scan<kCandThreads>(loc, scratch, nullptr);
+    uint32_t cum = incl - loc;
+    if (cum < need && need <= incl) {
+#pragma unroll
+        for (int j = 0; j < BPT; ++j) {
+            if (cum + c[j] >= need) {
+                scratch[40] = (uint32_t)(nb - 1 - (BPT * t + j));
+                scratch[41] = cum;
+                scratch[42] = c[j];
+                break;
+            }
+            cum += c[j];
+        }
+    }
+    __syncthreads();
+    const DigitPick p{scratch[40], scratch[41], scratch[42]};
+    __syncthreads();
+    return p;
+}
+
+// The need-th largest v = val(key, index) among the candidates with
+// in(key, index), by 8-bit digits from the top (four passes);
+// *need_at = how many of the elements equal to it are taken.
+template <bool STAGED, class In, class Val>
+IDX_DEVI uint32_t cand_radix_select(const CandRow& R, uint32_t need, In in, Val val,
+                                    uint32_t* hist, uint32_t* scratch, uint32_t* need_at) {
+    uint32_t pre = 0u;
+    for (int shift = 24; shift >= 0; shift -= 8) {
+        for (int i = threadIdx.x; i < 256; i += kCandThreads) hist[i] = 0u;
+        __syncthreads();
+        const uint32_t above_mask = shift == 24 ? 0u : ~0u << (shift + 8);
+        cand_each<STAGED>(R, [&](uint32_t key, uint32_t ix) {
+            if (!in(key, ix)) return;
+            const uint32_t v = val(key, ix);
+            if ((v & above_mask) == pre) atomicAdd(&hist[(v >> shift) & 255u], 1u);
+        });
+        __syncthreads();
+        const DigitPick p = cand_pick(hist, 256, need, scratch);
+        need -= p.above;
+        pre |= p.digit << shift;
+    }
+    *need_at = need;
+    return pre;
+}
+
+// Shared memory of cand_topk_kernel, in 32-bit words.
+struct CandSmem {
+    int nruns, topk, cap_q;
+    bool staged;
+    __host__ __device__ CandSmem(int nruns_, int topk_, int cap_q_, bool staged_)
+        : nruns(nruns_), topk(topk_), cap_q(cap_q_), staged(staged_) {}
+    // the bitmap, or the selected indices and their ordered copy (2 x topk)
+    __host__ __device__ int region_words() const {
+        return 2 * topk > kCandBitmapWords ? 2 * topk : kCandBitmapWords;
+    }
+    // staged pairs: a whole row's slab (eight runs) plus a padding slot per run
+    __host__ __device__ int cap() const { return staged ? kRuns * cap_q + nruns : 0; }
+    __host__ __device__ int hist() const { return 0; }                         // [1024]
+    __host__ __device__ int region() const { return kCandBins; }
+    __host__ __device__ int gather() const { return region() + region_words(); }  // [256] x 2
+    __host__ __device__ int scratch() const { return gather() + 2 * kCandGather; }  // [64]
+    __host__ __device__ int bar() const { return scratch() + 64; }             // 2 (8-byte aligned)
+    __host__ __device__ int runs() const { return bar() + 2; }                 // [nruns]
+    __host__ __device__ int offs() const { return runs() + nruns; }            // [nruns + 1] staged
+    __host__ __device__ int pairs() const {
+        return (offs() + (staged ? nruns + 1 : 0) + 3) / 4 * 4;  // 16-byte aligned
+    }
+    __host__ __device__ int words() const { return pairs() + 2 * cap(); }
+};
+
+template <bool STAGED>
+__global__ void __launch_bounds__(kCandThreads, STAGED ? 1 : 6)  // streamed: six rows per SM
 cand_topk_kernel(CandArgs a) {
     constexpr int THREADS = kCandThreads;
     extern __shared__ __align__(16) uint32_t smem[];
     pdl_wait();
-    const CandSmem L(a.nruns, a.topk, a.cap_q);
+    const CandSmem L(a.nruns, a.topk, a.cap_q, STAGED);
     uint32_t* hist = smem + L.hist();
-    uint32_t* scratch = smem + L.scratch();  // [0,35) scans, [40,48) results, [48,64) row state
+    uint32_t* reg = smem + L.region();
+    uint2* gat = reinterpret_cast<uint2*>(smem + L.gather());  // (key, index)
+    uint32_t* scratch = smem + L.scratch();  // [0,16) scans, [40,43) picks, [48,53) row state
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L.bar());
-    uint32_t* run_off = smem + L.run_off();
-    uint32_t* sel = smem + L.sel();
-    int2* cmp = reinterpret_cast<int2*>(smem + L.gather());  // (key, index) of one digit
+    uint32_t* cnt = smem + L.runs();         // run lengths (capped)
+    uint32_t* offs = smem + L.offs();        // staged: where each run's copy starts
     int2* pairs = reinterpret_cast<int2*>(smem + L.pairs());
     const int tid = threadIdx.x;
-    const int CR = a.nruns * a.cap_q;  // slab row (all key splits)
+    const long long CR = (long long)a.nruns * a.cap_q;  // slab row (all key splits)
     const uint32_t k = (uint32_t)a.topk;
 
     if (a.fallback && *(volatile int*)(a.fb_cnt + 6) == 0) return;  // no row was re-emitted
-    if (tid == 0) {
+    if (STAGED && tid == 0) {
         mbar_init(bar, 1);
         fence_barrier_init();
     }
     uint32_t phase = 0;
     // runs of this thread: a contiguous range, so that offsets follow run order
     const int per = (a.nruns + THREADS - 1) / THREADS;
-    const int q0 = tid * per < a.nruns ? tid * per : a.nruns;
-    const int q1 = q0 + per < a.nruns ? q0 + per : a.nruns;
-
+    const int q0 = min(a.nruns, tid * per), q1 = min(a.nruns, q0 + per);
     for (int r = blockIdx.x; r < a.rows; r += gridDim.x) {
         __syncthreads();  // the previous row's shared state is no longer read
         RowPlan* plan = a.plan + r;
@@ -1399,6 +1435,9 @@ cand_topk_kernel(CandArgs a) {
         if (tid == 0) {
             scratch[48] = (uint32_t)plan->state;
             scratch[49] = 0u;  // candidates (uncapped)
+            scratch[50] = plan->thr;
+            scratch[51] = 0u;  // gathered
+            scratch[52] = 0u;  // listed
         }
         __syncthreads();
         const int state = (int)scratch[48];
@@ -1410,31 +1449,26 @@ cand_topk_kernel(CandArgs a) {
             continue;
         }
 
-        // ---- run offsets (even lengths, 16-byte aligned copies)
+        // ---- run lengths
         const int* rc = a.run_cnt + (long long)r * a.nruns;
-        uint32_t lpad = 0, lcnt = 0;
+        const int2* srow = a.slab + (long long)r * CR;
+        uint32_t lcnt = 0, lpad = 0;
         bool ltr = false;
-        for (int q = q0; q < q1; ++q) {
+        for (int q = STAGED ? q0 : tid; q < (STAGED ? q1 : a.nruns); q += STAGED ? 1 : THREADS) {
             const uint32_t c = (uint32_t)rc[q];
             const uint32_t cl = c < (uint32_t)a.cap_q ? c : (uint32_t)a.cap_q;
             ltr |= c > (uint32_t)a.cap_q;
             lcnt += c;
             lpad += (cl + 1u) & ~1u;
+            cnt[q] = cl;
         }
-        uint32_t ptot;
-        uint32_t off = block_incl_scan<THREADS>(lpad, scratch, &ptot) - lpad;
-        for (int q = q0; q < q1; ++q) {
-            const uint32_t c = (uint32_t)rc[q];
-            const uint32_t cl = c < (uint32_t)a.cap_q ? c : (uint32_t)a.cap_q;
-            run_off[q] = off;
-            off += (cl + 1u) & ~1u;
-        }
-        if (tid == 0) run_off[a.nruns] = ptot;
-        atomicAdd(&scratch[49], lcnt);
-        // more candidates than the buffer holds (possible with key splits):
-        // the exact rescan takes the row
-        const bool trunc = __syncthreads_or(ltr || ptot > (uint32_t)L.cap);
+        if (lcnt) atomicAdd(&scratch[49], lcnt);
+        // a run that overflowed lost candidates, and a row of key splits may
+        // hold more than the slab of a whole row (eight runs): either way the
+        // exact rescan takes the row
+        const bool lost = __syncthreads_or(ltr);
         const uint32_t total = scratch[49];
+        const bool trunc = lost || total > (uint32_t)(kRuns * a.cap_q);
         if (tid == 0 && a.d_stats && !a.fallback) atomicMax(&a.d_stats->max_count, (int)total);
         if (trunc || total < k) {
             if (!a.fallback && !a.fb_hist) {
@@ -1471,157 +1505,129 @@ cand_topk_kernel(CandArgs a) {
             continue;
         }
 
-        // ---- the runs into shared memory, one bulk copy each
-        if (tid == 0) mbar_arrive_expect_tx(bar, ptot * (uint32_t)sizeof(int2));
-        __syncthreads();
-        const int2* srow = a.slab + (long long)r * CR;
-        for (int q = q0; q < q1; ++q) {
-            const uint32_t len = run_off[q + 1] - run_off[q];
-            if (len) bulk_g2s(pairs + run_off[q], srow + (long long)q * a.cap_q, len * 8u, bar);
+        CandRow R{srow, cnt, a.nruns, a.cap_q, pairs, 0u};
+        if (STAGED) {
+            // ---- the runs into shared memory, one bulk copy each (even
+            // lengths: 16-byte multiples; the runs hold them, cap_q is even)
+            uint32_t ptot;
+            uint32_t off = block_incl_scan<THREADS>(lpad, scratch, &ptot) - lpad;
+            for (int q = q0; q < q1; ++q) {
+                offs[q] = off;
+                off += (cnt[q] + 1u) & ~1u;
+            }
+            if (tid == 0) mbar_arrive_expect_tx(bar, ptot * (uint32_t)sizeof(int2));
+            __syncthreads();
+            for (int q = q0; q < q1; ++q) {
+                const uint32_t len = (cnt[q] + 1u) & ~1u;
+                if (len) bulk_g2s(pairs + offs[q], srow + (long long)q * a.cap_q, len * 8u, bar);
+            }
+            if (!mbar_wait(bar, phase, nullptr, 1ll << 30)) {
+                // copies that never completed: report and leave (bounded wait for them)
+                if (tid == 0) raise_status(a.d_status, IDX_DEV_TIMEOUT);
+                mbar_wait(bar, phase, nullptr, 1ll << 30);
+                return;
+            }
+            phase ^= 1u;
+            // the slot that rounded a run up to an even length holds no candidate
+            for (int q = q0; q < q1; ++q)
+                if (cnt[q] & 1u) pairs[offs[q] + cnt[q]].x = -1;  // order key kEmptyKey
+            __syncthreads();
+            R.n = ptot;
         }
-        if (!mbar_wait(bar, phase, nullptr, 1ll << 30)) {
-            // copies that never completed: report and leave (bounded wait for them)
-            if (tid == 0) raise_status(a.d_status, IDX_DEV_TIMEOUT);
-            mbar_wait(bar, phase, nullptr, 1ll << 30);
-            return;
-        }
-        phase ^= 1u;
-        // the slot that rounded a run up to an even length holds no candidate
-        for (int q = q0; q < q1; ++q) {
-            const uint32_t c = (uint32_t)rc[q];
-            const uint32_t cl = c < (uint32_t)a.cap_q ? c : (uint32_t)a.cap_q;
-            if (cl & 1u) pairs[run_off[q] + cl].x = -1;  // 0xffffffff: order key kEmptyKey
-        }
-        __syncthreads();
-        uint32_t mx = 0u, mn = 0xffffffffu;
-        for (uint32_t e = tid; e < ptot; e += THREADS) {
-            const uint32_t key = fkey(__int_as_float(pairs[e].x));
-            pairs[e].x = (int)key;
-            if (key != kEmptyKey) {
+
+        // ---- the bins: base B, width 2^sh
+        const uint32_t thr = scratch[50];
+        uint32_t B, sh;
+        if (!a.fallback && thr != 0u) {
+            B = thr;
+            sh = (uint32_t)kCandRelShift;
+        } else {
+            uint32_t mx = 0u, mn = 0xffffffffu;
+            cand_each<STAGED>(R, [&](uint32_t key, uint32_t) {
                 mx = max(mx, key);
                 mn = min(mn, key);
-            }
+            });
+            block_max_min(mx, mn, scratch);
+            B = mn;
+            const uint32_t span = mx - mn;
+            sh = span < (uint32_t)kCandBins ? 0u : (uint32_t)(32 - __clz(span)) - 10u;
         }
+        auto bin = [&](uint32_t key) -> uint32_t {
+            if (key < B) return 0u;
+            const uint32_t d = (key - B) >> sh;
+            return d < (uint32_t)kCandBins ? d : (uint32_t)kCandBins - 1u;
+        };
+        const bool use_bm = n <= 32ll * L.region_words();
+        const uint32_t bm_words = use_bm ? (uint32_t)((n + 31) / 32) : 0u;
+        for (int i = tid; i < kCandBins; i += THREADS) hist[i] = 0u;
+        for (uint32_t i = tid; i < bm_words; i += THREADS) reg[i] = 0u;
         __syncthreads();
-        block_max_min(mx, mn, scratch);
-
-        // ---- the selection rule: key > T, or key == T and index <= idx_cut
-        auto key_of = [&](uint32_t e) { return (uint32_t)pairs[e].x; };
-        auto real = [&](uint32_t e) { return (uint32_t)pairs[e].x != kEmptyKey; };
-        uint32_t T = mx, need = k, idx_cut = 0xffffffffu;
-        bool gathered = false;
-        if (mx != mn) {
-            // one digit of up to 10 bits from the highest bit in which the
-            // candidates differ, over one 1024-bin histogram
-            const int top = 31 - __clz(mx ^ mn);
-            const int width = top + 1 >= 10 ? 10 : top + 1;
-            const int shift = top + 1 - width;
-            const uint32_t nb = 1u << width;
-            for (int i = tid; i < kCandBins; i += THREADS) hist[i] = 0u;
-            __syncthreads();
-            for (uint32_t e = tid; e < ptot; e += THREADS) {
-                const uint32_t key = key_of(e);
-                if (key != kEmptyKey) atomicAdd(&hist[(key >> shift) & (nb - 1u)], 1u);
-            }
-            __syncthreads();
-            // thread t owns the 4 bins 1023 - 4t ... 1020 - 4t, scanned from the top
-            constexpr int BPT = kCandBins / THREADS;
-            uint32_t cb[BPT], loc = 0;
-#pragma unroll
-            for (int j = 0; j < BPT; ++j) {
-                cb[j] = hist[kCandBins - 1 - (BPT * tid + j)];
-                loc += cb[j];
-            }
-            const uint32_t incl = block_incl_scan<THREADS>(loc, scratch, nullptr);
-            uint32_t cum = incl - loc;
-            if (cum < k && k <= incl) {
-#pragma unroll
-                for (int j = 0; j < BPT; ++j) {
-                    if (cum + cb[j] >= k) {
-                        scratch[40] = (uint32_t)(kCandBins - 1 - (BPT * tid + j));
-                        scratch[41] = cum;
-                        scratch[42] = cb[j];
-                        break;
-                    }
-                    cum += cb[j];
-                }
-            }
-            __syncthreads();
-            const uint32_t d = scratch[40], count = scratch[42];
-            need = k - scratch[41];
-            const uint64_t pre = (((uint64_t)mx >> (top + 1)) << width) | d;
-            if (count <= (uint32_t)kCandGather) {
-                // gather that digit's candidates; the one ranked need-th among
-                // them by (key desc, index asc) fixes T and idx_cut at once
-                if (tid == 0) scratch[50] = 0u;
-                __syncthreads();
-                for (uint32_t e = tid; e < ptot; e += THREADS) {
-                    const int2 pv = pairs[e];
-                    if ((uint32_t)pv.x != kEmptyKey && ((uint64_t)(uint32_t)pv.x >> shift) == pre)
-                        cmp[atomicAdd(&scratch[50], 1u)] = pv;
-                }
-                __syncthreads();
-                const uint32_t ng = scratch[50];
-                for (uint32_t i = tid; i < ng; i += THREADS) {
-                    const uint32_t ki = (uint32_t)cmp[i].x, xi = (uint32_t)cmp[i].y;
-                    uint32_t rank = 0;
-                    for (uint32_t j = 0; j < ng; ++j) {
-                        const int2 cj = cmp[j];
-                        rank += (uint32_t)cj.x > ki || ((uint32_t)cj.x == ki && (uint32_t)cj.y < xi);
-                    }
-                    if (rank == need - 1u) {
-                        scratch[51] = ki;
-                        scratch[52] = xi;
-                    }
-                }
-                __syncthreads();
-                T = scratch[51];
-                idx_cut = scratch[52];
-                gathered = true;
-            } else if (shift == 0) {
-                T = (uint32_t)pre;
+        cand_each<STAGED>(R, [&](uint32_t key, uint32_t) { atomicAdd(&hist[bin(key)], 1u); });
+        __syncthreads();
+        const DigitPick pk = cand_pick(hist, kCandBins, k, scratch);
+        const uint32_t bs = pk.digit, need = k - pk.above;
+        const bool direct = pk.count <= (uint32_t)kCandGather;
+        // a selected index: its bit, or an entry of the (unordered) list
+        auto mark = [&](uint32_t ix) {
+            if (use_bm) {
+                atomicOr(&reg[ix >> 5], 1u << (ix & 31u));
             } else {
-                T = cand_select(ptot, need, shift - 1, pre, real, key_of, hist, scratch, &need);
+                const uint32_t p = atomicAdd(&scratch[52], 1u);
+                if (p < k) reg[p] = ix;
             }
-        }
-        if (!gathered) {
-            // the lowest `need` indices among the keys equal to T
+        };
+
+        // ---- the higher bins, and the threshold bin's candidates
+        cand_each<STAGED>(R, [&](uint32_t key, uint32_t ix) {
+            const uint32_t d = bin(key);
+            if (d > bs)
+                mark(ix);
+            else if (d == bs && direct)
+                gat[atomicAdd(&scratch[51], 1u)] = make_uint2(key, ix);
+        });
+        __syncthreads();
+        if (direct) {
+            const uint32_t ng = scratch[51];
+            for (uint32_t i = tid; i < ng; i += THREADS) {
+                const uint2 gi = gat[i];
+                uint32_t rank = 0;
+                for (uint32_t j = 0; j < ng; ++j) {
+                    const uint2 gj = gat[j];
+                    rank += gj.x > gi.x || (gj.x == gi.x && gj.y < gi.y);
+                }
+                if (rank < need) mark(gi.y);
+            }
+        } else {
+            // T = the need-th largest key of the bin, then the lowest indices
+            // among the keys equal to T
+            uint32_t need_t;
+            const uint32_t T = cand_radix_select<STAGED>(
+                R, need, [&](uint32_t key, uint32_t) { return bin(key) == bs; },
+                [](uint32_t key, uint32_t) { return key; }, hist, scratch, &need_t);
             uint32_t nt = 0;
-            for (uint32_t e = tid; e < ptot; e += THREADS) nt += key_of(e) == T;
+            cand_each<STAGED>(R, [&](uint32_t key, uint32_t) { nt += key == T; });
             uint32_t ntie;
             block_incl_scan<THREADS>(nt, scratch, &ntie);
-            if (ntie > need) {
+            uint32_t cut = 0xffffffffu;
+            if (ntie > need_t) {
                 uint32_t unused;
-                idx_cut = ~cand_select(
-                    ptot, need, 31, 0ull, [&](uint32_t e) { return key_of(e) == T; },
-                    [&](uint32_t e) { return ~(uint32_t)pairs[e].y; }, hist, scratch, &unused);
+                cut = ~cand_radix_select<STAGED>(
+                    R, need_t, [&](uint32_t key, uint32_t) { return key == T; },
+                    [](uint32_t, uint32_t ix) { return ~ix; }, hist, scratch, &unused);
             }
+            cand_each<STAGED>(R, [&](uint32_t key, uint32_t ix) {
+                if (bin(key) == bs && (key > T || (key == T && ix <= cut))) mark(ix);
+            });
         }
-        __syncthreads();  // the histograms are done: the bucket counts reuse them
-
-        auto chosen = [&](int2 pv) {
-            const uint32_t key = (uint32_t)pv.x;
-            return key > T || (key == T && (uint32_t)pv.y <= idx_cut);
-        };
-        // ---- ascending output, rows of at most 32 (1024 + topk) keys: a bitmap
-        // over the row's indices in the histogram and selection words (scratch
-        // follows them), one bit set per selected index; each thread then owns
-        // a contiguous range of bitmap words and writes the indices of their
-        // set bits from its offset in a block scan of the bit counts
-        const uint32_t bm_words = (uint32_t)((n + 31) / 32);
-        if (bm_words <= (uint32_t)L.sel() + (uint32_t)a.topk) {
-            uint32_t* bm = smem + L.hist();
-            for (uint32_t i = tid; i < bm_words; i += THREADS) bm[i] = 0u;
-            __syncthreads();
-            for (uint32_t e = tid; e < ptot; e += THREADS) {
-                const int2 pv = pairs[e];
-                if (chosen(pv)) atomicOr(&bm[(uint32_t)pv.y >> 5], 1u << ((uint32_t)pv.y & 31u));
-            }
-            __syncthreads();
+        __syncthreads();
+        if (use_bm) {
+            // ---- ascending output from the bitmap: each thread owns a
+            // contiguous range of words and writes the indices of their set
+            // bits from its offset in a block scan of the bit counts
             const uint32_t per = (bm_words + THREADS - 1) / THREADS;
             const uint32_t w0 = min(bm_words, tid * per), w1 = min(bm_words, w0 + per);
             uint32_t c = 0;
-            for (uint32_t i = w0; i < w1; ++i) c += __popc(bm[i]);
+            for (uint32_t i = w0; i < w1; ++i) c += __popc(reg[i]);
             uint32_t nsel;
             uint32_t pos = block_incl_scan<THREADS>(c, scratch, &nsel) - c;
             if (nsel != k) {
@@ -1635,7 +1641,7 @@ cand_topk_kernel(CandArgs a) {
                 continue;
             }
             for (uint32_t i = w0; i < w1; ++i) {
-                uint32_t m = bm[i];
+                uint32_t m = reg[i];
                 while (m) {
                     const int b = __ffs(m) - 1;
                     m &= m - 1u;
@@ -1645,19 +1651,23 @@ cand_topk_kernel(CandArgs a) {
             if (tid == 0) plan->state = ST_DONE;
             continue;
         }
-        // ---- ascending output, longer rows: the selected indices bucketed by
-        // index (1024 buckets of a power-of-two width over the row), buckets
-        // placed by a scan, and each entry placed in its bucket by its rank
-        // among the bucket's entries (a bucket holds at most its width of
-        // indices)
-        int bsh = 0;  // bucket width 2^bsh >= n / kCandBins
+        // ---- ascending output, longer rows: the listed indices bucketed by
+        // index (1024 buckets of width 2^bsh >= n / 1024), the buckets placed
+        // by a scan, and each index placed by its rank among its bucket's
+        if (scratch[52] != k) {
+            for (int i = tid; i < a.topk; i += THREADS) out[i] = -1;
+            if (tid == 0) {
+                raise_status(a.d_status, IDX_DEV_STATE);
+                plan->state = ST_DONE;
+            }
+            continue;
+        }
+        uint32_t* ord = reg + k;
+        int bsh = 0;
         while (((long long)kCandBins << bsh) < n) ++bsh;
         for (int i = tid; i < kCandBins; i += THREADS) hist[i] = 0u;
         __syncthreads();
-        for (uint32_t e = tid; e < ptot; e += THREADS) {
-            const int2 pv = pairs[e];
-            if (chosen(pv)) atomicAdd(&hist[(uint32_t)pv.y >> bsh], 1u);
-        }
+        for (uint32_t p = tid; p < k; p += THREADS) atomicAdd(&hist[reg[p] >> bsh], 1u);
         __syncthreads();
         {
             // bucket starts: thread t owns buckets BPT t .. BPT t + BPT - 1
@@ -1668,37 +1678,26 @@ cand_topk_kernel(CandArgs a) {
                 cb[j] = hist[BPT * tid + j];
                 loc += cb[j];
             }
-            uint32_t nsel;
-            uint32_t st = block_incl_scan<THREADS>(loc, scratch, &nsel) - loc;
+            uint32_t st = block_incl_scan<THREADS>(loc, scratch, nullptr) - loc;
 #pragma unroll
             for (int j = 0; j < BPT; ++j) {
                 hist[BPT * tid + j] = st;
                 st += cb[j];
             }
-            if (nsel != k) {
-                // cannot happen for finite scores: report it rather than write past
-                // the selection buffer
-                for (int i = tid; i < a.topk; i += THREADS) out[i] = -1;
-                if (tid == 0) {
-                    raise_status(a.d_status, IDX_DEV_STATE);
-                    plan->state = ST_DONE;
-                }
-                continue;
-            }
         }
         __syncthreads();
-        for (uint32_t e = tid; e < ptot; e += THREADS) {
-            const int2 pv = pairs[e];
-            if (chosen(pv)) sel[atomicAdd(&hist[(uint32_t)pv.y >> bsh], 1u)] = (uint32_t)pv.y;
+        for (uint32_t p = tid; p < k; p += THREADS) {
+            const uint32_t x = reg[p];
+            ord[atomicAdd(&hist[x >> bsh], 1u)] = x;
         }
         __syncthreads();
         // hist[b] is now the end of bucket b (the start of b + 1)
         for (uint32_t p = tid; p < k; p += THREADS) {
-            const uint32_t x = sel[p];
+            const uint32_t x = ord[p];
             const uint32_t b = x >> bsh;
             const uint32_t lo = b ? hist[b - 1] : 0u, hi = hist[b];
             uint32_t rank = 0;
-            for (uint32_t j = lo; j < hi; ++j) rank += sel[j] < x;
+            for (uint32_t j = lo; j < hi; ++j) rank += ord[j] < x;
             out[lo + rank] = (int)x;
         }
         if (tid == 0) plan->state = ST_DONE;
@@ -1755,25 +1754,27 @@ size_t split_workspace_bytes(int rows, int g) {
            (size_t)rows * sizeof(unsigned long long) + 256;
 }
 
-size_t cand_smem_bytes(int cap_q, int nruns, int topk) {
-    return (size_t)CandSmem(nruns, topk, cap_q).words() * sizeof(uint32_t);
+size_t cand_smem_bytes(int cap_q, int nruns, int topk, bool staged) {
+    return (size_t)CandSmem(nruns, topk, cap_q, staged).words() * sizeof(uint32_t);
 }
 
 cudaError_t launch_cand_topk(const CandArgs& a, cudaStream_t s) {
-    const CandSmem L(a.nruns, a.topk, a.cap_q);
-    // the mbarrier needs 8 bytes, the pair buffer (bulk copies) 16 bytes of alignment
-    if (L.bar() % 2 != 0 || L.gather() % 2 != 0 || L.pairs() % 4 != 0 || a.cap_q % 2 != 0)
+    bool staged = a.nruns > kCandStreamRuns && a.rows < 3 * a.sm_count &&
+                  cand_smem_bytes(a.cap_q, a.nruns, a.topk, true) <= 227u * 1024u;
+    const CandSmem L(a.nruns, a.topk, a.cap_q, staged);
+    // the gathered (key, index) pairs and the mbarrier are 8-byte aligned; the
+    // staged runs' bulk copies want 16-byte aligned runs
+    if (L.gather() % 2 != 0 || L.bar() % 2 != 0 || a.cap_q % 2 != 0)
         return cudaErrorInvalidValue;
-    const size_t sm = cand_smem_bytes(a.cap_q, a.nruns, a.topk);
-    cudaError_t e =
-        cudaFuncSetAttribute(cand_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    const size_t sm = cand_smem_bytes(a.cap_q, a.nruns, a.topk, staged);
+    auto kern = staged ? cand_topk_kernel<true> : cand_topk_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e != cudaSuccess) return e;
     if (a.rows == 0) return cudaSuccess;
     // the rescan's pass usually has no row to select: a short grid that strides
     // over the rows exits at once
     const int grid = a.fallback ? (a.rows < a.grid_limit ? a.rows : a.grid_limit) : a.rows;
-    return launch_k(cand_topk_kernel, dim3((unsigned)grid), dim3(kCandThreads), sm, s, a.pdl != 0,
-                    a);
+    return launch_k(kern, dim3((unsigned)grid), dim3(kCandThreads), sm, s, a.pdl != 0, a);
 }
 
 }  // namespace idx

@@ -73,6 +73,7 @@ struct CandArgs {
     int rows, topk, cap;
     int fallback;         // 0: main pass (flags rows), 1: rows re-emitted by the rescan
     int grid_limit;       // CTAs of the rescan's pass (they stride over the rows)
+    int sm_count;         // SMs of the device (the launch copies the runs of few rows)
     int* out;
     int pdl;              // launch overlapping the kernel before it on the stream
     int* d_status;
@@ -82,7 +83,7 @@ struct CandArgs {
 
 cudaError_t launch_topk_rows(const TopkRowsArgs& a, cudaStream_t s);
 cudaError_t launch_cand_topk(const CandArgs& a, cudaStream_t s);
-size_t cand_smem_bytes(int cap_q, int nruns, int topk);
+size_t cand_smem_bytes(int cap_q, int nruns, int topk, bool staged);
 size_t split_workspace_bytes(int rows, int g);
 
 }  // namespace idx
