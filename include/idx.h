@@ -82,8 +82,11 @@ typedef struct idx_stats {
 /* Every field 0 selects the default.  Pass NULL for all defaults. */
 typedef struct idx_options {
     float cap_factor;     /* candidate slab cap = ceil(cap_factor * topk) when given;
-                             default max(ceil(2.25 * topk), 4096) (page 1: about
-                             2.25 x topk candidates).  Caps above 12288 are refused. */
+                             default min(max(ceil(3.5 * topk), 4096), 12288) (page 1
+                             sizes its slab at about 2.25 x topk; the larger default
+                             lets the threshold sample take a wider stride, so the
+                             sample pass costs less than the extra candidates add).
+                             Caps above 12288 are refused. */
     float target_factor;  /* expected candidates / topk that the sampled threshold aims
                              at; default sqrt(cap/topk).  Test knob to force short or
                              overflowing rows. */
@@ -225,8 +228,8 @@ idx_status idx_score_topk_noalloc(const void* q, const void* k, const float* k_s
  * faster).
  *
  * idx_route_fused(max_len, topk) is the gate: 1 (the fused path) when
- * max_len >= 24576 keys, or when every row fits the default candidate slab
- * (max_len <= max(ceil(2.25 topk), 4096): all keys are emitted, no sampling);
+ * max_len >= 24576 keys, or when max_len <= max(ceil(2.25 topk), 4096) (every
+ * row fits the default candidate slab: all keys are emitted, no sampling);
  * 0 otherwise (idx_score_materialise into the workspace, then
  * idx_topk_from_scores).  24576 is the crossover measured on GB300 for e4m3
  * q/k with H = 32 and 64 and topk 512 and 2048 (4096 causal rows): the

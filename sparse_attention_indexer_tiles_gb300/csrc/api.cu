@@ -149,7 +149,10 @@ struct FusedParams {
 
 // Slab cap, threshold target and sample stride of the fused path.
 //   cap    = ceil(cap_factor * topk) when cap_factor is given, else
-//            max(ceil(2.25 * topk), 4096)
+//            min(max(ceil(3.5 * topk), 4096), kMaxCap): the page's slab holds
+//            about 2.25 topk; at 3.5 topk the rule below reaches the widest
+//            stride of the table for topk >= 1170, and the sample pass, which
+//            scores keys / S of every row, costs less than the larger slab adds
 //   target = expected candidates / topk the sampled threshold aims at; the
 //            geometric middle sqrt(cap / topk) of [1, cap / topk] by default
 //   S      = the largest odd stride from the table that still leaves about
@@ -162,7 +165,7 @@ FusedParams fused_params(int topk, const idx_options* opt) {
     if (cf > 0.0)
         p.cap = (int)std::ceil(cf * topk);
     else
-        p.cap = std::max((int)std::ceil(2.25 * topk), 4096);
+        p.cap = std::min(std::max((int)std::ceil(3.5 * topk), 4096), kMaxCap);
     if (p.cap < topk) p.cap = topk;
     p.cap_q = ((p.cap + kRuns - 1) / kRuns + 64 + 1) / 2 * 2;  // even: 16-byte run copies
     const double ratio = (double)p.cap / topk;
@@ -573,7 +576,8 @@ idx_status idx_score_materialise(const void* q, const void* k, const float* k_sc
 }
 
 int idx_route_fused(long long max_len, int topk) {
-    // rows that fit the default slab are emitted whole (no sampling): fused
+    // rows of at most max(2.25 topk, 4096) keys fit the default slab and are
+    // emitted whole (no sampling): fused, as measured
     const long long cap = std::max<long long>((long long)std::ceil(2.25 * topk), 4096);
     return (max_len <= cap || max_len >= kRouteMinKeys) ? 1 : 0;
 }

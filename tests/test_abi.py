@@ -129,7 +129,7 @@ def _documented_workspace(rows, max_len, topk, nruns):
     counters)."""
     def up(x):
         return (x + 255) // 256 * 256
-    cap = max(math.ceil(2.25 * topk), 4096)
+    cap = min(max(math.ceil(3.5 * topk), 4096), 12288)
     cap_q = (-(-cap // 8) + 64 + 1) // 2 * 2
     target = math.sqrt(cap / topk)
     t = max(32.0, (4.5 / math.log(max(target, 1.0001))) ** 2)
@@ -160,7 +160,7 @@ def test_fused_workspace_follows_the_documented_layout(lib):
     for rows, keys, topk, k in cases:
         expect, S = _documented_workspace(rows, keys, topk, 8 * k)
         assert ws(rows, keys, 0, 64, 128, topk, 2) == expect, (rows, keys, topk, k)
-    assert _documented_workspace(1, 1, 2048, 8)[1] == 23  # the stride for topk 2048
+    assert _documented_workspace(1, 1, 2048, 8)[1] == 63  # the stride for topk 2048
     assert _documented_workspace(1, 1, 512, 8)[1] == 45
 
 
