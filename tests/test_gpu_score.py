@@ -204,6 +204,46 @@ def test_fused_ties_below_positive_keys(idx):
     assert st["fallback_rows"] == 6 and st["status"] == 0
 
 
+def _two_level_ties(rows, keys, n_top, n_tied, seed):
+    """Scores 2.0 on n_top keys, 1.0 on n_tied keys and 0 elsewhere (head 0 and
+    dimension 0 only, unit weight and key scale): the sampled threshold falls
+    on 1.0, the slab holds every candidate, and the threshold value is a tie of
+    n_tied keys that the slab top-k resolves by index."""
+    inp = synth.indexer_inputs(rows, keys, 32, 128, 400, "fp8", seed=seed, ranges="full")
+    inp.q.zero_()
+    inp.q[:, 0, 0] = 1.0
+    inp.w[:, 0] = 1.0
+    inp.k_scale.fill_(1.0)
+    g = torch.Generator().manual_seed(seed + 1)
+    k = inp.k.float()
+    k[:, 0] = -1.0
+    pos = torch.randperm(keys, generator=g)[:n_top + n_tied]
+    k[pos[:n_top], 0] = 2.0
+    k[pos[n_top:], 0] = 1.0
+    inp.k = k.to(torch.float8_e4m3fn)
+    return inp
+
+
+@pytest.mark.parametrize("rows,keys,n_tied,check_rows", [
+    (8, 12000, 2500, None),          # one launch of few runs: the streamed slab top-k
+    (8, 150000, 3000, [0, 7])])      # key splits into many short runs: the staged one
+def test_fused_slab_resolves_a_tied_threshold_bin(idx, rows, keys, n_tied, check_rows):
+    """More than 256 candidates in the threshold bin (exact ties at 1.0), no
+    rescan: the slab top-k's radix selection over keys, then over the tied
+    indices, against the oracle.  (topk 400: cap 4096, stride 31, the sample's
+    42nd largest key sets the threshold; (150 + n_tied) / 31 sampled keys reach
+    1.0, at least 4.8 standard deviations above 42.)"""
+    inp = _two_level_ties(rows, keys, 150, n_tied, seed=60 + keys % 7)
+    stats = idx.Stats(torch.device(DEV))
+    got = fused(idx, inp, stats=stats)
+    st = stats.read()
+    assert st["fallback_rows"] == 0 and st["status"] == 0, st
+    assert st["max_count"] == 150 + n_tied
+    ref = oracle.score_topk(inp, rows=check_rows)
+    sel = got if check_rows is None else got[check_rows]
+    assert np.array_equal(sel, ref)
+
+
 def test_fused_mixed_ranges(idx):
     """Rows of one CTA with different visible ranges, empty rows, rows shorter
     than topk (padded with -1) and rows longer than the slab."""
