@@ -152,6 +152,40 @@ idx_status idx_score_topk(const void* q, const void* k, const float* k_scale, co
                           void* stream);
 
 /* ------------------------------------------------------------------------
+ * idx_score_topk_host - idx_score_topk on inputs and output in HOST memory:
+ * the call a host that holds q, k, ... (and wants the indices back) makes.
+ * Page-locked host memory lets the copies run asynchronously and overlap the
+ * compute; pageable memory gives the same result without the overlap.
+ *
+ * The rows are taken in two chunks (whole row blocks each).  k and
+ * k_scale go up first, then each chunk's q, w, ks and ke on a copy stream;
+ * chunk c is scored and selected on `stream` once its inputs are up, while
+ * chunk c + 1 goes up and chunk c - 1's indices come back on a second copy
+ * stream.  The call returns with everything enqueued and `stream` waiting
+ * for the last copy back: once `stream` is synchronised, out_idx is
+ * complete.  The copy streams and their events are the library's, one pair
+ * per device; calls on one device are serialised on the host.
+ *
+ *   q, k, k_scale, w, ks, ke, out_idx : HOST pointers, shapes as for
+ *                              idx_score_topk (no alignment needed)
+ *   ws, ws_bytes             : DEVICE workspace (256-byte aligned), at least
+ *                              idx_score_topk_host_workspace(...): the device
+ *                              copies of the inputs and of out_idx, and the
+ *                              fused workspace of one chunk
+ *   opt                      : as for idx_score_topk; stage_events [0] start
+ *                              and [1] end on `stream`
+ * Returns IDX_OK or an error from the list above (arguments are checked
+ * before anything is copied).
+ * ------------------------------------------------------------------------ */
+size_t idx_score_topk_host_workspace(int rows, long long keys, long long max_len, int H, int D,
+                                     int topk, idx_dtype dt, const idx_options* opt);
+idx_status idx_score_topk_host(const void* q, const void* k, const float* k_scale,
+                               const float* w, const int* ks, const int* ke, int rows,
+                               long long keys, long long max_len, int H, int D, int topk,
+                               idx_dtype dt, int* out_idx, void* ws, size_t ws_bytes,
+                               const idx_options* opt, void* stream);
+
+/* ------------------------------------------------------------------------
  * idx_topk_from_scores - exact top-k of given fp32 scores (page "[sglang] ROCm
  * DSA Indexer Top-K 최적화": fp32 12-bit coarse histogram, radix tie
  * refinement, full-row rescan when the threshold bin overflows the tie

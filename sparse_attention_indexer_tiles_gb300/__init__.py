@@ -7,6 +7,7 @@ library is missing or the GPU is not an sm_103 part, the calls raise.
 
 Entry points (same names as the C ABI in ``include/idx.h``):
   idx_score_topk            fused score + exact top-k (no [rows, keys] logits)
+  idx_score_topk_host       the same on host-memory inputs and output (copies overlap the compute)
   idx_topk_from_scores      exact radix top-k of given fp32 scores
   idx_score_materialise     the two-pass baseline's score pass
   idx_score_topk_mxfp4, idx_score_materialise_mxfp4, idx_mxfp4_to_e4m3
@@ -22,6 +23,7 @@ import torch
 
 __all__ = [
     "IdxError", "Options", "Stats", "load", "idx_score_topk", "idx_score_topk_workspace",
+    "idx_score_topk_host", "idx_score_topk_host_workspace",
     "idx_topk_from_scores", "idx_topk_workspace", "idx_score_materialise",
     "idx_status_string", "DTYPES", "STAT_FIELDS", "StageEvents", "idx_launch_count",
     "idx_score_topk_noalloc", "idx_page_table_transform", "idx_route_fused",
@@ -96,6 +98,10 @@ def load(path: str | None = None):
     lib.idx_score_topk_workspace.restype = SZ
     lib.idx_score_topk.argtypes = [P, P, P, P, P, P, I, LL, LL, I, I, I, I, P, P, SZ, P, P]
     lib.idx_score_topk.restype = I
+    lib.idx_score_topk_host_workspace.argtypes = [I, LL, LL, I, I, I, I, P]
+    lib.idx_score_topk_host_workspace.restype = SZ
+    lib.idx_score_topk_host.argtypes = [P, P, P, P, P, P, I, LL, LL, I, I, I, I, P, P, SZ, P, P]
+    lib.idx_score_topk_host.restype = I
     lib.idx_topk_workspace.argtypes = [I, LL, I, P]
     lib.idx_topk_workspace.restype = SZ
     lib.idx_topk_from_scores.argtypes = [P, LL, P, P, I, I, P, P, SZ, P, P]
@@ -237,6 +243,44 @@ def idx_score_topk(q, k, k_scale, w, ks, ke, topk: int, *, max_len: int = 0, out
         _check("idx_score_topk", load().idx_score_topk(
             _ptr(q), _ptr(k), _ptr(k_scale), _ptr(w), _ptr(ks), _ptr(ke), rows, keys, max_len, H, D,
             topk, dt, _ptr(out), _ptr(ws), ws.numel() * ws.element_size(), _opt_ref(o),
+            _stream(stream)))
+        return out
+
+
+def idx_score_topk_host_workspace(rows: int, keys: int, max_len: int, H: int, D: int, topk: int,
+                                  dtype, options=None) -> int:
+    dt = DTYPES[dtype] if not isinstance(dtype, int) else dtype
+    return int(load().idx_score_topk_host_workspace(rows, keys, max_len, H, D, topk, dt,
+                                                    _opt_ref(make_options(options))))
+
+
+def idx_score_topk_host(q, k, k_scale, w, ks, ke, topk: int, *, max_len: int = 0, out=None,
+                        ws=None, device=None, options=None, stats: Stats | None = None,
+                        stream=None):
+    """idx_score_topk on inputs in host memory (CPU tensors; pinned ones let the
+    copies overlap the compute): returns the indices [rows, topk] int32 in host
+    memory, complete once `stream` is synchronised.  ws is a device uint8
+    tensor (allocated on `device`, default the current one, when None)."""
+    for t in (q, k, k_scale, w, ks, ke, out):
+        if t is not None and (t.is_cuda or not t.is_contiguous()):
+            raise ValueError("idx_score_topk_host: inputs and out are contiguous CPU tensors")
+    dev = ws.device if ws is not None else torch.device("cuda", torch.cuda.current_device()) \
+        if device is None else torch.device(device)
+    if not dev.type == "cuda":
+        raise ValueError("idx_score_topk_host: the workspace lives on a CUDA device")
+    with torch.cuda.device(dev):
+        rows, H, D = q.shape
+        keys = k.shape[0]
+        dt = DTYPES[q.dtype]
+        o = make_options(options, stats)
+        need = idx_score_topk_host_workspace(rows, keys, max_len, H, D, topk, dt, o)
+        if out is None:
+            out = torch.empty(rows, topk, dtype=torch.int32, pin_memory=True)
+        if ws is None:
+            ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+        _check("idx_score_topk_host", load().idx_score_topk_host(
+            _ptr(q), _ptr(k), _ptr(k_scale), _ptr(w), _ptr(ks), _ptr(ke), rows, keys, max_len, H,
+            D, topk, dt, _ptr(out), _ptr(ws), ws.numel() * ws.element_size(), _opt_ref(o),
             _stream(stream)))
         return out
 

@@ -295,6 +295,84 @@ SplitPlan score_split(int rows, int H, long long max_len) {
     return p;
 }
 
+// ------------------------------------------------------------ host entry
+
+// Rows per chunk of idx_score_topk_host: two chunks of whole row blocks.  A
+// chunk is one fused call with its fixed costs (the sample, threshold and slab
+// launches, the emit pass's last wave: ~0.05 ms at 4096 x 65536, H 64), while
+// the copies left exposed (k, the first chunk's inputs, the last chunk's
+// indices) shrink only slowly with more chunks.  Measured at that shape: one
+// call 2.082 ms of compute, two chunks 2.135, three 2.19, four 2.27.
+constexpr int kHostChunks = 2;
+
+struct HostChunks {
+    int rows_per_chunk, n;
+};
+
+HostChunks host_chunks(int rows, int H) {
+    const int rpb = score_rows_per_block(H);
+    const int nblk = (rows + rpb - 1) / rpb;
+    const int per = std::max((nblk + kHostChunks - 1) / kHostChunks, 1) * rpb;
+    return {per, (rows + per - 1) / per};
+}
+
+// The device copies of an idx_score_topk_host call at the front of its
+// workspace, then one chunk's fused workspace.
+struct HostLayout {
+    size_t q, k, k_scale, w, ks, ke, out, fused, total;
+};
+
+HostLayout host_layout(int rows, long long keys, int H, int D, int topk, idx_dtype dt,
+                       size_t fused_bytes) {
+    auto up = [](size_t b) { return (b + 255) / 256 * 256; };
+    const size_t es = dt == IDX_BF16 ? 2 : 1;
+    HostLayout L;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off += up(bytes);
+        return o;
+    };
+    L.q = take((size_t)rows * H * D * es);
+    L.k = take((size_t)keys * D * es);
+    L.k_scale = take((size_t)keys * sizeof(float));
+    L.w = take((size_t)rows * H * sizeof(float));
+    L.ks = take((size_t)rows * sizeof(int));
+    L.ke = take((size_t)rows * sizeof(int));
+    L.out = take((size_t)rows * topk * sizeof(int));
+    L.fused = take(fused_bytes);
+    L.total = off;
+    return L;
+}
+
+// One upload and one download stream per device, with the events that order
+// them against the compute stream; a call holds the device's mutex while it
+// enqueues.
+struct HostPipe {
+    std::mutex mu;
+    bool ready = false;
+    cudaStream_t up = nullptr, down = nullptr;
+    cudaEvent_t start = nullptr, fin = nullptr;
+    cudaEvent_t in_ready[kHostChunks + 1] = {}, done[kHostChunks] = {};
+};
+
+constexpr int kMaxDevices = 64;
+HostPipe g_host_pipes[kMaxDevices];
+
+cudaError_t host_pipe_init(HostPipe& p) {
+    if (p.ready) return cudaSuccess;
+    cudaError_t e = cudaStreamCreateWithFlags(&p.up, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&p.down, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p.start, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p.fin, cudaEventDisableTiming);
+    for (int i = 0; e == cudaSuccess && i <= kHostChunks; ++i)
+        e = cudaEventCreateWithFlags(&p.in_ready[i], cudaEventDisableTiming);
+    for (int i = 0; e == cudaSuccess && i < kHostChunks; ++i)
+        e = cudaEventCreateWithFlags(&p.done[i], cudaEventDisableTiming);
+    if (e == cudaSuccess) p.ready = true;
+    return e;
+}
+
 void record(const idx_options* opt, int i, cudaStream_t s) {
     if (opt && opt->stage_events && opt->stage_events[i])
         cudaEventRecord(static_cast<cudaEvent_t>(opt->stage_events[i]), s);
@@ -497,6 +575,106 @@ idx_status idx_score_topk(const void* q, const void* k, const float* k_scale, co
         count_launches(1);
     }
     record(opt, 4, s);
+    return IDX_OK;
+}
+
+size_t idx_score_topk_host_workspace(int rows, long long keys, long long max_len, int H, int D,
+                                     int topk, idx_dtype dt, const idx_options* opt) {
+    if (rows <= 0 || keys <= 0 || topk < 1) return 0;
+    if (max_len <= 0 || max_len > keys) max_len = keys;
+    const HostChunks hc = host_chunks(rows, H);
+    const size_t fused = idx_score_topk_workspace(std::min(rows, hc.rows_per_chunk), keys, max_len,
+                                                  H, D, topk, dt, opt);
+    return host_layout(rows, keys, H, D, topk, dt, fused).total;
+}
+
+idx_status idx_score_topk_host(const void* q, const void* k, const float* k_scale,
+                               const float* w, const int* ks, const int* ke, int rows,
+                               long long keys, long long max_len, int H, int D, int topk,
+                               idx_dtype dt, int* out_idx, void* ws, size_t ws_bytes,
+                               const idx_options* opt, void* stream) {
+    if (topk < 1) return IDX_EINVAL;
+    if (topk > kMaxTopk) return IDX_EUNSUPPORTED;
+    if (rows < 0 || keys < 0) return IDX_EINVAL;
+    if (dt != IDX_BF16 && dt != IDX_FP8_E4M3) return IDX_EUNSUPPORTED;
+    if (!score_supported(dt, H, D)) return IDX_EUNSUPPORTED;
+    if (rows == 0) return IDX_OK;
+    if (!q || !k || !k_scale || !w || !ks || !ke || !out_idx || !ws) return IDX_EINVAL;
+    if (keys < 1 || keys > 0x7fffff00ll || (long long)rows * H > 0x7fffff00ll) return IDX_EUNSUPPORTED;
+    if (!aligned(ws, 256)) return IDX_EALIGN;
+    if (max_len <= 0 || max_len > keys) max_len = keys;
+    const FusedParams fp = fused_params(topk, opt);
+    if (fp.cap > kMaxCap || fp.S < 1) return IDX_EUNSUPPORTED;
+    if (!arch_ok()) return IDX_EUNSUPPORTED;
+    const HostChunks hc = host_chunks(rows, H);
+    const size_t fused_bytes = idx_score_topk_workspace(std::min(rows, hc.rows_per_chunk), keys,
+                                                        max_len, H, D, topk, dt, opt);
+    const HostLayout L = host_layout(rows, keys, H, D, topk, dt, fused_bytes);
+    if (ws_bytes < L.total) return IDX_EWORKSPACE;
+
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_status(e);
+    if (dev < 0 || dev >= kMaxDevices) return IDX_EUNSUPPORTED;
+    HostPipe& P = g_host_pipes[dev];
+    std::lock_guard<std::mutex> lock(P.mu);
+    if ((e = host_pipe_init(P)) != cudaSuccess) return cuda_status(e);
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    record(opt, 0, s);
+    idx_options o;
+    if (opt) o = *opt;
+    else std::memset(&o, 0, sizeof(o));
+    o.stage_events = nullptr;
+
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    const size_t es = dt == IDX_BF16 ? 2 : 1;
+    const size_t q_row = (size_t)H * D * es, w_row = (size_t)H * sizeof(float);
+    auto h2d = [&](size_t dst, const void* src, size_t bytes) {
+        return cudaMemcpyAsync(base + dst, src, bytes, cudaMemcpyHostToDevice, P.up);
+    };
+    // the copies start after the work the caller queued before this call (the
+    // workspace may still be in use there)
+    if ((e = cudaEventRecord(P.start, s)) != cudaSuccess) return cuda_status(e);
+    if ((e = cudaStreamWaitEvent(P.up, P.start, 0)) != cudaSuccess) return cuda_status(e);
+    if ((e = cudaStreamWaitEvent(P.down, P.start, 0)) != cudaSuccess) return cuda_status(e);
+    if ((e = h2d(L.k, k, (size_t)keys * D * es)) != cudaSuccess) return cuda_status(e);
+    if ((e = h2d(L.k_scale, k_scale, (size_t)keys * sizeof(float))) != cudaSuccess)
+        return cuda_status(e);
+    for (int c = 0; c < hc.n; ++c) {
+        const int r0 = c * hc.rows_per_chunk, nr = std::min(hc.rows_per_chunk, rows - r0);
+        if ((e = h2d(L.q + r0 * q_row, static_cast<const uint8_t*>(q) + r0 * q_row, nr * q_row)) !=
+                cudaSuccess ||
+            (e = h2d(L.w + r0 * w_row, w + (size_t)r0 * H, nr * w_row)) != cudaSuccess ||
+            (e = h2d(L.ks + r0 * sizeof(int), ks + r0, nr * sizeof(int))) != cudaSuccess ||
+            (e = h2d(L.ke + r0 * sizeof(int), ke + r0, nr * sizeof(int))) != cudaSuccess ||
+            (e = cudaEventRecord(P.in_ready[c], P.up)) != cudaSuccess)
+            return cuda_status(e);
+    }
+    for (int c = 0; c < hc.n; ++c) {
+        const int r0 = c * hc.rows_per_chunk, nr = std::min(hc.rows_per_chunk, rows - r0);
+        if ((e = cudaStreamWaitEvent(s, P.in_ready[c], 0)) != cudaSuccess) return cuda_status(e);
+        const idx_status st = idx_score_topk(
+            base + L.q + r0 * q_row, base + L.k, reinterpret_cast<const float*>(base + L.k_scale),
+            reinterpret_cast<const float*>(base + L.w + r0 * w_row),
+            reinterpret_cast<const int*>(base + L.ks) + r0,
+            reinterpret_cast<const int*>(base + L.ke) + r0, nr, keys, max_len, H, D, topk, dt,
+            reinterpret_cast<int*>(base + L.out) + (size_t)r0 * topk, base + L.fused, fused_bytes,
+            &o, stream);
+        if (st != IDX_OK) return st;
+        if ((e = cudaEventRecord(P.done[c], s)) != cudaSuccess ||
+            (e = cudaStreamWaitEvent(P.down, P.done[c], 0)) != cudaSuccess ||
+            (e = cudaMemcpyAsync(out_idx + (size_t)r0 * topk,
+                                 reinterpret_cast<int*>(base + L.out) + (size_t)r0 * topk,
+                                 (size_t)nr * topk * sizeof(int), cudaMemcpyDeviceToHost,
+                                 P.down)) != cudaSuccess)
+            return cuda_status(e);
+    }
+    // the caller's stream (and the next call's copies) wait for the last copy back
+    if ((e = cudaEventRecord(P.fin, P.down)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(s, P.fin, 0)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(P.up, P.fin, 0)) != cudaSuccess)
+        return cuda_status(e);
+    record(opt, 1, s);
     return IDX_OK;
 }
 

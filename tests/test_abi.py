@@ -208,3 +208,28 @@ def test_bindings_refuse_tensors_on_two_devices():
     assert pkg._dev(fake("cuda:1"), None, fake("cuda:1")) == "cuda:1"
     with pytest.raises(ValueError, match="different devices"):
         pkg._dev(fake("cuda:0"), fake("cuda:1"))
+
+
+def test_host_entry_checks_arguments_before_any_copy(lib):
+    """idx_score_topk_host (host-memory inputs and output) validates on the
+    host: bad sizes and missing pointers come back before anything is copied
+    or launched, and its workspace holds the device copies of the inputs and
+    of the indices plus the fused workspace of one row chunk."""
+    import torch
+    import sparse_attention_indexer_tiles_gb300 as pkg
+    before = pkg.idx_launch_count()
+    args = [None] * 6 + [4, 100, 0, 8, 64]
+    assert lib.idx_score_topk_host(*args, 0, 1, None, None, 0, None, None) == 1   # topk < 1
+    assert lib.idx_score_topk_host(*args, 16, 3, None, None, 0, None, None) == 4  # MXFP4 here
+    assert lib.idx_score_topk_host(*args, 16, 1, None, None, 0, None, None) == 1  # no pointers
+    assert lib.idx_score_topk_host(*([None] * 6), 0, 100, 0, 8, 64, 16, 1, None, None, 0,
+                                   None, None) == 0                                # no rows
+    assert pkg.idx_launch_count() == before
+    rows, keys, H, D, topk = 4096, 65536, 64, 128, 2048
+    ws = pkg.idx_score_topk_host_workspace(rows, keys, 0, H, D, topk, 2)
+    copies = rows * H * D + keys * D + keys * 4 + rows * H * 4 + 2 * rows * 4 + rows * topk * 4
+    chunk = pkg.idx_score_topk_workspace(rows // 2, keys, 0, H, D, topk, 2)
+    assert copies + chunk <= ws <= copies + chunk + 8 * 256
+    with pytest.raises(ValueError):
+        pkg.idx_score_topk_host(torch.zeros(8, 4, 64, dtype=torch.bfloat16)[::2], None, None,
+                                None, None, None, 16)
