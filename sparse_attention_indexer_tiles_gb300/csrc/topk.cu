@@ -421,17 +421,20 @@ IDX_DEVI void stream_collect(const RowView& v, uint32_t L, uint32_t* rkey, uint3
 // The one-pass collection of a whole row by one CTA, lower bound included.
 // The sample is the first SAMPLE float4 slots of every lane in the first step
 // of every warp's slice (P <= 8192 values for 512 threads), values the filter
-// loads anyway.  With tg = ceil(3 k P / (2 n)), L is the 20-bit floor of the
-// sample's tg-th largest order key: the 12-bit digit that holds it, then the
-// next 8 bits among the sample keys of that digit.  The number of keys >= L is
-// then about 1.5 k; it falls below k only when tg or more sample keys exceed
-// the row's k-th largest, a binomial count whose mean is 2 tg / 3 (for n =
-// 131072: 192 against a mean of 128, 5.7 standard deviations).  A miss costs
-// time only (the row takes the exact multi-pass path).  hist leaves holding
-// the histogram of the hits relative to the returned key B (bins of 4096 keys
-// from B up, the last bin open), B being the order key of the float bound
-// (every hit has key >= B: fkey folds -0 onto +0, so a bound of zero holds
-// both zeros at B).
+// loads anyway.  L is the 20-bit floor of the sample's tg-th largest order
+// key: the 12-bit digit that holds it, then the next 8 bits among the sample
+// keys of that digit.  The row has fewer than k keys >= L only when tg or more
+// sample keys exceed the row's k-th largest, a binomial count of mean
+// m = k P / n.  tg = max(1.5 m, min(m + 5.7 sqrt(m) + 1, c)), c being the rank
+// at which the expected count of keys >= L (tg n / P) fills 70 % of the runs:
+// a miss is a 5.7-spread event whatever n / k is (about 1.5 k keys reach L for
+// n = 131072 and k = 2048, m = 128; for a long row and a small k, m is a few
+// and the margin above m decides, not 1.5 m), while the runs keep room.  A
+// miss costs time only (the row takes the exact multi-pass path).  hist leaves
+// holding the histogram of the hits relative to the returned key B (bins of
+// 4096 keys from B up, the last bin open), B being the order key of the float
+// bound (every hit has key >= B: fkey folds -0 onto +0, so a bound of zero
+// holds both zeros at B).
 template <int THREADS, int UNROLL>
 IDX_DEVI uint32_t stream_collect_estimate(const RowView& v, uint32_t k, uint32_t* hist,
                                       uint32_t* scratch, uint32_t* rkey, uint32_t* ridx,
@@ -471,8 +474,15 @@ IDX_DEVI uint32_t stream_collect_estimate(const RowView& v, uint32_t k, uint32_t
     if (lane == 0) atomicAdd(&scratch[44], ns);
     __syncthreads();
     const uint32_t P = scratch[44];
-    unsigned long long tg64 = (3ull * k * P + 2ull * (uint32_t)n - 1ull) / (2ull * (uint32_t)n);
-    const uint32_t tg = tg64 < 1ull ? 1u : tg64 > P ? P : (uint32_t)tg64;
+    // m = the sample keys expected above the row's k-th largest; a miss needs
+    // tg of them, so tg = m + 5.7 sqrt(m) + 1 keeps it a 5.7-spread event at
+    // any n / k (1.5 m alone, the floor, is that only for m >= ~130), as long
+    // as the expected candidates (tg n / P) fill at most 70 % of the runs
+    const float m = (float)k * (float)P / (float)n;
+    const float t_safe = m + 5.7f * sqrtf(m) + 1.0f;
+    const float t_cap = 0.7f * (float)((THREADS / 32) * kRunCap) * (float)P / (float)n;
+    const float t = fmaxf(ceilf(1.5f * m), fminf(t_safe, t_cap));
+    const uint32_t tg = t < 1.0f ? 1u : t >= (float)P ? P : (uint32_t)ceilf(t);
     const DigitPick d0 = pick_digit<THREADS>(hist, kHistBins, tg, scratch);
     // the next 8 bits of the sample keys in digit d0 (pick_digit ends on a barrier)
     zero_shared<THREADS>(hist, 256);
@@ -1017,9 +1027,18 @@ topk_split_kernel(TopkRowsArgs a) {
         if (lane == 0 && ns) atomicAdd(&scratch[44], ns);
         __syncthreads();
         const uint32_t P = scratch[44];
-        // ceil(2 k P / n) in integers: 2 k P < 2^25 and n < 2^31, so nothing wraps
-        uint32_t tg = (2u * k * P + (uint32_t)n - 1u) / (uint32_t)n;
-        tg = tg < 1u ? 1u : tg > P ? P : tg;
+        // m = this slice's sample keys expected above the row's k-th largest
+        // (k / g of those in P of its n / g values); the slice's bound lies
+        // above the row's threshold (the row then takes the exact path) only
+        // when tg of them do, so tg = max(2 m, min(m + 4 sqrt(m) + 1, c)), c
+        // the rank at which the row's expected kept count (tg n / P over the
+        // slices) fills 70 % of the merge buffer (4 spreads: the bound is the
+        // 12-bit floor of the tg-th sample key, well below it)
+        const float m = (float)k * (float)P / (float)n;
+        const float t = fmaxf(ceilf(2.0f * m),
+                              fminf(m + 4.0f * sqrtf(m) + 1.0f,
+                                    0.7f * (float)kMergeCap * (float)P / (float)n));
+        const uint32_t tg = t < 1.0f ? 1u : t >= (float)P ? P : (uint32_t)ceilf(t);
         const uint32_t d = pick_digit<THREADS>(hist, kHistBins, tg, scratch).digit;
         L = P ? d << 20 : 0u;  // an empty slice takes nothing and bounds nothing
     }

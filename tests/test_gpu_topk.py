@@ -180,6 +180,24 @@ def test_forced_row_split(idx, g):
     assert stats.read()["split_rows"] > 0
 
 
+@pytest.mark.parametrize("row_split", [-1, 0])
+def test_long_rows_small_topk_keep_the_one_pass_bound(idx, row_split):
+    """512K keys per row, topk 512: the sample holds only a few keys above a
+    row's 512th largest (m = k P / n ~ 8 of 8192, ~4 per split slice), so the
+    sample rank carries a margin of spreads above m rather than a fixed
+    multiple of it; no row falls back to the exact multi-pass path, unsplit or
+    split, and the result is exact."""
+    si = synth.score_inputs(16, 1 << 19, 512, seed=31, short_frac=0.0, bf16_grid=False)
+    stats = idx.Stats(torch.device(DEV))
+    got = gpu_topk(idx, si.scores, si.ks, si.ke, 512, options={"row_split": row_split},
+                   stats=stats)
+    ref = oracle.topk_from_scores(si.scores, si.ks, si.ke, 512)
+    assert np.array_equal(got, ref)
+    st = stats.read()
+    assert st["tie_rescan_rows"] == 0 and st["status"] == 0, st
+    assert st["split_rows"] == (0 if row_split == -1 else 16)
+
+
 def test_row_split_merge_refinement_paths(idx):
     """The merge block's refinement over the slices' candidates, one row per
     branch: fp32 scores (several keys in the threshold bin: a second
