@@ -676,7 +676,7 @@ def route_sweep(idx, dev):
             print(json.dumps({"H": H, "topk": topk, "rows": rows, "keys": keys,
                               "fused_ms": tf, "two_pass_ms": tt, "two_pass_over_fused": tt / tf,
                               "identical": bool(torch.equal(out, out2)),
-                              "gate_fused": idx.idx_route_fused(keys, topk)}), flush=True)
+                              "gate_fused": idx.idx_route_fused(rows, keys, topk)}), flush=True)
             del S, g, inp
             torch.cuda.empty_cache()
 

@@ -261,11 +261,15 @@ idx_status idx_score_topk_noalloc(const void* q, const void* k, const float* k_s
  * keys; below that the filter passes most keys and the dense path is
  * faster).
  *
- * idx_route_fused(max_len, topk) is the gate: 1 (the fused path) when
- * max_len >= 24576 keys, or when max_len <= max(ceil(2.25 topk), 4096) (every
- * row fits the default candidate slab: all keys are emitted, no sampling);
- * 0 otherwise (idx_score_materialise into the workspace, then
- * idx_topk_from_scores).  24576 is the crossover measured on GB300 for e4m3
+ * idx_route_fused(rows, max_len, topk) is the gate.  1 (the fused path)
+ * when max_len <= max(ceil(2.25 topk), 4096) (every row fits the default
+ * candidate slab: all keys are emitted, no sampling); else 0 (the two-pass
+ * path: idx_score_materialise into the workspace, then idx_topk_from_scores)
+ * for few rows, rows <= SMs / 4 with rows x max_len <= 2^25 (the logits are
+ * small and the top-k splits each long row over >= 4 blocks, while the fused
+ * path pays its sample, threshold and slab launches: at 8-32 rows x 1M keys,
+ * H 32, the two-pass path is 1.36-1.02x faster); else 1 when max_len >= 24576
+ * keys and 0 below.  24576 is the crossover measured on GB300 for e4m3
  * q/k with H = 32 and 64 and topk 512 and 2048 (4096 causal rows): the
  * two-pass path is faster from 6144 to 16384 keys, the two are within 1 % at
  * 24576 and 32768 (where the fused path needs no logits workspace), and the
@@ -275,7 +279,7 @@ idx_status idx_score_topk_noalloc(const void* q, const void* k, const float* k_s
  * Arguments as idx_score_topk; max_len 0 = keys.  The workspace of the
  * two-pass route holds the [rows, max_len] fp32 logits.
  * ------------------------------------------------------------------------ */
-int idx_route_fused(long long max_len, int topk);
+int idx_route_fused(int rows, long long max_len, int topk);
 size_t idx_score_topk_routed_workspace(int rows, long long keys, long long max_len, int H,
                                        int D, int topk, idx_dtype dt, const idx_options* opt);
 idx_status idx_score_topk_routed(const void* q, const void* k, const float* k_scale,

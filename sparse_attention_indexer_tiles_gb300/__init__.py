@@ -108,7 +108,7 @@ def load(path: str | None = None):
     lib.idx_topk_from_scores.restype = I
     lib.idx_score_materialise.argtypes = [P, P, P, P, P, P, I, LL, I, I, I, P, LL, P, P]
     lib.idx_score_materialise.restype = I
-    lib.idx_route_fused.argtypes = [LL, I]
+    lib.idx_route_fused.argtypes = [I, LL, I]
     lib.idx_route_fused.restype = I
     lib.idx_score_topk_routed_workspace.argtypes = [I, LL, LL, I, I, I, I, P]
     lib.idx_score_topk_routed_workspace.restype = SZ
@@ -441,10 +441,10 @@ def idx_page_table_transform(idx, table, page_size: int = 64, *, row_map=None, o
         return idx
 
 
-def idx_route_fused(max_len: int, topk: int) -> bool:
-    """The routing gate: True when a call whose longest row sees max_len keys
-    takes the fused path."""
-    return bool(load().idx_route_fused(max_len, topk))
+def idx_route_fused(rows: int, max_len: int, topk: int) -> bool:
+    """The routing gate: True when a call of `rows` rows whose longest row sees
+    max_len keys takes the fused path."""
+    return bool(load().idx_route_fused(rows, max_len, topk))
 
 
 def idx_score_topk_routed_workspace(rows: int, keys: int, max_len: int, H: int, D: int,

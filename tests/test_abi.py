@@ -101,15 +101,23 @@ def test_product_path_has_no_oracle_import():
 
 
 def test_routing_gate_rule(lib):
-    """The gate is host logic: fused from 24576 keys in the longest row on."""
+    """The gate is host logic: fused from 24576 keys in the longest row on,
+    two-pass for few rows (rows <= SMs / 4, rows x max_len <= 2^25; no device
+    answers here: 148 SMs)."""
     import sparse_attention_indexer_tiles_gb300 as pkg
-    assert pkg.idx_route_fused(4608, 2048)       # fits the slab: every key emitted
-    assert not pkg.idx_route_fused(4609, 2048)
-    assert not pkg.idx_route_fused(24575, 2048)
-    assert not pkg.idx_route_fused(12288, 2048)
-    assert not pkg.idx_route_fused(6144, 512)
-    assert pkg.idx_route_fused(24576, 2048)
-    assert pkg.idx_route_fused(1 << 20, 512)
+    assert pkg.idx_route_fused(4096, 4608, 2048)       # fits the slab: every key emitted
+    assert pkg.idx_route_fused(8, 4608, 2048)
+    assert not pkg.idx_route_fused(4096, 4609, 2048)
+    assert not pkg.idx_route_fused(4096, 24575, 2048)
+    assert not pkg.idx_route_fused(4096, 12288, 2048)
+    assert not pkg.idx_route_fused(4096, 6144, 512)
+    assert pkg.idx_route_fused(4096, 24576, 2048)
+    assert pkg.idx_route_fused(4096, 1 << 20, 512)
+    assert not pkg.idx_route_fused(16, 1 << 20, 2048)  # few rows over long keys
+    assert not pkg.idx_route_fused(32, 1 << 20, 2048)
+    assert pkg.idx_route_fused(33, 1 << 20, 2048)      # 33 x 2^20 > 2^25
+    assert not pkg.idx_route_fused(37, 1 << 18, 2048)
+    assert pkg.idx_route_fused(38, 1 << 18, 2048)      # 4 x 38 > 148
     # the dense route's workspace holds the logits; the fused one its slab
     dense = pkg.idx_score_topk_routed_workspace(64, 8192, 0, 64, 128, 2048, 2)
     assert dense >= 64 * 8192 * 4

@@ -28,12 +28,15 @@ def call(idx, fn, inp, **kw):
     return out.cpu().numpy()
 
 
-@pytest.mark.parametrize("keys,H,topk,dense", [(6144, 64, 512, True), (9000, 32, 300, True),
-                                                (20000, 16, 128, True), (24576, 64, 256, False),
-                                                (30000, 16, 128, False), (3000, 64, 512, False)])
-def test_routed_equals_fused(idx, keys, H, topk, dense):
-    assert idx.idx_route_fused(keys, topk) == (not dense)
-    inp = synth.indexer_inputs(256 // H * 4 + 3, keys, H, 128, topk, "fp8", seed=80 + H)
+@pytest.mark.parametrize("keys,H,topk,few,dense", [
+    (6144, 64, 512, False, True), (9000, 32, 300, False, True), (20000, 16, 128, False, True),
+    (24576, 64, 256, False, False), (30000, 16, 128, False, False), (3000, 64, 512, False, False),
+    (65536, 32, 512, True, True)])      # few rows over long keys: the two-pass route
+def test_routed_equals_fused(idx, keys, H, topk, few, dense):
+    sm = torch.cuda.get_device_properties(0).multi_processor_count
+    rows = 12 if few else max(256 // H * 4 + 3, sm // 4 + 1)
+    assert idx.idx_route_fused(rows, keys, topk) == (not dense)
+    inp = synth.indexer_inputs(rows, keys, H, 128, topk, "fp8", seed=80 + H)
     stats = idx.Stats(torch.device(DEV))
     got = call(idx, idx.idx_score_topk_routed, inp, stats=stats)
     ref = call(idx, idx.idx_score_topk, inp)
