@@ -368,3 +368,17 @@ def test_full_size_scores_on_sampled_rows(idx, name):
     _, sc = oracle.score_topk(inp, rows=rows, want_scores=True)
     for i, r in enumerate(rows):
         check_scores(got[i, :n[r]], sc[i, :n[r]])
+
+
+@pytest.mark.parametrize("rows,keys", [(8, 40000), (4, 300000)])
+def test_fused_largest_topk(idx, rows, keys):
+    """topk 4096, the largest: the default slab clamps to 12288 candidates, and
+    the slab top-k writes the output from its bitmap (40000-key rows) or from
+    its ordered index list (300000-key rows: beyond the bitmap's 131072)."""
+    inp = synth.indexer_inputs(rows, keys, 32, 128, 4096, "fp8", seed=70 + rows, ranges="full")
+    stats = idx.Stats(torch.device(DEV))
+    got = fused(idx, inp, stats=stats)
+    assert np.array_equal(got, two_pass(idx, inp))
+    check_fused(inp, got, rows=[0, rows - 1])
+    st = stats.read()
+    assert st["status"] == 0 and st["fallback_rows"] == 0, st
